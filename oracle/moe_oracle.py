@@ -1,0 +1,276 @@
+"""CPU oracle for the forward pass of one Mixture-of-Experts layer (numpy, fp64).
+
+TEST INFRASTRUCTURE ONLY. Nothing on the product path imports this module: only the
+tests, ``__graft_entry__.smoke()`` and ``bench.py``'s CPU-baseline leg call it. It shares
+no code with the CUDA library (no headers, tables, helpers or constants).
+
+Every step is the plain definition, written in the order the pages give it. The pages:
+
+* [Tirogla] "Mixture of experts (MoE)" (tirogla.com): section "How it works", steps 1-6
+  (score, select, dispatch, compute, combine, balance), and section "Code".
+* [DL-S077] "DL S077 - Mixture of Experts (MoE) Intuition" (dineshblog.com): section 1.1
+  (the SwiGLU expert), section 2 (top-k gating, with a worked example).
+* [Starphix] "Mixture of Experts (MoE)" (learn.starphix.com): "Key Equations",
+  "Shared + Specialized".
+
+Readings where the pages are silent or disagree (also listed in the design doc):
+
+* selection compares raw logits, descending, the lower expert index winning ties;
+* gates: softmax over all E ("softmax_all"), softmax over the k selected logits
+  ("softmax_topk"), or sigmoid affinities renormalised over the selected k ("sigmoid_topk");
+* expert FFN is w2(silu(w1 x) * w3 x): w1 = gate, w3 = up, w2 = down, no biases;
+* dispatch keeps, per expert, the first C assignments in token order (assignment
+  a = t*k + slot), drops the rest, and gates are not renormalised after a drop;
+* f_i = (assignments routed to i before the drop) / (T*k); P_i = mean softmax-over-all
+  probability; L_aux = alpha*E*sum_i f_i*P_i; L_z = beta*mean_t(logsumexp(l_t)^2);
+* capacity C = ceil(cf*T*k/E), computed in fp64; "no drop" is C = T.
+
+Every function here is pinned by a ``-m "not gpu"`` test against closed forms, the
+pages' worked example, or brute force; none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+GATE_MODES = ("softmax_all", "softmax_topk", "sigmoid_topk")
+
+
+def _f64(a) -> np.ndarray:
+    a = np.asarray(a, dtype=np.float64)
+    return a
+
+
+# ---------------------------------------------------------------------------------------
+# Step 1: score.  [Tirogla] "How it works", step 1; [Starphix] "Key Equations".
+# ---------------------------------------------------------------------------------------
+def router_logits(x, w_router, bias=None) -> np.ndarray:
+    """Router logits l = x . W_r^T (+ b): x [T, d], W_r [E, d] (nn.Linear layout), b [E]."""
+    l = _f64(x) @ _f64(w_router).T
+    if bias is not None:
+        l = l + _f64(bias)[None, :]
+    return l
+
+
+def softmax_all(logits) -> np.ndarray:
+    """Softmax over all E experts per token (the Switch/GShard router probability)."""
+    l = _f64(logits)
+    assert np.all(np.isfinite(l)), "router logits must be finite"
+    m = l.max(axis=1, keepdims=True)
+    e = np.exp(l - m)
+    return e / e.sum(axis=1, keepdims=True)
+
+
+def logsumexp(logits) -> np.ndarray:
+    """Per-token log(sum_j exp(l_j)), in the max-shifted form."""
+    l = _f64(logits)
+    m = l.max(axis=1)
+    return m + np.log(np.exp(l - m[:, None]).sum(axis=1))
+
+
+# ---------------------------------------------------------------------------------------
+# Step 2: select.  [Tirogla] "How it works", step 2, and "Code" (route: a stable sort by
+# descending logit, so among equal logits the lower index comes first).
+# ---------------------------------------------------------------------------------------
+def select_topk(logits, k: int) -> np.ndarray:
+    """Indices [T, k] (int64) of the k largest logits per token, descending; ties -> lower
+    index first (stable sort on the negated logits)."""
+    l = _f64(logits)
+    assert np.all(np.isfinite(l)), "router logits must be finite"
+    E = l.shape[1]
+    assert 1 <= k <= E
+    order = np.argsort(-l, axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
+
+
+def gates(logits, idx, mode: str) -> np.ndarray:
+    """Gate weights [T, k] for the selected experts ``idx`` under one of three conventions.
+
+    softmax_all  -- [Tirogla] step 1 (Switch, GShard): the softmax-over-all probability of
+                    each selected expert, kept as is.
+    softmax_topk -- [Tirogla] step 1 (Mixtral), [DL-S077] section 2: softmax over the k
+                    selected logits only.
+    sigmoid_topk -- [Tirogla] step 1 (DeepSeek-V3): sigmoid affinities of the selected
+                    experts divided by their sum.
+    """
+    l = _f64(logits)
+    sel = np.take_along_axis(l, np.asarray(idx), axis=1)
+    if mode == "softmax_all":
+        return np.take_along_axis(softmax_all(l), np.asarray(idx), axis=1)
+    if mode == "softmax_topk":
+        m = sel.max(axis=1, keepdims=True)
+        e = np.exp(sel - m)
+        return e / e.sum(axis=1, keepdims=True)
+    if mode == "sigmoid_topk":
+        s = 1.0 / (1.0 + np.exp(-sel))
+        return s / s.sum(axis=1, keepdims=True)
+    raise ValueError(f"unknown gate mode {mode!r}")
+
+
+# ---------------------------------------------------------------------------------------
+# Step 3: dispatch.  [Tirogla] "How it works", step 3 (group the (token, expert)
+# assignments by expert with a counting sort, keep at most C per expert) and "Code"
+# (dispatch: one pass over assignments in token order, which is the priority).
+# ---------------------------------------------------------------------------------------
+def capacity(cf: float, T: int, k: int, E: int) -> int:
+    """C = ceil(cf * T * k / E), evaluated in fp64. [Tirogla] "Code" (main) and
+    "Complexity and constants" (capacity factor)."""
+    return int(math.ceil(cf * T * k / E))
+
+
+def dispatch(idx, E: int, C: int) -> dict:
+    """Counting sort of the T*k assignments by expert, keeping the first C per expert.
+
+    Assignment a = t*k + slot. Returns int64 arrays:
+      counts  [E]    assignments routed to each expert before the drop (n_e),
+      offsets [E+1]  exclusive prefix sum of kept_e = min(n_e, C),
+      perm    [R]    assignment id held by each kept row, grouped by expert, token order,
+      inv     [T*k]  kept row of each assignment, or -1 if dropped,
+      dropped        number of dropped assignments.
+    """
+    flat = np.asarray(idx).reshape(-1)
+    slots = [[] for _ in range(E)]
+    counts = np.zeros(E, dtype=np.int64)
+    dropped = 0
+    for a in range(flat.shape[0]):           # token order = priority
+        e = int(flat[a])
+        counts[e] += 1
+        if len(slots[e]) < C:
+            slots[e].append(a)
+        else:
+            dropped += 1
+    offsets = np.zeros(E + 1, dtype=np.int64)
+    for e in range(E):
+        offsets[e + 1] = offsets[e] + len(slots[e])
+    perm = np.array([a for e in range(E) for a in slots[e]], dtype=np.int64)
+    inv = np.full(flat.shape[0], -1, dtype=np.int64)
+    inv[perm] = np.arange(perm.shape[0], dtype=np.int64)
+    return dict(counts=counts, offsets=offsets, perm=perm, inv=inv, dropped=dropped)
+
+
+# ---------------------------------------------------------------------------------------
+# Step 4: compute.  [DL-S077] section 1.1: each expert is a SwiGLU MLP,
+# w2(silu(w1 x) * w3 x), no biases; w1 = gate, w3 = up, w2 = down.
+# ---------------------------------------------------------------------------------------
+def silu(z) -> np.ndarray:
+    """silu(z) = z * sigmoid(z)."""
+    z = _f64(z)
+    with np.errstate(over="ignore"):
+        return z / (1.0 + np.exp(-z))
+
+
+def swiglu_ffn(x_rows, w1, w3, w2) -> np.ndarray:
+    """SwiGLU FFN of row vectors: x [n, d], w1/w3 [F, d], w2 [d, F] -> [n, d]."""
+    x = _f64(x_rows)
+    g = x @ _f64(w1).T
+    u = x @ _f64(w3).T
+    return (silu(g) * u) @ _f64(w2).T
+
+
+def expert_outputs(x, disp: dict, k: int, w1, w3, w2) -> np.ndarray:
+    """Ungated FFN output of every kept row: row r holds FFN_e(x_t) for the assignment
+    a = perm[r] (t = a // k) and its expert e (the segment r falls in). [R, d]."""
+    x = _f64(x)
+    offsets, perm = disp["offsets"], disp["perm"]
+    E = offsets.shape[0] - 1
+    out = np.zeros((perm.shape[0], x.shape[1]), dtype=np.float64)
+    for e in range(E):
+        lo, hi = int(offsets[e]), int(offsets[e + 1])
+        if hi > lo:
+            toks = perm[lo:hi] // k
+            out[lo:hi] = swiglu_ffn(x[toks], w1[e], w3[e], w2[e])
+    return out
+
+
+# ---------------------------------------------------------------------------------------
+# Step 5: combine.  [Tirogla] "How it works", step 5: y_t = sum over the token's selected
+# experts of g_{t,e} * FFN_e(x_t); a dropped assignment contributes nothing.
+# [Starphix] "Shared + Specialized": an always-active shared expert is added.
+# ---------------------------------------------------------------------------------------
+def combine(g, inv, rows, T: int, k: int, shared=None) -> np.ndarray:
+    """y [T, d] = sum_{slot} [inv >= 0] g[t, slot] * rows[inv[t*k+slot]]  (+ shared[t]).
+
+    ``rows`` are ungated expert outputs indexed by kept row; summed in slot order."""
+    rows = _f64(rows)
+    g = _f64(g).reshape(T, k)
+    inv = np.asarray(inv).reshape(T, k)
+    d = rows.shape[1] if rows.ndim == 2 and rows.shape[0] > 0 else (
+        np.asarray(shared).shape[1] if shared is not None else 0)
+    y = np.zeros((T, d), dtype=np.float64)
+    for s in range(k):
+        kept = inv[:, s] >= 0
+        if np.any(kept):
+            y[kept] += g[kept, s][:, None] * rows[inv[kept, s]]
+    if shared is not None:
+        y = y + _f64(shared)
+    return y
+
+
+# ---------------------------------------------------------------------------------------
+# Step 6: balance.  [Tirogla] "How it works", step 6, and "Code" (aux_loss, z_loss).
+# ---------------------------------------------------------------------------------------
+def load_fractions(idx, E: int) -> np.ndarray:
+    """f_i: fraction of all T*k routing decisions that chose expert i (before any drop)."""
+    flat = np.asarray(idx).reshape(-1)
+    return np.bincount(flat, minlength=E).astype(np.float64) / flat.shape[0]
+
+
+def aux_loss(logits, idx, alpha: float) -> float:
+    """Switch load-balancing loss alpha * E * sum_i f_i * P_i, with P_i the mean over tokens
+    of the softmax-over-all probability of expert i."""
+    l = _f64(logits)
+    E = l.shape[1]
+    f = load_fractions(idx, E)
+    P = softmax_all(l).mean(axis=0)
+    return float(alpha * E * np.dot(f, P))
+
+
+def z_loss(logits, beta: float) -> float:
+    """Router z-loss beta * mean_t(logsumexp(l_t)^2) (ST-MoE form)."""
+    lse = logsumexp(logits)
+    return float(beta * np.mean(lse * lse))
+
+
+# ---------------------------------------------------------------------------------------
+# The whole layer, for inputs small enough to hold in fp64.
+# ---------------------------------------------------------------------------------------
+def route(logits, k: int, mode: str) -> dict:
+    """Steps 1-2 on given logits: top-k indices and gates."""
+    idx = select_topk(logits, k)
+    return dict(idx=idx, gate=gates(logits, idx, mode))
+
+
+def forward(x, w_router, w1, w3, w2, *, k: int, mode: str, C: int, router_bias=None,
+            w1s=None, w3s=None, w2s=None, alpha: float = 0.01, beta: float = 1e-3,
+            idx_override=None) -> dict:
+    """Full forward of one MoE layer in fp64.
+
+    ``idx_override`` replaces the selected experts (the gates are then taken for those
+    experts from the same logits); it lets a test recompute steps 3-6 on another
+    implementation's routing decisions.
+    Returns y, logits, idx, gate, the dispatch dict, l_aux, l_z."""
+    x = _f64(x)
+    T = x.shape[0]
+    E = np.asarray(w_router).shape[0]
+    logits = router_logits(x, w_router, router_bias)
+    idx = select_topk(logits, k) if idx_override is None else np.asarray(idx_override, dtype=np.int64)
+    g = gates(logits, idx, mode)
+    disp = dispatch(idx, E, C)
+    rows = expert_outputs(x, disp, k, w1, w3, w2)
+    shared = swiglu_ffn(x, w1s, w3s, w2s) if w1s is not None else None
+    y = combine(g, disp["inv"], rows, T, k, shared)
+    return dict(y=y, logits=logits, idx=idx, gate=g, dispatch=disp,
+                l_aux=aux_loss(logits, idx, alpha), l_z=z_loss(logits, beta))
+
+
+def near_tie_tokens(logits, k: int, eps: float = 1e-3) -> np.ndarray:
+    """Tokens whose k-th and (k+1)-th largest logits differ by less than ``eps``: the only
+    tokens whose expert set may legitimately differ between two implementations that
+    round the router differently."""
+    l = _f64(logits)
+    E = l.shape[1]
+    if k >= E:
+        return np.zeros(0, dtype=np.int64)
+    s = -np.sort(-l, axis=1)
+    return np.nonzero(s[:, k - 1] - s[:, k] < eps)[0]

@@ -1,0 +1,333 @@
+"""Pins of the CPU oracle against what the pages and the mathematics fix.
+
+Each test checks one oracle function against something other than itself: the pages'
+worked example, the demo's stated invariants, closed forms, or brute force on tiny
+inputs. The cases are chosen so that a dropped term, a wrong sign, a wrong index or a
+transposed operand in the oracle fails at least one of them.
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+
+
+# ---------------------------------------------------------------- gating / selection
+def test_worked_example_top2(golden_dir):
+    """'DL S077' section 2: logits -> experts {2, 4}, gates 0.668 / 0.332."""
+    g = json.load(open(os.path.join(golden_dir, "worked_example_top2.json")))
+    l = np.array([g["logits"]])
+    idx = O.select_topk(l, g["k"])
+    assert idx[0].tolist() == g["experts"]
+    gate = O.gates(l, idx, "softmax_topk")
+    assert np.round(gate[0], 3).tolist() == g["gates_3dp"]
+
+
+def test_softmax_all_closed_form():
+    """Logits ln(1..4): probabilities 0.1..0.4; top-2 = experts 3, 2 with gates 0.4, 0.3."""
+    l = np.log(np.array([[1.0, 2.0, 3.0, 4.0]]))
+    p = O.softmax_all(l)
+    np.testing.assert_allclose(p[0], [0.1, 0.2, 0.3, 0.4], rtol=0, atol=1e-15)
+    idx = O.select_topk(l, 2)
+    assert idx[0].tolist() == [3, 2]
+    np.testing.assert_allclose(O.gates(l, idx, "softmax_all")[0], [0.4, 0.3], atol=1e-15)
+    np.testing.assert_allclose(O.gates(l, idx, "softmax_topk")[0], [4 / 7, 3 / 7], atol=1e-15)
+
+
+def test_sigmoid_topk_closed_form():
+    """sigma(ln 3) = 0.75 and sigma(0) = 0.5 -> renormalised gates 0.6 / 0.4; k=1 -> 1."""
+    l = np.array([[-30.0, 0.0, math.log(3.0), -20.0]])
+    idx = O.select_topk(l, 2)
+    assert idx[0].tolist() == [2, 1]
+    np.testing.assert_allclose(O.gates(l, idx, "sigmoid_topk")[0], [0.6, 0.4], atol=1e-15)
+    idx1 = O.select_topk(l, 1)
+    np.testing.assert_allclose(O.gates(l, idx1, "sigmoid_topk")[0], [1.0], atol=0)
+
+
+@pytest.mark.parametrize("E", [3, 8, 16])
+def test_topk_softmax_equals_softmax_all_when_k_is_E(E):
+    """With k = E the softmax over the selected logits is the softmax over all experts."""
+    l = np.random.default_rng(E).normal(size=(40, E)) * 3
+    idx = O.select_topk(l, E)
+    np.testing.assert_allclose(O.gates(l, idx, "softmax_topk"), O.gates(l, idx, "softmax_all"),
+                               rtol=1e-13, atol=1e-15)
+
+
+@pytest.mark.parametrize("k", [1, 2, 5])
+def test_topk_softmax_is_renormalised_softmax_all(k):
+    l = np.random.default_rng(k).normal(size=(50, 8)) * 2
+    idx = O.select_topk(l, k)
+    p = O.gates(l, idx, "softmax_all")
+    np.testing.assert_allclose(O.gates(l, idx, "softmax_topk"), p / p.sum(axis=1, keepdims=True),
+                               rtol=1e-13)
+
+
+def _brute_topk(row, k):
+    """The unique k-subset S with every member beating every non-member (a larger logit,
+    or an equal logit and a lower index); ordered by descending logit, then index."""
+    E = len(row)
+    found = []
+    for S in itertools.combinations(range(E), k):
+        rest = [i for i in range(E) if i not in S]
+        if all(row[j] > row[i] or (row[j] == row[i] and j < i) for j in S for i in rest):
+            found.append(S)
+    assert len(found) == 1
+    return sorted(found[0], key=lambda j: (-row[j], j))
+
+
+@pytest.mark.parametrize("E", [4, 6, 8])
+@pytest.mark.parametrize("kind", ["random", "tied", "equal"])
+def test_topk_brute_force(E, kind):
+    rng = np.random.default_rng(E * 7 + len(kind))
+    if kind == "random":
+        l = rng.normal(size=(12, E))
+    elif kind == "tied":
+        l = np.round(rng.normal(size=(12, E)) * 2) / 2
+        l[0, :] = 0.0
+        l[0, 1] = -0.0          # -0.0 and +0.0 compare equal: a tie
+    else:
+        l = np.full((3, E), 0.7)
+    for k in range(1, E + 1):
+        idx = O.select_topk(l, k)
+        for t in range(l.shape[0]):
+            assert idx[t].tolist() == _brute_topk(l[t].tolist(), k)
+    if kind == "equal":
+        assert O.select_topk(l, 3)[0].tolist() == [0, 1, 2]
+
+
+def test_gates_sum_to_one_on_demo_logits(golden_dir):
+    """'Mixture of experts (MoE)' (tirogla.com) demo: hashed logits, renormalised top-2
+    gates sum to 1 within 1e-5; capacity at cf 1.25 is 20."""
+    g = json.load(open(os.path.join(golden_dir, "demo_capacity.json")))
+    T, E, k = g["T"], g["E"], g["k"]
+    l = np.array([((i * 2654435761) >> 7) % 1000 / 250.0 for i in range(T * E)]).reshape(T, E)
+    idx = O.select_topk(l, k)
+    for mode in ("softmax_topk", "sigmoid_topk"):
+        s = O.gates(l, idx, mode).sum(axis=1)
+        assert np.all(np.abs(s - 1.0) < g["gate_sum_tol"])
+    C = O.capacity(g["cf"], T, k, E)
+    assert C == g["capacity"]
+    d = O.dispatch(idx, E, C)
+    kept = np.diff(d["offsets"])
+    assert np.all(kept <= C)
+    assert d["dropped"] == int(np.maximum(d["counts"] - C, 0).sum())
+
+
+# ---------------------------------------------------------------- dispatch
+def _brute_dispatch(flat, E, C):
+    """Rank formulation: rank(a) = #earlier assignments to the same expert; a is kept
+    iff rank < C, at row sum_{e' < e} min(n_e', C) + rank."""
+    n = [sum(1 for v in flat if v == e) for e in range(E)]
+    base = [sum(min(n[j], C) for j in range(e)) for e in range(E)]
+    inv = []
+    for a, e in enumerate(flat):
+        rank = sum(1 for b in range(a) if flat[b] == e)
+        inv.append(base[e] + rank if rank < C else -1)
+    return n, inv
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_dispatch_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    E = int(rng.integers(1, 9))
+    k = int(rng.integers(1, E + 1))
+    T = int(rng.integers(0, 40))
+    l = rng.normal(size=(T, E))
+    idx = O.select_topk(l, k) if T > 0 else np.zeros((0, k), dtype=np.int64)
+    for C in (0, 1, 3, max(1, T * k // E), T):
+        d = O.dispatch(idx, E, C)
+        flat = idx.reshape(-1).tolist()
+        n, inv = _brute_dispatch(flat, E, C)
+        assert d["counts"].tolist() == n
+        assert d["inv"].tolist() == inv
+        assert d["dropped"] == sum(max(0, v - C) for v in n)
+        # perm is the inverse of inv on the kept assignments and increasing per segment
+        R = int(d["offsets"][-1])
+        assert d["perm"].shape[0] == R == sum(1 for v in inv if v >= 0)
+        for r in range(R):
+            assert inv[d["perm"][r]] == r
+        for e in range(E):
+            seg = d["perm"][d["offsets"][e]:d["offsets"][e + 1]]
+            assert np.all(np.diff(seg) > 0)
+            assert all(flat[a] == e for a in seg)
+
+
+def test_dispatch_collapse_closed_form():
+    """All-equal logits send every token to experts 0..k-1: k*max(0, T-C) drops."""
+    T, E, k = 50, 8, 2
+    idx = O.select_topk(np.zeros((T, E)), k)
+    assert np.all(idx == np.arange(k))
+    for C in (0, 7, 50, 80):
+        d = O.dispatch(idx, E, C)
+        assert d["dropped"] == k * max(0, T - C)
+        assert d["counts"].tolist() == [T] * k + [0] * (E - k)
+
+
+def test_capacity_formula():
+    assert O.capacity(1.25, 256, 2, 8) == 80
+    assert O.capacity(1.0, 16384, 1, 128) == 128
+    assert O.capacity(1.0, 10, 1, 3) == 4          # ceil(10/3)
+    assert O.capacity(1.0, 12, 1, 3) == 4          # exact, no rounding up
+
+
+# ---------------------------------------------------------------- losses
+@pytest.mark.parametrize("E,k,m", [(8, 2, 3), (16, 1, 2), (4, 3, 5)])
+def test_aux_loss_uniform_split_equals_alpha(E, k, m):
+    """'Mixture of experts (MoE)' (tirogla.com): the balance loss equals alpha for a
+    perfectly uniform split. Rows are the E cyclic rotations of one vector (m times),
+    so every expert receives the same load and the same mean probability."""
+    v = np.linspace(-1.0, 2.0, E)[np.random.default_rng(E).permutation(E)]
+    l = np.stack([np.roll(v, s) for _ in range(m) for s in range(E)])
+    idx = O.select_topk(l, k)
+    np.testing.assert_allclose(O.load_fractions(idx, E), 1.0 / E, atol=1e-15)
+    assert O.aux_loss(l, idx, 0.01) == pytest.approx(0.01, rel=1e-12)
+
+
+def test_aux_loss_constant_logits():
+    """Constant logits: P_i = 1/E, top-k = experts 0..k-1, f_i = 1/k there -> alpha."""
+    for E, k in ((8, 2), (5, 1), (6, 6)):
+        l = np.full((9, E), 0.3)
+        idx = O.select_topk(l, k)
+        assert O.aux_loss(l, idx, 0.02) == pytest.approx(0.02, rel=1e-12)
+
+
+def test_aux_loss_collapse_closed_form():
+    """k=1, expert 0 gets +L: f_0 = 1 and P_0 = e^L / (e^L + E - 1) -> alpha*E*P_0."""
+    E, L = 8, 2.0
+    l = np.zeros((11, E))
+    l[:, 0] = L
+    idx = O.select_topk(l, 1)
+    P0 = math.exp(L) / (math.exp(L) + E - 1)
+    assert O.aux_loss(l, idx, 0.01) == pytest.approx(0.01 * E * P0, rel=1e-12)
+
+
+def test_z_loss_closed_forms():
+    """Zero logits: beta*(ln E)^2. Mixed rows: the mean of squares, not the square of
+    the mean. Large constant logits do not overflow."""
+    E, beta = 8, 1e-3
+    assert O.z_loss(np.zeros((5, E)), beta) == pytest.approx(beta * math.log(E) ** 2, rel=1e-13)
+    l = np.stack([np.zeros(E), np.full(E, 2.0)])
+    a, b = math.log(E), 2.0 + math.log(E)
+    assert O.z_loss(l, beta) == pytest.approx(beta * (a * a + b * b) / 2, rel=1e-13)
+    assert O.z_loss(np.full((2, E), 1000.0), 1.0) == pytest.approx((1000 + math.log(E)) ** 2, rel=1e-13)
+
+
+# ---------------------------------------------------------------- score and FFN
+def test_router_logits_selects_components():
+    """W_r rows are unit vectors e_{pi(e)}: logits[t, e] = x[t, pi(e)] + b[e] (E != d)."""
+    d, E = 6, 4
+    pi = [4, 0, 5, 2]
+    W = np.zeros((E, d))
+    W[np.arange(E), pi] = 1.0
+    x = np.random.default_rng(0).normal(size=(7, d))
+    b = np.array([0.5, -1.0, 0.0, 2.0])
+    np.testing.assert_array_equal(O.router_logits(x, W, b), x[:, pi] + b)
+
+
+def test_silu_closed_forms():
+    np.testing.assert_allclose(O.silu([0.0, 1.0, -1.0]),
+                               [0.0, 1 / (1 + math.exp(-1)), -1 / (1 + math.e)], atol=1e-16)
+    assert O.silu([800.0])[0] == 800.0
+    assert O.silu([-800.0])[0] == 0.0
+
+
+def test_swiglu_structured_closed_form():
+    """W1 = diag(a), W3 = diag(b), W2 = cyclic shift P (not symmetric):
+    y = P (silu(a*x) * (b*x)). Swapping gate/up or transposing W2 fails."""
+    n = 5
+    a = np.array([1.0, -2.0, 0.5, 3.0, -1.0])
+    b = np.array([2.0, 1.0, -1.0, 0.5, 4.0])
+    P = np.roll(np.eye(n), 1, axis=0)          # (P v)[i] = v[i-1]
+    x = np.array([[0.3, -1.2, 2.0, 0.7, -0.4]])
+    h = (a * x) / (1 + np.exp(-(a * x))) * (b * x)
+    expect = np.roll(h, 1, axis=1)
+    np.testing.assert_allclose(O.swiglu_ffn(x, np.diag(a), np.diag(b), P), expect, atol=1e-15)
+
+
+def test_swiglu_matches_torch_library():
+    """Rectangular shapes against torch's own fp64 silu and matmul."""
+    rng = np.random.default_rng(3)
+    x, w1, w3, w2 = rng.normal(size=(9, 12)), rng.normal(size=(20, 12)), rng.normal(size=(20, 12)), rng.normal(size=(12, 20))
+    tx, t1, t3, t2 = (torch.from_numpy(a) for a in (x, w1, w3, w2))
+    ref = torch.nn.functional.linear(torch.nn.functional.silu(torch.nn.functional.linear(tx, t1))
+                                     * torch.nn.functional.linear(tx, t3), t2)
+    np.testing.assert_allclose(O.swiglu_ffn(x, w1, w3, w2), ref.numpy(), rtol=1e-12, atol=1e-12)
+
+
+# ---------------------------------------------------------------- combine / forward
+def test_combine_scale_experts_closed_form():
+    """Experts that return (e+1)*x_t (the demo's stand-in experts): y_t is the sum over
+    kept slots of g * (e+1) * x_t; dropped slots add nothing."""
+    rng = np.random.default_rng(5)
+    T, E, k, d = 20, 4, 2, 3
+    x = rng.normal(size=(T, d))
+    l = rng.normal(size=(T, E))
+    idx = O.select_topk(l, k)
+    g = O.gates(l, idx, "softmax_topk")
+    disp = O.dispatch(idx, E, 6)
+    rows = np.zeros((disp["perm"].shape[0], d))
+    for r, a in enumerate(disp["perm"]):
+        rows[r] = x[a // k] * (idx.reshape(-1)[a] + 1)
+    y = O.combine(g, disp["inv"], rows, T, k)
+    inv = disp["inv"].reshape(T, k)
+    for t in range(T):
+        s = sum(g[t, j] * (idx[t, j] + 1) for j in range(k) if inv[t, j] >= 0)
+        np.testing.assert_allclose(y[t], s * x[t], atol=1e-14)
+    assert disp["dropped"] > 0 and np.any(np.all(inv < 0, axis=1)) is not None
+
+
+def _rand_weights(rng, E, F, d):
+    return (rng.normal(size=(E, F, d)) / math.sqrt(d), rng.normal(size=(E, F, d)) / math.sqrt(d),
+            rng.normal(size=(E, d, F)) / math.sqrt(F))
+
+
+def test_identical_experts_reproduce_dense_ffn():
+    """Identical experts, gates that sum to 1 and no drop give one dense SwiGLU FFN."""
+    rng = np.random.default_rng(11)
+    T, d, E, F, k = 32, 8, 6, 12, 3
+    w1, w3, w2 = _rand_weights(rng, 1, F, d)
+    W1, W3, W2 = (np.repeat(w, E, axis=0) for w in (w1, w3, w2))
+    x = rng.normal(size=(T, d))
+    wr = rng.normal(size=(E, d))
+    for mode in ("softmax_topk", "sigmoid_topk"):
+        out = O.forward(x, wr, W1, W3, W2, k=k, mode=mode, C=T)
+        np.testing.assert_allclose(out["y"], O.swiglu_ffn(x, w1[0], w3[0], w2[0]), rtol=1e-12, atol=1e-12)
+
+
+def test_shared_expert_only_when_everything_drops():
+    """C = 0 drops every routed assignment: y is the shared expert's output alone."""
+    rng = np.random.default_rng(12)
+    T, d, E, F, k = 10, 8, 4, 6, 2
+    w1, w3, w2 = _rand_weights(rng, E, F, d)
+    s1, s3, s2 = (a[0] for a in _rand_weights(rng, 1, 5, d))
+    x = rng.normal(size=(T, d))
+    out = O.forward(x, rng.normal(size=(E, d)), w1, w3, w2, k=k, mode="sigmoid_topk", C=0,
+                    w1s=s1, w3s=s3, w2s=s2)
+    assert out["dispatch"]["dropped"] == T * k
+    np.testing.assert_allclose(out["y"], O.swiglu_ffn(x, s1, s3, s2), atol=1e-14)
+
+
+def test_forward_single_token_by_hand():
+    """One token, E=3, k=2, d=F=1: y = sum_j g_j * w2_j silu(w1_j x) w3_j x."""
+    x = np.array([[1.5]])
+    wr = np.array([[1.0], [-1.0], [0.5]])        # logits 1.5, -1.5, 0.75 -> experts 0, 2
+    w1 = np.array([[[2.0]], [[1.0]], [[-1.0]]])
+    w3 = np.array([[[0.5]], [[1.0]], [[3.0]]])
+    w2 = np.array([[[1.0]], [[1.0]], [[-2.0]]])
+    out = O.forward(x, wr, w1, w3, w2, k=2, mode="softmax_topk", C=1)
+    g0 = 1 / (1 + math.exp(0.75 - 1.5))
+    f = lambda a, b, c: c * (a * 1.5) / (1 + math.exp(-a * 1.5)) * (b * 1.5)
+    expect = g0 * f(2.0, 0.5, 1.0) + (1 - g0) * f(-1.0, 3.0, -2.0)
+    assert out["idx"].tolist() == [[0, 2]]
+    assert out["y"][0, 0] == pytest.approx(expect, rel=1e-14)
+
+
+def test_near_tie_tokens():
+    l = np.array([[3.0, 1.0, 0.9995, 0.0], [3.0, 1.0, 0.5, 0.0], [1.0, 1.0, 1.0, 1.0]])
+    assert O.near_tie_tokens(l, 2).tolist() == [0, 2]
+    assert O.near_tie_tokens(l, 4).tolist() == []
