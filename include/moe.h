@@ -1,0 +1,203 @@
+/*
+ * moe.h -- C ABI of libmoe: the single-GPU forward pass of one Mixture-of-Experts layer.
+ *
+ * The layer (pages: "Mixture of experts (MoE)", tirogla.com, section "How it works",
+ * steps 1-6; "DL S077 - Mixture of Experts (MoE) Intuition", dineshblog.com, sections
+ * 1.1 and 2) maps tokens x [T, d] to y [T, d]:
+ *
+ *   score    l_t = x_t . W_r^T (+ b)                      router weight W_r [E, d]
+ *   select   top-k of l_t, descending, the lower expert index winning ties
+ *   gates    softmax over all E | softmax over the k selected | sigmoid / sum over selected
+ *   dispatch stable counting sort of the T*k assignments (a = t*k + slot) by expert,
+ *            token order as priority, at most C kept per expert, the rest dropped
+ *   compute  per-expert SwiGLU FFN  w2 (silu(w1 x) * w3 x)  as a grouped GEMM
+ *   combine  y_t = sum over kept slots of g_{t,slot} * FFN_e(x_t)  (+ shared expert)
+ *   balance  L_aux = alpha * E * sum_i f_i P_i,  L_z = beta * mean_t lse(l_t)^2
+ *
+ * Conventions for every entry point:
+ *   - Every pointer argument is a DEVICE pointer unless stated otherwise. The caller owns
+ *     all buffers; the library allocates no device memory and keeps no state between
+ *     calls, except a per-device cache of kernel attributes and tensor-map entry point.
+ *   - Matrices are row-major and contiguous. Element type is moe_shape.dtype (fp32 or
+ *     bf16) for x, weights, y and the permuted buffers; logits, gates, statistics and
+ *     losses are always fp32; indices and counts are int32.
+ *   - Data pointers must be 16-byte aligned, and d * sizeof(dtype) must be a multiple of
+ *     16 bytes; for bf16, d, d_ff and d_ff_shared must be multiples of 8 (TMA strides).
+ *   - Calls are asynchronous on `stream` (a cudaStream_t, NULL = legacy default stream)
+ *     and never synchronise the host: counts, drops and losses stay on the device.
+ *   - Return value: MOE_OK, or a negative moe_status found on the host before any launch
+ *     (invalid arguments, workspace too small) or reported by a launch. Errors detected on
+ *     the device (an out-of-range expert index, non-finite logits, a pipeline wait that
+ *     timed out) set a sticky error word in the workspace; read it with moe_get_error.
+ *     The device never traps.
+ *   - `ws` is a device workspace of at least moe_workspace_size(shape) bytes, 256-byte
+ *     aligned. Every entry point takes the same workspace layout; calls that overlap on
+ *     the GPU must not share a workspace.
+ */
+#ifndef MOE_H_
+#define MOE_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID = -1,      /* bad shape, null or misaligned pointer, bad index      */
+  MOE_ERR_UNSUPPORTED = -2,  /* valid but not handled (e.g. bf16 with d % 8 != 0)      */
+  MOE_ERR_CUDA = -3,         /* a CUDA runtime call or launch failed                   */
+  MOE_ERR_WORKSPACE = -4,    /* workspace missing, misaligned or smaller than needed   */
+  MOE_ERR_TIMEOUT = -5,      /* a device pipeline wait exceeded its bound              */
+  MOE_ERR_NONFINITE = -6     /* a router logit was NaN or infinite                     */
+} moe_status;
+
+/* Gate conventions ("Mixture of experts (MoE)", tirogla.com, How it works, step 1). */
+typedef enum {
+  MOE_GATE_SOFTMAX_ALL = 0,   /* Switch/GShard: softmax over all E, selected probs kept  */
+  MOE_GATE_SOFTMAX_TOPK = 1,  /* Mixtral: softmax over the k selected logits              */
+  MOE_GATE_SIGMOID_TOPK = 2   /* DeepSeek-V3: sigmoid affinities / their sum over the k   */
+} moe_gate_mode;
+
+typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
+
+typedef struct {
+  int32_t T;            /* tokens (>= 0)                                               */
+  int32_t d;            /* model width (>= 1)                                          */
+  int32_t E;            /* routed experts, 1..1024                                     */
+  int32_t k;            /* experts per token, 1..E                                     */
+  int32_t d_ff;         /* routed expert hidden width (>= 1)                           */
+  int32_t d_ff_shared;  /* always-active shared expert hidden width, 0 = none          */
+  int32_t capacity;     /* C: kept assignments per expert (>= 0); C >= T means no drop */
+  int32_t gate;         /* moe_gate_mode                                               */
+  int32_t dtype;        /* moe_dtype of x, weights, y                                  */
+  float alpha;          /* load-balancing loss coefficient                             */
+  float beta;           /* router z-loss coefficient                                   */
+} moe_shape;
+
+/* Number of stages moe_forward_events records events around (see there). */
+#define MOE_NUM_STAGES 8
+
+/* C = ceil(cf * T * k / E) evaluated in double, clamped to [0, T] (C = T already means
+ * no drop, since one token sends at most one assignment to an expert). ("Mixture of
+ * experts (MoE)", tirogla.com, section Code: the demo's capacity; section Complexity and
+ * constants: capacity factor.) Returns -1 for E < 1, k < 1, T < 0 or cf < 0. Host only. */
+int moe_capacity(double cf, int32_t T, int32_t k, int32_t E);
+
+/* Validates a shape; returns MOE_OK or the moe_status the entry points would return.
+ * Host only, touches no device. */
+int moe_check_shape(const moe_shape* s);
+
+/* Workspace bytes every entry point below needs for this shape (0 if the shape is
+ * invalid). Host only. */
+size_t moe_workspace_size(const moe_shape* s);
+
+/* Steps 1-2 (score, select, gates) -- "Mixture of experts (MoE)", tirogla.com, How it
+ * works, steps 1-2.
+ *   x [T, d], w_router [E, d] (nn.Linear layout, logits = x . w_router^T),
+ *   router_bias [E] fp32 or NULL (added to the logits: it shifts selection, gates, the
+ *   probabilities P_i and the z-loss).
+ *   logits_in [T, E] fp32 or NULL: precomputed logits; x, w_router and router_bias are
+ *   then ignored (may be NULL).
+ *   logits_out [T, E] fp32 or NULL: receives the logits (fp32 accumulate).
+ *   topk_idx [T, k] int32 out: selected experts per token in slot order (descending
+ *   logit, ties -> lower index). topk_gate [T, k] fp32 out: gate of each slot.
+ *   stats [E + 1] fp32 out or NULL: stats[i] = sum_t softmax_all(l_t)_i for i < E and
+ *   stats[E] = sum_t lse(l_t)^2, each summed in a fixed order (deterministic). */
+int moe_route_topk(const moe_shape* s, const void* x, const void* w_router,
+                   const float* router_bias, const float* logits_in, float* logits_out,
+                   int32_t* topk_idx, float* topk_gate, float* stats, void* ws,
+                   size_t ws_bytes, void* stream);
+
+/* Step 3 (dispatch) -- "Mixture of experts (MoE)", tirogla.com, How it works, step 3 and
+ * section Code (dispatch): a stable counting sort of the T*k assignments by expert with
+ * token order as priority; the first s->capacity of each expert are kept.
+ *   topk_idx [T, k] int32, or NULL to take the top-k of logits_in [T, E] fp32 first.
+ *   counts [E] out: n_e, assignments routed to e before the drop.
+ *   offsets [E + 1] out: exclusive prefix sum of kept_e = min(n_e, C); R = offsets[E].
+ *   perm [T * k] out: rows 0..R-1 hold the assignment id a = t*k + slot of each kept
+ *   assignment, grouped by expert, increasing within an expert; rows >= R untouched.
+ *   inv [T * k] out: the row of each assignment in perm, or -1 if it was dropped.
+ *   dropped [1] out: sum_e max(0, n_e - C).
+ * All outputs are bit-exact functions of topk_idx (no floating point). */
+int moe_dispatch(const moe_shape* s, const int32_t* topk_idx, const float* logits_in,
+                 int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv,
+                 int32_t* dropped, void* ws, size_t ws_bytes, void* stream);
+
+/* Step 4 (compute) -- "Mixture of experts (MoE)", tirogla.com, How it works, step 4 and
+ * Implementation notes (grouped GEMM over contiguous expert batches); "DL S077", section
+ * 1.1 (SwiGLU expert: w1 = gate, w3 = up, w2 = down, no biases).
+ *   x [T, d]; perm, offsets as returned by moe_dispatch.
+ *   topk_gate [T, k] fp32 or NULL: row r of y_perm is scaled by topk_gate[perm[r]]
+ *   (NULL: unscaled FFN outputs).
+ *   w1, w3 [E, d_ff, d]; w2 [E, d, d_ff].
+ *   w1s, w3s [d_ff_shared, d], w2s [d, d_ff_shared]: the shared expert, used iff
+ *   s->d_ff_shared > 0 (then all three are required).
+ *   y_perm [T * k, d] out: row r < R = g * FFN_e(x_t) for assignment perm[r] of expert e;
+ *   rows >= R untouched.
+ *   y_shared [T, d] out, required iff d_ff_shared > 0: shared expert FFN(x_t).
+ * bf16 runs on the tcgen05 tensor cores with fp32 accumulation (the hidden activations are
+ * rounded to bf16 between the two GEMMs); fp32 runs on the CUDA cores in fp32. */
+int moe_grouped_swiglu(const moe_shape* s, const void* x, const int32_t* perm,
+                       const int32_t* offsets, const float* topk_gate, const void* w1,
+                       const void* w3, const void* w2, const void* w1s, const void* w3s,
+                       const void* w2s, void* y_perm, void* y_shared, void* ws,
+                       size_t ws_bytes, void* stream);
+
+/* Step 5 (combine) -- "Mixture of experts (MoE)", tirogla.com, How it works, step 5:
+ * y_t = sum over slots s < k with inv[t*k+s] >= 0 of y_perm[inv[t*k+s]]  (+ y_shared[t]),
+ * summed in slot order in fp32, no atomics (deterministic). A fully dropped token gives
+ * y_t = 0 (+ y_shared[t]). y_shared may be NULL. y [T, d] out. */
+int moe_combine(const moe_shape* s, const void* y_perm, const int32_t* inv,
+                const void* y_shared, void* y, void* stream);
+
+/* Step 6 (balance) -- "Mixture of experts (MoE)", tirogla.com, How it works, step 6:
+ *   losses[0] = alpha * E * sum_i f_i * P_i with f_i = counts[i] / (T * k) (pre-drop) and
+ *               P_i = stats[i] / T;
+ *   losses[1] = beta * stats[E] / T.
+ * stats as written by moe_route_topk, counts by moe_dispatch. Accumulated in double, in a
+ * fixed order. T = 0 gives losses 0. */
+int moe_aux_loss(const moe_shape* s, const float* stats, const int32_t* counts,
+                 float* losses, void* stream);
+
+/* The whole layer: steps 1-6 on one stream, no host synchronisation.
+ *   x [T, d], w_router [E, d], router_bias [E] or NULL, w1/w3/w2 as above,
+ *   w1s/w3s/w2s or NULL (required iff d_ff_shared > 0), y [T, d] out,
+ *   counts [E] / dropped [1] / losses [2] out, each may be NULL. */
+int moe_forward(const moe_shape* s, const void* x, const void* w_router,
+                const float* router_bias, const void* w1, const void* w3, const void* w2,
+                const void* w1s, const void* w3s, const void* w2s, void* y,
+                int32_t* counts, int32_t* dropped, float* losses, void* ws, size_t ws_bytes,
+                void* stream);
+
+/* moe_forward, recording events[i] (cudaEvent_t handles created by the caller) on the
+ * stream before stage i and events[MOE_NUM_STAGES] after the last one, so that each
+ * stage's device time can be read with cudaEventElapsedTime. Stages: 0 router GEMM,
+ * 1 gates + top-k, 2 dispatch, 3 gather, 4 gate/up GEMM + SwiGLU, 5 down GEMM + gate
+ * scale, 6 combine, 7 balance losses. n_events must be MOE_NUM_STAGES + 1. */
+int moe_forward_events(const moe_shape* s, const void* x, const void* w_router,
+                       const float* router_bias, const void* w1, const void* w3,
+                       const void* w2, const void* w1s, const void* w3s, const void* w2s,
+                       void* y, int32_t* counts, int32_t* dropped, float* losses, void* ws,
+                       size_t ws_bytes, void* stream, void* const* events, int n_events);
+
+/* Reads (synchronising `stream`) the sticky device error word in the workspace:
+ * MOE_OK, or the first moe_status a kernel recorded since the last moe_clear_error. */
+int moe_get_error(const void* ws, void* stream);
+
+/* Clears the sticky device error word (asynchronous on `stream`). */
+int moe_clear_error(void* ws, void* stream);
+
+/* Static description of a status code. */
+const char* moe_status_string(int status);
+
+/* Host-side detail of the last error returned on this thread ("" if none). */
+const char* moe_last_error_detail(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H_ */

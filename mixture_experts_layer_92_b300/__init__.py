@@ -1,0 +1,70 @@
+"""B300-native forward pass of one Mixture-of-Experts layer.
+
+The computation runs in libmoe.so (hand-written CUDA for sm_103a behind a C ABI,
+include/moe.h). This package is its thin ctypes binding (``_lib``) plus ``MoELayer``, a
+convenience holder of the layer's weights and workspace whose ``forward`` is one call of
+``moe_forward``. PyTorch only provides device memory and streams.
+"""
+from __future__ import annotations
+
+from typing import Optional
+
+import torch
+
+from . import _lib
+from ._lib import (MoeError, alloc_workspace, make_shape, moe_aux_loss, moe_capacity,  # noqa: F401
+                   moe_check_shape, moe_clear_error, moe_combine, moe_dispatch, moe_forward,
+                   moe_get_error, moe_grouped_swiglu, moe_route_topk, moe_status_string,
+                   moe_workspace_size, NUM_STAGES, STAGE_NAMES)
+
+
+class MoELayer:
+    """Weights (device tensors) + shape + workspace of one MoE layer.
+
+    w_router [E, d]; w1, w3 [E, d_ff, d]; w2 [E, d, d_ff]; optional router_bias [E] fp32 and
+    shared expert w1s, w3s [d_ff_shared, d], w2s [d, d_ff_shared]. ``capacity`` None means
+    no drop.
+    """
+
+    def __init__(self, w_router, w1, w3, w2, *, k: int, gate: str, capacity: Optional[int] = None,
+                 router_bias=None, w1s=None, w3s=None, w2s=None, alpha=0.01, beta=1e-3,
+                 max_tokens: int):
+        E, d = w_router.shape
+        self.w = dict(w_router=w_router, w1=w1, w3=w3, w2=w2, router_bias=router_bias,
+                      w1s=w1s, w3s=w3s, w2s=w2s)
+        self.E, self.d, self.k, self.d_ff = E, d, k, w1.shape[1]
+        self.d_ff_shared = 0 if w1s is None else w1s.shape[0]
+        self.gate, self.capacity, self.alpha, self.beta = gate, capacity, alpha, beta
+        self.dtype = w1.dtype
+        self.device = w1.device
+        self.ws = alloc_workspace(self.shape(max_tokens), device=self.device)
+        self.counts = torch.zeros(E, dtype=torch.int32, device=self.device)
+        self.dropped = torch.zeros(1, dtype=torch.int32, device=self.device)
+        self.losses = torch.zeros(2, dtype=torch.float32, device=self.device)
+
+    def shape(self, T: int):
+        return make_shape(T, self.d, self.E, self.k, self.d_ff, gate=self.gate, dtype=self.dtype,
+                          capacity=self.capacity, d_ff_shared=self.d_ff_shared, alpha=self.alpha,
+                          beta=self.beta)
+
+    def forward(self, x: torch.Tensor, y: Optional[torch.Tensor] = None, stream=None, events=None):
+        """y = MoE(x) for device x [T, d]; counts, dropped and losses stay on the device."""
+        T = x.shape[0]
+        if y is None:
+            y = torch.empty_like(x)
+        moe_forward(self.shape(T), self.ws, x, self.w["w_router"], self.w["w1"], self.w["w3"],
+                    self.w["w2"], y, router_bias=self.w["router_bias"], w1s=self.w["w1s"],
+                    w3s=self.w["w3s"], w2s=self.w["w2s"], counts=self.counts,
+                    dropped=self.dropped, losses=self.losses, stream=stream, events=events)
+        return y
+
+    def forward_host(self, x_host: torch.Tensor, x_dev: torch.Tensor, y_dev: torch.Tensor,
+                     y_host: torch.Tensor, losses_host: Optional[torch.Tensor] = None):
+        """End-to-end call from host memory: copy x (pinned) to the device, run the layer,
+        copy y (and the two losses) back, all on the current stream."""
+        x_dev.copy_(x_host, non_blocking=True)
+        self.forward(x_dev, y_dev)
+        y_host.copy_(y_dev, non_blocking=True)
+        if losses_host is not None:
+            losses_host.copy_(self.losses, non_blocking=True)
+        return y_host

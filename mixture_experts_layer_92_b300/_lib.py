@@ -1,0 +1,185 @@
+"""ctypes binding of libmoe (include/moe.h): argument marshalling only.
+
+Every function here passes torch tensors' device pointers, sizes and the current CUDA
+stream to the C ABI of the same name. No step of the layer runs in Python or PyTorch.
+If libmoe.so is missing the import of this module fails loudly; there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+import torch
+
+LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
+
+MOE_OK = 0
+STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
+          -4: "MOE_ERR_WORKSPACE", -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_NONFINITE"}
+GATE_MODES = {"softmax_all": 0, "softmax_topk": 1, "sigmoid_topk": 2}
+DTYPES = {torch.float32: 0, torch.bfloat16: 1}
+NUM_STAGES = 8
+STAGE_NAMES = ("router_gemm", "gates_topk", "dispatch", "gather", "gemm_gateup_swiglu",
+               "gemm_down_scale", "combine", "aux_loss")
+
+EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_topk",
+            "moe_dispatch", "moe_grouped_swiglu", "moe_combine", "moe_aux_loss", "moe_forward",
+            "moe_forward_events", "moe_get_error", "moe_clear_error", "moe_status_string",
+            "moe_last_error_detail")
+
+
+class MoeError(RuntimeError):
+    def __init__(self, status: int, where: str, detail: str):
+        self.status = status
+        super().__init__(f"{where}: {STATUS.get(status, status)} ({detail})")
+
+
+class moe_shape(ctypes.Structure):
+    _fields_ = [("T", ctypes.c_int32), ("d", ctypes.c_int32), ("E", ctypes.c_int32),
+                ("k", ctypes.c_int32), ("d_ff", ctypes.c_int32), ("d_ff_shared", ctypes.c_int32),
+                ("capacity", ctypes.c_int32), ("gate", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float)]
+
+
+def _load() -> ctypes.CDLL:
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libmoe.so is not built ({LIB_PATH}); run "
+                          "`python -m mixture_experts_layer_92_b300.build`")
+    lib = ctypes.CDLL(LIB_PATH)
+    vp, i32, sz, dbl = ctypes.c_void_p, ctypes.c_int32, ctypes.c_size_t, ctypes.c_double
+    sp = ctypes.POINTER(moe_shape)
+    sig = {
+        "moe_capacity": (ctypes.c_int, [dbl, i32, i32, i32]),
+        "moe_check_shape": (ctypes.c_int, [sp]),
+        "moe_workspace_size": (sz, [sp]),
+        "moe_route_topk": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "moe_dispatch": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, sz, vp]),
+        "moe_grouped_swiglu": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              vp, sz, vp]),
+        "moe_combine": (ctypes.c_int, [sp, vp, vp, vp, vp, vp]),
+        "moe_aux_loss": (ctypes.c_int, [sp, vp, vp, vp, vp]),
+        "moe_forward": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                       vp, sz, vp]),
+        "moe_forward_events": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                              vp, vp, sz, vp, ctypes.POINTER(vp), ctypes.c_int]),
+        "moe_get_error": (ctypes.c_int, [vp, vp]),
+        "moe_clear_error": (ctypes.c_int, [vp, vp]),
+        "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
+        "moe_last_error_detail": (ctypes.c_char_p, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    return lib
+
+
+LIB = _load()
+
+
+def _p(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        if not torch.cuda.is_available():
+            return ctypes.c_void_p(None)
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(rc: int, where: str):
+    if rc != MOE_OK:
+        raise MoeError(rc, where, LIB.moe_last_error_detail().decode())
+
+
+def make_shape(T, d, E, k, d_ff, gate="softmax_topk", dtype=torch.bfloat16, capacity=None,
+               d_ff_shared=0, alpha=0.01, beta=1e-3) -> moe_shape:
+    """capacity None means no drop (C = T)."""
+    return moe_shape(T=T, d=d, E=E, k=k, d_ff=d_ff, d_ff_shared=d_ff_shared,
+                     capacity=T if capacity is None else capacity,
+                     gate=GATE_MODES[gate] if isinstance(gate, str) else int(gate),
+                     dtype=DTYPES[dtype] if isinstance(dtype, torch.dtype) else int(dtype),
+                     alpha=alpha, beta=beta)
+
+
+def moe_capacity(cf: float, T: int, k: int, E: int) -> int:
+    return LIB.moe_capacity(cf, T, k, E)
+
+
+def moe_check_shape(s: moe_shape) -> int:
+    return LIB.moe_check_shape(ctypes.byref(s))
+
+
+def moe_workspace_size(s: moe_shape) -> int:
+    return LIB.moe_workspace_size(ctypes.byref(s))
+
+
+def alloc_workspace(s: moe_shape, device="cuda") -> torch.Tensor:
+    """Zero-filled uint8 device buffer of moe_workspace_size bytes (zero = no error)."""
+    n = moe_workspace_size(s)
+    if n == 0:
+        _check(moe_check_shape(s), "moe_workspace_size")
+    ws = torch.zeros(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def moe_route_topk(s, ws, topk_idx, topk_gate, x=None, w_router=None, router_bias=None,
+                   logits_in=None, logits_out=None, stats=None, stream=None):
+    _check(LIB.moe_route_topk(ctypes.byref(s), _p(x), _p(w_router), _p(router_bias), _p(logits_in),
+                              _p(logits_out), _p(topk_idx), _p(topk_gate), _p(stats), _p(ws),
+                              ws.numel(), _stream(stream)), "moe_route_topk")
+
+
+def moe_dispatch(s, ws, counts, offsets, perm, inv, dropped, topk_idx=None, logits_in=None,
+                 stream=None):
+    _check(LIB.moe_dispatch(ctypes.byref(s), _p(topk_idx), _p(logits_in), _p(counts), _p(offsets),
+                            _p(perm), _p(inv), _p(dropped), _p(ws), ws.numel(), _stream(stream)),
+           "moe_dispatch")
+
+
+def moe_grouped_swiglu(s, ws, x, perm, offsets, w1, w3, w2, y_perm, topk_gate=None, w1s=None,
+                       w3s=None, w2s=None, y_shared=None, stream=None):
+    _check(LIB.moe_grouped_swiglu(ctypes.byref(s), _p(x), _p(perm), _p(offsets), _p(topk_gate),
+                                  _p(w1), _p(w3), _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(y_perm),
+                                  _p(y_shared), _p(ws), ws.numel(), _stream(stream)),
+           "moe_grouped_swiglu")
+
+
+def moe_combine(s, y_perm, inv, y, y_shared=None, stream=None):
+    _check(LIB.moe_combine(ctypes.byref(s), _p(y_perm), _p(inv), _p(y_shared), _p(y),
+                           _stream(stream)), "moe_combine")
+
+
+def moe_aux_loss(s, stats, counts, losses, stream=None):
+    _check(LIB.moe_aux_loss(ctypes.byref(s), _p(stats), _p(counts), _p(losses), _stream(stream)),
+           "moe_aux_loss")
+
+
+def moe_forward(s, ws, x, w_router, w1, w3, w2, y, router_bias=None, w1s=None, w3s=None, w2s=None,
+                counts=None, dropped=None, losses=None, stream=None, events=None):
+    if events is None:
+        _check(LIB.moe_forward(ctypes.byref(s), _p(x), _p(w_router), _p(router_bias), _p(w1), _p(w3),
+                               _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(y), _p(counts), _p(dropped),
+                               _p(losses), _p(ws), ws.numel(), _stream(stream)), "moe_forward")
+        return
+    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    _check(LIB.moe_forward_events(ctypes.byref(s), _p(x), _p(w_router), _p(router_bias), _p(w1),
+                                  _p(w3), _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(y), _p(counts),
+                                  _p(dropped), _p(losses), _p(ws), ws.numel(), _stream(stream),
+                                  arr, len(events)), "moe_forward_events")
+
+
+def moe_get_error(ws, stream=None) -> int:
+    return LIB.moe_get_error(_p(ws), _stream(stream))
+
+
+def moe_clear_error(ws, stream=None):
+    _check(LIB.moe_clear_error(_p(ws), _stream(stream)), "moe_clear_error")
+
+
+def moe_status_string(status: int) -> str:
+    return LIB.moe_status_string(status).decode()

@@ -1,0 +1,90 @@
+// Internal host-side launchers shared between the kernel files and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+struct DeviceError;
+
+// ---------------------------------------------------------------- tcgen05 grouped GEMM
+enum TcMode : int { TC_F32OUT = 0, TC_SWIGLU = 1, TC_SCALE = 2 };
+
+struct TcArgs {
+  int groups;               // routed groups G, 1..1024
+  const int32_t* offsets;   // device [G+1] row offsets, or nullptr: one group of m_single rows
+  int m_single;
+  int n_routed;             // output columns per routed group
+  int k_routed;             // reduction length (routed)
+  void* out_routed;
+  long long ldo_routed;     // output row stride, elements
+  int has_shared;           // 1: one extra group over rows [0, m_shared) of its own A and B
+  int m_shared, n_shared, k_shared;
+  void* out_shared;
+  long long ldo_shared;
+  const int32_t* perm;      // TC_SCALE: row r is scaled by gate[perm[r]] (gate == nullptr: 1)
+  const float* gate;
+  const float* bias;        // TC_F32OUT: per-column bias or nullptr
+  DeviceError* err;
+};
+
+struct TcProblem {
+  TcArgs args;
+  const void* a;            // routed A [a_rows, k_routed] bf16
+  long long a_rows;
+  const void* b0;           // routed B [b_groups, b_rows, k_routed] bf16 (TC_SWIGLU: W1)
+  const void* b1;           // TC_SWIGLU: W3, same shape
+  long long b_rows;
+  int b_groups;
+  const void* a_s;          // shared A [m_shared, k_shared]
+  const void* b0_s;         // shared B [b_rows_s, k_shared]
+  const void* b1_s;
+  long long b_rows_s;
+  long long max_tiles;      // host upper bound on the tile count (sizes the grid)
+  int num_sms;
+};
+
+int launch_tc_gemm(int mode, int bn, const TcProblem& p, cudaStream_t stream);
+int tc_smem_bytes(int mode, int bn, int groups);
+
+// ---------------------------------------------------------------- CUDA-core fp32 path
+struct SimtArgs {
+  int groups;               // G; offsets == nullptr means one group of m_single rows
+  const int32_t* offsets;
+  int m_single;
+  int max_rows;             // upper bound of rows in any group (grid.y)
+  const float* a;           // A [*, k] fp32, rows addressed by group offsets
+  const float* b0;          // B [G, n, k] (TC_SWIGLU: W1)
+  const float* b1;          // TC_SWIGLU: W3
+  int n, k;
+  float* out;               // [*, n]
+  const int32_t* perm;      // TC_SCALE gates
+  const float* gate;
+  const float* bias;        // TC_F32OUT bias
+};
+int launch_simt_gemm(int mode, const SimtArgs& a, cudaStream_t stream);
+
+// ---------------------------------------------------------------- routing
+int route_blocks(int T);
+int launch_route_topk(const float* logits, int T, int E, int k, int gate_mode, int32_t* topk_idx,
+                      float* topk_gate, float* partials, DeviceError* err, cudaStream_t stream);
+int launch_stats_reduce(const float* partials, int nblocks, int E, float* stats,
+                        cudaStream_t stream);
+int launch_aux_loss(const float* stats, const int32_t* counts, int T, int E, int k, float alpha,
+                    float beta, float* losses, cudaStream_t stream);
+
+// ---------------------------------------------------------------- dispatch
+int launch_dispatch(const int32_t* topk_idx, int A, int E, int C, int32_t* counts,
+                    int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dropped,
+                    DeviceError* err, cudaStream_t stream);
+
+// ---------------------------------------------------------------- data movement
+int launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, int E, int k,
+                  int row_bytes, int max_rows, void* xp, int num_sms, cudaStream_t stream);
+int launch_combine(int dtype, const void* yp, const int32_t* inv, const void* ys, void* y, int T,
+                   int k, int d, int num_sms, cudaStream_t stream);
+
+}  // namespace moe

@@ -1,0 +1,641 @@
+// C ABI of libmoe (declared in include/moe.h): argument checks on the host, the workspace
+// layout, and the launch sequence of the forward pass on the caller's stream.
+#include <algorithm>
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+
+#include "common.cuh"
+#include "launchers.h"
+
+namespace moe {
+namespace {
+
+thread_local std::string g_detail;
+
+int fail(int status, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof(buf), fmt, ap);
+  va_end(ap);
+  g_detail = buf;
+  return status;
+}
+
+int ok() {
+  g_detail.clear();
+  return MOE_OK;
+}
+
+size_t esize(const moe_shape* s) { return s->dtype == MOE_BF16 ? 2 : 4; }
+
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
+
+struct Layout {
+  size_t err, logits, idx, gate, partials, stats, counts, offsets, perm, inv, dropped, losses;
+  size_t xp, h, yp, hs, ys, total;
+};
+
+Layout layout(const moe_shape* s) {
+  const size_t T = s->T, E = s->E, k = s->k, d = s->d, F = s->d_ff, Fs = s->d_ff_shared;
+  const size_t es = esize(s);
+  const size_t A = T * k;
+  Layout L;
+  size_t o = 0;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + std::max<size_t>(bytes, 1));
+    return at;
+  };
+  L.err = take(sizeof(DeviceError));
+  L.logits = take(T * E * 4);
+  L.idx = take(A * 4);
+  L.gate = take(A * 4);
+  L.partials = take(static_cast<size_t>(route_blocks(s->T)) * (E + 1) * 4);
+  L.stats = take((E + 1) * 4);
+  L.counts = take(E * 4);
+  L.offsets = take((E + 1) * 4);
+  L.perm = take(A * 4);
+  L.inv = take(A * 4);
+  L.dropped = take(4);
+  L.losses = take(2 * 4);
+  L.xp = take(A * d * es);
+  L.h = take(A * F * es);
+  L.yp = take(A * d * es);
+  L.hs = take(Fs > 0 ? T * Fs * es : 0);
+  L.ys = take(Fs > 0 ? T * d * es : 0);
+  L.total = o;
+  return L;
+}
+
+int check_shape(const moe_shape* s) {
+  if (s == nullptr) return fail(MOE_ERR_INVALID, "shape is NULL");
+  if (s->T < 0) return fail(MOE_ERR_INVALID, "T = %d < 0", s->T);
+  if (s->d < 1) return fail(MOE_ERR_INVALID, "d = %d < 1", s->d);
+  if (s->E < 1 || s->E > 1024) return fail(MOE_ERR_INVALID, "E = %d outside 1..1024", s->E);
+  if (s->k < 1 || s->k > s->E) return fail(MOE_ERR_INVALID, "k = %d outside 1..E (E = %d)", s->k, s->E);
+  if (s->d_ff < 1) return fail(MOE_ERR_INVALID, "d_ff = %d < 1", s->d_ff);
+  if (s->d_ff_shared < 0) return fail(MOE_ERR_INVALID, "d_ff_shared = %d < 0", s->d_ff_shared);
+  if (s->capacity < 0) return fail(MOE_ERR_INVALID, "capacity = %d < 0", s->capacity);
+  if (s->gate < MOE_GATE_SOFTMAX_ALL || s->gate > MOE_GATE_SIGMOID_TOPK)
+    return fail(MOE_ERR_INVALID, "gate mode %d unknown", s->gate);
+  if (s->dtype != MOE_F32 && s->dtype != MOE_BF16)
+    return fail(MOE_ERR_INVALID, "dtype %d unknown", s->dtype);
+  if (static_cast<long long>(s->T) * s->k >= (1ll << 31))
+    return fail(MOE_ERR_INVALID, "T*k = %lld does not fit int32", static_cast<long long>(s->T) * s->k);
+  if ((static_cast<size_t>(s->d) * esize(s)) % 16 != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "d * sizeof(dtype) = %zu is not a multiple of 16 bytes",
+                static_cast<size_t>(s->d) * esize(s));
+  if (s->dtype == MOE_BF16 && (s->d_ff % 8 != 0 || s->d_ff_shared % 8 != 0))
+    return fail(MOE_ERR_UNSUPPORTED, "bf16 needs d_ff and d_ff_shared multiples of 8");
+  if (s->dtype == MOE_F32 && ((s->T + 31) / 32 > 65535))
+    return fail(MOE_ERR_UNSUPPORTED, "fp32 path supports T <= %d", 65535 * 32);
+  return MOE_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+#define REQUIRE_PTR(p, name)                                                 \
+  do {                                                                       \
+    if ((p) == nullptr) return fail(MOE_ERR_INVALID, "%s is NULL", name);    \
+    if (!aligned16(p)) return fail(MOE_ERR_INVALID, "%s is not 16-byte aligned", name); \
+  } while (0)
+#define REQUIRE_PTR4(p, name)                                                \
+  do {                                                                       \
+    if ((p) == nullptr) return fail(MOE_ERR_INVALID, "%s is NULL", name);    \
+    if (!aligned4(p)) return fail(MOE_ERR_INVALID, "%s is not 4-byte aligned", name); \
+  } while (0)
+#define OPT_PTR4(p, name)                                                    \
+  do {                                                                       \
+    if ((p) != nullptr && !aligned4(p))                                      \
+      return fail(MOE_ERR_INVALID, "%s is not 4-byte aligned", name);        \
+  } while (0)
+#define TRY(expr)                       \
+  do {                                  \
+    const int rc_ = (expr);             \
+    if (rc_ != MOE_OK) return rc_;      \
+  } while (0)
+
+int check_ws(const moe_shape* s, const void* ws, size_t ws_bytes) {
+  if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+    return fail(MOE_ERR_WORKSPACE, "workspace is not %zu-byte aligned", kAlign);
+  const size_t need = layout(s).total;
+  if (ws_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, need);
+  return MOE_OK;
+}
+
+template <typename T>
+T* at(void* ws, size_t off) {
+  return reinterpret_cast<T*>(static_cast<uint8_t*>(ws) + off);
+}
+
+int num_sms() {
+  int dev = 0, n = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 148;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 148;
+  return n;
+}
+
+int cuda_status(const char* what) {
+  const cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  return MOE_OK;
+}
+
+#define LAUNCH(expr, what)                                                   \
+  do {                                                                       \
+    const int rc_ = (expr);                                                  \
+    if (rc_ != MOE_OK) {                                                     \
+      if (rc_ == MOE_ERR_CUDA) return cuda_status(what);                     \
+      return fail(rc_, "%s failed", what);                                   \
+    }                                                                        \
+  } while (0)
+
+int pick_router_bn(int E) {
+  if (E <= 16) return 16;
+  if (E <= 32) return 32;
+  if (E <= 64) return 64;
+  if (E <= 128) return 128;
+  return 256;
+}
+
+// ---------------------------------------------------------------- stage 0: router GEMM
+int run_router(const moe_shape* s, const void* x, const void* wr, const float* bias, float* logits,
+               DeviceError* err, cudaStream_t st) {
+  if (s->T == 0) return MOE_OK;
+  if (s->dtype == MOE_F32) {
+    SimtArgs a{};
+    a.groups = 1;
+    a.offsets = nullptr;
+    a.m_single = s->T;
+    a.max_rows = s->T;
+    a.a = static_cast<const float*>(x);
+    a.b0 = static_cast<const float*>(wr);
+    a.n = s->E;
+    a.k = s->d;
+    a.out = logits;
+    a.bias = bias;
+    LAUNCH(launch_simt_gemm(TC_F32OUT, a, st), "router GEMM (fp32)");
+    return MOE_OK;
+  }
+  const int bn = pick_router_bn(s->E);
+  TcProblem p{};
+  p.args.groups = 1;
+  p.args.offsets = nullptr;
+  p.args.m_single = s->T;
+  p.args.n_routed = s->E;
+  p.args.k_routed = s->d;
+  p.args.out_routed = logits;
+  p.args.ldo_routed = s->E;
+  p.args.bias = bias;
+  p.args.err = err;
+  p.a = x;
+  p.a_rows = s->T;
+  p.b0 = wr;
+  p.b_rows = s->E;
+  p.b_groups = 1;
+  p.max_tiles = static_cast<long long>((s->T + 127) / 128) * ((s->E + bn - 1) / bn);
+  p.num_sms = num_sms();
+  LAUNCH(launch_tc_gemm(TC_F32OUT, bn, p, st), "router GEMM (tcgen05)");
+  return MOE_OK;
+}
+
+// ---------------------------------------------------------------- stages 4-5: expert GEMMs
+int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const int32_t* offsets,
+                const float* gate, const void* w1, const void* w3, const void* w2, const void* w1s,
+                const void* w3s, const void* w2s, void* y_perm, void* y_shared, void* ws,
+                cudaStream_t st, void* const* ev, int ev_first) {
+  const Layout L = layout(s);
+  DeviceError* err = at<DeviceError>(ws, L.err);
+  const int A = s->T * s->k;
+  const bool shared = s->d_ff_shared > 0;
+  void* xp = at<void>(ws, L.xp);
+  void* h = at<void>(ws, L.h);
+  void* hs = at<void>(ws, L.hs);
+  const int sms = num_sms();
+  const int max_group_rows = std::min(s->T, s->capacity);
+
+  auto rec = [&](int i) {
+    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+  };
+
+  // stage 3: gather
+  rec(ev_first);
+  LAUNCH(launch_gather(x, perm, offsets, s->E, s->k, static_cast<int>(s->d * esize(s)), A, xp, sms, st),
+         "gather");
+
+  if (s->dtype == MOE_F32) {
+    rec(ev_first + 1);
+    SimtArgs g1{};
+    g1.groups = s->E;
+    g1.offsets = offsets;
+    g1.max_rows = max_group_rows;
+    g1.a = static_cast<const float*>(xp);
+    g1.b0 = static_cast<const float*>(w1);
+    g1.b1 = static_cast<const float*>(w3);
+    g1.n = s->d_ff;
+    g1.k = s->d;
+    g1.out = static_cast<float*>(h);
+    LAUNCH(launch_simt_gemm(TC_SWIGLU, g1, st), "gate/up GEMM (fp32)");
+    if (shared) {
+      SimtArgs gs = g1;
+      gs.groups = 1;
+      gs.offsets = nullptr;
+      gs.m_single = s->T;
+      gs.max_rows = s->T;
+      gs.a = static_cast<const float*>(x);
+      gs.b0 = static_cast<const float*>(w1s);
+      gs.b1 = static_cast<const float*>(w3s);
+      gs.n = s->d_ff_shared;
+      gs.out = static_cast<float*>(hs);
+      LAUNCH(launch_simt_gemm(TC_SWIGLU, gs, st), "shared gate/up GEMM (fp32)");
+    }
+    rec(ev_first + 2);
+    SimtArgs g2{};
+    g2.groups = s->E;
+    g2.offsets = offsets;
+    g2.max_rows = max_group_rows;
+    g2.a = static_cast<const float*>(h);
+    g2.b0 = static_cast<const float*>(w2);
+    g2.n = s->d;
+    g2.k = s->d_ff;
+    g2.out = static_cast<float*>(y_perm);
+    g2.perm = perm;
+    g2.gate = gate;
+    LAUNCH(launch_simt_gemm(TC_SCALE, g2, st), "down GEMM (fp32)");
+    if (shared) {
+      SimtArgs gs = g2;
+      gs.groups = 1;
+      gs.offsets = nullptr;
+      gs.m_single = s->T;
+      gs.max_rows = s->T;
+      gs.a = static_cast<const float*>(hs);
+      gs.b0 = static_cast<const float*>(w2s);
+      gs.k = s->d_ff_shared;
+      gs.out = static_cast<float*>(y_shared);
+      gs.perm = nullptr;
+      gs.gate = nullptr;
+      LAUNCH(launch_simt_gemm(TC_SCALE, gs, st), "shared down GEMM (fp32)");
+    }
+    return MOE_OK;
+  }
+
+  // bf16: tcgen05 grouped GEMMs, routed experts and the shared expert in one launch each
+  const long long kept_max = std::min<long long>(A, static_cast<long long>(s->E) * max_group_rows);
+  const long long mt_routed = (kept_max + 127) / 128 + s->E;
+  const long long mt_shared = shared ? (s->T + 127) / 128 : 0;
+
+  rec(ev_first + 1);
+  {
+    TcProblem p{};
+    p.args.groups = s->E;
+    p.args.offsets = offsets;
+    p.args.n_routed = s->d_ff;
+    p.args.k_routed = s->d;
+    p.args.out_routed = h;
+    p.args.ldo_routed = s->d_ff;
+    p.args.has_shared = shared;
+    p.args.m_shared = s->T;
+    p.args.n_shared = s->d_ff_shared;
+    p.args.k_shared = s->d;
+    p.args.out_shared = hs;
+    p.args.ldo_shared = s->d_ff_shared;
+    p.args.err = err;
+    p.a = xp;
+    p.a_rows = std::max(A, 1);
+    p.b0 = w1;
+    p.b1 = w3;
+    p.b_rows = s->d_ff;
+    p.b_groups = s->E;
+    p.a_s = x;
+    p.b0_s = w1s;
+    p.b1_s = w3s;
+    p.b_rows_s = s->d_ff_shared;
+    p.max_tiles = mt_routed * ((s->d_ff + 127) / 128) + mt_shared * ((s->d_ff_shared + 127) / 128);
+    p.num_sms = sms;
+    LAUNCH(launch_tc_gemm(TC_SWIGLU, 256, p, st), "gate/up GEMM (tcgen05)");
+  }
+  rec(ev_first + 2);
+  {
+    TcProblem p{};
+    p.args.groups = s->E;
+    p.args.offsets = offsets;
+    p.args.n_routed = s->d;
+    p.args.k_routed = s->d_ff;
+    p.args.out_routed = y_perm;
+    p.args.ldo_routed = s->d;
+    p.args.has_shared = shared;
+    p.args.m_shared = s->T;
+    p.args.n_shared = s->d;
+    p.args.k_shared = s->d_ff_shared;
+    p.args.out_shared = y_shared;
+    p.args.ldo_shared = s->d;
+    p.args.perm = perm;
+    p.args.gate = gate;
+    p.args.err = err;
+    p.a = h;
+    p.a_rows = std::max(A, 1);
+    p.b0 = w2;
+    p.b_rows = s->d;
+    p.b_groups = s->E;
+    p.a_s = hs;
+    p.b0_s = w2s;
+    p.b_rows_s = s->d;
+    const int bn = 256;
+    p.max_tiles = (mt_routed + mt_shared) * ((s->d + bn - 1) / bn);
+    p.num_sms = sms;
+    LAUNCH(launch_tc_gemm(TC_SCALE, bn, p, st), "down GEMM (tcgen05)");
+  }
+  return MOE_OK;
+}
+
+int forward_impl(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
+                 const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
+                 const void* w2s, void* y, int32_t* counts, int32_t* dropped, float* losses,
+                 void* ws, size_t ws_bytes, void* stream, void* const* ev, int n_ev) {
+  TRY(check_shape(s));
+  TRY(check_ws(s, ws, ws_bytes));
+  if (ev != nullptr && n_ev != MOE_NUM_STAGES + 1)
+    return fail(MOE_ERR_INVALID, "n_events = %d, expected %d", n_ev, MOE_NUM_STAGES + 1);
+  if (s->T > 0) {
+    REQUIRE_PTR(x, "x");
+    REQUIRE_PTR(w_router, "w_router");
+    REQUIRE_PTR(w1, "w1");
+    REQUIRE_PTR(w3, "w3");
+    REQUIRE_PTR(w2, "w2");
+    REQUIRE_PTR(y, "y");
+    if (s->d_ff_shared > 0) {
+      REQUIRE_PTR(w1s, "w1s");
+      REQUIRE_PTR(w3s, "w3s");
+      REQUIRE_PTR(w2s, "w2s");
+    }
+  }
+  OPT_PTR4(router_bias, "router_bias");
+  OPT_PTR4(counts, "counts");
+  OPT_PTR4(dropped, "dropped");
+  OPT_PTR4(losses, "losses");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(s);
+  DeviceError* err = at<DeviceError>(ws, L.err);
+  float* logits = at<float>(ws, L.logits);
+  int32_t* idx = at<int32_t>(ws, L.idx);
+  float* gate = at<float>(ws, L.gate);
+  float* partials = at<float>(ws, L.partials);
+  float* stats = at<float>(ws, L.stats);
+  int32_t* cnt = counts ? counts : at<int32_t>(ws, L.counts);
+  int32_t* off = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* inv = at<int32_t>(ws, L.inv);
+  int32_t* drp = dropped ? dropped : at<int32_t>(ws, L.dropped);
+  float* los = losses ? losses : at<float>(ws, L.losses);
+  void* yp = at<void>(ws, L.yp);
+  void* ys = s->d_ff_shared > 0 ? at<void>(ws, L.ys) : nullptr;
+  auto rec = [&](int i) {
+    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+  };
+
+  rec(0);
+  TRY(run_router(s, x, w_router, router_bias, logits, err, st));
+  rec(1);
+  if (s->T > 0)
+    LAUNCH(launch_route_topk(logits, s->T, s->E, s->k, s->gate, idx, gate, partials, err, st),
+           "gates/top-k");
+  rec(2);
+  LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, cnt, off, perm, inv, drp, err, st),
+         "dispatch");
+  if (s->T > 0) {
+    TRY(run_experts(s, x, perm, off, gate, w1, w3, w2, w1s, w3s, w2s, yp, ys, ws, st, ev, 3));
+  } else {
+    rec(3);
+    rec(4);
+    rec(5);
+  }
+  rec(6);
+  LAUNCH(launch_combine(s->dtype, yp, inv, ys, y, s->T, s->k, s->d, num_sms(), st), "combine");
+  rec(7);
+  if (s->T > 0) {
+    LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
+  }
+  LAUNCH(launch_aux_loss(stats, cnt, s->T, s->E, s->k, s->alpha, s->beta, los, st), "aux loss");
+  rec(8);
+  return ok();
+}
+
+}  // namespace
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_capacity(double cf, int32_t T, int32_t k, int32_t E) {
+  if (E < 1 || k < 1 || T < 0 || !(cf >= 0.0)) return -1;
+  const double c = std::ceil(cf * static_cast<double>(T) * static_cast<double>(k) /
+                             static_cast<double>(E));
+  if (c >= static_cast<double>(T)) return T;
+  return static_cast<int>(c);
+}
+
+int moe_check_shape(const moe_shape* s) {
+  const int rc = check_shape(s);
+  return rc == MOE_OK ? ok() : rc;
+}
+
+size_t moe_workspace_size(const moe_shape* s) {
+  if (check_shape(s) != MOE_OK) return 0;
+  return layout(s).total;
+}
+
+int moe_route_topk(const moe_shape* s, const void* x, const void* w_router,
+                   const float* router_bias, const float* logits_in, float* logits_out,
+                   int32_t* topk_idx, float* topk_gate, float* stats, void* ws, size_t ws_bytes,
+                   void* stream) {
+  TRY(check_shape(s));
+  TRY(check_ws(s, ws, ws_bytes));
+  if (s->T > 0) {
+    if (logits_in == nullptr) {
+      REQUIRE_PTR(x, "x");
+      REQUIRE_PTR(w_router, "w_router");
+      OPT_PTR4(router_bias, "router_bias");
+    } else {
+      REQUIRE_PTR4(logits_in, "logits_in");
+    }
+    REQUIRE_PTR4(topk_idx, "topk_idx");
+    REQUIRE_PTR4(topk_gate, "topk_gate");
+  }
+  OPT_PTR4(logits_out, "logits_out");
+  OPT_PTR4(stats, "stats");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(s);
+  DeviceError* err = at<DeviceError>(ws, L.err);
+  if (s->T == 0) {
+    if (stats && cudaMemsetAsync(stats, 0, (s->E + 1) * sizeof(float), st) != cudaSuccess)
+      return cuda_status("memset stats");
+    return ok();
+  }
+  const float* logits = logits_in;
+  if (logits == nullptr) {
+    float* dst = logits_out ? logits_out : at<float>(ws, L.logits);
+    TRY(run_router(s, x, w_router, router_bias, dst, err, st));
+    logits = dst;
+  } else if (logits_out != nullptr && logits_out != logits_in) {
+    if (cudaMemcpyAsync(logits_out, logits_in, static_cast<size_t>(s->T) * s->E * sizeof(float),
+                        cudaMemcpyDeviceToDevice, st) != cudaSuccess)
+      return cuda_status("copy logits");
+  }
+  float* partials = at<float>(ws, L.partials);
+  LAUNCH(launch_route_topk(logits, s->T, s->E, s->k, s->gate, topk_idx, topk_gate, partials, err, st),
+         "gates/top-k");
+  if (stats) LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
+  return ok();
+}
+
+int moe_dispatch(const moe_shape* s, const int32_t* topk_idx, const float* logits_in,
+                 int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dropped,
+                 void* ws, size_t ws_bytes, void* stream) {
+  TRY(check_shape(s));
+  TRY(check_ws(s, ws, ws_bytes));
+  REQUIRE_PTR4(counts, "counts");
+  REQUIRE_PTR4(offsets, "offsets");
+  REQUIRE_PTR4(dropped, "dropped");
+  if (s->T > 0) {
+    if (topk_idx == nullptr) REQUIRE_PTR4(logits_in, "logits_in (topk_idx is NULL)");
+    else REQUIRE_PTR4(topk_idx, "topk_idx");
+    REQUIRE_PTR4(perm, "perm");
+    REQUIRE_PTR4(inv, "inv");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(s);
+  DeviceError* err = at<DeviceError>(ws, L.err);
+  const int32_t* idx = topk_idx;
+  if (idx == nullptr && s->T > 0) {
+    int32_t* widx = at<int32_t>(ws, L.idx);
+    LAUNCH(launch_route_topk(logits_in, s->T, s->E, s->k, s->gate, widx, at<float>(ws, L.gate),
+                             at<float>(ws, L.partials), err, st),
+           "gates/top-k");
+    idx = widx;
+  }
+  LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, counts, offsets, perm, inv, dropped,
+                         err, st),
+         "dispatch");
+  return ok();
+}
+
+int moe_grouped_swiglu(const moe_shape* s, const void* x, const int32_t* perm,
+                       const int32_t* offsets, const float* topk_gate, const void* w1,
+                       const void* w3, const void* w2, const void* w1s, const void* w3s,
+                       const void* w2s, void* y_perm, void* y_shared, void* ws, size_t ws_bytes,
+                       void* stream) {
+  TRY(check_shape(s));
+  TRY(check_ws(s, ws, ws_bytes));
+  if (s->T == 0) return ok();
+  REQUIRE_PTR(x, "x");
+  REQUIRE_PTR4(perm, "perm");
+  REQUIRE_PTR4(offsets, "offsets");
+  OPT_PTR4(topk_gate, "topk_gate");
+  REQUIRE_PTR(w1, "w1");
+  REQUIRE_PTR(w3, "w3");
+  REQUIRE_PTR(w2, "w2");
+  REQUIRE_PTR(y_perm, "y_perm");
+  if (s->d_ff_shared > 0) {
+    REQUIRE_PTR(w1s, "w1s");
+    REQUIRE_PTR(w3s, "w3s");
+    REQUIRE_PTR(w2s, "w2s");
+    REQUIRE_PTR(y_shared, "y_shared");
+  }
+  TRY(run_experts(s, x, perm, offsets, topk_gate, w1, w3, w2, w1s, w3s, w2s, y_perm,
+                  s->d_ff_shared > 0 ? y_shared : nullptr, ws, static_cast<cudaStream_t>(stream),
+                  nullptr, 0));
+  return ok();
+}
+
+int moe_combine(const moe_shape* s, const void* y_perm, const int32_t* inv, const void* y_shared,
+                void* y, void* stream) {
+  TRY(check_shape(s));
+  if (s->T == 0) return ok();
+  REQUIRE_PTR(y_perm, "y_perm");
+  REQUIRE_PTR4(inv, "inv");
+  REQUIRE_PTR(y, "y");
+  if (y_shared != nullptr && !aligned16(y_shared))
+    return fail(MOE_ERR_INVALID, "y_shared is not 16-byte aligned");
+  LAUNCH(launch_combine(s->dtype, y_perm, inv, y_shared, y, s->T, s->k, s->d, num_sms(),
+                        static_cast<cudaStream_t>(stream)),
+         "combine");
+  return ok();
+}
+
+int moe_aux_loss(const moe_shape* s, const float* stats, const int32_t* counts, float* losses,
+                 void* stream) {
+  TRY(check_shape(s));
+  REQUIRE_PTR4(stats, "stats");
+  REQUIRE_PTR4(counts, "counts");
+  REQUIRE_PTR4(losses, "losses");
+  LAUNCH(launch_aux_loss(stats, counts, s->T, s->E, s->k, s->alpha, s->beta, losses,
+                         static_cast<cudaStream_t>(stream)),
+         "aux loss");
+  return ok();
+}
+
+int moe_forward(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
+                const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
+                const void* w2s, void* y, int32_t* counts, int32_t* dropped, float* losses,
+                void* ws, size_t ws_bytes, void* stream) {
+  return forward_impl(s, x, w_router, router_bias, w1, w3, w2, w1s, w3s, w2s, y, counts, dropped,
+                      losses, ws, ws_bytes, stream, nullptr, 0);
+}
+
+int moe_forward_events(const moe_shape* s, const void* x, const void* w_router,
+                       const float* router_bias, const void* w1, const void* w3, const void* w2,
+                       const void* w1s, const void* w3s, const void* w2s, void* y,
+                       int32_t* counts, int32_t* dropped, float* losses, void* ws,
+                       size_t ws_bytes, void* stream, void* const* events, int n_events) {
+  if (events == nullptr) return fail(MOE_ERR_INVALID, "events is NULL");
+  return forward_impl(s, x, w_router, router_bias, w1, w3, w2, w1s, w3s, w2s, y, counts, dropped,
+                      losses, ws, ws_bytes, stream, events, n_events);
+}
+
+int moe_get_error(const void* ws, void* stream) {
+  if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  DeviceError h{};
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (cudaMemcpyAsync(&h, ws, sizeof(h), cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return cuda_status("read error word");
+  if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_status("synchronize");
+  if (h.code != 0) {
+    g_detail = "device error at site " + std::to_string(h.where) + ", detail " +
+               std::to_string(h.detail);
+    return h.code;
+  }
+  return ok();
+}
+
+int moe_clear_error(void* ws, void* stream) {
+  if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if (cudaMemsetAsync(ws, 0, sizeof(DeviceError), static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return cuda_status("clear error word");
+  return ok();
+}
+
+const char* moe_status_string(int status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported shape";
+    case MOE_ERR_CUDA: return "CUDA error";
+    case MOE_ERR_WORKSPACE: return "workspace missing or too small";
+    case MOE_ERR_TIMEOUT: return "device wait timed out";
+    case MOE_ERR_NONFINITE: return "non-finite router logit";
+    default: return "unknown status";
+  }
+}
+
+const char* moe_last_error_detail(void) { return g_detail.c_str(); }
+
+}  // extern "C"

@@ -1,0 +1,229 @@
+// Gates and top-k selection (one warp per token), the router statistics needed by the
+// balance losses, and the losses themselves.
+//
+// "Mixture of experts (MoE)" (tirogla.com), How it works:
+//   step 1 (score): gate conventions -- softmax over all E (Switch, GShard), softmax over
+//          only the selected logits (Mixtral), sigmoid affinities normalised over the
+//          selected experts (DeepSeek-V3);
+//   step 2 (select): top-k experts per token;
+//   step 6 (balance): L_aux = alpha*E*sum_i f_i*P_i and the z-loss beta*mean(lse^2).
+// "DL S077 - Mixture of Experts (MoE) Intuition", section 2: top-2 then softmax over the
+// two selected logits.
+//
+// Selection compares the raw fp32 logits: largest first, the lower expert index winning a
+// tie (-0.0 and +0.0 tie). Every reduction runs in a fixed order, so results are
+// bit-for-bit reproducible run to run.
+#include <algorithm>
+
+#include "common.cuh"
+#include "launchers.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kRouteWarps = 8;
+constexpr int kRouteThreads = kRouteWarps * 32;
+constexpr int kNoIdx = 0x7fffffff;
+
+// JM = values per lane: lane l holds the logits of experts l, l+32, ..., l+32*(JM-1).
+template <int JM>
+__global__ void __launch_bounds__(kRouteThreads)
+route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int gate_mode,
+                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
+                  float* __restrict__ partials, DeviceError* err) {
+  extern __shared__ float s_part[];  // [kRouteWarps][E + 1]
+  const int lane = threadIdx.x & 31;
+  const int warp = threadIdx.x >> 5;
+
+  float pacc[JM];
+#pragma unroll
+  for (int j = 0; j < JM; ++j) pacc[j] = 0.f;
+  float lse2 = 0.f;
+
+  const int nwarps = gridDim.x * kRouteWarps;
+  for (int t = blockIdx.x * kRouteWarps + warp; t < T; t += nwarps) {
+    const float* row = logits + static_cast<size_t>(t) * E;
+    float v[JM], ex[JM];
+    int slot[JM];
+    bool bad = false;
+#pragma unroll
+    for (int j = 0; j < JM; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = (e < E) ? __ldg(row + e) : -INFINITY;
+      slot[j] = -1;
+      if (e < E && !isfinite(v[j])) bad = true;
+    }
+    if (__any_sync(0xffffffffu, bad)) {
+      if (lane == 0) record_error(err, MOE_ERR_NONFINITE, SITE_ROUTE_NONFINITE, t);
+    }
+
+    // softmax over all E (for the gates of SOFTMAX_ALL and for P_i), and lse for L_z
+    float m = -INFINITY;
+#pragma unroll
+    for (int j = 0; j < JM; ++j) m = fmaxf(m, v[j]);
+    m = warp_max(m);
+    float s = 0.f;
+#pragma unroll
+    for (int j = 0; j < JM; ++j) {
+      ex[j] = (lane + 32 * j < E) ? expf(v[j] - m) : 0.f;
+      s += ex[j];
+    }
+    s = warp_sum(s);
+#pragma unroll
+    for (int j = 0; j < JM; ++j) pacc[j] += ex[j] / s;
+    const float lse = m + logf(s);
+    if (lane == 0) lse2 += lse * lse;
+
+    // k rounds of a warp arg-max over the not-yet-selected experts
+    for (int r = 0; r < k; ++r) {
+      float bv = -INFINITY;
+      int bi = kNoIdx;
+#pragma unroll
+      for (int j = 0; j < JM; ++j) {
+        const int e = lane + 32 * j;
+        // j ascending means e ascending: a strict '>' keeps the lowest index among equals
+        if (e < E && slot[j] < 0 && (bi == kNoIdx || v[j] > bv)) {
+          bv = v[j];
+          bi = e;
+        }
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+        if (oi != kNoIdx && (bi == kNoIdx || ov > bv || (ov == bv && oi < bi))) {
+          bv = ov;
+          bi = oi;
+        }
+      }
+      if ((bi & 31) == lane) {
+#pragma unroll
+        for (int j = 0; j < JM; ++j)
+          if (j == (bi >> 5)) slot[j] = r;
+      }
+    }
+
+    // gates of the selected experts
+    float sel_sum = 0.f;
+    float aff[JM];
+#pragma unroll
+    for (int j = 0; j < JM; ++j) {
+      aff[j] = 0.f;
+      if (slot[j] >= 0) {
+        if (gate_mode == MOE_GATE_SIGMOID_TOPK)
+          aff[j] = 1.0f / (1.0f + expf(-v[j]));
+        else
+          aff[j] = ex[j];
+        sel_sum += aff[j];
+      }
+    }
+    if (gate_mode != MOE_GATE_SOFTMAX_ALL) sel_sum = warp_sum(sel_sum);
+    const float denom = (gate_mode == MOE_GATE_SOFTMAX_ALL) ? s : sel_sum;
+#pragma unroll
+    for (int j = 0; j < JM; ++j) {
+      if (slot[j] >= 0) {
+        const size_t o = static_cast<size_t>(t) * k + slot[j];
+        topk_idx[o] = lane + 32 * j;
+        topk_gate[o] = aff[j] / denom;
+      }
+    }
+  }
+
+  // per-block partial sums of p_{t,i} and lse^2, reduced over warps in a fixed order
+#pragma unroll
+  for (int j = 0; j < JM; ++j) {
+    const int e = lane + 32 * j;
+    if (e < E) s_part[warp * (E + 1) + e] = pacc[j];
+  }
+  if (lane == 0) s_part[warp * (E + 1) + E] = lse2;
+  __syncthreads();
+  for (int e = threadIdx.x; e <= E; e += blockDim.x) {
+    float acc = 0.f;
+    for (int w = 0; w < kRouteWarps; ++w) acc += s_part[w * (E + 1) + e];
+    partials[static_cast<size_t>(blockIdx.x) * (E + 1) + e] = acc;
+  }
+}
+
+// stats[e] = sum over blocks (in block order) of partials[b][e], accumulated in double.
+__global__ void stats_reduce_kernel(const float* __restrict__ partials, int nb, int E,
+                                    float* __restrict__ stats) {
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e <= E; e += gridDim.x * blockDim.x) {
+    double acc = 0.0;
+    for (int b = 0; b < nb; ++b) acc += partials[static_cast<size_t>(b) * (E + 1) + e];
+    stats[e] = static_cast<float>(acc);
+  }
+}
+
+// losses[0] = alpha*E*sum_i (counts_i/(T*k)) * (stats_i/T); losses[1] = beta*stats[E]/T.
+__global__ void aux_loss_kernel(const float* __restrict__ stats, const int32_t* __restrict__ counts,
+                                int T, int E, int k, float alpha, float beta,
+                                float* __restrict__ losses) {
+  __shared__ double s_red[256];
+  double acc = 0.0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    acc += static_cast<double>(counts[i]) * static_cast<double>(stats[i]);
+  s_red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    if (T == 0) {
+      losses[0] = 0.f;
+      losses[1] = 0.f;
+    } else {
+      const double Td = static_cast<double>(T);
+      losses[0] = static_cast<float>(static_cast<double>(alpha) * E * s_red[0] /
+                                     (Td * static_cast<double>(k) * Td));
+      losses[1] = static_cast<float>(static_cast<double>(beta) * stats[E] / Td);
+    }
+  }
+}
+
+template <int JM>
+int launch_jm(const float* logits, int T, int E, int k, int gate_mode, int32_t* idx, float* gate,
+              float* partials, DeviceError* err, cudaStream_t stream) {
+  const int nb = route_blocks(T);
+  const size_t smem = static_cast<size_t>(kRouteWarps) * (E + 1) * sizeof(float);
+  route_topk_kernel<JM><<<nb, kRouteThreads, smem, stream>>>(logits, T, E, k, gate_mode, idx,
+                                                              gate, partials, err);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+// Grid of the top-k kernel: a function of T alone, so the reduction order (and hence every
+// bit of the statistics) does not depend on the device.
+int route_blocks(int T) {
+  const int nb = (T + kRouteWarps - 1) / kRouteWarps;
+  return std::max(1, std::min(nb, 1024));
+}
+
+int launch_route_topk(const float* logits, int T, int E, int k, int gate_mode, int32_t* topk_idx,
+                      float* topk_gate, float* partials, DeviceError* err, cudaStream_t stream) {
+  const int jm = (E + 31) / 32;
+  if (jm <= 1) return launch_jm<1>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
+  if (jm <= 2) return launch_jm<2>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
+  if (jm <= 4) return launch_jm<4>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
+  if (jm <= 8) return launch_jm<8>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
+  if (jm <= 16) return launch_jm<16>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
+  return launch_jm<32>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
+}
+
+int launch_stats_reduce(const float* partials, int nblocks, int E, float* stats,
+                        cudaStream_t stream) {
+  const int threads = 256;
+  const int blocks = (E + 1 + threads - 1) / threads;
+  stats_reduce_kernel<<<blocks, threads, 0, stream>>>(partials, nblocks, E, stats);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_aux_loss(const float* stats, const int32_t* counts, int T, int E, int k, float alpha,
+                    float beta, float* losses, cudaStream_t stream) {
+  aux_loss_kernel<<<1, 256, 0, stream>>>(stats, counts, T, E, k, alpha, beta, losses);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace moe

@@ -1,0 +1,515 @@
+// Grouped GEMM on the 5th-generation tensor cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// One persistent kernel computes C = A . B^T for a list of groups that share B's shape:
+// the routed experts (group e owns the contiguous rows [offsets[e], offsets[e+1]) of A and
+// the weight slice B[e]) and, optionally, one always-active shared expert (rows [0, M_s)
+// of its own A and B). This is the "grouped GEMM over the contiguous per-expert batches"
+// of "Mixture of experts (MoE)" (tirogla.com), How it works step 4 and Implementation
+// notes; the expert is the SwiGLU MLP of "DL S077 - Mixture of Experts (MoE) Intuition",
+// section 1.1 (w1 = gate, w3 = up, w2 = down).
+//
+// Three epilogues share the main loop:
+//   TC_SWIGLU : B tile = [W1 rows n0..n0+BN/2 ; W3 rows n0..n0+BN/2]; one MMA of width BN
+//               gives gate and up side by side in TMEM; the epilogue writes
+//               H = silu(gate) * up as bf16 (BN/2 output columns per tile).
+//   TC_SCALE  : down projection; the epilogue writes g_r * acc as bf16, with the gate
+//               g_r = topk_gate[perm[r]] of the row's assignment (1 for the shared expert).
+//   TC_F32OUT : router logits; the epilogue writes acc (+ bias) as fp32.
+//
+// Roles (192 threads, one CTA per SM, persistent over tiles):
+//   warp 0 lane 0  TMA producer: A tile 128 x 64 and B tile BN x 64 (bf16, 128-byte swizzle)
+//                  into a STAGES-deep shared-memory ring;
+//   warp 1         allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16) into one of
+//                  two TMEM accumulators, so the epilogue of tile i overlaps the MMAs of i+1;
+//   warps 2..5     epilogue: tcgen05.ld (each warp reads its 32-lane quarter of TMEM),
+//                  element-wise math, predicated 16-byte global stores (rows past the
+//                  group's end are masked: A tiles may straddle two experts' rows).
+// Every mbarrier wait is bounded (common.cuh): on a timeout the kernel records
+// MOE_ERR_TIMEOUT in the workspace error word, drains its own copies and MMAs, frees TMEM
+// and returns.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "launchers.h"
+
+namespace moe {
+
+namespace {
+
+constexpr int kThreads = 192;
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kMaxGroups = 1024;
+
+__host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
+  uint32_t p = 32;
+  while (p < v) p <<= 1;
+  return p;
+}
+
+template <int MODE, int BN>
+struct Cfg {
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = BN * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGES_RAW = (196 * 1024) / STAGE_BYTES;
+  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int BN_OUT = (MODE == TC_SWIGLU) ? BN / 2 : BN;
+  static constexpr uint32_t TMEM_COLS = pow2_at_least(2 * BN);
+  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  // shared memory layout (offsets from a 1024-byte aligned base)
+  static constexpr int OFF_TILES = 0;
+  static constexpr int OFF_BARS = STAGES * STAGE_BYTES;
+  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+  static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;     // tmem slot, abort flag
+  static constexpr int OFF_TABLE = OFF_MISC + 16;              // offsets[G+1], prefix[G+1]
+  static constexpr int smem_bytes(int groups) {
+    return 1024 + OFF_TABLE + 2 * (groups + 1) * 4;
+  }
+  static_assert(STAGES >= 2, "pipeline needs at least two stages");
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N % 16 == 0, 16..256");
+  static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
+  static_assert((STAGE_BYTES % 1024) == 0, "stages must stay 1024-byte aligned");
+};
+
+struct Tile {
+  int shared;   // 1 = the shared-expert problem
+  int group;    // expert (routed) or 0
+  int n_blk;
+  int row0;     // first row of A / output
+  int rows;     // valid rows in this tile (<= BM)
+};
+
+__device__ __forceinline__ Tile decode_tile(int tile, const int* s_off, const int* s_pre, int G,
+                                            int nt_routed, int m_shared, int nt_shared) {
+  Tile t;
+  const int routed_total = s_pre[G];
+  if (tile < routed_total) {
+    int lo = 0, hi = G - 1;  // largest g with s_pre[g] <= tile
+    while (lo < hi) {
+      const int mid = (lo + hi + 1) >> 1;
+      if (s_pre[mid] <= tile) lo = mid; else hi = mid - 1;
+    }
+    const int g = lo;
+    const int local = tile - s_pre[g];
+    const int mt = (s_pre[g + 1] - s_pre[g]) / nt_routed;
+    const int n = local / mt, m = local - n * mt;
+    t.shared = 0;
+    t.group = g;
+    t.n_blk = n;
+    t.row0 = s_off[g] + m * BM;
+    t.rows = min(BM, s_off[g + 1] - t.row0);
+  } else {
+    const int local = tile - routed_total;
+    const int mt = (m_shared + BM - 1) / BM;
+    const int n = local / mt, m = local - n * mt;
+    t.shared = 1;
+    t.group = 0;
+    t.n_blk = n;
+    t.row0 = m * BM;
+    t.rows = min(BM, m_shared - t.row0);
+  }
+  (void)nt_shared;
+  return t;
+}
+
+template <int MODE, int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
+                       const __grid_constant__ CUtensorMap tmB0,
+                       const __grid_constant__ CUtensorMap tmB1,
+                       const __grid_constant__ CUtensorMap tmAs,
+                       const __grid_constant__ CUtensorMap tmB0s,
+                       const __grid_constant__ CUtensorMap tmB1s, const TcArgs args) {
+  using C = Cfg<MODE, BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  uint8_t* tiles = smem + C::OFF_TILES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::OFF_BARS);
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + C::STAGES;
+  uint64_t* tfull_bar = bars + 2 * C::STAGES;
+  uint64_t* tempty_bar = tfull_bar + 2;
+  uint64_t* drain_bar = tfull_bar + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
+  int* s_off = reinterpret_cast<int*>(smem + C::OFF_TABLE);
+  const int G = args.groups;
+  int* s_pre = s_off + (G + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  DeviceError* err = args.err;
+
+  // ---- set-up: barriers (thread 0), TMEM (warp 1), group/tile tables (warp 2)
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < C::STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull_bar[a], 1);
+      mbar_init(&tempty_bar[a], 4);
+    }
+    mbar_init(drain_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == 2) {
+    // s_off[g] = first row of group g; s_pre[g] = first tile of group g (exclusive scan).
+    const int nt = (args.n_routed + C::BN_OUT - 1) / C::BN_OUT;
+    int carry = 0;
+    for (int base = 0; base < G; base += 32) {
+      const int g = base + lane;
+      int lo = 0, hi = 0;
+      if (g < G) {
+        if (args.offsets != nullptr) {
+          lo = args.offsets[g];
+          hi = args.offsets[g + 1];
+        } else {
+          lo = 0;
+          hi = args.m_single;
+        }
+        s_off[g] = lo;
+      }
+      int tiles_g = (g < G) ? ((hi - lo + BM - 1) / BM) * nt : 0;
+      int incl = tiles_g;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int v = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o) incl += v;
+      }
+      if (g < G) s_pre[g] = carry + incl - tiles_g;
+      carry += __shfl_sync(0xffffffffu, incl, 31);
+      if (g == G - 1) s_off[G] = hi;
+    }
+    if (lane == 0) s_pre[G] = carry;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  const int nt_routed = (args.n_routed + C::BN_OUT - 1) / C::BN_OUT;
+  const int nt_shared = args.has_shared ? (args.n_shared + C::BN_OUT - 1) / C::BN_OUT : 0;
+  const int mt_shared = args.has_shared ? (args.m_shared + BM - 1) / BM : 0;
+  const int total = s_pre[G] + mt_shared * nt_shared;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      tma_prefetch_desc(&tmA);
+      tma_prefetch_desc(&tmB0);
+      if (MODE == TC_SWIGLU) tma_prefetch_desc(&tmB1);
+      if (args.has_shared) {
+        tma_prefetch_desc(&tmAs);
+        tma_prefetch_desc(&tmB0s);
+        if (MODE == TC_SWIGLU) tma_prefetch_desc(&tmB1s);
+      }
+      uint32_t issued_mask = 0, parity_mask = 0;
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+        const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, args.m_shared, nt_shared);
+        const CUtensorMap* mA = t.shared ? &tmAs : &tmA;
+        const CUtensorMap* mB0 = t.shared ? &tmB0s : &tmB0;
+        const CUtensorMap* mB1 = t.shared ? &tmB1s : &tmB1;
+        const int K = t.shared ? args.k_shared : args.k_routed;
+        const int nk = (K + BK - 1) / BK;
+        bool ok = true;
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, err,
+                                 SITE_GEMM_WAIT_EMPTY)) {
+            ok = false;
+            break;
+          }
+          uint8_t* sa = tiles + stage * C::STAGE_BYTES;
+          uint8_t* sb = sa + C::A_BYTES;
+          mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+          tma_load_2d(sa, mA, &full_bar[stage], kb * BK, t.row0);
+          if (MODE == TC_SWIGLU) {
+            tma_load_3d(sb, mB0, &full_bar[stage], kb * BK, t.n_blk * (BN / 2), t.group);
+            tma_load_3d(sb + C::B_BYTES / 2, mB1, &full_bar[stage], kb * BK, t.n_blk * (BN / 2),
+                        t.group);
+          } else {
+            tma_load_3d(sb, mB0, &full_bar[stage], kb * BK, t.n_blk * BN, t.group);
+          }
+          issued_mask |= 1u << stage;
+          parity_mask = (parity_mask & ~(1u << stage)) | (phase << stage);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (!ok) break;
+      }
+      // Drain: every copy this thread issued has landed before the CTA may exit.
+      for (int s = 0; s < C::STAGES; ++s)
+        if (issued_mask & (1u << s))
+          mbar_wait_bounded(&full_bar[s], (parity_mask >> s) & 1u, nullptr, err,
+                            SITE_GEMM_WAIT_DRAIN);
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      int stage = 0;
+      uint32_t phase = 0;
+      int it = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+        const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, args.m_shared, nt_shared);
+        const int K = t.shared ? args.k_shared : args.k_routed;
+        const int nk = (K + BK - 1) / BK;
+        const int acc = it & 1;
+        const uint32_t acc_phase = (it >> 1) & 1;
+        if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1, abort_flag, err,
+                               SITE_GEMM_WAIT_TMEM_EMPTY))
+          break;
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        for (int kb = 0; kb < nk; ++kb) {
+          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, err, SITE_GEMM_WAIT_FULL)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t a_addr = smem_u32(tiles + stage * C::STAGE_BYTES);
+          const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+          for (int kk = 0; kk < BK / 16; ++kk) {
+            tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32),
+                        C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+          }
+          tc_commit(&empty_bar[stage]);
+          if (++stage == C::STAGES) {
+            stage = 0;
+            phase ^= 1;
+          }
+        }
+        if (ok) tc_commit(&tfull_bar[acc]);
+      }
+      // Drain: all MMAs issued by this thread have completed before TMEM is freed.
+      tc_commit(drain_bar);
+      mbar_wait_bounded(drain_bar, 0, nullptr, err, SITE_GEMM_WAIT_DRAIN);
+    }
+  } else {
+    // ================= epilogue (warps 2..5) =================
+    const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
+    const int r_local = quarter * 32 + lane;
+    int it = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+      const int acc = it & 1;
+      const uint32_t acc_phase = (it >> 1) & 1;
+      if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, err,
+                             SITE_GEMM_WAIT_TMEM_FULL))
+        break;
+      tc_fence_after();
+      const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, args.m_shared, nt_shared);
+      const bool rvalid = r_local < t.rows;
+      const long long row = static_cast<long long>(t.row0) + r_local;
+      const int N = t.shared ? args.n_shared : args.n_routed;
+      const long long ldo = t.shared ? args.ldo_shared : args.ldo_routed;
+      const uint32_t tbase =
+          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
+      const int col_base = t.n_blk * C::BN_OUT;
+
+      if (MODE == TC_SWIGLU) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.shared ? args.out_shared
+                                                                        : args.out_routed);
+#pragma unroll 1
+        for (int c = 0; c < C::BN_OUT / 32; ++c) {
+          uint32_t g[32], u[32];
+          tmem_ld_32cols(tbase + c * 32, g);
+          tmem_ld_32cols(tbase + BN / 2 + c * 32, u);
+          tmem_ld_wait();
+          if (rvalid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const float h0 = silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+              const float h1 =
+                  silu_f(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+              packed[i] = pack_bf16x2(h0, h1);
+            }
+            const int col0 = col_base + c * 32;
+            __nv_bfloat16* dst = out + row * ldo + col0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (col0 + q * 8 < N)
+                *reinterpret_cast<uint4*>(dst + q * 8) =
+                    make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+          }
+        }
+      } else if (MODE == TC_SCALE) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.shared ? args.out_shared
+                                                                        : args.out_routed);
+        float gscale = 1.0f;
+        if (rvalid && !t.shared && args.gate != nullptr) gscale = args.gate[args.perm[row]];
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld_32cols(tbase + c * 32, v);
+          tmem_ld_wait();
+          if (rvalid) {
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+              packed[i] = pack_bf16x2(gscale * __uint_as_float(v[2 * i]),
+                                      gscale * __uint_as_float(v[2 * i + 1]));
+            const int col0 = col_base + c * 32;
+            __nv_bfloat16* dst = out + row * ldo + col0;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              if (col0 + q * 8 < N)
+                *reinterpret_cast<uint4*>(dst + q * 8) =
+                    make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+          }
+        }
+      } else {  // TC_F32OUT
+        float* out = reinterpret_cast<float*>(args.out_routed);
+#pragma unroll 1
+        for (int c = 0; c < BN / 16; ++c) {
+          uint32_t v[16];
+          tmem_ld_16cols(tbase + c * 16, v);
+          tmem_ld_wait();
+          if (rvalid) {
+            const int col0 = col_base + c * 16;
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+              const int col = col0 + i;
+              if (col < N) {
+                float val = __uint_as_float(v[i]);
+                if (args.bias != nullptr) val += args.bias[col];
+                out[row * ldo + col] = val;
+              }
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&tempty_bar[acc]);
+    }
+  }
+
+  // ---- teardown: all roles are done with TMEM before it is freed
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// Host side: tensor maps and launch
+// ------------------------------------------------------------------------------------
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encoder() {
+  std::call_once(g_encode_once, []() {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &fn, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 2-D bf16 map over a row-major [rows, inner] matrix; box = [box_rows, 64], 128-byte swizzle.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+// 3-D bf16 map over [groups, rows, inner]; box = [1, box_rows, 64], 128-byte swizzle.
+bool encode_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t groups,
+               uint32_t box_rows) {
+  cuuint64_t dims[3] = {inner, rows, groups};
+  cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int MODE, int BN>
+int launch_impl(const TcProblem& p, cudaStream_t stream) {
+  using C = Cfg<MODE, BN>;
+  if (!get_encoder()) return MOE_ERR_CUDA;
+  const int groups = p.args.groups;
+  if (groups < 1 || groups > kMaxGroups) return MOE_ERR_INVALID;
+  const uint32_t brows = (MODE == TC_SWIGLU) ? BN / 2 : BN;
+
+  CUtensorMap mA{}, mB0{}, mB1{}, mAs{}, mB0s{}, mB1s{};
+  if (!encode_2d(&mA, p.a, p.args.k_routed, p.a_rows, BM)) return MOE_ERR_CUDA;
+  if (!encode_3d(&mB0, p.b0, p.args.k_routed, p.b_rows, p.b_groups, brows)) return MOE_ERR_CUDA;
+  if (MODE == TC_SWIGLU && !encode_3d(&mB1, p.b1, p.args.k_routed, p.b_rows, p.b_groups, brows))
+    return MOE_ERR_CUDA;
+  if (p.args.has_shared) {
+    if (!encode_2d(&mAs, p.a_s, p.args.k_shared, p.args.m_shared, BM)) return MOE_ERR_CUDA;
+    if (!encode_3d(&mB0s, p.b0_s, p.args.k_shared, p.b_rows_s, 1, brows)) return MOE_ERR_CUDA;
+    if (MODE == TC_SWIGLU && !encode_3d(&mB1s, p.b1_s, p.args.k_shared, p.b_rows_s, 1, brows))
+      return MOE_ERR_CUDA;
+  }
+
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
+  const int smem = C::smem_bytes(groups);
+  static std::once_flag attr_once[64];
+  static bool attr_ok[64];
+  if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  std::call_once(attr_once[dev], [&]() {
+    attr_ok[dev] = cudaFuncSetAttribute(tc_grouped_gemm_kernel<MODE, BN>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::smem_bytes(kMaxGroups)) == cudaSuccess;
+  });
+  if (!attr_ok[dev]) return MOE_ERR_CUDA;
+
+  long long grid = std::min<long long>(p.max_tiles, p.num_sms);
+  if (grid < 1) return MOE_OK;
+  tc_grouped_gemm_kernel<MODE, BN><<<static_cast<int>(grid), kThreads, smem, stream>>>(
+      mA, mB0, mB1, mAs, mB0s, mB1s, p.args);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+int tc_smem_bytes(int mode, int bn, int groups) {
+  switch (mode * 1000 + bn) {
+    case TC_SWIGLU * 1000 + 256: return Cfg<TC_SWIGLU, 256>::smem_bytes(groups);
+    case TC_SCALE * 1000 + 256: return Cfg<TC_SCALE, 256>::smem_bytes(groups);
+    case TC_SCALE * 1000 + 128: return Cfg<TC_SCALE, 128>::smem_bytes(groups);
+    default: return Cfg<TC_F32OUT, 256>::smem_bytes(groups);
+  }
+}
+
+int launch_tc_gemm(int mode, int bn, const TcProblem& p, cudaStream_t stream) {
+  switch (mode * 1000 + bn) {
+    case TC_SWIGLU * 1000 + 256: return launch_impl<TC_SWIGLU, 256>(p, stream);
+    case TC_SCALE * 1000 + 256: return launch_impl<TC_SCALE, 256>(p, stream);
+    case TC_SCALE * 1000 + 128: return launch_impl<TC_SCALE, 128>(p, stream);
+    case TC_F32OUT * 1000 + 16: return launch_impl<TC_F32OUT, 16>(p, stream);
+    case TC_F32OUT * 1000 + 32: return launch_impl<TC_F32OUT, 32>(p, stream);
+    case TC_F32OUT * 1000 + 64: return launch_impl<TC_F32OUT, 64>(p, stream);
+    case TC_F32OUT * 1000 + 128: return launch_impl<TC_F32OUT, 128>(p, stream);
+    case TC_F32OUT * 1000 + 256: return launch_impl<TC_F32OUT, 256>(p, stream);
+    default: return MOE_ERR_UNSUPPORTED;
+  }
+}
+
+}  // namespace moe

@@ -1,0 +1,123 @@
+"""Host-side tests of the C ABI (no GPU): the library loads, exports every declared
+symbol, and rejects bad arguments before touching a device."""
+import ctypes
+import re
+import os
+
+import pytest
+import torch
+
+import mixture_experts_layer_92_b300 as moe
+from mixture_experts_layer_92_b300 import _lib
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def declared_symbols():
+    src = open(os.path.join(ROOT, "include", "moe.h")).read()
+    return sorted(set(re.findall(r"^\s*(?:int|size_t|const char\*)\s+(moe_\w+)\s*\(", src, re.M)))
+
+
+def test_every_declared_symbol_is_exported():
+    names = declared_symbols()
+    assert len(names) >= 14
+    lib = ctypes.CDLL(_lib.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert sorted(_lib.EXPORTED) == names
+
+
+def test_capacity():
+    assert moe.moe_capacity(1.25, 256, 2, 8) == 80
+    assert moe.moe_capacity(1.0, 16384, 1, 128) == 128
+    assert moe.moe_capacity(1.25, 64, 2, 8) == 20
+    assert moe.moe_capacity(100.0, 50, 2, 4) == 50          # clamped: C = T means no drop
+    assert moe.moe_capacity(0.0, 50, 2, 4) == 0
+    assert moe.moe_capacity(1.0, 10, 1, 0) == -1
+    assert moe.moe_capacity(-1.0, 10, 1, 2) == -1
+
+
+def shape(**kw):
+    base = dict(T=64, d=128, E=8, k=2, d_ff=256, gate="softmax_topk", dtype=torch.bfloat16)
+    base.update(kw)
+    return moe.make_shape(**base)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(k=0), -1), (dict(k=9), -1), (dict(E=0), -1), (dict(E=1025, k=2), -1),
+    (dict(T=-1), -1), (dict(d=0), -1), (dict(d_ff=0), -1), (dict(capacity=-1), -1),
+    (dict(gate=7), -1), (dict(dtype=5), -1), (dict(d_ff_shared=-8), -1),
+    (dict(d=100), -2), (dict(d_ff=260), -2), (dict(d_ff_shared=12), -2),
+    (dict(T=1 << 30, k=2), -1),
+    (dict(dtype=torch.float32, d=6), -2),
+])
+def test_invalid_shapes(kw, status):
+    s = shape(**kw)
+    assert moe.moe_check_shape(s) == status
+    assert moe.moe_workspace_size(s) == 0
+    assert _lib.LIB.moe_last_error_detail().decode() != ""
+
+
+def test_valid_shapes_and_workspace_monotone():
+    s1 = shape(T=64)
+    s2 = shape(T=128)
+    assert moe.moe_check_shape(s1) == 0
+    n1, n2 = moe.moe_workspace_size(s1), moe.moe_workspace_size(s2)
+    assert 0 < n1 < n2 and n1 % 256 == 0
+    # the largest workload fits comfortably in HBM
+    ds = shape(T=8192, d=7168, E=256, k=8, d_ff=2048, d_ff_shared=2048, gate="sigmoid_topk")
+    assert moe.moe_workspace_size(ds) < 4 << 30
+
+
+def _ws_bytes(n):
+    return ctypes.c_size_t(n)
+
+
+def test_entry_points_reject_before_any_launch():
+    """Invalid arguments return an error on the host: no CUDA call is made, so these run
+    on a machine without a GPU."""
+    L = _lib.LIB
+    s = shape()
+    need = moe.moe_workspace_size(s)
+    fake = ctypes.c_void_p(0x7f0000000000)          # never dereferenced
+    null = ctypes.c_void_p(None)
+    # no workspace
+    assert L.moe_forward(ctypes.byref(s), fake, fake, null, fake, fake, fake, null, null, null,
+                         fake, null, null, null, null, need, null) == -4
+    # workspace too small
+    assert L.moe_forward(ctypes.byref(s), fake, fake, null, fake, fake, fake, null, null, null,
+                         fake, null, null, null, fake, need - 1, null) == -4
+    # misaligned workspace
+    assert L.moe_forward(ctypes.byref(s), fake, fake, null, fake, fake, fake, null, null, null,
+                         fake, null, null, null, ctypes.c_void_p(0x7f0000000010), need, null) == -4
+    # missing x
+    assert L.moe_forward(ctypes.byref(s), null, fake, null, fake, fake, fake, null, null, null,
+                         fake, null, null, null, fake, need, null) == -1
+    # misaligned weight
+    assert L.moe_forward(ctypes.byref(s), fake, fake, null, ctypes.c_void_p(0x7f0000000002), fake,
+                         fake, null, null, null, fake, null, null, null, fake, need, null) == -1
+    # shared expert declared but its weights missing
+    s2 = shape(d_ff_shared=128)
+    n2 = moe.moe_workspace_size(s2)
+    assert L.moe_forward(ctypes.byref(s2), fake, fake, null, fake, fake, fake, null, null, null,
+                         fake, null, null, null, fake, n2, null) == -1
+    # wrong event count
+    ev = (ctypes.c_void_p * 3)()
+    assert L.moe_forward_events(ctypes.byref(s), fake, fake, null, fake, fake, fake, null, null,
+                                null, fake, null, null, null, fake, need, null, ev, 3) == -1
+    # dispatch without indices or logits
+    assert L.moe_dispatch(ctypes.byref(s), null, null, fake, fake, fake, fake, fake, fake, need,
+                          null) == -1
+    # route without logits and without x
+    assert L.moe_route_topk(ctypes.byref(s), null, fake, null, null, null, fake, fake, null, fake,
+                            need, null) == -1
+    # combine with a misaligned output
+    assert L.moe_combine(ctypes.byref(s), fake, fake, null, ctypes.c_void_p(0x7f0000000004),
+                         null) == -1
+    assert L.moe_aux_loss(ctypes.byref(s), null, fake, fake, null) == -1
+
+
+def test_status_strings():
+    for code in (0, -1, -2, -3, -4, -5, -6):
+        assert moe.moe_status_string(code) != "unknown status"
+    assert moe.moe_status_string(42) == "unknown status"
