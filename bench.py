@@ -1,0 +1,400 @@
+"""Benchmark of the MoE layer forward on B300: tokens/s and roofline fractions.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+A step is one moe_forward (router GEMM, gates/top-k, dispatch, gather, gate/up GEMM +
+SwiGLU, down GEMM + gate scale, combine, balance losses) over one batch of the workload
+(default: the Mixtral-shaped prefill layer, T=4096, d=4096, E=8, d_ff=14336, top-2, bf16).
+Inputs are synthetic and seeded (moe_inputs.py), resident in HBM before the timed region.
+L2 is flushed (a 256 MiB write) between timed steps, outside the timed events.
+
+Under torchrun (N > 1) every rank runs an independent replica of the layer on its own GPU:
+the layer has no cross-GPU exchange on one node's data-parallel path, so `value` is the sum
+of all ranks' tokens divided by the slowest rank's time (weak scaling).
+
+--impl reference times the CPU oracle (fp64 numpy, oracle/) on bounded samples of the same
+workload on this host's cores; under torchrun only rank 0 runs it.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from moe_inputs import WORKLOADS, make_inputs  # noqa: E402
+
+METRIC = "MoE layer fwd tokens/sec (1 B300) + % of BF16 tensor / HBM roofline"
+UNIT = "tokens/s"
+STAGES = ("router_gemm", "gates_topk", "dispatch", "gather", "gemm_gateup_swiglu",
+          "gemm_down_scale", "combine", "aux_loss")
+DOMINANT = "gemm_gateup_swiglu"
+FLUSH_BYTES = 256 << 20
+
+
+# ------------------------------------------------------------------------------ helpers
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return dict(hbm_gbs=d["hbm_gbs"], bf16_tflops=d["bf16_tflops"],
+                    bf16_tflops_sustained=d.get("bf16_tflops_sustained"), source="measured")
+    return dict(hbm_gbs=6400.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="fallback")
+
+
+def capacity(w):
+    # the C ABI's own capacity helper (ceil(cf*T*k/E), clamped to T)
+    from mixture_experts_layer_92_b300 import moe_capacity
+    return w.T if w.cf is None else moe_capacity(w.cf, w.T, w.k, w.E)
+
+
+def algorithmic_work(w, R: int, touched: int):
+    """FLOPs and bytes the method itself must compute and move for one forward.
+
+    FLOPs: router 2*T*d*E, experts 6*d*d_ff per kept assignment (three GEMMs), shared expert
+    6*d*d_ff_s per token. Bytes: x + W_r + weights of the experts that received at least one
+    token (3*d*d_ff each) + shared expert weights + y. Per kernel (for the roofline of one
+    launch): gate/up GEMM 4*R*d*d_ff flops, down GEMM 2*R*d*d_ff flops (+ shared)."""
+    es = 4 if w.dtype == "f32" else 2
+    T, d, E, F, Fs = w.T, w.d, w.E, w.d_ff, w.d_ff_shared
+    flops_router = 2.0 * T * d * E
+    flops_gateup = 4.0 * R * d * F + 4.0 * T * d * Fs
+    flops_down = 2.0 * R * d * F + 2.0 * T * d * Fs
+    bytes_total = (T * d * es + E * d * es + touched * 3.0 * d * F * es + 3.0 * d * Fs * es
+                   + T * d * es)
+    return dict(flops=flops_router + flops_gateup + flops_down, bytes=bytes_total,
+                per_stage=dict(
+                    router_gemm=("hbm", T * d * es + E * d * es + T * E * 4.0),
+                    gates_topk=("hbm", T * E * 4.0 + T * w.k * 8.0),
+                    dispatch=("hbm", T * w.k * 4.0 * 3 + R * 4.0),
+                    gather=("hbm", 2.0 * R * d * es),
+                    gemm_gateup_swiglu=("tensor", flops_gateup),
+                    gemm_down_scale=("tensor", flops_down),
+                    combine=("hbm", R * d * es + T * d * es * (2 if Fs else 1)),
+                    aux_loss=("hbm", 0.0)))
+
+
+def source_sha(path):
+    return hashlib.sha256(open(path, "rb").read()).hexdigest()[:16]
+
+
+def traffic_from_profile(workload: str, kernel: str):
+    """dram bytes per launch from a committed ncu summary, or None if there is none or the
+    kernel's source changed since it was captured."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}__{workload}.txt")
+    if not os.path.exists(p):
+        return None
+    vals = {}
+    for line in open(p):
+        if ":" in line:
+            k, v = line.split(":", 1)
+            vals[k.strip()] = v.strip()
+    src = os.path.join(ROOT, "mixture_experts_layer_92_b300", "csrc", vals.get("source_file", ""))
+    if "dram_bytes_per_launch" not in vals or not os.path.exists(src):
+        return None
+    if source_sha(src) != vals.get("source_sha256_16"):
+        return None
+    return float(vals["dram_bytes_per_launch"])
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples every 200 ms while running."""
+    Q = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.rows = []
+        self.proc = None
+        self.thread = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.Q}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) == 8:
+                self.rows.append(parts)
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread is not None:
+            self.thread.join(timeout=5)
+
+    def summary(self):
+        if not self.rows:
+            return dict(sm_mhz=None, sm_max_mhz=None, reasons=[], samples=0)
+        def num(v):
+            try:
+                return float(v)
+            except ValueError:
+                return None
+        sm = [num(r[0]) for r in self.rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in self.rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v == "Active"})
+        busy = [s for s, p in zip(sm, pw) if p is not None and p > 300] or sm
+        return dict(sm_mhz=statistics.median(busy) if busy else None,
+                    sm_max_mhz=max(mx) if mx else None, reasons=reasons, samples=len(self.rows),
+                    power_w_max=max(pw) if pw else None)
+
+
+# ------------------------------------------------------------------------------ CPU oracle arm
+def oracle_sample(w, inp_host: dict, n_tokens: int, seed: int = 0):
+    """Run the CPU oracle (as it stands) on a batch of n_tokens tokens of the workload;
+    returns seconds."""
+    import oracle as O
+    C = w.T if w.cf is None else O.capacity(w.cf, n_tokens, w.k, w.E)
+    x = inp_host["x"][:n_tokens]
+    t0 = time.perf_counter()
+    O.forward(x, inp_host["w_router"], inp_host["w1"], inp_host["w3"], inp_host["w2"], k=w.k,
+              mode=w.gate, C=min(C, n_tokens), router_bias=inp_host["router_bias"],
+              w1s=inp_host["w1s"], w3s=inp_host["w3s"], w2s=inp_host["w2s"], alpha=w.alpha,
+              beta=w.beta)
+    return time.perf_counter() - t0
+
+
+def host_inputs(inp: dict) -> dict:
+    return {k: (None if v is None else v.float().cpu().numpy()) for k, v in inp.items()}
+
+
+def oracle_threads() -> int:
+    try:
+        from threadpoolctl import threadpool_info
+        return max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def cpu_baseline(w, inp_host: dict, target_s: float = 15.0):
+    n = min(w.T, 16)
+    t = oracle_sample(w, inp_host, n)
+    n2 = int(min(w.T, max(n, n * target_s / max(t, 1e-3) * 0.8)))
+    if n2 > n:
+        t = oracle_sample(w, inp_host, n2)
+        n = n2
+    return dict(value=n / t, unit=UNIT, cores=oracle_threads(), kind="oracle",
+                sample=f"first {n} tokens of {w.name} (full routing/dispatch/FFN/combine/losses of "
+                       f"that batch, fp64 numpy), {t:.2f} s")
+
+
+def run_reference(args, w, rank):
+    if rank != 0:
+        return
+    inp = make_inputs(w, device="cuda" if torch.cuda.is_available() else "cpu")
+    ih = host_inputs(inp)
+    del inp
+    # size one step to a few seconds
+    n = min(w.T, 8)
+    t = oracle_sample(w, ih, n)
+    n = int(min(w.T, max(n, n * 3.0 / max(t, 1e-3))))
+    for _ in range(args.warmup):
+        oracle_sample(w, ih, n)
+    total = 0.0
+    for _ in range(args.steps):
+        total += oracle_sample(w, ih, n)
+    val = n * args.steps / total
+    cores = oracle_threads()
+    sample = f"first {n} tokens of {w.name} per step (fp64 numpy oracle)"
+    print(json.dumps(dict(
+        impl="reference", metric=METRIC, value=val, unit=UNIT, n_gpus=args.gpus,
+        steps=args.steps, warmup=args.warmup, ms_per_step=1e3 * total / args.steps,
+        higher_is_better=True, scaling="weak", vs_baseline=None, dtype="f64", data="synthetic",
+        config=dict(workload=w.name, tokens_per_step=n),
+        cpu_baseline=dict(value=val, unit=UNIT, cores=cores, kind="oracle", sample=sample),
+        e2e=dict(value=val, unit=UNIT, h2d_bytes_per_step=0, d2h_bytes_per_step=0))), flush=True)
+
+
+# ------------------------------------------------------------------------------ GPU arm
+def launches_per_forward(w) -> int:
+    # router, top-k, dispatch, gather, gate/up GEMM, down GEMM, combine, stats, losses;
+    # the fp32 path launches the shared expert's two GEMMs separately
+    return 9 + (2 if (w.dtype == "f32" and w.d_ff_shared) else 0)
+
+
+def run_ours(args, w, rank, world, local_rank):
+    import mixture_experts_layer_92_b300 as moe
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    inp = make_inputs(w, device=dev)
+    C = capacity(w)
+    layer = moe.MoELayer(inp["w_router"], inp["w1"], inp["w3"], inp["w2"], k=w.k, gate=w.gate,
+                         capacity=C, router_bias=inp["router_bias"], w1s=inp["w1s"],
+                         w3s=inp["w3s"], w2s=inp["w2s"], alpha=w.alpha, beta=w.beta, max_tokens=w.T)
+    x = inp["x"]
+    y = torch.empty_like(x)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+           for _ in range(args.steps)]
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    sampler = ClockSampler(visible[local_rank] if local_rank < len(visible) else local_rank)
+    sampler.start()
+    for _ in range(args.warmup):
+        flush.zero_()
+        layer.forward(x, y)
+    barrier()
+    t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        layer.forward(x, y, events=evs[i])
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    err = moe.moe_get_error(layer.ws)
+    if err != 0:
+        raise RuntimeError(f"device error {moe.moe_status_string(err)}")
+    step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(args.steps)]
+    stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
+                for j, name in enumerate(STAGES)}
+    total_ms = sum(step_ms)
+
+    # end to end through the public API from pinned host memory
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    loss_host = torch.empty(2, dtype=torch.float32, pin_memory=True)
+    e0 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    e1 = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    for _ in range(max(1, args.warmup // 2)):
+        layer.forward_host(x_host, x, y, y_host, loss_host)
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        e0[i].record(stream)
+        layer.forward_host(x_host, x, y, y_host, loss_host)
+        e1[i].record(stream)
+    barrier()
+    sampler.stop()
+    e2e_ms = sum(a.elapsed_time(b) for a, b in zip(e0, e1))
+
+    # the slowest rank sets the time
+    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = t.tolist()
+    counts = layer.counts.cpu().numpy()
+    R = int(np.minimum(counts, C).sum())
+    touched = int((counts > 0).sum())
+    if rank != 0:
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    pk = peaks()
+    work = algorithmic_work(w, R, touched)
+    tokens = w.T * args.steps * world
+    value = tokens / (total_ms / 1e3)
+    ms_per_step = total_ms / args.steps
+    stages = {}
+    for name in STAGES:
+        ms = statistics.mean(stage_ms[name])
+        bound, amount = work["per_stage"][name]
+        if bound == "tensor":
+            ach = amount / (ms / 1e3) / 1e12
+            stages[name] = dict(ms=ms, bound="tensor", achieved=ach, unit="TFLOP/s",
+                                frac=ach / pk["bf16_tflops"])
+        else:
+            ach = amount / (ms / 1e3) / 1e9 if ms > 0 else 0.0
+            stages[name] = dict(ms=ms, bound="hbm", achieved=ach, unit="GB/s",
+                                frac=ach / pk["hbm_gbs"])
+    dom = stages[DOMINANT] if w.dtype == "bf16" else None
+    roofline = None
+    if dom is not None:
+        tr = traffic_from_profile(w.name, DOMINANT)
+        roofline = dict(bound="tensor", kernel=DOMINANT, achieved=dom["achieved"],
+                        peak=pk["bf16_tflops"], unit="TFLOP/s", frac=dom["frac"], traffic=tr,
+                        peak_source=f"{pk['source']} bf16 burst",
+                        algorithmic=f"{work['per_stage'][DOMINANT][1]:.4e} FLOP per launch")
+    t_roof = max(work["flops"] / (pk["bf16_tflops"] * 1e12), work["bytes"] / (pk["hbm_gbs"] * 1e9))
+    layer_roof = dict(flops=work["flops"], bytes=work["bytes"], roofline_ms=t_roof * 1e3,
+                      measured_ms=ms_per_step, frac=t_roof * 1e3 / ms_per_step,
+                      note="max(FLOPs / bf16 peak, bytes / HBM peak), measured peaks")
+    clk = sampler.summary()
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(w, host_inputs(inp), target_s=args.cpu_seconds)
+    es = x.element_size()
+    line = dict(
+        metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
+        warmup=args.warmup, ms_per_step=ms_per_step, higher_is_better=True, scaling="weak",
+        vs_baseline=None, dtype=w.dtype, data="synthetic (seeded; random-init weights)",
+        config=dict(workload=w.name, T=w.T, d=w.d, E=w.E, k=w.k, d_ff=w.d_ff,
+                    d_ff_shared=w.d_ff_shared, gate=w.gate, capacity=C,
+                    l2="flushed between timed steps (256 MiB write, outside the events); "
+                       "expert weights also exceed L2",
+                    kept_assignments=R, experts_touched=touched,
+                    wall_s=t_wall),
+        roofline=roofline, layer_roofline=layer_roof, stages=stages,
+        cpu_baseline=cpu,
+        e2e=dict(value=tokens / (e2e_ms / 1e3), unit=UNIT, h2d_bytes_per_step=w.T * w.d * es,
+                 d2h_bytes_per_step=w.T * w.d * es + 8),
+        gpu_launches=launches_per_forward(w) * args.steps,
+        clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"], reasons=clk["reasons"],
+                    samples=clk["samples"]))
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default="mixtral_prefill", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)          # timing rule: at least 3 warm-up steps
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    w = WORKLOADS[args.workload]
+    if args.impl == "reference":
+        run_reference(args, w, rank)
+        return
+    run_ours(args, w, rank, world, local_rank)
+
+
+if __name__ == "__main__":
+    main()

@@ -166,6 +166,9 @@ def moe_forward(s, ws, x, w_router, w1, w3, w2, y, router_bias=None, w1s=None, w
                                _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(y), _p(counts), _p(dropped),
                                _p(losses), _p(ws), ws.numel(), _stream(stream)), "moe_forward")
         return
+    for e in events:
+        if e.cuda_event == 0:          # torch creates the CUDA event on first record
+            e.record()
     arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
     _check(LIB.moe_forward_events(ctypes.byref(s), _p(x), _p(w_router), _p(router_bias), _p(w1),
                                   _p(w3), _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(y), _p(counts),

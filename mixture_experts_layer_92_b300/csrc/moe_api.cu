@@ -364,6 +364,9 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   TRY(check_ws(s, ws, ws_bytes));
   if (ev != nullptr && n_ev != MOE_NUM_STAGES + 1)
     return fail(MOE_ERR_INVALID, "n_events = %d, expected %d", n_ev, MOE_NUM_STAGES + 1);
+  if (ev != nullptr)
+    for (int i = 0; i < n_ev; ++i)
+      if (ev[i] == nullptr) return fail(MOE_ERR_INVALID, "events[%d] is NULL", i);
   if (s->T > 0) {
     REQUIRE_PTR(x, "x");
     REQUIRE_PTR(w_router, "w_router");

@@ -105,3 +105,25 @@ def test_fp32_deterministic():
     a = gpu_forward(w, inp)
     b = gpu_forward(w, inp)
     assert torch.equal(a["y"], b["y"]) and torch.equal(a["losses"], b["losses"])
+
+
+def test_forward_events_time_every_stage():
+    """moe_forward_events records one event per stage boundary on the caller's stream and
+    gives the same output as moe_forward."""
+    w = WORKLOADS["tiny_fp32"]
+    inp = {k: (v.to(DEV) if v is not None else None) for k, v in make_inputs(w).items()}
+    s = L.make_shape(w.T, w.d, w.E, w.k, w.d_ff, gate=w.gate, dtype=torch.float32,
+                     capacity=capacity_of(w))
+    ws = L.alloc_workspace(s, DEV)
+    y1 = torch.empty_like(inp["x"])
+    y2 = torch.empty_like(inp["x"])
+    L.moe_forward(s, ws, inp["x"], inp["w_router"], inp["w1"], inp["w3"], inp["w2"], y1)
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(L.NUM_STAGES + 1)]
+    L.moe_forward(s, ws, inp["x"], inp["w_router"], inp["w1"], inp["w3"], inp["w2"], y2, events=evs)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+    ms = [evs[i].elapsed_time(evs[i + 1]) for i in range(L.NUM_STAGES)]
+    assert all(m >= 0 for m in ms) and sum(ms) > 0
+    with pytest.raises(L.MoeError):
+        L.moe_forward(s, ws, inp["x"], inp["w_router"], inp["w1"], inp["w3"], inp["w2"], y2,
+                      events=evs[:3])
