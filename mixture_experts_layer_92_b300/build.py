@@ -1,6 +1,6 @@
 """Build libmoe.so (the C-ABI CUDA library) in-tree for sm_103a.
 
-    python -m mixture_experts_layer_92_b300.build [--force] [--verbose]
+    python mixture_experts_layer_92_b300/build.py [--force] [--verbose] [--ptxas-info]
 
 Each csrc/*.cu is compiled with nvcc for sm_103a into _build/, then linked into
 mixture_experts_layer_92_b300/libmoe.so with the CUDA runtime linked statically, so the
