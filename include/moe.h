@@ -183,6 +183,29 @@ int moe_forward_events(const moe_shape* s, const void* x, const void* w_router,
                        void* y, int32_t* counts, int32_t* dropped, float* losses, void* ws,
                        size_t ws_bytes, void* stream, void* const* events, int n_events);
 
+/* moe_route_topk for precomputed logits, for callers that cannot allocate device memory.
+ * (No counterpart in the pages: it is a deployment variant, not a step of the method.)
+ * Some callers cannot hand the library a workspace: code running inside a host framework
+ * that owns all device memory and forbids cudaMalloc (an allocation synchronises the device
+ * and can stall unrelated work), or a call site with no allocator at hand. This entry point
+ * computes exactly what moe_route_topk computes from logits_in -- topk_idx [T, k] int32,
+ * topk_gate [T, k] fp32 and, if stats is not NULL, stats [E + 1] fp32 -- and keeps its only
+ * scratch (the per-block partial sums behind stats) in a fixed 2 MiB array inside the
+ * library's own device memory, so it allocates nothing.
+ *   - Limit: route_blocks(T) * (E + 1) * 4 bytes must fit in 2 MiB, where route_blocks(T) =
+ *     min(ceil(T / 8), 1024): any T for E <= 511. Larger sizes return MOE_ERR_UNSUPPORTED
+ *     with the needed and available bytes in moe_last_error_detail().
+ *   - The array exists once per GPU that loads the library and is held until the process
+ *     exits. Every call on a device shares it, so calls that overlap on the GPU (e.g. on two
+ *     streams) race; serialise them. Each call writes the scratch before reading it.
+ *   - The first call on each device looks up the array's device address (a one-time set-up
+ *     with that device current); make that first call before any stream capture.
+ *   - Device-side error reporting needs a workspace, so this variant does not flag
+ *     non-finite logits (moe_route_topk does).
+ * Pointers are device pointers; asynchronous on `stream`. */
+int moe_route_topk_noalloc(const moe_shape* s, const float* logits_in, int32_t* topk_idx,
+                           float* topk_gate, float* stats, void* stream);
+
 /* Reads (synchronising `stream`) the sticky device error word in the workspace:
  * MOE_OK, or the first moe_status a kernel recorded since the last moe_clear_error. */
 int moe_get_error(const void* ws, void* stream);

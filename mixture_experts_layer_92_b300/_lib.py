@@ -26,7 +26,7 @@ STAGE_NAMES = ("router_gemm", "gates_topk", "dispatch", "gather", "gemm_gateup_s
 EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_topk",
             "moe_dispatch", "moe_grouped_swiglu", "moe_combine", "moe_aux_loss", "moe_forward",
             "moe_forward_events", "moe_get_error", "moe_clear_error", "moe_status_string",
-            "moe_last_error_detail")
+            "moe_last_error_detail", "moe_route_topk_noalloc")
 
 
 class MoeError(RuntimeError):
@@ -67,6 +67,7 @@ def _load() -> ctypes.CDLL:
         "moe_clear_error": (ctypes.c_int, [vp, vp]),
         "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "moe_last_error_detail": (ctypes.c_char_p, []),
+        "moe_route_topk_noalloc": (ctypes.c_int, [sp, vp, vp, vp, vp, vp]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -174,6 +175,12 @@ def moe_forward(s, ws, x, w_router, w1, w3, w2, y, router_bias=None, w1s=None, w
                                   _p(w3), _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(y), _p(counts),
                                   _p(dropped), _p(losses), _p(ws), ws.numel(), _stream(stream),
                                   arr, len(events)), "moe_forward_events")
+
+
+def moe_route_topk_noalloc(s, logits_in, topk_idx, topk_gate, stats=None, stream=None):
+    """moe_route_topk on precomputed logits with no workspace (scratch inside the library)."""
+    _check(LIB.moe_route_topk_noalloc(ctypes.byref(s), _p(logits_in), _p(topk_idx), _p(topk_gate),
+                                      _p(stats), _stream(stream)), "moe_route_topk_noalloc")
 
 
 def moe_get_error(ws, stream=None) -> int:

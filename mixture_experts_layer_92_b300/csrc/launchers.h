@@ -10,6 +10,9 @@ namespace moe {
 
 struct DeviceError;
 
+// Sets the text moe_last_error_detail() returns on this thread; returns `status`.
+int set_error_detail(int status, const char* text);
+
 // ---------------------------------------------------------------- tcgen05 grouped GEMM
 enum TcMode : int { TC_F32OUT = 0, TC_SWIGLU = 1, TC_SCALE = 2 };
 

@@ -432,6 +432,12 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
 }
 
 }  // namespace
+
+int set_error_detail(int status, const char* text) {
+  g_detail = text;
+  return status;
+}
+
 }  // namespace moe
 
 using namespace moe;

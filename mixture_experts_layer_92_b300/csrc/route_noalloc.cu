@@ -1,0 +1,85 @@
+// moe_route_topk_noalloc: gates and top-k from precomputed logits without any workspace.
+//
+// Some callers cannot hand this library device memory: code that runs inside a host
+// framework which owns every device allocation and forbids cudaMalloc (allocation
+// synchronises the device and can stall other work), or a call site that has no allocator
+// at hand. For them this entry point keeps its only scratch -- the per-block partial sums
+// of the router statistics -- in a fixed-size array in the library's own device memory.
+//
+// The array is file-scope `static __device__` storage: every GPU that loads the library
+// holds kNoAllocScratchBytes of it until the process exits, and every call on a device uses
+// the same array. Calls that overlap on the GPU (for instance on two streams at once) race
+// on it; serialise them. The kernels write every partial before reading it, so nothing has
+// to be cleared between calls.
+#include <cstdio>
+#include <mutex>
+
+#include "common.cuh"
+#include "launchers.h"
+
+namespace moe {
+namespace {
+
+// 2 MiB: partials of route_blocks(T) blocks x (E + 1) floats. Enough for any T when
+// E <= 511 (at most 1024 blocks), and for larger E while T is small enough.
+constexpr size_t kNoAllocScratchBytes = 2u << 20;
+
+static __device__ __align__(256) float g_route_scratch[kNoAllocScratchBytes / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+std::once_flag g_setup_once[kMaxDevices];
+float* g_scratch_ptr[kMaxDevices];
+cudaError_t g_setup_status[kMaxDevices];
+
+// Host code cannot use g_route_scratch as an address (it names a host-side stand-in); the
+// device address is looked up once per device, with that device current.
+cudaError_t scratch_for_current_device(float** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::call_once(g_setup_once[dev], [dev]() {
+    void* p = nullptr;
+    g_setup_status[dev] = cudaGetSymbolAddress(&p, g_route_scratch);
+    g_scratch_ptr[dev] = static_cast<float*>(p);
+  });
+  if (g_setup_status[dev] != cudaSuccess) return g_setup_status[dev];
+  *out = g_scratch_ptr[dev];
+  return cudaSuccess;
+}
+
+}  // namespace
+}  // namespace moe
+
+extern "C" int moe_route_topk_noalloc(const moe_shape* s, const float* logits_in,
+                                      int32_t* topk_idx, float* topk_gate, float* stats,
+                                      void* stream) {
+  using namespace moe;
+  const int rc = moe_check_shape(s);
+  if (rc != MOE_OK) return rc;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (s->T == 0) {
+    if (stats != nullptr && cudaMemsetAsync(stats, 0, (s->E + 1) * sizeof(float), st) != cudaSuccess)
+      return MOE_ERR_CUDA;
+    return MOE_OK;
+  }
+  if (logits_in == nullptr || topk_idx == nullptr || topk_gate == nullptr)
+    return set_error_detail(MOE_ERR_INVALID, "logits_in, topk_idx and topk_gate are required");
+  const size_t need = static_cast<size_t>(route_blocks(s->T)) * (s->E + 1) * sizeof(float);
+  if (need > kNoAllocScratchBytes) {
+    char msg[160];
+    snprintf(msg, sizeof(msg),
+             "needs %zu bytes of scratch for T = %d, E = %d; the built-in scratch holds %zu",
+             need, s->T, s->E, kNoAllocScratchBytes);
+    return set_error_detail(MOE_ERR_UNSUPPORTED, msg);
+  }
+  float* partials = nullptr;
+  const cudaError_t se = scratch_for_current_device(&partials);
+  if (se != cudaSuccess) return set_error_detail(MOE_ERR_CUDA, cudaGetErrorString(se));
+  int r = launch_route_topk(logits_in, s->T, s->E, s->k, s->gate, topk_idx, topk_gate, partials,
+                            nullptr, st);
+  if (r != MOE_OK) return set_error_detail(r, "gates/top-k launch failed");
+  if (stats != nullptr) r = launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st);
+  if (r != MOE_OK) return set_error_detail(r, "statistics launch failed");
+  return set_error_detail(MOE_OK, "");
+}
