@@ -63,27 +63,43 @@ def capacity(w):
 def algorithmic_work(w, R: int, touched: int):
     """FLOPs and bytes the method itself must compute and move for one forward.
 
-    FLOPs: router 2*T*d*E, experts 6*d*d_ff per kept assignment (three GEMMs), shared expert
-    6*d*d_ff_s per token. Bytes: x + W_r + weights of the experts that received at least one
-    token (3*d*d_ff each) + shared expert weights + y. Per kernel (for the roofline of one
-    launch): gate/up GEMM 4*R*d*d_ff flops, down GEMM 2*R*d*d_ff flops (+ shared)."""
+    Layer: FLOPs = router 2*T*d*E + 6*d*d_ff per kept assignment (three GEMMs) + 6*d*d_ff_s
+    per token for the shared expert; bytes = x + W_r + weights of the experts that received
+    at least one token (3*d*d_ff each) + shared expert weights + y.
+    Per kernel (one launch): gate/up GEMM 4*R*d*d_ff FLOPs over W1+W3 of the touched
+    experts + its rows in and out; down GEMM 2*R*d*d_ff FLOPs over W2 + rows; the
+    bandwidth kernels their rows in and out."""
     es = 4 if w.dtype == "f32" else 2
-    T, d, E, F, Fs = w.T, w.d, w.E, w.d_ff, w.d_ff_shared
+    T, d, E, F, Fs, k = w.T, w.d, w.E, w.d_ff, w.d_ff_shared, w.k
     flops_router = 2.0 * T * d * E
     flops_gateup = 4.0 * R * d * F + 4.0 * T * d * Fs
     flops_down = 2.0 * R * d * F + 2.0 * T * d * Fs
-    bytes_total = (T * d * es + E * d * es + touched * 3.0 * d * F * es + 3.0 * d * Fs * es
-                   + T * d * es)
+    bytes_gateup = (touched * 2.0 * F * d + R * d + R * F + (2.0 * Fs * d + T * d + T * Fs)) * es
+    bytes_down = (touched * 1.0 * F * d + R * F + R * d + (Fs * d + T * Fs + T * d)) * es
+    bytes_total = (T * d + E * d + touched * 3.0 * d * F + 3.0 * d * Fs + T * d) * es
     return dict(flops=flops_router + flops_gateup + flops_down, bytes=bytes_total,
                 per_stage=dict(
-                    router_gemm=("hbm", T * d * es + E * d * es + T * E * 4.0),
-                    gates_topk=("hbm", T * E * 4.0 + T * w.k * 8.0),
-                    dispatch=("hbm", T * w.k * 4.0 * 3 + R * 4.0),
-                    gather=("hbm", 2.0 * R * d * es),
-                    gemm_gateup_swiglu=("tensor", flops_gateup),
-                    gemm_down_scale=("tensor", flops_down),
-                    combine=("hbm", R * d * es + T * d * es * (2 if Fs else 1)),
-                    aux_loss=("hbm", 0.0)))
+                    router_gemm=(flops_router, (T * d + E * d) * es + T * E * 4.0),
+                    gates_topk=(0.0, T * E * 4.0 + T * k * 8.0),
+                    dispatch=(0.0, T * k * 4.0 * 3 + R * 4.0),
+                    gather=(0.0, 2.0 * R * d * es),
+                    gemm_gateup_swiglu=(flops_gateup, bytes_gateup),
+                    gemm_down_scale=(flops_down, bytes_down),
+                    combine=(0.0, (R * d + T * d * (2 if Fs else 1)) * es),
+                    aux_loss=(0.0, 0.0)))
+
+
+def stage_roofline(flops, nbytes, ms, pk):
+    """Achieved rate of one kernel against whichever roofline binds it."""
+    t_tensor = flops / (pk["bf16_tflops"] * 1e12)
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    if flops > 0 and t_tensor >= t_hbm:
+        ach = flops / (ms / 1e3) / 1e12
+        return dict(ms=ms, bound="tensor", achieved=ach, unit="TFLOP/s", peak=pk["bf16_tflops"],
+                    frac=ach / pk["bf16_tflops"], algorithmic=flops)
+    ach = nbytes / (ms / 1e3) / 1e9 if ms > 0 else 0.0
+    return dict(ms=ms, bound="hbm", achieved=ach, unit="GB/s", peak=pk["hbm_gbs"],
+                frac=ach / pk["hbm_gbs"], algorithmic=nbytes)
 
 
 def source_sha(path):
@@ -325,24 +341,17 @@ def run_ours(args, w, rank, world, local_rank):
     ms_per_step = total_ms / args.steps
     stages = {}
     for name in STAGES:
-        ms = statistics.mean(stage_ms[name])
-        bound, amount = work["per_stage"][name]
-        if bound == "tensor":
-            ach = amount / (ms / 1e3) / 1e12
-            stages[name] = dict(ms=ms, bound="tensor", achieved=ach, unit="TFLOP/s",
-                                frac=ach / pk["bf16_tflops"])
-        else:
-            ach = amount / (ms / 1e3) / 1e9 if ms > 0 else 0.0
-            stages[name] = dict(ms=ms, bound="hbm", achieved=ach, unit="GB/s",
-                                frac=ach / pk["hbm_gbs"])
-    dom = stages[DOMINANT] if w.dtype == "bf16" else None
+        flops, nbytes = work["per_stage"][name]
+        stages[name] = stage_roofline(flops, nbytes, statistics.mean(stage_ms[name]), pk)
     roofline = None
-    if dom is not None:
+    if w.dtype == "bf16":
+        dom = stages[DOMINANT]
         tr = traffic_from_profile(w.name, DOMINANT)
-        roofline = dict(bound="tensor", kernel=DOMINANT, achieved=dom["achieved"],
-                        peak=pk["bf16_tflops"], unit="TFLOP/s", frac=dom["frac"], traffic=tr,
-                        peak_source=f"{pk['source']} bf16 burst",
-                        algorithmic=f"{work['per_stage'][DOMINANT][1]:.4e} FLOP per launch")
+        roofline = dict(bound=dom["bound"], kernel=DOMINANT, achieved=dom["achieved"],
+                        peak=dom["peak"], unit=dom["unit"], frac=dom["frac"], traffic=tr,
+                        peak_source=f"{pk['source']} " + ("bf16 burst" if dom["bound"] == "tensor"
+                                                          else "HBM copy"),
+                        algorithmic_per_launch=dom["algorithmic"])
     t_roof = max(work["flops"] / (pk["bf16_tflops"] * 1e12), work["bytes"] / (pk["hbm_gbs"] * 1e9))
     layer_roof = dict(flops=work["flops"], bytes=work["bytes"], roofline_ms=t_roof * 1e3,
                       measured_ms=ms_per_step, frac=t_roof * 1e3 / ms_per_step,

@@ -31,8 +31,10 @@
  *     timed out) set a sticky error word in the workspace; read it with moe_get_error.
  *     The device never traps.
  *   - `ws` is a device workspace of at least moe_workspace_size(shape) bytes, 256-byte
- *     aligned. Every entry point takes the same workspace layout; calls that overlap on
- *     the GPU must not share a workspace.
+ *     aligned. Its first 256 bytes (the error word and the dispatch kernel's grid-barrier
+ *     counters) must be zero before its first use -- moe_clear_error does that; later calls
+ *     keep the counters consistent by themselves. Every entry point takes the same workspace layout;
+ *     calls that overlap on the GPU must not share a workspace.
  */
 #ifndef MOE_H_
 #define MOE_H_

@@ -20,6 +20,8 @@ struct DeviceError {
   int where;      // kernel/site id of the first error
   int detail;     // site-specific detail (e.g. offending index)
   int pad;
+  unsigned grid_count;  // grid barrier of the dispatch kernel: arrivals (back to 0 after use)
+  unsigned grid_gen;    //                                     generation
 };
 
 enum ErrSite : int {
@@ -30,6 +32,7 @@ enum ErrSite : int {
   SITE_GEMM_WAIT_TMEM_FULL = 12,
   SITE_GEMM_WAIT_TMEM_EMPTY = 13,
   SITE_GEMM_WAIT_DRAIN = 14,
+  SITE_DISPATCH_GRID_BARRIER = 20,
 };
 
 __device__ __forceinline__ void record_error(DeviceError* e, int code, int where, int detail) {

@@ -6,15 +6,20 @@
 // assignments are visited in token order, which decides who is kept; the overflow is
 // dropped and counted).
 //
-// One CTA of 1024 threads (32 warps). Warp w owns a contiguous chunk of assignments, so
-// "earlier chunk" = "earlier tokens". Three phases:
-//   1. per-warp histogram hist[w][e] (warp match + popcount, one writer per (w, e));
-//   2. for each expert an exclusive scan over warps gives the rank of the warp's first
-//      assignment to e; n_e = total; kept_e = min(n_e, C); offsets = exclusive scan of kept;
-//   3. each warp re-walks its chunk in 32-wide pieces; an assignment's rank is its warp's
-//      base + the running count + the number of lower lanes in the piece with the same
-//      expert. rank < C -> perm[offsets[e] + rank] = a, inv[a] = that row; else inv[a] = -1.
-// Integer-only and order-preserving: the outputs are bit-exact functions of the input.
+// One cooperative launch of nb CTAs x 1024 threads (all co-resident). CTA b owns the
+// contiguous assignments [b*chunk, (b+1)*chunk) and warp w of it a contiguous slice, so
+// "earlier CTA / earlier warp" = "earlier tokens". Phases:
+//   1. per-warp histogram hist[w][e] (warp match + popcount, one writer per (w, e)); turned
+//      into per-warp exclusive prefixes inside the CTA; the CTA total goes to blk_hist[b][e];
+//   -- grid barrier (bounded wait) --
+//   2. every CTA sums blk_hist in CTA order: base_b[e] (assignments to e in earlier CTAs) and
+//      n_e; kept_e = min(n_e, C); offsets = exclusive scan of kept (CTA 0 writes them);
+//   3. each warp re-walks its slice in 32-wide pieces; an assignment's rank among those
+//      routed to its expert is base_b + its warp's prefix + the running count + the number
+//      of lower lanes in the piece with the same expert. rank < C -> kept at offsets[e] + rank.
+// Integer-only and order-preserving: the outputs are bit-exact and independent of nb.
+#include <algorithm>
+
 #include "common.cuh"
 #include "launchers.h"
 
@@ -24,14 +29,45 @@ namespace {
 
 constexpr int kDispThreads = 1024;
 constexpr int kDispWarps = kDispThreads / 32;
+constexpr int kChunk = 1024;  // assignments per CTA (one 32-wide piece per warp), or a multiple
+
+// All CTAs of the (cooperative, co-resident) grid meet here. Bounded: after kWaitLimitNs the
+// waiting CTA records MOE_ERR_TIMEOUT and carries on.
+__device__ __forceinline__ void grid_barrier(DeviceError* sync, unsigned nblocks) {
+  __syncthreads();
+  if (threadIdx.x == 0 && nblocks > 1) {
+    volatile unsigned* gen = &sync->grid_gen;
+    const unsigned g = *gen;
+    __threadfence();
+    const unsigned arrived = atomicAdd(&sync->grid_count, 1u);
+    if (arrived == nblocks - 1) {
+      atomicExch(&sync->grid_count, 0u);
+      __threadfence();
+      atomicAdd(&sync->grid_gen, 1u);
+    } else {
+      const unsigned long long t0 = global_timer_ns();
+      while (*gen == g) {
+        __nanosleep(64);
+        if (global_timer_ns() - t0 > kWaitLimitNs) {
+          record_error(sync, MOE_ERR_TIMEOUT, SITE_DISPATCH_GRID_BARRIER, blockIdx.x);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+}
 
 __global__ void __launch_bounds__(kDispThreads)
-dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int32_t* __restrict__ counts,
-                int32_t* __restrict__ offsets, int32_t* __restrict__ perm,
-                int32_t* __restrict__ inv, int32_t* __restrict__ dropped, DeviceError* err) {
+dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int chunk,
+                int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
+                int32_t* __restrict__ perm, int32_t* __restrict__ inv,
+                int32_t* __restrict__ dropped, int32_t* __restrict__ blk_hist, DeviceError* err) {
   extern __shared__ int s_mem[];
   int* hist = s_mem;                       // [kDispWarps][E]
-  int* s_off = hist + kDispWarps * E;      // [E + 1]
+  int* s_base = hist + kDispWarps * E;     // [E]
+  int* s_off = s_base + E;                 // [E + 1]
   int* s_wsum = s_off + E + 1;             // [kDispWarps]
   const int tid = threadIdx.x;
   const int lane = tid & 31;
@@ -41,11 +77,12 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int32_t* _
   for (int i = tid; i < kDispWarps * E; i += kDispThreads) hist[i] = 0;
   __syncthreads();
 
-  const int per_warp = (((A + kDispWarps - 1) / kDispWarps) + 31) & ~31;
-  const int a_begin = warp * per_warp;
-  const int a_end = min(A, a_begin + per_warp);
+  const int blk_begin = blockIdx.x * chunk;
+  const int per_warp = chunk / kDispWarps;
+  const int a_begin = blk_begin + warp * per_warp;
+  const int a_end = min(min(A, blk_begin + chunk), a_begin + per_warp);
 
-  // phase 1: histogram of this warp's chunk
+  // phase 1: histogram of this warp's slice
   for (int base = a_begin; base < a_end; base += 32) {
     const int a = base + lane;
     int key = -1;
@@ -58,8 +95,6 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int32_t* _
     if (key >= 0 && lane == __ffs(peers) - 1) hist[warp * E + key] += __popc(peers);
   }
   __syncthreads();
-
-  // phase 2: per-expert scan over warps, then the kept counts
   for (int e = tid; e < E; e += kDispThreads) {
     int run = 0;
     for (int w = 0; w < kDispWarps; ++w) {
@@ -67,12 +102,25 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int32_t* _
       hist[w * E + e] = run;
       run += c;
     }
-    counts[e] = run;
-    s_off[e] = min(run, C);
+    blk_hist[static_cast<size_t>(blockIdx.x) * E + e] = run;
+  }
+  grid_barrier(err, gridDim.x);
+
+  // phase 2: this CTA's base per expert, the totals, the kept counts
+  for (int e = tid; e < E; e += kDispThreads) {
+    int before = 0, total = 0;
+    for (int b = 0; b < static_cast<int>(gridDim.x); ++b) {
+      const int c = __ldcg(blk_hist + static_cast<size_t>(b) * E + e);
+      if (b < static_cast<int>(blockIdx.x)) before += c;
+      total += c;
+    }
+    s_base[e] = before;
+    s_off[e] = min(total, C);
+    if (blockIdx.x == 0) counts[e] = total;
   }
   __syncthreads();
-  // exclusive scan of s_off[0..E) (E <= 1024: one element per thread)
   {
+    // exclusive scan of s_off[0..E) (E <= 1024: one element per thread)
     const int v = (tid < E) ? s_off[tid] : 0;
     int incl = v;
 #pragma unroll
@@ -89,7 +137,7 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int32_t* _
         const int n = __shfl_up_sync(0xffffffffu, w, o);
         if (lane >= o) w += n;
       }
-      s_wsum[lane] = w;  // inclusive over warps
+      s_wsum[lane] = w;
     }
     __syncthreads();
     const int excl = incl - v + (warp > 0 ? s_wsum[warp - 1] : 0);
@@ -97,8 +145,10 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int32_t* _
     if (tid == 0) s_off[E] = s_wsum[kDispWarps - 1];
     __syncthreads();
   }
-  for (int e = tid; e <= E; e += kDispThreads) offsets[e] = s_off[e];
-  if (tid == 0) *dropped = A - s_off[E];
+  if (blockIdx.x == 0) {
+    for (int e = tid; e <= E; e += kDispThreads) offsets[e] = s_off[e];
+    if (tid == 0) *dropped = A - s_off[E];
+  }
 
   // phase 3: stable scatter
   for (int base = a_begin; base < a_end; base += 32) {
@@ -110,7 +160,7 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int32_t* _
     }
     const unsigned peers = __match_any_sync(0xffffffffu, key);
     if (key >= 0) {
-      const int rank = hist[warp * E + key] + __popc(peers & lt_mask);
+      const int rank = s_base[key] + hist[warp * E + key] + __popc(peers & lt_mask);
       if (rank < C) {
         const int row = s_off[key] + rank;
         perm[row] = a;
@@ -129,18 +179,34 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int32_t* _
 
 }  // namespace
 
+int dispatch_max_blocks(int num_sms) { return std::max(1, std::min(num_sms, 148)); }
+
 int launch_dispatch(const int32_t* topk_idx, int A, int E, int C, int32_t* counts,
                     int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dropped,
-                    DeviceError* err, cudaStream_t stream) {
-  const size_t smem = (static_cast<size_t>(kDispWarps) * E + E + 1 + kDispWarps) * sizeof(int);
-  if (smem > 48 * 1024) {
-    if (cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             static_cast<int>(smem)) != cudaSuccess)
-      return MOE_ERR_CUDA;
+                    int32_t* blk_hist, DeviceError* err, int num_sms, cudaStream_t stream) {
+  const size_t smem =
+      (static_cast<size_t>(kDispWarps) * E + E + E + 1 + kDispWarps) * sizeof(int);
+  if (cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(smem)) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, dispatch_kernel, kDispThreads, smem) !=
+          cudaSuccess ||
+      per_sm < 1)
+    return MOE_ERR_CUDA;
+  const int max_blocks = std::min(dispatch_max_blocks(num_sms), num_sms * per_sm);
+  int chunk = kChunk;
+  int nb = std::max(1, (A + chunk - 1) / chunk);
+  if (nb > max_blocks) {
+    chunk = ((A + max_blocks - 1) / max_blocks + kChunk - 1) / kChunk * kChunk;
+    nb = std::max(1, (A + chunk - 1) / chunk);
   }
-  dispatch_kernel<<<1, kDispThreads, smem, stream>>>(topk_idx, A, E, C, counts, offsets, perm, inv,
-                                                     dropped, err);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  void* args[] = {const_cast<int32_t**>(&topk_idx), &A, &E, &C, &chunk, &counts, &offsets, &perm,
+                  &inv, &dropped, &blk_hist, &err};
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(dispatch_kernel), dim3(nb),
+                                  dim3(kDispThreads), args, smem, stream) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 }  // namespace moe

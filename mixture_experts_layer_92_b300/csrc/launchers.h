@@ -31,6 +31,9 @@ struct TcArgs {
   const int32_t* perm;      // TC_SCALE: row r is scaled by gate[perm[r]] (gate == nullptr: 1)
   const float* gate;
   const float* bias;        // TC_F32OUT: per-column bias or nullptr
+  int splits;               // TC_F32OUT: split-K factor (>= 1); split s writes out + s*split_stride
+  int kb_per_split;         //            k-blocks (of 64) per split
+  long long split_stride;   //            elements
   DeviceError* err;
 };
 
@@ -72,17 +75,31 @@ int launch_simt_gemm(int mode, const SimtArgs& a, cudaStream_t stream);
 
 // ---------------------------------------------------------------- routing
 int route_blocks(int T);
-int launch_route_topk(const float* logits, int T, int E, int k, int gate_mode, int32_t* topk_idx,
-                      float* topk_gate, float* partials, DeviceError* err, cudaStream_t stream);
+struct RouteArgs {
+  const float* logits;      // [nsplit][T][E] fp32 partial logits, summed in split order
+  int nsplit;
+  size_t split_stride;      // elements between splits
+  const float* bias;        // [E] added after the sum, or nullptr
+  float* logits_out;        // [T][E] receives the final logits, or nullptr
+  int T, E, k, gate_mode;
+  int32_t* topk_idx;        // [T][k]
+  float* topk_gate;         // [T][k]
+  float* partials;          // [route_blocks(T)][E + 1]
+  DeviceError* err;         // nullptr: no device error reporting
+};
+int launch_route_topk(const RouteArgs& a, cudaStream_t stream);
 int launch_stats_reduce(const float* partials, int nblocks, int E, float* stats,
                         cudaStream_t stream);
 int launch_aux_loss(const float* stats, const int32_t* counts, int T, int E, int k, float alpha,
                     float beta, float* losses, cudaStream_t stream);
 
 // ---------------------------------------------------------------- dispatch
+// blk_hist: [dispatch_max_blocks(num_sms)][E] int32 scratch; err: the workspace header
+// (required: it also holds the grid-barrier words).
+int dispatch_max_blocks(int num_sms);
 int launch_dispatch(const int32_t* topk_idx, int A, int E, int C, int32_t* counts,
                     int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dropped,
-                    DeviceError* err, cudaStream_t stream);
+                    int32_t* blk_hist, DeviceError* err, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- data movement
 int launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, int E, int k,

@@ -35,8 +35,34 @@ size_t esize(const moe_shape* s) { return s->dtype == MOE_BF16 ? 2 : 4; }
 constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) / kAlign * kAlign; }
 
+int pick_router_bn(int E) {
+  if (E <= 16) return 16;
+  if (E <= 32) return 32;
+  if (E <= 64) return 64;
+  if (E <= 128) return 128;
+  return 256;
+}
+
+// Split-K factor of the tensor-core router GEMM: enough CTAs to stream x at HBM speed when
+// T/128 row tiles alone would leave most SMs idle. A function of the shape only (148 is the
+// B300 SM count), so the summation order -- and every bit of the logits -- is fixed.
+struct RouterSplit {
+  int splits, kb_per_split;
+};
+RouterSplit router_split(const moe_shape* s) {
+  if (s->dtype != MOE_BF16 || s->T == 0) return {1, 0};
+  const int bn = pick_router_bn(s->E);
+  const long long tiles = static_cast<long long>((s->T + 127) / 128) * ((s->E + bn - 1) / bn);
+  const int nk = (s->d + 63) / 64;
+  long long want = 148 / std::max<long long>(tiles, 1);
+  want = std::max<long long>(1, std::min<long long>(want, std::min(16, nk)));
+  const int kb = (nk + static_cast<int>(want) - 1) / static_cast<int>(want);
+  return {(nk + kb - 1) / kb, kb};
+}
+
 struct Layout {
-  size_t err, logits, idx, gate, partials, stats, counts, offsets, perm, inv, dropped, losses;
+  size_t err, logits, idx, gate, partials, stats, counts, offsets, perm, inv, dropped, losses,
+      blk_hist;
   size_t xp, h, yp, hs, ys, total;
 };
 
@@ -52,7 +78,7 @@ Layout layout(const moe_shape* s) {
     return at;
   };
   L.err = take(sizeof(DeviceError));
-  L.logits = take(T * E * 4);
+  L.logits = take(static_cast<size_t>(router_split(s).splits) * T * E * 4);
   L.idx = take(A * 4);
   L.gate = take(A * 4);
   L.partials = take(static_cast<size_t>(route_blocks(s->T)) * (E + 1) * 4);
@@ -63,6 +89,7 @@ Layout layout(const moe_shape* s) {
   L.inv = take(A * 4);
   L.dropped = take(4);
   L.losses = take(2 * 4);
+  L.blk_hist = take(static_cast<size_t>(dispatch_max_blocks(148)) * E * 4);
   L.xp = take(A * d * es);
   L.h = take(A * F * es);
   L.yp = take(A * d * es);
@@ -158,17 +185,10 @@ int cuda_status(const char* what) {
     }                                                                        \
   } while (0)
 
-int pick_router_bn(int E) {
-  if (E <= 16) return 16;
-  if (E <= 32) return 32;
-  if (E <= 64) return 64;
-  if (E <= 128) return 128;
-  return 256;
-}
-
 // ---------------------------------------------------------------- stage 0: router GEMM
-int run_router(const moe_shape* s, const void* x, const void* wr, const float* bias, float* logits,
-               DeviceError* err, cudaStream_t st) {
+// Writes router_split(s).splits partial logit planes [T, E] (fp32, no bias) to `logits`.
+int run_router(const moe_shape* s, const void* x, const void* wr, float* logits, DeviceError* err,
+               cudaStream_t st) {
   if (s->T == 0) return MOE_OK;
   if (s->dtype == MOE_F32) {
     SimtArgs a{};
@@ -181,11 +201,12 @@ int run_router(const moe_shape* s, const void* x, const void* wr, const float* b
     a.n = s->E;
     a.k = s->d;
     a.out = logits;
-    a.bias = bias;
+    a.bias = nullptr;  // added by the top-k kernel
     LAUNCH(launch_simt_gemm(TC_F32OUT, a, st), "router GEMM (fp32)");
     return MOE_OK;
   }
   const int bn = pick_router_bn(s->E);
+  const RouterSplit sp = router_split(s);
   TcProblem p{};
   p.args.groups = 1;
   p.args.offsets = nullptr;
@@ -194,17 +215,40 @@ int run_router(const moe_shape* s, const void* x, const void* wr, const float* b
   p.args.k_routed = s->d;
   p.args.out_routed = logits;
   p.args.ldo_routed = s->E;
-  p.args.bias = bias;
+  p.args.bias = nullptr;  // added by the top-k kernel, after the split-K sum
+  p.args.splits = sp.splits;
+  p.args.kb_per_split = sp.kb_per_split;
+  p.args.split_stride = static_cast<long long>(s->T) * s->E;
   p.args.err = err;
   p.a = x;
   p.a_rows = s->T;
   p.b0 = wr;
   p.b_rows = s->E;
   p.b_groups = 1;
-  p.max_tiles = static_cast<long long>((s->T + 127) / 128) * ((s->E + bn - 1) / bn);
+  p.max_tiles = static_cast<long long>((s->T + 127) / 128) * ((s->E + bn - 1) / bn) * sp.splits;
   p.num_sms = num_sms();
   LAUNCH(launch_tc_gemm(TC_F32OUT, bn, p, st), "router GEMM (tcgen05)");
   return MOE_OK;
+}
+
+RouteArgs route_args(const moe_shape* s, const float* logits, int nsplit, const float* bias,
+                     float* logits_out, int32_t* idx, float* gate, float* partials,
+                     DeviceError* err) {
+  RouteArgs a{};
+  a.logits = logits;
+  a.nsplit = nsplit;
+  a.split_stride = static_cast<size_t>(s->T) * s->E;
+  a.bias = bias;
+  a.logits_out = logits_out;
+  a.T = s->T;
+  a.E = s->E;
+  a.k = s->k;
+  a.gate_mode = s->gate;
+  a.topk_idx = idx;
+  a.topk_gate = gate;
+  a.partials = partials;
+  a.err = err;
+  return a;
 }
 
 // ---------------------------------------------------------------- stages 4-5: expert GEMMs
@@ -405,13 +449,16 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   };
 
   rec(0);
-  TRY(run_router(s, x, w_router, router_bias, logits, err, st));
+  TRY(run_router(s, x, w_router, logits, err, st));
   rec(1);
   if (s->T > 0)
-    LAUNCH(launch_route_topk(logits, s->T, s->E, s->k, s->gate, idx, gate, partials, err, st),
+    LAUNCH(launch_route_topk(route_args(s, logits, router_split(s).splits, router_bias, nullptr,
+                                        idx, gate, partials, err),
+                             st),
            "gates/top-k");
   rec(2);
-  LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, cnt, off, perm, inv, drp, err, st),
+  LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, cnt, off, perm, inv, drp,
+                         at<int32_t>(ws, L.blk_hist), err, num_sms(), st),
          "dispatch");
   if (s->T > 0) {
     TRY(run_experts(s, x, perm, off, gate, w1, w3, w2, w1s, w3s, w2s, yp, ys, ws, st, ev, 3));
@@ -489,19 +536,21 @@ int moe_route_topk(const moe_shape* s, const void* x, const void* w_router,
       return cuda_status("memset stats");
     return ok();
   }
-  const float* logits = logits_in;
-  if (logits == nullptr) {
-    float* dst = logits_out ? logits_out : at<float>(ws, L.logits);
-    TRY(run_router(s, x, w_router, router_bias, dst, err, st));
-    logits = dst;
-  } else if (logits_out != nullptr && logits_out != logits_in) {
-    if (cudaMemcpyAsync(logits_out, logits_in, static_cast<size_t>(s->T) * s->E * sizeof(float),
-                        cudaMemcpyDeviceToDevice, st) != cudaSuccess)
-      return cuda_status("copy logits");
-  }
   float* partials = at<float>(ws, L.partials);
-  LAUNCH(launch_route_topk(logits, s->T, s->E, s->k, s->gate, topk_idx, topk_gate, partials, err, st),
-         "gates/top-k");
+  if (logits_in == nullptr) {
+    float* planes = at<float>(ws, L.logits);
+    TRY(run_router(s, x, w_router, planes, err, st));
+    LAUNCH(launch_route_topk(route_args(s, planes, router_split(s).splits, router_bias, logits_out,
+                                        topk_idx, topk_gate, partials, err),
+                             st),
+           "gates/top-k");
+  } else {
+    LAUNCH(launch_route_topk(route_args(s, logits_in, 1, nullptr,
+                                        logits_out == logits_in ? nullptr : logits_out, topk_idx,
+                                        topk_gate, partials, err),
+                             st),
+           "gates/top-k");
+  }
   if (stats) LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
   return ok();
 }
@@ -526,13 +575,14 @@ int moe_dispatch(const moe_shape* s, const int32_t* topk_idx, const float* logit
   const int32_t* idx = topk_idx;
   if (idx == nullptr && s->T > 0) {
     int32_t* widx = at<int32_t>(ws, L.idx);
-    LAUNCH(launch_route_topk(logits_in, s->T, s->E, s->k, s->gate, widx, at<float>(ws, L.gate),
-                             at<float>(ws, L.partials), err, st),
+    LAUNCH(launch_route_topk(route_args(s, logits_in, 1, nullptr, nullptr, widx,
+                                        at<float>(ws, L.gate), at<float>(ws, L.partials), err),
+                             st),
            "gates/top-k");
     idx = widx;
   }
   LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, counts, offsets, perm, inv, dropped,
-                         err, st),
+                         at<int32_t>(ws, L.blk_hist), err, num_sms(), st),
          "dispatch");
   return ok();
 }

@@ -54,53 +54,87 @@ __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 v) {
   }
 }
 
-// One warp per token; each lane owns 16-byte chunks of the row (8 bf16 values).
-__global__ void __launch_bounds__(kMoveThreads)
-combine_bf16_kernel(const uint4* __restrict__ yp, const int32_t* __restrict__ inv,
-                    const uint4* __restrict__ ys, uint4* __restrict__ y, int T, int k, int nvec) {
-  const int lane = threadIdx.x & 31;
-  const int nw = gridDim.x * kMoveWarps;
-  for (int t = blockIdx.x * kMoveWarps + (threadIdx.x >> 5); t < T; t += nw) {
-    const int32_t* slots = inv + static_cast<size_t>(t) * k;
-    for (int i = lane; i < nvec; i += 32) {
-      float acc[8];
-#pragma unroll
-      for (int q = 0; q < 8; ++q) acc[q] = 0.f;
-      for (int s = 0; s < k; ++s) {
-        const int r = __ldg(slots + s);
-        if (r >= 0) add_bf16x8(acc, __ldg(yp + static_cast<size_t>(r) * nvec + i));
-      }
-      if (ys != nullptr) add_bf16x8(acc, __ldg(ys + static_cast<size_t>(t) * nvec + i));
-      y[static_cast<size_t>(t) * nvec + i] =
-          make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
-                     pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
-    }
-  }
+__device__ __forceinline__ void add_f32x4(float (&acc)[8], const uint4 v) {
+  acc[0] += __uint_as_float(v.x);
+  acc[1] += __uint_as_float(v.y);
+  acc[2] += __uint_as_float(v.z);
+  acc[3] += __uint_as_float(v.w);
 }
 
-// fp32 variant: 16-byte chunks of 4 floats.
+template <bool BF16>
+__device__ __forceinline__ void add_chunk(float (&acc)[8], const uint4 v) {
+  if (BF16) add_bf16x8(acc, v); else add_f32x4(acc, v);
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint4 pack_chunk(const float (&acc)[8]) {
+  if (BF16)
+    return make_uint4(pack_bf16x2(acc[0], acc[1]), pack_bf16x2(acc[2], acc[3]),
+                      pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+  return make_uint4(__float_as_uint(acc[0]), __float_as_uint(acc[1]), __float_as_uint(acc[2]),
+                    __float_as_uint(acc[3]));
+}
+
+// One warp per (token, segment of 64 16-byte chunks); each lane owns chunks c and c + 32
+// of the segment. KS > 0 unrolls the slot loop (all 2*KS loads issued before the adds);
+// KS == 0 handles any k. Sums run in slot order in fp32, the shared expert last.
+template <bool BF16, int KS>
 __global__ void __launch_bounds__(kMoveThreads)
-combine_f32_kernel(const float4* __restrict__ yp, const int32_t* __restrict__ inv,
-                   const float4* __restrict__ ys, float4* __restrict__ y, int T, int k, int nvec) {
+combine_kernel(const uint4* __restrict__ yp, const int32_t* __restrict__ inv,
+               const uint4* __restrict__ ys, uint4* __restrict__ y, int T, int k, int nvec) {
   const int lane = threadIdx.x & 31;
-  const int nw = gridDim.x * kMoveWarps;
-  for (int t = blockIdx.x * kMoveWarps + (threadIdx.x >> 5); t < T; t += nw) {
+  const int nseg = (nvec + 63) / 64;
+  const long long total = static_cast<long long>(T) * nseg;
+  const long long nw = static_cast<long long>(gridDim.x) * kMoveWarps;
+  for (long long w = static_cast<long long>(blockIdx.x) * kMoveWarps + (threadIdx.x >> 5); w < total;
+       w += nw) {
+    const int t = static_cast<int>(w / nseg);
+    const int seg = static_cast<int>(w - static_cast<long long>(t) * nseg);
+    const int c0 = seg * 64 + lane, c1 = c0 + 32;
+    const bool h0 = c0 < nvec, h1 = c1 < nvec;
     const int32_t* slots = inv + static_cast<size_t>(t) * k;
-    for (int i = lane; i < nvec; i += 32) {
-      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float a0[8], a1[8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q) a0[q] = a1[q] = 0.f;
+    if (KS > 0) {
+      int r[KS > 0 ? KS : 1];
+      uint4 v0[KS > 0 ? KS : 1], v1[KS > 0 ? KS : 1];
+#pragma unroll
+      for (int s = 0; s < KS; ++s) r[s] = __ldg(slots + s);
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        v0[s] = v1[s] = make_uint4(0, 0, 0, 0);
+        if (r[s] >= 0) {
+          const uint4* row = yp + static_cast<size_t>(r[s]) * nvec;
+          if (h0) v0[s] = __ldg(row + c0);
+          if (h1) v1[s] = __ldg(row + c1);
+        }
+      }
+#pragma unroll
+      for (int s = 0; s < KS; ++s) {
+        if (r[s] >= 0) {
+          add_chunk<BF16>(a0, v0[s]);
+          add_chunk<BF16>(a1, v1[s]);
+        }
+      }
+    } else {
       for (int s = 0; s < k; ++s) {
         const int r = __ldg(slots + s);
         if (r >= 0) {
-          const float4 v = __ldg(yp + static_cast<size_t>(r) * nvec + i);
-          acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+          const uint4* row = yp + static_cast<size_t>(r) * nvec;
+          if (h0) add_chunk<BF16>(a0, __ldg(row + c0));
+          if (h1) add_chunk<BF16>(a1, __ldg(row + c1));
         }
       }
-      if (ys != nullptr) {
-        const float4 v = __ldg(ys + static_cast<size_t>(t) * nvec + i);
-        acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
-      }
-      y[static_cast<size_t>(t) * nvec + i] = acc;
     }
+    if (ys != nullptr) {
+      const uint4* row = ys + static_cast<size_t>(t) * nvec;
+      if (h0) add_chunk<BF16>(a0, __ldg(row + c0));
+      if (h1) add_chunk<BF16>(a1, __ldg(row + c1));
+    }
+    uint4* out = y + static_cast<size_t>(t) * nvec;
+    if (h0) out[c0] = pack_chunk<BF16>(a0);
+    if (h1) out[c1] = pack_chunk<BF16>(a1);
   }
 }
 
@@ -120,19 +154,31 @@ int launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, in
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
+template <bool BF16>
+void combine_dispatch_k(int grid, const uint4* yp, const int32_t* inv, const uint4* ys, uint4* y,
+                        int T, int k, int nvec, cudaStream_t stream) {
+  switch (k) {
+    case 1: combine_kernel<BF16, 1><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec); break;
+    case 2: combine_kernel<BF16, 2><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec); break;
+    case 4: combine_kernel<BF16, 4><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec); break;
+    case 6: combine_kernel<BF16, 6><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec); break;
+    case 8: combine_kernel<BF16, 8><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec); break;
+    default: combine_kernel<BF16, 0><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec);
+  }
+}
+
 int launch_combine(int dtype, const void* yp, const int32_t* inv, const void* ys, void* y, int T,
                    int k, int d, int num_sms, cudaStream_t stream) {
   if (T <= 0) return MOE_OK;
-  const int grid = grid_for_rows(T, num_sms);
-  if (dtype == MOE_BF16) {
-    combine_bf16_kernel<<<grid, kMoveThreads, 0, stream>>>(
-        static_cast<const uint4*>(yp), inv, static_cast<const uint4*>(ys), static_cast<uint4*>(y),
-        T, k, d / 8);
-  } else {
-    combine_f32_kernel<<<grid, kMoveThreads, 0, stream>>>(
-        static_cast<const float4*>(yp), inv, static_cast<const float4*>(ys),
-        static_cast<float4*>(y), T, k, d / 4);
-  }
+  const int row_bytes = d * (dtype == MOE_BF16 ? 2 : 4);
+  const int nvec = row_bytes / 16;
+  const long long warps = static_cast<long long>(T) * ((nvec + 63) / 64);
+  const int grid = grid_for_rows(warps, num_sms);
+  const uint4* a = static_cast<const uint4*>(yp);
+  const uint4* b = static_cast<const uint4*>(ys);
+  uint4* o = static_cast<uint4*>(y);
+  if (dtype == MOE_BF16) combine_dispatch_k<true>(grid, a, inv, b, o, T, k, nvec, stream);
+  else combine_dispatch_k<false>(grid, a, inv, b, o, T, k, nvec, stream);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

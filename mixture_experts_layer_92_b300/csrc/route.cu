@@ -29,9 +29,10 @@ constexpr int kNoIdx = 0x7fffffff;
 // JM = values per lane: lane l holds the logits of experts l, l+32, ..., l+32*(JM-1).
 template <int JM>
 __global__ void __launch_bounds__(kRouteThreads)
-route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int gate_mode,
-                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
-                  float* __restrict__ partials, DeviceError* err) {
+route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_stride,
+                  const float* __restrict__ bias, float* __restrict__ logits_out, int T, int E,
+                  int k, int gate_mode, int32_t* __restrict__ topk_idx,
+                  float* __restrict__ topk_gate, float* __restrict__ partials, DeviceError* err) {
   extern __shared__ float s_part[];  // [kRouteWarps][E + 1]
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -50,9 +51,18 @@ route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int gat
 #pragma unroll
     for (int j = 0; j < JM; ++j) {
       const int e = lane + 32 * j;
-      v[j] = (e < E) ? __ldg(row + e) : -INFINITY;
       slot[j] = -1;
-      if (e < E && !isfinite(v[j])) bad = true;
+      if (e < E) {
+        // split-K partial sums of the router GEMM, added in split order, then the bias
+        float acc = __ldg(row + e);
+        for (int sp = 1; sp < nsplit; ++sp) acc += __ldg(row + sp * split_stride + e);
+        if (bias != nullptr) acc += __ldg(bias + e);
+        if (logits_out != nullptr) logits_out[static_cast<size_t>(t) * E + e] = acc;
+        v[j] = acc;
+        if (!isfinite(acc)) bad = true;
+      } else {
+        v[j] = -INFINITY;
+      }
     }
     if (__any_sync(0xffffffffu, bad)) {
       if (lane == 0) record_error(err, MOE_ERR_NONFINITE, SITE_ROUTE_NONFINITE, t);
@@ -145,14 +155,22 @@ route_topk_kernel(const float* __restrict__ logits, int T, int E, int k, int gat
   }
 }
 
-// stats[e] = sum over blocks (in block order) of partials[b][e], accumulated in double.
-__global__ void stats_reduce_kernel(const float* __restrict__ partials, int nb, int E,
-                                    float* __restrict__ stats) {
-  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e <= E; e += gridDim.x * blockDim.x) {
-    double acc = 0.0;
-    for (int b = 0; b < nb; ++b) acc += partials[static_cast<size_t>(b) * (E + 1) + e];
-    stats[e] = static_cast<float>(acc);
+// stats[e] = sum over the blocks of partials[b][e]: one CTA per column e, each thread sums
+// a fixed stride of blocks in double, then a fixed-shape tree in shared memory
+// (deterministic: the order depends only on the block count).
+__global__ void __launch_bounds__(256)
+stats_reduce_kernel(const float* __restrict__ partials, int nb, int E, float* __restrict__ stats) {
+  __shared__ double s_red[256];
+  const int e = blockIdx.x;
+  double acc = 0.0;
+  for (int b = threadIdx.x; b < nb; b += 256) acc += partials[static_cast<size_t>(b) * (E + 1) + e];
+  s_red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
+    __syncthreads();
   }
+  if (threadIdx.x == 0) stats[e] = static_cast<float>(s_red[0]);
 }
 
 // losses[0] = alpha*E*sum_i (counts_i/(T*k)) * (stats_i/T); losses[1] = beta*stats[E]/T.
@@ -183,12 +201,12 @@ __global__ void aux_loss_kernel(const float* __restrict__ stats, const int32_t* 
 }
 
 template <int JM>
-int launch_jm(const float* logits, int T, int E, int k, int gate_mode, int32_t* idx, float* gate,
-              float* partials, DeviceError* err, cudaStream_t stream) {
-  const int nb = route_blocks(T);
-  const size_t smem = static_cast<size_t>(kRouteWarps) * (E + 1) * sizeof(float);
-  route_topk_kernel<JM><<<nb, kRouteThreads, smem, stream>>>(logits, T, E, k, gate_mode, idx,
-                                                              gate, partials, err);
+int launch_jm(const RouteArgs& a, cudaStream_t stream) {
+  const int nb = route_blocks(a.T);
+  const size_t smem = static_cast<size_t>(kRouteWarps) * (a.E + 1) * sizeof(float);
+  route_topk_kernel<JM><<<nb, kRouteThreads, smem, stream>>>(
+      a.logits, a.nsplit, a.split_stride, a.bias, a.logits_out, a.T, a.E, a.k, a.gate_mode,
+      a.topk_idx, a.topk_gate, a.partials, a.err);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -201,22 +219,19 @@ int route_blocks(int T) {
   return std::max(1, std::min(nb, 1024));
 }
 
-int launch_route_topk(const float* logits, int T, int E, int k, int gate_mode, int32_t* topk_idx,
-                      float* topk_gate, float* partials, DeviceError* err, cudaStream_t stream) {
-  const int jm = (E + 31) / 32;
-  if (jm <= 1) return launch_jm<1>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
-  if (jm <= 2) return launch_jm<2>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
-  if (jm <= 4) return launch_jm<4>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
-  if (jm <= 8) return launch_jm<8>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
-  if (jm <= 16) return launch_jm<16>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
-  return launch_jm<32>(logits, T, E, k, gate_mode, topk_idx, topk_gate, partials, err, stream);
+int launch_route_topk(const RouteArgs& a, cudaStream_t stream) {
+  const int jm = (a.E + 31) / 32;
+  if (jm <= 1) return launch_jm<1>(a, stream);
+  if (jm <= 2) return launch_jm<2>(a, stream);
+  if (jm <= 4) return launch_jm<4>(a, stream);
+  if (jm <= 8) return launch_jm<8>(a, stream);
+  if (jm <= 16) return launch_jm<16>(a, stream);
+  return launch_jm<32>(a, stream);
 }
 
 int launch_stats_reduce(const float* partials, int nblocks, int E, float* stats,
                         cudaStream_t stream) {
-  const int threads = 256;
-  const int blocks = (E + 1 + threads - 1) / threads;
-  stats_reduce_kernel<<<blocks, threads, 0, stream>>>(partials, nblocks, E, stats);
+  stats_reduce_kernel<<<E + 1, 256, 0, stream>>>(partials, nblocks, E, stats);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

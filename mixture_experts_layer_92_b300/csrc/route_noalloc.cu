@@ -76,8 +76,17 @@ extern "C" int moe_route_topk_noalloc(const moe_shape* s, const float* logits_in
   float* partials = nullptr;
   const cudaError_t se = scratch_for_current_device(&partials);
   if (se != cudaSuccess) return set_error_detail(MOE_ERR_CUDA, cudaGetErrorString(se));
-  int r = launch_route_topk(logits_in, s->T, s->E, s->k, s->gate, topk_idx, topk_gate, partials,
-                            nullptr, st);
+  RouteArgs a{};
+  a.logits = logits_in;
+  a.nsplit = 1;
+  a.T = s->T;
+  a.E = s->E;
+  a.k = s->k;
+  a.gate_mode = s->gate;
+  a.topk_idx = topk_idx;
+  a.topk_gate = topk_gate;
+  a.partials = partials;
+  int r = launch_route_topk(a, st);
   if (r != MOE_OK) return set_error_detail(r, "gates/top-k launch failed");
   if (stats != nullptr) r = launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st);
   if (r != MOE_OK) return set_error_detail(r, "statistics launch failed");

@@ -79,10 +79,15 @@ struct Tile {
   int n_blk;
   int row0;     // first row of A / output
   int rows;     // valid rows in this tile (<= BM)
+  int split;    // split-K index (router mode), else 0
+  int kb0;      // first k-block (of BK) of this tile's K range
+  int nk;       // k-blocks in the range
 };
 
+// Tile order inside a routed group: split fastest, then row tile, then column tile, so the
+// CTAs that run at the same time share the group's weight tiles through L2.
 __device__ __forceinline__ Tile decode_tile(int tile, const int* s_off, const int* s_pre, int G,
-                                            int nt_routed, int m_shared, int nt_shared) {
+                                            int nt_routed, int splits, const TcArgs& a) {
   Tile t;
   const int routed_total = s_pre[G];
   if (tile < routed_total) {
@@ -93,24 +98,37 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* s_off, const in
     }
     const int g = lo;
     const int local = tile - s_pre[g];
-    const int mt = (s_pre[g + 1] - s_pre[g]) / nt_routed;
-    const int n = local / mt, m = local - n * mt;
+    const int mt = (s_pre[g + 1] - s_pre[g]) / (nt_routed * splits);
+    const int sp = local % splits;
+    const int rest = local / splits;
+    const int n = rest / mt, m = rest - n * mt;
+    const int nk_all = (a.k_routed + BK - 1) / BK;
     t.shared = 0;
     t.group = g;
     t.n_blk = n;
     t.row0 = s_off[g] + m * BM;
     t.rows = min(BM, s_off[g + 1] - t.row0);
+    t.split = sp;
+    if (splits > 1) {
+      t.kb0 = sp * a.kb_per_split;
+      t.nk = min(nk_all - t.kb0, a.kb_per_split);
+    } else {
+      t.kb0 = 0;
+      t.nk = nk_all;
+    }
   } else {
     const int local = tile - routed_total;
-    const int mt = (m_shared + BM - 1) / BM;
+    const int mt = (a.m_shared + BM - 1) / BM;
     const int n = local / mt, m = local - n * mt;
     t.shared = 1;
     t.group = 0;
     t.n_blk = n;
     t.row0 = m * BM;
-    t.rows = min(BM, m_shared - t.row0);
+    t.rows = min(BM, a.m_shared - t.row0);
+    t.split = 0;
+    t.kb0 = 0;
+    t.nk = (a.k_shared + BK - 1) / BK;
   }
-  (void)nt_shared;
   return t;
 }
 
@@ -160,7 +178,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   if (warp == 2) {
     // s_off[g] = first row of group g; s_pre[g] = first tile of group g (exclusive scan).
-    const int nt = (args.n_routed + C::BN_OUT - 1) / C::BN_OUT;
+    const int nt = (args.n_routed + C::BN_OUT - 1) / C::BN_OUT * (MODE == TC_F32OUT ? args.splits : 1);
     int carry = 0;
     for (int base = 0; base < G; base += 32) {
       const int g = base + lane;
@@ -194,6 +212,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const uint32_t tmem_base = *tmem_slot;
 
   const int nt_routed = (args.n_routed + C::BN_OUT - 1) / C::BN_OUT;
+  const int splits = (MODE == TC_F32OUT) ? args.splits : 1;
   const int nt_shared = args.has_shared ? (args.n_shared + C::BN_OUT - 1) / C::BN_OUT : 0;
   const int mt_shared = args.has_shared ? (args.m_shared + BM - 1) / BM : 0;
   const int total = s_pre[G] + mt_shared * nt_shared;
@@ -213,14 +232,12 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, args.m_shared, nt_shared);
+        const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, splits, args);
         const CUtensorMap* mA = t.shared ? &tmAs : &tmA;
         const CUtensorMap* mB0 = t.shared ? &tmB0s : &tmB0;
         const CUtensorMap* mB1 = t.shared ? &tmB1s : &tmB1;
-        const int K = t.shared ? args.k_shared : args.k_routed;
-        const int nk = (K + BK - 1) / BK;
         bool ok = true;
-        for (int kb = 0; kb < nk; ++kb) {
+        for (int kb = t.kb0; kb < t.kb0 + t.nk; ++kb) {
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, err,
                                  SITE_GEMM_WAIT_EMPTY)) {
             ok = false;
@@ -260,9 +277,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int it = 0;
       bool ok = true;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-        const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, args.m_shared, nt_shared);
-        const int K = t.shared ? args.k_shared : args.k_routed;
-        const int nk = (K + BK - 1) / BK;
+        const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, splits, args);
+        const int nk = t.nk;
         const int acc = it & 1;
         const uint32_t acc_phase = (it >> 1) & 1;
         if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1, abort_flag, err,
@@ -307,7 +323,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                              SITE_GEMM_WAIT_TMEM_FULL))
         break;
       tc_fence_after();
-      const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, args.m_shared, nt_shared);
+      const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, splits, args);
       const bool rvalid = r_local < t.rows;
       const long long row = static_cast<long long>(t.row0) + r_local;
       const int N = t.shared ? args.n_shared : args.n_routed;
@@ -369,7 +385,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           }
         }
       } else {  // TC_F32OUT
-        float* out = reinterpret_cast<float*>(args.out_routed);
+        float* out = reinterpret_cast<float*>(args.out_routed) + t.split * args.split_stride;
 #pragma unroll 1
         for (int c = 0; c < BN / 16; ++c) {
           uint32_t v[16];
