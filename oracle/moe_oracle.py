@@ -23,7 +23,8 @@ Readings where the pages are silent or disagree (also listed in the design doc):
   a = t*k + slot), drops the rest, and gates are not renormalised after a drop;
 * f_i = (assignments routed to i before the drop) / (T*k); P_i = mean softmax-over-all
   probability; L_aux = alpha*E*sum_i f_i*P_i; L_z = beta*mean_t(logsumexp(l_t)^2);
-* capacity C = ceil(cf*T*k/E), computed in fp64; "no drop" is C = T.
+* capacity C = ceil(cf*T*k/E), computed in fp64; "no drop" is C = T;
+* an empty batch (T = 0) has both losses 0 (f and P are undefined there).
 
 Every function here is pinned by a ``-m "not gpu"`` test against closed forms, the
 pages' worked example, or brute force; none is "parity unpinned".
@@ -221,6 +222,8 @@ def aux_loss(logits, idx, alpha: float) -> float:
     of the softmax-over-all probability of expert i."""
     l = _f64(logits)
     E = l.shape[1]
+    if l.shape[0] == 0:          # no tokens: f and P are undefined; reported as 0
+        return 0.0
     f = load_fractions(idx, E)
     P = softmax_all(l).mean(axis=0)
     return float(alpha * E * np.dot(f, P))
@@ -228,6 +231,8 @@ def aux_loss(logits, idx, alpha: float) -> float:
 
 def z_loss(logits, beta: float) -> float:
     """Router z-loss beta * mean_t(logsumexp(l_t)^2) (ST-MoE form)."""
+    if _f64(logits).shape[0] == 0:   # no tokens: reported as 0
+        return 0.0
     lse = logsumexp(logits)
     return float(beta * np.mean(lse * lse))
 

@@ -206,6 +206,12 @@ def test_aux_loss_collapse_closed_form():
     assert O.aux_loss(l, idx, 0.01) == pytest.approx(0.01 * E * P0, rel=1e-12)
 
 
+def test_losses_of_an_empty_batch_are_zero():
+    l = np.zeros((0, 8))
+    idx = np.zeros((0, 2), dtype=np.int64)
+    assert O.aux_loss(l, idx, 0.01) == 0.0 and O.z_loss(l, 1e-3) == 0.0
+
+
 def test_z_loss_closed_forms():
     """Zero logits: beta*(ln E)^2. Mixed rows: the mean of squares, not the square of
     the mean. Large constant logits do not overflow."""
