@@ -58,6 +58,44 @@ class MoELayer:
                     dropped=self.dropped, losses=self.losses, stream=stream, events=events)
         return y
 
+    def forward_host_stream(self, x_hosts, y_hosts):
+        """End-to-end layer over a sequence of host batches (pinned memory), pipelined.
+
+        Batch i's x is copied to the device on one stream, the layer runs on the current
+        stream, and y is copied back on a third; two device buffer pairs let the upload of
+        batch i+1 and the download of batch i-1 overlap the layer on batch i. Every batch
+        still moves its own x in and its own y out. Returns after queuing all work."""
+        comp = torch.cuda.current_stream(self.device)
+        if not hasattr(self, "_pipe"):
+            self._pipe = dict(h2d=torch.cuda.Stream(self.device), d2h=torch.cuda.Stream(self.device),
+                              xbuf=[None, None], ybuf=[None, None],
+                              h2d_done=[torch.cuda.Event(), torch.cuda.Event()],
+                              fwd_done=[torch.cuda.Event(), torch.cuda.Event()],
+                              d2h_done=[torch.cuda.Event(), torch.cuda.Event()])
+        p = self._pipe
+        for i, (xh, yh) in enumerate(zip(x_hosts, y_hosts)):
+            b = i % 2
+            if p["xbuf"][b] is None or p["xbuf"][b].shape[0] < xh.shape[0]:
+                p["xbuf"][b] = torch.empty(xh.shape, dtype=xh.dtype, device=self.device)
+                p["ybuf"][b] = torch.empty(xh.shape, dtype=xh.dtype, device=self.device)
+            xd, yd = p["xbuf"][b][:xh.shape[0]], p["ybuf"][b][:xh.shape[0]]
+            if i >= 2:
+                p["h2d"].wait_event(p["fwd_done"][b])      # x buffer b free
+            with torch.cuda.stream(p["h2d"]):
+                xd.copy_(xh, non_blocking=True)
+                p["h2d_done"][b].record(p["h2d"])
+            comp.wait_event(p["h2d_done"][b])
+            if i >= 2:
+                comp.wait_event(p["d2h_done"][b])          # y buffer b free
+            self.forward(xd, yd, stream=comp)
+            p["fwd_done"][b].record(comp)
+            p["d2h"].wait_event(p["fwd_done"][b])
+            with torch.cuda.stream(p["d2h"]):
+                yh.copy_(yd, non_blocking=True)
+                p["d2h_done"][b].record(p["d2h"])
+        comp.wait_stream(p["d2h"])
+        return y_hosts
+
     def forward_host(self, x_host: torch.Tensor, x_dev: torch.Tensor, y_dev: torch.Tensor,
                      y_host: torch.Tensor, losses_host: Optional[torch.Tensor] = None):
         """End-to-end call from host memory: copy x (pinned) to the device, run the layer,

@@ -8,7 +8,7 @@
 #include <cudaTypedefs.h>
 #include <stdint.h>
 
-#include "../../include/moe.h"
+#include "moe.h"  // include/ is on the include path
 
 namespace moe {
 
@@ -77,6 +77,10 @@ __device__ __forceinline__ float warp_max(float v) {
 }
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
+
+// silu with CUDA's fast exponential and an IEEE reciprocal, for results rounded to bf16:
+// z * 1/(1 + e^-z); e^-z = inf for very negative z gives 0.
+__device__ __forceinline__ float silu_fast(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

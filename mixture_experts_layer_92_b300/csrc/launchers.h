@@ -4,7 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/moe.h"
+#include "moe.h"  // include/ is on the include path
 
 namespace moe {
 
@@ -53,8 +53,8 @@ struct TcProblem {
   int num_sms;
 };
 
-int launch_tc_gemm(int mode, int bn, const TcProblem& p, cudaStream_t stream);
-int tc_smem_bytes(int mode, int bn, int groups);
+// mt: 128-row tiles per CTA tile (1, or 2 for TC_SWIGLU / TC_SCALE with BN = 256).
+int launch_tc_gemm(int mode, int bn, int mt, const TcProblem& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- CUDA-core fp32 path
 struct SimtArgs {

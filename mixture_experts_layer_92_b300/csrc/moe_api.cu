@@ -227,7 +227,7 @@ int run_router(const moe_shape* s, const void* x, const void* wr, float* logits,
   p.b_groups = 1;
   p.max_tiles = static_cast<long long>((s->T + 127) / 128) * ((s->E + bn - 1) / bn) * sp.splits;
   p.num_sms = num_sms();
-  LAUNCH(launch_tc_gemm(TC_F32OUT, bn, p, st), "router GEMM (tcgen05)");
+  LAUNCH(launch_tc_gemm(TC_F32OUT, bn, 1, p, st), "router GEMM (tcgen05)");
   return MOE_OK;
 }
 
@@ -331,10 +331,15 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     return MOE_OK;
   }
 
-  // bf16: tcgen05 grouped GEMMs, routed experts and the shared expert in one launch each
+  // bf16: tcgen05 grouped GEMMs, routed experts and the shared expert in one launch each.
+  // 256-row CTA tiles (one weight tile feeds two MMAs, but the accumulators fill TMEM, so the
+  // epilogue is not double-buffered) pay off only when the K loop is long against the
+  // epilogue: the down projection with d_ff >= 8192 and groups averaging >= 512 rows.
+  // Everything else runs 128-row tiles with double-buffered accumulators.
   const long long kept_max = std::min<long long>(A, static_cast<long long>(s->E) * max_group_rows);
-  const long long mt_routed = (kept_max + 127) / 128 + s->E;
-  const long long mt_shared = shared ? (s->T + 127) / 128 : 0;
+  const int mt_gateup = 1;
+  const int mt_down = (kept_max / s->E >= 512 && s->d_ff >= 8192) ? 2 : 1;
+  auto row_tiles = [&](int mt, long long rows) { return (rows + 128 * mt - 1) / (128 * mt); };
 
   rec(ev_first + 1);
   {
@@ -362,9 +367,10 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.b0_s = w1s;
     p.b1_s = w3s;
     p.b_rows_s = s->d_ff_shared;
-    p.max_tiles = mt_routed * ((s->d_ff + 127) / 128) + mt_shared * ((s->d_ff_shared + 127) / 128);
+    p.max_tiles = (row_tiles(mt_gateup, kept_max) + s->E) * ((s->d_ff + 127) / 128) +
+                  (shared ? row_tiles(mt_gateup, s->T) * ((s->d_ff_shared + 127) / 128) : 0);
     p.num_sms = sms;
-    LAUNCH(launch_tc_gemm(TC_SWIGLU, 256, p, st), "gate/up GEMM (tcgen05)");
+    LAUNCH(launch_tc_gemm(TC_SWIGLU, 256, mt_gateup, p, st), "gate/up GEMM (tcgen05)");
   }
   rec(ev_first + 2);
   {
@@ -393,9 +399,10 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.b0_s = w2s;
     p.b_rows_s = s->d;
     const int bn = 256;
-    p.max_tiles = (mt_routed + mt_shared) * ((s->d + bn - 1) / bn);
+    p.max_tiles = (row_tiles(mt_down, kept_max) + s->E + (shared ? row_tiles(mt_down, s->T) : 0)) *
+                  ((s->d + bn - 1) / bn);
     p.num_sms = sms;
-    LAUNCH(launch_tc_gemm(TC_SCALE, bn, p, st), "down GEMM (tcgen05)");
+    LAUNCH(launch_tc_gemm(TC_SCALE, bn, mt_down, p, st), "down GEMM (tcgen05)");
   }
   return MOE_OK;
 }

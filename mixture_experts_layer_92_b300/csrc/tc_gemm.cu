@@ -14,16 +14,24 @@
 //               H = silu(gate) * up as bf16 (BN/2 output columns per tile).
 //   TC_SCALE  : down projection; the epilogue writes g_r * acc as bf16, with the gate
 //               g_r = topk_gate[perm[r]] of the row's assignment (1 for the shared expert).
-//   TC_F32OUT : router logits; the epilogue writes acc (+ bias) as fp32.
+//   TC_F32OUT : router logits (split-K planes); the epilogue writes acc as fp32.
 //
-// Roles (192 threads, one CTA per SM, persistent over tiles):
-//   warp 0 lane 0  TMA producer: A tile 128 x 64 and B tile BN x 64 (bf16, 128-byte swizzle)
-//                  into a STAGES-deep shared-memory ring;
-//   warp 1         allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16) into one of
-//                  two TMEM accumulators, so the epilogue of tile i overlaps the MMAs of i+1;
-//   warps 2..5     epilogue: tcgen05.ld (each warp reads its 32-lane quarter of TMEM),
-//                  element-wise math, predicated 16-byte global stores (rows past the
-//                  group's end are masked: A tiles may straddle two experts' rows).
+// A CTA tile is MT x 128 rows by BN columns. With MT = 2 the B tile loaded for a k-block
+// feeds two M=128 MMAs (rows r..r+127 and r+128..r+255), halving the weight bytes per FLOP
+// that cross L2 and shared memory, so the 3-stage ring covers more latency than the
+// 4-stage ring of MT = 1 (the kernel is bound by how many bytes it keeps in flight). The
+// last row tile of a group may have only its first half valid: then the second half is
+// neither loaded nor multiplied.
+//
+// Roles (one CTA per SM, persistent over tiles):
+//   warp 0 lane 0  TMA producer: A tiles 128 x 64 and a B tile BN x 64 (bf16, 128-byte
+//                  swizzle) into a STAGES-deep shared-memory ring;
+//   warp 1         allocates TMEM; lane 0 issues tcgen05.mma (M=128, N=BN, K=16). MT = 1
+//                  keeps two accumulators so the epilogue of tile i overlaps the MMAs of
+//                  i+1; MT = 2 uses all 512 columns for the two row halves;
+//   warps 2..      epilogue, 4 warps per row half: tcgen05.ld (each warp reads its 32-lane
+//                  quarter of TMEM), element-wise math, predicated 16-byte global stores
+//                  (rows past the group's end are masked: A tiles may straddle two experts).
 // Every mbarrier wait is bounded (common.cuh): on a timeout the kernel records
 // MOE_ERR_TIMEOUT in the workspace error word, drains its own copies and MMAs, frees TMEM
 // and returns.
@@ -37,7 +45,6 @@ namespace moe {
 
 namespace {
 
-constexpr int kThreads = 192;
 constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kMaxGroups = 1024;
@@ -48,15 +55,18 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, int MT>
 struct Cfg {
-  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int THREADS = 64 + 128 * MT;
+  static constexpr int EPI_WARPS = 4 * MT;
+  static constexpr int A_BYTES = BM * BK * 2;          // one 128-row A tile
   static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
   static constexpr int STAGES_RAW = (196 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int BN_OUT = (MODE == TC_SWIGLU) ? BN / 2 : BN;
-  static constexpr uint32_t TMEM_COLS = pow2_at_least(2 * BN);
+  static constexpr int NUM_ACC = (MT == 1) ? 2 : 1;    // accumulator sets (double buffering)
+  static constexpr uint32_t TMEM_COLS = pow2_at_least(NUM_ACC * MT * BN);
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int OFF_TILES = 0;
@@ -67,6 +77,7 @@ struct Cfg {
   static constexpr int smem_bytes(int groups) {
     return 1024 + OFF_TABLE + 2 * (groups + 1) * 4;
   }
+  static_assert(MT == 1 || MT == 2, "one or two 128-row tiles per CTA tile");
   static_assert(STAGES >= 2, "pipeline needs at least two stages");
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N % 16 == 0, 16..256");
   static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
@@ -78,7 +89,7 @@ struct Tile {
   int group;    // expert (routed) or 0
   int n_blk;
   int row0;     // first row of A / output
-  int rows;     // valid rows in this tile (<= BM)
+  int rows;     // valid rows in this tile (<= MT * BM)
   int split;    // split-K index (router mode), else 0
   int kb0;      // first k-block (of BK) of this tile's K range
   int nk;       // k-blocks in the range
@@ -86,6 +97,7 @@ struct Tile {
 
 // Tile order inside a routed group: split fastest, then row tile, then column tile, so the
 // CTAs that run at the same time share the group's weight tiles through L2.
+template <int TM>
 __device__ __forceinline__ Tile decode_tile(int tile, const int* s_off, const int* s_pre, int G,
                                             int nt_routed, int splits, const TcArgs& a) {
   Tile t;
@@ -106,8 +118,8 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* s_off, const in
     t.shared = 0;
     t.group = g;
     t.n_blk = n;
-    t.row0 = s_off[g] + m * BM;
-    t.rows = min(BM, s_off[g + 1] - t.row0);
+    t.row0 = s_off[g] + m * TM;
+    t.rows = min(TM, s_off[g + 1] - t.row0);
     t.split = sp;
     if (splits > 1) {
       t.kb0 = sp * a.kb_per_split;
@@ -118,13 +130,13 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* s_off, const in
     }
   } else {
     const int local = tile - routed_total;
-    const int mt = (a.m_shared + BM - 1) / BM;
+    const int mt = (a.m_shared + TM - 1) / TM;
     const int n = local / mt, m = local - n * mt;
     t.shared = 1;
     t.group = 0;
     t.n_blk = n;
-    t.row0 = m * BM;
-    t.rows = min(BM, a.m_shared - t.row0);
+    t.row0 = m * TM;
+    t.rows = min(TM, a.m_shared - t.row0);
     t.split = 0;
     t.kb0 = 0;
     t.nk = (a.k_shared + BK - 1) / BK;
@@ -132,15 +144,16 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* s_off, const in
   return t;
 }
 
-template <int MODE, int BN>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int MODE, int BN, int MT>
+__global__ void __launch_bounds__(Cfg<MODE, BN, MT>::THREADS, 1)
 tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1,
                        const __grid_constant__ CUtensorMap tmAs,
                        const __grid_constant__ CUtensorMap tmB0s,
                        const __grid_constant__ CUtensorMap tmB1s, const TcArgs args) {
-  using C = Cfg<MODE, BN>;
+  using C = Cfg<MODE, BN, MT>;
+  constexpr int TM = MT * BM;  // rows per CTA tile
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -169,7 +182,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
-      mbar_init(&tempty_bar[a], 4);
+      mbar_init(&tempty_bar[a], C::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
     *abort_flag = 0;
@@ -193,7 +206,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         s_off[g] = lo;
       }
-      int tiles_g = (g < G) ? ((hi - lo + BM - 1) / BM) * nt : 0;
+      const int tiles_g = (g < G) ? ((hi - lo + TM - 1) / TM) * nt : 0;
       int incl = tiles_g;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -214,7 +227,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   const int nt_routed = (args.n_routed + C::BN_OUT - 1) / C::BN_OUT;
   const int splits = (MODE == TC_F32OUT) ? args.splits : 1;
   const int nt_shared = args.has_shared ? (args.n_shared + C::BN_OUT - 1) / C::BN_OUT : 0;
-  const int mt_shared = args.has_shared ? (args.m_shared + BM - 1) / BM : 0;
+  const int mt_shared = args.has_shared ? (args.m_shared + TM - 1) / TM : 0;
   const int total = s_pre[G] + mt_shared * nt_shared;
 
   if (warp == 0) {
@@ -232,10 +245,12 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, splits, args);
+        const Tile t = decode_tile<TM>(tile, s_off, s_pre, G, nt_routed, splits, args);
         const CUtensorMap* mA = t.shared ? &tmAs : &tmA;
         const CUtensorMap* mB0 = t.shared ? &tmB0s : &tmB0;
         const CUtensorMap* mB1 = t.shared ? &tmB1s : &tmB1;
+        const bool two = (MT == 2) && (t.rows > BM);
+        const uint32_t bytes = C::B_BYTES + (two ? 2 : 1) * C::A_BYTES;
         bool ok = true;
         for (int kb = t.kb0; kb < t.kb0 + t.nk; ++kb) {
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, err,
@@ -244,9 +259,10 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             break;
           }
           uint8_t* sa = tiles + stage * C::STAGE_BYTES;
-          uint8_t* sb = sa + C::A_BYTES;
-          mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+          uint8_t* sb = sa + MT * C::A_BYTES;
+          mbar_arrive_expect_tx(&full_bar[stage], bytes);
           tma_load_2d(sa, mA, &full_bar[stage], kb * BK, t.row0);
+          if (two) tma_load_2d(sa + C::A_BYTES, mA, &full_bar[stage], kb * BK, t.row0 + BM);
           if (MODE == TC_SWIGLU) {
             tma_load_3d(sb, mB0, &full_bar[stage], kb * BK, t.n_blk * (BN / 2), t.group);
             tma_load_3d(sb + C::B_BYTES / 2, mB1, &full_bar[stage], kb * BK, t.n_blk * (BN / 2),
@@ -275,30 +291,35 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int stage = 0;
       uint32_t phase = 0;
       int it = 0;
-      bool ok = true;
+      bool ok = true, issued_any = false;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-        const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, splits, args);
-        const int nk = t.nk;
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
+        const Tile t = decode_tile<TM>(tile, s_off, s_pre, G, nt_routed, splits, args);
+        const bool two = (MT == 2) && (t.rows > BM);
+        const int acc = it % C::NUM_ACC;
+        const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
         if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1, abort_flag, err,
                                SITE_GEMM_WAIT_TMEM_EMPTY))
           break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-        for (int kb = 0; kb < nk; ++kb) {
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MT * BN);
+        for (int kb = 0; kb < t.nk; ++kb) {
           if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, err, SITE_GEMM_WAIT_FULL)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(tiles + stage * C::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + C::A_BYTES;
+          const uint32_t b_addr = a_addr + MT * C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), smem_desc_sw128(b_addr + kk * 32),
-                        C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32);
+            const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
+            tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), bdesc, C::IDESC, accumulate);
+            if (two)
+              tc_mma_bf16(d_tmem + BN, smem_desc_sw128(a_addr + C::A_BYTES + kk * 32), bdesc,
+                          C::IDESC, accumulate);
           }
+          issued_any = true;
           tc_commit(&empty_bar[stage]);
           if (++stage == C::STAGES) {
             stage = 0;
@@ -308,98 +329,104 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (ok) tc_commit(&tfull_bar[acc]);
       }
       // Drain: all MMAs issued by this thread have completed before TMEM is freed.
-      tc_commit(drain_bar);
-      mbar_wait_bounded(drain_bar, 0, nullptr, err, SITE_GEMM_WAIT_DRAIN);
+      if (issued_any) {
+        tc_commit(drain_bar);
+        mbar_wait_bounded(drain_bar, 0, nullptr, err, SITE_GEMM_WAIT_DRAIN);
+      }
     }
   } else {
-    // ================= epilogue (warps 2..5) =================
-    const int quarter = warp & 3;  // TMEM lanes this warp may read: 32*quarter .. +31
-    const int r_local = quarter * 32 + lane;
+    // ================= epilogue (warps 2 .. 2 + 4*MT - 1) =================
+    const int half = (warp - 2) >> 2;      // which 128-row half of the CTA tile
+    const int quarter = warp & 3;          // TMEM lanes this warp may read: 32*quarter .. +31
+    const int r_local = half * BM + quarter * 32 + lane;
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
+      const int acc = it % C::NUM_ACC;
+      const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, err,
                              SITE_GEMM_WAIT_TMEM_FULL))
         break;
       tc_fence_after();
-      const Tile t = decode_tile(tile, s_off, s_pre, G, nt_routed, splits, args);
-      const bool rvalid = r_local < t.rows;
-      const long long row = static_cast<long long>(t.row0) + r_local;
-      const int N = t.shared ? args.n_shared : args.n_routed;
-      const long long ldo = t.shared ? args.ldo_shared : args.ldo_routed;
-      const uint32_t tbase =
-          tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + static_cast<uint32_t>(acc * BN);
-      const int col_base = t.n_blk * C::BN_OUT;
+      const Tile t = decode_tile<TM>(tile, s_off, s_pre, G, nt_routed, splits, args);
+      // a half with no valid row was not multiplied this tile: skip it (warp-uniform)
+      if (half * BM < t.rows) {
+        const bool rvalid = r_local < t.rows;
+        const long long row = static_cast<long long>(t.row0) + r_local;
+        const int N = t.shared ? args.n_shared : args.n_routed;
+        const long long ldo = t.shared ? args.ldo_shared : args.ldo_routed;
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
+                               static_cast<uint32_t>((acc * MT + half) * BN);
+        const int col_base = t.n_blk * C::BN_OUT;
 
-      if (MODE == TC_SWIGLU) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.shared ? args.out_shared
-                                                                        : args.out_routed);
+        if (MODE == TC_SWIGLU) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.shared ? args.out_shared
+                                                                          : args.out_routed);
 #pragma unroll 1
-        for (int c = 0; c < C::BN_OUT / 32; ++c) {
-          uint32_t g[32], u[32];
-          tmem_ld_32cols(tbase + c * 32, g);
-          tmem_ld_32cols(tbase + BN / 2 + c * 32, u);
-          tmem_ld_wait();
-          if (rvalid) {
-            uint32_t packed[16];
+          for (int c = 0; c < C::BN_OUT / 32; ++c) {
+            uint32_t g[32], u[32];
+            tmem_ld_32cols(tbase + c * 32, g);
+            tmem_ld_32cols(tbase + BN / 2 + c * 32, u);
+            tmem_ld_wait();
+            if (rvalid) {
+              uint32_t packed[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const float h0 = silu_f(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
-              const float h1 =
-                  silu_f(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-              packed[i] = pack_bf16x2(h0, h1);
+              for (int i = 0; i < 16; ++i) {
+                const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
+                const float h1 =
+                    silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
+                packed[i] = pack_bf16x2(h0, h1);
+              }
+              const int col0 = col_base + c * 32;
+              __nv_bfloat16* dst = out + row * ldo + col0;
+#pragma unroll
+              for (int q = 0; q < 4; ++q)
+                if (col0 + q * 8 < N)
+                  *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
+                      packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
             }
-            const int col0 = col_base + c * 32;
-            __nv_bfloat16* dst = out + row * ldo + col0;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (col0 + q * 8 < N)
-                *reinterpret_cast<uint4*>(dst + q * 8) =
-                    make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
           }
-        }
-      } else if (MODE == TC_SCALE) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.shared ? args.out_shared
-                                                                        : args.out_routed);
-        float gscale = 1.0f;
-        if (rvalid && !t.shared && args.gate != nullptr) gscale = args.gate[args.perm[row]];
+        } else if (MODE == TC_SCALE) {
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.shared ? args.out_shared
+                                                                          : args.out_routed);
+          float gscale = 1.0f;
+          if (rvalid && !t.shared && args.gate != nullptr) gscale = args.gate[args.perm[row]];
 #pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld_32cols(tbase + c * 32, v);
-          tmem_ld_wait();
-          if (rvalid) {
-            uint32_t packed[16];
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t v[32];
+            tmem_ld_32cols(tbase + c * 32, v);
+            tmem_ld_wait();
+            if (rvalid) {
+              uint32_t packed[16];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
-              packed[i] = pack_bf16x2(gscale * __uint_as_float(v[2 * i]),
-                                      gscale * __uint_as_float(v[2 * i + 1]));
-            const int col0 = col_base + c * 32;
-            __nv_bfloat16* dst = out + row * ldo + col0;
+              for (int i = 0; i < 16; ++i)
+                packed[i] = pack_bf16x2(gscale * __uint_as_float(v[2 * i]),
+                                        gscale * __uint_as_float(v[2 * i + 1]));
+              const int col0 = col_base + c * 32;
+              __nv_bfloat16* dst = out + row * ldo + col0;
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
-              if (col0 + q * 8 < N)
-                *reinterpret_cast<uint4*>(dst + q * 8) =
-                    make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+              for (int q = 0; q < 4; ++q)
+                if (col0 + q * 8 < N)
+                  *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
+                      packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+            }
           }
-        }
-      } else {  // TC_F32OUT
-        float* out = reinterpret_cast<float*>(args.out_routed) + t.split * args.split_stride;
+        } else {  // TC_F32OUT
+          float* out = reinterpret_cast<float*>(args.out_routed) + t.split * args.split_stride;
 #pragma unroll 1
-        for (int c = 0; c < BN / 16; ++c) {
-          uint32_t v[16];
-          tmem_ld_16cols(tbase + c * 16, v);
-          tmem_ld_wait();
-          if (rvalid) {
-            const int col0 = col_base + c * 16;
+          for (int c = 0; c < BN / 16; ++c) {
+            uint32_t v[16];
+            tmem_ld_16cols(tbase + c * 16, v);
+            tmem_ld_wait();
+            if (rvalid) {
+              const int col0 = col_base + c * 16;
 #pragma unroll
-            for (int i = 0; i < 16; ++i) {
-              const int col = col0 + i;
-              if (col < N) {
-                float val = __uint_as_float(v[i]);
-                if (args.bias != nullptr) val += args.bias[col];
-                out[row * ldo + col] = val;
+              for (int i = 0; i < 16; ++i) {
+                const int col = col0 + i;
+                if (col < N) {
+                  float val = __uint_as_float(v[i]);
+                  if (args.bias != nullptr) val += args.bias[col];
+                  out[row * ldo + col] = val;
+                }
               }
             }
           }
@@ -463,9 +490,9 @@ bool encode_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
          CUDA_SUCCESS;
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, int MT>
 int launch_impl(const TcProblem& p, cudaStream_t stream) {
-  using C = Cfg<MODE, BN>;
+  using C = Cfg<MODE, BN, MT>;
   if (!get_encoder()) return MOE_ERR_CUDA;
   const int groups = p.args.groups;
   if (groups < 1 || groups > kMaxGroups) return MOE_ERR_INVALID;
@@ -490,7 +517,7 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
   static bool attr_ok[64];
   if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   std::call_once(attr_once[dev], [&]() {
-    attr_ok[dev] = cudaFuncSetAttribute(tc_grouped_gemm_kernel<MODE, BN>,
+    attr_ok[dev] = cudaFuncSetAttribute(tc_grouped_gemm_kernel<MODE, BN, MT>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::smem_bytes(kMaxGroups)) == cudaSuccess;
   });
@@ -498,32 +525,24 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
 
   long long grid = std::min<long long>(p.max_tiles, p.num_sms);
   if (grid < 1) return MOE_OK;
-  tc_grouped_gemm_kernel<MODE, BN><<<static_cast<int>(grid), kThreads, smem, stream>>>(
+  tc_grouped_gemm_kernel<MODE, BN, MT><<<static_cast<int>(grid), C::THREADS, smem, stream>>>(
       mA, mB0, mB1, mAs, mB0s, mB1s, p.args);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
 
-int tc_smem_bytes(int mode, int bn, int groups) {
-  switch (mode * 1000 + bn) {
-    case TC_SWIGLU * 1000 + 256: return Cfg<TC_SWIGLU, 256>::smem_bytes(groups);
-    case TC_SCALE * 1000 + 256: return Cfg<TC_SCALE, 256>::smem_bytes(groups);
-    case TC_SCALE * 1000 + 128: return Cfg<TC_SCALE, 128>::smem_bytes(groups);
-    default: return Cfg<TC_F32OUT, 256>::smem_bytes(groups);
-  }
-}
-
-int launch_tc_gemm(int mode, int bn, const TcProblem& p, cudaStream_t stream) {
-  switch (mode * 1000 + bn) {
-    case TC_SWIGLU * 1000 + 256: return launch_impl<TC_SWIGLU, 256>(p, stream);
-    case TC_SCALE * 1000 + 256: return launch_impl<TC_SCALE, 256>(p, stream);
-    case TC_SCALE * 1000 + 128: return launch_impl<TC_SCALE, 128>(p, stream);
-    case TC_F32OUT * 1000 + 16: return launch_impl<TC_F32OUT, 16>(p, stream);
-    case TC_F32OUT * 1000 + 32: return launch_impl<TC_F32OUT, 32>(p, stream);
-    case TC_F32OUT * 1000 + 64: return launch_impl<TC_F32OUT, 64>(p, stream);
-    case TC_F32OUT * 1000 + 128: return launch_impl<TC_F32OUT, 128>(p, stream);
-    case TC_F32OUT * 1000 + 256: return launch_impl<TC_F32OUT, 256>(p, stream);
+int launch_tc_gemm(int mode, int bn, int mt, const TcProblem& p, cudaStream_t stream) {
+  switch (mode * 10000 + bn * 10 + mt) {
+    case TC_SWIGLU * 10000 + 2560 + 1: return launch_impl<TC_SWIGLU, 256, 1>(p, stream);
+    case TC_SWIGLU * 10000 + 2560 + 2: return launch_impl<TC_SWIGLU, 256, 2>(p, stream);
+    case TC_SCALE * 10000 + 2560 + 1: return launch_impl<TC_SCALE, 256, 1>(p, stream);
+    case TC_SCALE * 10000 + 2560 + 2: return launch_impl<TC_SCALE, 256, 2>(p, stream);
+    case TC_F32OUT * 10000 + 160 + 1: return launch_impl<TC_F32OUT, 16, 1>(p, stream);
+    case TC_F32OUT * 10000 + 320 + 1: return launch_impl<TC_F32OUT, 32, 1>(p, stream);
+    case TC_F32OUT * 10000 + 640 + 1: return launch_impl<TC_F32OUT, 64, 1>(p, stream);
+    case TC_F32OUT * 10000 + 1280 + 1: return launch_impl<TC_F32OUT, 128, 1>(p, stream);
+    case TC_F32OUT * 10000 + 2560 + 1: return launch_impl<TC_F32OUT, 256, 1>(p, stream);
     default: return MOE_ERR_UNSUPPORTED;
   }
 }

@@ -41,14 +41,16 @@ def test_router_tcgen05_logits():
         np.testing.assert_allclose(logits.cpu().numpy(), ref, rtol=1e-5, atol=2e-5)
 
 
-def grouped_check(T, d, E, k, F, Fs=0, cf=None, gate="softmax_topk", seed=0):
-    """moe_grouped_swiglu alone, on the oracle's own dispatch of random routing."""
+def grouped_check(T, d, E, k, F, Fs=0, cf=None, gate="softmax_topk", seed=0, idx=None):
+    """moe_grouped_swiglu alone, on the oracle's own dispatch of random routing (or of the
+    given expert indices [T, k])."""
     w = WORKLOADS["mixtral_prefill"].scaled(T=T, d=d, E=E, k=k, d_ff=F, d_ff_shared=Fs, cf=cf,
                                             gate=gate)
     inp = dev_inputs(w, seed=seed)
     C = capacity_of(w)
     l64 = np.random.default_rng(seed).normal(size=(T, E))
-    idx = O.select_topk(l64, k)
+    if idx is None:
+        idx = O.select_topk(l64, k)
     g = O.gates(l64, idx, gate)
     disp = O.dispatch(idx, E, C)
     s = L.make_shape(T, d, E, k, F, gate=gate, dtype=torch.bfloat16, capacity=C, d_ff_shared=Fs)
@@ -93,6 +95,17 @@ def test_grouped_swiglu_tcgen05(T, d, E, k, F):
     grouped_check(T, d, E, k, F)
 
 
+def test_grouped_swiglu_tcgen05_256_row_tiles():
+    """The down projection runs 256-row CTA tiles (two MMAs per weight tile) when d_ff >= 8192
+    and experts average >= 512 rows. Loads 612 / 1224 / 642 rows: last tiles with the second
+    half empty (100 rows), partly valid (200 rows) and nearly empty (130 rows: 2 rows in the
+    second half)."""
+    counts = [612, 1224, 642]
+    idx = np.concatenate([np.full(c, e) for e, c in enumerate(counts)])
+    idx = idx[np.random.default_rng(5).permutation(idx.shape[0])][:, None]
+    grouped_check(int(idx.shape[0]), 256, 3, 1, 8192, idx=idx, seed=5)
+
+
 def test_grouped_swiglu_tcgen05_capacity_and_shared():
     grouped_check(500, 256, 8, 2, 256, Fs=128, cf=0.75, gate="sigmoid_topk", seed=3)
 
@@ -120,13 +133,15 @@ def layer_check(w, seed=0, sample=None):
     return g, disp, len(bad)
 
 
-@pytest.mark.parametrize("name", ["mixtral_prefill", "switch_top1", "deepseek_fine",
-                                  "mixtral_decode"])
+@pytest.mark.parametrize("name", ["mixtral_prefill", "mixtral_prefill_256", "switch_top1",
+                                  "deepseek_fine", "mixtral_decode"])
 def test_bf16_layer_scaled_workloads(name):
     """Each bf16 workload's recipe (gate mode, k, bias, capacity, shared expert) at reduced
-    sizes that still span several tiles and ragged tails."""
-    base = WORKLOADS[name]
+    sizes that still span several tiles and ragged tails (mixtral_prefill_256: ~512 rows per
+    expert, so the expert GEMMs run 256-row CTA tiles)."""
+    base = WORKLOADS[name.replace("_256", "")]
     small = dict(mixtral_prefill=dict(T=600, d=512, d_ff=768),
+                 mixtral_prefill_256=dict(T=2048, d=512, d_ff=768),
                  switch_top1=dict(T=1500, d=256, E=32, d_ff=384),
                  deepseek_fine=dict(T=400, d=384, E=24, k=4, d_ff=256, d_ff_shared=256),
                  mixtral_decode=dict(T=32, d=512, d_ff=1024))[name]
@@ -142,3 +157,22 @@ def test_bf16_deterministic():
     b = gpu_forward(w, inp)
     assert torch.equal(a["y"], b["y"]) and torch.equal(a["losses"], b["losses"])
     assert torch.equal(a["idx"], b["idx"]) and torch.equal(a["stats"], b["stats"])
+
+
+def test_forward_host_stream_matches_device_forward():
+    """MoELayer.forward_host_stream (pipelined host->device->host over several batches)
+    returns, batch by batch, exactly what the device-resident forward returns."""
+    import mixture_experts_layer_92_b300 as moe
+    w = WORKLOADS["mixtral_prefill"].scaled(T=256, d=256, E=8, k=2, d_ff=384)
+    inp = dev_inputs(w)
+    layer = moe.MoELayer(inp["w_router"], inp["w1"], inp["w3"], inp["w2"], k=w.k, gate=w.gate,
+                         max_tokens=w.T)
+    xs = [torch.randn(w.T, w.d, generator=torch.Generator().manual_seed(i)).to(torch.bfloat16)
+          .pin_memory() for i in range(5)]
+    ys = [torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory() for _ in range(5)]
+    layer.forward_host_stream(xs, ys)
+    torch.cuda.synchronize()
+    for xh, yh in zip(xs, ys):
+        ref = layer.forward(xh.to(DEV))
+        torch.cuda.synchronize()
+        assert torch.equal(yh, ref.cpu())
