@@ -238,6 +238,43 @@ def z_loss(logits, beta: float) -> float:
 
 
 # ---------------------------------------------------------------------------------------
+# Auxiliary-loss-free balancing (DeepSeek-V3).  [Tirogla] "Implementation notes": a
+# per-expert bias is added to the scores used for top-k selection only (not to the gates)
+# and nudged up or down after each step by load. [DL-S077] section 8.2: up when an expert
+# is under-used, down when over-used. Readings: the score is the gate affinity (sigmoid of
+# the logit for sigmoid gating, the softmax-over-all probability otherwise); the nudge is a
+# fixed step gamma by the sign of (mean load - load), loads counted before any drop.
+# ---------------------------------------------------------------------------------------
+def affinity(logits, mode: str) -> np.ndarray:
+    """Per-expert routing score the gates are built from: sigmoid(l) or softmax_all(l)."""
+    l = _f64(logits)
+    if mode == "sigmoid_topk":
+        return 1.0 / (1.0 + np.exp(-l))
+    return softmax_all(l)
+
+
+def select_topk_biased(logits, k: int, mode: str, select_bias) -> np.ndarray:
+    """Top-k of affinity + bias per token (descending, ties -> lower index)."""
+    key = affinity(logits, mode) + _f64(select_bias)[None, :]
+    order = np.argsort(-key, axis=1, kind="stable")
+    return order[:, :k].astype(np.int64)
+
+
+def update_select_bias(select_bias, counts, T: int, k: int, gamma: float) -> np.ndarray:
+    """b_i + gamma if expert i received fewer than T*k/E assignments, - gamma if more,
+    unchanged at exactly the mean; evaluated in fp32 like the bias it updates."""
+    b = np.asarray(select_bias, dtype=np.float32).copy()
+    n = np.asarray(counts, dtype=np.int64)
+    E = b.shape[0]
+    g = np.float32(gamma)
+    under = n * E < T * k           # n_i < T*k/E without rounding
+    over = n * E > T * k
+    b[under] = b[under] + g
+    b[over] = b[over] - g
+    return b
+
+
+# ---------------------------------------------------------------------------------------
 # The whole layer, for inputs small enough to hold in fp64.
 # ---------------------------------------------------------------------------------------
 def route(logits, k: int, mode: str) -> dict:
@@ -248,18 +285,24 @@ def route(logits, k: int, mode: str) -> dict:
 
 def forward(x, w_router, w1, w3, w2, *, k: int, mode: str, C: int, router_bias=None,
             w1s=None, w3s=None, w2s=None, alpha: float = 0.01, beta: float = 1e-3,
-            idx_override=None) -> dict:
+            idx_override=None, select_bias=None) -> dict:
     """Full forward of one MoE layer in fp64.
 
     ``idx_override`` replaces the selected experts (the gates are then taken for those
     experts from the same logits); it lets a test recompute steps 3-6 on another
-    implementation's routing decisions.
+    implementation's routing decisions. ``select_bias`` [E] selects on affinity + bias
+    (auxiliary-loss-free balancing); gates never include it.
     Returns y, logits, idx, gate, the dispatch dict, l_aux, l_z."""
     x = _f64(x)
     T = x.shape[0]
     E = np.asarray(w_router).shape[0]
     logits = router_logits(x, w_router, router_bias)
-    idx = select_topk(logits, k) if idx_override is None else np.asarray(idx_override, dtype=np.int64)
+    if idx_override is not None:
+        idx = np.asarray(idx_override, dtype=np.int64)
+    elif select_bias is not None:
+        idx = select_topk_biased(logits, k, mode, select_bias)
+    else:
+        idx = select_topk(logits, k)
     g = gates(logits, idx, mode)
     disp = dispatch(idx, E, C)
     rows = expert_outputs(x, disp, k, w1, w3, w2)

@@ -337,3 +337,54 @@ def test_near_tie_tokens():
     l = np.array([[3.0, 1.0, 0.9995, 0.0], [3.0, 1.0, 0.5, 0.0], [1.0, 1.0, 1.0, 1.0]])
     assert O.near_tie_tokens(l, 2).tolist() == [0, 2]
     assert O.near_tie_tokens(l, 4).tolist() == []
+
+
+# ---------------------------------------------------------------- aux-loss-free balancing
+@pytest.mark.parametrize("mode", ["softmax_all", "softmax_topk", "sigmoid_topk"])
+def test_zero_selection_bias_is_plain_top_k(mode):
+    """Affinity is monotone in the logit, so a zero bias selects exactly the top-k logits."""
+    l = np.random.default_rng(21).normal(size=(60, 16)) * 2
+    for k in (1, 3, 8):
+        np.testing.assert_array_equal(O.select_topk_biased(l, k, mode, np.zeros(16)),
+                                      O.select_topk(l, k))
+
+
+def test_large_selection_bias_forces_expert_but_not_the_gate():
+    """A bias of +10 on expert 5 puts it in every token's top-k (affinities are <= 1), while
+    its gate is still sigma(l_5) / sum over the selected of sigma(l)."""
+    l = np.random.default_rng(22).normal(size=(30, 8))
+    b = np.zeros(8)
+    b[5] = 10.0
+    idx = O.select_topk_biased(l, 2, "sigmoid_topk", b)
+    assert np.all(idx[:, 0] == 5)
+    g = O.gates(l, idx, "sigmoid_topk")
+    s = 1 / (1 + np.exp(-np.take_along_axis(l, idx, 1)))
+    np.testing.assert_allclose(g, s / s.sum(1, keepdims=True), rtol=1e-14)
+    # and the other slot is the best remaining expert by plain sigmoid (i.e. by logit)
+    rest = np.where(np.arange(8)[None, :] == 5, -np.inf, l)
+    np.testing.assert_array_equal(idx[:, 1], np.argmax(rest, axis=1))
+
+
+def test_selection_bias_update_closed_form():
+    """Mean load T*k/E = 6: loads 11, 6, 3, 4 -> -gamma, 0, +gamma, +gamma."""
+    b = np.array([0.5, -0.25, 0.0, 1.0], dtype=np.float32)
+    nb = O.update_select_bias(b, [11, 6, 3, 4], T=12, k=2, gamma=0.125)
+    np.testing.assert_array_equal(nb, np.array([0.375, -0.25, 0.125, 1.125], dtype=np.float32))
+
+
+def test_selection_bias_loop_balances_a_skewed_router():
+    """Routing on a strongly skewed router (Zipf log-popularity added to the logits) with
+    the bias nudged after every step drives the per-expert load towards uniform."""
+    rng = np.random.default_rng(23)
+    T, E, k = 512, 16, 2
+    zipf = np.log(np.arange(1, E + 1) ** -1.2 / np.sum(np.arange(1, E + 1) ** -1.2))
+    b = np.zeros(E, dtype=np.float32)
+    spread = []
+    for step in range(200):
+        l = rng.normal(size=(T, E)) + zipf
+        idx = O.select_topk_biased(l, k, "sigmoid_topk", b)
+        n = np.bincount(idx.reshape(-1), minlength=E)
+        spread.append(n.max() / (T * k / E))
+        b = O.update_select_bias(b, n, T, k, 0.01)
+    assert spread[0] > 3.0                      # starts badly unbalanced
+    assert np.mean(spread[-20:]) < 1.5          # ends close to uniform
