@@ -269,7 +269,8 @@ def run_ours(args, w, rank, world, local_rank):
     C = capacity(w)
     layer = moe.MoELayer(inp["w_router"], inp["w1"], inp["w3"], inp["w2"], k=w.k, gate=w.gate,
                          capacity=C, router_bias=inp["router_bias"], w1s=inp["w1s"],
-                         w3s=inp["w3s"], w2s=inp["w2s"], alpha=w.alpha, beta=w.beta, max_tokens=w.T)
+                         w3s=inp["w3s"], w2s=inp["w2s"], alpha=w.alpha, beta=w.beta, max_tokens=w.T,
+                         balance_gamma=args.balance_gamma)
     x = inp["x"]
     y = torch.empty_like(x)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -285,9 +286,12 @@ def run_ours(args, w, rank, world, local_rank):
     visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
     sampler = ClockSampler(visible[local_rank] if local_rank < len(visible) else local_rank)
     sampler.start()
-    for _ in range(args.warmup):
+    spread = []
+    for i in range(args.warmup):
         flush.zero_()
         layer.forward(x, y)
+        if i == 0:
+            spread.append(float(layer.counts.max().item()) / (w.T * w.k / w.E))
     barrier()
     t_wall = time.perf_counter()
     for i in range(args.steps):
@@ -324,6 +328,7 @@ def run_ours(args, w, rank, world, local_rank):
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
     total_ms, e2e_ms = t.tolist()
     counts = layer.counts.cpu().numpy()
+    spread.append(float(counts.max()) / (w.T * w.k / w.E))
     R = int(np.minimum(counts, C).sum())
     touched = int((counts > 0).sum())
     if rank != 0:
@@ -374,9 +379,15 @@ def run_ours(args, w, rank, world, local_rank):
                  d2h_bytes_per_step=w.T * w.d * es,
                  note="MoELayer.forward_host_stream: per step, x (pinned) -> device, layer, y -> "
                       "host; uploads/downloads of neighbouring steps overlap the layer"),
-        gpu_launches=launches_per_forward(w) * args.steps,
+        gpu_launches=(launches_per_forward(w) + (1 if args.balance_gamma is not None else 0))
+        * args.steps,
         clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"], reasons=clk["reasons"],
                     samples=clk["samples"]))
+    if args.balance_gamma is not None:
+        line["balance"] = dict(gamma=args.balance_gamma, load_spread_first_step=spread[0],
+                               load_spread_last_step=spread[-1],
+                               note="max expert load / mean load (pre-drop); the selection "
+                                    "bias is nudged after every forward, warm-up included")
     print(json.dumps(line), flush=True)
     if dist is not None:
         dist.barrier()
@@ -392,12 +403,20 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--balance-gamma", type=float, default=None,
+                    help="auxiliary-loss-free balancing: nudge a selection bias by this step")
+    ap.add_argument("--zipf", type=float, default=None,
+                    help="add a Zipf(s) log-popularity bias to the router logits (skewed load)")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)          # timing rule: at least 3 warm-up steps
     rank = int(os.environ.get("RANK", "0"))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     w = WORKLOADS[args.workload]
+    if args.zipf is not None:
+        w = w.scaled(zipf_s=args.zipf, name=f"{w.name}+zipf{args.zipf}")
+    if args.balance_gamma is not None:
+        w = w.scaled(name=f"{w.name}+balanced")
     if args.impl == "reference":
         run_reference(args, w, rank)
         return

@@ -185,6 +185,39 @@ int moe_forward_events(const moe_shape* s, const void* x, const void* w_router,
                        void* y, int32_t* counts, int32_t* dropped, float* losses, void* ws,
                        size_t ws_bytes, void* stream, void* const* events, int n_events);
 
+/* Auxiliary-loss-free balancing (DeepSeek-V3) -- "Mixture of experts (MoE)", tirogla.com,
+ * Implementation notes: a per-expert bias is added to the scores used for top-k selection
+ * only (never to the gates) and nudged after each step by load; "DL S077 - Mixture of
+ * Experts (MoE) Intuition", section 8.2: up when under-used, down when over-used.
+ *
+ * moe_route_topk_balanced: moe_route_topk, except that expert e is ranked by
+ *   affinity_e + select_bias[e], with affinity = sigmoid(l_e) for MOE_GATE_SIGMOID_TOPK and
+ *   the softmax-over-all probability otherwise (ties -> lower index). Gates, statistics and
+ *   logits are exactly those of moe_route_topk for the selected experts.
+ *   select_bias [E] fp32 (device), read only. */
+int moe_route_topk_balanced(const moe_shape* s, const void* x, const void* w_router,
+                            const float* router_bias, const float* logits_in,
+                            const float* select_bias, float* logits_out, int32_t* topk_idx,
+                            float* topk_gate, float* stats, void* ws, size_t ws_bytes,
+                            void* stream);
+
+/* The per-step nudge: select_bias[e] += gamma if counts[e] < T*k/E, -= gamma if
+ * counts[e] > T*k/E (compared exactly as counts[e]*E vs T*k), unchanged otherwise.
+ * counts [E] int32: pre-drop loads as written by moe_dispatch. gamma >= 0. In place, fp32. */
+int moe_update_select_bias(const moe_shape* s, const int32_t* counts, float* select_bias,
+                           float gamma, void* stream);
+
+/* moe_forward with auxiliary-loss-free balancing: routes with moe_route_topk_balanced's
+ * rule on select_bias [E] (device, fp32), runs the layer, then applies
+ * moe_update_select_bias with this step's counts, so the next call sees the nudged bias.
+ * events/n_events as in moe_forward_events, or NULL/0 (the bias update runs in stage 7). */
+int moe_forward_balanced(const moe_shape* s, const void* x, const void* w_router,
+                         const float* router_bias, const void* w1, const void* w3, const void* w2,
+                         const void* w1s, const void* w3s, const void* w2s, void* y,
+                         int32_t* counts, int32_t* dropped, float* losses, float* select_bias,
+                         float gamma, void* ws, size_t ws_bytes, void* stream,
+                         void* const* events, int n_events);
+
 /* moe_route_topk for precomputed logits, for callers that cannot allocate device memory.
  * (No counterpart in the pages: it is a deployment variant, not a step of the method.)
  * Some callers cannot hand the library a workspace: code running inside a host framework

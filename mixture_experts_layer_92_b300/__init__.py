@@ -14,8 +14,9 @@ import torch
 from . import _lib
 from ._lib import (MoeError, alloc_workspace, make_shape, moe_aux_loss, moe_capacity,  # noqa: F401
                    moe_check_shape, moe_clear_error, moe_combine, moe_dispatch, moe_forward,
-                   moe_get_error, moe_grouped_swiglu, moe_route_topk, moe_status_string,
-                   moe_workspace_size, NUM_STAGES, STAGE_NAMES)
+                   moe_forward_balanced, moe_get_error, moe_grouped_swiglu, moe_route_topk,
+                   moe_route_topk_balanced, moe_route_topk_noalloc, moe_status_string,
+                   moe_update_select_bias, moe_workspace_size, NUM_STAGES, STAGE_NAMES)
 
 
 class MoELayer:
@@ -28,7 +29,7 @@ class MoELayer:
 
     def __init__(self, w_router, w1, w3, w2, *, k: int, gate: str, capacity: Optional[int] = None,
                  router_bias=None, w1s=None, w3s=None, w2s=None, alpha=0.01, beta=1e-3,
-                 max_tokens: int):
+                 max_tokens: int, balance_gamma: Optional[float] = None):
         E, d = w_router.shape
         self.w = dict(w_router=w_router, w1=w1, w3=w3, w2=w2, router_bias=router_bias,
                       w1s=w1s, w3s=w3s, w2s=w2s)
@@ -41,6 +42,10 @@ class MoELayer:
         self.counts = torch.zeros(E, dtype=torch.int32, device=self.device)
         self.dropped = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.losses = torch.zeros(2, dtype=torch.float32, device=self.device)
+        # auxiliary-loss-free balancing: a selection bias nudged by gamma after every forward
+        self.balance_gamma = balance_gamma
+        self.select_bias = (torch.zeros(E, dtype=torch.float32, device=self.device)
+                            if balance_gamma is not None else None)
 
     def shape(self, T: int):
         return make_shape(T, self.d, self.E, self.k, self.d_ff, gate=self.gate, dtype=self.dtype,
@@ -52,6 +57,14 @@ class MoELayer:
         T = x.shape[0]
         if y is None:
             y = torch.empty_like(x)
+        if self.select_bias is not None:
+            moe_forward_balanced(self.shape(T), self.ws, x, self.w["w_router"], self.w["w1"],
+                                 self.w["w3"], self.w["w2"], y, self.select_bias,
+                                 self.balance_gamma, router_bias=self.w["router_bias"],
+                                 w1s=self.w["w1s"], w3s=self.w["w3s"], w2s=self.w["w2s"],
+                                 counts=self.counts, dropped=self.dropped, losses=self.losses,
+                                 stream=stream, events=events)
+            return y
         moe_forward(self.shape(T), self.ws, x, self.w["w_router"], self.w["w1"], self.w["w3"],
                     self.w["w2"], y, router_bias=self.w["router_bias"], w1s=self.w["w1s"],
                     w3s=self.w["w3s"], w2s=self.w["w2s"], counts=self.counts,

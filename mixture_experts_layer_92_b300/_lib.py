@@ -26,7 +26,8 @@ STAGE_NAMES = ("router_gemm", "gates_topk", "dispatch", "gather", "gemm_gateup_s
 EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_topk",
             "moe_dispatch", "moe_grouped_swiglu", "moe_combine", "moe_aux_loss", "moe_forward",
             "moe_forward_events", "moe_get_error", "moe_clear_error", "moe_status_string",
-            "moe_last_error_detail", "moe_route_topk_noalloc")
+            "moe_last_error_detail", "moe_route_topk_noalloc", "moe_route_topk_balanced",
+            "moe_update_select_bias", "moe_forward_balanced")
 
 
 class MoeError(RuntimeError):
@@ -68,6 +69,12 @@ def _load() -> ctypes.CDLL:
         "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "moe_last_error_detail": (ctypes.c_char_p, []),
         "moe_route_topk_noalloc": (ctypes.c_int, [sp, vp, vp, vp, vp, vp]),
+        "moe_route_topk_balanced": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                                   vp]),
+        "moe_update_select_bias": (ctypes.c_int, [sp, vp, vp, ctypes.c_float, vp]),
+        "moe_forward_balanced": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                vp, vp, ctypes.c_float, vp, sz, vp,
+                                                ctypes.POINTER(vp), ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -181,6 +188,38 @@ def moe_route_topk_noalloc(s, logits_in, topk_idx, topk_gate, stats=None, stream
     """moe_route_topk on precomputed logits with no workspace (scratch inside the library)."""
     _check(LIB.moe_route_topk_noalloc(ctypes.byref(s), _p(logits_in), _p(topk_idx), _p(topk_gate),
                                       _p(stats), _stream(stream)), "moe_route_topk_noalloc")
+
+
+def moe_route_topk_balanced(s, ws, topk_idx, topk_gate, select_bias, x=None, w_router=None,
+                            router_bias=None, logits_in=None, logits_out=None, stats=None,
+                            stream=None):
+    _check(LIB.moe_route_topk_balanced(ctypes.byref(s), _p(x), _p(w_router), _p(router_bias),
+                                       _p(logits_in), _p(select_bias), _p(logits_out),
+                                       _p(topk_idx), _p(topk_gate), _p(stats), _p(ws), ws.numel(),
+                                       _stream(stream)), "moe_route_topk_balanced")
+
+
+def moe_update_select_bias(s, counts, select_bias, gamma, stream=None):
+    _check(LIB.moe_update_select_bias(ctypes.byref(s), _p(counts), _p(select_bias), gamma,
+                                      _stream(stream)), "moe_update_select_bias")
+
+
+def _event_array(events):
+    for e in events:
+        if e.cuda_event == 0:          # torch creates the CUDA event on first record
+            e.record()
+    return (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+
+
+def moe_forward_balanced(s, ws, x, w_router, w1, w3, w2, y, select_bias, gamma, router_bias=None,
+                         w1s=None, w3s=None, w2s=None, counts=None, dropped=None, losses=None,
+                         stream=None, events=None):
+    arr = None if events is None else _event_array(events)
+    _check(LIB.moe_forward_balanced(ctypes.byref(s), _p(x), _p(w_router), _p(router_bias), _p(w1),
+                                    _p(w3), _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(y), _p(counts),
+                                    _p(dropped), _p(losses), _p(select_bias), gamma, _p(ws),
+                                    ws.numel(), _stream(stream), arr,
+                                    0 if events is None else len(events)), "moe_forward_balanced")
 
 
 def moe_get_error(ws, stream=None) -> int:

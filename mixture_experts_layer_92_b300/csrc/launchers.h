@@ -80,6 +80,7 @@ struct RouteArgs {
   int nsplit;
   size_t split_stride;      // elements between splits
   const float* bias;        // [E] added after the sum, or nullptr
+  const float* select_bias; // [E] auxiliary-loss-free balancing bias (selection only), or nullptr
   float* logits_out;        // [T][E] receives the final logits, or nullptr
   int T, E, k, gate_mode;
   int32_t* topk_idx;        // [T][k]
@@ -88,6 +89,8 @@ struct RouteArgs {
   DeviceError* err;         // nullptr: no device error reporting
 };
 int launch_route_topk(const RouteArgs& a, cudaStream_t stream);
+int launch_update_select_bias(const int32_t* counts, float* select_bias, int T, int E, int k,
+                              float gamma, cudaStream_t stream);
 int launch_stats_reduce(const float* partials, int nblocks, int E, float* stats,
                         cudaStream_t stream);
 int launch_aux_loss(const float* stats, const int32_t* counts, int T, int E, int k, float alpha,

@@ -233,12 +233,13 @@ int run_router(const moe_shape* s, const void* x, const void* wr, float* logits,
 
 RouteArgs route_args(const moe_shape* s, const float* logits, int nsplit, const float* bias,
                      float* logits_out, int32_t* idx, float* gate, float* partials,
-                     DeviceError* err) {
+                     DeviceError* err, const float* select_bias = nullptr) {
   RouteArgs a{};
   a.logits = logits;
   a.nsplit = nsplit;
   a.split_stride = static_cast<size_t>(s->T) * s->E;
   a.bias = bias;
+  a.select_bias = select_bias;
   a.logits_out = logits_out;
   a.T = s->T;
   a.E = s->E;
@@ -410,7 +411,8 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
 int forward_impl(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
                  const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
                  const void* w2s, void* y, int32_t* counts, int32_t* dropped, float* losses,
-                 void* ws, size_t ws_bytes, void* stream, void* const* ev, int n_ev) {
+                 void* ws, size_t ws_bytes, void* stream, void* const* ev, int n_ev,
+                 float* select_bias = nullptr, float gamma = 0.f) {
   TRY(check_shape(s));
   TRY(check_ws(s, ws, ws_bytes));
   if (ev != nullptr && n_ev != MOE_NUM_STAGES + 1)
@@ -460,7 +462,7 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   rec(1);
   if (s->T > 0)
     LAUNCH(launch_route_topk(route_args(s, logits, router_split(s).splits, router_bias, nullptr,
-                                        idx, gate, partials, err),
+                                        idx, gate, partials, err, select_bias),
                              st),
            "gates/top-k");
   rec(2);
@@ -481,6 +483,9 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
     LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
   }
   LAUNCH(launch_aux_loss(stats, cnt, s->T, s->E, s->k, s->alpha, s->beta, los, st), "aux loss");
+  if (select_bias != nullptr)
+    LAUNCH(launch_update_select_bias(cnt, select_bias, s->T, s->E, s->k, gamma, st),
+           "selection bias update");
   rec(8);
   return ok();
 }
@@ -516,10 +521,13 @@ size_t moe_workspace_size(const moe_shape* s) {
   return layout(s).total;
 }
 
-int moe_route_topk(const moe_shape* s, const void* x, const void* w_router,
-                   const float* router_bias, const float* logits_in, float* logits_out,
-                   int32_t* topk_idx, float* topk_gate, float* stats, void* ws, size_t ws_bytes,
-                   void* stream) {
+}  // extern "C"
+
+namespace {
+int route_impl(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
+               const float* logits_in, const float* select_bias, float* logits_out,
+               int32_t* topk_idx, float* topk_gate, float* stats, void* ws, size_t ws_bytes,
+               void* stream) {
   TRY(check_shape(s));
   TRY(check_ws(s, ws, ws_bytes));
   if (s->T > 0) {
@@ -548,18 +556,66 @@ int moe_route_topk(const moe_shape* s, const void* x, const void* w_router,
     float* planes = at<float>(ws, L.logits);
     TRY(run_router(s, x, w_router, planes, err, st));
     LAUNCH(launch_route_topk(route_args(s, planes, router_split(s).splits, router_bias, logits_out,
-                                        topk_idx, topk_gate, partials, err),
+                                        topk_idx, topk_gate, partials, err, select_bias),
                              st),
            "gates/top-k");
   } else {
     LAUNCH(launch_route_topk(route_args(s, logits_in, 1, nullptr,
                                         logits_out == logits_in ? nullptr : logits_out, topk_idx,
-                                        topk_gate, partials, err),
+                                        topk_gate, partials, err, select_bias),
                              st),
            "gates/top-k");
   }
   if (stats) LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
   return ok();
+}
+}  // namespace
+
+extern "C" {
+
+int moe_route_topk(const moe_shape* s, const void* x, const void* w_router,
+                   const float* router_bias, const float* logits_in, float* logits_out,
+                   int32_t* topk_idx, float* topk_gate, float* stats, void* ws, size_t ws_bytes,
+                   void* stream) {
+  return route_impl(s, x, w_router, router_bias, logits_in, nullptr, logits_out, topk_idx,
+                    topk_gate, stats, ws, ws_bytes, stream);
+}
+
+int moe_route_topk_balanced(const moe_shape* s, const void* x, const void* w_router,
+                            const float* router_bias, const float* logits_in,
+                            const float* select_bias, float* logits_out, int32_t* topk_idx,
+                            float* topk_gate, float* stats, void* ws, size_t ws_bytes,
+                            void* stream) {
+  if (select_bias == nullptr) return fail(MOE_ERR_INVALID, "select_bias is NULL");
+  if (!aligned4(select_bias)) return fail(MOE_ERR_INVALID, "select_bias is not 4-byte aligned");
+  return route_impl(s, x, w_router, router_bias, logits_in, select_bias, logits_out, topk_idx,
+                    topk_gate, stats, ws, ws_bytes, stream);
+}
+
+int moe_update_select_bias(const moe_shape* s, const int32_t* counts, float* select_bias,
+                           float gamma, void* stream) {
+  TRY(check_shape(s));
+  REQUIRE_PTR4(counts, "counts");
+  REQUIRE_PTR4(select_bias, "select_bias");
+  if (!(gamma >= 0.f)) return fail(MOE_ERR_INVALID, "gamma must be >= 0");
+  LAUNCH(launch_update_select_bias(counts, select_bias, s->T, s->E, s->k, gamma,
+                                   static_cast<cudaStream_t>(stream)),
+         "selection bias update");
+  return ok();
+}
+
+int moe_forward_balanced(const moe_shape* s, const void* x, const void* w_router,
+                         const float* router_bias, const void* w1, const void* w3, const void* w2,
+                         const void* w1s, const void* w3s, const void* w2s, void* y,
+                         int32_t* counts, int32_t* dropped, float* losses, float* select_bias,
+                         float gamma, void* ws, size_t ws_bytes, void* stream,
+                         void* const* events, int n_events) {
+  if (select_bias == nullptr) return fail(MOE_ERR_INVALID, "select_bias is NULL");
+  if (!aligned4(select_bias)) return fail(MOE_ERR_INVALID, "select_bias is not 4-byte aligned");
+  if (!(gamma >= 0.f)) return fail(MOE_ERR_INVALID, "gamma must be >= 0");
+  return forward_impl(s, x, w_router, router_bias, w1, w3, w2, w1s, w3s, w2s, y, counts, dropped,
+                      losses, ws, ws_bytes, stream, events, events ? n_events : 0, select_bias,
+                      gamma);
 }
 
 int moe_dispatch(const moe_shape* s, const int32_t* topk_idx, const float* logits_in,

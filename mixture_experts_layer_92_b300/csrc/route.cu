@@ -30,9 +30,10 @@ constexpr int kNoIdx = 0x7fffffff;
 template <int JM>
 __global__ void __launch_bounds__(kRouteThreads)
 route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_stride,
-                  const float* __restrict__ bias, float* __restrict__ logits_out, int T, int E,
-                  int k, int gate_mode, int32_t* __restrict__ topk_idx,
-                  float* __restrict__ topk_gate, float* __restrict__ partials, DeviceError* err) {
+                  const float* __restrict__ bias, const float* __restrict__ select_bias,
+                  float* __restrict__ logits_out, int T, int E, int k, int gate_mode,
+                  int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
+                  float* __restrict__ partials, DeviceError* err) {
   extern __shared__ float s_part[];  // [kRouteWarps][E + 1]
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
@@ -85,6 +86,21 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
     const float lse = m + logf(s);
     if (lane == 0) lse2 += lse * lse;
 
+    // selection key: the raw logit, or (auxiliary-loss-free balancing) the gate affinity
+    // plus the expert's selection bias -- sigmoid(l) for sigmoid gating, the softmax
+    // probability otherwise. The gates below never include the bias.
+    float key[JM];
+#pragma unroll
+    for (int j = 0; j < JM; ++j) {
+      key[j] = v[j];
+      const int e = lane + 32 * j;
+      if (select_bias != nullptr && e < E) {
+        const float a = (gate_mode == MOE_GATE_SIGMOID_TOPK) ? 1.0f / (1.0f + expf(-v[j]))
+                                                             : ex[j] / s;
+        key[j] = a + __ldg(select_bias + e);
+      }
+    }
+
     // k rounds of a warp arg-max over the not-yet-selected experts
     for (int r = 0; r < k; ++r) {
       float bv = -INFINITY;
@@ -93,8 +109,8 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
       for (int j = 0; j < JM; ++j) {
         const int e = lane + 32 * j;
         // j ascending means e ascending: a strict '>' keeps the lowest index among equals
-        if (e < E && slot[j] < 0 && (bi == kNoIdx || v[j] > bv)) {
-          bv = v[j];
+        if (e < E && slot[j] < 0 && (bi == kNoIdx || key[j] > bv)) {
+          bv = key[j];
           bi = e;
         }
       }
@@ -200,12 +216,26 @@ __global__ void aux_loss_kernel(const float* __restrict__ stats, const int32_t* 
   }
 }
 
+// Auxiliary-loss-free balancing: b_i += gamma if expert i got fewer than T*k/E assignments,
+// -= gamma if more (integer comparison n_i * E vs T * k), unchanged at the mean.
+__global__ void update_select_bias_kernel(const int32_t* __restrict__ counts,
+                                          float* __restrict__ select_bias, int T, int E, int k,
+                                          float gamma) {
+  for (int e = blockIdx.x * blockDim.x + threadIdx.x; e < E; e += gridDim.x * blockDim.x) {
+    const long long n = static_cast<long long>(counts[e]) * E;
+    const long long mean = static_cast<long long>(T) * k;
+    if (n < mean) select_bias[e] = select_bias[e] + gamma;
+    else if (n > mean) select_bias[e] = select_bias[e] - gamma;
+  }
+}
+
 template <int JM>
 int launch_jm(const RouteArgs& a, cudaStream_t stream) {
   const int nb = route_blocks(a.T);
   const size_t smem = static_cast<size_t>(kRouteWarps) * (a.E + 1) * sizeof(float);
   route_topk_kernel<JM><<<nb, kRouteThreads, smem, stream>>>(
-      a.logits, a.nsplit, a.split_stride, a.bias, a.logits_out, a.T, a.E, a.k, a.gate_mode,
+      a.logits, a.nsplit, a.split_stride, a.bias, a.select_bias, a.logits_out, a.T, a.E, a.k,
+      a.gate_mode,
       a.topk_idx, a.topk_gate, a.partials, a.err);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
@@ -232,6 +262,13 @@ int launch_route_topk(const RouteArgs& a, cudaStream_t stream) {
 int launch_stats_reduce(const float* partials, int nblocks, int E, float* stats,
                         cudaStream_t stream) {
   stats_reduce_kernel<<<E + 1, 256, 0, stream>>>(partials, nblocks, E, stats);
+  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_update_select_bias(const int32_t* counts, float* select_bias, int T, int E, int k,
+                              float gamma, cudaStream_t stream) {
+  update_select_bias_kernel<<<(E + 255) / 256, 256, 0, stream>>>(counts, select_bias, T, E, k,
+                                                                 gamma);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -419,13 +419,22 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             tmem_ld_wait();
             if (rvalid) {
               const int col0 = col_base + c * 16;
+              float* dst = out + row * ldo + col0;
+              if (args.bias == nullptr && col0 + 16 <= N && (ldo & 3) == 0) {
+                // whole 16-column chunk inside the row: four 16-byte stores
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
-                const int col = col0 + i;
-                if (col < N) {
-                  float val = __uint_as_float(v[i]);
-                  if (args.bias != nullptr) val += args.bias[col];
-                  out[row * ldo + col] = val;
+                for (int q = 0; q < 4; ++q)
+                  *reinterpret_cast<uint4*>(dst + 4 * q) =
+                      make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+              } else {
+#pragma unroll
+                for (int i = 0; i < 16; ++i) {
+                  const int col = col0 + i;
+                  if (col < N) {
+                    float val = __uint_as_float(v[i]);
+                    if (args.bias != nullptr) val += args.bias[col];
+                    dst[i] = val;
+                  }
                 }
               }
             }
