@@ -275,6 +275,64 @@ def update_select_bias(select_bias, counts, T: int, k: int, gamma: float) -> np.
 
 
 # ---------------------------------------------------------------------------------------
+# Expert-choice routing.  [Starphix] "Router Variants": experts choose their tokens (rather
+# than tokens choosing experts), which balances the load perfectly. Readings: the score is
+# the softmax-over-all router probability; expert e takes the C tokens with the highest
+# score for e (ties -> lower token index); the gate of that pair is the score; a token's
+# output sums, in expert order, over the experts that chose it (possibly none).
+# ---------------------------------------------------------------------------------------
+def expert_choice(logits, C: int) -> dict:
+    """Per-expert token choice. Returns
+      perm    [E*C']  token of each row, expert-major, ascending tokens inside an expert,
+      offsets [E+1]   e*C' (C' = min(C, T)),
+      gate    [E*C']  router probability of (token, expert) for each row,
+      inv     [T, E]  row of (t, e), or -1 when expert e did not choose token t,
+      counts  [E]     C' each, unrouted: tokens no expert chose."""
+    p = softmax_all(logits)
+    T, E = p.shape
+    Cp = min(C, T)
+    perm = np.zeros(E * Cp, dtype=np.int64)
+    gate = np.zeros(E * Cp, dtype=np.float64)
+    inv = np.full((T, E), -1, dtype=np.int64)
+    for e in range(E):
+        chosen = np.sort(np.argsort(-p[:, e], kind="stable")[:Cp])
+        rows = np.arange(e * Cp, (e + 1) * Cp)
+        perm[rows] = chosen
+        gate[rows] = p[chosen, e]
+        inv[chosen, e] = rows
+    return dict(perm=perm, offsets=np.arange(E + 1, dtype=np.int64) * Cp, gate=gate, inv=inv,
+                counts=np.full(E, Cp, dtype=np.int64),
+                unrouted=int(np.sum(np.all(inv < 0, axis=1))))
+
+
+def expert_choice_forward(x, w_router, w1, w3, w2, *, C: int, router_bias=None, w1s=None,
+                          w3s=None, w2s=None, alpha: float = 0.01, beta: float = 1e-3,
+                          k: int = 1) -> dict:
+    """The layer with expert-choice routing, in fp64. The balance loss uses f_i = C'/(T*k)."""
+    x = _f64(x)
+    T = x.shape[0]
+    logits = router_logits(x, w_router, router_bias)
+    ec = expert_choice(logits, C)
+    E = logits.shape[1]
+    rows = np.zeros((ec["perm"].shape[0], x.shape[1]), dtype=np.float64)
+    for e in range(E):
+        lo, hi = int(ec["offsets"][e]), int(ec["offsets"][e + 1])
+        if hi > lo:
+            rows[lo:hi] = swiglu_ffn(x[ec["perm"][lo:hi]], w1[e], w3[e], w2[e])
+    y = np.zeros_like(x)
+    for e in range(E):                      # expert order
+        sel = ec["inv"][:, e] >= 0
+        r = ec["inv"][sel, e]
+        y[sel] += ec["gate"][r][:, None] * rows[r]
+    if w1s is not None:
+        y = y + swiglu_ffn(x, w1s, w3s, w2s)
+    P = softmax_all(logits).mean(axis=0) if T else np.zeros(E)
+    f = ec["counts"] / float(T * k) if T else np.zeros(E)
+    l_aux = float(alpha * E * np.dot(f, P)) if T else 0.0
+    return dict(y=y, logits=logits, ec=ec, l_aux=l_aux, l_z=z_loss(logits, beta))
+
+
+# ---------------------------------------------------------------------------------------
 # The whole layer, for inputs small enough to hold in fp64.
 # ---------------------------------------------------------------------------------------
 def route(logits, k: int, mode: str) -> dict:

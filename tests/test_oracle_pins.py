@@ -388,3 +388,46 @@ def test_selection_bias_loop_balances_a_skewed_router():
         b = O.update_select_bias(b, n, T, k, 0.01)
     assert spread[0] > 3.0                      # starts badly unbalanced
     assert np.mean(spread[-20:]) < 1.5          # ends close to uniform
+
+
+# ---------------------------------------------------------------- expert-choice routing
+def test_expert_choice_brute_force():
+    """Each expert's chosen set beats every unchosen token (higher probability, or equal
+    and lower index); every expert takes exactly min(C, T) tokens."""
+    rng = np.random.default_rng(31)
+    for trial in range(6):
+        T, E = int(rng.integers(1, 14)), int(rng.integers(1, 6))
+        l = np.round(rng.normal(size=(T, E)) * 2) / 2         # frequent ties
+        C = int(rng.integers(0, T + 3))
+        ec = O.expert_choice(l, C)
+        p = O.softmax_all(l)
+        Cp = min(C, T)
+        assert ec["counts"].tolist() == [Cp] * E
+        for e in range(E):
+            chosen = set(ec["perm"][e * Cp:(e + 1) * Cp].tolist())
+            assert len(chosen) == Cp
+            for t in chosen:
+                for u in set(range(T)) - chosen:
+                    assert p[t, e] > p[u, e] or (p[t, e] == p[u, e] and t < u)
+            for j, t in enumerate(ec["perm"][e * Cp:(e + 1) * Cp]):
+                assert ec["inv"][t, e] == e * Cp + j and ec["gate"][e * Cp + j] == p[t, e]
+        assert ec["unrouted"] == sum(1 for t in range(T) if all(ec["inv"][t] < 0))
+
+
+def test_expert_choice_single_expert_takes_the_first_tokens():
+    """E = 1: every probability is 1 (a full tie), so the expert takes tokens 0..C-1."""
+    ec = O.expert_choice(np.random.default_rng(32).normal(size=(10, 1)), 4)
+    assert ec["perm"].tolist() == [0, 1, 2, 3] and ec["unrouted"] == 6
+
+
+def test_expert_choice_everyone_chosen_with_identical_experts_is_the_dense_ffn():
+    """C = T: every expert takes every token, the gates of a token sum to 1 (softmax), so
+    identical experts give exactly one dense SwiGLU FFN."""
+    rng = np.random.default_rng(33)
+    T, d, E, F = 12, 6, 4, 10
+    w1, w3, w2 = rng.normal(size=(F, d)), rng.normal(size=(F, d)), rng.normal(size=(d, F))
+    W1, W3, W2 = (np.repeat(w[None], E, axis=0) for w in (w1, w3, w2))
+    x = rng.normal(size=(T, d))
+    out = O.expert_choice_forward(x, rng.normal(size=(E, d)), W1, W3, W2, C=T)
+    np.testing.assert_allclose(out["y"], O.swiglu_ffn(x, w1, w3, w2), rtol=1e-12, atol=1e-12)
+    assert out["ec"]["unrouted"] == 0
