@@ -253,8 +253,10 @@ def run_reference(args, w, rank):
 # ------------------------------------------------------------------------------ GPU arm
 def launches_per_forward(w) -> int:
     # router, top-k, dispatch, gather, gate/up GEMM, down GEMM, combine, stats, losses;
-    # the fp32 path launches the shared expert's two GEMMs separately
-    return 9 + (2 if (w.dtype == "f32" and w.d_ff_shared) else 0)
+    # the fp32 path launches the shared expert's two GEMMs separately; expert choice runs a
+    # selection and an unrouted-token count in place of the dispatch
+    n = 9 + (2 if (w.dtype == "f32" and w.d_ff_shared) else 0)
+    return n + (1 if w.gate == "expert_choice" else 0)
 
 
 def run_ours(args, w, rank, world, local_rank):
@@ -405,6 +407,9 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--balance-gamma", type=float, default=None,
                     help="auxiliary-loss-free balancing: nudge a selection bias by this step")
+    ap.add_argument("--expert-choice", action="store_true",
+                    help="expert-choice routing: each expert takes C = ceil(cf*T*k/E) tokens "
+                         "(cf = 1 when the workload has none)")
     ap.add_argument("--zipf", type=float, default=None,
                     help="add a Zipf(s) log-popularity bias to the router logits (skewed load)")
     args = ap.parse_args(argv)
@@ -417,6 +422,9 @@ def main(argv=None):
         w = w.scaled(zipf_s=args.zipf, name=f"{w.name}+zipf{args.zipf}")
     if args.balance_gamma is not None:
         w = w.scaled(name=f"{w.name}+balanced")
+    if args.expert_choice:
+        w = w.scaled(gate="expert_choice", cf=w.cf if w.cf is not None else 1.0,
+                     name=f"{w.name}+expert_choice")
     if args.impl == "reference":
         run_reference(args, w, rank)
         return

@@ -60,7 +60,8 @@ typedef enum {
 typedef enum {
   MOE_GATE_SOFTMAX_ALL = 0,   /* Switch/GShard: softmax over all E, selected probs kept  */
   MOE_GATE_SOFTMAX_TOPK = 1,  /* Mixtral: softmax over the k selected logits              */
-  MOE_GATE_SIGMOID_TOPK = 2   /* DeepSeek-V3: sigmoid affinities / their sum over the k   */
+  MOE_GATE_SIGMOID_TOPK = 2,  /* DeepSeek-V3: sigmoid affinities / their sum over the k   */
+  MOE_GATE_EXPERT_CHOICE = 3  /* experts choose tokens: see moe_expert_choice               */
 } moe_gate_mode;
 
 typedef enum { MOE_F32 = 0, MOE_BF16 = 1 } moe_dtype;
@@ -184,6 +185,26 @@ int moe_forward_events(const moe_shape* s, const void* x, const void* w_router,
                        const void* w2, const void* w1s, const void* w3s, const void* w2s,
                        void* y, int32_t* counts, int32_t* dropped, float* losses, void* ws,
                        size_t ws_bytes, void* stream, void* const* events, int n_events);
+
+/* Expert-choice routing -- "Mixture of Experts (MoE)", learn.starphix.com, Router Variants:
+ * experts choose their tokens (perfect load balance). For shapes with gate =
+ * MOE_GATE_EXPERT_CHOICE: the score of (t, e) is the softmax-over-all router probability;
+ * expert e keeps the C' = min(capacity, T) tokens with the highest score for it (ties ->
+ * lower token index), stored in ascending token order; the gate is that probability.
+ *   x/w_router/router_bias or logits_in as in moe_route_topk.
+ *   perm [E*C'] out: token index of each row (expert e owns rows e*C' .. (e+1)*C'-1).
+ *   offsets [E+1] out: e*C'.  row_gate [E*C'] out: gate of each row.
+ *   inv [T, E] out: row of (t, e), or -1 when e did not choose t.
+ *   counts [E] out: C' each.  unrouted [1] out: tokens that no expert chose.
+ *   stats [E+1] or NULL: as in moe_route_topk.
+ * In this mode moe_forward runs router -> expert choice -> grouped SwiGLU (perm holds tokens,
+ * gates per row) -> combine over inv in expert order; moe_grouped_swiglu reads perm as token
+ * indices and topk_gate as the per-row gate; moe_combine reads inv as [T, E]; its
+ * `dropped` output is the unrouted count; moe_route_topk and moe_dispatch refuse the mode. */
+int moe_expert_choice(const moe_shape* s, const void* x, const void* w_router,
+                      const float* router_bias, const float* logits_in, int32_t* perm,
+                      int32_t* offsets, float* row_gate, int32_t* inv, int32_t* counts,
+                      int32_t* unrouted, float* stats, void* ws, size_t ws_bytes, void* stream);
 
 /* Auxiliary-loss-free balancing (DeepSeek-V3) -- "Mixture of experts (MoE)", tirogla.com,
  * Implementation notes: a per-expert bias is added to the scores used for top-k selection

@@ -17,7 +17,7 @@ LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 MOE_OK = 0
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
           -4: "MOE_ERR_WORKSPACE", -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_NONFINITE"}
-GATE_MODES = {"softmax_all": 0, "softmax_topk": 1, "sigmoid_topk": 2}
+GATE_MODES = {"softmax_all": 0, "softmax_topk": 1, "sigmoid_topk": 2, "expert_choice": 3}
 DTYPES = {torch.float32: 0, torch.bfloat16: 1}
 NUM_STAGES = 8
 STAGE_NAMES = ("router_gemm", "gates_topk", "dispatch", "gather", "gemm_gateup_swiglu",
@@ -27,7 +27,7 @@ EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_
             "moe_dispatch", "moe_grouped_swiglu", "moe_combine", "moe_aux_loss", "moe_forward",
             "moe_forward_events", "moe_get_error", "moe_clear_error", "moe_status_string",
             "moe_last_error_detail", "moe_route_topk_noalloc", "moe_route_topk_balanced",
-            "moe_update_select_bias", "moe_forward_balanced")
+            "moe_update_select_bias", "moe_forward_balanced", "moe_expert_choice")
 
 
 class MoeError(RuntimeError):
@@ -72,6 +72,8 @@ def _load() -> ctypes.CDLL:
         "moe_route_topk_balanced": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                                                    vp]),
         "moe_update_select_bias": (ctypes.c_int, [sp, vp, vp, ctypes.c_float, vp]),
+        "moe_expert_choice": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
+                                             vp]),
         "moe_forward_balanced": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                 vp, vp, ctypes.c_float, vp, sz, vp,
                                                 ctypes.POINTER(vp), ctypes.c_int]),
@@ -197,6 +199,14 @@ def moe_route_topk_balanced(s, ws, topk_idx, topk_gate, select_bias, x=None, w_r
                                        _p(logits_in), _p(select_bias), _p(logits_out),
                                        _p(topk_idx), _p(topk_gate), _p(stats), _p(ws), ws.numel(),
                                        _stream(stream)), "moe_route_topk_balanced")
+
+
+def moe_expert_choice(s, ws, perm, offsets, row_gate, inv, counts, unrouted, x=None,
+                      w_router=None, router_bias=None, logits_in=None, stats=None, stream=None):
+    _check(LIB.moe_expert_choice(ctypes.byref(s), _p(x), _p(w_router), _p(router_bias),
+                                 _p(logits_in), _p(perm), _p(offsets), _p(row_gate), _p(inv),
+                                 _p(counts), _p(unrouted), _p(stats), _p(ws), ws.numel(),
+                                 _stream(stream)), "moe_expert_choice")
 
 
 def moe_update_select_bias(s, counts, select_bias, gamma, stream=None):

@@ -30,6 +30,7 @@ struct TcArgs {
   long long ldo_shared;
   const int32_t* perm;      // TC_SCALE: row r is scaled by gate[perm[r]] (gate == nullptr: 1)
   const float* gate;
+  const float* row_gate;    // TC_SCALE: if set, row r is scaled by row_gate[r] instead
   const float* bias;        // TC_F32OUT: per-column bias or nullptr
   int splits;               // TC_F32OUT: split-K factor (>= 1); split s writes out + s*split_stride
   int kb_per_split;         //            k-blocks (of 64) per split
@@ -67,8 +68,9 @@ struct SimtArgs {
   const float* b1;          // TC_SWIGLU: W3
   int n, k;
   float* out;               // [*, n]
-  const int32_t* perm;      // TC_SCALE gates
+  const int32_t* perm;      // TC_SCALE gates: gate[perm[r]], or row_gate[r] if set
   const float* gate;
+  const float* row_gate;
   const float* bias;        // TC_F32OUT bias
 };
 int launch_simt_gemm(int mode, const SimtArgs& a, cudaStream_t stream);
@@ -82,7 +84,8 @@ struct RouteArgs {
   const float* bias;        // [E] added after the sum, or nullptr
   const float* select_bias; // [E] auxiliary-loss-free balancing bias (selection only), or nullptr
   float* logits_out;        // [T][E] receives the final logits, or nullptr
-  int T, E, k, gate_mode;
+  float* probs_t;           // [E][T] receives the softmax probabilities, or nullptr
+  int T, E, k, gate_mode;   // k = 0: no selection (probabilities and statistics only)
   int32_t* topk_idx;        // [T][k]
   float* topk_gate;         // [T][k]
   float* partials;          // [route_blocks(T)][E + 1]
@@ -103,6 +106,13 @@ int dispatch_max_blocks(int num_sms);
 int launch_dispatch(const int32_t* topk_idx, int A, int E, int C, int32_t* counts,
                     int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dropped,
                     int32_t* blk_hist, DeviceError* err, int num_sms, cudaStream_t stream);
+
+// ---------------------------------------------------------------- expert-choice routing
+// probs_t [E][T]; writes perm/row_gate [E*C'] (C' = min(C, T)), inv [T][E] (-1 = not chosen),
+// counts [E] = C', offsets [E+1], unrouted [1] = tokens no expert chose.
+int launch_expert_choice(const float* probs_t, int T, int E, int C, int32_t* perm,
+                         float* row_gate, int32_t* inv, int32_t* counts, int32_t* offsets,
+                         int32_t* unrouted, cudaStream_t stream);
 
 // ---------------------------------------------------------------- data movement
 int launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, int E, int k,

@@ -60,9 +60,18 @@ RouterSplit router_split(const moe_shape* s) {
   return {(nk + kb - 1) / kb, kb};
 }
 
+bool expert_choice(const moe_shape* s) { return s->gate == MOE_GATE_EXPERT_CHOICE; }
+
+// Rows of the permuted activations: T*k assignments, or E*min(C, T) for expert choice.
+size_t perm_rows(const moe_shape* s) {
+  if (expert_choice(s))
+    return static_cast<size_t>(s->E) * static_cast<size_t>(std::min(s->capacity, s->T));
+  return static_cast<size_t>(s->T) * s->k;
+}
+
 struct Layout {
   size_t err, logits, idx, gate, partials, stats, counts, offsets, perm, inv, dropped, losses,
-      blk_hist;
+      blk_hist, probs;
   size_t xp, h, yp, hs, ys, total;
 };
 
@@ -70,6 +79,8 @@ Layout layout(const moe_shape* s) {
   const size_t T = s->T, E = s->E, k = s->k, d = s->d, F = s->d_ff, Fs = s->d_ff_shared;
   const size_t es = esize(s);
   const size_t A = T * k;
+  const size_t R = perm_rows(s);
+  const bool ec = expert_choice(s);
   Layout L;
   size_t o = 0;
   auto take = [&](size_t bytes) {
@@ -80,19 +91,20 @@ Layout layout(const moe_shape* s) {
   L.err = take(sizeof(DeviceError));
   L.logits = take(static_cast<size_t>(router_split(s).splits) * T * E * 4);
   L.idx = take(A * 4);
-  L.gate = take(A * 4);
+  L.gate = take(std::max(A, R) * 4);
   L.partials = take(static_cast<size_t>(route_blocks(s->T)) * (E + 1) * 4);
   L.stats = take((E + 1) * 4);
   L.counts = take(E * 4);
   L.offsets = take((E + 1) * 4);
-  L.perm = take(A * 4);
-  L.inv = take(A * 4);
+  L.perm = take(std::max(A, R) * 4);
+  L.inv = take(ec ? T * E * 4 : A * 4);
   L.dropped = take(4);
   L.losses = take(2 * 4);
   L.blk_hist = take(static_cast<size_t>(dispatch_max_blocks(148)) * E * 4);
-  L.xp = take(A * d * es);
-  L.h = take(A * F * es);
-  L.yp = take(A * d * es);
+  L.probs = take(ec ? T * E * 4 : 0);
+  L.xp = take(R * d * es);
+  L.h = take(R * F * es);
+  L.yp = take(R * d * es);
   L.hs = take(Fs > 0 ? T * Fs * es : 0);
   L.ys = take(Fs > 0 ? T * d * es : 0);
   L.total = o;
@@ -108,12 +120,15 @@ int check_shape(const moe_shape* s) {
   if (s->d_ff < 1) return fail(MOE_ERR_INVALID, "d_ff = %d < 1", s->d_ff);
   if (s->d_ff_shared < 0) return fail(MOE_ERR_INVALID, "d_ff_shared = %d < 0", s->d_ff_shared);
   if (s->capacity < 0) return fail(MOE_ERR_INVALID, "capacity = %d < 0", s->capacity);
-  if (s->gate < MOE_GATE_SOFTMAX_ALL || s->gate > MOE_GATE_SIGMOID_TOPK)
+  if (s->gate < MOE_GATE_SOFTMAX_ALL || s->gate > MOE_GATE_EXPERT_CHOICE)
     return fail(MOE_ERR_INVALID, "gate mode %d unknown", s->gate);
   if (s->dtype != MOE_F32 && s->dtype != MOE_BF16)
     return fail(MOE_ERR_INVALID, "dtype %d unknown", s->dtype);
   if (static_cast<long long>(s->T) * s->k >= (1ll << 31))
     return fail(MOE_ERR_INVALID, "T*k = %lld does not fit int32", static_cast<long long>(s->T) * s->k);
+  if (s->gate == MOE_GATE_EXPERT_CHOICE &&
+      static_cast<long long>(s->T) * s->E >= (1ll << 31))
+    return fail(MOE_ERR_INVALID, "expert choice needs T*E < 2^31");
   if ((static_cast<size_t>(s->d) * esize(s)) % 16 != 0)
     return fail(MOE_ERR_UNSUPPORTED, "d * sizeof(dtype) = %zu is not a multiple of 16 bytes",
                 static_cast<size_t>(s->d) * esize(s));
@@ -253,13 +268,16 @@ RouteArgs route_args(const moe_shape* s, const float* logits, int nsplit, const 
 }
 
 // ---------------------------------------------------------------- stages 4-5: expert GEMMs
+// Expert-choice layers pass row_gate (gate per row) and perm holding token indices; top-k
+// layers pass gate (per assignment, looked up through perm) and perm holding assignments.
 int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const int32_t* offsets,
-                const float* gate, const void* w1, const void* w3, const void* w2, const void* w1s,
-                const void* w3s, const void* w2s, void* y_perm, void* y_shared, void* ws,
-                cudaStream_t st, void* const* ev, int ev_first) {
+                const float* gate, const float* row_gate, const void* w1, const void* w3,
+                const void* w2, const void* w1s, const void* w3s, const void* w2s, void* y_perm,
+                void* y_shared, void* ws, cudaStream_t st, void* const* ev, int ev_first) {
   const Layout L = layout(s);
   DeviceError* err = at<DeviceError>(ws, L.err);
-  const int A = s->T * s->k;
+  const int A = static_cast<int>(perm_rows(s));
+  const int gather_k = expert_choice(s) ? 1 : s->k;
   const bool shared = s->d_ff_shared > 0;
   void* xp = at<void>(ws, L.xp);
   void* h = at<void>(ws, L.h);
@@ -273,7 +291,8 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
 
   // stage 3: gather
   rec(ev_first);
-  LAUNCH(launch_gather(x, perm, offsets, s->E, s->k, static_cast<int>(s->d * esize(s)), A, xp, sms, st),
+  LAUNCH(launch_gather(x, perm, offsets, s->E, gather_k, static_cast<int>(s->d * esize(s)), A, xp,
+                       sms, st),
          "gather");
 
   if (s->dtype == MOE_F32) {
@@ -314,6 +333,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     g2.out = static_cast<float*>(y_perm);
     g2.perm = perm;
     g2.gate = gate;
+    g2.row_gate = row_gate;
     LAUNCH(launch_simt_gemm(TC_SCALE, g2, st), "down GEMM (fp32)");
     if (shared) {
       SimtArgs gs = g2;
@@ -327,6 +347,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
       gs.out = static_cast<float*>(y_shared);
       gs.perm = nullptr;
       gs.gate = nullptr;
+      gs.row_gate = nullptr;
       LAUNCH(launch_simt_gemm(TC_SCALE, gs, st), "shared down GEMM (fp32)");
     }
     return MOE_OK;
@@ -390,6 +411,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.args.ldo_shared = s->d;
     p.args.perm = perm;
     p.args.gate = gate;
+    p.args.row_gate = row_gate;
     p.args.err = err;
     p.a = h;
     p.a_rows = std::max(A, 1);
@@ -457,27 +479,42 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
     if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
   };
 
+  const bool ec = expert_choice(s);
+  if (ec && select_bias != nullptr)
+    return fail(MOE_ERR_UNSUPPORTED, "selection bias applies to top-k routing only");
   rec(0);
   TRY(run_router(s, x, w_router, logits, err, st));
   rec(1);
-  if (s->T > 0)
-    LAUNCH(launch_route_topk(route_args(s, logits, router_split(s).splits, router_bias, nullptr,
-                                        idx, gate, partials, err, select_bias),
-                             st),
-           "gates/top-k");
-  rec(2);
-  LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, cnt, off, perm, inv, drp,
-                         at<int32_t>(ws, L.blk_hist), err, num_sms(), st),
-         "dispatch");
   if (s->T > 0) {
-    TRY(run_experts(s, x, perm, off, gate, w1, w3, w2, w1s, w3s, w2s, yp, ys, ws, st, ev, 3));
+    RouteArgs ra = route_args(s, logits, router_split(s).splits, router_bias, nullptr, idx, gate,
+                              partials, err, select_bias);
+    if (ec) {
+      ra.k = 0;  // probabilities and statistics only; the experts choose below
+      ra.probs_t = at<float>(ws, L.probs);
+    }
+    LAUNCH(launch_route_topk(ra, st), "gates/top-k");
+  }
+  rec(2);
+  if (ec) {
+    LAUNCH(launch_expert_choice(at<float>(ws, L.probs), s->T, s->E, s->capacity, perm, gate, inv,
+                                cnt, off, drp, st),
+           "expert choice");
+  } else {
+    LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, cnt, off, perm, inv, drp,
+                           at<int32_t>(ws, L.blk_hist), err, num_sms(), st),
+           "dispatch");
+  }
+  if (s->T > 0) {
+    TRY(run_experts(s, x, perm, off, ec ? nullptr : gate, ec ? gate : nullptr, w1, w3, w2, w1s,
+                    w3s, w2s, yp, ys, ws, st, ev, 3));
   } else {
     rec(3);
     rec(4);
     rec(5);
   }
   rec(6);
-  LAUNCH(launch_combine(s->dtype, yp, inv, ys, y, s->T, s->k, s->d, num_sms(), st), "combine");
+  LAUNCH(launch_combine(s->dtype, yp, inv, ys, y, s->T, ec ? s->E : s->k, s->d, num_sms(), st),
+         "combine");
   rec(7);
   if (s->T > 0) {
     LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
@@ -529,6 +566,8 @@ int route_impl(const moe_shape* s, const void* x, const void* w_router, const fl
                int32_t* topk_idx, float* topk_gate, float* stats, void* ws, size_t ws_bytes,
                void* stream) {
   TRY(check_shape(s));
+  if (expert_choice(s))
+    return fail(MOE_ERR_UNSUPPORTED, "expert-choice layers route with moe_expert_choice");
   TRY(check_ws(s, ws, ws_bytes));
   if (s->T > 0) {
     if (logits_in == nullptr) {
@@ -592,6 +631,54 @@ int moe_route_topk_balanced(const moe_shape* s, const void* x, const void* w_rou
                     topk_gate, stats, ws, ws_bytes, stream);
 }
 
+int moe_expert_choice(const moe_shape* s, const void* x, const void* w_router,
+                      const float* router_bias, const float* logits_in, int32_t* perm,
+                      int32_t* offsets, float* row_gate, int32_t* inv, int32_t* counts,
+                      int32_t* unrouted, float* stats, void* ws, size_t ws_bytes, void* stream) {
+  TRY(check_shape(s));
+  if (!expert_choice(s))
+    return fail(MOE_ERR_INVALID, "moe_expert_choice needs gate = MOE_GATE_EXPERT_CHOICE");
+  TRY(check_ws(s, ws, ws_bytes));
+  REQUIRE_PTR4(offsets, "offsets");
+  REQUIRE_PTR4(counts, "counts");
+  REQUIRE_PTR4(unrouted, "unrouted");
+  OPT_PTR4(stats, "stats");
+  if (s->T > 0) {
+    if (logits_in == nullptr) {
+      REQUIRE_PTR(x, "x");
+      REQUIRE_PTR(w_router, "w_router");
+      OPT_PTR4(router_bias, "router_bias");
+    } else {
+      REQUIRE_PTR4(logits_in, "logits_in");
+    }
+    REQUIRE_PTR4(perm, "perm");
+    REQUIRE_PTR4(row_gate, "row_gate");
+    REQUIRE_PTR4(inv, "inv");
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  const Layout L = layout(s);
+  DeviceError* err = at<DeviceError>(ws, L.err);
+  float* partials = at<float>(ws, L.partials);
+  if (s->T > 0) {
+    RouteArgs ra = (logits_in == nullptr)
+                       ? route_args(s, at<float>(ws, L.logits), router_split(s).splits,
+                                    router_bias, nullptr, nullptr, nullptr, partials, err)
+                       : route_args(s, logits_in, 1, nullptr, nullptr, nullptr, nullptr, partials,
+                                    err);
+    if (logits_in == nullptr) TRY(run_router(s, x, w_router, at<float>(ws, L.logits), err, st));
+    ra.k = 0;
+    ra.probs_t = at<float>(ws, L.probs);
+    LAUNCH(launch_route_topk(ra, st), "router probabilities");
+    if (stats) LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
+  } else if (stats && cudaMemsetAsync(stats, 0, (s->E + 1) * sizeof(float), st) != cudaSuccess) {
+    return cuda_status("memset stats");
+  }
+  LAUNCH(launch_expert_choice(at<float>(ws, L.probs), s->T, s->E, s->capacity, perm, row_gate,
+                              inv, counts, offsets, unrouted, st),
+         "expert choice");
+  return ok();
+}
+
 int moe_update_select_bias(const moe_shape* s, const int32_t* counts, float* select_bias,
                            float gamma, void* stream) {
   TRY(check_shape(s));
@@ -622,6 +709,8 @@ int moe_dispatch(const moe_shape* s, const int32_t* topk_idx, const float* logit
                  int32_t* counts, int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dropped,
                  void* ws, size_t ws_bytes, void* stream) {
   TRY(check_shape(s));
+  if (expert_choice(s))
+    return fail(MOE_ERR_UNSUPPORTED, "expert-choice layers route with moe_expert_choice");
   TRY(check_ws(s, ws, ws_bytes));
   REQUIRE_PTR4(counts, "counts");
   REQUIRE_PTR4(offsets, "offsets");
@@ -672,9 +761,10 @@ int moe_grouped_swiglu(const moe_shape* s, const void* x, const int32_t* perm,
     REQUIRE_PTR(w2s, "w2s");
     REQUIRE_PTR(y_shared, "y_shared");
   }
-  TRY(run_experts(s, x, perm, offsets, topk_gate, w1, w3, w2, w1s, w3s, w2s, y_perm,
-                  s->d_ff_shared > 0 ? y_shared : nullptr, ws, static_cast<cudaStream_t>(stream),
-                  nullptr, 0));
+  const bool ec = expert_choice(s);
+  TRY(run_experts(s, x, perm, offsets, ec ? nullptr : topk_gate, ec ? topk_gate : nullptr, w1, w3,
+                  w2, w1s, w3s, w2s, y_perm, s->d_ff_shared > 0 ? y_shared : nullptr, ws,
+                  static_cast<cudaStream_t>(stream), nullptr, 0));
   return ok();
 }
 
@@ -687,7 +777,8 @@ int moe_combine(const moe_shape* s, const void* y_perm, const int32_t* inv, cons
   REQUIRE_PTR(y, "y");
   if (y_shared != nullptr && !aligned16(y_shared))
     return fail(MOE_ERR_INVALID, "y_shared is not 16-byte aligned");
-  LAUNCH(launch_combine(s->dtype, y_perm, inv, y_shared, y, s->T, s->k, s->d, num_sms(),
+  LAUNCH(launch_combine(s->dtype, y_perm, inv, y_shared, y, s->T,
+                        expert_choice(s) ? s->E : s->k, s->d, num_sms(),
                         static_cast<cudaStream_t>(stream)),
          "combine");
   return ok();

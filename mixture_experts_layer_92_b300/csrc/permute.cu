@@ -118,9 +118,15 @@ combine_kernel(const uint4* __restrict__ yp, const int32_t* __restrict__ inv,
         }
       }
     } else {
-      for (int s = 0; s < k; ++s) {
-        const int r = __ldg(slots + s);
-        if (r >= 0) {
+      // any k (e.g. the dense [T, E] inverse of expert choice): lanes read 32 slots at a
+      // time, a ballot marks the used ones, and they are added in slot order
+      for (int base = 0; base < k; base += 32) {
+        const int mine = (base + lane < k) ? __ldg(slots + base + lane) : -1;
+        unsigned used = __ballot_sync(0xffffffffu, mine >= 0);
+        while (used) {
+          const int j = __ffs(used) - 1;
+          used &= used - 1;
+          const int r = __shfl_sync(0xffffffffu, mine, j);
           const uint4* row = yp + static_cast<size_t>(r) * nvec;
           if (h0) add_chunk<BF16>(a0, __ldg(row + c0));
           if (h1) add_chunk<BF16>(a1, __ldg(row + c1));

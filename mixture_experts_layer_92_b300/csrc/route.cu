@@ -31,7 +31,8 @@ template <int JM>
 __global__ void __launch_bounds__(kRouteThreads)
 route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_stride,
                   const float* __restrict__ bias, const float* __restrict__ select_bias,
-                  float* __restrict__ logits_out, int T, int E, int k, int gate_mode,
+                  float* __restrict__ logits_out, float* __restrict__ probs_t, int T, int E,
+                  int k, int gate_mode,
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
                   float* __restrict__ partials, DeviceError* err) {
   extern __shared__ float s_part[];  // [kRouteWarps][E + 1]
@@ -82,7 +83,13 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
     }
     s = warp_sum(s);
 #pragma unroll
-    for (int j = 0; j < JM; ++j) pacc[j] += ex[j] / s;
+    for (int j = 0; j < JM; ++j) {
+      const float pj = ex[j] / s;
+      pacc[j] += pj;
+      // expert-choice routing reads the probabilities expert-major: probs_t[e][t]
+      if (probs_t != nullptr && lane + 32 * j < E)
+        probs_t[static_cast<size_t>(lane + 32 * j) * T + t] = pj;
+    }
     const float lse = m + logf(s);
     if (lane == 0) lse2 += lse * lse;
 
@@ -234,8 +241,8 @@ int launch_jm(const RouteArgs& a, cudaStream_t stream) {
   const int nb = route_blocks(a.T);
   const size_t smem = static_cast<size_t>(kRouteWarps) * (a.E + 1) * sizeof(float);
   route_topk_kernel<JM><<<nb, kRouteThreads, smem, stream>>>(
-      a.logits, a.nsplit, a.split_stride, a.bias, a.select_bias, a.logits_out, a.T, a.E, a.k,
-      a.gate_mode,
+      a.logits, a.nsplit, a.split_stride, a.bias, a.select_bias, a.logits_out, a.probs_t, a.T,
+      a.E, a.k, a.gate_mode,
       a.topk_idx, a.topk_gate, a.partials, a.err);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

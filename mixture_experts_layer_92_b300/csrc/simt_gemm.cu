@@ -65,7 +65,8 @@ __global__ void __launch_bounds__(256) simt_gemm_kernel(const SimtArgs p) {
     const int row = m0 + ty * 2 + i;
     if (row >= hi) continue;
     float scale = 1.f;
-    if (MODE == TC_SCALE && p.gate != nullptr) scale = p.gate[p.perm[row]];
+    if (MODE == TC_SCALE && p.row_gate != nullptr) scale = p.row_gate[row];
+    else if (MODE == TC_SCALE && p.gate != nullptr) scale = p.gate[p.perm[row]];
 #pragma unroll
     for (int j = 0; j < 2; ++j) {
       const int col = n0 + tx * 2 + j;

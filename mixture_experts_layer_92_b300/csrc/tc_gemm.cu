@@ -389,7 +389,10 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.shared ? args.out_shared
                                                                           : args.out_routed);
           float gscale = 1.0f;
-          if (rvalid && !t.shared && args.gate != nullptr) gscale = args.gate[args.perm[row]];
+          if (rvalid && !t.shared) {
+            if (args.row_gate != nullptr) gscale = args.row_gate[row];
+            else if (args.gate != nullptr) gscale = args.gate[args.perm[row]];
+          }
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             uint32_t v[32];

@@ -307,13 +307,24 @@ def expert_choice(logits, C: int) -> dict:
 
 def expert_choice_forward(x, w_router, w1, w3, w2, *, C: int, router_bias=None, w1s=None,
                           w3s=None, w2s=None, alpha: float = 0.01, beta: float = 1e-3,
-                          k: int = 1) -> dict:
-    """The layer with expert-choice routing, in fp64. The balance loss uses f_i = C'/(T*k)."""
+                          k: int = 1, choice=None) -> dict:
+    """The layer with expert-choice routing, in fp64. The balance loss uses f_i = C'/(T*k).
+
+    ``choice`` (perm, offsets, inv of another implementation) replaces the experts' choices;
+    the gates are then this oracle's probabilities of the given pairs."""
     x = _f64(x)
     T = x.shape[0]
     logits = router_logits(x, w_router, router_bias)
     ec = expert_choice(logits, C)
     E = logits.shape[1]
+    if choice is not None:
+        p = softmax_all(logits)
+        ec = dict(ec)
+        ec["perm"] = np.asarray(choice["perm"], dtype=np.int64)
+        ec["offsets"] = np.asarray(choice["offsets"], dtype=np.int64)
+        ec["inv"] = np.asarray(choice["inv"], dtype=np.int64).reshape(T, E)
+        owner = np.repeat(np.arange(E), np.diff(ec["offsets"]))
+        ec["gate"] = p[ec["perm"], owner]
     rows = np.zeros((ec["perm"].shape[0], x.shape[1]), dtype=np.float64)
     for e in range(E):
         lo, hi = int(ec["offsets"][e]), int(ec["offsets"][e + 1])
