@@ -78,9 +78,9 @@ __device__ __forceinline__ float warp_max(float v) {
 
 __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z)); }
 
-// silu with CUDA's fast exponential and an IEEE reciprocal, for results rounded to bf16:
-// z * 1/(1 + e^-z); e^-z = inf for very negative z gives 0.
-__device__ __forceinline__ float silu_fast(float z) { return z * __frcp_rn(1.0f + __expf(-z)); }
+// silu with CUDA's fast exponential and fast division, for results rounded to bf16:
+// z / (1 + e^-z); for very negative z, e^-z = inf and the quotient is 0.
+__device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -191,15 +191,18 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
                : "memory");
 }
 
-// Shared-memory matrix descriptor for a K-major operand tile written by TMA with
-// 128-byte swizzle: rows of 128 bytes, 8-row groups 1024 bytes apart.
-__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+// Shared-memory matrix descriptor for a K-major operand tile written by TMA with a 128- or
+// 64-byte swizzle: rows of SW bytes, 8-row groups 8*SW bytes apart. Advancing along K inside
+// a row is a plain start-address offset (the swizzle is applied to the absolute address).
+template <int SW>
+__device__ __forceinline__ uint64_t smem_desc_kmajor(uint32_t saddr) {
+  static_assert(SW == 128 || SW == 64, "128- or 64-byte swizzle");
   uint64_t d = 0;
   d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address, 16-byte units
   d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (unused)
-  d |= static_cast<uint64_t>(1024 >> 4) << 32;            // stride byte offset: 8 rows
+  d |= static_cast<uint64_t>((8 * SW) >> 4) << 32;        // stride byte offset: 8 rows
   d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
-  d |= static_cast<uint64_t>(2) << 61;                    // 128-byte swizzle
+  d |= static_cast<uint64_t>(SW == 128 ? 2 : 4) << 61;    // swizzle mode
   return d;
 }
 

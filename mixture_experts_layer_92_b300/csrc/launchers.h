@@ -54,8 +54,9 @@ struct TcProblem {
   int num_sms;
 };
 
-// mt: 128-row tiles per CTA tile (1, or 2 for TC_SWIGLU / TC_SCALE with BN = 256).
-int launch_tc_gemm(int mode, int bn, int mt, const TcProblem& p, cudaStream_t stream);
+// mt: 128-row tiles per CTA tile (1, or 2 for TC_SWIGLU / TC_SCALE with BN = 256);
+// kb: K elements per pipeline stage (64: 128-byte swizzle, 32: 64-byte swizzle).
+int launch_tc_gemm(int mode, int bn, int mt, int kb, const TcProblem& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- CUDA-core fp32 path
 struct SimtArgs {

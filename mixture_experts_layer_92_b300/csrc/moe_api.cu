@@ -242,7 +242,7 @@ int run_router(const moe_shape* s, const void* x, const void* wr, float* logits,
   p.b_groups = 1;
   p.max_tiles = static_cast<long long>((s->T + 127) / 128) * ((s->E + bn - 1) / bn) * sp.splits;
   p.num_sms = num_sms();
-  LAUNCH(launch_tc_gemm(TC_F32OUT, bn, 1, p, st), "router GEMM (tcgen05)");
+  LAUNCH(launch_tc_gemm(TC_F32OUT, bn, 1, 64, p, st), "router GEMM (tcgen05)");
   return MOE_OK;
 }
 
@@ -354,13 +354,16 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
   }
 
   // bf16: tcgen05 grouped GEMMs, routed experts and the shared expert in one launch each.
-  // 256-row CTA tiles (one weight tile feeds two MMAs, but the accumulators fill TMEM, so the
-  // epilogue is not double-buffered) pay off only when the K loop is long against the
-  // epilogue: the down projection with d_ff >= 8192 and groups averaging >= 512 rows.
-  // Everything else runs 128-row tiles with double-buffered accumulators.
+  // The kernel is bound by load latency: 256-row CTA tiles (one weight tile feeds two MMAs,
+  // twice the MMA work per staged byte) hide more of it, but fill TMEM, so their epilogue is
+  // not double-buffered, and they pull every weight tile from DRAM in one CTA instead of
+  // sharing it through L2 with a neighbour. They win when experts average >= 512 rows (and,
+  // for the down projection, with its lighter epilogue, when d_ff >= 8192); otherwise
+  // 128-row tiles with double-buffered accumulators.
   const long long kept_max = std::min<long long>(A, static_cast<long long>(s->E) * max_group_rows);
-  const int mt_gateup = 1;
+  const int mt_gateup = (kept_max / s->E >= 512) ? 2 : 1;
   const int mt_down = (kept_max / s->E >= 512 && s->d_ff >= 8192) ? 2 : 1;
+  const int kb_gateup = 64, kb_down = 64;
   auto row_tiles = [&](int mt, long long rows) { return (rows + 128 * mt - 1) / (128 * mt); };
 
   rec(ev_first + 1);
@@ -392,7 +395,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.max_tiles = (row_tiles(mt_gateup, kept_max) + s->E) * ((s->d_ff + 127) / 128) +
                   (shared ? row_tiles(mt_gateup, s->T) * ((s->d_ff_shared + 127) / 128) : 0);
     p.num_sms = sms;
-    LAUNCH(launch_tc_gemm(TC_SWIGLU, 256, mt_gateup, p, st), "gate/up GEMM (tcgen05)");
+    LAUNCH(launch_tc_gemm(TC_SWIGLU, 256, mt_gateup, kb_gateup, p, st), "gate/up GEMM (tcgen05)");
   }
   rec(ev_first + 2);
   {
@@ -425,7 +428,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.max_tiles = (row_tiles(mt_down, kept_max) + s->E + (shared ? row_tiles(mt_down, s->T) : 0)) *
                   ((s->d + bn - 1) / bn);
     p.num_sms = sms;
-    LAUNCH(launch_tc_gemm(TC_SCALE, bn, mt_down, p, st), "down GEMM (tcgen05)");
+    LAUNCH(launch_tc_gemm(TC_SCALE, bn, mt_down, kb_down, p, st), "down GEMM (tcgen05)");
   }
   return MOE_OK;
 }

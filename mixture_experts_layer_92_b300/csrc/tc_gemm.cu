@@ -46,7 +46,6 @@ namespace moe {
 namespace {
 
 constexpr int BM = 128;
-constexpr int BK = 64;
 constexpr int kMaxGroups = 1024;
 
 __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
@@ -55,15 +54,19 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
   return p;
 }
 
-template <int MODE, int BN, int MT>
+// KB: K elements per pipeline stage -- 64 (128-byte rows, 128-byte swizzle) or 32 (64-byte
+// rows, 64-byte swizzle: half the bytes per stage, twice the stages in flight).
+template <int MODE, int BN, int MT, int KB>
 struct Cfg {
+  static constexpr int BK = KB;
+  static constexpr int SW = KB * 2;                     // swizzle span = bytes per row
   static constexpr int THREADS = 64 + 128 * MT;
   static constexpr int EPI_WARPS = 4 * MT;
   static constexpr int A_BYTES = BM * BK * 2;          // one 128-row A tile
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
   static constexpr int STAGES_RAW = (196 * 1024) / STAGE_BYTES;
-  static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
   static constexpr int BN_OUT = (MODE == TC_SWIGLU) ? BN / 2 : BN;
   static constexpr int NUM_ACC = (MT == 1) ? 2 : 1;    // accumulator sets (double buffering)
   static constexpr uint32_t TMEM_COLS = pow2_at_least(NUM_ACC * MT * BN);
@@ -82,6 +85,7 @@ struct Cfg {
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N % 16 == 0, 16..256");
   static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
   static_assert((STAGE_BYTES % 1024) == 0, "stages must stay 1024-byte aligned");
+  static_assert(KB == 64 || KB == 32, "64- or 32-element k-blocks");
 };
 
 struct Tile {
@@ -97,7 +101,7 @@ struct Tile {
 
 // Tile order inside a routed group: split fastest, then row tile, then column tile, so the
 // CTAs that run at the same time share the group's weight tiles through L2.
-template <int TM>
+template <int TM, int BK>
 __device__ __forceinline__ Tile decode_tile(int tile, const int* s_off, const int* s_pre, int G,
                                             int nt_routed, int splits, const TcArgs& a) {
   Tile t;
@@ -144,16 +148,17 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* s_off, const in
   return t;
 }
 
-template <int MODE, int BN, int MT>
-__global__ void __launch_bounds__(Cfg<MODE, BN, MT>::THREADS, 1)
+template <int MODE, int BN, int MT, int KB>
+__global__ void __launch_bounds__(Cfg<MODE, BN, MT, KB>::THREADS, 1)
 tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1,
                        const __grid_constant__ CUtensorMap tmAs,
                        const __grid_constant__ CUtensorMap tmB0s,
                        const __grid_constant__ CUtensorMap tmB1s, const TcArgs args) {
-  using C = Cfg<MODE, BN, MT>;
+  using C = Cfg<MODE, BN, MT, KB>;
   constexpr int TM = MT * BM;  // rows per CTA tile
+  constexpr int BK = C::BK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -245,7 +250,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int stage = 0;
       uint32_t phase = 0;
       for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
-        const Tile t = decode_tile<TM>(tile, s_off, s_pre, G, nt_routed, splits, args);
+        const Tile t = decode_tile<TM, BK>(tile, s_off, s_pre, G, nt_routed, splits, args);
         const CUtensorMap* mA = t.shared ? &tmAs : &tmA;
         const CUtensorMap* mB0 = t.shared ? &tmB0s : &tmB0;
         const CUtensorMap* mB1 = t.shared ? &tmB1s : &tmB1;
@@ -293,7 +298,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       int it = 0;
       bool ok = true, issued_any = false;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
-        const Tile t = decode_tile<TM>(tile, s_off, s_pre, G, nt_routed, splits, args);
+        const Tile t = decode_tile<TM, BK>(tile, s_off, s_pre, G, nt_routed, splits, args);
         const bool two = (MT == 2) && (t.rows > BM);
         const int acc = it % C::NUM_ACC;
         const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
@@ -312,12 +317,13 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           const uint32_t b_addr = a_addr + MT * C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
-            const uint64_t bdesc = smem_desc_sw128(b_addr + kk * 32);
+            const uint64_t bdesc = smem_desc_kmajor<C::SW>(b_addr + kk * 32);
             const uint32_t accumulate = (kb | kk) != 0 ? 1u : 0u;
-            tc_mma_bf16(d_tmem, smem_desc_sw128(a_addr + kk * 32), bdesc, C::IDESC, accumulate);
+            tc_mma_bf16(d_tmem, smem_desc_kmajor<C::SW>(a_addr + kk * 32), bdesc, C::IDESC,
+                        accumulate);
             if (two)
-              tc_mma_bf16(d_tmem + BN, smem_desc_sw128(a_addr + C::A_BYTES + kk * 32), bdesc,
-                          C::IDESC, accumulate);
+              tc_mma_bf16(d_tmem + BN, smem_desc_kmajor<C::SW>(a_addr + C::A_BYTES + kk * 32),
+                          bdesc, C::IDESC, accumulate);
           }
           issued_any = true;
           tc_commit(&empty_bar[stage]);
@@ -347,7 +353,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                              SITE_GEMM_WAIT_TMEM_FULL))
         break;
       tc_fence_after();
-      const Tile t = decode_tile<TM>(tile, s_off, s_pre, G, nt_routed, splits, args);
+      const Tile t = decode_tile<TM, BK>(tile, s_off, s_pre, G, nt_routed, splits, args);
       // a half with no valid row was not multiplied this tile: skip it (warp-uniform)
       if (half * BM < t.rows) {
         const bool rvalid = r_local < t.rows;
@@ -477,48 +483,54 @@ bool get_encoder() {
   return g_encode != nullptr;
 }
 
-// 2-D bf16 map over a row-major [rows, inner] matrix; box = [box_rows, 64], 128-byte swizzle.
-bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+CUtensorMapSwizzle swizzle_of(int kb) {
+  return kb == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
+}
+
+// 2-D bf16 map over a row-major [rows, inner] matrix; box = [box_rows, kb], kb*2-byte swizzle.
+bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+               int kb) {
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+  cuuint32_t box[2] = {static_cast<cuuint32_t>(kb), box_rows};
   cuuint32_t es[2] = {1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kb),
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
 
-// 3-D bf16 map over [groups, rows, inner]; box = [1, box_rows, 64], 128-byte swizzle.
+// 3-D bf16 map over [groups, rows, inner]; box = [1, box_rows, kb], kb*2-byte swizzle.
 bool encode_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t groups,
-               uint32_t box_rows) {
+               uint32_t box_rows, int kb) {
   cuuint64_t dims[3] = {inner, rows, groups};
   cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(BK), box_rows, 1};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kb), box_rows, 1};
   cuuint32_t es[3] = {1, 1, 1};
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kb),
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
          CUDA_SUCCESS;
 }
 
-template <int MODE, int BN, int MT>
+template <int MODE, int BN, int MT, int KB>
 int launch_impl(const TcProblem& p, cudaStream_t stream) {
-  using C = Cfg<MODE, BN, MT>;
+  using C = Cfg<MODE, BN, MT, KB>;
   if (!get_encoder()) return MOE_ERR_CUDA;
   const int groups = p.args.groups;
   if (groups < 1 || groups > kMaxGroups) return MOE_ERR_INVALID;
   const uint32_t brows = (MODE == TC_SWIGLU) ? BN / 2 : BN;
 
   CUtensorMap mA{}, mB0{}, mB1{}, mAs{}, mB0s{}, mB1s{};
-  if (!encode_2d(&mA, p.a, p.args.k_routed, p.a_rows, BM)) return MOE_ERR_CUDA;
-  if (!encode_3d(&mB0, p.b0, p.args.k_routed, p.b_rows, p.b_groups, brows)) return MOE_ERR_CUDA;
-  if (MODE == TC_SWIGLU && !encode_3d(&mB1, p.b1, p.args.k_routed, p.b_rows, p.b_groups, brows))
+  if (!encode_2d(&mA, p.a, p.args.k_routed, p.a_rows, BM, KB)) return MOE_ERR_CUDA;
+  if (!encode_3d(&mB0, p.b0, p.args.k_routed, p.b_rows, p.b_groups, brows, KB)) return MOE_ERR_CUDA;
+  if (MODE == TC_SWIGLU &&
+      !encode_3d(&mB1, p.b1, p.args.k_routed, p.b_rows, p.b_groups, brows, KB))
     return MOE_ERR_CUDA;
   if (p.args.has_shared) {
-    if (!encode_2d(&mAs, p.a_s, p.args.k_shared, p.args.m_shared, BM)) return MOE_ERR_CUDA;
-    if (!encode_3d(&mB0s, p.b0_s, p.args.k_shared, p.b_rows_s, 1, brows)) return MOE_ERR_CUDA;
-    if (MODE == TC_SWIGLU && !encode_3d(&mB1s, p.b1_s, p.args.k_shared, p.b_rows_s, 1, brows))
+    if (!encode_2d(&mAs, p.a_s, p.args.k_shared, p.args.m_shared, BM, KB)) return MOE_ERR_CUDA;
+    if (!encode_3d(&mB0s, p.b0_s, p.args.k_shared, p.b_rows_s, 1, brows, KB)) return MOE_ERR_CUDA;
+    if (MODE == TC_SWIGLU && !encode_3d(&mB1s, p.b1_s, p.args.k_shared, p.b_rows_s, 1, brows, KB))
       return MOE_ERR_CUDA;
   }
 
@@ -529,7 +541,7 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
   static bool attr_ok[64];
   if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   std::call_once(attr_once[dev], [&]() {
-    attr_ok[dev] = cudaFuncSetAttribute(tc_grouped_gemm_kernel<MODE, BN, MT>,
+    attr_ok[dev] = cudaFuncSetAttribute(tc_grouped_gemm_kernel<MODE, BN, MT, KB>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::smem_bytes(kMaxGroups)) == cudaSuccess;
   });
@@ -537,24 +549,27 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
 
   long long grid = std::min<long long>(p.max_tiles, p.num_sms);
   if (grid < 1) return MOE_OK;
-  tc_grouped_gemm_kernel<MODE, BN, MT><<<static_cast<int>(grid), C::THREADS, smem, stream>>>(
+  tc_grouped_gemm_kernel<MODE, BN, MT, KB><<<static_cast<int>(grid), C::THREADS, smem, stream>>>(
       mA, mB0, mB1, mAs, mB0s, mB1s, p.args);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
 
-int launch_tc_gemm(int mode, int bn, int mt, const TcProblem& p, cudaStream_t stream) {
-  switch (mode * 10000 + bn * 10 + mt) {
-    case TC_SWIGLU * 10000 + 2560 + 1: return launch_impl<TC_SWIGLU, 256, 1>(p, stream);
-    case TC_SWIGLU * 10000 + 2560 + 2: return launch_impl<TC_SWIGLU, 256, 2>(p, stream);
-    case TC_SCALE * 10000 + 2560 + 1: return launch_impl<TC_SCALE, 256, 1>(p, stream);
-    case TC_SCALE * 10000 + 2560 + 2: return launch_impl<TC_SCALE, 256, 2>(p, stream);
-    case TC_F32OUT * 10000 + 160 + 1: return launch_impl<TC_F32OUT, 16, 1>(p, stream);
-    case TC_F32OUT * 10000 + 320 + 1: return launch_impl<TC_F32OUT, 32, 1>(p, stream);
-    case TC_F32OUT * 10000 + 640 + 1: return launch_impl<TC_F32OUT, 64, 1>(p, stream);
-    case TC_F32OUT * 10000 + 1280 + 1: return launch_impl<TC_F32OUT, 128, 1>(p, stream);
-    case TC_F32OUT * 10000 + 2560 + 1: return launch_impl<TC_F32OUT, 256, 1>(p, stream);
+int launch_tc_gemm(int mode, int bn, int mt, int kb, const TcProblem& p, cudaStream_t stream) {
+  switch (mode * 100000 + bn * 100 + mt * 10 + kb / 32) {
+#define MOE_TC_CASE(M, N, T, K) \
+  case M * 100000 + N * 100 + T * 10 + K / 32: return launch_impl<M, N, T, K>(p, stream);
+    MOE_TC_CASE(TC_SWIGLU, 256, 1, 64)
+    MOE_TC_CASE(TC_SWIGLU, 256, 2, 64)
+    MOE_TC_CASE(TC_SCALE, 256, 1, 64)
+    MOE_TC_CASE(TC_SCALE, 256, 2, 64)
+    MOE_TC_CASE(TC_F32OUT, 16, 1, 64)
+    MOE_TC_CASE(TC_F32OUT, 32, 1, 64)
+    MOE_TC_CASE(TC_F32OUT, 64, 1, 64)
+    MOE_TC_CASE(TC_F32OUT, 128, 1, 64)
+    MOE_TC_CASE(TC_F32OUT, 256, 1, 64)
+#undef MOE_TC_CASE
     default: return MOE_ERR_UNSUPPORTED;
   }
 }
