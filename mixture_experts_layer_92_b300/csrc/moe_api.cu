@@ -364,6 +364,20 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
   const int mt_gateup = (kept_max / s->E >= 512) ? 2 : 1;
   const int mt_down = (kept_max / s->E >= 512 && s->d_ff >= 8192) ? 2 : 1;
   const int kb_gateup = 64, kb_down = 64;
+  // Gate/up MMA width with 128-row tiles: 256 (128 H columns per tile) or 224 (112), which
+  // ever leaves fewer SMs idle in the last wave of the estimated tile count (e.g. the
+  // Mixtral-shaped decode step: 896 tiles = 6.05 waves at 256, 1024 = 6.92 waves at 224).
+  int bn_gateup = 256;
+  if (mt_gateup == 1 && s->d_ff % 112 == 0) {
+    const long long rows_e = std::max<long long>(1, (kept_max + s->E - 1) / s->E);
+    const long long row_tiles_est = ((rows_e + 127) / 128) * s->E;
+    auto wave_eff = [&](int bn_out) {
+      const long long tiles = row_tiles_est * ((s->d_ff + bn_out - 1) / bn_out);
+      const long long rounds = (tiles + sms - 1) / sms;
+      return static_cast<double>(tiles) / static_cast<double>(rounds * sms);
+    };
+    if (wave_eff(112) > wave_eff(128) + 0.02) bn_gateup = 224;
+  }
   auto row_tiles = [&](int mt, long long rows) { return (rows + 128 * mt - 1) / (128 * mt); };
 
   rec(ev_first + 1);
@@ -392,10 +406,12 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.b0_s = w1s;
     p.b1_s = w3s;
     p.b_rows_s = s->d_ff_shared;
-    p.max_tiles = (row_tiles(mt_gateup, kept_max) + s->E) * ((s->d_ff + 127) / 128) +
-                  (shared ? row_tiles(mt_gateup, s->T) * ((s->d_ff_shared + 127) / 128) : 0);
+    const int bno = bn_gateup / 2;
+    p.max_tiles = (row_tiles(mt_gateup, kept_max) + s->E) * ((s->d_ff + bno - 1) / bno) +
+                  (shared ? row_tiles(mt_gateup, s->T) * ((s->d_ff_shared + bno - 1) / bno) : 0);
     p.num_sms = sms;
-    LAUNCH(launch_tc_gemm(TC_SWIGLU, 256, mt_gateup, kb_gateup, p, st), "gate/up GEMM (tcgen05)");
+    LAUNCH(launch_tc_gemm(TC_SWIGLU, bn_gateup, mt_gateup, kb_gateup, p, st),
+           "gate/up GEMM (tcgen05)");
   }
   rec(ev_first + 2);
   {

@@ -367,25 +367,32 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (MODE == TC_SWIGLU) {
           __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.shared ? args.out_shared
                                                                           : args.out_routed);
+          // chunks of CW columns of H: gate columns [c*CW, +CW) and up columns BN/2 later
+          constexpr int CW = (C::BN_OUT % 32 == 0) ? 32 : 16;
 #pragma unroll 1
-          for (int c = 0; c < C::BN_OUT / 32; ++c) {
-            uint32_t g[32], u[32];
-            tmem_ld_32cols(tbase + c * 32, g);
-            tmem_ld_32cols(tbase + BN / 2 + c * 32, u);
+          for (int c = 0; c < C::BN_OUT / CW; ++c) {
+            uint32_t g[CW], u[CW];
+            if constexpr (CW == 32) {
+              tmem_ld_32cols(tbase + c * CW, g);
+              tmem_ld_32cols(tbase + BN / 2 + c * CW, u);
+            } else {
+              tmem_ld_16cols(tbase + c * CW, g);
+              tmem_ld_16cols(tbase + BN / 2 + c * CW, u);
+            }
             tmem_ld_wait();
             if (rvalid) {
-              uint32_t packed[16];
+              uint32_t packed[CW / 2];
 #pragma unroll
-              for (int i = 0; i < 16; ++i) {
+              for (int i = 0; i < CW / 2; ++i) {
                 const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
                 const float h1 =
                     silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
                 packed[i] = pack_bf16x2(h0, h1);
               }
-              const int col0 = col_base + c * 32;
+              const int col0 = col_base + c * CW;
               __nv_bfloat16* dst = out + row * ldo + col0;
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
+              for (int q = 0; q < CW / 8; ++q)
                 if (col0 + q * 8 < N)
                   *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
                       packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
@@ -561,6 +568,7 @@ int launch_tc_gemm(int mode, int bn, int mt, int kb, const TcProblem& p, cudaStr
 #define MOE_TC_CASE(M, N, T, K) \
   case M * 100000 + N * 100 + T * 10 + K / 32: return launch_impl<M, N, T, K>(p, stream);
     MOE_TC_CASE(TC_SWIGLU, 256, 1, 64)
+    MOE_TC_CASE(TC_SWIGLU, 224, 1, 64)
     MOE_TC_CASE(TC_SWIGLU, 256, 2, 64)
     MOE_TC_CASE(TC_SCALE, 256, 1, 64)
     MOE_TC_CASE(TC_SCALE, 256, 2, 64)

@@ -90,6 +90,7 @@ def grouped_check(T, d, E, k, F, Fs=0, cf=None, gate="softmax_topk", seed=0, idx
     (300, 200, 5, 1, 328),      # ragged K (200 = 3*64 + 8) and ragged N (328)
     (64, 512, 8, 2, 512),       # ~16 rows per expert: tiles straddle expert boundaries
     (2048, 1024, 4, 2, 1024),   # 8 row tiles per expert, persistent loop over many tiles
+    (64, 256, 8, 2, 1120),      # 1120 = 10 * 112: the 224-wide gate/up MMA (112 H columns)
 ])
 def test_grouped_swiglu_tcgen05(T, d, E, k, F):
     grouped_check(T, d, E, k, F)
