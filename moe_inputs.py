@@ -137,3 +137,13 @@ def random_logits(T: int, E: int, seed: int = 0, device="cpu", ties: bool = Fals
 def logits_with_popularity_bias(T: int, E: int, s: float, seed: int = 0, device="cpu") -> torch.Tensor:
     """fp32 logits N(0,1) plus a Zipf(s) log-popularity bias: a skewed, heavy-drop load."""
     return random_logits(T, E, seed, device) + zipf_log_popularity(E, s).to(device)
+
+
+def quantize_rows_e4m3(w: torch.Tensor):
+    """8-bit expert weights for weight streaming: per output row n, scale = max|w[n, :]| / 448
+    and codes = round-to-nearest E4M3 of w / scale (torch's float8_e4m3fn cast). Returns
+    (codes uint8, same shape as w; scales fp32, w.shape[:-1]). Works on any device."""
+    wf = w.float()
+    scale = wf.abs().amax(dim=-1).clamp_min(1e-12) / 448.0
+    codes = (wf / scale.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8)
+    return codes, scale.contiguous()

@@ -344,6 +344,31 @@ def expert_choice_forward(x, w_router, w1, w3, w2, *, C: int, router_bias=None, 
 
 
 # ---------------------------------------------------------------------------------------
+# Low-precision expert weights (weight streaming): each expert weight row n is stored as
+# 8-bit E4M3 codes q[n, :] and one scale s[n], W[n, k] = decode(q[n, k]) * s[n]. The FFN
+# is then the plain SwiGLU FFN of the decoded weights.
+# E4M3 (the OCP 8-bit float "E4M3FN"): sign bit, 4 exponent bits with bias 7, 3 mantissa
+# bits; exponent 0 encodes subnormals m/8 * 2^-6; exponent 15 with mantissa 7 is NaN; no
+# infinities; the largest finite value is 448.
+# ---------------------------------------------------------------------------------------
+def decode_e4m3(codes) -> np.ndarray:
+    """E4M3 byte codes (uint8 array) -> fp64 values."""
+    b = np.asarray(codes, dtype=np.uint8).astype(np.int64)
+    sign = np.where(b >> 7, -1.0, 1.0)
+    e = (b >> 3) & 0xF
+    m = (b & 0x7).astype(np.float64)
+    normal = (1.0 + m / 8.0) * np.exp2(e.astype(np.float64) - 7.0)
+    sub = (m / 8.0) * 2.0 ** -6
+    v = sign * np.where(e == 0, sub, normal)
+    return np.where((e == 15) & ((b & 7) == 7), np.nan, v)
+
+
+def dequantize_rows(codes, scales) -> np.ndarray:
+    """W[..., n, k] = decode(codes[..., n, k]) * scales[..., n]."""
+    return decode_e4m3(codes) * _f64(scales)[..., None]
+
+
+# ---------------------------------------------------------------------------------------
 # The whole layer, for inputs small enough to hold in fp64.
 # ---------------------------------------------------------------------------------------
 def route(logits, k: int, mode: str) -> dict:

@@ -431,3 +431,27 @@ def test_expert_choice_everyone_chosen_with_identical_experts_is_the_dense_ffn()
     out = O.expert_choice_forward(x, rng.normal(size=(E, d)), W1, W3, W2, C=T)
     np.testing.assert_allclose(out["y"], O.swiglu_ffn(x, w1, w3, w2), rtol=1e-12, atol=1e-12)
     assert out["ec"]["unrouted"] == 0
+
+
+# ---------------------------------------------------------------- 8-bit expert weights
+def test_e4m3_decode_closed_forms():
+    """Bit patterns of the E4M3 format: 1.0, 1.5, 2.0, the largest 448, the smallest normal
+    2^-6, the smallest subnormal 2^-9, signed zero, -1 and NaN."""
+    codes = np.array([0x38, 0x3C, 0x40, 0x7E, 0x08, 0x01, 0x00, 0x80, 0xB8, 0x7F, 0xFF],
+                     dtype=np.uint8)
+    v = O.decode_e4m3(codes)
+    np.testing.assert_array_equal(v[:9], [1.0, 1.5, 2.0, 448.0, 2.0 ** -6, 2.0 ** -9, 0.0, -0.0, -1.0])
+    assert np.signbit(v[7]) and np.isnan(v[9]) and np.isnan(v[10])
+
+
+def test_e4m3_decode_matches_torch_float8_on_every_code():
+    """All 256 codes against torch's own float8_e4m3fn -> float64 conversion."""
+    codes = np.arange(256, dtype=np.uint8)
+    ref = torch.from_numpy(codes).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.decode_e4m3(codes), ref)
+
+
+def test_dequantize_rows_applies_one_scale_per_row():
+    codes = np.array([[[0x38, 0x40], [0xB8, 0x3C]]], dtype=np.uint8)   # [1, 2, 2]
+    w = O.dequantize_rows(codes, np.array([[0.5, 4.0]]))
+    np.testing.assert_array_equal(w, [[[0.5, 1.0], [-4.0, 6.0]]])
