@@ -60,7 +60,7 @@ def capacity(w):
     return w.T if w.cf is None else moe_capacity(w.cf, w.T, w.k, w.E)
 
 
-def algorithmic_work(w, R: int, touched: int):
+def algorithmic_work(w, R: int, touched: int, wb=None):
     """FLOPs and bytes the method itself must compute and move for one forward.
 
     Layer: FLOPs = router 2*T*d*E + 6*d*d_ff per kept assignment (three GEMMs) + 6*d*d_ff_s
@@ -70,13 +70,18 @@ def algorithmic_work(w, R: int, touched: int):
     experts + its rows in and out; down GEMM 2*R*d*d_ff FLOPs over W2 + rows; the
     bandwidth kernels their rows in and out."""
     es = 4 if w.dtype == "f32" else 2
+    wb = es if wb is None else wb          # bytes per routed-expert weight (1: 8-bit codes)
     T, d, E, F, Fs, k = w.T, w.d, w.E, w.d_ff, w.d_ff_shared, w.k
     flops_router = 2.0 * T * d * E
     flops_gateup = 4.0 * R * d * F + 4.0 * T * d * Fs
     flops_down = 2.0 * R * d * F + 2.0 * T * d * Fs
-    bytes_gateup = (touched * 2.0 * F * d + R * d + R * F + (2.0 * Fs * d + T * d + T * Fs)) * es
-    bytes_down = (touched * 1.0 * F * d + R * F + R * d + (Fs * d + T * Fs + T * d)) * es
-    bytes_total = (T * d + E * d + touched * 3.0 * d * F + 3.0 * d * Fs + T * d) * es
+    sc = 4.0 if wb != es else 0.0          # fp32 per-row scales of 8-bit weights
+    bytes_gateup = (touched * 2.0 * F * (d * wb + sc) + (R * d + R * F + (2.0 * Fs * d + T * d
+                                                                            + T * Fs)) * es)
+    bytes_down = (touched * 1.0 * d * (F * wb + sc) + (R * F + R * d + (Fs * d + T * Fs + T * d))
+                  * es)
+    bytes_total = ((T * d + E * d + 3.0 * d * Fs + T * d) * es
+                   + touched * (3.0 * d * F * wb + (2.0 * F + d) * sc))
     return dict(flops=flops_router + flops_gateup + flops_down, bytes=bytes_total,
                 per_stage=dict(
                     router_gemm=(flops_router, (T * d + E * d) * es + T * E * 4.0),
@@ -269,10 +274,18 @@ def run_ours(args, w, rank, world, local_rank):
         dist.init_process_group("nccl", device_id=dev)
     inp = make_inputs(w, device=dev)
     C = capacity(w)
+    fp8 = None
+    if args.fp8_weights:
+        from moe_inputs import quantize_rows_e4m3
+        fp8 = {}
+        for nm in ("w1", "w3", "w2"):
+            fp8[nm + "q"], fp8[nm + "s"] = quantize_rows_e4m3(inp[nm])
+            inp[nm] = None                         # only the 8-bit copy stays resident
+        torch.cuda.empty_cache()
     layer = moe.MoELayer(inp["w_router"], inp["w1"], inp["w3"], inp["w2"], k=w.k, gate=w.gate,
                          capacity=C, router_bias=inp["router_bias"], w1s=inp["w1s"],
                          w3s=inp["w3s"], w2s=inp["w2s"], alpha=w.alpha, beta=w.beta, max_tokens=w.T,
-                         balance_gamma=args.balance_gamma)
+                         balance_gamma=args.balance_gamma, fp8=fp8)
     x = inp["x"]
     y = torch.empty_like(x)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -339,7 +352,7 @@ def run_ours(args, w, rank, world, local_rank):
             dist.destroy_process_group()
         return
     pk = peaks()
-    work = algorithmic_work(w, R, touched)
+    work = algorithmic_work(w, R, touched, wb=1 if args.fp8_weights else None)
     tokens = w.T * args.steps * world
     value = tokens / (total_ms / 1e3)
     ms_per_step = total_ms / args.steps
@@ -410,6 +423,8 @@ def main(argv=None):
     ap.add_argument("--expert-choice", action="store_true",
                     help="expert-choice routing: each expert takes C = ceil(cf*T*k/E) tokens "
                          "(cf = 1 when the workload has none)")
+    ap.add_argument("--fp8-weights", action="store_true",
+                    help="8-bit (E4M3, per-row scale) routed expert weights (weight streaming)")
     ap.add_argument("--zipf", type=float, default=None,
                     help="add a Zipf(s) log-popularity bias to the router logits (skewed load)")
     args = ap.parse_args(argv)
@@ -422,6 +437,8 @@ def main(argv=None):
         w = w.scaled(zipf_s=args.zipf, name=f"{w.name}+zipf{args.zipf}")
     if args.balance_gamma is not None:
         w = w.scaled(name=f"{w.name}+balanced")
+    if args.fp8_weights:
+        w = w.scaled(name=f"{w.name}+fp8w")
     if args.expert_choice:
         w = w.scaled(gate="expert_choice", cf=w.cf if w.cf is not None else 1.0,
                      name=f"{w.name}+expert_choice")

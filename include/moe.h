@@ -239,6 +239,34 @@ int moe_forward_balanced(const moe_shape* s, const void* x, const void* w_router
                          float gamma, void* ws, size_t ws_bytes, void* stream,
                          void* const* events, int n_events);
 
+/* Low-precision expert weights for weight streaming (8-bit E4M3, one fp32 scale per weight
+ * row): W[e][n][k] = e4m3(wq[e][n][k]) * w_scale[e][n]. The decode-sized layers are bound by
+ * the bytes of the experts they touch ("Mixture of experts (MoE)", tirogla.com, Complexity
+ * and constants: all E experts' weights stay resident; "DL S077", section 4: one Mixtral
+ * expert is 3 x 4096 x 14336 parameters), so halving those bytes halves their time.
+ *   w1q, w3q [E, d_ff, d] and w2q [E, d, d_ff] uint8 codes; w1_scale, w3_scale [E, d_ff] and
+ *   w2_scale [E, d] fp32. The tensor cores multiply fp16 copies of the weights (the E4M3 ->
+ *   fp16 expansion in shared memory is exact) by fp16 activations, and the scales are applied
+ *   to the fp32 accumulators. x (bf16) is converted to fp16 when it is gathered (exact for
+ *   |x| in [2^-14, 65504]; smaller values round to fp16's 2^-24 grid) and H is kept in fp16.
+ *   An activation or H value beyond 65504 in magnitude sets the error word to
+ *   MOE_ERR_NONFINITE (the layer's output is then not valid). x and y stay bf16.
+ *   Requires dtype bf16, d_ff_shared = 0, d and d_ff multiples of 16.
+ * moe_grouped_swiglu_fp8w: moe_grouped_swiglu (no shared expert) on 8-bit weights.
+ * moe_forward_fp8w: moe_forward on 8-bit weights (router weight stays bf16); events/n_events
+ * as in moe_forward_events, or NULL/0. */
+int moe_grouped_swiglu_fp8w(const moe_shape* s, const void* x, const int32_t* perm,
+                            const int32_t* offsets, const float* topk_gate, const uint8_t* w1q,
+                            const float* w1_scale, const uint8_t* w3q, const float* w3_scale,
+                            const uint8_t* w2q, const float* w2_scale, void* y_perm, void* ws,
+                            size_t ws_bytes, void* stream);
+int moe_forward_fp8w(const moe_shape* s, const void* x, const void* w_router,
+                     const float* router_bias, const uint8_t* w1q, const float* w1_scale,
+                     const uint8_t* w3q, const float* w3_scale, const uint8_t* w2q,
+                     const float* w2_scale, void* y, int32_t* counts, int32_t* dropped,
+                     float* losses, void* ws, size_t ws_bytes, void* stream, void* const* events,
+                     int n_events);
+
 /* moe_route_topk for precomputed logits, for callers that cannot allocate device memory.
  * (No counterpart in the pages: it is a deployment variant, not a step of the method.)
  * Some callers cannot hand the library a workspace: code running inside a host framework

@@ -14,7 +14,8 @@ import torch
 from . import _lib
 from ._lib import (MoeError, alloc_workspace, make_shape, moe_aux_loss, moe_capacity,  # noqa: F401
                    moe_check_shape, moe_clear_error, moe_combine, moe_dispatch, moe_forward,
-                   moe_forward_balanced, moe_get_error, moe_grouped_swiglu, moe_route_topk,
+                   moe_forward_balanced, moe_forward_fp8w, moe_get_error, moe_grouped_swiglu,
+                   moe_grouped_swiglu_fp8w, moe_route_topk,
                    moe_route_topk_balanced, moe_route_topk_noalloc, moe_status_string,
                    moe_update_select_bias, moe_workspace_size, NUM_STAGES, STAGE_NAMES)
 
@@ -29,19 +30,22 @@ class MoELayer:
 
     def __init__(self, w_router, w1, w3, w2, *, k: int, gate: str, capacity: Optional[int] = None,
                  router_bias=None, w1s=None, w3s=None, w2s=None, alpha=0.01, beta=1e-3,
-                 max_tokens: int, balance_gamma: Optional[float] = None):
+                 max_tokens: int, balance_gamma: Optional[float] = None, fp8: Optional[dict] = None):
         E, d = w_router.shape
         self.w = dict(w_router=w_router, w1=w1, w3=w3, w2=w2, router_bias=router_bias,
                       w1s=w1s, w3s=w3s, w2s=w2s)
-        self.E, self.d, self.k, self.d_ff = E, d, k, w1.shape[1]
+        d_ff = (w1 if w1 is not None else fp8["w1q"]).shape[1]
+        self.E, self.d, self.k, self.d_ff = E, d, k, d_ff
         self.d_ff_shared = 0 if w1s is None else w1s.shape[0]
         self.gate, self.capacity, self.alpha, self.beta = gate, capacity, alpha, beta
-        self.dtype = w1.dtype
-        self.device = w1.device
+        self.dtype = w_router.dtype
+        self.device = w_router.device
         self.ws = alloc_workspace(self.shape(max_tokens), device=self.device)
         self.counts = torch.zeros(E, dtype=torch.int32, device=self.device)
         self.dropped = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.losses = torch.zeros(2, dtype=torch.float32, device=self.device)
+        # 8-bit expert weights: dict(w1q, w1s, w3q, w3s, w2q, w2s) (E4M3 codes + per-row scales)
+        self.fp8 = fp8
         # auxiliary-loss-free balancing: a selection bias nudged by gamma after every forward
         self.balance_gamma = balance_gamma
         self.select_bias = (torch.zeros(E, dtype=torch.float32, device=self.device)
@@ -57,6 +61,13 @@ class MoELayer:
         T = x.shape[0]
         if y is None:
             y = torch.empty_like(x)
+        if self.fp8 is not None:
+            q = self.fp8
+            moe_forward_fp8w(self.shape(T), self.ws, x, self.w["w_router"], q["w1q"], q["w1s"],
+                             q["w3q"], q["w3s"], q["w2q"], q["w2s"], y,
+                             router_bias=self.w["router_bias"], counts=self.counts,
+                             dropped=self.dropped, losses=self.losses, stream=stream, events=events)
+            return y
         if self.select_bias is not None:
             moe_forward_balanced(self.shape(T), self.ws, x, self.w["w_router"], self.w["w1"],
                                  self.w["w3"], self.w["w2"], y, self.select_bias,

@@ -15,6 +15,7 @@ import torch
 LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "libmoe.so")
 
 MOE_OK = 0
+MOE_ERR_NONFINITE = -6
 STATUS = {0: "MOE_OK", -1: "MOE_ERR_INVALID", -2: "MOE_ERR_UNSUPPORTED", -3: "MOE_ERR_CUDA",
           -4: "MOE_ERR_WORKSPACE", -5: "MOE_ERR_TIMEOUT", -6: "MOE_ERR_NONFINITE"}
 GATE_MODES = {"softmax_all": 0, "softmax_topk": 1, "sigmoid_topk": 2, "expert_choice": 3}
@@ -27,7 +28,8 @@ EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_
             "moe_dispatch", "moe_grouped_swiglu", "moe_combine", "moe_aux_loss", "moe_forward",
             "moe_forward_events", "moe_get_error", "moe_clear_error", "moe_status_string",
             "moe_last_error_detail", "moe_route_topk_noalloc", "moe_route_topk_balanced",
-            "moe_update_select_bias", "moe_forward_balanced", "moe_expert_choice")
+            "moe_update_select_bias", "moe_forward_balanced", "moe_expert_choice",
+            "moe_grouped_swiglu_fp8w", "moe_forward_fp8w")
 
 
 class MoeError(RuntimeError):
@@ -74,6 +76,10 @@ def _load() -> ctypes.CDLL:
         "moe_update_select_bias": (ctypes.c_int, [sp, vp, vp, ctypes.c_float, vp]),
         "moe_expert_choice": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, sz,
                                              vp]),
+        "moe_grouped_swiglu_fp8w": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                   vp, sz, vp]),
+        "moe_forward_fp8w": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            vp, sz, vp, ctypes.POINTER(vp), ctypes.c_int]),
         "moe_forward_balanced": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                 vp, vp, ctypes.c_float, vp, sz, vp,
                                                 ctypes.POINTER(vp), ctypes.c_int]),
@@ -207,6 +213,25 @@ def moe_expert_choice(s, ws, perm, offsets, row_gate, inv, counts, unrouted, x=N
                                  _p(logits_in), _p(perm), _p(offsets), _p(row_gate), _p(inv),
                                  _p(counts), _p(unrouted), _p(stats), _p(ws), ws.numel(),
                                  _stream(stream)), "moe_expert_choice")
+
+
+def moe_grouped_swiglu_fp8w(s, ws, x, perm, offsets, w1q, w1_scale, w3q, w3_scale, w2q, w2_scale,
+                            y_perm, topk_gate=None, stream=None):
+    _check(LIB.moe_grouped_swiglu_fp8w(ctypes.byref(s), _p(x), _p(perm), _p(offsets),
+                                       _p(topk_gate), _p(w1q), _p(w1_scale), _p(w3q), _p(w3_scale),
+                                       _p(w2q), _p(w2_scale), _p(y_perm), _p(ws), ws.numel(),
+                                       _stream(stream)), "moe_grouped_swiglu_fp8w")
+
+
+def moe_forward_fp8w(s, ws, x, w_router, w1q, w1_scale, w3q, w3_scale, w2q, w2_scale, y,
+                     router_bias=None, counts=None, dropped=None, losses=None, stream=None,
+                     events=None):
+    arr = None if events is None else _event_array(events)
+    _check(LIB.moe_forward_fp8w(ctypes.byref(s), _p(x), _p(w_router), _p(router_bias), _p(w1q),
+                                _p(w1_scale), _p(w3q), _p(w3_scale), _p(w2q), _p(w2_scale), _p(y),
+                                _p(counts), _p(dropped), _p(losses), _p(ws), ws.numel(),
+                                _stream(stream), arr, 0 if events is None else len(events)),
+           "moe_forward_fp8w")
 
 
 def moe_update_select_bias(s, counts, select_bias, gamma, stream=None):

@@ -4,6 +4,7 @@
 
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <stdint.h>
@@ -33,6 +34,8 @@ enum ErrSite : int {
   SITE_GEMM_WAIT_TMEM_EMPTY = 13,
   SITE_GEMM_WAIT_DRAIN = 14,
   SITE_DISPATCH_GRID_BARRIER = 20,
+  SITE_F16_RANGE_X = 30,   // 8-bit-weight path: an activation outside fp16's finite range
+  SITE_F16_RANGE_H = 31,   //                    an H value outside fp16's finite range
 };
 
 __device__ __forceinline__ void record_error(DeviceError* e, int code, int where, int detail) {
@@ -62,6 +65,37 @@ __device__ __forceinline__ float bf16_bits_to_float(uint16_t b) {
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
   return *reinterpret_cast<uint32_t*>(&v);
+}
+
+// Codes 2P and 2P+1 of four E4M3 codes (low byte first) -> two fp16 numbers equal to the
+// codes' values divided by 256, exactly: an E4M3 code s.eeee.mmm read as fp16 bits
+// s.0eeee.mmm0000000 has the same significand and an exponent 8 lower (bias 15 against 7),
+// and E4M3 subnormals land on fp16 subnormals the same way; the factor 256 goes into the
+// weight scale. With each code c in the low byte of its 16-bit half, the fp16 bits are
+// c*128 with the sign moved from bit 14 to bit 15, i.e. V + (V & 0x4000) for V = c*128 (the
+// add carries bit 14 into bit 15). Two integer-pipe operations (a byte permute and an AND)
+// and two that the compiler can issue on the FMA pipe (the multiply and the add): the
+// conversion runs on the integer pipe, which is the bottleneck of the 8-bit path. The two
+// E4M3 NaN codes read as +-480 (this path expects finite codes).
+template <int P>
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_div256(uint32_t four_codes) {
+  const uint32_t c = __byte_perm(four_codes, 0u, P == 0 ? 0x4140u : 0x4342u);
+  const uint32_t v = c * 128u;
+  return v + (v & 0x40004000u);
+}
+
+__device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
+  const __half2 v = __floats2half2_rn(lo, hi);
+  return *reinterpret_cast<const uint32_t*>(&v);
+}
+
+// Largest finite fp16 value.
+constexpr float kF16Max = 65504.0f;
+
+// Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
+// (tensor-core operand fetches) of the same memory.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
 __device__ __forceinline__ float warp_sum(float v) {
@@ -211,6 +245,13 @@ __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N) {
   return (1u << 4)                                   // D format: f32
          | (1u << 7)                                 // A format: bf16
          | (1u << 10)                                // B format: bf16
+         | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
+         | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
+}
+
+// The same with fp16 A/B (format code 0): both operands of one MMA are fp16.
+__host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
+  return (1u << 4)                                   // D format: f32
          | (static_cast<uint32_t>(N >> 3) << 17)     // N / 8
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }

@@ -32,6 +32,8 @@ struct TcArgs {
   const float* gate;
   const float* row_gate;    // TC_SCALE: if set, row r is scaled by row_gate[r] instead
   const float* bias;        // TC_F32OUT: per-column bias or nullptr
+  const float* scale0;      // 8-bit weights: per-row scale of B0 [groups][rows] (W1 or W2)
+  const float* scale1;      //                per-row scale of B1 (W3)
   int splits;               // TC_F32OUT: split-K factor (>= 1); split s writes out + s*split_stride
   int kb_per_split;         //            k-blocks (of 64) per split
   long long split_stride;   //            elements
@@ -55,8 +57,14 @@ struct TcProblem {
 };
 
 // mt: 128-row tiles per CTA tile (1, or 2 for TC_SWIGLU / TC_SCALE with BN = 256);
-// kb: K elements per pipeline stage (64: 128-byte swizzle, 32: 64-byte swizzle).
-int launch_tc_gemm(int mode, int bn, int mt, int kb, const TcProblem& p, cudaStream_t stream);
+// kb: K elements per pipeline stage (64: 128-byte swizzle);
+// w8: B (the routed weights) are E4M3 codes with per-row scales (args.scale0/scale1),
+//     expanded to fp16 in shared memory (A is fp16 too: the gather converts it, the
+//     SwiGLU epilogue writes H as fp16); mt must be 1 and there is no shared expert;
+// ar: rows per CTA tile, 128 (times mt), or 32 with mt = 1 (short row tiles: correct for
+//     any group size, efficient when no group has more than 32 rows).
+int launch_tc_gemm(int mode, int bn, int mt, int kb, bool w8, int ar, const TcProblem& p,
+                   cudaStream_t stream);
 
 // ---------------------------------------------------------------- CUDA-core fp32 path
 struct SimtArgs {
@@ -116,8 +124,11 @@ int launch_expert_choice(const float* probs_t, int T, int E, int C, int32_t* per
                          int32_t* unrouted, cudaStream_t stream);
 
 // ---------------------------------------------------------------- data movement
+// to_f16_err != nullptr: x is bf16 and Xp is written as fp16 (the 8-bit-weight GEMMs'
+// operand); values outside fp16's range are recorded in *to_f16_err.
 int launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, int E, int k,
-                  int row_bytes, int max_rows, void* xp, int num_sms, cudaStream_t stream);
+                  int row_bytes, int max_rows, void* xp, int num_sms, cudaStream_t stream,
+                  DeviceError* to_f16_err = nullptr);
 int launch_combine(int dtype, const void* yp, const int32_t* inv, const void* ys, void* y, int T,
                    int k, int d, int num_sms, cudaStream_t stream);
 

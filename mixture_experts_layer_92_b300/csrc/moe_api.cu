@@ -242,7 +242,7 @@ int run_router(const moe_shape* s, const void* x, const void* wr, float* logits,
   p.b_groups = 1;
   p.max_tiles = static_cast<long long>((s->T + 127) / 128) * ((s->E + bn - 1) / bn) * sp.splits;
   p.num_sms = num_sms();
-  LAUNCH(launch_tc_gemm(TC_F32OUT, bn, 1, 64, p, st), "router GEMM (tcgen05)");
+  LAUNCH(launch_tc_gemm(TC_F32OUT, bn, 1, 64, false, 128, p, st), "router GEMM (tcgen05)");
   return MOE_OK;
 }
 
@@ -268,12 +268,35 @@ RouteArgs route_args(const moe_shape* s, const float* logits, int nsplit, const 
 }
 
 // ---------------------------------------------------------------- stages 4-5: expert GEMMs
+// 8-bit expert weights: E4M3 codes [E, rows, K] and one fp32 scale per row [E, rows].
+struct Fp8Weights {
+  const uint8_t *w1q, *w3q, *w2q;
+  const float *w1s, *w3s, *w2s;
+};
+
+int check_fp8(const moe_shape* s, const Fp8Weights* q) {
+  if (s->dtype != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "8-bit weights need a bf16 layer");
+  if (s->d_ff_shared != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "8-bit weights: no shared expert supported");
+  if (s->d % 16 != 0 || s->d_ff % 16 != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "8-bit weights need d and d_ff multiples of 16");
+  REQUIRE_PTR(q->w1q, "w1q");
+  REQUIRE_PTR(q->w3q, "w3q");
+  REQUIRE_PTR(q->w2q, "w2q");
+  REQUIRE_PTR4(q->w1s, "w1_scale");
+  REQUIRE_PTR4(q->w3s, "w3_scale");
+  REQUIRE_PTR4(q->w2s, "w2_scale");
+  return MOE_OK;
+}
+
 // Expert-choice layers pass row_gate (gate per row) and perm holding token indices; top-k
 // layers pass gate (per assignment, looked up through perm) and perm holding assignments.
+// q != nullptr: the routed expert weights are 8-bit (w1/w3/w2 are ignored).
 int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const int32_t* offsets,
                 const float* gate, const float* row_gate, const void* w1, const void* w3,
                 const void* w2, const void* w1s, const void* w3s, const void* w2s, void* y_perm,
-                void* y_shared, void* ws, cudaStream_t st, void* const* ev, int ev_first) {
+                void* y_shared, void* ws, cudaStream_t st, void* const* ev, int ev_first,
+                const Fp8Weights* q = nullptr) {
   const Layout L = layout(s);
   DeviceError* err = at<DeviceError>(ws, L.err);
   const int A = static_cast<int>(perm_rows(s));
@@ -292,7 +315,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
   // stage 3: gather
   rec(ev_first);
   LAUNCH(launch_gather(x, perm, offsets, s->E, gather_k, static_cast<int>(s->d * esize(s)), A, xp,
-                       sms, st),
+                       sms, st, q != nullptr ? err : nullptr),
          "gather");
 
   if (s->dtype == MOE_F32) {
@@ -361,8 +384,9 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
   // for the down projection, with its lighter epilogue, when d_ff >= 8192); otherwise
   // 128-row tiles with double-buffered accumulators.
   const long long kept_max = std::min<long long>(A, static_cast<long long>(s->E) * max_group_rows);
-  const int mt_gateup = (kept_max / s->E >= 512) ? 2 : 1;
-  const int mt_down = (kept_max / s->E >= 512 && s->d_ff >= 8192) ? 2 : 1;
+  const bool w8 = q != nullptr;  // 8-bit weights: 128-row tiles only
+  const int mt_gateup = (!w8 && kept_max / s->E >= 512) ? 2 : 1;
+  const int mt_down = (!w8 && kept_max / s->E >= 512 && s->d_ff >= 8192) ? 2 : 1;
   const int kb_gateup = 64, kb_down = 64;
   // Gate/up MMA width with 128-row tiles: 256 (128 H columns per tile) or 224 (112), which
   // ever leaves fewer SMs idle in the last wave of the estimated tile count (e.g. the
@@ -378,7 +402,15 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     };
     if (wave_eff(112) > wave_eff(128) + 0.02) bn_gateup = 224;
   }
-  auto row_tiles = [&](int mt, long long rows) { return (rows + 128 * mt - 1) / (128 * mt); };
+  // Short row tiles (32 rows of A per k-block instead of 128) when no group has more than
+  // 32 rows, e.g. a decode step: a quarter of the A bytes per stage, so more stages and
+  // more weight bytes in flight.
+  const int ar = (mt_gateup == 1 && mt_down == 1 && (shared ? s->T : max_group_rows) <= 32)
+                     ? 32 : 128;
+  auto row_tiles = [&](int mt, long long rows) {
+    const int tm = ar < 128 ? ar : 128 * mt;
+    return (rows + tm - 1) / tm;
+  };
 
   rec(ev_first + 1);
   {
@@ -389,6 +421,10 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.args.k_routed = s->d;
     p.args.out_routed = h;
     p.args.ldo_routed = s->d_ff;
+    if (w8) {
+      p.args.scale0 = q->w1s;
+      p.args.scale1 = q->w3s;
+    }
     p.args.has_shared = shared;
     p.args.m_shared = s->T;
     p.args.n_shared = s->d_ff_shared;
@@ -398,8 +434,8 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.args.err = err;
     p.a = xp;
     p.a_rows = std::max(A, 1);
-    p.b0 = w1;
-    p.b1 = w3;
+    p.b0 = w8 ? static_cast<const void*>(q->w1q) : w1;
+    p.b1 = w8 ? static_cast<const void*>(q->w3q) : w3;
     p.b_rows = s->d_ff;
     p.b_groups = s->E;
     p.a_s = x;
@@ -410,7 +446,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.max_tiles = (row_tiles(mt_gateup, kept_max) + s->E) * ((s->d_ff + bno - 1) / bno) +
                   (shared ? row_tiles(mt_gateup, s->T) * ((s->d_ff_shared + bno - 1) / bno) : 0);
     p.num_sms = sms;
-    LAUNCH(launch_tc_gemm(TC_SWIGLU, bn_gateup, mt_gateup, kb_gateup, p, st),
+    LAUNCH(launch_tc_gemm(TC_SWIGLU, bn_gateup, mt_gateup, kb_gateup, w8, ar, p, st),
            "gate/up GEMM (tcgen05)");
   }
   rec(ev_first + 2);
@@ -422,6 +458,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.args.k_routed = s->d_ff;
     p.args.out_routed = y_perm;
     p.args.ldo_routed = s->d;
+    if (w8) p.args.scale0 = q->w2s;
     p.args.has_shared = shared;
     p.args.m_shared = s->T;
     p.args.n_shared = s->d;
@@ -434,7 +471,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.args.err = err;
     p.a = h;
     p.a_rows = std::max(A, 1);
-    p.b0 = w2;
+    p.b0 = w8 ? static_cast<const void*>(q->w2q) : w2;
     p.b_rows = s->d;
     p.b_groups = s->E;
     p.a_s = hs;
@@ -444,7 +481,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.max_tiles = (row_tiles(mt_down, kept_max) + s->E + (shared ? row_tiles(mt_down, s->T) : 0)) *
                   ((s->d + bn - 1) / bn);
     p.num_sms = sms;
-    LAUNCH(launch_tc_gemm(TC_SCALE, bn, mt_down, kb_down, p, st), "down GEMM (tcgen05)");
+    LAUNCH(launch_tc_gemm(TC_SCALE, bn, mt_down, kb_down, w8, ar, p, st), "down GEMM (tcgen05)");
   }
   return MOE_OK;
 }
@@ -453,9 +490,11 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
                  const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
                  const void* w2s, void* y, int32_t* counts, int32_t* dropped, float* losses,
                  void* ws, size_t ws_bytes, void* stream, void* const* ev, int n_ev,
-                 float* select_bias = nullptr, float gamma = 0.f) {
+                 float* select_bias = nullptr, float gamma = 0.f,
+                 const Fp8Weights* q = nullptr) {
   TRY(check_shape(s));
   TRY(check_ws(s, ws, ws_bytes));
+  if (q != nullptr) TRY(check_fp8(s, q));
   if (ev != nullptr && n_ev != MOE_NUM_STAGES + 1)
     return fail(MOE_ERR_INVALID, "n_events = %d, expected %d", n_ev, MOE_NUM_STAGES + 1);
   if (ev != nullptr)
@@ -464,9 +503,11 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   if (s->T > 0) {
     REQUIRE_PTR(x, "x");
     REQUIRE_PTR(w_router, "w_router");
-    REQUIRE_PTR(w1, "w1");
-    REQUIRE_PTR(w3, "w3");
-    REQUIRE_PTR(w2, "w2");
+    if (q == nullptr) {
+      REQUIRE_PTR(w1, "w1");
+      REQUIRE_PTR(w3, "w3");
+      REQUIRE_PTR(w2, "w2");
+    }
     REQUIRE_PTR(y, "y");
     if (s->d_ff_shared > 0) {
       REQUIRE_PTR(w1s, "w1s");
@@ -525,7 +566,7 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   }
   if (s->T > 0) {
     TRY(run_experts(s, x, perm, off, ec ? nullptr : gate, ec ? gate : nullptr, w1, w3, w2, w1s,
-                    w3s, w2s, yp, ys, ws, st, ev, 3));
+                    w3s, w2s, yp, ys, ws, st, ev, 3, q));
   } else {
     rec(3);
     rec(4);
@@ -696,6 +737,40 @@ int moe_expert_choice(const moe_shape* s, const void* x, const void* w_router,
                               inv, counts, offsets, unrouted, st),
          "expert choice");
   return ok();
+}
+
+int moe_grouped_swiglu_fp8w(const moe_shape* s, const void* x, const int32_t* perm,
+                            const int32_t* offsets, const float* topk_gate, const uint8_t* w1q,
+                            const float* w1_scale, const uint8_t* w3q, const float* w3_scale,
+                            const uint8_t* w2q, const float* w2_scale, void* y_perm, void* ws,
+                            size_t ws_bytes, void* stream) {
+  TRY(check_shape(s));
+  TRY(check_ws(s, ws, ws_bytes));
+  const Fp8Weights q{w1q, w3q, w2q, w1_scale, w3_scale, w2_scale};
+  TRY(check_fp8(s, &q));
+  if (s->T == 0) return ok();
+  REQUIRE_PTR(x, "x");
+  REQUIRE_PTR4(perm, "perm");
+  REQUIRE_PTR4(offsets, "offsets");
+  OPT_PTR4(topk_gate, "topk_gate");
+  REQUIRE_PTR(y_perm, "y_perm");
+  const bool ec = expert_choice(s);
+  TRY(run_experts(s, x, perm, offsets, ec ? nullptr : topk_gate, ec ? topk_gate : nullptr, nullptr,
+                  nullptr, nullptr, nullptr, nullptr, nullptr, y_perm, nullptr, ws,
+                  static_cast<cudaStream_t>(stream), nullptr, 0, &q));
+  return ok();
+}
+
+int moe_forward_fp8w(const moe_shape* s, const void* x, const void* w_router,
+                     const float* router_bias, const uint8_t* w1q, const float* w1_scale,
+                     const uint8_t* w3q, const float* w3_scale, const uint8_t* w2q,
+                     const float* w2_scale, void* y, int32_t* counts, int32_t* dropped,
+                     float* losses, void* ws, size_t ws_bytes, void* stream, void* const* events,
+                     int n_events) {
+  const Fp8Weights q{w1q, w3q, w2q, w1_scale, w3_scale, w2_scale};
+  return forward_impl(s, x, w_router, router_bias, nullptr, nullptr, nullptr, nullptr, nullptr,
+                      nullptr, y, counts, dropped, losses, ws, ws_bytes, stream, events,
+                      events ? n_events : 0, nullptr, 0.f, &q);
 }
 
 int moe_update_select_bias(const moe_shape* s, const int32_t* counts, float* select_bias,

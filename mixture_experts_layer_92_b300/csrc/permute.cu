@@ -45,6 +45,35 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm
   }
 }
 
+// Gather with a bf16 -> fp16 conversion (operand of the 8-bit-weight GEMMs). A value outside
+// fp16's finite range records MOE_ERR_NONFINITE (site SITE_F16_RANGE_X, detail = row).
+__device__ __forceinline__ uint32_t bf16x2_to_f16x2(uint32_t w, bool& bad) {
+  const float lo = __uint_as_float(w << 16), hi = __uint_as_float(w & 0xffff0000u);
+  bad |= fabsf(lo) > kF16Max || fabsf(hi) > kF16Max;
+  return pack_f16x2(lo, hi);
+}
+
+__global__ void __launch_bounds__(kMoveThreads)
+gather_rows_f16_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
+                       const int32_t* __restrict__ offsets, int E, int k, int nvec,
+                       uint4* __restrict__ xp, DeviceError* err) {
+  const int R = offsets[E];
+  const int lane = threadIdx.x & 31;
+  const int nw = gridDim.x * kMoveWarps;
+  for (int r = blockIdx.x * kMoveWarps + (threadIdx.x >> 5); r < R; r += nw) {
+    const int t = perm[r] / k;
+    const uint4* src = x + static_cast<size_t>(t) * nvec;
+    uint4* dst = xp + static_cast<size_t>(r) * nvec;
+    bool bad = false;
+    for (int i = lane; i < nvec; i += 32) {
+      const uint4 v = __ldg(src + i);
+      dst[i] = make_uint4(bf16x2_to_f16x2(v.x, bad), bf16x2_to_f16x2(v.y, bad),
+                          bf16x2_to_f16x2(v.z, bad), bf16x2_to_f16x2(v.w, bad));
+    }
+    if (bad) record_error(err, MOE_ERR_NONFINITE, SITE_F16_RANGE_X, r);
+  }
+}
+
 __device__ __forceinline__ void add_bf16x8(float (&acc)[8], const uint4 v) {
   const uint32_t w[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
@@ -153,10 +182,16 @@ int grid_for_rows(long long rows, int num_sms) {
 }  // namespace
 
 int launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, int E, int k,
-                  int row_bytes, int max_rows, void* xp, int num_sms, cudaStream_t stream) {
+                  int row_bytes, int max_rows, void* xp, int num_sms, cudaStream_t stream,
+                  DeviceError* to_f16_err) {
   if (max_rows <= 0) return MOE_OK;
-  gather_rows_kernel<<<grid_for_rows(max_rows, num_sms), kMoveThreads, 0, stream>>>(
-      static_cast<const uint4*>(x), perm, offsets, E, k, row_bytes / 16, static_cast<uint4*>(xp));
+  if (to_f16_err != nullptr)
+    gather_rows_f16_kernel<<<grid_for_rows(max_rows, num_sms), kMoveThreads, 0, stream>>>(
+        static_cast<const uint4*>(x), perm, offsets, E, k, row_bytes / 16, static_cast<uint4*>(xp),
+        to_f16_err);
+  else
+    gather_rows_kernel<<<grid_for_rows(max_rows, num_sms), kMoveThreads, 0, stream>>>(
+        static_cast<const uint4*>(x), perm, offsets, E, k, row_bytes / 16, static_cast<uint4*>(xp));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

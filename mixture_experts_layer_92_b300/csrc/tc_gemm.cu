@@ -23,6 +23,12 @@
 // last row tile of a group may have only its first half valid: then the second half is
 // neither loaded nor multiplied.
 //
+// Short row tiles (AR = 32, used when no group has more than 32 rows, e.g. a decode step):
+// only 32 rows of A are loaded per k-block (4 KB instead of 16 KB), so more stages fit and
+// more weight bytes stay in flight. The M=128 MMA still reads a 16 KB A window; its rows
+// 32..127 are the bytes that follow inside the same stage (already landed), and the
+// accumulator rows they produce are never stored.
+//
 // Roles (one CTA per SM, persistent over tiles):
 //   warp 0 lane 0  TMA producer: A tiles 128 x 64 and a B tile BN x 64 (bf16, 128-byte
 //                  swizzle) into a STAGES-deep shared-memory ring;
@@ -31,7 +37,16 @@
 //                  i+1; MT = 2 uses all 512 columns for the two row halves;
 //   warps 2..      epilogue, 4 warps per row half: tcgen05.ld (each warp reads its 32-lane
 //                  quarter of TMEM), element-wise math, predicated 16-byte global stores
-//                  (rows past the group's end are masked: A tiles may straddle two experts).
+//                  (rows past the group's end are masked: A tiles may straddle two experts);
+//   (W8) 8 warps   converters: E4M3 weight tile in the TMA ring -> fp16 tile in a separate
+//                  2-slot ring that the MMA reads, so the TMA ring holds only A and the
+//                  8-bit staging and keeps more weight bytes in flight. The conversion is
+//                  the 8-bit path's bottleneck (integer-pipe issue), so it is a bit
+//                  placement of four operations per weight pair that yields value / 256 in
+//                  fp16 (the 256 is folded into the scale); bf16 operands would need a
+//                  real conversion. So the 8-bit path runs its MMAs on fp16 operands: the
+//                  gather converts the activations to fp16 and the SwiGLU epilogue writes H
+//                  as fp16.
 // Every mbarrier wait is bounded (common.cuh): on a timeout the kernel records
 // MOE_ERR_TIMEOUT in the workspace error word, drains its own copies and MMAs, frees TMEM
 // and returns.
@@ -56,25 +71,37 @@ __host__ __device__ constexpr uint32_t pow2_at_least(uint32_t v) {
 
 // KB: K elements per pipeline stage -- 64 (128-byte rows, 128-byte swizzle) or 32 (64-byte
 // rows, 64-byte swizzle: half the bytes per stage, twice the stages in flight).
-template <int MODE, int BN, int MT, int KB>
+// W8: the B operand arrives as E4M3 codes (one byte per element) in the TMA stage and
+// CONV_WARPS converter warps expand it to fp16 in a slot of the conversion ring.
+// AR: rows of A loaded per k-block, 128 or 32 (short row tiles, MT = 1 only).
+template <int MODE, int BN, int MT, int KB, bool W8 = false, int AR = 128>
 struct Cfg {
   static constexpr int BK = KB;
   static constexpr int SW = KB * 2;                     // swizzle span = bytes per row
-  static constexpr int THREADS = 64 + 128 * MT;
   static constexpr int EPI_WARPS = 4 * MT;
-  static constexpr int A_BYTES = BM * BK * 2;          // one 128-row A tile
-  static constexpr int B_BYTES = BN * BK * 2;
-  static constexpr int STAGE_BYTES = MT * A_BYTES + B_BYTES;
-  static constexpr int STAGES_RAW = (196 * 1024) / STAGE_BYTES;
+  static constexpr int CONV_WARPS = W8 ? 8 : 0;
+  static constexpr int THREADS = 64 + 32 * (EPI_WARPS + CONV_WARPS);
+  static constexpr int TM = (AR < BM) ? AR : MT * BM;   // rows per CTA tile
+  static constexpr int A_BYTES = AR * BK * 2;           // one A tile as loaded
+  static constexpr int B_BYTES = BN * BK * 2;           // 16-bit B tile (the MMA operand)
+  static constexpr int B8_BYTES = W8 ? BN * BK : 0;     // 8-bit B tile as loaded
+  // TMA ring: A tile(s) then the B tile (bf16, or 8-bit for W8)
+  static constexpr int STAGE_BYTES = MT * A_BYTES + (W8 ? B8_BYTES : B_BYTES);
+  // conversion ring (W8): fp16 B tiles written by the converters, read by the MMA
+  static constexpr int CSTAGES = W8 ? 2 : 0;
+  static constexpr int CSTAGE_BYTES = W8 ? B_BYTES : 0;
+  static constexpr int STAGES_RAW = (196 * 1024 - CSTAGES * CSTAGE_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 12 ? 12 : STAGES_RAW;
   static constexpr int BN_OUT = (MODE == TC_SWIGLU) ? BN / 2 : BN;
   static constexpr int NUM_ACC = (MT == 1) ? 2 : 1;    // accumulator sets (double buffering)
   static constexpr uint32_t TMEM_COLS = pow2_at_least(NUM_ACC * MT * BN);
-  static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+  static constexpr uint32_t IDESC = W8 ? idesc_f16_f32(BM, BN) : idesc_bf16_f32(BM, BN);
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int OFF_TILES = 0;
-  static constexpr int OFF_BARS = STAGES * STAGE_BYTES;
-  static constexpr int NUM_BARS = 2 * STAGES + 5;  // full, empty, tmem_full[2], tmem_empty[2], drain
+  static constexpr int OFF_CONV = STAGES * STAGE_BYTES;
+  static constexpr int OFF_BARS = OFF_CONV + CSTAGES * CSTAGE_BYTES;
+  // full, empty, tmem_full[2], tmem_empty[2], drain, converted[CSTAGES], conv_free[CSTAGES]
+  static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * CSTAGES;
   static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;     // tmem slot, abort flag
   static constexpr int OFF_TABLE = OFF_MISC + 16;              // offsets[G+1], prefix[G+1]
   static constexpr int smem_bytes(int groups) {
@@ -86,6 +113,10 @@ struct Cfg {
   static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
   static_assert((STAGE_BYTES % 1024) == 0, "stages must stay 1024-byte aligned");
   static_assert(KB == 64 || KB == 32, "64- or 32-element k-blocks");
+  static_assert(!W8 || (MT == 1 && KB == 64), "8-bit weights use 128-row tiles, 64-wide k");
+  static_assert(AR == BM || (MT == 1 && AR % 8 == 0 && AR >= 8), "short row tiles: MT = 1");
+  static_assert(STAGE_BYTES >= BM * BK * 2, "the MMA's 128-row A window stays in its stage");
+  static_assert((CSTAGE_BYTES % 1024) == 0, "conversion slots stay 1024-byte aligned");
 };
 
 struct Tile {
@@ -148,16 +179,16 @@ __device__ __forceinline__ Tile decode_tile(int tile, const int* s_off, const in
   return t;
 }
 
-template <int MODE, int BN, int MT, int KB>
-__global__ void __launch_bounds__(Cfg<MODE, BN, MT, KB>::THREADS, 1)
+template <int MODE, int BN, int MT, int KB, bool W8, int AR>
+__global__ void __launch_bounds__(Cfg<MODE, BN, MT, KB, W8, AR>::THREADS, 1)
 tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0,
                        const __grid_constant__ CUtensorMap tmB1,
                        const __grid_constant__ CUtensorMap tmAs,
                        const __grid_constant__ CUtensorMap tmB0s,
                        const __grid_constant__ CUtensorMap tmB1s, const TcArgs args) {
-  using C = Cfg<MODE, BN, MT, KB>;
-  constexpr int TM = MT * BM;  // rows per CTA tile
+  using C = Cfg<MODE, BN, MT, KB, W8, AR>;
+  constexpr int TM = C::TM;  // rows per CTA tile
   constexpr int BK = C::BK;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -169,6 +200,9 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   uint64_t* tfull_bar = bars + 2 * C::STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* drain_bar = tfull_bar + 4;
+  uint64_t* conv_full = tfull_bar + 5;            // [CSTAGES], W8 only
+  uint64_t* conv_empty = conv_full + C::CSTAGES;  // [CSTAGES], W8 only
+  uint8_t* conv_tiles = smem + C::OFF_CONV;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::OFF_MISC + 4);
   int* s_off = reinterpret_cast<int*>(smem + C::OFF_TABLE);
@@ -190,6 +224,10 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       mbar_init(&tempty_bar[a], C::EPI_WARPS);
     }
     mbar_init(drain_bar, 1);
+    for (int s = 0; s < C::CSTAGES; ++s) {
+      mbar_init(&conv_full[s], C::CONV_WARPS);
+      mbar_init(&conv_empty[s], 1);
+    }
     *abort_flag = 0;
     fence_barrier_init();
   }
@@ -255,7 +293,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         const CUtensorMap* mB0 = t.shared ? &tmB0s : &tmB0;
         const CUtensorMap* mB1 = t.shared ? &tmB1s : &tmB1;
         const bool two = (MT == 2) && (t.rows > BM);
-        const uint32_t bytes = C::B_BYTES + (two ? 2 : 1) * C::A_BYTES;
+        const uint32_t bytes = (W8 ? C::B8_BYTES : C::B_BYTES) + (two ? 2 : 1) * C::A_BYTES;
         bool ok = true;
         for (int kb = t.kb0; kb < t.kb0 + t.nk; ++kb) {
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, err,
@@ -270,8 +308,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           if (two) tma_load_2d(sa + C::A_BYTES, mA, &full_bar[stage], kb * BK, t.row0 + BM);
           if (MODE == TC_SWIGLU) {
             tma_load_3d(sb, mB0, &full_bar[stage], kb * BK, t.n_blk * (BN / 2), t.group);
-            tma_load_3d(sb + C::B_BYTES / 2, mB1, &full_bar[stage], kb * BK, t.n_blk * (BN / 2),
-                        t.group);
+            tma_load_3d(sb + (W8 ? C::B8_BYTES : C::B_BYTES) / 2, mB1, &full_bar[stage], kb * BK,
+                        t.n_blk * (BN / 2), t.group);
           } else {
             tma_load_3d(sb, mB0, &full_bar[stage], kb * BK, t.n_blk * BN, t.group);
           }
@@ -293,8 +331,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
   } else if (warp == 1) {
     // ================= MMA issuer =================
     if (lane == 0) {
-      int stage = 0;
-      uint32_t phase = 0;
+      int stage = 0, cstage = 0;
+      uint32_t phase = 0, cphase = 0;
       int it = 0;
       bool ok = true, issued_any = false;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
@@ -308,13 +346,16 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MT * BN);
         for (int kb = 0; kb < t.nk; ++kb) {
-          if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, err, SITE_GEMM_WAIT_FULL)) {
+          // W8: the converters waited for this stage's copies before filling the slot
+          if (!mbar_wait_bounded(W8 ? &conv_full[cstage] : &full_bar[stage], W8 ? cphase : phase,
+                                 abort_flag, err, SITE_GEMM_WAIT_FULL)) {
             ok = false;
             break;
           }
           tc_fence_after();
           const uint32_t a_addr = smem_u32(tiles + stage * C::STAGE_BYTES);
-          const uint32_t b_addr = a_addr + MT * C::A_BYTES;
+          const uint32_t b_addr =
+              W8 ? smem_u32(conv_tiles + cstage * C::CSTAGE_BYTES) : a_addr + MT * C::A_BYTES;
 #pragma unroll
           for (int kk = 0; kk < BK / 16; ++kk) {
             const uint64_t bdesc = smem_desc_kmajor<C::SW>(b_addr + kk * 32);
@@ -331,6 +372,13 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             stage = 0;
             phase ^= 1;
           }
+          if (W8) {
+            tc_commit(&conv_empty[cstage]);
+            if (++cstage == C::CSTAGES) {
+              cstage = 0;
+              cphase ^= 1;
+            }
+          }
         }
         if (ok) tc_commit(&tfull_bar[acc]);
       }
@@ -339,6 +387,69 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         tc_commit(drain_bar);
         mbar_wait_bounded(drain_bar, 0, nullptr, err, SITE_GEMM_WAIT_DRAIN);
       }
+    }
+  } else if (W8 && warp >= 2 + C::EPI_WARPS) {
+    // ================= converters (8-bit weights) =================
+    // Expand the staged E4M3 B tile (row r at r*64 bytes) to fp16 in the 128-byte swizzled
+    // layout the MMA reads (16-byte chunk j of row r at chunk j ^ (r % 8)).
+    const int ct = threadIdx.x - (2 + C::EPI_WARPS) * 32;
+    int stage = 0, cstage = 0;
+    uint32_t phase = 0, cphase = 0;
+    for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
+      const Tile t = decode_tile<TM, BK>(tile, s_off, s_pre, G, nt_routed, splits, args);
+      bool ok = true;
+      for (int kb = 0; kb < t.nk; ++kb) {
+        if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, err, SITE_GEMM_WAIT_FULL) ||
+            !mbar_wait_bounded(&conv_empty[cstage], cphase ^ 1, abort_flag, err,
+                               SITE_GEMM_WAIT_EMPTY)) {
+          ok = false;
+          break;
+        }
+        const uint8_t* s8 = tiles + stage * C::STAGE_BYTES + MT * C::A_BYTES;
+        uint8_t* sb = conv_tiles + cstage * C::CSTAGE_BYTES;
+        // 16-byte chunk q of the staged tile holds row q / 4, bytes 16 * (q % 4) ..; every
+        // thread issues all its loads before converting, so several are in flight
+        constexpr int CT = 32 * (C::CONV_WARPS > 0 ? C::CONV_WARPS : 1);
+        constexpr int CHUNKS = BN * 4;
+        constexpr int PER = (CHUNKS + CT - 1) / CT;
+        uint4 v[PER];
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+          const int q = ct + j * CT;
+          if (q < CHUNKS) v[j] = *reinterpret_cast<const uint4*>(s8 + q * 16);
+        }
+#pragma unroll
+        for (int j = 0; j < PER; ++j) {
+          const int q = ct + j * CT;
+          if (q < CHUNKS) {
+            const int r = q >> 2, c = 2 * (q & 3);
+            const uint32_t w[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+            uint32_t o[8];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              o[2 * i] = e4m3x2_to_f16x2_div256<0>(w[i]);
+              o[2 * i + 1] = e4m3x2_to_f16x2_div256<1>(w[i]);
+            }
+            uint8_t* row = sb + r * 128;
+            *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
+                make_uint4(o[0], o[1], o[2], o[3]);
+            *reinterpret_cast<uint4*>(row + (((c + 1) ^ (r & 7)) << 4)) =
+                make_uint4(o[4], o[5], o[6], o[7]);
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&conv_full[cstage]);
+        if (++stage == C::STAGES) {
+          stage = 0;
+          phase ^= 1;
+        }
+        if (++cstage == C::CSTAGES) {
+          cstage = 0;
+          cphase ^= 1;
+        }
+      }
+      if (!ok) break;
     }
   } else {
     // ================= epilogue (warps 2 .. 2 + 4*MT - 1) =================
@@ -354,8 +465,9 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         break;
       tc_fence_after();
       const Tile t = decode_tile<TM, BK>(tile, s_off, s_pre, G, nt_routed, splits, args);
-      // a half with no valid row was not multiplied this tile: skip it (warp-uniform)
-      if (half * BM < t.rows) {
+      // a half with no valid row was not multiplied this tile, and a warp whose 32 rows are
+      // all past the tile's end has nothing to store: skip (warp-uniform)
+      if (half * BM < t.rows && half * BM + quarter * 32 < t.rows) {
         const bool rvalid = r_local < t.rows;
         const long long row = static_cast<long long>(t.row0) + r_local;
         const int N = t.shared ? args.n_shared : args.n_routed;
@@ -381,15 +493,36 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             tmem_ld_wait();
             if (rvalid) {
+              const int col0 = col_base + c * CW;
+              if (W8) {
+                // per-row weight scales of W1 and W3 (times the 256 the converters divided
+                // out), applied before the SiLU
+                const float* s1 = args.scale0 + static_cast<size_t>(t.group) * N + col0;
+                const float* s3 = args.scale1 + static_cast<size_t>(t.group) * N + col0;
+#pragma unroll
+                for (int i = 0; i < CW; ++i) {
+                  const bool in = col0 + i < N;
+                  g[i] = __float_as_uint(__uint_as_float(g[i]) * (in ? 256.f * __ldg(s1 + i) : 0.f));
+                  u[i] = __float_as_uint(__uint_as_float(u[i]) * (in ? 256.f * __ldg(s3 + i) : 0.f));
+                }
+              }
               uint32_t packed[CW / 2];
+              bool out_of_range = false;
 #pragma unroll
               for (int i = 0; i < CW / 2; ++i) {
                 const float h0 = silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]);
                 const float h1 =
                     silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]);
-                packed[i] = pack_bf16x2(h0, h1);
+                if (W8) {
+                  // H is the down projection's fp16 operand
+                  out_of_range |= fabsf(h0) > kF16Max || fabsf(h1) > kF16Max;
+                  packed[i] = pack_f16x2(h0, h1);
+                } else {
+                  packed[i] = pack_bf16x2(h0, h1);
+                }
               }
-              const int col0 = col_base + c * CW;
+              if (W8 && out_of_range)
+                record_error(args.err, MOE_ERR_NONFINITE, SITE_F16_RANGE_H, static_cast<int>(row));
               __nv_bfloat16* dst = out + row * ldo + col0;
 #pragma unroll
               for (int q = 0; q < CW / 8; ++q)
@@ -412,12 +545,21 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             tmem_ld_32cols(tbase + c * 32, v);
             tmem_ld_wait();
             if (rvalid) {
+              const int col0 = col_base + c * 32;
+              if (W8) {
+                // per-row scale of W2 (one per output column of the down projection), times
+                // the 256 the converters divided out
+                const float* s2 = args.scale0 + static_cast<size_t>(t.group) * N + col0;
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                  v[i] = __float_as_uint(__uint_as_float(v[i]) *
+                                         (col0 + i < N ? 256.f * __ldg(s2 + i) : 0.f));
+              }
               uint32_t packed[16];
 #pragma unroll
               for (int i = 0; i < 16; ++i)
                 packed[i] = pack_bf16x2(gscale * __uint_as_float(v[2 * i]),
                                         gscale * __uint_as_float(v[2 * i + 1]));
-              const int col0 = col_base + c * 32;
               __nv_bfloat16* dst = out + row * ldo + col0;
 #pragma unroll
               for (int q = 0; q < 4; ++q)
@@ -520,22 +662,48 @@ bool encode_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, 
          CUDA_SUCCESS;
 }
 
-template <int MODE, int BN, int MT, int KB>
+// 3-D uint8 map over [groups, rows, inner] bytes (8-bit weights); box = [1, box_rows, kb],
+// no swizzle (the converters read it row by row).
+bool encode_3d_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t groups,
+                  uint32_t box_rows, int kb) {
+  cuuint64_t dims[3] = {inner, rows, groups};
+  cuuint64_t strides[2] = {inner, inner * rows};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(kb), box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
+                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+template <int MODE, int BN, int MT, int KB, bool W8, int AR>
 int launch_impl(const TcProblem& p, cudaStream_t stream) {
-  using C = Cfg<MODE, BN, MT, KB>;
+  using C = Cfg<MODE, BN, MT, KB, W8, AR>;
   if (!get_encoder()) return MOE_ERR_CUDA;
   const int groups = p.args.groups;
   if (groups < 1 || groups > kMaxGroups) return MOE_ERR_INVALID;
   const uint32_t brows = (MODE == TC_SWIGLU) ? BN / 2 : BN;
 
   CUtensorMap mA{}, mB0{}, mB1{}, mAs{}, mB0s{}, mB1s{};
-  if (!encode_2d(&mA, p.a, p.args.k_routed, p.a_rows, BM, KB)) return MOE_ERR_CUDA;
-  if (!encode_3d(&mB0, p.b0, p.args.k_routed, p.b_rows, p.b_groups, brows, KB)) return MOE_ERR_CUDA;
-  if (MODE == TC_SWIGLU &&
-      !encode_3d(&mB1, p.b1, p.args.k_routed, p.b_rows, p.b_groups, brows, KB))
-    return MOE_ERR_CUDA;
+  if (!encode_2d(&mA, p.a, p.args.k_routed, p.a_rows, AR, KB)) return MOE_ERR_CUDA;
+  if (W8) {
+    if (p.args.has_shared || p.args.scale0 == nullptr ||
+        (MODE == TC_SWIGLU && p.args.scale1 == nullptr))
+      return MOE_ERR_INVALID;
+    if (!encode_3d_u8(&mB0, p.b0, p.args.k_routed, p.b_rows, p.b_groups, brows, KB))
+      return MOE_ERR_CUDA;
+    if (MODE == TC_SWIGLU &&
+        !encode_3d_u8(&mB1, p.b1, p.args.k_routed, p.b_rows, p.b_groups, brows, KB))
+      return MOE_ERR_CUDA;
+  } else {
+    if (!encode_3d(&mB0, p.b0, p.args.k_routed, p.b_rows, p.b_groups, brows, KB))
+      return MOE_ERR_CUDA;
+    if (MODE == TC_SWIGLU &&
+        !encode_3d(&mB1, p.b1, p.args.k_routed, p.b_rows, p.b_groups, brows, KB))
+      return MOE_ERR_CUDA;
+  }
   if (p.args.has_shared) {
-    if (!encode_2d(&mAs, p.a_s, p.args.k_shared, p.args.m_shared, BM, KB)) return MOE_ERR_CUDA;
+    if (!encode_2d(&mAs, p.a_s, p.args.k_shared, p.args.m_shared, AR, KB)) return MOE_ERR_CUDA;
     if (!encode_3d(&mB0s, p.b0_s, p.args.k_shared, p.b_rows_s, 1, brows, KB)) return MOE_ERR_CUDA;
     if (MODE == TC_SWIGLU && !encode_3d(&mB1s, p.b1_s, p.args.k_shared, p.b_rows_s, 1, brows, KB))
       return MOE_ERR_CUDA;
@@ -548,7 +716,7 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
   static bool attr_ok[64];
   if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   std::call_once(attr_once[dev], [&]() {
-    attr_ok[dev] = cudaFuncSetAttribute(tc_grouped_gemm_kernel<MODE, BN, MT, KB>,
+    attr_ok[dev] = cudaFuncSetAttribute(tc_grouped_gemm_kernel<MODE, BN, MT, KB, W8, AR>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::smem_bytes(kMaxGroups)) == cudaSuccess;
   });
@@ -556,30 +724,40 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
 
   long long grid = std::min<long long>(p.max_tiles, p.num_sms);
   if (grid < 1) return MOE_OK;
-  tc_grouped_gemm_kernel<MODE, BN, MT, KB><<<static_cast<int>(grid), C::THREADS, smem, stream>>>(
+  tc_grouped_gemm_kernel<MODE, BN, MT, KB, W8, AR><<<static_cast<int>(grid), C::THREADS, smem,
+                                                     stream>>>(
       mA, mB0, mB1, mAs, mB0s, mB1s, p.args);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
 
-int launch_tc_gemm(int mode, int bn, int mt, int kb, const TcProblem& p, cudaStream_t stream) {
-  switch (mode * 100000 + bn * 100 + mt * 10 + kb / 32) {
-#define MOE_TC_CASE(M, N, T, K) \
-  case M * 100000 + N * 100 + T * 10 + K / 32: return launch_impl<M, N, T, K>(p, stream);
-    MOE_TC_CASE(TC_SWIGLU, 256, 1, 64)
-    MOE_TC_CASE(TC_SWIGLU, 224, 1, 64)
-    MOE_TC_CASE(TC_SWIGLU, 256, 2, 64)
-    MOE_TC_CASE(TC_SCALE, 256, 1, 64)
-    MOE_TC_CASE(TC_SCALE, 256, 2, 64)
-    MOE_TC_CASE(TC_F32OUT, 16, 1, 64)
-    MOE_TC_CASE(TC_F32OUT, 32, 1, 64)
-    MOE_TC_CASE(TC_F32OUT, 64, 1, 64)
-    MOE_TC_CASE(TC_F32OUT, 128, 1, 64)
-    MOE_TC_CASE(TC_F32OUT, 256, 1, 64)
+int launch_tc_gemm(int mode, int bn, int mt, int kb, bool w8, int ar, const TcProblem& p,
+                   cudaStream_t stream) {
+#define MOE_TC_CASE(M, N, T, K, W, R)                                             \
+  if (mode == M && bn == N && mt == T && kb == K && w8 == (W != 0) && ar == R) \
+    return launch_impl<M, N, T, K, W != 0, R>(p, stream);
+  MOE_TC_CASE(TC_SWIGLU, 256, 1, 64, 0, 128)
+  MOE_TC_CASE(TC_SWIGLU, 224, 1, 64, 0, 128)
+  MOE_TC_CASE(TC_SWIGLU, 256, 2, 64, 0, 128)
+  MOE_TC_CASE(TC_SWIGLU, 256, 1, 64, 0, 32)
+  MOE_TC_CASE(TC_SWIGLU, 224, 1, 64, 0, 32)
+  MOE_TC_CASE(TC_SCALE, 256, 1, 64, 0, 128)
+  MOE_TC_CASE(TC_SCALE, 256, 2, 64, 0, 128)
+  MOE_TC_CASE(TC_SCALE, 256, 1, 64, 0, 32)
+  MOE_TC_CASE(TC_SWIGLU, 256, 1, 64, 1, 128)
+  MOE_TC_CASE(TC_SWIGLU, 224, 1, 64, 1, 128)
+  MOE_TC_CASE(TC_SWIGLU, 256, 1, 64, 1, 32)
+  MOE_TC_CASE(TC_SWIGLU, 224, 1, 64, 1, 32)
+  MOE_TC_CASE(TC_SCALE, 256, 1, 64, 1, 128)
+  MOE_TC_CASE(TC_SCALE, 256, 1, 64, 1, 32)
+  MOE_TC_CASE(TC_F32OUT, 16, 1, 64, 0, 128)
+  MOE_TC_CASE(TC_F32OUT, 32, 1, 64, 0, 128)
+  MOE_TC_CASE(TC_F32OUT, 64, 1, 64, 0, 128)
+  MOE_TC_CASE(TC_F32OUT, 128, 1, 64, 0, 128)
+  MOE_TC_CASE(TC_F32OUT, 256, 1, 64, 0, 128)
 #undef MOE_TC_CASE
-    default: return MOE_ERR_UNSUPPORTED;
-  }
+  return MOE_ERR_UNSUPPORTED;
 }
 
 }  // namespace moe

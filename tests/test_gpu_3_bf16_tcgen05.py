@@ -111,6 +111,19 @@ def test_grouped_swiglu_tcgen05_capacity_and_shared():
     grouped_check(500, 256, 8, 2, 256, Fs=128, cf=0.75, gate="sigmoid_topk", seed=3)
 
 
+@pytest.mark.parametrize("T,d,E,k,F,Fs,cf", [
+    (32, 256, 8, 2, 1120, 0, None),   # decode-sized: every expert <= 32 rows, 224-wide MMA
+    (1, 256, 4, 2, 512, 0, None),     # one token: two 1-row groups, two empty ones
+    (32, 512, 8, 2, 512, 128, None),  # with the shared expert (32 rows)
+    (20, 200, 5, 1, 328, 0, None),    # ragged K (200) and N (328)
+    (200, 256, 8, 2, 256, 0, 0.5),    # C = 25: many tokens, every group cut to <= 25 rows
+])
+def test_grouped_swiglu_tcgen05_short_row_tiles(T, d, E, k, F, Fs, cf):
+    """No group above 32 rows: the GEMMs load 32-row A tiles (the MMA's other 96 rows read
+    bytes of the same stage and are never stored)."""
+    grouped_check(T, d, E, k, F, Fs=Fs, cf=cf, seed=T)
+
+
 def layer_check(w, seed=0, sample=None):
     inp = dev_inputs(w, seed=seed)
     C = capacity_of(w)
