@@ -14,6 +14,10 @@ of all ranks' tokens divided by the slowest rank's time (weak scaling).
 
 --impl reference times the CPU oracle (fp64 numpy, oracle/) on bounded samples of the same
 workload on this host's cores; under torchrun only rank 0 runs it.
+
+--backward times a training step instead: moe_forward followed by moe_backward (all input
+and weight gradients of sum(dy*y) + L_aux + L_z, dy synthetic and seeded), with the per-stage
+events of both and the roofline of the dominant backward kernel.
 """
 from __future__ import annotations
 
@@ -228,6 +232,22 @@ def cpu_baseline(w, inp_host: dict, target_s: float = 15.0):
                        f"that batch, fp64 numpy), {t:.2f} s")
 
 
+def oracle_train_sample(w, inp_host: dict, dy_host, n_tokens: int):
+    """The CPU oracle's forward and backward on the first n_tokens tokens; returns seconds."""
+    import oracle as O
+    C = w.T if w.cf is None else O.capacity(w.cf, n_tokens, w.k, w.E)
+    t0 = time.perf_counter()
+    O.forward(inp_host["x"][:n_tokens], inp_host["w_router"], inp_host["w1"], inp_host["w3"],
+              inp_host["w2"], k=w.k, mode=w.gate, C=min(C, n_tokens),
+              router_bias=inp_host["router_bias"], w1s=inp_host["w1s"], w3s=inp_host["w3s"],
+              w2s=inp_host["w2s"], alpha=w.alpha, beta=w.beta)
+    O.backward(inp_host["x"][:n_tokens], inp_host["w_router"], inp_host["w1"], inp_host["w3"],
+               inp_host["w2"], dy_host[:n_tokens], k=w.k, mode=w.gate, C=min(C, n_tokens),
+               router_bias=inp_host["router_bias"], w1s=inp_host["w1s"], w3s=inp_host["w3s"],
+               w2s=inp_host["w2s"], alpha=w.alpha, beta=w.beta)
+    return time.perf_counter() - t0
+
+
 def run_reference(args, w, rank):
     if rank != 0:
         return
@@ -409,6 +429,210 @@ def run_ours(args, w, rank, world, local_rank):
         dist.destroy_process_group()
 
 
+# ------------------------------------------------------------------------------ training step
+TRAIN_METRIC = "MoE layer fwd+bwd (training step) tokens/sec (1 B300) + % of BF16 tensor / HBM roofline"
+BWD_STAGES = ("route_dispatch", "gather_x_dy", "recompute_gu", "gemm_dh_swiglu_bwd",
+              "gate_logit_grads", "gemm_dx", "dx_combine", "gemm_wgrad")
+BWD_DOMINANT = "gemm_wgrad"
+
+
+def backward_work(w, R: int, touched: int):
+    """FLOPs and bytes of one moe_backward, per stage (the same conventions as
+    algorithmic_work). GEMM FLOPs: recomputed G|U 4RdF, dH 2RdF, dX 4RdF, weight gradients
+    6RdF (+ the shared expert's over T rows, + router dx and dW_r 2TdE each)."""
+    es = 2
+    T, d, E, F, Fs, k = w.T, w.d, w.E, w.d_ff, w.d_ff_shared, w.k
+    wts = touched * 3.0 * d * F * es + 3.0 * d * Fs * es
+    per = dict(
+        route_dispatch=(2.0 * T * d * E, (T * d + E * d) * es + T * E * 8.0 + T * k * 16.0),
+        gather_x_dy=(0.0, (2 * R * d + 3 * R * d) * es),
+        recompute_gu=(4.0 * d * (R * F + T * Fs),
+                      touched * 2.0 * F * d * es + 2.0 * Fs * d * es + (R * d + 2 * R * F
+                                                                        + T * d + 2 * T * Fs) * es),
+        gemm_dh_swiglu_bwd=(2.0 * d * (R * F + T * Fs),
+                            touched * d * F * es + Fs * d * es + (R * d + 5 * R * F
+                                                                  + T * d + 5 * T * Fs) * es),
+        gate_logit_grads=(0.0, T * k * 8.0 + T * E * 14.0),
+        gemm_dx=(4.0 * d * (R * F + T * Fs) + 2.0 * T * E * d,
+                 touched * 2.0 * F * d * es + 2.0 * Fs * d * es + (2 * R * F + R * d + 2 * T * Fs
+                                                                   + 2 * T * d) * es),
+        dx_combine=(0.0, (R * d + 3 * T * d) * es),
+        gemm_wgrad=(6.0 * d * (R * F + T * Fs) + 2.0 * T * E * d,
+                    (R * (2 * F + 2 * d + F) + T * (3 * Fs + 2 * d)) * es + (E * 3.0 * d * F
+                                                                              + 3.0 * d * Fs + E * d) * 4.0))
+    flops = sum(v[0] for v in per.values())
+    nbytes = wts + (2 * T * d * es) + (E * 3.0 * d * F + 3.0 * d * Fs + E * d) * 4.0
+    return dict(flops=flops, bytes=nbytes, per_stage=per)
+
+
+def run_train(args, w, rank, world, local_rank):
+    import mixture_experts_layer_92_b300 as moe
+    from mixture_experts_layer_92_b300 import _lib as L
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    dist = None
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    inp = make_inputs(w, device=dev)
+    C = capacity(w)
+    gen = torch.Generator(device=dev).manual_seed(1)
+    dy = torch.randn(inp["x"].shape, generator=gen, device=dev).to(inp["x"].dtype)
+    layer = moe.MoELayer(inp["w_router"], inp["w1"], inp["w3"], inp["w2"], k=w.k, gate=w.gate,
+                         capacity=C, router_bias=inp["router_bias"], w1s=inp["w1s"],
+                         w3s=inp["w3s"], w2s=inp["w2s"], alpha=w.alpha, beta=w.beta, max_tokens=w.T)
+    s = layer.shape(w.T)
+    bws = L.alloc_workspace_backward(s, dev)
+    f32 = dict(device=dev, dtype=torch.float32)
+    grads = dict(dx=torch.empty_like(inp["x"]), dw_router=torch.empty((w.E, w.d), **f32),
+                 dw1=torch.empty((w.E, w.d_ff, w.d), **f32), dw3=torch.empty((w.E, w.d_ff, w.d), **f32),
+                 dw2=torch.empty((w.E, w.d, w.d_ff), **f32))
+    if w.d_ff_shared:
+        grads.update(dw1s=torch.empty((w.d_ff_shared, w.d), **f32),
+                     dw3s=torch.empty((w.d_ff_shared, w.d), **f32),
+                     dw2s=torch.empty((w.d, w.d_ff_shared), **f32))
+    x = inp["x"]
+    y = torch.empty_like(x)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def backward(xx, dyy, events=None):
+        L.moe_backward(s, bws, xx, inp["w_router"], inp["w1"], inp["w3"], inp["w2"], dyy,
+                       grads["dx"], grads["dw_router"], grads["dw1"], grads["dw3"], grads["dw2"],
+                       router_bias=inp["router_bias"], w1s=inp["w1s"], w3s=inp["w3s"],
+                       w2s=inp["w2s"], dw1s=grads.get("dw1s"), dw3s=grads.get("dw3s"),
+                       dw2s=grads.get("dw2s"), events=events)
+
+    fevs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
+            for _ in range(args.steps)]
+    bevs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(BWD_STAGES) + 1)]
+            for _ in range(args.steps)]
+
+    def barrier():
+        if dist is not None:
+            dist.barrier()
+        torch.cuda.synchronize(dev)
+
+    visible = [v for v in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if v.strip()]
+    sampler = ClockSampler(visible[local_rank] if local_rank < len(visible) else local_rank)
+    sampler.start()
+    for _ in range(args.warmup):
+        flush.zero_()
+        layer.forward(x, y)
+        backward(x, dy)
+    barrier()
+    for i in range(args.steps):
+        flush.zero_()
+        layer.forward(x, y, events=fevs[i])
+        backward(x, dy, events=bevs[i])
+    barrier()
+    for ws in (layer.ws, bws):
+        if moe.moe_get_error(ws) != 0:
+            raise RuntimeError("device error")
+    step_ms = [fevs[i][0].elapsed_time(bevs[i][-1]) for i in range(args.steps)]
+    fwd_ms = [fevs[i][0].elapsed_time(fevs[i][-1]) for i in range(args.steps)]
+    bwd_ms = [bevs[i][0].elapsed_time(bevs[i][-1]) for i in range(args.steps)]
+    bstage_ms = {name: [bevs[i][j].elapsed_time(bevs[i][j + 1]) for i in range(args.steps)]
+                 for j, name in enumerate(BWD_STAGES)}
+    total_ms = sum(step_ms)
+
+    # end to end: x and dy from pinned host memory in, y and dx out, every step
+    xh, dyh = x.cpu().pin_memory(), dy.cpu().pin_memory()
+    yh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    dxh = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+    xd, dyd = torch.empty_like(x), torch.empty_like(dy)
+
+    def e2e_step():
+        xd.copy_(xh, non_blocking=True)
+        dyd.copy_(dyh, non_blocking=True)
+        layer.forward(xd, y)
+        backward(xd, dyd)
+        yh.copy_(y, non_blocking=True)
+        dxh.copy_(grads["dx"], non_blocking=True)
+
+    for _ in range(args.warmup):
+        e2e_step()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        e2e_step()
+    e1.record(stream)
+    barrier()
+    sampler.stop()
+    e2e_ms = e0.elapsed_time(e1)
+    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    total_ms, e2e_ms = t.tolist()
+    counts = layer.counts.cpu().numpy()
+    R = int(np.minimum(counts, C).sum())
+    touched = int((counts > 0).sum())
+    if rank != 0:
+        if dist is not None:
+            dist.barrier()
+            dist.destroy_process_group()
+        return
+    pk = peaks()
+    fw = algorithmic_work(w, R, touched)
+    bw = backward_work(w, R, touched)
+    tokens = w.T * args.steps * world
+    stages = {name: stage_roofline(*bw["per_stage"][name], statistics.mean(bstage_ms[name]), pk)
+              for name in BWD_STAGES}
+    dom = stages[BWD_DOMINANT]
+    roofline = dict(bound=dom["bound"], kernel=BWD_DOMINANT, achieved=dom["achieved"],
+                    peak=dom["peak"], unit=dom["unit"], frac=dom["frac"],
+                    traffic=traffic_from_profile(w.name + "+train", BWD_DOMINANT),
+                    peak_source=f"{pk['source']} " + ("bf16 burst" if dom["bound"] == "tensor"
+                                                      else "HBM copy"),
+                    algorithmic_per_step=dom["algorithmic"],
+                    note="gemm_wgrad = all weight-gradient GEMM launches of one backward")
+    flops = fw["flops"] + bw["flops"]
+    nbytes = fw["bytes"] + bw["bytes"]
+    ms_per_step = total_ms / args.steps
+    t_roof = max(flops / (pk["bf16_tflops"] * 1e12), nbytes / (pk["hbm_gbs"] * 1e9))
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        ih = host_inputs(inp)
+        dyh64 = dy.float().cpu().numpy()
+        n = min(w.T, 4)
+        tt = oracle_train_sample(w, ih, dyh64, n)
+        n2 = int(min(w.T, max(n, n * args.cpu_seconds / max(tt, 1e-3) * 0.8)))
+        if n2 > n:
+            tt = oracle_train_sample(w, ih, dyh64, n2)
+            n = n2
+        cpu = dict(value=n / tt, unit=UNIT, cores=oracle_threads(), kind="oracle",
+                   sample=f"first {n} tokens of {w.name}: oracle forward + backward (fp64 numpy), "
+                          f"{tt:.2f} s")
+    es = x.element_size()
+    clk = sampler.summary()
+    line = dict(
+        metric=TRAIN_METRIC, value=tokens / (total_ms / 1e3), unit=UNIT, n_gpus=world,
+        steps=args.steps, warmup=args.warmup, ms_per_step=ms_per_step, higher_is_better=True,
+        scaling="weak", vs_baseline=None, dtype=w.dtype,
+        data="synthetic (seeded; random-init weights; dy ~ N(0,1))",
+        config=dict(workload=w.name + "+train", T=w.T, d=w.d, E=w.E, k=w.k, d_ff=w.d_ff,
+                    d_ff_shared=w.d_ff_shared, gate=w.gate, capacity=C,
+                    l2="flushed between timed steps (256 MiB write, outside the events)",
+                    kept_assignments=R, experts_touched=touched,
+                    forward_ms=statistics.mean(fwd_ms), backward_ms=statistics.mean(bwd_ms)),
+        roofline=roofline,
+        layer_roofline=dict(flops=flops, bytes=nbytes, roofline_ms=t_roof * 1e3,
+                            measured_ms=ms_per_step, frac=t_roof * 1e3 / ms_per_step),
+        stages=stages, cpu_baseline=cpu,
+        e2e=dict(value=tokens / (e2e_ms / 1e3), unit=UNIT, h2d_bytes_per_step=2 * w.T * w.d * es,
+                 d2h_bytes_per_step=2 * w.T * w.d * es,
+                 note="per step: x and dy (pinned) -> device, forward, backward, y and dx -> host; "
+                      "the weight gradients stay on the device"),
+        gpu_launches=(launches_per_forward(w) + 15 + (4 if w.d_ff_shared else 0)) * args.steps,
+        clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"], reasons=clk["reasons"],
+                    samples=clk["samples"]))
+    print(json.dumps(line), flush=True)
+    if dist is not None:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
 def main(argv=None):
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -425,6 +649,8 @@ def main(argv=None):
                          "(cf = 1 when the workload has none)")
     ap.add_argument("--fp8-weights", action="store_true",
                     help="8-bit (E4M3, per-row scale) routed expert weights (weight streaming)")
+    ap.add_argument("--backward", action="store_true",
+                    help="time a training step: moe_forward + moe_backward")
     ap.add_argument("--zipf", type=float, default=None,
                     help="add a Zipf(s) log-popularity bias to the router logits (skewed load)")
     args = ap.parse_args(argv)
@@ -444,6 +670,9 @@ def main(argv=None):
                      name=f"{w.name}+expert_choice")
     if args.impl == "reference":
         run_reference(args, w, rank)
+        return
+    if args.backward:
+        run_train(args, w, rank, world, local_rank)
         return
     run_ours(args, w, rank, world, local_rank)
 

@@ -267,6 +267,51 @@ int moe_forward_fp8w(const moe_shape* s, const void* x, const void* w_router,
                      float* losses, void* ws, size_t ws_bytes, void* stream, void* const* events,
                      int n_events);
 
+/* Backward pass (training) of the layer moe_forward computes, for top-k bf16 layers.
+ * It returns the gradient of
+ *     J = sum_t dy_t . y_t + d_aux * L_aux + d_z * L_z
+ * with respect to every input of the layer, the routing decisions (top-k selection and
+ * dispatch, i.e. which assignments are kept) held at their forward values. The load
+ * fraction f_i carries no gradient and the mean router probability P_i does ("Mixture of
+ * experts (MoE)", tirogla.com, How it works, step 6). The gradients follow the chain rule
+ * through the forward's steps: score l = x W_r^T + b, gates (step 1's three conventions),
+ * the SwiGLU experts ("DL S077", section 1.1: O = w2 (silu(w1 x) * w3 x)), the combine
+ * y_t = sum g O (step 5) and the two balance losses (step 6).
+ *   Inputs: the forward's inputs (x, w_router, router_bias, w1, w3, w2 and the shared
+ *   expert's w1s, w3s, w2s, with the layouts of moe_forward), dy [T, d] bf16, and the loss
+ *   weights d_aux, d_z (host scalars; 1 for the plain sum of the losses).
+ *   Outputs (overwritten, not accumulated): dx [T, d] bf16; dw_router [E, d], dw1 and
+ *   dw3 [E, d_ff, d], dw2 [E, d, d_ff] fp32; the shared expert's dw1s, dw3s [d_ff_shared, d]
+ *   and dw2s [d, d_ff_shared] fp32 (required when d_ff_shared > 0, else ignored);
+ *   d_router_bias [E] fp32 (nullable); dlogits [T, E] and dgate [T, k] fp32 (nullable: the
+ *   intermediate gradients of the logits and of the gates, 0 for dropped assignments).
+ *   An expert that receives no rows gets a zero gradient; T = 0 zeroes every gradient.
+ *   Nothing is saved between calls: the call recomputes the routing, the dispatch and the
+ *   pre-activations G = Xp w1^T, U = Xp w3^T on the tensor cores, then runs the backward
+ *   GEMMs (dH = dy w2 with the SwiGLU backward in its epilogue, dXp = dG w1 + dU w3, and per
+ *   expert dW1 = dG^T Xp, dW3 = dU^T Xp, dW2 = (g dy)^T H; the router's dx = dl W_r and
+ *   dW_r = dl^T x), reading transposed operands MN-major instead of transposing them.
+ *   Precision: bf16 operands, fp32 accumulation; G, U, H, dG, dU, g dy and the logit
+ *   gradient (as a GEMM operand) are rounded to bf16; weight gradients are fp32.
+ *   Requires dtype bf16, top-k gating (not expert choice), d, d_ff and d_ff_shared
+ *   multiples of 64 and E a multiple of 8 (else MOE_ERR_UNSUPPORTED); the workspace is
+ *   moe_backward_workspace_size(s) bytes (a superset of the forward's; its first 256 bytes
+ *   zero before first use, like the forward's).
+ *   events/n_events: NULL/0, or MOE_NUM_BWD_STAGES + 1 CUDA events recorded before each
+ *   stage and after the last: 0 routing + dispatch, 1 gathers of x and dy, 2 recomputed
+ *   G | U, 3 dH GEMMs, 4 gate and logit gradients, 5 dX GEMMs, 6 dx combine, 7 weight
+ *   gradient GEMMs.
+ * Device pointers; asynchronous on `stream`; host-side argument errors return before any
+ * launch, device-side errors go to the workspace error word (moe_get_error). */
+#define MOE_NUM_BWD_STAGES 8
+size_t moe_backward_workspace_size(const moe_shape* s);
+int moe_backward(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
+                 const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
+                 const void* w2s, const void* dy, float d_aux, float d_z, void* dx,
+                 float* dw_router, float* d_router_bias, float* dw1, float* dw3, float* dw2,
+                 float* dw1s, float* dw3s, float* dw2s, float* dlogits, float* dgate, void* ws,
+                 size_t ws_bytes, void* stream, void* const* events, int n_events);
+
 /* moe_route_topk for precomputed logits, for callers that cannot allocate device memory.
  * (No counterpart in the pages: it is a deployment variant, not a step of the method.)
  * Some callers cannot hand the library a workspace: code running inside a host framework

@@ -17,7 +17,8 @@ from ._lib import (MoeError, alloc_workspace, make_shape, moe_aux_loss, moe_capa
                    moe_forward_balanced, moe_forward_fp8w, moe_get_error, moe_grouped_swiglu,
                    moe_grouped_swiglu_fp8w, moe_route_topk,
                    moe_route_topk_balanced, moe_route_topk_noalloc, moe_status_string,
-                   moe_update_select_bias, moe_workspace_size, NUM_STAGES, STAGE_NAMES)
+                   moe_update_select_bias, moe_workspace_size, NUM_STAGES, STAGE_NAMES,
+                   alloc_workspace_backward, moe_backward, moe_backward_workspace_size)
 
 
 class MoELayer:

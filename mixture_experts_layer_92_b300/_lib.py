@@ -29,7 +29,11 @@ EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_
             "moe_forward_events", "moe_get_error", "moe_clear_error", "moe_status_string",
             "moe_last_error_detail", "moe_route_topk_noalloc", "moe_route_topk_balanced",
             "moe_update_select_bias", "moe_forward_balanced", "moe_expert_choice",
-            "moe_grouped_swiglu_fp8w", "moe_forward_fp8w")
+            "moe_grouped_swiglu_fp8w", "moe_forward_fp8w", "moe_backward_workspace_size",
+            "moe_backward")
+NUM_BWD_STAGES = 8
+BWD_STAGE_NAMES = ("route_dispatch", "gather_x_dy", "recompute_gu", "gemm_dh_swiglu_bwd",
+                   "gate_logit_grads", "gemm_dx", "dx_combine", "gemm_wgrad")
 
 
 class MoeError(RuntimeError):
@@ -83,6 +87,10 @@ def _load() -> ctypes.CDLL:
         "moe_forward_balanced": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                 vp, vp, ctypes.c_float, vp, sz, vp,
                                                 ctypes.POINTER(vp), ctypes.c_int]),
+        "moe_backward_workspace_size": (sz, [sp]),
+        "moe_backward": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
+                                        ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                        vp, sz, vp, ctypes.POINTER(vp), ctypes.c_int]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -141,6 +149,33 @@ def alloc_workspace(s: moe_shape, device="cuda") -> torch.Tensor:
     ws = torch.zeros(n + 256, dtype=torch.uint8, device=device)
     off = (-ws.data_ptr()) % 256
     return ws[off:off + n]
+
+
+def moe_backward_workspace_size(s: moe_shape) -> int:
+    return LIB.moe_backward_workspace_size(ctypes.byref(s))
+
+
+def alloc_workspace_backward(s: moe_shape, device="cuda") -> torch.Tensor:
+    """Zero-filled uint8 device buffer of moe_backward_workspace_size bytes."""
+    n = moe_backward_workspace_size(s)
+    if n == 0:
+        raise MoeError(-2, "moe_backward_workspace_size", "shape not supported by the backward pass")
+    ws = torch.zeros(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def moe_backward(s, ws, x, w_router, w1, w3, w2, dy, dx, dw_router, dw1, dw3, dw2,
+                 router_bias=None, w1s=None, w3s=None, w2s=None, d_aux=1.0, d_z=1.0,
+                 d_router_bias=None, dw1s=None, dw3s=None, dw2s=None, dlogits=None, dgate=None,
+                 stream=None, events=None):
+    arr = None if events is None else _event_array(events)
+    _check(LIB.moe_backward(ctypes.byref(s), _p(x), _p(w_router), _p(router_bias), _p(w1), _p(w3),
+                            _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(dy), float(d_aux), float(d_z),
+                            _p(dx), _p(dw_router), _p(d_router_bias), _p(dw1), _p(dw3), _p(dw2),
+                            _p(dw1s), _p(dw3s), _p(dw2s), _p(dlogits), _p(dgate), _p(ws), ws.numel(),
+                            _stream(stream), arr, 0 if events is None else len(events)),
+           "moe_backward")
 
 
 def moe_route_topk(s, ws, topk_idx, topk_gate, x=None, w_router=None, router_bias=None,

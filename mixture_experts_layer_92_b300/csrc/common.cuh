@@ -256,6 +256,27 @@ __host__ __device__ constexpr uint32_t idesc_f16_f32(int M, int N) {
          | (static_cast<uint32_t>(M >> 4) << 24);    // M / 16
 }
 
+// Shared-memory matrix descriptor for an MN-major operand tile written by TMA with a 128-byte
+// swizzle as 64-element-wide chunks (boxes of [64 K rows, 64 M/N elements]): inside a chunk
+// K row k sits at k*128 bytes and 8-row groups are 1024 bytes apart (stride byte offset);
+// the chunks lie `chunk_bytes` apart along M/N (leading byte offset). Advancing K by 16 is
+// a start-address offset of 2048 bytes.
+__device__ __forceinline__ uint64_t smem_desc_mn_sw128(uint32_t saddr, uint32_t chunk_bytes) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);            // start address
+  d |= static_cast<uint64_t>((chunk_bytes >> 4) & 0x3FFFu) << 16;  // leading byte offset
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;                     // stride byte offset
+  d |= static_cast<uint64_t>(1) << 46;                             // descriptor version
+  d |= static_cast<uint64_t>(2) << 61;                             // 128-byte swizzle
+  return d;
+}
+
+// Operand major-ness bits of the kind::f16 instruction descriptor: A (bit 15) and B (bit 16)
+// read MN-major instead of K-major.
+__host__ __device__ constexpr uint32_t idesc_major(bool a_mn, bool b_mn) {
+  return (a_mn ? 1u << 15 : 0u) | (b_mn ? 1u << 16 : 0u);
+}
+
 __device__ __forceinline__ void tc_mma_bf16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
                                             uint32_t idesc, uint32_t accumulate) {
   asm volatile(

@@ -37,6 +37,9 @@ struct TcArgs {
   int splits;               // TC_F32OUT: split-K factor (>= 1); split s writes out + s*split_stride
   int kb_per_split;         //            k-blocks (of 64) per split
   long long split_stride;   //            elements
+  void* gu_routed;          // TC_SWIGLU, optional: the pre-activations G = A.W1^T and U = A.W3^T
+  void* gu_shared;          //   as bf16 [rows, 2N] (G in columns 0..N-1, U in N..2N-1); out_* may
+                            //   then be nullptr (H not written)
   DeviceError* err;
 };
 
@@ -65,6 +68,68 @@ struct TcProblem {
 //     any group size, efficient when no group has more than 32 rows).
 int launch_tc_gemm(int mode, int bn, int mt, int kb, bool w8, int ar, const TcProblem& p,
                    cudaStream_t stream);
+
+// ---------------------------------------------------------------- tcgen05 backward GEMMs
+enum BwdMode : int {
+  BW_DGRAD_H = 0,  // dH = dY.W2 (B = W2 read MN-major) + SwiGLU backward and dgate partials
+  BW_DGRAD_X = 1,  // dX = [dG dU].[W1; W3] (B = W1 / W3 read MN-major), bf16 out
+  BW_WGRAD = 2,    // dW[g] = A_g^T . B_g over the rows of group g (both read MN-major), fp32 out
+};
+
+struct BwdArgs {
+  int groups;               // row groups (expert segments), 1..1024
+  const int32_t* offsets;   // device [groups+1] row offsets, or nullptr: one group of m_single
+  int m_single;
+  int M;                    // BW_WGRAD: output rows (A's columns)
+  int N;                    // output columns
+  int K;                    // DGRAD: reduction length (A's columns)
+  int k_split;              // BW_DGRAD_X: k < k_split reads B0 (W1), k >= k_split reads B1 (W3)
+  void* out;                // DGRAD_X: bf16 [rows, N] (ldo); WGRAD: fp32 [groups, m_split, N]
+  long long ldo;
+  void* out1;               // WGRAD: rows m >= m_split go to out1 [groups, M - m_split, N]
+  int m_split;
+  // BW_DGRAD_H epilogue
+  const void* gu;           // G | U of the forward, bf16 [rows, 2N]
+  void* dgu;                // out: dG | dU, bf16 [rows, 2N]
+  void* h;                  // out: H = silu(G) U, bf16 [rows, N]
+  float* dg_part;           // out (nullable): per row and column tile, sum_f dH_raw * H
+  int n_tiles;              //   [rows, n_tiles]
+  const int32_t* perm;      // gate of row r = gate[perm[r]] (gate == nullptr: 1)
+  const float* gate;
+  DeviceError* err;
+};
+
+struct BwdProblem {
+  BwdArgs args;
+  const void* a;            // A: DGRAD [a_rows, K] K-major; WGRAD [a_rows, a_inner] MN-major
+  long long a_rows, a_inner;
+  const void* b0;           // DGRAD: weights [b_groups, b_rows, b_inner]; WGRAD: [b_rows, b_inner]
+  const void* b1;           // DGRAD_X: W3 (same shape as b0)
+  long long b_rows, b_inner;
+  int b_groups;
+  long long max_tiles;
+  int num_sms;
+};
+
+int launch_bwd_gemm(int mode, int bn, const BwdProblem& p, cudaStream_t stream);
+
+// Non-GEMM steps of the backward pass (backward.cu)
+// dyp[r] = dy[perm[r] / k], dO[r] = gate[perm[r]] * dy[perm[r] / k] (bf16), r < offsets[E]
+int launch_gather_dy(const void* dy, const int32_t* perm, const int32_t* offsets, const float* gate,
+                     int E, int k, int d, int max_rows, void* dyp, void* dO, int num_sms,
+                     cudaStream_t stream);
+// dgate[a] = sum_j dg_part[inv[a]][j] (fixed order), 0 for a dropped assignment
+int launch_dgate(const float* dg_part, int n_tiles, const int32_t* inv, int A, float* dgate,
+                 cudaStream_t stream);
+// dl = dJ/dlogits [T, E] (fp32, and a bf16 copy) from the gate, balance and z-loss terms
+int launch_dlogits(const float* logits, const int32_t* idx, const float* dgate,
+                   const int32_t* counts, int T, int E, int k, int gate_mode, float alpha,
+                   float beta, float d_aux, float d_z, float* dl, void* dl16, cudaStream_t stream);
+// out[e] = sum over t (in order) of dl[t][e]
+int launch_column_sum(const float* dl, int T, int E, float* out, cudaStream_t stream);
+// dx[t] = sum_s [inv >= 0] dxp[inv[t*k+s]] + dxr[t] (+ dxs[t]), fp32 sums, bf16 out
+int launch_dx_combine(const void* dxp, const int32_t* inv, const void* dxr, const void* dxs,
+                      void* dx, int T, int k, int d, int num_sms, cudaStream_t stream);
 
 // ---------------------------------------------------------------- CUDA-core fp32 path
 struct SimtArgs {

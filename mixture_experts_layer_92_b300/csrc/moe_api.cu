@@ -668,6 +668,389 @@ int route_impl(const moe_shape* s, const void* x, const void* w_router, const fl
   if (stats) LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
   return ok();
 }
+
+// ---------------------------------------------------------------- backward pass
+// Workspace of moe_backward: the forward's layout, then the backward's own buffers.
+struct BwdLayout {
+  Layout f;
+  size_t logits_full, gu, dyp, dO, hbuf, dgu, dxp, dgp, dgate, dl, dl16, dxr, gus, hsb, dgus, dxs;
+  size_t total;
+};
+
+constexpr int kBwdBn = 256;
+
+BwdLayout layout_bwd(const moe_shape* s) {
+  BwdLayout B;
+  B.f = layout(s);
+  const size_t T = s->T, E = s->E, k = s->k, d = s->d, F = s->d_ff, Fs = s->d_ff_shared;
+  const size_t A = T * k;
+  const size_t nt = (F + kBwdBn - 1) / kBwdBn;
+  size_t o = B.f.total;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + std::max<size_t>(bytes, 1));
+    return at;
+  };
+  B.logits_full = take(T * E * 4);
+  B.gu = take(A * 2 * F * 2);
+  B.dyp = take(A * d * 2);
+  B.dO = take(A * d * 2);
+  B.hbuf = take(A * F * 2);
+  B.dgu = take(A * 2 * F * 2);
+  B.dxp = take(A * d * 2);
+  B.dgp = take(A * nt * 4);
+  B.dgate = take(A * 4);
+  B.dl = take(T * E * 4);
+  B.dl16 = take(T * E * 2);
+  B.dxr = take(T * d * 2);
+  B.gus = take(T * 2 * Fs * 2);
+  B.hsb = take(T * Fs * 2);
+  B.dgus = take(T * 2 * Fs * 2);
+  B.dxs = take(Fs > 0 ? T * d * 2 : 0);
+  B.total = o;
+  return B;
+}
+
+int check_backward_shape(const moe_shape* s) {
+  TRY(check_shape(s));
+  if (s->dtype != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "the backward pass needs a bf16 layer");
+  if (expert_choice(s)) return fail(MOE_ERR_UNSUPPORTED, "the backward pass needs top-k routing");
+  if (s->d % 64 != 0 || s->d_ff % 64 != 0 || s->d_ff_shared % 64 != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "the backward pass needs d, d_ff, d_ff_shared multiples of 64");
+  if (s->E % 8 != 0) return fail(MOE_ERR_UNSUPPORTED, "the backward pass needs E a multiple of 8");
+  return MOE_OK;
+}
+
+// One backward GEMM launch; `rows_bound` bounds the DGRAD row tiles (sizes the grid).
+int bwd_gemm(int mode, BwdProblem p, long long row_tiles, cudaStream_t st, const char* what) {
+  const int nt = (p.args.N + kBwdBn - 1) / kBwdBn;
+  if (mode == BW_WGRAD)
+    p.max_tiles = static_cast<long long>(p.args.groups) * ((p.args.M + 127) / 128) * nt;
+  else
+    p.max_tiles = row_tiles * nt;
+  p.num_sms = num_sms();
+  LAUNCH(launch_bwd_gemm(mode, kBwdBn, p, st), what);
+  return MOE_OK;
+}
+
+int backward_impl(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
+                  const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
+                  const void* w2s, const void* dy, float d_aux, float d_z, void* dx, float* dw_router,
+                  float* d_router_bias, float* dw1, float* dw3, float* dw2, float* dw1s,
+                  float* dw3s, float* dw2s, float* dlogits_out, float* dgate_out, void* ws,
+                  size_t ws_bytes, void* stream, void* const* ev, int n_ev) {
+  TRY(check_backward_shape(s));
+  if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+    return fail(MOE_ERR_WORKSPACE, "workspace is not %zu-byte aligned", kAlign);
+  const BwdLayout B = layout_bwd(s);
+  if (ws_bytes < B.total)
+    return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, B.total);
+  if (ev != nullptr && n_ev != MOE_NUM_BWD_STAGES + 1)
+    return fail(MOE_ERR_INVALID, "n_events = %d, expected %d", n_ev, MOE_NUM_BWD_STAGES + 1);
+  if (ev != nullptr)
+    for (int i = 0; i < n_ev; ++i)
+      if (ev[i] == nullptr) return fail(MOE_ERR_INVALID, "events[%d] is NULL", i);
+  const bool shared = s->d_ff_shared > 0;
+  REQUIRE_PTR(dw_router, "dw_router");
+  REQUIRE_PTR(dw1, "dw1");
+  REQUIRE_PTR(dw3, "dw3");
+  REQUIRE_PTR(dw2, "dw2");
+  if (shared) {
+    REQUIRE_PTR(dw1s, "dw1s");
+    REQUIRE_PTR(dw3s, "dw3s");
+    REQUIRE_PTR(dw2s, "dw2s");
+  }
+  OPT_PTR4(router_bias, "router_bias");
+  OPT_PTR4(d_router_bias, "d_router_bias");
+  OPT_PTR4(dlogits_out, "dlogits_out");
+  OPT_PTR4(dgate_out, "dgate_out");
+  if (s->T > 0) {
+    REQUIRE_PTR(x, "x");
+    REQUIRE_PTR(w_router, "w_router");
+    REQUIRE_PTR(w1, "w1");
+    REQUIRE_PTR(w3, "w3");
+    REQUIRE_PTR(w2, "w2");
+    REQUIRE_PTR(dy, "dy");
+    REQUIRE_PTR(dx, "dx");
+    if (shared) {
+      REQUIRE_PTR(w1s, "w1s");
+      REQUIRE_PTR(w3s, "w3s");
+      REQUIRE_PTR(w2s, "w2s");
+    }
+  }
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto rec = [&](int i) {
+    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+  };
+  const size_t T = s->T, E = s->E, d = s->d, F = s->d_ff, Fs = s->d_ff_shared;
+  const size_t A = T * s->k;
+  if (s->T == 0) {
+    // no tokens: every gradient is 0
+    auto zero = [&](void* p, size_t bytes) {
+      return p == nullptr || bytes == 0 || cudaMemsetAsync(p, 0, bytes, st) == cudaSuccess;
+    };
+    if (!zero(dw_router, E * d * 4) || !zero(d_router_bias, E * 4) || !zero(dw1, E * F * d * 4) ||
+        !zero(dw3, E * F * d * 4) || !zero(dw2, E * d * F * 4) || !zero(dw1s, Fs * d * 4) ||
+        !zero(dw3s, Fs * d * 4) || !zero(dw2s, d * Fs * 4))
+      return cuda_status("memset gradients");
+    for (int i = 0; ev != nullptr && i < n_ev; ++i) rec(i);
+    return ok();
+  }
+  const Layout& L = B.f;
+  DeviceError* err = at<DeviceError>(ws, L.err);
+  float* logits = at<float>(ws, B.logits_full);
+  int32_t* idx = at<int32_t>(ws, L.idx);
+  float* gate = at<float>(ws, L.gate);
+  int32_t* cnt = at<int32_t>(ws, L.counts);
+  int32_t* off = at<int32_t>(ws, L.offsets);
+  int32_t* perm = at<int32_t>(ws, L.perm);
+  int32_t* inv = at<int32_t>(ws, L.inv);
+  void* xp = at<void>(ws, L.xp);
+  void* gu = at<void>(ws, B.gu);
+  void* dyp = at<void>(ws, B.dyp);
+  void* dO = at<void>(ws, B.dO);
+  void* hbuf = at<void>(ws, B.hbuf);
+  void* dgu = at<void>(ws, B.dgu);
+  void* dxp = at<void>(ws, B.dxp);
+  float* dgp = at<float>(ws, B.dgp);
+  float* dgate = dgate_out ? dgate_out : at<float>(ws, B.dgate);
+  float* dl = dlogits_out ? dlogits_out : at<float>(ws, B.dl);
+  void* dl16 = at<void>(ws, B.dl16);
+  void* dxr = at<void>(ws, B.dxr);
+  void* gus = at<void>(ws, B.gus);
+  void* hsb = at<void>(ws, B.hsb);
+  void* dgus = at<void>(ws, B.dgus);
+  void* dxs = shared ? at<void>(ws, B.dxs) : nullptr;
+  const int sms = num_sms();
+  const int nt = static_cast<int>((F + kBwdBn - 1) / kBwdBn);
+  const long long row_tiles = static_cast<long long>((A + 127) / 128) + static_cast<long long>(E);
+  const long long row_tiles_T = static_cast<long long>((T + 127) / 128);
+
+  // 1. recompute the routing: logits (with bias), top-k, gates, dispatch
+  rec(0);
+  TRY(run_router(s, x, w_router, at<float>(ws, L.logits), err, st));
+  LAUNCH(launch_route_topk(route_args(s, at<float>(ws, L.logits), router_split(s).splits,
+                                      router_bias, logits, idx, gate, at<float>(ws, L.partials), err),
+                           st),
+         "gates/top-k");
+  LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, cnt, off, perm, inv,
+                         at<int32_t>(ws, L.dropped), at<int32_t>(ws, L.blk_hist), err, sms, st),
+         "dispatch");
+  // 2. gather the rows of x and of dy
+  rec(1);
+  LAUNCH(launch_gather(x, perm, off, s->E, s->k, static_cast<int>(d * 2), static_cast<int>(A), xp,
+                       sms, st),
+         "gather x");
+  LAUNCH(launch_gather_dy(dy, perm, off, gate, s->E, s->k, s->d, static_cast<int>(A), dyp, dO, sms,
+                          st),
+         "gather dy");
+  // 3. recompute the pre-activations G | U (routed experts and the shared expert)
+  rec(2);
+  {
+    TcProblem p{};
+    p.args.groups = s->E;
+    p.args.offsets = off;
+    p.args.n_routed = s->d_ff;
+    p.args.k_routed = s->d;
+    p.args.out_routed = nullptr;
+    p.args.gu_routed = gu;
+    p.args.has_shared = shared;
+    p.args.m_shared = s->T;
+    p.args.n_shared = s->d_ff_shared;
+    p.args.k_shared = s->d;
+    p.args.out_shared = nullptr;
+    p.args.gu_shared = gus;
+    p.args.err = err;
+    p.a = xp;
+    p.a_rows = static_cast<long long>(A);
+    p.b0 = w1;
+    p.b1 = w3;
+    p.b_rows = s->d_ff;
+    p.b_groups = s->E;
+    p.a_s = x;
+    p.b0_s = w1s;
+    p.b1_s = w3s;
+    p.b_rows_s = s->d_ff_shared;
+    p.max_tiles = (row_tiles) * ((s->d_ff + 127) / 128) +
+                  (shared ? row_tiles_T * ((s->d_ff_shared + 127) / 128) : 0);
+    p.num_sms = sms;
+    LAUNCH(launch_tc_gemm(TC_SWIGLU, 256, 1, 64, false, 128, p, st), "gate/up recompute (tcgen05)");
+  }
+  // 4. dH_raw = dy W2 with the SwiGLU backward and the gate-gradient partials
+  rec(3);
+  {
+    BwdProblem p{};
+    p.args.groups = s->E;
+    p.args.offsets = off;
+    p.args.N = s->d_ff;
+    p.args.K = s->d;
+    p.args.gu = gu;
+    p.args.dgu = dgu;
+    p.args.h = hbuf;
+    p.args.dg_part = dgp;
+    p.args.n_tiles = nt;
+    p.args.perm = perm;
+    p.args.gate = gate;
+    p.args.err = err;
+    p.a = dyp;
+    p.a_rows = static_cast<long long>(A);
+    p.b0 = w2;
+    p.b_inner = s->d_ff;
+    p.b_rows = s->d;
+    p.b_groups = s->E;
+    TRY(bwd_gemm(BW_DGRAD_H, p, row_tiles, st, "dH GEMM (tcgen05)"));
+    if (shared) {
+      BwdProblem q{};
+      q.args.groups = 1;
+      q.args.m_single = s->T;
+      q.args.N = s->d_ff_shared;
+      q.args.K = s->d;
+      q.args.gu = gus;
+      q.args.dgu = dgus;
+      q.args.h = hsb;
+      q.args.err = err;
+      q.a = dy;
+      q.a_rows = s->T;
+      q.b0 = w2s;
+      q.b_inner = s->d_ff_shared;
+      q.b_rows = s->d;
+      q.b_groups = 1;
+      TRY(bwd_gemm(BW_DGRAD_H, q, row_tiles_T, st, "shared dH GEMM (tcgen05)"));
+    }
+  }
+  // 5. gate gradients -> router logit gradients (gates, balance loss, z-loss)
+  rec(4);
+  LAUNCH(launch_dgate(dgp, nt, inv, static_cast<int>(A), dgate, st), "gate gradient");
+  LAUNCH(launch_dlogits(logits, idx, dgate, cnt, s->T, s->E, s->k, s->gate, s->alpha, s->beta,
+                        d_aux, d_z, dl, dl16, st),
+         "logit gradient");
+  if (d_router_bias != nullptr)
+    LAUNCH(launch_column_sum(dl, s->T, s->E, d_router_bias, st), "router bias gradient");
+  // 6. dXp = dG W1 + dU W3 (routed, shared) and the router's dx = dl W_r
+  rec(5);
+  {
+    BwdProblem p{};
+    p.args.groups = s->E;
+    p.args.offsets = off;
+    p.args.N = s->d;
+    p.args.K = 2 * s->d_ff;
+    p.args.k_split = s->d_ff;
+    p.args.out = dxp;
+    p.args.ldo = s->d;
+    p.args.err = err;
+    p.a = dgu;
+    p.a_rows = static_cast<long long>(A);
+    p.b0 = w1;
+    p.b1 = w3;
+    p.b_inner = s->d;
+    p.b_rows = s->d_ff;
+    p.b_groups = s->E;
+    TRY(bwd_gemm(BW_DGRAD_X, p, row_tiles, st, "dX GEMM (tcgen05)"));
+    if (shared) {
+      BwdProblem q = p;
+      q.args.groups = 1;
+      q.args.offsets = nullptr;
+      q.args.m_single = s->T;
+      q.args.K = 2 * s->d_ff_shared;
+      q.args.k_split = s->d_ff_shared;
+      q.args.out = dxs;
+      q.a = dgus;
+      q.a_rows = s->T;
+      q.b0 = w1s;
+      q.b1 = w3s;
+      q.b_rows = s->d_ff_shared;
+      q.b_groups = 1;
+      TRY(bwd_gemm(BW_DGRAD_X, q, row_tiles_T, st, "shared dX GEMM (tcgen05)"));
+    }
+    BwdProblem r{};
+    r.args.groups = 1;
+    r.args.m_single = s->T;
+    r.args.N = s->d;
+    r.args.K = s->E;
+    r.args.k_split = s->E;
+    r.args.out = dxr;
+    r.args.ldo = s->d;
+    r.args.err = err;
+    r.a = dl16;
+    r.a_rows = s->T;
+    r.b0 = w_router;
+    r.b_inner = s->d;
+    r.b_rows = s->E;
+    r.b_groups = 1;
+    TRY(bwd_gemm(BW_DGRAD_X, r, row_tiles_T, st, "router dX GEMM (tcgen05)"));
+  }
+  rec(6);
+  LAUNCH(launch_dx_combine(dxp, inv, dxr, dxs, dx, s->T, s->k, s->d, sms, st), "dx combine");
+  // 7. weight gradients: per expert dW1 | dW3 = [dG dU]^T Xp, dW2 = (g dy)^T H; router; shared
+  rec(7);
+  {
+    BwdProblem p{};
+    p.args.groups = s->E;
+    p.args.offsets = off;
+    p.args.M = 2 * s->d_ff;
+    p.args.m_split = s->d_ff;
+    p.args.N = s->d;
+    p.args.out = dw1;
+    p.args.out1 = dw3;
+    p.args.err = err;
+    p.a = dgu;
+    p.a_rows = static_cast<long long>(A);
+    p.a_inner = 2 * s->d_ff;
+    p.b0 = xp;
+    p.b_rows = static_cast<long long>(A);
+    p.b_inner = s->d;
+    TRY(bwd_gemm(BW_WGRAD, p, 0, st, "dW1/dW3 GEMM (tcgen05)"));
+    BwdProblem q = p;
+    q.args.M = s->d;
+    q.args.m_split = s->d;
+    q.args.N = s->d_ff;
+    q.args.out = dw2;
+    q.args.out1 = nullptr;
+    q.a = dO;
+    q.a_inner = s->d;
+    q.b0 = hbuf;
+    q.b_inner = s->d_ff;
+    TRY(bwd_gemm(BW_WGRAD, q, 0, st, "dW2 GEMM (tcgen05)"));
+    BwdProblem r{};
+    r.args.groups = 1;
+    r.args.m_single = s->T;
+    r.args.M = s->E;
+    r.args.m_split = s->E;
+    r.args.N = s->d;
+    r.args.out = dw_router;
+    r.args.err = err;
+    r.a = dl16;
+    r.a_rows = s->T;
+    r.a_inner = s->E;
+    r.b0 = x;
+    r.b_rows = s->T;
+    r.b_inner = s->d;
+    TRY(bwd_gemm(BW_WGRAD, r, 0, st, "router dW GEMM (tcgen05)"));
+    if (shared) {
+      BwdProblem u = r;
+      u.args.M = 2 * s->d_ff_shared;
+      u.args.m_split = s->d_ff_shared;
+      u.args.out = dw1s;
+      u.args.out1 = dw3s;
+      u.a = dgus;
+      u.a_inner = 2 * s->d_ff_shared;
+      TRY(bwd_gemm(BW_WGRAD, u, 0, st, "shared dW1/dW3 GEMM (tcgen05)"));
+      BwdProblem v = r;
+      v.args.M = s->d;
+      v.args.m_split = s->d;
+      v.args.N = s->d_ff_shared;
+      v.args.out = dw2s;
+      v.a = dy;
+      v.a_inner = s->d;
+      v.b0 = hsb;
+      v.b_inner = s->d_ff_shared;
+      TRY(bwd_gemm(BW_WGRAD, v, 0, st, "shared dW2 GEMM (tcgen05)"));
+    }
+  }
+  rec(8);
+  return ok();
+}
 }  // namespace
 
 extern "C" {
@@ -938,11 +1321,27 @@ const char* moe_status_string(int status) {
     case MOE_ERR_CUDA: return "CUDA error";
     case MOE_ERR_WORKSPACE: return "workspace missing or too small";
     case MOE_ERR_TIMEOUT: return "device wait timed out";
-    case MOE_ERR_NONFINITE: return "non-finite router logit";
+    case MOE_ERR_NONFINITE: return "non-finite value (router logit, or beyond fp16 on the 8-bit path)";
     default: return "unknown status";
   }
 }
 
 const char* moe_last_error_detail(void) { return g_detail.c_str(); }
+
+size_t moe_backward_workspace_size(const moe_shape* s) {
+  if (check_backward_shape(s) != MOE_OK) return 0;
+  return layout_bwd(s).total;
+}
+
+int moe_backward(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
+                 const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
+                 const void* w2s, const void* dy, float d_aux, float d_z, void* dx,
+                 float* dw_router, float* d_router_bias, float* dw1, float* dw3, float* dw2,
+                 float* dw1s, float* dw3s, float* dw2s, float* dlogits, float* dgate, void* ws,
+                 size_t ws_bytes, void* stream, void* const* events, int n_events) {
+  return backward_impl(s, x, w_router, router_bias, w1, w3, w2, w1s, w3s, w2s, dy, d_aux, d_z, dx,
+                       dw_router, d_router_bias, dw1, dw3, dw2, dw1s, dw3s, dw2s, dlogits, dgate,
+                       ws, ws_bytes, stream, events, n_events);
+}
 
 }  // extern "C"

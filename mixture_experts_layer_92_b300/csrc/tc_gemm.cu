@@ -55,6 +55,7 @@
 
 #include "common.cuh"
 #include "launchers.h"
+#include "tma_host.h"
 
 namespace moe {
 
@@ -492,7 +493,28 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               tmem_ld_16cols(tbase + BN / 2 + c * CW, u);
             }
             tmem_ld_wait();
-            if (rvalid) {
+            void* gu = t.shared ? args.gu_shared : args.gu_routed;
+            if (rvalid && gu != nullptr && !W8) {
+              // pre-activations for the backward pass: G | U as bf16 [rows, 2N]
+              const int col0 = col_base + c * CW;
+              __nv_bfloat16* gdst = static_cast<__nv_bfloat16*>(gu) + row * 2 * N + col0;
+#pragma unroll
+              for (int q = 0; q < CW / 8; ++q)
+                if (col0 + q * 8 < N) {
+                  uint32_t pg[4], pu[4];
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    pg[i] = pack_bf16x2(__uint_as_float(g[8 * q + 2 * i]),
+                                        __uint_as_float(g[8 * q + 2 * i + 1]));
+                    pu[i] = pack_bf16x2(__uint_as_float(u[8 * q + 2 * i]),
+                                        __uint_as_float(u[8 * q + 2 * i + 1]));
+                  }
+                  *reinterpret_cast<uint4*>(gdst + q * 8) = make_uint4(pg[0], pg[1], pg[2], pg[3]);
+                  *reinterpret_cast<uint4*>(gdst + N + q * 8) =
+                      make_uint4(pu[0], pu[1], pu[2], pu[3]);
+                }
+            }
+            if (rvalid && out != nullptr) {
               const int col0 = col_base + c * CW;
               if (W8) {
                 // per-row weight scales of W1 and W3 (times the 256 the converters divided
@@ -617,65 +639,6 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
 // ------------------------------------------------------------------------------------
 // Host side: tensor maps and launch
 // ------------------------------------------------------------------------------------
-PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
-std::once_flag g_encode_once;
-
-bool get_encoder() {
-  std::call_once(g_encode_once, []() {
-    void* fn = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPoint("cuTensorMapEncodeTiled", &fn, cudaEnableDefault, &q) ==
-            cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
-  });
-  return g_encode != nullptr;
-}
-
-CUtensorMapSwizzle swizzle_of(int kb) {
-  return kb == 64 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B;
-}
-
-// 2-D bf16 map over a row-major [rows, inner] matrix; box = [box_rows, kb], kb*2-byte swizzle.
-bool encode_2d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
-               int kb) {
-  cuuint64_t dims[2] = {inner, rows};
-  cuuint64_t strides[1] = {inner * 2};
-  cuuint32_t box[2] = {static_cast<cuuint32_t>(kb), box_rows};
-  cuuint32_t es[2] = {1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kb),
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
-// 3-D bf16 map over [groups, rows, inner]; box = [1, box_rows, kb], kb*2-byte swizzle.
-bool encode_3d(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t groups,
-               uint32_t box_rows, int kb) {
-  cuuint64_t dims[3] = {inner, rows, groups};
-  cuuint64_t strides[2] = {inner * 2, inner * rows * 2};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kb), box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides,
-                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle_of(kb),
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
-// 3-D uint8 map over [groups, rows, inner] bytes (8-bit weights); box = [1, box_rows, kb],
-// no swizzle (the converters read it row by row).
-bool encode_3d_u8(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint64_t groups,
-                  uint32_t box_rows, int kb) {
-  cuuint64_t dims[3] = {inner, rows, groups};
-  cuuint64_t strides[2] = {inner, inner * rows};
-  cuuint32_t box[3] = {static_cast<cuuint32_t>(kb), box_rows, 1};
-  cuuint32_t es[3] = {1, 1, 1};
-  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims, strides, box,
-                  es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
-         CUDA_SUCCESS;
-}
-
 template <int MODE, int BN, int MT, int KB, bool W8, int AR>
 int launch_impl(const TcProblem& p, cudaStream_t stream) {
   using C = Cfg<MODE, BN, MT, KB, W8, AR>;

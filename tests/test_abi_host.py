@@ -121,3 +121,38 @@ def test_status_strings():
     for code in (0, -1, -2, -3, -4, -5, -6):
         assert moe.moe_status_string(code) != "unknown status"
     assert moe.moe_status_string(42) == "unknown status"
+
+
+@pytest.mark.parametrize("kw", [
+    dict(dtype=torch.float32), dict(gate="expert_choice"), dict(d=96), dict(d_ff=200),
+    dict(d_ff_shared=96), dict(E=12, k=2),
+])
+def test_backward_unsupported_shapes(kw):
+    """The backward pass needs a bf16 top-k layer with d, d_ff, d_ff_shared multiples of 64
+    and E a multiple of 8: anything else is refused on the host (workspace size 0)."""
+    s = shape(**kw)
+    assert moe.moe_backward_workspace_size(s) == 0
+
+
+def test_backward_rejects_before_any_launch():
+    L = _lib.LIB
+    s = shape()
+    need = moe.moe_backward_workspace_size(s)
+    assert need > moe.moe_workspace_size(s) > 0 and need % 256 == 0
+    fake = ctypes.c_void_p(0x7f0000000000)
+    null = ctypes.c_void_p(None)
+
+    def call(ws=fake, nbytes=need, x=fake, dy=fake, dw1=fake, dw1s=null, shp=s, ev=None, nev=0):
+        return L.moe_backward(ctypes.byref(shp), x, fake, null, fake, fake, fake, null, null, null,
+                              dy, 1.0, 1.0, fake, fake, null, dw1, fake, fake, dw1s, null, null,
+                              null, null, ws, nbytes, null, ev, nev)
+    assert call(ws=null) == -4
+    assert call(nbytes=need - 1) == -4
+    assert call(x=null) == -1
+    assert call(dy=null) == -1
+    assert call(dw1=null) == -1
+    assert call(dw1=ctypes.c_void_p(0x7f0000000008)) == -1
+    s2 = shape(d_ff_shared=128)
+    assert call(shp=s2, nbytes=moe.moe_backward_workspace_size(s2)) == -1   # shared grads missing
+    assert call(ev=(ctypes.c_void_p * 3)(), nev=3) == -1
+    assert call(shp=shape(dtype=torch.float32)) == -2
