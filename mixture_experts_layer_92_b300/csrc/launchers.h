@@ -92,8 +92,8 @@ struct BwdArgs {
   const void* gu;           // G | U of the forward, bf16 [rows, 2N]
   void* dgu;                // out: dG | dU, bf16 [rows, 2N]
   void* h;                  // out: H = silu(G) U, bf16 [rows, N]
-  float* dg_part;           // out (nullable): per row and column tile, sum_f dH_raw * H
-  int n_tiles;              //   [rows, n_tiles]
+  float* dg_part;           // out (nullable): per row, column tile and column half,
+  int n_tiles;              //   sum_f dH_raw * H: [rows, n_tiles] with n_tiles = 2 * tiles
   const int32_t* perm;      // gate of row r = gate[perm[r]] (gate == nullptr: 1)
   const float* gate;
   DeviceError* err;

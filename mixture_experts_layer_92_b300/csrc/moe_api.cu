@@ -684,7 +684,7 @@ BwdLayout layout_bwd(const moe_shape* s) {
   B.f = layout(s);
   const size_t T = s->T, E = s->E, k = s->k, d = s->d, F = s->d_ff, Fs = s->d_ff_shared;
   const size_t A = T * k;
-  const size_t nt = (F + kBwdBn - 1) / kBwdBn;
+  const size_t nt = 2 * ((F + kBwdBn - 1) / kBwdBn);   // dgate partials per row
   size_t o = B.f.total;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -823,7 +823,7 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
   void* dgus = at<void>(ws, B.dgus);
   void* dxs = shared ? at<void>(ws, B.dxs) : nullptr;
   const int sms = num_sms();
-  const int nt = static_cast<int>((F + kBwdBn - 1) / kBwdBn);
+  const int nt = static_cast<int>(2 * ((F + kBwdBn - 1) / kBwdBn));  // dgate partials per row
   const long long row_tiles = static_cast<long long>((A + 127) / 128) + static_cast<long long>(E);
   const long long row_tiles_T = static_cast<long long>((T + 127) / 128);
 

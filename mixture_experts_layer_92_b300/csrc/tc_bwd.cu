@@ -25,10 +25,15 @@
 //
 // Roles (one CTA per SM, persistent): warp 0 lane 0 issues TMA; warp 1 allocates TMEM and
 // lane 0 issues tcgen05.mma (M = 128, N = BN, K = 16) into one of two accumulators; warps
-// 2..5 are the epilogue (each reads its 32-lane quarter of TMEM). BW_WGRAD adds warps 6..9:
+// 2..9 are the epilogue, two per 32-lane quarter of TMEM (warp w reads lanes 32*(w % 4)..,
+// one half of the columns). BW_WGRAD writes its fp32 tiles through shared memory with TMA
+// tensor stores (a thread holds one output row, so direct stores would touch 32 rows per
+// instruction), and adds warps 10..13:
 // the last k-block of an expert may run past the expert's rows (into the next expert's rows
 // or the rows past the end), so they zero those rows of both staged tiles before the MMA
-// reads them. Every mbarrier wait is bounded (common.cuh): on a timeout the kernel records
+// reads them. The MMA waits for them on such tail k-blocks only; they look at every k-block
+// in order and the producer reuses a stage only after they have (so they never fall a ring
+// cycle behind and never touch a stage that holds another k-block). Every mbarrier wait is bounded (common.cuh): on a timeout the kernel records
 // MOE_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
 #include <algorithm>
 #include <mutex>
@@ -45,24 +50,31 @@ constexpr int BM = 128;
 constexpr int BK = 64;
 constexpr int kMaxGroups = 1024;
 constexpr int kChunk = 64 * 128;  // one MN-major TMA box: 64 K rows x 128 bytes
+// BW_WGRAD tensor stores: blocks of 32 rows x kStgCols fp32 columns staged per epilogue warp
+constexpr int kStgCols = 16;
+constexpr int kStgBytes = 32 * kStgCols * 4;
 
 template <int MODE, int BN>
 struct BCfg {
   static constexpr bool A_MN = (MODE == BW_WGRAD);
-  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_WARPS = 8;    // two per TMEM lane quarter, half the columns each
   static constexpr int MASK_WARPS = (MODE == BW_WGRAD) ? 4 : 0;
   static constexpr int THREADS = 64 + 32 * (EPI_WARPS + MASK_WARPS);
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  static constexpr int STAGES_RAW = (196 * 1024) / STAGE_BYTES;
+  // BW_WGRAD: one staging block per epilogue warp for the tensor stores
+  static constexpr int STG_BYTES = (MODE == BW_WGRAD) ? EPI_WARPS * kStgBytes : 0;
+  static constexpr int STAGES_RAW = (212 * 1024 - STG_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
+  static constexpr int OFF_STG = STAGES * STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64
                                        : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN) | idesc_major(A_MN, true);
-  static constexpr int OFF_BARS = STAGES * STAGE_BYTES;
-  // full, empty, ready (rows masked), tmem_full[2], tmem_empty[2], drain
-  static constexpr int NUM_BARS = 3 * STAGES + 5;
+  static constexpr int OFF_BARS = OFF_STG + STG_BYTES;
+  // full, empty, ready (tail rows masked), seen (maskers done with the stage),
+  // tmem_full[2], tmem_empty[2], drain
+  static constexpr int NUM_BARS = 4 * STAGES + 5;
   static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
   static constexpr int OFF_TABLE = OFF_MISC + 16;
   static constexpr int smem_bytes(int groups) { return 1024 + OFF_TABLE + 2 * (groups + 1) * 4; }
@@ -116,7 +128,8 @@ __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w 
 template <int MODE, int BN>
 __global__ void __launch_bounds__(BCfg<MODE, BN>::THREADS, 1)
 tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-              const __grid_constant__ CUtensorMap tmB1, const BwdArgs args) {
+              const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
+              const __grid_constant__ CUtensorMap tmO1, const BwdArgs args) {
   using C = BCfg<MODE, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -125,7 +138,8 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   uint64_t* full_bar = bars;
   uint64_t* empty_bar = bars + C::STAGES;
   uint64_t* ready_bar = bars + 2 * C::STAGES;
-  uint64_t* tfull_bar = bars + 3 * C::STAGES;
+  uint64_t* seen_bar = bars + 3 * C::STAGES;
+  uint64_t* tfull_bar = bars + 4 * C::STAGES;
   uint64_t* tempty_bar = tfull_bar + 2;
   uint64_t* drain_bar = tfull_bar + 4;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::OFF_MISC);
@@ -145,6 +159,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
       mbar_init(&ready_bar[s], C::MASK_WARPS > 0 ? C::MASK_WARPS : 1);
+      mbar_init(&seen_bar[s], C::MASK_WARPS > 0 ? C::MASK_WARPS : 1);
     }
     for (int a = 0; a < 2; ++a) {
       mbar_init(&tfull_bar[a], 1);
@@ -198,8 +213,11 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
         const BTile t = decode<MODE>(tile, s_off, s_pre, G, nt, mt, args);
         for (int kb = 0; kb < t.nk; ++kb) {
+          // BW_WGRAD: the maskers must have looked at the stage's previous contents too
           if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, err,
-                                 SITE_GEMM_WAIT_EMPTY)) {
+                                 SITE_GEMM_WAIT_EMPTY) ||
+              (MODE == BW_WGRAD && !mbar_wait_bounded(&seen_bar[stage], phase ^ 1, abort_flag,
+                                                      err, SITE_GEMM_WAIT_EMPTY))) {
             ok = false;
             break;
           }
@@ -243,6 +261,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     if (lane == 0) {
       int stage = 0;
       uint32_t phase = 0;
+      uint32_t ready_phase = 0;   // BW_WGRAD: phase bit per stage of ready_bar (tails only)
       int it = 0;
       bool ok = true, issued_any = false;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
@@ -255,11 +274,16 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
         for (int kb = 0; kb < t.nk; ++kb) {
-          if (!mbar_wait_bounded(MODE == BW_WGRAD ? &ready_bar[stage] : &full_bar[stage], phase,
-                                 abort_flag, err, SITE_GEMM_WAIT_FULL)) {
+          // a k-block with rows past the group's end waits for the maskers, the rest only
+          // for the copies
+          const bool tail = (MODE == BW_WGRAD) && (t.rows - kb * BK < BK);
+          if (!mbar_wait_bounded(tail ? &ready_bar[stage] : &full_bar[stage],
+                                 tail ? (ready_phase >> stage) & 1u : phase, abort_flag, err,
+                                 SITE_GEMM_WAIT_FULL)) {
             ok = false;
             break;
           }
+          if (tail) ready_phase ^= 1u << stage;
           tc_fence_after();
           const uint32_t a_addr = smem_u32(smem + stage * C::STAGE_BYTES);
           const uint32_t b_addr = a_addr + C::A_BYTES;
@@ -305,8 +329,8 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           break;
         }
         const int krows = min(BK, t.rows - kb * BK);
-        const int kend = min(BK, (krows + 15) & ~15);
-        if (krows < kend) {
+        if (krows < BK) {
+          const int kend = min(BK, (krows + 15) & ~15);
           uint8_t* st = smem + stage * C::STAGE_BYTES;  // A chunks then B chunks, contiguous
           const int per_row = 8;                         // 16-byte stores per row
           const int work = NCHUNK * (kend - krows) * per_row;
@@ -319,9 +343,11 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 make_uint4(0u, 0u, 0u, 0u);
           }
           fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) mbar_arrive(&ready_bar[stage]);
         }
         __syncwarp();
-        if (lane == 0) mbar_arrive(&ready_bar[stage]);
+        if (lane == 0) mbar_arrive(&seen_bar[stage]);
         if (++stage == C::STAGES) {
           stage = 0;
           phase ^= 1;
@@ -330,9 +356,13 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       if (!ok) break;
     }
   } else {
-    // ================= epilogue (warps 2..5) =================
+    // ================= epilogue (warps 2..9) =================
     const int quarter = warp & 3;
+    const int chalf = (warp - 2) >> 2;         // which half of the BN columns
     const int r_local = quarter * 32 + lane;
+    constexpr int CPW = BN / 64;               // 32-column chunks per warp
+    uint8_t* stg = smem + C::OFF_STG + (warp - 2) * kStgBytes;
+    bool stg_busy = false;                     // a tensor store may still read `stg`
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const int acc = it & 1;
@@ -347,35 +377,46 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       const int n0 = t.n_blk * BN;
       const int N = args.N;
       if (MODE == BW_WGRAD) {
-        const int m = t.m_blk * BM + r_local;
-        const bool mvalid = m < args.M;
-        float* orow = nullptr;
-        if (mvalid) {
-          if (m < args.m_split)
-            orow = static_cast<float*>(args.out) +
-                   (static_cast<size_t>(t.group) * args.m_split + m) * N;
-          else
-            orow = static_cast<float*>(args.out1) +
-                   (static_cast<size_t>(t.group) * (args.M - args.m_split) + (m - args.m_split)) * N;
-        }
-        if (quarter * 32 + t.m_blk * BM < args.M) {
+        const int m_blk0 = t.m_blk * BM + quarter * 32;   // first output row of this warp
+        if (m_blk0 < args.M) {
+          const bool second = m_blk0 >= args.m_split;
+          const int ym = second ? m_blk0 - args.m_split : m_blk0;
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int cc = 0; cc < CPW; ++cc) {
+            const int c = chalf * CPW + cc;
+            const int col0 = n0 + c * 32;
+            if (col0 >= N) break;
             uint32_t v[32];
             if (t.nk > 0) {
               tmem_ld_32cols(tbase + c * 32, v);
               tmem_ld_wait();
             } else {
 #pragma unroll
-              for (int i = 0; i < 32; ++i) v[i] = 0u;  // a group with no rows: dW = 0
+              for (int i = 0; i < 32; ++i) v[i] = 0u;   // a group with no rows: dW = 0
             }
-            const int col0 = n0 + c * 32;
-            if (mvalid && col0 < N) {
 #pragma unroll
-              for (int q = 0; q < 8; ++q)
-                if (col0 + 4 * q < N)
-                  *reinterpret_cast<uint4*>(orow + col0 + 4 * q) =
-                      make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+            for (int part = 0; part < 32 / kStgCols; ++part) {
+              if (col0 + part * kStgCols >= N) break;
+              if (stg_busy) {
+                if (lane == 0) bulk_wait_group_read0();
+                __syncwarp();
+              }
+              // row `lane` of the 32-row block; 16-byte unit q goes where the tensor map's
+              // swizzle expects it (128-byte rows: q ^ (lane % 8); 64-byte rows: q ^ (lane/2 % 4))
+#pragma unroll
+              for (int q = 0; q < kStgCols / 4; ++q) {
+                const int pos = kStgCols == 32 ? (q ^ (lane & 7)) : (q ^ ((lane >> 1) & 3));
+                const int vi = part * kStgCols + 4 * q;
+                *reinterpret_cast<uint4*>(stg + lane * (kStgCols * 4) + (pos << 4)) =
+                    make_uint4(v[vi], v[vi + 1], v[vi + 2], v[vi + 3]);
+              }
+              fence_proxy_async_smem();
+              __syncwarp();
+              if (lane == 0) {
+                tma_store_3d(second ? &tmO1 : &tmO0, stg, col0 + part * kStgCols, ym, t.group);
+                bulk_commit_group();
+              }
+              stg_busy = true;
             }
           }
         }
@@ -385,7 +426,8 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         if (MODE == BW_DGRAD_X) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int cc = 0; cc < CPW; ++cc) {
+            const int c = chalf * CPW + cc;
             uint32_t v[32];
             tmem_ld_32cols(tbase + c * 32, v);
             tmem_ld_wait();
@@ -411,7 +453,8 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(args.h) + row * N;
           float dg = 0.0f;
 #pragma unroll 1
-          for (int c = 0; c < BN / 32; ++c) {
+          for (int cc = 0; cc < CPW; ++cc) {
+            const int c = chalf * CPW + cc;
             uint32_t v[32];
             tmem_ld_32cols(tbase + c * 32, v);
             tmem_ld_wait();
@@ -434,7 +477,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                     const float uz = h ? bf16_hi(uw[i]) : bf16_lo(uw[i]);
                     const float raw = __uint_as_float(v[8 * q + 2 * i + h]);
                     const float sg = __fdividef(1.0f, 1.0f + __expf(-gz));
-                    const float si = gz * sg;                       // silu(G)
+                    const float si = gz * sg;                          // silu(G)
                     const float dsi = sg * (1.0f + gz * (1.0f - sg));  // silu'(G)
                     const float dh = g_r * raw;
                     hv[h] = si * uz;
@@ -455,14 +498,16 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
               }
             }
           }
+          // one partial per row, column tile and column half: [rows][n_tiles][2]
           if (rvalid && args.dg_part != nullptr)
-            args.dg_part[row * args.n_tiles + t.n_blk] = dg;
+            args.dg_part[row * args.n_tiles + 2 * t.n_blk + chalf] = dg;
         }
       }
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
     }
+    if (MODE == BW_WGRAD && lane == 0) bulk_wait_group0();   // tensor stores done before exit
   }
 
   tc_fence_before();
@@ -479,11 +524,22 @@ int launch_impl(const BwdProblem& p, cudaStream_t stream) {
   if (!get_encoder()) return MOE_ERR_CUDA;
   const int groups = p.args.groups;
   if (groups < 1 || groups > kMaxGroups) return MOE_ERR_INVALID;
-  CUtensorMap mA{}, mB0{}, mB1{};
+  CUtensorMap mA{}, mB0{}, mB1{}, mO0{}, mO1{};
   if (MODE == BW_WGRAD) {
     if (!encode_2d_mn(&mA, p.a, p.a_inner, p.a_rows, p.a_inner)) return MOE_ERR_CUDA;
     if (!encode_2d_mn(&mB0, p.b0, p.b_inner, p.b_rows, p.b_inner)) return MOE_ERR_CUDA;
     mB1 = mB0;
+    const int g = p.args.groups;
+    if (p.args.m_split % 32 != 0 && p.args.m_split != p.args.M) return MOE_ERR_INVALID;
+    if (!encode_3d_f32_store(&mO0, p.args.out, p.args.N, p.args.m_split, g, kStgCols))
+      return MOE_ERR_CUDA;
+    if (p.args.M > p.args.m_split) {
+      if (!encode_3d_f32_store(&mO1, p.args.out1, p.args.N, p.args.M - p.args.m_split, g,
+                               kStgCols))
+        return MOE_ERR_CUDA;
+    } else {
+      mO1 = mO0;
+    }
   } else {
     if (!encode_2d(&mA, p.a, p.args.K, p.a_rows, BM, BK)) return MOE_ERR_CUDA;
     if (!encode_3d_mn(&mB0, p.b0, p.b_inner, p.b_rows, p.b_groups)) return MOE_ERR_CUDA;
@@ -506,7 +562,7 @@ int launch_impl(const BwdProblem& p, cudaStream_t stream) {
   const long long grid = std::min<long long>(p.max_tiles, p.num_sms);
   if (grid < 1) return MOE_OK;
   tc_bwd_kernel<MODE, BN><<<static_cast<int>(grid), C::THREADS, C::smem_bytes(groups), stream>>>(
-      mA, mB0, mB1, p.args);
+      mA, mB0, mB1, mO0, mO1, p.args);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

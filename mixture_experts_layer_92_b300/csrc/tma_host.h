@@ -98,4 +98,20 @@ inline bool encode_3d_mn(CUtensorMap* m, const void* base, uint64_t inner, uint6
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D fp32 map over [groups, rows, inner] for tensor stores of 32-row blocks: box =
+// [1, 32 rows, cols] with cols = 32 (128-byte rows, 128-byte swizzle) or 16 (64-byte rows,
+// 64-byte swizzle).
+inline bool encode_3d_f32_store(CUtensorMap* m, void* base, uint64_t inner, uint64_t rows,
+                                uint64_t groups, int cols) {
+  cuuint64_t dims[3] = {inner, rows, groups};
+  cuuint64_t strides[2] = {inner * 4, inner * rows * 4};
+  cuuint32_t box[3] = {static_cast<cuuint32_t>(cols), 32, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encoder_slot()(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        cols == 32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 }  // namespace moe
