@@ -131,7 +131,7 @@ def traffic_from_profile(workload: str, kernel: str):
         return None
     if source_sha(src) != vals.get("source_sha256_16"):
         return None
-    return float(vals["dram_bytes_per_launch"])
+    return float(vals["dram_bytes_per_launch"].split()[0])
 
 
 class ClockSampler:
@@ -649,6 +649,10 @@ def main(argv=None):
                          "(cf = 1 when the workload has none)")
     ap.add_argument("--fp8-weights", action="store_true",
                     help="8-bit (E4M3, per-row scale) routed expert weights (weight streaming)")
+    ap.add_argument("--tokens", type=int, default=None,
+                    help="override the workload's token count (smaller cases for profiling)")
+    ap.add_argument("--d-ff", type=int, default=None,
+                    help="override the workload's expert width d_ff (smaller cases for profiling)")
     ap.add_argument("--backward", action="store_true",
                     help="time a training step: moe_forward + moe_backward")
     ap.add_argument("--zipf", type=float, default=None,
@@ -659,6 +663,10 @@ def main(argv=None):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     local_rank = int(os.environ.get("LOCAL_RANK", "0"))
     w = WORKLOADS[args.workload]
+    if args.tokens is not None:
+        w = w.scaled(T=args.tokens, name=f"{w.name}+T{args.tokens}")
+    if args.d_ff is not None:
+        w = w.scaled(d_ff=args.d_ff, name=f"{w.name}+F{args.d_ff}")
     if args.zipf is not None:
         w = w.scaled(zipf_s=args.zipf, name=f"{w.name}+zipf{args.zipf}")
     if args.balance_gamma is not None:
