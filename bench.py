@@ -277,10 +277,10 @@ def run_reference(args, w, rank):
 
 # ------------------------------------------------------------------------------ GPU arm
 def launches_per_forward(w) -> int:
-    # router, top-k, dispatch, gather, gate/up GEMM, down GEMM, combine, stats, losses;
+    # router, top-k, dispatch, gather, gate/up GEMM, down GEMM, combine, statistics + losses;
     # the fp32 path launches the shared expert's two GEMMs separately; expert choice runs a
     # selection and an unrouted-token count in place of the dispatch
-    n = 9 + (2 if (w.dtype == "f32" and w.d_ff_shared) else 0)
+    n = 8 + (2 if (w.dtype == "f32" and w.d_ff_shared) else 0)
     return n + (1 if w.gate == "expert_choice" else 0)
 
 
@@ -312,6 +312,8 @@ def run_ours(args, w, rank, world, local_rank):
     stream = torch.cuda.current_stream(dev)
     evs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(STAGES) + 1)]
            for _ in range(args.steps)]
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
 
     def barrier():
         if dist is not None:
@@ -328,16 +330,25 @@ def run_ours(args, w, rank, world, local_rank):
         if i == 0:
             spread.append(float(layer.counts.max().item()) / (w.T * w.k / w.E))
     barrier()
+    # timed steps: one event before and one after each forward (stage events between the
+    # kernels would keep each launch from overlapping the previous kernel's tail)
     t_wall = time.perf_counter()
+    for i in range(args.steps):
+        flush.zero_()
+        ev_step[i][0].record(stream)
+        layer.forward(x, y)
+        ev_step[i][1].record(stream)
+    barrier()
+    t_wall = time.perf_counter() - t_wall
+    # the per-stage breakdown: the same steps again with an event at every stage boundary
     for i in range(args.steps):
         flush.zero_()
         layer.forward(x, y, events=evs[i])
     barrier()
-    t_wall = time.perf_counter() - t_wall
     err = moe.moe_get_error(layer.ws)
     if err != 0:
         raise RuntimeError(f"device error {moe.moe_status_string(err)}")
-    step_ms = [evs[i][0].elapsed_time(evs[i][-1]) for i in range(args.steps)]
+    step_ms = [ev_step[i][0].elapsed_time(ev_step[i][1]) for i in range(args.steps)]
     stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
                 for j, name in enumerate(STAGES)}
     total_ms = sum(step_ms)
@@ -507,6 +518,8 @@ def run_train(args, w, rank, world, local_rank):
             for _ in range(args.steps)]
     bevs = [[torch.cuda.Event(enable_timing=True) for _ in range(len(BWD_STAGES) + 1)]
             for _ in range(args.steps)]
+    ev_step = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
 
     def barrier():
         if dist is not None:
@@ -521,7 +534,14 @@ def run_train(args, w, rank, world, local_rank):
         layer.forward(x, y)
         backward(x, dy)
     barrier()
-    for i in range(args.steps):
+    for i in range(args.steps):                 # timed: start and end events only
+        flush.zero_()
+        ev_step[i][0].record(stream)
+        layer.forward(x, y)
+        backward(x, dy)
+        ev_step[i][1].record(stream)
+    barrier()
+    for i in range(args.steps):                 # per-stage breakdown
         flush.zero_()
         layer.forward(x, y, events=fevs[i])
         backward(x, dy, events=bevs[i])
@@ -529,7 +549,7 @@ def run_train(args, w, rank, world, local_rank):
     for ws in (layer.ws, bws):
         if moe.moe_get_error(ws) != 0:
             raise RuntimeError("device error")
-    step_ms = [fevs[i][0].elapsed_time(bevs[i][-1]) for i in range(args.steps)]
+    step_ms = [ev_step[i][0].elapsed_time(ev_step[i][1]) for i in range(args.steps)]
     fwd_ms = [fevs[i][0].elapsed_time(fevs[i][-1]) for i in range(args.steps)]
     bwd_ms = [bevs[i][0].elapsed_time(bevs[i][-1]) for i in range(args.steps)]
     bstage_ms = {name: [bevs[i][j].elapsed_time(bevs[i][j + 1]) for i in range(args.steps)]

@@ -20,7 +20,7 @@ struct DeviceError {
   int code;       // first moe_status recorded (0 = none)
   int where;      // kernel/site id of the first error
   int detail;     // site-specific detail (e.g. offending index)
-  int pad;
+  unsigned done_count;  // statistics/loss kernel: finished column blocks (back to 0 after use)
   unsigned grid_count;  // grid barrier of the dispatch kernel: arrivals (back to 0 after use)
   unsigned grid_gen;    //                                     generation
 };
@@ -115,6 +115,17 @@ __device__ __forceinline__ float silu_f(float z) { return z / (1.0f + expf(-z));
 // silu with CUDA's fast exponential and fast division, for results rounded to bf16:
 // z / (1 + e^-z); for very negative z, e^-z = inf and the quotient is 0.
 __device__ __forceinline__ float silu_fast(float z) { return __fdividef(z, 1.0f + __expf(-z)); }
+
+// Programmatic dependent launch. A kernel launched with the programmatic-serialization
+// attribute may start while the previous kernel in the stream is still running: pdl_wait()
+// blocks until the kernels it depends on have completed and their writes are visible (it
+// returns at once for an ordinary launch), and pdl_launch_dependents() lets the next such
+// kernel start launching. Every kernel launched through launch_pdl calls pdl_wait() before
+// it reads anything an earlier kernel wrote.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));

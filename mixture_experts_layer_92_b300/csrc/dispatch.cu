@@ -70,6 +70,7 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int chunk,
   int* s_off = s_base + E;                 // [E + 1]
   int* s_wsum = s_off + E + 1;             // [kDispWarps]
   const int tid = threadIdx.x;
+  pdl_launch_dependents();                 // the gather may start launching (it waits for us)
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;

@@ -10,6 +10,25 @@ namespace moe {
 
 struct DeviceError;
 
+// Launches `kernel` with programmatic stream serialization: its launch and set-up overlap the
+// end of the previous kernel in the stream. Only for kernels that call pdl_wait() (common.cuh)
+// before reading what earlier kernels wrote.
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Sets the text moe_last_error_detail() returns on this thread; returns `status`.
 int set_error_detail(int status, const char* text);
 
@@ -170,6 +189,10 @@ int launch_update_select_bias(const int32_t* counts, float* select_bias, int T, 
                               float gamma, cudaStream_t stream);
 int launch_stats_reduce(const float* partials, int nblocks, int E, float* stats,
                         cudaStream_t stream);
+// launch_stats_reduce + launch_aux_loss in one launch (T > 0); uses hdr->done_count.
+int launch_stats_loss(const float* partials, int nblocks, int E, float* stats,
+                      const int32_t* counts, int T, int k, float alpha, float beta, float* losses,
+                      DeviceError* hdr, cudaStream_t stream);
 int launch_aux_loss(const float* stats, const int32_t* counts, int T, int E, int k, float alpha,
                     float beta, float* losses, cudaStream_t stream);
 

@@ -577,9 +577,12 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
          "combine");
   rec(7);
   if (s->T > 0) {
-    LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
+    LAUNCH(launch_stats_loss(partials, route_blocks(s->T), s->E, stats, cnt, s->T, s->k, s->alpha,
+                             s->beta, los, err, st),
+           "router statistics and losses");
+  } else {
+    LAUNCH(launch_aux_loss(stats, cnt, s->T, s->E, s->k, s->alpha, s->beta, los, st), "aux loss");
   }
-  LAUNCH(launch_aux_loss(stats, cnt, s->T, s->E, s->k, s->alpha, s->beta, los, st), "aux loss");
   if (select_bias != nullptr)
     LAUNCH(launch_update_select_bias(cnt, select_bias, s->T, s->E, s->k, gamma, st),
            "selection bias update");

@@ -25,6 +25,8 @@ __global__ void __launch_bounds__(kMoveThreads)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
                    const int32_t* __restrict__ offsets, int E, int k, int nvec,
                    uint4* __restrict__ xp) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int R = offsets[E];
   const int lane = threadIdx.x & 31;
   const int nw = gridDim.x * kMoveWarps;
@@ -57,6 +59,8 @@ __global__ void __launch_bounds__(kMoveThreads)
 gather_rows_f16_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
                        const int32_t* __restrict__ offsets, int E, int k, int nvec,
                        uint4* __restrict__ xp, DeviceError* err) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int R = offsets[E];
   const int lane = threadIdx.x & 31;
   const int nw = gridDim.x * kMoveWarps;
@@ -111,6 +115,8 @@ template <bool BF16, int KS>
 __global__ void __launch_bounds__(kMoveThreads)
 combine_kernel(const uint4* __restrict__ yp, const int32_t* __restrict__ inv,
                const uint4* __restrict__ ys, uint4* __restrict__ y, int T, int k, int nvec) {
+  pdl_wait();
+  pdl_launch_dependents();
   const int lane = threadIdx.x & 31;
   const int nseg = (nvec + 63) / 64;
   const long long total = static_cast<long long>(T) * nseg;
@@ -186,25 +192,30 @@ int launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, in
                   DeviceError* to_f16_err) {
   if (max_rows <= 0) return MOE_OK;
   if (to_f16_err != nullptr)
-    gather_rows_f16_kernel<<<grid_for_rows(max_rows, num_sms), kMoveThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), perm, offsets, E, k, row_bytes / 16, static_cast<uint4*>(xp),
-        to_f16_err);
-  else
-    gather_rows_kernel<<<grid_for_rows(max_rows, num_sms), kMoveThreads, 0, stream>>>(
-        static_cast<const uint4*>(x), perm, offsets, E, k, row_bytes / 16, static_cast<uint4*>(xp));
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    return launch_pdl(gather_rows_f16_kernel, dim3(grid_for_rows(max_rows, num_sms)),
+                      dim3(kMoveThreads), 0, stream, static_cast<const uint4*>(x), perm, offsets,
+                      E, k, row_bytes / 16, static_cast<uint4*>(xp), to_f16_err) == cudaSuccess
+               ? MOE_OK : MOE_ERR_CUDA;
+  return launch_pdl(gather_rows_kernel, dim3(grid_for_rows(max_rows, num_sms)), dim3(kMoveThreads),
+                    0, stream, static_cast<const uint4*>(x), perm, offsets, E, k, row_bytes / 16,
+                    static_cast<uint4*>(xp)) == cudaSuccess
+             ? MOE_OK : MOE_ERR_CUDA;
 }
 
 template <bool BF16>
-void combine_dispatch_k(int grid, const uint4* yp, const int32_t* inv, const uint4* ys, uint4* y,
-                        int T, int k, int nvec, cudaStream_t stream) {
+cudaError_t combine_dispatch_k(int grid, const uint4* yp, const int32_t* inv, const uint4* ys,
+                               uint4* y, int T, int k, int nvec, cudaStream_t stream) {
+  auto go = [&](auto kernel) {
+    return launch_pdl(kernel, dim3(grid), dim3(kMoveThreads), 0, stream, yp, inv, ys, y, T, k,
+                      nvec);
+  };
   switch (k) {
-    case 1: combine_kernel<BF16, 1><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec); break;
-    case 2: combine_kernel<BF16, 2><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec); break;
-    case 4: combine_kernel<BF16, 4><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec); break;
-    case 6: combine_kernel<BF16, 6><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec); break;
-    case 8: combine_kernel<BF16, 8><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec); break;
-    default: combine_kernel<BF16, 0><<<grid, kMoveThreads, 0, stream>>>(yp, inv, ys, y, T, k, nvec);
+    case 1: return go(combine_kernel<BF16, 1>);
+    case 2: return go(combine_kernel<BF16, 2>);
+    case 4: return go(combine_kernel<BF16, 4>);
+    case 6: return go(combine_kernel<BF16, 6>);
+    case 8: return go(combine_kernel<BF16, 8>);
+    default: return go(combine_kernel<BF16, 0>);
   }
 }
 
@@ -218,9 +229,10 @@ int launch_combine(int dtype, const void* yp, const int32_t* inv, const void* ys
   const uint4* a = static_cast<const uint4*>(yp);
   const uint4* b = static_cast<const uint4*>(ys);
   uint4* o = static_cast<uint4*>(y);
-  if (dtype == MOE_BF16) combine_dispatch_k<true>(grid, a, inv, b, o, T, k, nvec, stream);
-  else combine_dispatch_k<false>(grid, a, inv, b, o, T, k, nvec, stream);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  const cudaError_t e = dtype == MOE_BF16
+                            ? combine_dispatch_k<true>(grid, a, inv, b, o, T, k, nvec, stream)
+                            : combine_dispatch_k<false>(grid, a, inv, b, o, T, k, nvec, stream);
+  return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace moe

@@ -38,6 +38,8 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
   extern __shared__ float s_part[];  // [kRouteWarps][E + 1]
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  pdl_wait();
+  pdl_launch_dependents();
 
   float pacc[JM];
 #pragma unroll
@@ -196,6 +198,52 @@ stats_reduce_kernel(const float* __restrict__ partials, int nb, int E, float* __
   if (threadIdx.x == 0) stats[e] = static_cast<float>(s_red[0]);
 }
 
+// stats as stats_reduce_kernel, and the block that finishes last (a counter in the workspace
+// header) then computes the two losses from them, as aux_loss_kernel does: one launch instead
+// of two. The counter goes back to 0 for the next call.
+__global__ void __launch_bounds__(256)
+stats_loss_kernel(const float* __restrict__ partials, int nb, int E, float* __restrict__ stats,
+                  const int32_t* __restrict__ counts, int T, int k, float alpha, float beta,
+                  float* __restrict__ losses, DeviceError* hdr) {
+  __shared__ double s_red[256];
+  __shared__ bool s_last;
+  const int e = blockIdx.x;
+  pdl_wait();
+  pdl_launch_dependents();
+  double acc = 0.0;
+  for (int b = threadIdx.x; b < nb; b += 256) acc += partials[static_cast<size_t>(b) * (E + 1) + e];
+  s_red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    stats[e] = static_cast<float>(s_red[0]);
+    __threadfence();
+    s_last = atomicAdd(&hdr->done_count, 1u) == static_cast<unsigned>(E);
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  acc = 0.0;
+  for (int i = threadIdx.x; i < E; i += blockDim.x)
+    acc += static_cast<double>(counts[i]) * static_cast<double>(__ldcg(stats + i));
+  s_red[threadIdx.x] = acc;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) {
+    const double Td = static_cast<double>(T);
+    losses[0] = static_cast<float>(static_cast<double>(alpha) * E * s_red[0] /
+                                   (Td * static_cast<double>(k) * Td));
+    losses[1] = static_cast<float>(static_cast<double>(beta) * __ldcg(stats + E) / Td);
+    hdr->done_count = 0u;
+  }
+}
+
 // losses[0] = alpha*E*sum_i (counts_i/(T*k)) * (stats_i/T); losses[1] = beta*stats[E]/T.
 __global__ void aux_loss_kernel(const float* __restrict__ stats, const int32_t* __restrict__ counts,
                                 int T, int E, int k, float alpha, float beta,
@@ -240,11 +288,12 @@ template <int JM>
 int launch_jm(const RouteArgs& a, cudaStream_t stream) {
   const int nb = route_blocks(a.T);
   const size_t smem = static_cast<size_t>(kRouteWarps) * (a.E + 1) * sizeof(float);
-  route_topk_kernel<JM><<<nb, kRouteThreads, smem, stream>>>(
-      a.logits, a.nsplit, a.split_stride, a.bias, a.select_bias, a.logits_out, a.probs_t, a.T,
-      a.E, a.k, a.gate_mode,
-      a.topk_idx, a.topk_gate, a.partials, a.err);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (launch_pdl(route_topk_kernel<JM>, dim3(nb), dim3(kRouteThreads), smem, stream, a.logits,
+                 a.nsplit, a.split_stride, a.bias, a.select_bias, a.logits_out, a.probs_t, a.T,
+                 a.E, a.k, a.gate_mode, a.topk_idx, a.topk_gate, a.partials,
+                 a.err) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 }  // namespace
@@ -277,6 +326,15 @@ int launch_update_select_bias(const int32_t* counts, float* select_bias, int T, 
   update_select_bias_kernel<<<(E + 255) / 256, 256, 0, stream>>>(counts, select_bias, T, E, k,
                                                                  gamma);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_stats_loss(const float* partials, int nblocks, int E, float* stats,
+                      const int32_t* counts, int T, int k, float alpha, float beta, float* losses,
+                      DeviceError* hdr, cudaStream_t stream) {
+  if (launch_pdl(stats_loss_kernel, dim3(E + 1), dim3(256), 0, stream, partials, nblocks, E, stats,
+                 counts, T, k, alpha, beta, losses, hdr) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 int launch_aux_loss(const float* stats, const int32_t* counts, int T, int E, int k, float alpha,

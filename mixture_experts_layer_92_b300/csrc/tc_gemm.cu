@@ -233,6 +233,10 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     fence_barrier_init();
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  // everything above touches only this CTA's own resources; from here on the kernel reads
+  // what earlier kernels wrote (offsets, A)
+  pdl_wait();
+  pdl_launch_dependents();
   if (warp == 2) {
     // s_off[g] = first row of group g; s_pre[g] = first tile of group g (exclusive scan).
     const int nt = (args.n_routed + C::BN_OUT - 1) / C::BN_OUT * (MODE == TC_F32OUT ? args.splits : 1);
@@ -687,10 +691,11 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
 
   long long grid = std::min<long long>(p.max_tiles, p.num_sms);
   if (grid < 1) return MOE_OK;
-  tc_grouped_gemm_kernel<MODE, BN, MT, KB, W8, AR><<<static_cast<int>(grid), C::THREADS, smem,
-                                                     stream>>>(
-      mA, mB0, mB1, mAs, mB0s, mB1s, p.args);
-  return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+  if (launch_pdl(tc_grouped_gemm_kernel<MODE, BN, MT, KB, W8, AR>, dim3(static_cast<int>(grid)),
+                 dim3(C::THREADS), smem, stream, mA, mB0, mB1, mAs, mB0s, mB1s,
+                 p.args) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
 }
 
 }  // namespace
