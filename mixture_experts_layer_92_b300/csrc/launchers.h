@@ -130,7 +130,8 @@ struct BwdProblem {
   int num_sms;
 };
 
-int launch_bwd_gemm(int mode, int bn, const BwdProblem& p, cudaStream_t stream);
+// mt: 128-row output tiles per CTA tile (2 only for BW_WGRAD).
+int launch_bwd_gemm(int mode, int bn, int mt, const BwdProblem& p, cudaStream_t stream);
 
 // Non-GEMM steps of the backward pass (backward.cu)
 // dyp[r] = dy[perm[r] / k], dO[r] = gate[perm[r]] * dy[perm[r] / k] (bf16), r < offsets[E]

@@ -724,15 +724,17 @@ int check_backward_shape(const moe_shape* s) {
   return MOE_OK;
 }
 
-// One backward GEMM launch; `rows_bound` bounds the DGRAD row tiles (sizes the grid).
-int bwd_gemm(int mode, BwdProblem p, long long row_tiles, cudaStream_t st, const char* what) {
+// One backward GEMM launch; `row_tiles` bounds the DGRAD row tiles (sizes the grid); `mt`
+// 256-row weight-gradient tiles (2) or 128-row ones (1).
+int bwd_gemm(int mode, BwdProblem p, long long row_tiles, cudaStream_t st, const char* what,
+             int mt = 1) {
   const int nt = (p.args.N + kBwdBn - 1) / kBwdBn;
   if (mode == BW_WGRAD)
-    p.max_tiles = static_cast<long long>(p.args.groups) * ((p.args.M + 127) / 128) * nt;
+    p.max_tiles = static_cast<long long>(p.args.groups) * ((p.args.M + 128 * mt - 1) / (128 * mt)) * nt;
   else
     p.max_tiles = row_tiles * nt;
   p.num_sms = num_sms();
-  LAUNCH(launch_bwd_gemm(mode, kBwdBn, p, st), what);
+  LAUNCH(launch_bwd_gemm(mode, kBwdBn, mt, p, st), what);
   return MOE_OK;
 }
 
@@ -1003,7 +1005,10 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
     p.b0 = xp;
     p.b_rows = static_cast<long long>(A);
     p.b_inner = s->d;
-    TRY(bwd_gemm(BW_WGRAD, p, 0, st, "dW1/dW3 GEMM (tcgen05)"));
+    // Experts with many rows (long K per output tile): 256-row tiles, twice the MMA work per
+    // staged byte (the weight-gradient GEMMs read both operands through L2); few rows: 128.
+    const int mt_w = (A / s->E >= 512) ? 2 : 1;
+    TRY(bwd_gemm(BW_WGRAD, p, 0, st, "dW1/dW3 GEMM (tcgen05)", mt_w));
     BwdProblem q = p;
     q.args.M = s->d;
     q.args.m_split = s->d;
@@ -1014,7 +1019,7 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
     q.a_inner = s->d;
     q.b0 = hbuf;
     q.b_inner = s->d_ff;
-    TRY(bwd_gemm(BW_WGRAD, q, 0, st, "dW2 GEMM (tcgen05)"));
+    TRY(bwd_gemm(BW_WGRAD, q, 0, st, "dW2 GEMM (tcgen05)", mt_w));
     BwdProblem r{};
     r.args.groups = 1;
     r.args.m_single = s->T;

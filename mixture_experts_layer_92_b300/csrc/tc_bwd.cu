@@ -54,15 +54,19 @@ constexpr int kChunk = 64 * 128;  // one MN-major TMA box: 64 K rows x 128 bytes
 constexpr int kStgCols = 16;
 constexpr int kStgBytes = 32 * kStgCols * 4;
 
-template <int MODE, int BN>
+// MT (BW_WGRAD only): 128-row output tiles per CTA tile, 1 or 2. With MT = 2 one B tile
+// feeds two M = 128 MMAs (output rows m0.. and m0 + 128..), twice the MMA work per staged
+// byte; the two accumulators fill TMEM, so the epilogue is not double-buffered.
+template <int MODE, int BN, int MT = 1>
 struct BCfg {
   static constexpr bool A_MN = (MODE == BW_WGRAD);
-  static constexpr int EPI_WARPS = 8;    // two per TMEM lane quarter, half the columns each
+  static constexpr int EPI_WARPS = 8;    // two per TMEM lane quarter
   static constexpr int MASK_WARPS = (MODE == BW_WGRAD) ? 4 : 0;
   static constexpr int THREADS = 64 + 32 * (EPI_WARPS + MASK_WARPS);
-  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int A_BYTES = MT * BM * BK * 2;
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr int NUM_ACC = (MT == 1) ? 2 : 1;   // accumulator sets (double buffering)
   // BW_WGRAD: one staging block per epilogue warp for the tensor stores
   static constexpr int STG_BYTES = (MODE == BW_WGRAD) ? EPI_WARPS * kStgBytes : 0;
   static constexpr int STAGES_RAW = (212 * 1024 - STG_BYTES) / STAGE_BYTES;
@@ -70,6 +74,7 @@ struct BCfg {
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;
   static constexpr uint32_t TMEM_COLS = (2 * BN <= 32) ? 32 : (2 * BN <= 64) ? 64
                                        : (2 * BN <= 128) ? 128 : (2 * BN <= 256) ? 256 : 512;
+  static_assert(MT == 1 || (MT == 2 && MODE == BW_WGRAD && 2 * BN <= 512), "MT = 2: weight grads");
   static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN) | idesc_major(A_MN, true);
   static constexpr int OFF_BARS = OFF_STG + STG_BYTES;
   // full, empty, ready (tail rows masked), seen (maskers done with the stage),
@@ -125,12 +130,12 @@ __device__ __forceinline__ BTile decode(int tile, const int* s_off, const int* s
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t w) { return __uint_as_float(w & 0xffff0000u); }
 
-template <int MODE, int BN>
-__global__ void __launch_bounds__(BCfg<MODE, BN>::THREADS, 1)
+template <int MODE, int BN, int MT>
+__global__ void __launch_bounds__(BCfg<MODE, BN, MT>::THREADS, 1)
 tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
               const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO0,
               const __grid_constant__ CUtensorMap tmO1, const BwdArgs args) {
-  using C = BCfg<MODE, BN>;
+  using C = BCfg<MODE, BN, MT>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -152,7 +157,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   DeviceError* err = args.err;
 
   const int nt = (args.N + BN - 1) / BN;
-  const int mt = (MODE == BW_WGRAD) ? (args.M + BM - 1) / BM : 1;
+  const int mt = (MODE == BW_WGRAD) ? (args.M + MT * BM - 1) / (MT * BM) : 1;
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -227,9 +232,10 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           const int n0 = t.n_blk * BN;
           if (MODE == BW_WGRAD) {
             const int krow = t.row0 + kb * BK;
-            const int m0 = t.m_blk * BM;
-            tma_load_2d(sa, &tmA, &full_bar[stage], m0, krow);
-            tma_load_2d(sa + kChunk, &tmA, &full_bar[stage], m0 + 64, krow);
+            const int m0 = t.m_blk * MT * BM;
+#pragma unroll
+            for (int c = 0; c < 2 * MT; ++c)
+              tma_load_2d(sa + c * kChunk, &tmA, &full_bar[stage], m0 + 64 * c, krow);
 #pragma unroll
             for (int c = 0; c < BN / 64; ++c)
               tma_load_2d(sb + c * kChunk, &tmB0, &full_bar[stage], n0 + 64 * c, krow);
@@ -266,13 +272,15 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       bool ok = true, issued_any = false;
       for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
         const BTile t = decode<MODE>(tile, s_off, s_pre, G, nt, mt, args);
-        const int acc = it & 1;
-        const uint32_t acc_phase = (it >> 1) & 1;
+        const int acc = it % C::NUM_ACC;
+        const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
         if (!mbar_wait_bounded(&tempty_bar[acc], acc_phase ^ 1, abort_flag, err,
                                SITE_GEMM_WAIT_TMEM_EMPTY))
           break;
         tc_fence_after();
-        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+        const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * MT * BN);
+        // MT = 2: the second 128 output rows exist only if they start below M
+        const bool two = (MT == 2) && (t.m_blk * MT * BM + BM < args.M);
         for (int kb = 0; kb < t.nk; ++kb) {
           // a k-block with rows past the group's end waits for the maskers, the rest only
           // for the copies
@@ -295,6 +303,9 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                                            : smem_desc_kmajor<128>(a_addr + kk * 32);
             const uint64_t bdesc = smem_desc_mn_sw128(b_addr + kk * 2048, kChunk);
             tc_mma_bf16(d_tmem, adesc, bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
+            if (two)   // rows 128..255: A chunks 2 and 3, the same B tile
+              tc_mma_bf16(d_tmem + BN, smem_desc_mn_sw128(a_addr + 2 * kChunk + kk * 2048, kChunk),
+                          bdesc, C::IDESC, (kb | kk) != 0 ? 1u : 0u);
           }
           issued_any = true;
           tc_commit(&empty_bar[stage]);
@@ -317,7 +328,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     // lie past the matrix. A row is 128 contiguous bytes of its 64-wide chunk (the swizzle
     // only permutes 16-byte units inside the row).
     const int mt_id = threadIdx.x - (2 + C::EPI_WARPS) * 32;
-    constexpr int NCHUNK = 2 + BN / 64;
+    constexpr int NCHUNK = 2 * MT + BN / 64;
     int stage = 0;
     uint32_t phase = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x) {
@@ -358,26 +369,29 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   } else {
     // ================= epilogue (warps 2..9) =================
     const int quarter = warp & 3;
-    const int chalf = (warp - 2) >> 2;         // which half of the BN columns
+    // MT = 1: the two warps of a quarter split the BN columns; MT = 2: they take the two
+    // 128-row halves, all columns each
+    const int chalf = (MT == 1) ? (warp - 2) >> 2 : 0;
+    const int rhalf = (MT == 2) ? (warp - 2) >> 2 : 0;
     const int r_local = quarter * 32 + lane;
-    constexpr int CPW = BN / 64;               // 32-column chunks per warp
+    constexpr int CPW = (MT == 1) ? BN / 64 : BN / 32;   // 32-column chunks per warp
     uint8_t* stg = smem + C::OFF_STG + (warp - 2) * kStgBytes;
     bool stg_busy = false;                     // a tensor store may still read `stg`
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
-      const int acc = it & 1;
-      const uint32_t acc_phase = (it >> 1) & 1;
+      const int acc = it % C::NUM_ACC;
+      const uint32_t acc_phase = (it / C::NUM_ACC) & 1;
       if (!mbar_wait_bounded(&tfull_bar[acc], acc_phase, abort_flag, err,
                              SITE_GEMM_WAIT_TMEM_FULL))
         break;
       tc_fence_after();
       const BTile t = decode<MODE>(tile, s_off, s_pre, G, nt, mt, args);
       const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) +
-                             static_cast<uint32_t>(acc * BN);
+                             static_cast<uint32_t>((acc * MT + rhalf) * BN);
       const int n0 = t.n_blk * BN;
       const int N = args.N;
       if (MODE == BW_WGRAD) {
-        const int m_blk0 = t.m_blk * BM + quarter * 32;   // first output row of this warp
+        const int m_blk0 = t.m_blk * MT * BM + rhalf * BM + quarter * 32;  // first output row
         if (m_blk0 < args.M) {
           const bool second = m_blk0 >= args.m_split;
           const int ym = second ? m_blk0 - args.m_split : m_blk0;
@@ -460,11 +474,20 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             tmem_ld_wait();
             const int col0 = n0 + c * 32;
             if (rvalid && col0 < N) {
+              // all of the chunk's G and U loads first (read-only), then the math and stores
+              uint4 gqs[4], uqs[4];
+#pragma unroll
+              for (int q = 0; q < 4; ++q) {
+                if (col0 + 8 * q < N) {
+                  gqs[q] = __ldg(reinterpret_cast<const uint4*>(gu + col0 + 8 * q));
+                  uqs[q] = __ldg(reinterpret_cast<const uint4*>(gu + N + col0 + 8 * q));
+                }
+              }
 #pragma unroll
               for (int q = 0; q < 4; ++q) {
                 if (col0 + 8 * q >= N) continue;
-                const uint4 gq = *reinterpret_cast<const uint4*>(gu + col0 + 8 * q);
-                const uint4 uq = *reinterpret_cast<const uint4*>(gu + N + col0 + 8 * q);
+                const uint4 gq = gqs[q];
+                const uint4 uq = uqs[q];
                 const uint32_t gw[4] = {gq.x, gq.y, gq.z, gq.w};
                 const uint32_t uw[4] = {uq.x, uq.y, uq.z, uq.w};
                 uint32_t dgw[4], duw[4], hw[4];
@@ -518,9 +541,9 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
   }
 }
 
-template <int MODE, int BN>
+template <int MODE, int BN, int MT>
 int launch_impl(const BwdProblem& p, cudaStream_t stream) {
-  using C = BCfg<MODE, BN>;
+  using C = BCfg<MODE, BN, MT>;
   if (!get_encoder()) return MOE_ERR_CUDA;
   const int groups = p.args.groups;
   if (groups < 1 || groups > kMaxGroups) return MOE_ERR_INVALID;
@@ -554,29 +577,30 @@ int launch_impl(const BwdProblem& p, cudaStream_t stream) {
   static std::once_flag attr_once[64];
   static bool attr_ok[64];
   std::call_once(attr_once[dev], [&]() {
-    attr_ok[dev] = cudaFuncSetAttribute(tc_bwd_kernel<MODE, BN>,
+    attr_ok[dev] = cudaFuncSetAttribute(tc_bwd_kernel<MODE, BN, MT>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         C::smem_bytes(kMaxGroups)) == cudaSuccess;
   });
   if (!attr_ok[dev]) return MOE_ERR_CUDA;
   const long long grid = std::min<long long>(p.max_tiles, p.num_sms);
   if (grid < 1) return MOE_OK;
-  tc_bwd_kernel<MODE, BN><<<static_cast<int>(grid), C::THREADS, C::smem_bytes(groups), stream>>>(
+  tc_bwd_kernel<MODE, BN, MT><<<static_cast<int>(grid), C::THREADS, C::smem_bytes(groups), stream>>>(
       mA, mB0, mB1, mO0, mO1, p.args);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
 }  // namespace
 
-int launch_bwd_gemm(int mode, int bn, const BwdProblem& p, cudaStream_t stream) {
-#define MOE_BW_CASE(M, N) \
-  if (mode == M && bn == N) return launch_impl<M, N>(p, stream);
-  MOE_BW_CASE(BW_DGRAD_H, 256)
-  MOE_BW_CASE(BW_DGRAD_X, 256)
-  MOE_BW_CASE(BW_WGRAD, 256)
-  MOE_BW_CASE(BW_DGRAD_H, 128)
-  MOE_BW_CASE(BW_DGRAD_X, 128)
-  MOE_BW_CASE(BW_WGRAD, 128)
+int launch_bwd_gemm(int mode, int bn, int mt, const BwdProblem& p, cudaStream_t stream) {
+#define MOE_BW_CASE(M, N, T) \
+  if (mode == M && bn == N && mt == T) return launch_impl<M, N, T>(p, stream);
+  MOE_BW_CASE(BW_DGRAD_H, 256, 1)
+  MOE_BW_CASE(BW_DGRAD_X, 256, 1)
+  MOE_BW_CASE(BW_WGRAD, 256, 1)
+  MOE_BW_CASE(BW_WGRAD, 256, 2)
+  MOE_BW_CASE(BW_DGRAD_H, 128, 1)
+  MOE_BW_CASE(BW_DGRAD_X, 128, 1)
+  MOE_BW_CASE(BW_WGRAD, 128, 1)
 #undef MOE_BW_CASE
   return MOE_ERR_UNSUPPORTED;
 }

@@ -103,6 +103,10 @@ CASES = {
     "empty_experts": WORKLOADS["deepseek_fine"].scaled(T=6, d=128, E=16, k=1, d_ff=128,
                                                        d_ff_shared=0),
     "many_row_tiles": WORKLOADS["mixtral_prefill"].scaled(T=3072, d=512, E=8, k=2, d_ff=768),
+    # >= 512 rows per expert: 256-row weight-gradient tiles; M = 2*320 = 640 and d = 192 are
+    # not multiples of 256 (a last tile without, and one with a partial, second half)
+    "wide_tiles_ragged_m": WORKLOADS["mixtral_prefill"].scaled(T=2048, d=192, E=8, k=2,
+                                                               d_ff=320),
 }
 
 
