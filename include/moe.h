@@ -267,7 +267,7 @@ int moe_forward_fp8w(const moe_shape* s, const void* x, const void* w_router,
                      float* losses, void* ws, size_t ws_bytes, void* stream, void* const* events,
                      int n_events);
 
-/* Backward pass (training) of the layer moe_forward computes, for top-k bf16 layers.
+/* Backward pass (training) of the layer moe_forward computes, for top-k layers.
  * It returns the gradient of
  *     J = sum_t dy_t . y_t + d_aux * L_aux + d_z * L_z
  * with respect to every input of the layer, the routing decisions (top-k selection and
@@ -291,9 +291,11 @@ int moe_forward_fp8w(const moe_shape* s, const void* x, const void* w_router,
  *   GEMMs (dH = dy w2 with the SwiGLU backward in its epilogue, dXp = dG w1 + dU w3, and per
  *   expert dW1 = dG^T Xp, dW3 = dU^T Xp, dW2 = (g dy)^T H; the router's dx = dl W_r and
  *   dW_r = dl^T x), reading transposed operands MN-major instead of transposing them.
- *   Precision: bf16 operands, fp32 accumulation; G, U, H, dG, dU, g dy and the logit
- *   gradient (as a GEMM operand) are rounded to bf16; weight gradients are fp32.
- *   Requires dtype bf16, top-k gating (not expert choice), d, d_ff and d_ff_shared
+ *   Precision: bf16 layers: bf16 operands, fp32 accumulation; G, U, H, dG, dU, g dy and the
+ *   logit gradient (as a GEMM operand) are rounded to bf16; weight gradients are fp32. fp32
+ *   layers: everything in fp32 on the CUDA cores, one thread per output element (meant for
+ *   parity-scale layers), dx fp32.
+ *   Requires top-k gating (not expert choice); bf16 layers also need d, d_ff and d_ff_shared
  *   multiples of 64 and E a multiple of 8 (else MOE_ERR_UNSUPPORTED); the workspace is
  *   moe_backward_workspace_size(s) bytes (a superset of the forward's; its first 256 bytes
  *   zero before first use, like the forward's).

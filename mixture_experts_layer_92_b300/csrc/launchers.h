@@ -151,6 +151,26 @@ int launch_column_sum(const float* dl, int T, int E, float* out, cudaStream_t st
 int launch_dx_combine(const void* dxp, const int32_t* inv, const void* dxr, const void* dxs,
                       void* dx, int T, int k, int d, int num_sms, cudaStream_t stream);
 
+// fp32 layers' backward (backward_f32.cu): one thread per output element, fixed-order sums.
+// Rows of group g are offsets[g] .. offsets[g+1] (offsets == nullptr: one group of m_single).
+int launch_f32_gu(const float* a, const int32_t* offsets, int G, int m_single, int rows_max,
+                  const float* w1, const float* w3, int F, int d, float* gu, cudaStream_t st);
+int launch_f32_dh(const float* dyp, const int32_t* offsets, int G, int m_single, int rows_max,
+                  const float* w2, int F, int d, const float* gu, const int32_t* perm,
+                  const float* gate, float* dgu, float* h, float* dg_part, cudaStream_t st);
+int launch_f32_dx(const float* dgu, const int32_t* offsets, int G, int m_single, int rows_max,
+                  const float* w1, const float* w3, int F, int d, float* dxp, cudaStream_t st);
+int launch_f32_rdx(const float* dl, const float* wr, int T, int E, int d, float* dxr,
+                   cudaStream_t st);
+int launch_f32_wgrad(const float* a, int lda, const float* b, int ldb, const int32_t* offsets,
+                     int G, int m_single, int M, int N, int m_split, float* out, float* out1,
+                     cudaStream_t st);
+int launch_f32_gather_dy(const float* dy, const int32_t* perm, const int32_t* offsets,
+                         const float* gate, int E, int k, int d, int rows_max, float* dyp,
+                         float* dO, cudaStream_t st);
+int launch_f32_dx_combine(const float* dxp, const int32_t* inv, const float* dxr, const float* dxs,
+                          int T, int k, int d, float* dx, cudaStream_t st);
+
 // ---------------------------------------------------------------- CUDA-core fp32 path
 struct SimtArgs {
   int groups;               // G; offsets == nullptr means one group of m_single rows

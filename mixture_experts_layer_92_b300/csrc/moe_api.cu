@@ -687,7 +687,9 @@ BwdLayout layout_bwd(const moe_shape* s) {
   B.f = layout(s);
   const size_t T = s->T, E = s->E, k = s->k, d = s->d, F = s->d_ff, Fs = s->d_ff_shared;
   const size_t A = T * k;
-  const size_t nt = 2 * ((F + kBwdBn - 1) / kBwdBn);   // dgate partials per row
+  const size_t es = esize(s);
+  // dgate partials per row: per column tile and half (bf16), per element (fp32)
+  const size_t nt = s->dtype == MOE_BF16 ? 2 * ((F + kBwdBn - 1) / kBwdBn) : F;
   size_t o = B.f.total;
   auto take = [&](size_t bytes) {
     const size_t at = o;
@@ -695,29 +697,29 @@ BwdLayout layout_bwd(const moe_shape* s) {
     return at;
   };
   B.logits_full = take(T * E * 4);
-  B.gu = take(A * 2 * F * 2);
-  B.dyp = take(A * d * 2);
-  B.dO = take(A * d * 2);
-  B.hbuf = take(A * F * 2);
-  B.dgu = take(A * 2 * F * 2);
-  B.dxp = take(A * d * 2);
+  B.gu = take(A * 2 * F * es);
+  B.dyp = take(A * d * es);
+  B.dO = take(A * d * es);
+  B.hbuf = take(A * F * es);
+  B.dgu = take(A * 2 * F * es);
+  B.dxp = take(A * d * es);
   B.dgp = take(A * nt * 4);
   B.dgate = take(A * 4);
   B.dl = take(T * E * 4);
   B.dl16 = take(T * E * 2);
-  B.dxr = take(T * d * 2);
-  B.gus = take(T * 2 * Fs * 2);
-  B.hsb = take(T * Fs * 2);
-  B.dgus = take(T * 2 * Fs * 2);
-  B.dxs = take(Fs > 0 ? T * d * 2 : 0);
+  B.dxr = take(T * d * es);
+  B.gus = take(T * 2 * Fs * es);
+  B.hsb = take(T * Fs * es);
+  B.dgus = take(T * 2 * Fs * es);
+  B.dxs = take(Fs > 0 ? T * d * es : 0);
   B.total = o;
   return B;
 }
 
 int check_backward_shape(const moe_shape* s) {
   TRY(check_shape(s));
-  if (s->dtype != MOE_BF16) return fail(MOE_ERR_UNSUPPORTED, "the backward pass needs a bf16 layer");
   if (expert_choice(s)) return fail(MOE_ERR_UNSUPPORTED, "the backward pass needs top-k routing");
+  if (s->dtype == MOE_F32) return MOE_OK;   // CUDA-core kernels: no tile constraints
   if (s->d % 64 != 0 || s->d_ff % 64 != 0 || s->d_ff_shared % 64 != 0)
     return fail(MOE_ERR_UNSUPPORTED, "the backward pass needs d, d_ff, d_ff_shared multiples of 64");
   if (s->E % 8 != 0) return fail(MOE_ERR_UNSUPPORTED, "the backward pass needs E a multiple of 8");
@@ -844,9 +846,66 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
          "dispatch");
   // 2. gather the rows of x and of dy
   rec(1);
-  LAUNCH(launch_gather(x, perm, off, s->E, s->k, static_cast<int>(d * 2), static_cast<int>(A), xp,
-                       sms, st),
+  LAUNCH(launch_gather(x, perm, off, s->E, s->k, static_cast<int>(d * esize(s)),
+                       static_cast<int>(A), xp, sms, st),
          "gather x");
+  if (s->dtype == MOE_F32) {
+    // fp32 layers: the same steps on the CUDA cores (backward_f32.cu)
+    auto f = [](const void* p) { return static_cast<const float*>(p); };
+    auto fw = [](void* p) { return static_cast<float*>(p); };
+    const int Ai = static_cast<int>(A), Ti = s->T, Ei = s->E, di = s->d, Fi = s->d_ff,
+              Fsi = s->d_ff_shared;
+    LAUNCH(launch_f32_gather_dy(f(dy), perm, off, gate, Ei, s->k, di, Ai, fw(dyp), fw(dO), st),
+           "gather dy (fp32)");
+    rec(2);
+    LAUNCH(launch_f32_gu(f(xp), off, Ei, 0, Ai, f(w1), f(w3), Fi, di, fw(gu), st),
+           "gate/up recompute (fp32)");
+    if (shared)
+      LAUNCH(launch_f32_gu(f(x), nullptr, 1, Ti, Ti, f(w1s), f(w3s), Fsi, di, fw(gus), st),
+             "shared gate/up recompute (fp32)");
+    rec(3);
+    LAUNCH(launch_f32_dh(f(dyp), off, Ei, 0, Ai, f(w2), Fi, di, f(gu), perm, gate, fw(dgu),
+                         fw(hbuf), dgp, st),
+           "dH (fp32)");
+    if (shared)
+      LAUNCH(launch_f32_dh(f(dy), nullptr, 1, Ti, Ti, f(w2s), Fsi, di, f(gus), nullptr, nullptr,
+                           fw(dgus), fw(hsb), nullptr, st),
+             "shared dH (fp32)");
+    rec(4);
+    LAUNCH(launch_dgate(dgp, Fi, inv, Ai, dgate, st), "gate gradient");
+    LAUNCH(launch_dlogits(logits, idx, dgate, cnt, Ti, Ei, s->k, s->gate, s->alpha, s->beta,
+                          d_aux, d_z, dl, dl16, st),
+           "logit gradient");
+    if (d_router_bias != nullptr)
+      LAUNCH(launch_column_sum(dl, Ti, Ei, d_router_bias, st), "router bias gradient");
+    rec(5);
+    LAUNCH(launch_f32_dx(f(dgu), off, Ei, 0, Ai, f(w1), f(w3), Fi, di, fw(dxp), st), "dX (fp32)");
+    if (shared)
+      LAUNCH(launch_f32_dx(f(dgus), nullptr, 1, Ti, Ti, f(w1s), f(w3s), Fsi, di, fw(dxs), st),
+             "shared dX (fp32)");
+    LAUNCH(launch_f32_rdx(dl, f(w_router), Ti, Ei, di, fw(dxr), st), "router dX (fp32)");
+    rec(6);
+    LAUNCH(launch_f32_dx_combine(f(dxp), inv, f(dxr), shared ? f(dxs) : nullptr, Ti, s->k, di,
+                                 fw(dx), st),
+           "dx combine (fp32)");
+    rec(7);
+    LAUNCH(launch_f32_wgrad(f(dgu), 2 * Fi, f(xp), di, off, Ei, 0, 2 * Fi, di, Fi, dw1, dw3, st),
+           "dW1/dW3 (fp32)");
+    LAUNCH(launch_f32_wgrad(f(dO), di, f(hbuf), Fi, off, Ei, 0, di, Fi, di, dw2, nullptr, st),
+           "dW2 (fp32)");
+    LAUNCH(launch_f32_wgrad(dl, Ei, f(x), di, nullptr, 1, Ti, Ei, di, Ei, dw_router, nullptr, st),
+           "router dW (fp32)");
+    if (shared) {
+      LAUNCH(launch_f32_wgrad(f(dgus), 2 * Fsi, f(x), di, nullptr, 1, Ti, 2 * Fsi, di, Fsi, dw1s,
+                              dw3s, st),
+             "shared dW1/dW3 (fp32)");
+      LAUNCH(launch_f32_wgrad(f(dy), di, f(hsb), Fsi, nullptr, 1, Ti, di, Fsi, di, dw2s, nullptr,
+                              st),
+             "shared dW2 (fp32)");
+    }
+    rec(8);
+    return ok();
+  }
   LAUNCH(launch_gather_dy(dy, perm, off, gate, s->E, s->k, s->d, static_cast<int>(A), dyp, dO, sms,
                           st),
          "gather dy");

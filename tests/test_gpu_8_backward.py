@@ -23,7 +23,7 @@ TOL = 2e-2
 
 def run_backward(w, inp, dy, d_aux=1.0, d_z=1.0, C=None):
     C = capacity_of(w) if C is None else C
-    s = L.make_shape(w.T, w.d, w.E, w.k, w.d_ff, gate=w.gate, dtype=torch.bfloat16, capacity=C,
+    s = L.make_shape(w.T, w.d, w.E, w.k, w.d_ff, gate=w.gate, dtype=inp["x"].dtype, capacity=C,
                      d_ff_shared=w.d_ff_shared, alpha=w.alpha, beta=w.beta)
     ws = L.alloc_workspace_backward(s, DEV)
     f32 = dict(device=DEV, dtype=torch.float32)
@@ -87,7 +87,8 @@ def compare(w, g, ref):
 
 def dy_for(w, seed):
     g = torch.Generator(device=DEV).manual_seed(seed)
-    return torch.randn((w.T, w.d), generator=g, device=DEV).to(torch.bfloat16)
+    dt = torch.float32 if w.dtype == "f32" else torch.bfloat16
+    return torch.randn((w.T, w.d), generator=g, device=DEV).to(dt)
 
 
 CASES = {
@@ -151,3 +152,31 @@ def test_backward_deterministic():
     b, _ = run_backward(w, inp, dy)
     for name in ("dx", "dw_router", "dw1", "dw3", "dw2", "dw1s", "dw3s", "dw2s", "dlogits"):
         assert torch.equal(a[name], b[name]), name
+
+
+F32_CASES = {
+    "tiny_fp32": WORKLOADS["tiny_fp32"],                       # cf 1.25 with drops
+    "fp32_shared_sigmoid": WORKLOADS["deepseek_fine"].scaled(T=200, d=96, E=12, k=3, d_ff=80,
+                                                             d_ff_shared=48, dtype="f32",
+                                                             zipf_s=1.2),
+    "fp32_softmax_all_ragged": WORKLOADS["switch_top1"].scaled(T=150, d=40, E=5, k=1, d_ff=24,
+                                                               dtype="f32", cf=1.0),
+}
+
+
+@pytest.mark.parametrize("name", list(F32_CASES))
+def test_backward_fp32_matches_oracle(name):
+    """fp32 layers: every gradient within max-abs 1e-4 * RMS of the oracle's (the forward's
+    fp32 bar), on shapes without the bf16 path's tile constraints."""
+    w = F32_CASES[name]
+    inp = make_inputs(w, device=DEV, seed=3)
+    dy = dy_for(w, 4)
+    g, C = run_backward(w, inp, dy, d_aux=0.7, d_z=1.3)
+    ref = oracle_backward(w, inp, dy, g["idx"], C, d_aux=0.7, d_z=1.3)
+    names = ["dx", "dw_router", "dw1", "dw3", "dw2", "dgate", "dlogits", "d_router_bias"]
+    if w.d_ff_shared:
+        names += ["dw1s", "dw3s", "dw2s"]
+    for n in names:
+        got = g[n].double().cpu().numpy()
+        rms = np.sqrt(np.mean(ref[n] ** 2))
+        assert np.abs(got - ref[n]).max() <= 1e-4 * rms, (n, np.abs(got - ref[n]).max(), rms)
