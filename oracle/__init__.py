@@ -2,5 +2,5 @@
 (moe_backward). Test infrastructure only: the product path never imports it."""
 from .moe_oracle import *  # noqa: F401,F403
 from .moe_oracle import GATE_MODES  # noqa: F401
-from .moe_backward import (aux_loss_backward, backward, gate_backward,  # noqa: F401
-                           silu_grad, swiglu_ffn_backward, z_loss_backward)
+from .moe_backward import (aux_loss_backward, backward, expert_choice_backward,  # noqa: F401
+                           gate_backward, silu_grad, swiglu_ffn_backward, z_loss_backward)

@@ -186,3 +186,58 @@ def backward(x, w_router, w1, w3, w2, dy, *, k: int, mode: str, C: int, router_b
         out.update(dw1s=r["dw1"], dw3s=r["dw3"], dw2s=r["dw2"])
     out["dx"] = dx
     return out
+
+
+# ---------------------------------------------------------------------------------------
+# Expert-choice routing ([Starphix] "Router Variants": experts choose their tokens).
+# ---------------------------------------------------------------------------------------
+def expert_choice_backward(x, w_router, w1, w3, w2, dy, *, C: int, router_bias=None, w1s=None,
+                           w3s=None, w2s=None, alpha: float = 0.01, beta: float = 1e-3,
+                           k: int = 1, d_aux: float = 1.0, d_z: float = 1.0,
+                           choice=None) -> dict:
+    """Gradient of J = sum(dy * y) + d_aux L_aux + d_z L_z for the expert-choice layer of
+    moe_oracle.expert_choice_forward, the experts' choices held fixed (``choice`` as there).
+
+    Each row r of expert e holds token t = perm[r] with gate p[t, e] (softmax over all E), so
+    dO_r = p[t, e] dy_t and dgate_r = dy_t . O_r; the gates' gradient reaches the logits
+    through the softmax over all E: dl_t = p_t (a_t - sum_j p_tj a_tj), a[t, e] = dgate of the
+    row (t, e) or 0. f_i = C'/(T k) is the same for every expert, so L_aux = alpha E f sum_i
+    P_i = alpha E f is constant in the logits and has no gradient; the z-loss has its usual one.
+    Returns dx, dw_router, d_router_bias, dw1, dw3, dw2 (+ shared), dgate_rows [rows],
+    dlogits [T, E] and the choice dict ``ec``."""
+    from .moe_oracle import expert_choice_forward
+    x = _f64(x)
+    dy = _f64(dy)
+    T, d = x.shape
+    fwd = expert_choice_forward(x, w_router, w1, w3, w2, C=C, router_bias=router_bias,
+                                alpha=alpha, beta=beta, k=k, choice=choice)
+    ec, logits = fwd["ec"], fwd["logits"]
+    E = logits.shape[1]
+    w1, w3, w2 = _f64(w1), _f64(w3), _f64(w2)
+    dx = np.zeros((T, d))
+    dw1, dw3, dw2 = np.zeros_like(w1), np.zeros_like(w3), np.zeros_like(w2)
+    dgate_rows = np.zeros(ec["perm"].shape[0])
+    for e in range(E):
+        lo, hi = int(ec["offsets"][e]), int(ec["offsets"][e + 1])
+        if hi == lo:
+            continue
+        toks = ec["perm"][lo:hi]
+        r = swiglu_ffn_backward(x[toks], w1[e], w3[e], w2[e], ec["gate"][lo:hi][:, None] * dy[toks])
+        O = r["H"] @ w2[e].T
+        dgate_rows[lo:hi] = (dy[toks] * O).sum(axis=1)
+        np.add.at(dx, toks, r["dx"])
+        dw1[e], dw3[e], dw2[e] = r["dw1"], r["dw3"], r["dw2"]
+    a = np.where(ec["inv"] >= 0, dgate_rows[np.maximum(ec["inv"], 0)], 0.0)
+    p = softmax_all(logits)
+    dlogits = p * (a - (p * a).sum(axis=1, keepdims=True))
+    dlogits = dlogits + d_z * z_loss_backward(logits, beta)
+    dx += dlogits @ _f64(w_router)
+    out = dict(dw_router=dlogits.T @ x, d_router_bias=dlogits.sum(axis=0), dw1=dw1, dw3=dw3,
+               dw2=dw2, dw1s=None, dw3s=None, dw2s=None, dgate_rows=dgate_rows,
+               dlogits=dlogits, ec=ec)
+    if w1s is not None:
+        r = swiglu_ffn_backward(x, w1s, w3s, w2s, dy)
+        dx += r["dx"]
+        out.update(dw1s=r["dw1"], dw3s=r["dw3"], dw2s=r["dw2"])
+    out["dx"] = dx
+    return out

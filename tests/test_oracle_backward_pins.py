@@ -161,3 +161,47 @@ def test_fully_dropped_batch_has_no_expert_gradient():
                                                                 g["idx"], 0.1)
                                + O.z_loss_backward(O.router_logits(p["x"], p["w_router"]), 0.1),
                                rtol=1e-13, atol=1e-16)
+
+
+def ec_objective(p, dy, choice, *, C, alpha, beta, d_aux, d_z):
+    f = O.expert_choice_forward(p["x"], p["w_router"], p["w1"], p["w3"], p["w2"], C=C,
+                                router_bias=p["router_bias"], w1s=p["w1s"], w3s=p["w3s"],
+                                w2s=p["w2s"], alpha=alpha, beta=beta, k=2, choice=choice)
+    return float((dy * f["y"]).sum() + d_aux * f["l_aux"] + d_z * f["l_z"])
+
+
+@pytest.mark.parametrize("C,Fs,bias", [(5, 0, False), (2, 4, True), (12, 0, True)])
+def test_expert_choice_backward_matches_finite_differences(C, Fs, bias):
+    """Expert-choice layer: directional derivatives of J (choices held fixed) equal the
+    oracle's gradients for every input; C = 2 (10 choices for 12 tokens) leaves tokens no
+    expert chose, C = 12 (= T) lets every expert take every token."""
+    alpha, beta, d_aux, d_z = 0.3, 0.2, 0.7, 1.3
+    p, dy = make_case(31 + C, Fs=Fs, bias=bias)
+    g = O.expert_choice_backward(p["x"], p["w_router"], p["w1"], p["w3"], p["w2"], dy, C=C,
+                                 router_bias=p["router_bias"], w1s=p["w1s"], w3s=p["w3s"],
+                                 w2s=p["w2s"], alpha=alpha, beta=beta, k=2, d_aux=d_aux, d_z=d_z)
+    choice = dict(perm=g["ec"]["perm"], offsets=g["ec"]["offsets"], inv=g["ec"]["inv"])
+    if C == 2:
+        assert g["ec"]["unrouted"] > 0
+    rng = np.random.default_rng(8)
+    h = 1e-5
+    kw = dict(C=C, alpha=alpha, beta=beta, d_aux=d_aux, d_z=d_z)
+    for name, gname in GRAD_NAME.items():
+        if p[name] is None:
+            continue
+        v = rng.normal(size=p[name].shape)
+        fd = (ec_objective(dict(p, **{name: p[name] + h * v}), dy, choice, **kw)
+              - ec_objective(dict(p, **{name: p[name] - h * v}), dy, choice, **kw)) / (2 * h)
+        an = float((g[gname] * v).sum())
+        assert abs(fd - an) <= 1e-6 * max(1.0, abs(an)), (name, fd, an)
+
+
+def test_expert_choice_aux_loss_has_no_gradient():
+    """f_i = C'/(T k) for every expert and sum_i P_i = 1: L_aux is constant in the logits, so
+    with dy = 0 and d_z = 0 the router gets no gradient at all."""
+    p, _ = make_case(5)
+    dy = np.zeros_like(p["x"])
+    g = O.expert_choice_backward(p["x"], p["w_router"], p["w1"], p["w3"], p["w2"], dy, C=4,
+                                 alpha=0.9, beta=0.3, d_aux=1.0, d_z=0.0)
+    np.testing.assert_allclose(g["dlogits"], 0.0, atol=1e-16)
+    np.testing.assert_allclose(g["dw_router"], 0.0, atol=1e-15)
