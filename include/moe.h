@@ -267,7 +267,8 @@ int moe_forward_fp8w(const moe_shape* s, const void* x, const void* w_router,
                      float* losses, void* ws, size_t ws_bytes, void* stream, void* const* events,
                      int n_events);
 
-/* Backward pass (training) of the layer moe_forward computes, for top-k layers.
+/* Backward pass (training) of the layer moe_forward computes, for top-k and expert-choice
+ * layers.
  * It returns the gradient of
  *     J = sum_t dy_t . y_t + d_aux * L_aux + d_z * L_z
  * with respect to every input of the layer, the routing decisions (top-k selection and
@@ -286,6 +287,13 @@ int moe_forward_fp8w(const moe_shape* s, const void* x, const void* w_router,
  *   d_router_bias [E] fp32 (nullable); dlogits [T, E] and dgate [T, k] fp32 (nullable: the
  *   intermediate gradients of the logits and of the gates, 0 for dropped assignments).
  *   An expert that receives no rows gets a zero gradient; T = 0 zeroes every gradient.
+ *   Expert-choice layers (gate = MOE_GATE_EXPERT_CHOICE; "Mixture of Experts (MoE)",
+ *   learn.starphix.com, Router Variants): the experts' choices (moe_expert_choice) are held
+ *   fixed; row r of expert e holds token perm[r] with gate p[perm[r]][e] of the softmax over
+ *   all E, so the gates' gradient reaches the logits through that softmax. dgate is then per
+ *   row: [E * min(capacity, T)] in moe_expert_choice's perm order. Every expert takes the
+ *   same number of tokens, so f_i is the same for all i and L_aux = alpha E f sum_i P_i =
+ *   alpha E f is constant: it has no gradient (d_aux is ignored); the z-loss has its usual one.
  *   Nothing is saved between calls: the call recomputes the routing, the dispatch and the
  *   pre-activations G = Xp w1^T, U = Xp w3^T on the tensor cores, then runs the backward
  *   GEMMs (dH = dy w2 with the SwiGLU backward in its epilogue, dXp = dG w1 + dU w3, and per
@@ -295,7 +303,7 @@ int moe_forward_fp8w(const moe_shape* s, const void* x, const void* w_router,
  *   logit gradient (as a GEMM operand) are rounded to bf16; weight gradients are fp32. fp32
  *   layers: everything in fp32 on the CUDA cores, one thread per output element (meant for
  *   parity-scale layers), dx fp32.
- *   Requires top-k gating (not expert choice); bf16 layers also need d, d_ff and d_ff_shared
+ *   bf16 layers need d, d_ff and d_ff_shared
  *   multiples of 64 and E a multiple of 8 (else MOE_ERR_UNSUPPORTED); the workspace is
  *   moe_backward_workspace_size(s) bytes (a superset of the forward's; its first 256 bytes
  *   zero before first use, like the forward's).

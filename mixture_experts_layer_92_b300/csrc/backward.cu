@@ -13,6 +13,11 @@
 // column_sum  : router-bias gradient, sum over tokens in token order
 // dx_combine  : dx_t = sum over the token's kept slots of dXp[row] + the router's and the
 //               shared expert's dx, fp32 sums in slot order, bf16 out
+//
+// Expert-choice layers ("Mixture of Experts (MoE)", learn.starphix.com, Router Variants) use
+// the same kernels with rows in place of assignments: row r of expert e holds token perm[r]
+// with gate p[t][e], dgate is per row, and inv is the dense [T, E] map of pairs to rows (-1:
+// expert e did not choose token t), so the combine runs over E slots per token.
 #include <algorithm>
 
 #include "common.cuh"
@@ -33,13 +38,14 @@ int grid_for(long long warps, int num_sms) {
 __global__ void __launch_bounds__(kThreads)
 gather_dy_kernel(const uint4* __restrict__ dy, const int32_t* __restrict__ perm,
                  const int32_t* __restrict__ offsets, const float* __restrict__ gate, int E,
-                 int k, int nvec, uint4* __restrict__ dyp, uint4* __restrict__ dO) {
+                 int k, int gate_by_row, int nvec, uint4* __restrict__ dyp,
+                 uint4* __restrict__ dO) {
   const int R = offsets[E];
   const int lane = threadIdx.x & 31;
   const int nw = gridDim.x * kWarps;
   for (int r = blockIdx.x * kWarps + (threadIdx.x >> 5); r < R; r += nw) {
     const int a = perm[r];
-    const float g = gate[a];
+    const float g = gate[gate_by_row ? r : a];
     const uint4* src = dy + static_cast<size_t>(a / k) * nvec;
     uint4* d0 = dyp + static_cast<size_t>(r) * nvec;
     uint4* d1 = dO + static_cast<size_t>(r) * nvec;
@@ -60,7 +66,7 @@ __global__ void dgate_kernel(const float* __restrict__ dg_part, int n_tiles,
                              const int32_t* __restrict__ inv, int A, float* __restrict__ dgate) {
   const int a = blockIdx.x * blockDim.x + threadIdx.x;
   if (a >= A) return;
-  const int r = inv[a];
+  const int r = inv != nullptr ? inv[a] : a;
   float s = 0.0f;
   if (r >= 0)
     for (int j = 0; j < n_tiles; ++j) s += dg_part[static_cast<size_t>(r) * n_tiles + j];
@@ -97,7 +103,22 @@ dlogits_kernel(const float* __restrict__ logits, const int32_t* __restrict__ idx
     pa = warp_sum(pa);
     for (int j = lane; j < E; j += 32) gterm[j] = 0.0f;
     __syncwarp();
-    if (gate_mode == MOE_GATE_SOFTMAX_ALL) {
+    if (gate_mode == MOE_GATE_EXPERT_CHOICE) {
+      // expert choice: idx holds inv [T, E] (row of the pair (t, j) or -1) and dgate is per
+      // row; every chosen pair's gate is p_j of the softmax over all E, so as for softmax_all
+      // dl_j = p_j (a_j - sum_i p_i a_i) with a_j = dgate of the pair's row, or 0
+      const int32_t* iv = idx + static_cast<size_t>(t) * E;
+      float c = 0.0f;
+      for (int j = lane; j < E; j += 32) {
+        const int r = iv[j];
+        const float pa_j = r >= 0 ? __expf(l[j] - m) * inv_s * dgate[r] : 0.0f;
+        gterm[j] = pa_j;
+        c += pa_j;
+      }
+      c = warp_sum(c);
+      for (int j = lane; j < E; j += 32) gterm[j] -= __expf(l[j] - m) * inv_s * c;
+      __syncwarp();
+    } else if (gate_mode == MOE_GATE_SOFTMAX_ALL) {
       // g_s = p_{i_s}: dl_j = p_j (a_j - sum_i p_i a_i), a = dgate scattered onto the experts
       float c = 0.0f;
       for (int sl = lane; sl < k; sl += 32) c += __expf(l[ix[sl]] - m) * inv_s * dg[sl];
@@ -200,11 +221,12 @@ dx_combine_kernel(const uint4* __restrict__ dxp, const int32_t* __restrict__ inv
 }  // namespace
 
 int launch_gather_dy(const void* dy, const int32_t* perm, const int32_t* offsets, const float* gate,
-                     int E, int k, int d, int max_rows, void* dyp, void* dO, int num_sms,
-                     cudaStream_t stream) {
+                     int E, int k, int gate_by_row, int d, int max_rows, void* dyp, void* dO,
+                     int num_sms, cudaStream_t stream) {
   if (max_rows <= 0) return MOE_OK;
   gather_dy_kernel<<<grid_for(max_rows, num_sms), kThreads, 0, stream>>>(
-      static_cast<const uint4*>(dy), perm, offsets, gate, E, k, d / 8, static_cast<uint4*>(dyp),
+      static_cast<const uint4*>(dy), perm, offsets, gate, E, k, gate_by_row, d / 8,
+      static_cast<uint4*>(dyp),
       static_cast<uint4*>(dO));
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

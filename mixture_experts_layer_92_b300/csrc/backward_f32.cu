@@ -88,7 +88,7 @@ __global__ void f32_dh_kernel(const float* __restrict__ dyp, const int32_t* __re
     const float sg = 1.0f / (1.0f + expf(-gz));
     const float si = gz * sg;
     const float dsi = sg * (1.0f + gz * (1.0f - sg));
-    const float gr = gate != nullptr ? gate[perm[r]] : 1.0f;
+    const float gr = gate == nullptr ? 1.0f : perm != nullptr ? gate[perm[r]] : gate[r];
     const float dh = gr * raw;
     const float hv = si * uz;
     dgu[static_cast<size_t>(r) * 2 * F + f] = dh * uz * dsi;
@@ -156,8 +156,8 @@ __global__ void f32_wgrad_kernel(const float* __restrict__ a, int lda, const flo
 
 __global__ void f32_gather_dy_kernel(const float* __restrict__ dy, const int32_t* __restrict__ perm,
                                      const int32_t* __restrict__ offsets, const float* __restrict__ gate,
-                                     int E, int k, int d, int rows_max, float* __restrict__ dyp,
-                                     float* __restrict__ dO) {
+                                     int E, int k, int gate_by_row, int d, int rows_max,
+                                     float* __restrict__ dyp, float* __restrict__ dO) {
   const int R = offsets[E];
   const long long total = static_cast<long long>(rows_max) * d;
   for (long long i = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; i < total;
@@ -167,7 +167,7 @@ __global__ void f32_gather_dy_kernel(const float* __restrict__ dy, const int32_t
     const int a = perm[r];
     const float v = dy[static_cast<size_t>(a / k) * d + j];
     dyp[i] = v;
-    dO[i] = gate[a] * v;
+    dO[i] = gate[gate_by_row ? r : a] * v;
   }
 }
 
@@ -234,11 +234,11 @@ int launch_f32_wgrad(const float* a, int lda, const float* b, int ldb, const int
 }
 
 int launch_f32_gather_dy(const float* dy, const int32_t* perm, const int32_t* offsets,
-                         const float* gate, int E, int k, int d, int rows_max, float* dyp,
-                         float* dO, cudaStream_t st) {
+                         const float* gate, int E, int k, int gate_by_row, int d,
+                         int rows_max, float* dyp, float* dO, cudaStream_t st) {
   if (rows_max <= 0) return MOE_OK;
   f32_gather_dy_kernel<<<grid_of(static_cast<long long>(rows_max) * d), kT, 0, st>>>(
-      dy, perm, offsets, gate, E, k, d, rows_max, dyp, dO);
+      dy, perm, offsets, gate, E, k, gate_by_row, d, rows_max, dyp, dO);
   return last_error();
 }
 

@@ -113,7 +113,8 @@ struct BwdArgs {
   void* h;                  // out: H = silu(G) U, bf16 [rows, N]
   float* dg_part;           // out (nullable): per row, column tile and column half,
   int n_tiles;              //   sum_f dH_raw * H: [rows, n_tiles] with n_tiles = 2 * tiles
-  const int32_t* perm;      // gate of row r = gate[perm[r]] (gate == nullptr: 1)
+  const int32_t* perm;      // gate of row r = gate[perm[r]], or gate[r] when perm == nullptr
+                            //   (expert-choice rows); gate == nullptr: 1
   const float* gate;
   DeviceError* err;
 };
@@ -134,14 +135,18 @@ struct BwdProblem {
 int launch_bwd_gemm(int mode, int bn, int mt, const BwdProblem& p, cudaStream_t stream);
 
 // Non-GEMM steps of the backward pass (backward.cu)
-// dyp[r] = dy[perm[r] / k], dO[r] = gate[perm[r]] * dy[perm[r] / k] (bf16), r < offsets[E]
+// dyp[r] = dy[perm[r] / k], dO[r] = g_r * dy[perm[r] / k] (bf16), r < offsets[E], with
+// g_r = gate[perm[r]] (top-k: perm holds assignments) or gate[r] (gate_by_row: expert-choice
+// rows, perm holds tokens and k = 1)
 int launch_gather_dy(const void* dy, const int32_t* perm, const int32_t* offsets, const float* gate,
-                     int E, int k, int d, int max_rows, void* dyp, void* dO, int num_sms,
-                     cudaStream_t stream);
-// dgate[a] = sum_j dg_part[inv[a]][j] (fixed order), 0 for a dropped assignment
+                     int E, int k, int gate_by_row, int d, int max_rows, void* dyp, void* dO,
+                     int num_sms, cudaStream_t stream);
+// dgate[a] = sum_j dg_part[inv[a]][j] (fixed order), 0 for a dropped assignment; inv == NULL:
+// dgate[r] = sum_j dg_part[r][j] for every row r < A (expert-choice rows)
 int launch_dgate(const float* dg_part, int n_tiles, const int32_t* inv, int A, float* dgate,
                  cudaStream_t stream);
-// dl = dJ/dlogits [T, E] (fp32, and a bf16 copy) from the gate, balance and z-loss terms
+// dl = dJ/dlogits [T, E] (fp32, and a bf16 copy) from the gate, balance and z-loss terms;
+// expert choice (gate_mode MOE_GATE_EXPERT_CHOICE): idx = inv [T, E], dgate per row
 int launch_dlogits(const float* logits, const int32_t* idx, const float* dgate,
                    const int32_t* counts, int T, int E, int k, int gate_mode, float alpha,
                    float beta, float d_aux, float d_z, float* dl, void* dl16, cudaStream_t stream);
@@ -166,8 +171,8 @@ int launch_f32_wgrad(const float* a, int lda, const float* b, int ldb, const int
                      int G, int m_single, int M, int N, int m_split, float* out, float* out1,
                      cudaStream_t st);
 int launch_f32_gather_dy(const float* dy, const int32_t* perm, const int32_t* offsets,
-                         const float* gate, int E, int k, int d, int rows_max, float* dyp,
-                         float* dO, cudaStream_t st);
+                         const float* gate, int E, int k, int gate_by_row, int d,
+                         int rows_max, float* dyp, float* dO, cudaStream_t st);
 int launch_f32_dx_combine(const float* dxp, const int32_t* inv, const float* dxr, const float* dxs,
                           int T, int k, int d, float* dx, cudaStream_t st);
 

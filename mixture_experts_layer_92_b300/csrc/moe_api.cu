@@ -685,8 +685,8 @@ constexpr int kBwdBn = 256;
 BwdLayout layout_bwd(const moe_shape* s) {
   BwdLayout B;
   B.f = layout(s);
-  const size_t T = s->T, E = s->E, k = s->k, d = s->d, F = s->d_ff, Fs = s->d_ff_shared;
-  const size_t A = T * k;
+  const size_t T = s->T, E = s->E, d = s->d, F = s->d_ff, Fs = s->d_ff_shared;
+  const size_t A = perm_rows(s);  // rows: assignments (top-k) or expert-choice rows
   const size_t es = esize(s);
   // dgate partials per row: per column tile and half (bf16), per element (fp32)
   const size_t nt = s->dtype == MOE_BF16 ? 2 * ((F + kBwdBn - 1) / kBwdBn) : F;
@@ -718,7 +718,6 @@ BwdLayout layout_bwd(const moe_shape* s) {
 
 int check_backward_shape(const moe_shape* s) {
   TRY(check_shape(s));
-  if (expert_choice(s)) return fail(MOE_ERR_UNSUPPORTED, "the backward pass needs top-k routing");
   if (s->dtype == MOE_F32) return MOE_OK;   // CUDA-core kernels: no tile constraints
   if (s->d % 64 != 0 || s->d_ff % 64 != 0 || s->d_ff_shared % 64 != 0)
     return fail(MOE_ERR_UNSUPPORTED, "the backward pass needs d, d_ff, d_ff_shared multiples of 64");
@@ -791,7 +790,13 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
     if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
   };
   const size_t T = s->T, E = s->E, d = s->d, F = s->d_ff, Fs = s->d_ff_shared;
-  const size_t A = T * s->k;
+  const bool ec = expert_choice(s);
+  // rows of the permuted activations: T*k assignments, or E*min(C, T) expert-choice rows
+  // (whose gate is indexed by the row: perm holds tokens, inv is the dense [T, E] map)
+  const size_t A = perm_rows(s);
+  const int gather_k = ec ? 1 : s->k;
+  const int combine_k = ec ? s->E : s->k;
+  const int32_t* gate_perm = nullptr;
   if (s->T == 0) {
     // no tokens: every gradient is 0
     auto zero = [&](void* p, size_t bytes) {
@@ -834,19 +839,36 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
   const long long row_tiles = static_cast<long long>((A + 127) / 128) + static_cast<long long>(E);
   const long long row_tiles_T = static_cast<long long>((T + 127) / 128);
 
-  // 1. recompute the routing: logits (with bias), top-k, gates, dispatch
+  // 1. recompute the routing: logits (with bias), top-k, gates, dispatch -- or the experts'
+  //    choices and their gates
   rec(0);
   TRY(run_router(s, x, w_router, at<float>(ws, L.logits), err, st));
-  LAUNCH(launch_route_topk(route_args(s, at<float>(ws, L.logits), router_split(s).splits,
-                                      router_bias, logits, idx, gate, at<float>(ws, L.partials), err),
-                           st),
-         "gates/top-k");
-  LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, cnt, off, perm, inv,
-                         at<int32_t>(ws, L.dropped), at<int32_t>(ws, L.blk_hist), err, sms, st),
-         "dispatch");
+  {
+    RouteArgs ra = route_args(s, at<float>(ws, L.logits), router_split(s).splits, router_bias,
+                              logits, idx, gate, at<float>(ws, L.partials), err);
+    if (ec) {
+      ra.k = 0;  // logits and probabilities only
+      ra.probs_t = at<float>(ws, L.probs);
+    }
+    LAUNCH(launch_route_topk(ra, st), "gates/top-k");
+  }
+  if (ec) {
+    LAUNCH(launch_expert_choice(at<float>(ws, L.probs), s->T, s->E, s->capacity, perm, gate, inv,
+                                cnt, off, at<int32_t>(ws, L.dropped), st),
+           "expert choice");
+  } else {
+    gate_perm = perm;
+    LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, cnt, off, perm, inv,
+                           at<int32_t>(ws, L.dropped), at<int32_t>(ws, L.blk_hist), err, sms, st),
+           "dispatch");
+  }
+  // inputs of the logit gradient: top-k indices with per-assignment gate gradients, or the
+  // dense pair-to-row map with per-row ones; the balance loss is constant under expert choice
+  const int32_t* dl_sel = ec ? inv : idx;
+  const float dl_aux = ec ? 0.0f : d_aux;
   // 2. gather the rows of x and of dy
   rec(1);
-  LAUNCH(launch_gather(x, perm, off, s->E, s->k, static_cast<int>(d * esize(s)),
+  LAUNCH(launch_gather(x, perm, off, s->E, gather_k, static_cast<int>(d * esize(s)),
                        static_cast<int>(A), xp, sms, st),
          "gather x");
   if (s->dtype == MOE_F32) {
@@ -855,7 +877,8 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
     auto fw = [](void* p) { return static_cast<float*>(p); };
     const int Ai = static_cast<int>(A), Ti = s->T, Ei = s->E, di = s->d, Fi = s->d_ff,
               Fsi = s->d_ff_shared;
-    LAUNCH(launch_f32_gather_dy(f(dy), perm, off, gate, Ei, s->k, di, Ai, fw(dyp), fw(dO), st),
+    LAUNCH(launch_f32_gather_dy(f(dy), perm, off, gate, Ei, gather_k, ec, di, Ai, fw(dyp),
+                                fw(dO), st),
            "gather dy (fp32)");
     rec(2);
     LAUNCH(launch_f32_gu(f(xp), off, Ei, 0, Ai, f(w1), f(w3), Fi, di, fw(gu), st),
@@ -864,7 +887,7 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
       LAUNCH(launch_f32_gu(f(x), nullptr, 1, Ti, Ti, f(w1s), f(w3s), Fsi, di, fw(gus), st),
              "shared gate/up recompute (fp32)");
     rec(3);
-    LAUNCH(launch_f32_dh(f(dyp), off, Ei, 0, Ai, f(w2), Fi, di, f(gu), perm, gate, fw(dgu),
+    LAUNCH(launch_f32_dh(f(dyp), off, Ei, 0, Ai, f(w2), Fi, di, f(gu), gate_perm, gate, fw(dgu),
                          fw(hbuf), dgp, st),
            "dH (fp32)");
     if (shared)
@@ -872,9 +895,9 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
                            fw(dgus), fw(hsb), nullptr, st),
              "shared dH (fp32)");
     rec(4);
-    LAUNCH(launch_dgate(dgp, Fi, inv, Ai, dgate, st), "gate gradient");
-    LAUNCH(launch_dlogits(logits, idx, dgate, cnt, Ti, Ei, s->k, s->gate, s->alpha, s->beta,
-                          d_aux, d_z, dl, dl16, st),
+    LAUNCH(launch_dgate(dgp, Fi, ec ? nullptr : inv, Ai, dgate, st), "gate gradient");
+    LAUNCH(launch_dlogits(logits, dl_sel, dgate, cnt, Ti, Ei, s->k, s->gate, s->alpha, s->beta,
+                          dl_aux, d_z, dl, dl16, st),
            "logit gradient");
     if (d_router_bias != nullptr)
       LAUNCH(launch_column_sum(dl, Ti, Ei, d_router_bias, st), "router bias gradient");
@@ -885,7 +908,7 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
              "shared dX (fp32)");
     LAUNCH(launch_f32_rdx(dl, f(w_router), Ti, Ei, di, fw(dxr), st), "router dX (fp32)");
     rec(6);
-    LAUNCH(launch_f32_dx_combine(f(dxp), inv, f(dxr), shared ? f(dxs) : nullptr, Ti, s->k, di,
+    LAUNCH(launch_f32_dx_combine(f(dxp), inv, f(dxr), shared ? f(dxs) : nullptr, Ti, combine_k, di,
                                  fw(dx), st),
            "dx combine (fp32)");
     rec(7);
@@ -906,8 +929,8 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
     rec(8);
     return ok();
   }
-  LAUNCH(launch_gather_dy(dy, perm, off, gate, s->E, s->k, s->d, static_cast<int>(A), dyp, dO, sms,
-                          st),
+  LAUNCH(launch_gather_dy(dy, perm, off, gate, s->E, gather_k, ec, s->d, static_cast<int>(A), dyp,
+                          dO, sms, st),
          "gather dy");
   // 3. recompute the pre-activations G | U (routed experts and the shared expert)
   rec(2);
@@ -954,7 +977,7 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
     p.args.h = hbuf;
     p.args.dg_part = dgp;
     p.args.n_tiles = nt;
-    p.args.perm = perm;
+    p.args.perm = gate_perm;
     p.args.gate = gate;
     p.args.err = err;
     p.a = dyp;
@@ -985,9 +1008,9 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
   }
   // 5. gate gradients -> router logit gradients (gates, balance loss, z-loss)
   rec(4);
-  LAUNCH(launch_dgate(dgp, nt, inv, static_cast<int>(A), dgate, st), "gate gradient");
-  LAUNCH(launch_dlogits(logits, idx, dgate, cnt, s->T, s->E, s->k, s->gate, s->alpha, s->beta,
-                        d_aux, d_z, dl, dl16, st),
+  LAUNCH(launch_dgate(dgp, nt, ec ? nullptr : inv, static_cast<int>(A), dgate, st), "gate gradient");
+  LAUNCH(launch_dlogits(logits, dl_sel, dgate, cnt, s->T, s->E, s->k, s->gate, s->alpha, s->beta,
+                        dl_aux, d_z, dl, dl16, st),
          "logit gradient");
   if (d_router_bias != nullptr)
     LAUNCH(launch_column_sum(dl, s->T, s->E, d_router_bias, st), "router bias gradient");
@@ -1045,7 +1068,7 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
     TRY(bwd_gemm(BW_DGRAD_X, r, row_tiles_T, st, "router dX GEMM (tcgen05)"));
   }
   rec(6);
-  LAUNCH(launch_dx_combine(dxp, inv, dxr, dxs, dx, s->T, s->k, s->d, sms, st), "dx combine");
+  LAUNCH(launch_dx_combine(dxp, inv, dxr, dxs, dx, s->T, combine_k, s->d, sms, st), "dx combine");
   // 7. weight gradients: per expert dW1 | dW3 = [dG dU]^T Xp, dW2 = (g dy)^T H; router; shared
   rec(7);
   {

@@ -461,7 +461,8 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
           }
         } else {  // BW_DGRAD_H
           float g_r = 1.0f;
-          if (rvalid && args.gate != nullptr) g_r = args.gate[args.perm[row]];
+          if (rvalid && args.gate != nullptr)
+            g_r = args.perm != nullptr ? args.gate[args.perm[row]] : args.gate[row];
           const __nv_bfloat16* gu = static_cast<const __nv_bfloat16*>(args.gu) + row * 2 * N;
           __nv_bfloat16* dgu = static_cast<__nv_bfloat16*>(args.dgu) + row * 2 * N;
           __nv_bfloat16* hrow = static_cast<__nv_bfloat16*>(args.h) + row * N;

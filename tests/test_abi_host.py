@@ -124,15 +124,17 @@ def test_status_strings():
 
 
 @pytest.mark.parametrize("kw", [
-    dict(gate="expert_choice"), dict(d=96), dict(d_ff=200), dict(d_ff_shared=96), dict(E=12, k=2),
+    dict(d=96), dict(d_ff=200), dict(d_ff_shared=96), dict(E=12, k=2),
 ])
 def test_backward_unsupported_shapes(kw):
-    """The backward pass needs a top-k layer; bf16 layers also need d, d_ff, d_ff_shared
-    multiples of 64 and E a multiple of 8: anything else is refused on the host (workspace
-    size 0). fp32 layers have no tile constraints."""
+    """bf16 layers need d, d_ff, d_ff_shared multiples of 64 and E a multiple of 8 for the
+    backward pass: anything else is refused on the host (workspace size 0). fp32 layers have
+    no tile constraints; expert-choice layers are supported."""
     s = shape(**kw)
     assert moe.moe_backward_workspace_size(s) == 0
     assert moe.moe_backward_workspace_size(shape(dtype=torch.float32, d=96, d_ff=200, E=12)) > 0
+    ec = shape(gate="expert_choice", capacity=40)
+    assert moe.moe_backward_workspace_size(ec) > moe.moe_workspace_size(ec) > 0
 
 
 def test_backward_rejects_before_any_launch():
@@ -156,4 +158,4 @@ def test_backward_rejects_before_any_launch():
     s2 = shape(d_ff_shared=128)
     assert call(shp=s2, nbytes=moe.moe_backward_workspace_size(s2)) == -1   # shared grads missing
     assert call(ev=(ctypes.c_void_p * 3)(), nev=3) == -1
-    assert call(shp=shape(gate="expert_choice")) == -2
+    assert call(shp=shape(d=96)) == -2

@@ -124,3 +124,88 @@ def test_full_size_backward(name):
     assert err < TOL
     del inp, g, ws
     torch.cuda.empty_cache()
+
+
+def test_full_size_backward_expert_choice():
+    """The Mixtral prefill layer with expert-choice routing (C = T k / E = 1024 tokens per
+    expert), checked like the top-k layers: sampled hidden units of two experts, and the
+    gradients of sampled tokens through every expert that chose them (the oracle runs on the
+    GPU's own choices; the balance loss has no gradient under expert choice)."""
+    from mixture_experts_layer_92_b300 import _lib as L
+    w = WORKLOADS["mixtral_prefill"].scaled(gate="expert_choice", cf=1.0)
+    inp = make_inputs(w, device=DEV)
+    C = capacity_of(w)
+    R = w.E * min(C, w.T)
+    gen = torch.Generator(device=DEV).manual_seed(12)
+    dy = torch.randn(inp["x"].shape, generator=gen, device=DEV).to(torch.bfloat16)
+    s = L.make_shape(w.T, w.d, w.E, w.k, w.d_ff, gate=w.gate, dtype=torch.bfloat16, capacity=C,
+                     alpha=w.alpha, beta=w.beta)
+    ws = L.alloc_workspace_backward(s, DEV)
+    f32 = dict(device=DEV, dtype=torch.float32)
+    g = dict(dx=torch.empty_like(inp["x"]), dw_router=torch.empty((w.E, w.d), **f32),
+             dw1=torch.empty((w.E, w.d_ff, w.d), **f32), dw3=torch.empty((w.E, w.d_ff, w.d), **f32),
+             dw2=torch.empty((w.E, w.d, w.d_ff), **f32), dlogits=torch.empty((w.T, w.E), **f32),
+             dgate=torch.empty((R,), **f32))
+    L.moe_backward(s, ws, inp["x"], inp["w_router"], inp["w1"], inp["w3"], inp["w2"], dy,
+                   g["dx"], g["dw_router"], g["dw1"], g["dw3"], g["dw2"],
+                   dlogits=g["dlogits"], dgate=g["dgate"])
+    perm = torch.empty(R, dtype=torch.int32, device=DEV)
+    offsets = torch.empty(w.E + 1, dtype=torch.int32, device=DEV)
+    row_gate = torch.empty(R, device=DEV)
+    inv = torch.empty(w.T * w.E, dtype=torch.int32, device=DEV)
+    counts = torch.empty(w.E, dtype=torch.int32, device=DEV)
+    unrouted = torch.empty(1, dtype=torch.int32, device=DEV)
+    L.moe_expert_choice(s, L.alloc_workspace(s, DEV), perm, offsets, row_gate, inv, counts,
+                        unrouted, x=inp["x"], w_router=inp["w_router"])
+    torch.cuda.synchronize()
+    assert L.moe_get_error(ws) == 0
+    perm_h, offs = perm.cpu().numpy(), offsets.cpu().numpy()
+    inv_h = inv.cpu().numpy().reshape(w.T, w.E)
+
+    x64, dy64, wr64 = host64(inp["x"]), host64(dy), host64(inp["w_router"])
+    logits64 = O.router_logits(x64, wr64)
+    p64 = O.softmax_all(logits64)
+    rng = np.random.default_rng(4)
+
+    for e in sorted(rng.choice(w.E, size=2, replace=False)):
+        toks = perm_h[offs[e]:offs[e + 1]]
+        fs = np.sort(rng.choice(w.d_ff, size=16, replace=False))
+        fs_t = torch.as_tensor(fs, device=DEV)
+        r = O.swiglu_ffn_backward(x64[toks], host64(inp["w1"][e][fs_t]), host64(inp["w3"][e][fs_t]),
+                                  host64(inp["w2"][e][:, fs_t]), p64[toks, e][:, None] * dy64[toks])
+        assert rel_l2(g["dw1"][e][fs_t].double().cpu().numpy(), r["dw1"]) < TOL, ("dw1", e)
+        assert rel_l2(g["dw3"][e][fs_t].double().cpu().numpy(), r["dw3"]) < TOL, ("dw3", e)
+        assert rel_l2(g["dw2"][e][:, fs_t].double().cpu().numpy(), r["dw2"]) < TOL, ("dw2", e)
+
+    tokens = np.sort(rng.choice(w.T, size=6, replace=False))
+    dz = O.z_loss_backward(logits64, w.beta)
+    dx_ref, dl_ref, dg_ref, dg_got = [], [], [], []
+    dgate_h = g["dgate"].double().cpu().numpy()
+    cache = {}
+    for t in tokens:
+        dxt = np.zeros(w.d)
+        a = np.zeros(w.E)
+        for e in range(w.E):
+            r_ = inv_h[t, e]
+            if r_ < 0:
+                continue
+            if e not in cache:
+                cache[e] = (host64(inp["w1"][e]), host64(inp["w3"][e]), host64(inp["w2"][e]))
+            w1e, w3e, w2e = cache[e]
+            rb = O.swiglu_ffn_backward(x64[t:t + 1], w1e, w3e, w2e, p64[t, e] * dy64[t:t + 1])
+            dxt += rb["dx"][0]
+            a[e] = float(dy64[t] @ (rb["H"][0] @ w2e.T))
+            dg_ref.append(a[e])
+            dg_got.append(dgate_h[r_])
+        dlt = p64[t] * (a - p64[t] @ a) + dz[t]
+        dx_ref.append(dxt + dlt @ wr64)
+        dl_ref.append(dlt)
+    tt = torch.as_tensor(tokens, device=DEV)
+    assert len(dg_ref) > 0
+    assert rel_l2(np.array(dg_got), np.array(dg_ref)) < TOL
+    assert rel_l2(g["dlogits"][tt].double().cpu().numpy(), np.array(dl_ref)) < TOL
+    err = rel_l2(g["dx"][tt].double().cpu().numpy(), np.array(dx_ref))
+    print(f"mixtral_prefill + expert choice: sampled dx rel L2 = {err:.3e}")
+    assert err < TOL
+    del inp, g, ws
+    torch.cuda.empty_cache()
