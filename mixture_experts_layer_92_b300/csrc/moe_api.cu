@@ -959,10 +959,16 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
     p.b0_s = w1s;
     p.b1_s = w3s;
     p.b_rows_s = s->d_ff_shared;
-    p.max_tiles = (row_tiles) * ((s->d_ff + 127) / 128) +
-                  (shared ? row_tiles_T * ((s->d_ff_shared + 127) / 128) : 0);
+    // the forward's row-tile policy: 256-row tiles when experts average >= 512 rows
+    const int mt_gu = (A / s->E >= 512) ? 2 : 1;
+    const long long tm = 128ll * mt_gu;
+    p.max_tiles = (static_cast<long long>((A + tm - 1) / tm) + static_cast<long long>(E)) *
+                      ((s->d_ff + 127) / 128) +
+                  (shared ? static_cast<long long>((T + tm - 1) / tm) * ((s->d_ff_shared + 127) / 128)
+                          : 0);
     p.num_sms = sms;
-    LAUNCH(launch_tc_gemm(TC_SWIGLU, 256, 1, 64, false, 128, p, st), "gate/up recompute (tcgen05)");
+    LAUNCH(launch_tc_gemm(TC_SWIGLU, 256, mt_gu, 64, false, 128, p, st),
+           "gate/up recompute (tcgen05)");
   }
   // 4. dH_raw = dy W2 with the SwiGLU backward and the gate-gradient partials
   rec(3);
