@@ -87,6 +87,9 @@ struct TcProblem {
 //     any group size, efficient when no group has more than 32 rows).
 int launch_tc_gemm(int mode, int bn, int mt, int kb, bool w8, int ar, const TcProblem& p,
                    cudaStream_t stream);
+// The same GEMMs (TC_SWIGLU or TC_SCALE, bf16, BN = 256, no 8-bit weights) with 256-row
+// tiles on CTA pairs (tc_pair.cu); p.max_tiles counts 256-row tiles.
+int launch_tc_pair_gemm(int mode, const TcProblem& p, cudaStream_t stream);
 
 // ---------------------------------------------------------------- tcgen05 backward GEMMs
 enum BwdMode : int {

@@ -387,6 +387,12 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
   const bool w8 = q != nullptr;  // 8-bit weights: 128-row tiles only
   const int mt_gateup = (!w8 && kept_max / s->E >= 512) ? 2 : 1;
   const int mt_down = (!w8 && kept_max / s->E >= 512 && s->d_ff >= 8192) ? 2 : 1;
+  // 256-row tiles on CTA pairs (tc_pair.cu): both halves' accumulators double-buffered, but
+  // a pair always multiplies 256 rows, where a single CTA skips the empty second half of a
+  // group's last tile. So pairs only where the host knows every group's size and the last
+  // tile is more than half full: expert-choice layers, each expert holding min(C, T) rows.
+  const int ec_rows = std::min(s->capacity, s->T);
+  const bool pair_tiles = expert_choice(s) && (ec_rows % 256 == 0 || ec_rows % 256 > 128);
   const int kb_gateup = 64, kb_down = 64;
   // Gate/up MMA width with 128-row tiles: 256 (128 H columns per tile) or 224 (112), which
   // ever leaves fewer SMs idle in the last wave of the estimated tile count (e.g. the
@@ -446,7 +452,10 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.max_tiles = (row_tiles(mt_gateup, kept_max) + s->E) * ((s->d_ff + bno - 1) / bno) +
                   (shared ? row_tiles(mt_gateup, s->T) * ((s->d_ff_shared + bno - 1) / bno) : 0);
     p.num_sms = sms;
-    LAUNCH(launch_tc_gemm(TC_SWIGLU, bn_gateup, mt_gateup, kb_gateup, w8, ar, p, st),
+    if (mt_gateup == 2 && pair_tiles)
+      LAUNCH(launch_tc_pair_gemm(TC_SWIGLU, p, st), "gate/up GEMM (tcgen05, CTA pairs)");
+    else
+      LAUNCH(launch_tc_gemm(TC_SWIGLU, bn_gateup, mt_gateup, kb_gateup, w8, ar, p, st),
            "gate/up GEMM (tcgen05)");
   }
   rec(ev_first + 2);
@@ -481,7 +490,10 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.max_tiles = (row_tiles(mt_down, kept_max) + s->E + (shared ? row_tiles(mt_down, s->T) : 0)) *
                   ((s->d + bn - 1) / bn);
     p.num_sms = sms;
-    LAUNCH(launch_tc_gemm(TC_SCALE, bn, mt_down, kb_down, w8, ar, p, st), "down GEMM (tcgen05)");
+    if (mt_down == 2 && pair_tiles)
+      LAUNCH(launch_tc_pair_gemm(TC_SCALE, p, st), "down GEMM (tcgen05, CTA pairs)");
+    else
+      LAUNCH(launch_tc_gemm(TC_SCALE, bn, mt_down, kb_down, w8, ar, p, st), "down GEMM (tcgen05)");
   }
   return MOE_OK;
 }

@@ -26,6 +26,14 @@ constexpr int kRouteWarps = 8;
 constexpr int kRouteThreads = kRouteWarps * 32;
 constexpr int kNoIdx = 0x7fffffff;
 
+// Order-preserving 32-bit image of a selection key: a > b as floats iff key(a) > key(b) as
+// unsigned integers, -0.0 and +0.0 map to the same value, and every finite value maps above
+// 0 (0 marks "not a candidate").
+__device__ __forceinline__ uint32_t order_key(float f) {
+  const uint32_t u = (f == 0.0f) ? 0u : __float_as_uint(f);
+  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+}
+
 // JM = values per lane: lane l holds the logits of experts l, l+32, ..., l+32*(JM-1).
 template <int JM>
 __global__ void __launch_bounds__(kRouteThreads)
@@ -47,8 +55,17 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
   float lse2 = 0.f;
 
   const int nwarps = gridDim.x * kRouteWarps;
+  // the rows of a warp's next token are pulled into L2 while it works on this one
+  const int lines = (E * 4 + 127) / 128;
   for (int t = blockIdx.x * kRouteWarps + warp; t < T; t += nwarps) {
     const float* row = logits + static_cast<size_t>(t) * E;
+    if (t + nwarps < T) {
+      for (int i = lane; i < lines * nsplit; i += 32) {
+        const int sp = i / lines;
+        const float* p = row + static_cast<size_t>(nwarps) * E + sp * split_stride + (i - sp * lines) * 32;
+        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+      }
+    }
     float v[JM], ex[JM];
     int slot[JM];
     bool bad = false;
@@ -110,32 +127,31 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
       }
     }
 
-    // k rounds of a warp arg-max over the not-yet-selected experts
+    // k rounds of a warp arg-max over the not-yet-selected experts: each lane's best
+    // candidate (a strict '>' over ascending j keeps its lowest index among equals), the
+    // warp's largest key, then the lowest expert index holding it
+    uint32_t kk[JM];
+#pragma unroll
+    for (int j = 0; j < JM; ++j) kk[j] = (lane + 32 * j < E) ? order_key(key[j]) : 0u;
     for (int r = 0; r < k; ++r) {
-      float bv = -INFINITY;
-      int bi = kNoIdx;
+      uint32_t best = 0u;
+      int bj = 0;
 #pragma unroll
-      for (int j = 0; j < JM; ++j) {
-        const int e = lane + 32 * j;
-        // j ascending means e ascending: a strict '>' keeps the lowest index among equals
-        if (e < E && slot[j] < 0 && (bi == kNoIdx || key[j] > bv)) {
-          bv = key[j];
-          bi = e;
+      for (int j = 0; j < JM; ++j)
+        if (kk[j] > best) {
+          best = kk[j];
+          bj = j;
         }
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
-        const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
-        const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
-        if (oi != kNoIdx && (bi == kNoIdx || ov > bv || (ov == bv && oi < bi))) {
-          bv = ov;
-          bi = oi;
-        }
-      }
+      const uint32_t m = __reduce_max_sync(0xffffffffu, best);
+      const int bi = __reduce_min_sync(0xffffffffu, (best == m && best != 0u) ? lane + 32 * bj
+                                                                               : kNoIdx);
       if ((bi & 31) == lane) {
 #pragma unroll
         for (int j = 0; j < JM; ++j)
-          if (j == (bi >> 5)) slot[j] = r;
+          if (j == (bi >> 5)) {
+            slot[j] = r;
+            kk[j] = 0u;
+          }
       }
     }
 
@@ -165,7 +181,8 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
     }
   }
 
-  // per-block partial sums of p_{t,i} and lse^2, reduced over warps in a fixed order
+  // per-block partial sums of p_{t,i} and lse^2, reduced over warps in a fixed order and
+  // stored expert-major, partials[e][block], so that the reduction below reads rows
 #pragma unroll
   for (int j = 0; j < JM; ++j) {
     const int e = lane + 32 * j;
@@ -176,11 +193,11 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     float acc = 0.f;
     for (int w = 0; w < kRouteWarps; ++w) acc += s_part[w * (E + 1) + e];
-    partials[static_cast<size_t>(blockIdx.x) * (E + 1) + e] = acc;
+    partials[static_cast<size_t>(e) * gridDim.x + blockIdx.x] = acc;
   }
 }
 
-// stats[e] = sum over the blocks of partials[b][e]: one CTA per column e, each thread sums
+// stats[e] = sum over the blocks b of partials[e][b]: one CTA per expert e, each thread sums
 // a fixed stride of blocks in double, then a fixed-shape tree in shared memory
 // (deterministic: the order depends only on the block count).
 __global__ void __launch_bounds__(256)
@@ -188,7 +205,7 @@ stats_reduce_kernel(const float* __restrict__ partials, int nb, int E, float* __
   __shared__ double s_red[256];
   const int e = blockIdx.x;
   double acc = 0.0;
-  for (int b = threadIdx.x; b < nb; b += 256) acc += partials[static_cast<size_t>(b) * (E + 1) + e];
+  for (int b = threadIdx.x; b < nb; b += 256) acc += partials[static_cast<size_t>(e) * nb + b];
   s_red[threadIdx.x] = acc;
   __syncthreads();
   for (int w = 128; w > 0; w >>= 1) {
@@ -211,7 +228,7 @@ stats_loss_kernel(const float* __restrict__ partials, int nb, int E, float* __re
   pdl_wait();
   pdl_launch_dependents();
   double acc = 0.0;
-  for (int b = threadIdx.x; b < nb; b += 256) acc += partials[static_cast<size_t>(b) * (E + 1) + e];
+  for (int b = threadIdx.x; b < nb; b += 256) acc += partials[static_cast<size_t>(e) * nb + b];
   s_red[threadIdx.x] = acc;
   __syncthreads();
   for (int w = 128; w > 0; w >>= 1) {

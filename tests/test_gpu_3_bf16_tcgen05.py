@@ -107,6 +107,13 @@ def test_grouped_swiglu_tcgen05_256_row_tiles():
     grouped_check(int(idx.shape[0]), 256, 3, 1, 8192, idx=idx, seed=5)
 
 
+def test_grouped_swiglu_tcgen05_256_row_tiles_shared_ragged():
+    """256-row tiles in both expert GEMMs (768 rows per expert, d_ff >= 8192) together with
+    the shared expert's tiles (1536 rows, d_ff_shared = 200), on a ragged K of gate/up
+    (d = 328 = 5 * 64 + 8) and a ragged N of the down projection (328 = 256 + 72)."""
+    grouped_check(1536, 328, 2, 1, 8192, Fs=200, seed=6)
+
+
 def test_grouped_swiglu_tcgen05_capacity_and_shared():
     grouped_check(500, 256, 8, 2, 256, Fs=128, cf=0.75, gate="sigmoid_topk", seed=3)
 

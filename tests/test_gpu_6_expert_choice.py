@@ -114,3 +114,13 @@ def test_expert_choice_layer_bf16(T, d, E, F, C):
     w = WORKLOADS["mixtral_prefill"].scaled(T=T, d=d, E=E, k=2, d_ff=F)
     y, yref = layer(w, C=C, dtype=torch.bfloat16, seed=4)
     assert rel_l2(y, yref) < 2e-2
+
+
+def test_expert_choice_layer_bf16_pair_tiles_shared():
+    """Expert-choice layers whose experts hold whole 256-row tiles run both expert GEMMs on CTA
+    pairs (tcgen05 cta_group::2): here every expert takes C = 768 rows (three pair tiles),
+    d_ff >= 8192, with the shared expert's 1500 rows (a last tile of 220) on the same pairs and
+    a ragged K / N (d = 328 = 5 * 64 + 8)."""
+    w = WORKLOADS["mixtral_prefill"].scaled(T=1500, d=328, E=4, k=2, d_ff=8192, d_ff_shared=200)
+    y, yref = layer(w, C=768, dtype=torch.bfloat16, seed=8)
+    assert rel_l2(y, yref) < 2e-2
