@@ -197,22 +197,31 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
   }
 }
 
+// Sum over the 256 threads of a block in double, in a fixed order (each warp a butterfly of
+// shuffles, then the 8 warp sums in warp order); the result is valid in thread 0.
+__device__ __forceinline__ double block_sum_256(double v, double* s_w) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = v;
+  __syncthreads();
+  double t = 0.0;
+  if (threadIdx.x == 0)
+    for (int w = 0; w < 8; ++w) t += s_w[w];
+  __syncthreads();
+  return t;
+}
+
 // stats[e] = sum over the blocks b of partials[e][b]: one CTA per expert e, each thread sums
-// a fixed stride of blocks in double, then a fixed-shape tree in shared memory
-// (deterministic: the order depends only on the block count).
+// a fixed stride of blocks in double, then block_sum_256 (deterministic: the order depends
+// only on the block count).
 __global__ void __launch_bounds__(256)
 stats_reduce_kernel(const float* __restrict__ partials, int nb, int E, float* __restrict__ stats) {
-  __shared__ double s_red[256];
+  __shared__ double s_w[8];
   const int e = blockIdx.x;
   double acc = 0.0;
   for (int b = threadIdx.x; b < nb; b += 256) acc += partials[static_cast<size_t>(e) * nb + b];
-  s_red[threadIdx.x] = acc;
-  __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
-    __syncthreads();
-  }
-  if (threadIdx.x == 0) stats[e] = static_cast<float>(s_red[0]);
+  acc = block_sum_256(acc, s_w);
+  if (threadIdx.x == 0) stats[e] = static_cast<float>(acc);
 }
 
 // stats as stats_reduce_kernel, and the block that finishes last (a counter in the workspace
@@ -222,21 +231,16 @@ __global__ void __launch_bounds__(256)
 stats_loss_kernel(const float* __restrict__ partials, int nb, int E, float* __restrict__ stats,
                   const int32_t* __restrict__ counts, int T, int k, float alpha, float beta,
                   float* __restrict__ losses, DeviceError* hdr) {
-  __shared__ double s_red[256];
+  __shared__ double s_w[8];
   __shared__ bool s_last;
   const int e = blockIdx.x;
   pdl_wait();
   pdl_launch_dependents();
   double acc = 0.0;
   for (int b = threadIdx.x; b < nb; b += 256) acc += partials[static_cast<size_t>(e) * nb + b];
-  s_red[threadIdx.x] = acc;
-  __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
-    __syncthreads();
-  }
+  acc = block_sum_256(acc, s_w);
   if (threadIdx.x == 0) {
-    stats[e] = static_cast<float>(s_red[0]);
+    stats[e] = static_cast<float>(acc);
     __threadfence();
     s_last = atomicAdd(&hdr->done_count, 1u) == static_cast<unsigned>(E);
   }
@@ -246,15 +250,10 @@ stats_loss_kernel(const float* __restrict__ partials, int nb, int E, float* __re
   acc = 0.0;
   for (int i = threadIdx.x; i < E; i += blockDim.x)
     acc += static_cast<double>(counts[i]) * static_cast<double>(__ldcg(stats + i));
-  s_red[threadIdx.x] = acc;
-  __syncthreads();
-  for (int w = 128; w > 0; w >>= 1) {
-    if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
-    __syncthreads();
-  }
+  acc = block_sum_256(acc, s_w);
   if (threadIdx.x == 0) {
     const double Td = static_cast<double>(T);
-    losses[0] = static_cast<float>(static_cast<double>(alpha) * E * s_red[0] /
+    losses[0] = static_cast<float>(static_cast<double>(alpha) * E * acc /
                                    (Td * static_cast<double>(k) * Td));
     losses[1] = static_cast<float>(static_cast<double>(beta) * __ldcg(stats + E) / Td);
     hdr->done_count = 0u;
@@ -262,26 +261,22 @@ stats_loss_kernel(const float* __restrict__ partials, int nb, int E, float* __re
 }
 
 // losses[0] = alpha*E*sum_i (counts_i/(T*k)) * (stats_i/T); losses[1] = beta*stats[E]/T.
-__global__ void aux_loss_kernel(const float* __restrict__ stats, const int32_t* __restrict__ counts,
-                                int T, int E, int k, float alpha, float beta,
-                                float* __restrict__ losses) {
-  __shared__ double s_red[256];
+// One block of 256 threads; the sum in stats_loss_kernel's order.
+__global__ void __launch_bounds__(256)
+aux_loss_kernel(const float* __restrict__ stats, const int32_t* __restrict__ counts, int T, int E,
+                int k, float alpha, float beta, float* __restrict__ losses) {
+  __shared__ double s_w[8];
   double acc = 0.0;
   for (int i = threadIdx.x; i < E; i += blockDim.x)
     acc += static_cast<double>(counts[i]) * static_cast<double>(stats[i]);
-  s_red[threadIdx.x] = acc;
-  __syncthreads();
-  for (int w = blockDim.x / 2; w > 0; w >>= 1) {
-    if (threadIdx.x < w) s_red[threadIdx.x] += s_red[threadIdx.x + w];
-    __syncthreads();
-  }
+  acc = block_sum_256(acc, s_w);
   if (threadIdx.x == 0) {
     if (T == 0) {
       losses[0] = 0.f;
       losses[1] = 0.f;
     } else {
       const double Td = static_cast<double>(T);
-      losses[0] = static_cast<float>(static_cast<double>(alpha) * E * s_red[0] /
+      losses[0] = static_cast<float>(static_cast<double>(alpha) * E * acc /
                                      (Td * static_cast<double>(k) * Td));
       losses[1] = static_cast<float>(static_cast<double>(beta) * stats[E] / Td);
     }
