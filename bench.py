@@ -99,18 +99,19 @@ def algorithmic_work(w, R: int, touched: int, wb=None):
 
 
 def power_capped(clk):
-    """Did the timed region run under the power cap (the clock record's own evidence)?"""
+    """Did the timed region run with its clocks pulled down (the clock record's own evidence:
+    median SM clock under load below 90 % of maximum)? A momentary sw_power_cap flag with the
+    median at the maximum does not count."""
     if not clk or not clk.get("sm_mhz"):
         return False
-    return ("sw_power_cap" in (clk.get("reasons") or [])
-            or clk["sm_mhz"] < 0.9 * (clk.get("sm_max_mhz") or clk["sm_mhz"]))
+    return clk["sm_mhz"] < 0.9 * (clk.get("sm_max_mhz") or clk["sm_mhz"])
 
 
 def tensor_peak(pk, clk):
     """bf16 denominator: the sustained figure (the dense GEMM run back to back for seconds,
     under the power cap) when the timed region itself ran power-capped, else the burst one."""
     if power_capped(clk) and pk.get("bf16_tflops_sustained"):
-        return pk["bf16_tflops_sustained"], "bf16 sustained (the timed region ran power-capped)"
+        return pk["bf16_tflops_sustained"], "bf16 sustained (clocks pulled down by the power cap)"
     return pk["bf16_tflops"], "bf16 burst (clocks at maximum during the timed region)"
 
 
