@@ -1,0 +1,72 @@
+"""Host logic of bench.py (no GPU): the roofline denominators chosen from the clock record,
+the per-kernel roofline classification, and the algorithmic work of the headline workload
+against its closed forms."""
+import math
+
+import pytest
+
+import bench
+from moe_inputs import WORKLOADS
+
+PK = dict(hbm_gbs=6000.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="test")
+
+
+@pytest.mark.parametrize("clk,capped", [
+    (dict(sm_mhz=1300.0, sm_max_mhz=2032.0, reasons=["sw_power_cap"]), True),
+    (dict(sm_mhz=1800.0, sm_max_mhz=2032.0, reasons=[]), True),          # below 90 % of max
+    (dict(sm_mhz=2032.0, sm_max_mhz=2032.0, reasons=["sw_power_cap"]), False),  # a momentary flag
+    (dict(sm_mhz=1900.0, sm_max_mhz=2032.0, reasons=[]), False),
+    (dict(sm_mhz=None, sm_max_mhz=None, reasons=[]), False),
+    (None, False),
+])
+def test_power_capped(clk, capped):
+    assert bench.power_capped(clk) is capped
+
+
+def test_tensor_peak_follows_the_clock_record():
+    peak, name = bench.tensor_peak(PK, dict(sm_mhz=1200.0, sm_max_mhz=2032.0, reasons=[]))
+    assert peak == 1400.0 and "sustained" in name
+    peak, name = bench.tensor_peak(PK, dict(sm_mhz=2032.0, sm_max_mhz=2032.0, reasons=[]))
+    assert peak == 1800.0 and "burst" in name
+    no_sustained = dict(PK, bf16_tflops_sustained=None)
+    assert bench.tensor_peak(no_sustained, dict(sm_mhz=1200.0, sm_max_mhz=2032.0))[0] == 1800.0
+
+
+def test_stage_roofline_binds_the_slower_roof():
+    capped = dict(sm_mhz=1200.0, sm_max_mhz=2032.0, reasons=[])
+    # 1.4e12 FLOP and 6e9 bytes: 1.0 ms at the sustained tensor peak, 1.0 ms at HBM -> tensor
+    r = bench.stage_roofline(1.4e12, 6e9, 2.0, PK, capped)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
+    assert r["achieved"] == pytest.approx(700.0)
+    assert r["frac"] == pytest.approx(0.5) and r["frac_burst"] == pytest.approx(700.0 / 1800.0)
+    # bandwidth work only
+    r = bench.stage_roofline(0.0, 6e9, 2.0, PK, capped)
+    assert r["bound"] == "hbm" and r["achieved"] == pytest.approx(3000.0)
+    assert r["frac"] == pytest.approx(0.5)
+
+
+def test_algorithmic_work_of_the_prefill_layer():
+    """Mixtral prefill, no drop: R = T k kept rows, every expert touched."""
+    w = WORKLOADS["mixtral_prefill"]
+    T, d, E, F, k = w.T, w.d, w.E, w.d_ff, w.k
+    R = T * k
+    work = bench.algorithmic_work(w, R, E)
+    assert work["flops"] == pytest.approx(2 * T * d * E + 6 * d * F * R)
+    # x, W_r, all experts' three matrices and y, in bf16
+    assert work["bytes"] == pytest.approx((T * d + E * d + 3 * E * d * F + T * d) * 2)
+    st = work["per_stage"]
+    assert st["gemm_gateup_swiglu"][0] == pytest.approx(4 * R * d * F)
+    assert st["gemm_down_scale"][0] == pytest.approx(2 * R * d * F)
+    assert math.isclose(sum(v[0] for v in st.values()), work["flops"])
+    # the gather copies R rows in and out
+    assert st["gather"][1] == pytest.approx(2 * R * d * 2)
+
+
+def test_algorithmic_work_of_8bit_weights_counts_codes_and_scales():
+    w = WORKLOADS["mixtral_decode"]
+    R, E = w.T * w.k, w.E
+    b16 = bench.algorithmic_work(w, R, E)["bytes"]
+    b8 = bench.algorithmic_work(w, R, E, wb=1)["bytes"]
+    weights16 = 3 * E * w.d * w.d_ff * 2
+    weights8 = 3 * E * w.d * w.d_ff + E * (2 * w.d_ff + w.d) * 4
+    assert b16 - b8 == pytest.approx(weights16 - weights8)
