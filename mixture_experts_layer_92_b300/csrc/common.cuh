@@ -67,21 +67,16 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&v);
 }
 
-// Codes 2P and 2P+1 of four E4M3 codes (low byte first) -> two fp16 numbers equal to the
-// codes' values divided by 256, exactly: an E4M3 code s.eeee.mmm read as fp16 bits
-// s.0eeee.mmm0000000 has the same significand and an exponent 8 lower (bias 15 against 7),
-// and E4M3 subnormals land on fp16 subnormals the same way; the factor 256 goes into the
-// weight scale. With each code c in the low byte of its 16-bit half, the fp16 bits are
-// c*128 with the sign moved from bit 14 to bit 15, i.e. V + (V & 0x4000) for V = c*128 (the
-// add carries bit 14 into bit 15). Two integer-pipe operations (a byte permute and an AND)
-// and two that the compiler can issue on the FMA pipe (the multiply and the add): the
-// conversion runs on the integer pipe, which is the bottleneck of the 8-bit path. The two
-// E4M3 NaN codes read as +-480 (this path expects finite codes).
+// Codes 2P and 2P+1 of four E4M3 codes (low byte first) -> their two values as fp16 (code
+// 2P in the low half), with the hardware conversion (one instruction per pair; every finite
+// E4M3 value, subnormals included, is exact in fp16). The two E4M3 NaN codes give NaN (this
+// path expects finite codes).
 template <int P>
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2_div256(uint32_t four_codes) {
-  const uint32_t c = __byte_perm(four_codes, 0u, P == 0 ? 0x4140u : 0x4342u);
-  const uint32_t v = c * 128u;
-  return v + (v & 0x40004000u);
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t four_codes) {
+  const uint16_t two = static_cast<uint16_t>(P == 0 ? (four_codes & 0xffffu) : (four_codes >> 16));
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(two));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {

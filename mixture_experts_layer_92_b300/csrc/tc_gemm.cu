@@ -41,12 +41,11 @@
 //   (W8) 8 warps   converters: E4M3 weight tile in the TMA ring -> fp16 tile in a separate
 //                  2-slot ring that the MMA reads, so the TMA ring holds only A and the
 //                  8-bit staging and keeps more weight bytes in flight. The conversion is
-//                  the 8-bit path's bottleneck (integer-pipe issue), so it is a bit
-//                  placement of four operations per weight pair that yields value / 256 in
-//                  fp16 (the 256 is folded into the scale); bf16 operands would need a
-//                  real conversion. So the 8-bit path runs its MMAs on fp16 operands: the
-//                  gather converts the activations to fp16 and the SwiGLU epilogue writes H
-//                  as fp16.
+//                  the 8-bit path's bottleneck, so it targets fp16 (one hardware
+//                  conversion per weight pair, exact); bf16 operands would need a longer
+//                  one. So the 8-bit path runs its MMAs on fp16 operands: the gather
+//                  converts the activations to fp16 and the SwiGLU epilogue writes H as
+//                  fp16.
 // Every mbarrier wait is bounded (common.cuh): on a timeout the kernel records
 // MOE_ERR_TIMEOUT in the workspace error word, drains its own copies and MMAs, frees TMEM
 // and returns.
@@ -432,8 +431,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             uint32_t o[8];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-              o[2 * i] = e4m3x2_to_f16x2_div256<0>(w[i]);
-              o[2 * i + 1] = e4m3x2_to_f16x2_div256<1>(w[i]);
+              o[2 * i] = e4m3x2_to_f16x2<0>(w[i]);
+              o[2 * i + 1] = e4m3x2_to_f16x2<1>(w[i]);
             }
             uint8_t* row = sb + r * 128;
             *reinterpret_cast<uint4*>(row + ((c ^ (r & 7)) << 4)) =
@@ -521,15 +520,14 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             if (rvalid && out != nullptr) {
               const int col0 = col_base + c * CW;
               if (W8) {
-                // per-row weight scales of W1 and W3 (times the 256 the converters divided
-                // out), applied before the SiLU
+                // per-row weight scales of W1 and W3, applied before the SiLU
                 const float* s1 = args.scale0 + static_cast<size_t>(t.group) * N + col0;
                 const float* s3 = args.scale1 + static_cast<size_t>(t.group) * N + col0;
 #pragma unroll
                 for (int i = 0; i < CW; ++i) {
                   const bool in = col0 + i < N;
-                  g[i] = __float_as_uint(__uint_as_float(g[i]) * (in ? 256.f * __ldg(s1 + i) : 0.f));
-                  u[i] = __float_as_uint(__uint_as_float(u[i]) * (in ? 256.f * __ldg(s3 + i) : 0.f));
+                  g[i] = __float_as_uint(__uint_as_float(g[i]) * (in ? __ldg(s1 + i) : 0.f));
+                  u[i] = __float_as_uint(__uint_as_float(u[i]) * (in ? __ldg(s3 + i) : 0.f));
                 }
               }
               uint32_t packed[CW / 2];
@@ -573,13 +571,12 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             if (rvalid) {
               const int col0 = col_base + c * 32;
               if (W8) {
-                // per-row scale of W2 (one per output column of the down projection), times
-                // the 256 the converters divided out
+                // per-row scale of W2 (one per output column of the down projection)
                 const float* s2 = args.scale0 + static_cast<size_t>(t.group) * N + col0;
 #pragma unroll
                 for (int i = 0; i < 32; ++i)
                   v[i] = __float_as_uint(__uint_as_float(v[i]) *
-                                         (col0 + i < N ? 256.f * __ldg(s2 + i) : 0.f));
+                                         (col0 + i < N ? __ldg(s2 + i) : 0.f));
               }
               uint32_t packed[16];
 #pragma unroll
