@@ -98,6 +98,21 @@ def algorithmic_work(w, R: int, touched: int, wb=None):
                     aux_loss=(0.0, 0.0)))
 
 
+def slowest_rank_ms(times_ms, dist=None, device="cpu"):
+    """The timing of the slowest rank: every rank passes its own [total_ms, e2e_ms, ...], all
+    ranks get the element-wise maximum (a no-op with one process)."""
+    t = torch.tensor([float(v) for v in times_ms], dtype=torch.float64, device=device)
+    if dist is not None:
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def whole_job_rate(tokens_per_step, steps, world, total_ms):
+    """Replicas: every rank processes its own batch of tokens_per_step per step, so the job
+    processes world times as many tokens in the slowest rank's time."""
+    return tokens_per_step * steps * world / (total_ms / 1e3)
+
+
 def power_capped(clk):
     """Did the timed region run with its clocks pulled down (the clock record's own evidence:
     median SM clock under load below 90 % of maximum)? A momentary sw_power_cap flag with the
@@ -388,10 +403,7 @@ def run_ours(args, w, rank, world, local_rank):
     e2e_ms = e0.elapsed_time(e1)
 
     # the slowest rank sets the time
-    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = t.tolist()
+    total_ms, e2e_ms = slowest_rank_ms([total_ms, e2e_ms], dist, dev)
     counts = layer.counts.cpu().numpy()
     spread.append(float(counts.max()) / (w.T * w.k / w.E))
     R = int(np.minimum(counts, C).sum())
@@ -404,7 +416,7 @@ def run_ours(args, w, rank, world, local_rank):
     pk = peaks()
     work = algorithmic_work(w, R, touched, wb=1 if args.fp8_weights else None)
     tokens = w.T * args.steps * world
-    value = tokens / (total_ms / 1e3)
+    value = whole_job_rate(w.T, args.steps, world, total_ms)
     ms_per_step = total_ms / args.steps
     clk = sampler.summary()
     tpeak, tpeak_name = tensor_peak(pk, clk)
@@ -443,7 +455,8 @@ def run_ours(args, w, rank, world, local_rank):
                     wall_s=t_wall),
         roofline=roofline, layer_roofline=layer_roof, stages=stages,
         cpu_baseline=cpu,
-        e2e=dict(value=tokens / (e2e_ms / 1e3), unit=UNIT, h2d_bytes_per_step=w.T * w.d * es,
+        e2e=dict(value=whole_job_rate(w.T, args.steps, world, e2e_ms), unit=UNIT,
+                 h2d_bytes_per_step=w.T * w.d * es,
                  d2h_bytes_per_step=w.T * w.d * es,
                  note="MoELayer.forward_host_stream: per step, x (pinned) -> device, layer, y -> "
                       "host; uploads/downloads of neighbouring steps overlap the layer"),
@@ -603,10 +616,7 @@ def run_train(args, w, rank, world, local_rank):
     barrier()
     sampler.stop()
     e2e_ms = e0.elapsed_time(e1)
-    t = torch.tensor([total_ms, e2e_ms], dtype=torch.float64, device=dev)
-    if dist is not None:
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    total_ms, e2e_ms = t.tolist()
+    total_ms, e2e_ms = slowest_rank_ms([total_ms, e2e_ms], dist, dev)
     counts = layer.counts.cpu().numpy()
     R = int(np.minimum(counts, C).sum())
     touched = int((counts > 0).sum())
@@ -652,7 +662,8 @@ def run_train(args, w, rank, world, local_rank):
                           f"{tt:.2f} s")
     es = x.element_size()
     line = dict(
-        metric=TRAIN_METRIC, value=tokens / (total_ms / 1e3), unit=UNIT, n_gpus=world,
+        metric=TRAIN_METRIC, value=whole_job_rate(w.T, args.steps, world, total_ms), unit=UNIT,
+        n_gpus=world,
         steps=args.steps, warmup=args.warmup, ms_per_step=ms_per_step, higher_is_better=True,
         scaling="weak", vs_baseline=None, dtype=w.dtype,
         data="synthetic (seeded; random-init weights; dy ~ N(0,1))",
@@ -667,7 +678,8 @@ def run_train(args, w, rank, world, local_rank):
                             note=f"max(FLOPs / {tpeak_name.split(' (')[0]} peak, bytes / HBM "
                                  "peak), measured peaks"),
         stages=stages, cpu_baseline=cpu,
-        e2e=dict(value=tokens / (e2e_ms / 1e3), unit=UNIT, h2d_bytes_per_step=2 * w.T * w.d * es,
+        e2e=dict(value=whole_job_rate(w.T, args.steps, world, e2e_ms), unit=UNIT,
+                 h2d_bytes_per_step=2 * w.T * w.d * es,
                  d2h_bytes_per_step=2 * w.T * w.d * es,
                  note="per step: x and dy (pinned) -> device, forward, backward, y and dx -> host; "
                       "the weight gradients stay on the device"),
