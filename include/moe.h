@@ -352,6 +352,16 @@ int moe_get_error(const void* ws, void* stream);
 /* Clears the sticky device error word (asynchronous on `stream`). */
 int moe_clear_error(void* ws, void* stream);
 
+/* Diagnostic of the failure path above (no counterpart in the pages): one device thread waits
+ * on an mbarrier that nothing completes, with the bounded wait every pipeline kernel uses. The
+ * wait gives up after its limit (2 s of %globaltimer), records MOE_ERR_TIMEOUT in the
+ * workspace error word (moe_get_error then reports it, site 40 in moe_last_error_detail) and
+ * returns; the GPU is neither trapped nor hung and the workspace is usable again after
+ * moe_clear_error. `ws`: a workspace of at least 256 bytes (256-byte aligned), `ws_bytes` its
+ * size. Asynchronous on `stream`; MOE_ERR_WORKSPACE for a NULL, misaligned or short workspace
+ * (before any launch). */
+int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream);
+
 /* Static description of a status code. */
 const char* moe_status_string(int status);
 

@@ -30,7 +30,7 @@ EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_
             "moe_last_error_detail", "moe_route_topk_noalloc", "moe_route_topk_balanced",
             "moe_update_select_bias", "moe_forward_balanced", "moe_expert_choice",
             "moe_grouped_swiglu_fp8w", "moe_forward_fp8w", "moe_backward_workspace_size",
-            "moe_backward")
+            "moe_backward", "moe_selftest_wait_timeout")
 NUM_BWD_STAGES = 8
 BWD_STAGE_NAMES = ("route_dispatch", "gather_x_dy", "recompute_gu", "gemm_dh_swiglu_bwd",
                    "gate_logit_grads", "gemm_dx", "dx_combine", "gemm_wgrad")
@@ -72,6 +72,7 @@ def _load() -> ctypes.CDLL:
                                               vp, vp, sz, vp, ctypes.POINTER(vp), ctypes.c_int]),
         "moe_get_error": (ctypes.c_int, [vp, vp]),
         "moe_clear_error": (ctypes.c_int, [vp, vp]),
+        "moe_selftest_wait_timeout": (ctypes.c_int, [vp, sz, vp]),
         "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "moe_last_error_detail": (ctypes.c_char_p, []),
         "moe_route_topk_noalloc": (ctypes.c_int, [sp, vp, vp, vp, vp, vp]),
@@ -298,6 +299,13 @@ def moe_get_error(ws, stream=None) -> int:
 
 def moe_clear_error(ws, stream=None):
     _check(LIB.moe_clear_error(_p(ws), _stream(stream)), "moe_clear_error")
+
+
+def moe_selftest_wait_timeout(ws, stream=None):
+    """Runs the bounded-wait diagnostic on `ws` (see include/moe.h); read the result with
+    moe_get_error."""
+    _check(LIB.moe_selftest_wait_timeout(_p(ws), ws.numel(), _stream(stream)),
+           "moe_selftest_wait_timeout")
 
 
 def moe_status_string(status: int) -> str:

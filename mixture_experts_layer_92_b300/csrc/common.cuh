@@ -36,6 +36,7 @@ enum ErrSite : int {
   SITE_DISPATCH_GRID_BARRIER = 20,
   SITE_F16_RANGE_X = 30,   // 8-bit-weight path: an activation outside fp16's finite range
   SITE_F16_RANGE_H = 31,   //                    an H value outside fp16's finite range
+  SITE_SELFTEST_WAIT = 40, // moe_selftest_wait_timeout: a wait that nothing completes
 };
 
 __device__ __forceinline__ void record_error(DeviceError* e, int code, int where, int detail) {

@@ -29,6 +29,10 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
   return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
+// One thread waits on an mbarrier that nothing completes (selftest.cu): the bounded wait
+// records MOE_ERR_TIMEOUT at SITE_SELFTEST_WAIT in *err and returns.
+int launch_wait_timeout(DeviceError* err, cudaStream_t stream);
+
 // Sets the text moe_last_error_detail() returns on this thread; returns `status`.
 int set_error_detail(int status, const char* text);
 

@@ -1414,6 +1414,18 @@ int moe_get_error(const void* ws, void* stream) {
   return ok();
 }
 
+int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
+  if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
+  if ((reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+    return fail(MOE_ERR_WORKSPACE, "workspace is not %zu-byte aligned", kAlign);
+  if (ws_bytes < sizeof(DeviceError))
+    return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes,
+                sizeof(DeviceError));
+  LAUNCH(launch_wait_timeout(static_cast<DeviceError*>(ws), static_cast<cudaStream_t>(stream)),
+         "bounded-wait self-test");
+  return ok();
+}
+
 int moe_clear_error(void* ws, void* stream) {
   if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
   if (cudaMemsetAsync(ws, 0, sizeof(DeviceError), static_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -159,3 +159,11 @@ def test_backward_rejects_before_any_launch():
     assert call(shp=s2, nbytes=moe.moe_backward_workspace_size(s2)) == -1   # shared grads missing
     assert call(ev=(ctypes.c_void_p * 3)(), nev=3) == -1
     assert call(shp=shape(d=96)) == -2
+
+
+def test_selftest_rejects_bad_workspace_before_any_launch():
+    """The bounded-wait diagnostic validates its workspace on the host (no GPU needed)."""
+    L = _lib.LIB
+    assert L.moe_selftest_wait_timeout(None, 4096, None) == -4
+    assert L.moe_selftest_wait_timeout(ctypes.c_void_p(0x7f0000000008), 4096, None) == -4  # misaligned
+    assert L.moe_selftest_wait_timeout(ctypes.c_void_p(0x7f0000000000), 8, None) == -4      # too small
