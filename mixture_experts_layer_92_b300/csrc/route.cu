@@ -35,7 +35,8 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // JM = values per lane: lane l holds the logits of experts l, l+32, ..., l+32*(JM-1).
-template <int JM>
+// FULL: E == 32 * JM, every slot is an expert (no bounds predicates).
+template <int JM, bool FULL>
 __global__ void __launch_bounds__(kRouteThreads)
 route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_stride,
                   const float* __restrict__ bias, const float* __restrict__ select_bias,
@@ -73,7 +74,7 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
     for (int j = 0; j < JM; ++j) {
       const int e = lane + 32 * j;
       slot[j] = -1;
-      if (e < E) {
+      if (FULL || e < E) {
         // split-K partial sums of the router GEMM, added in split order, then the bias
         float acc = __ldg(row + e);
         for (int sp = 1; sp < nsplit; ++sp) acc += __ldg(row + sp * split_stride + e);
@@ -97,16 +98,17 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
     float s = 0.f;
 #pragma unroll
     for (int j = 0; j < JM; ++j) {
-      ex[j] = (lane + 32 * j < E) ? expf(v[j] - m) : 0.f;
+      ex[j] = (FULL || lane + 32 * j < E) ? expf(v[j] - m) : 0.f;
       s += ex[j];
     }
     s = warp_sum(s);
+    const float inv_s = 1.0f / s;
 #pragma unroll
     for (int j = 0; j < JM; ++j) {
-      const float pj = ex[j] / s;
+      const float pj = ex[j] * inv_s;
       pacc[j] += pj;
       // expert-choice routing reads the probabilities expert-major: probs_t[e][t]
-      if (probs_t != nullptr && lane + 32 * j < E)
+      if (probs_t != nullptr && (FULL || lane + 32 * j < E))
         probs_t[static_cast<size_t>(lane + 32 * j) * T + t] = pj;
     }
     const float lse = m + logf(s);
@@ -120,7 +122,7 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
     for (int j = 0; j < JM; ++j) {
       key[j] = v[j];
       const int e = lane + 32 * j;
-      if (select_bias != nullptr && e < E) {
+      if (select_bias != nullptr && (FULL || e < E)) {
         const float a = (gate_mode == MOE_GATE_SIGMOID_TOPK) ? 1.0f / (1.0f + expf(-v[j]))
                                                              : ex[j] / s;
         key[j] = a + __ldg(select_bias + e);
@@ -132,7 +134,7 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
     // warp's largest key, then the lowest expert index holding it
     uint32_t kk[JM];
 #pragma unroll
-    for (int j = 0; j < JM; ++j) kk[j] = (lane + 32 * j < E) ? order_key(key[j]) : 0u;
+    for (int j = 0; j < JM; ++j) kk[j] = (FULL || lane + 32 * j < E) ? order_key(key[j]) : 0u;
     for (int r = 0; r < k; ++r) {
       uint32_t best = 0u;
       int bj = 0;
@@ -170,13 +172,13 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
       }
     }
     if (gate_mode != MOE_GATE_SOFTMAX_ALL) sel_sum = warp_sum(sel_sum);
-    const float denom = (gate_mode == MOE_GATE_SOFTMAX_ALL) ? s : sel_sum;
+    const float inv_denom = (gate_mode == MOE_GATE_SOFTMAX_ALL) ? inv_s : 1.0f / sel_sum;
 #pragma unroll
     for (int j = 0; j < JM; ++j) {
       if (slot[j] >= 0) {
         const size_t o = static_cast<size_t>(t) * k + slot[j];
         topk_idx[o] = lane + 32 * j;
-        topk_gate[o] = aff[j] / denom;
+        topk_gate[o] = aff[j] * inv_denom;
       }
     }
   }
@@ -186,7 +188,7 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
 #pragma unroll
   for (int j = 0; j < JM; ++j) {
     const int e = lane + 32 * j;
-    if (e < E) s_part[warp * (E + 1) + e] = pacc[j];
+    if (FULL || e < E) s_part[warp * (E + 1) + e] = pacc[j];
   }
   if (lane == 0) s_part[warp * (E + 1) + E] = lse2;
   __syncthreads();
@@ -296,16 +298,22 @@ __global__ void update_select_bias_kernel(const int32_t* __restrict__ counts,
   }
 }
 
-template <int JM>
-int launch_jm(const RouteArgs& a, cudaStream_t stream) {
+template <int JM, bool FULL>
+int launch_full(const RouteArgs& a, cudaStream_t stream) {
   const int nb = route_blocks(a.T);
   const size_t smem = static_cast<size_t>(kRouteWarps) * (a.E + 1) * sizeof(float);
-  if (launch_pdl(route_topk_kernel<JM>, dim3(nb), dim3(kRouteThreads), smem, stream, a.logits,
-                 a.nsplit, a.split_stride, a.bias, a.select_bias, a.logits_out, a.probs_t, a.T,
-                 a.E, a.k, a.gate_mode, a.topk_idx, a.topk_gate, a.partials,
+  if (launch_pdl(route_topk_kernel<JM, FULL>, dim3(nb), dim3(kRouteThreads), smem, stream,
+                 a.logits, a.nsplit, a.split_stride, a.bias, a.select_bias, a.logits_out,
+                 a.probs_t, a.T, a.E, a.k, a.gate_mode, a.topk_idx, a.topk_gate, a.partials,
                  a.err) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
+}
+
+template <int JM>
+int launch_jm(const RouteArgs& a, cudaStream_t stream) {
+  if (a.E == 32 * JM) return launch_full<JM, true>(a, stream);
+  return launch_full<JM, false>(a, stream);
 }
 
 }  // namespace
