@@ -124,3 +124,12 @@ def test_expert_choice_layer_bf16_pair_tiles_shared():
     w = WORKLOADS["mixtral_prefill"].scaled(T=1500, d=328, E=4, k=2, d_ff=8192, d_ff_shared=200)
     y, yref = layer(w, C=768, dtype=torch.bfloat16, seed=8)
     assert rel_l2(y, yref) < 2e-2
+
+
+def test_expert_choice_layer_bf16_pair_tiles_partial_last_tile():
+    """C = 650 rows per expert: two whole pair tiles and a last one of 138 rows (more than
+    half full, so the layer still runs on CTA pairs; CTA 1 holds 10 valid rows of it), in both
+    expert GEMMs (d_ff >= 8192)."""
+    w = WORKLOADS["mixtral_prefill"].scaled(T=1400, d=256, E=4, k=2, d_ff=8192)
+    y, yref = layer(w, C=650, dtype=torch.bfloat16, seed=9)
+    assert rel_l2(y, yref) < 2e-2
