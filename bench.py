@@ -401,6 +401,9 @@ def run_ours(args, w, rank, world, local_rank):
     barrier()
     sampler.stop()
     e2e_ms = e0.elapsed_time(e1)
+    err = layer.device_error()
+    if err != 0:
+        raise RuntimeError(f"device error {moe.moe_status_string(err)} in the host-memory steps")
 
     # the slowest rank sets the time
     total_ms, e2e_ms = slowest_rank_ms([total_ms, e2e_ms], dist, dev)
@@ -458,8 +461,11 @@ def run_ours(args, w, rank, world, local_rank):
         e2e=dict(value=whole_job_rate(w.T, args.steps, world, e2e_ms), unit=UNIT,
                  h2d_bytes_per_step=w.T * w.d * es,
                  d2h_bytes_per_step=w.T * w.d * es,
-                 note="MoELayer.forward_host_stream: per step, x (pinned) -> device, layer, y -> "
-                      "host; uploads/downloads of neighbouring steps overlap the layer"),
+                 note="MoELayer.forward_host_stream: for plain bf16/fp32 layers one "
+                      "moe_host_pipeline_forward C-ABI call per step (x pinned host -> device on "
+                      "the pipeline's upload stream, the layer on the compute stream, y -> pinned "
+                      "host on its download stream; copies of neighbouring steps overlap the "
+                      "layer); 8-bit and balanced layers copy through torch around the call"),
         gpu_launches=(launches_per_forward(w) + (1 if args.balance_gamma is not None else 0))
         * args.steps,
         clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"], reasons=clk["reasons"],

@@ -175,6 +175,51 @@ int moe_forward(const moe_shape* s, const void* x, const void* w_router,
                 int32_t* counts, int32_t* dropped, float* losses, void* ws, size_t ws_bytes,
                 void* stream);
 
+/* moe_forward from and to host memory (the end-to-end call): on `stream`, copies x_host
+ * [T, d] into x_dev, runs moe_forward on x_dev into y_dev, copies y_dev into y_host [T, d]
+ * and, if losses_host is not NULL, the two balance losses into losses_host [2]. Returns after
+ * queuing; the host buffers must stay valid (and, for asynchronous copies, be page-locked)
+ * until the stream reaches the end of the call. x_dev / y_dev: device buffers of T*d
+ * elements; the other arguments as in moe_forward (counts and dropped stay in the
+ * workspace). Calls that overlap on the GPU need their own x_dev, y_dev and workspace.
+ * Host-side argument errors return before any copy or launch. For a stream of batches whose
+ * copies overlap the layer, see moe_host_pipeline below. */
+int moe_forward_host(const moe_shape* s, const void* x_host, const void* w_router,
+                     const float* router_bias, const void* w1, const void* w3, const void* w2,
+                     const void* w1s, const void* w3s, const void* w2s, void* y_host,
+                     float* losses_host, void* x_dev, void* y_dev, void* ws, size_t ws_bytes,
+                     void* stream);
+
+/* A pipeline for a stream of host batches through one layer: batch i's x is uploaded on the
+ * pipeline's own upload stream, the layer runs on the caller's stream, and y (and the two
+ * losses) come back on its own download stream, so the upload of batch i+1 and the download
+ * of batch i-1 overlap the layer on batch i and both copy directions stay busy. It owns two
+ * slots of device buffers (x and y [T_max, d], losses [2]), the two copy streams (non-blocking)
+ * and the events that order a slot's reuse: a slot's upload waits for the layer that last read
+ * it, and its layer waits for its upload and for the download that last read its outputs.
+ *
+ * moe_host_pipeline_create: `s_max` fixes d and dtype and the largest T; `*out` receives the
+ * handle (NULL on error). Allocates on the current CUDA device, which every later call on the
+ * handle must also have current.
+ * moe_host_pipeline_forward: one batch, arguments as in moe_forward_host (x_host [T, d] and
+ * y_host [T, d] page-locked, losses_host [2] or NULL), with s->d and s->dtype as at create
+ * and s->T <= T_max. The layer runs on `stream` with workspace `ws`; calls that share a
+ * workspace must pass the same stream. Counts and dropped stay in the workspace. Returns after
+ * queuing; the host buffers must stay valid until moe_host_pipeline_join's stream reaches the
+ * join. Host-side argument errors return before anything is queued.
+ * moe_host_pipeline_join: `stream` waits (on the device) for every download queued so far.
+ * moe_host_pipeline_destroy: waits for the pipeline's queued work, then frees it; NULL is a
+ * no-op. */
+typedef struct moe_host_pipeline moe_host_pipeline;
+int moe_host_pipeline_create(const moe_shape* s_max, moe_host_pipeline** out);
+int moe_host_pipeline_forward(moe_host_pipeline* p, const moe_shape* s, const void* x_host,
+                              const void* w_router, const float* router_bias, const void* w1,
+                              const void* w3, const void* w2, const void* w1s, const void* w3s,
+                              const void* w2s, void* y_host, float* losses_host, void* ws,
+                              size_t ws_bytes, void* stream);
+int moe_host_pipeline_join(moe_host_pipeline* p, void* stream);
+int moe_host_pipeline_destroy(moe_host_pipeline* p);
+
 /* moe_forward, recording events[i] (cudaEvent_t handles created by the caller) on the
  * stream before stage i and events[MOE_NUM_STAGES] after the last one, so that each
  * stage's device time can be read with cudaEventElapsedTime. Stages: 0 router GEMM,

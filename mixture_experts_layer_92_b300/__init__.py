@@ -18,7 +18,8 @@ from ._lib import (MoeError, alloc_workspace, make_shape, moe_aux_loss, moe_capa
                    moe_grouped_swiglu_fp8w, moe_route_topk,
                    moe_route_topk_balanced, moe_route_topk_noalloc, moe_status_string,
                    moe_update_select_bias, moe_workspace_size, NUM_STAGES, STAGE_NAMES,
-                   alloc_workspace_backward, moe_backward, moe_backward_workspace_size)
+                   alloc_workspace_backward, moe_backward, moe_backward_workspace_size,
+                   moe_forward_host, HostPipeline)
 
 
 class MoELayer:
@@ -41,6 +42,7 @@ class MoELayer:
         self.gate, self.capacity, self.alpha, self.beta = gate, capacity, alpha, beta
         self.dtype = w_router.dtype
         self.device = w_router.device
+        self.max_tokens = max_tokens
         self.ws = alloc_workspace(self.shape(max_tokens), device=self.device)
         self.counts = torch.zeros(E, dtype=torch.int32, device=self.device)
         self.dropped = torch.zeros(1, dtype=torch.int32, device=self.device)
@@ -83,21 +85,44 @@ class MoELayer:
                     dropped=self.dropped, losses=self.losses, stream=stream, events=events)
         return y
 
-    def forward_host_stream(self, x_hosts, y_hosts):
+    def forward_host_stream(self, x_hosts, y_hosts, losses_hosts=None):
         """End-to-end layer over a sequence of host batches (pinned memory), pipelined.
 
-        Batch i's x is copied to the device on one stream, the layer runs on the current
-        stream, and y is copied back on a third; two device buffer pairs let the upload of
-        batch i+1 and the download of batch i-1 overlap the layer on batch i. Every batch
-        still moves its own x in and its own y out. Returns after queuing all work."""
+        Plain bf16/fp32 layers go through the C ABI's host pipeline (moe_host_pipeline): each
+        batch's x is uploaded on the pipeline's upload stream, the layer runs on the current
+        stream and y (and, if losses_hosts is given, the batch's two losses) come back on its
+        download stream, so the upload of batch i+1 and the download of batch i-1 overlap the
+        layer on batch i. The current stream waits for every download. Returns after queuing
+        all work. (8-bit-weight and balanced layers copy through torch around their own
+        forward calls instead.)"""
+        if self.fp8 is not None or self.select_bias is not None:
+            return self._forward_host_stream_copies(x_hosts, y_hosts)
         comp = torch.cuda.current_stream(self.device)
-        if not hasattr(self, "_pipe"):
-            self._pipe = dict(h2d=torch.cuda.Stream(self.device), d2h=torch.cuda.Stream(self.device),
+        if getattr(self, "_host_pipe", None) is None:
+            self._host_pipe = HostPipeline(self.shape(self.max_tokens))
+        for i, (xh, yh) in enumerate(zip(x_hosts, y_hosts)):
+            self._host_pipe.forward(self.shape(xh.shape[0]), self.ws, xh, self.w["w_router"],
+                               self.w["w1"], self.w["w3"], self.w["w2"], yh,
+                               router_bias=self.w["router_bias"], w1s=self.w["w1s"],
+                               w3s=self.w["w3s"], w2s=self.w["w2s"],
+                               losses_host=None if losses_hosts is None else losses_hosts[i],
+                               stream=comp)
+        self._host_pipe.join(comp)
+        return y_hosts
+
+    def _forward_host_stream_copies(self, x_hosts, y_hosts):
+        """forward_host_stream for the layer variants without a host entry point: batch i's
+        x is copied to the device on one stream, the layer runs on the current stream, and y
+        is copied back on a third; two device buffer pairs let the upload of batch i+1 and the
+        download of batch i-1 overlap the layer on batch i."""
+        comp = torch.cuda.current_stream(self.device)
+        if getattr(self, "_copy_pipe", None) is None:
+            self._copy_pipe = dict(h2d=torch.cuda.Stream(self.device), d2h=torch.cuda.Stream(self.device),
                               xbuf=[None, None], ybuf=[None, None],
                               h2d_done=[torch.cuda.Event(), torch.cuda.Event()],
                               fwd_done=[torch.cuda.Event(), torch.cuda.Event()],
                               d2h_done=[torch.cuda.Event(), torch.cuda.Event()])
-        p = self._pipe
+        p = self._copy_pipe
         for i, (xh, yh) in enumerate(zip(x_hosts, y_hosts)):
             b = i % 2
             if p["xbuf"][b] is None or p["xbuf"][b].shape[0] < xh.shape[0]:
@@ -120,6 +145,11 @@ class MoELayer:
                 p["d2h_done"][b].record(p["d2h"])
         comp.wait_stream(p["d2h"])
         return y_hosts
+
+    def device_error(self) -> int:
+        """The device error status recorded in this layer's workspace (0 if none).
+        Synchronises with the device."""
+        return moe_get_error(self.ws)
 
     def forward_host(self, x_host: torch.Tensor, x_dev: torch.Tensor, y_dev: torch.Tensor,
                      y_host: torch.Tensor, losses_host: Optional[torch.Tensor] = None):

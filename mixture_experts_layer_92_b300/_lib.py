@@ -30,7 +30,9 @@ EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_
             "moe_last_error_detail", "moe_route_topk_noalloc", "moe_route_topk_balanced",
             "moe_update_select_bias", "moe_forward_balanced", "moe_expert_choice",
             "moe_grouped_swiglu_fp8w", "moe_forward_fp8w", "moe_backward_workspace_size",
-            "moe_backward", "moe_selftest_wait_timeout")
+            "moe_backward", "moe_selftest_wait_timeout", "moe_forward_host",
+            "moe_host_pipeline_create", "moe_host_pipeline_forward", "moe_host_pipeline_join",
+            "moe_host_pipeline_destroy")
 NUM_BWD_STAGES = 8
 BWD_STAGE_NAMES = ("route_dispatch", "gather_x_dy", "recompute_gu", "gemm_dh_swiglu_bwd",
                    "gate_logit_grads", "gemm_dx", "dx_combine", "gemm_wgrad")
@@ -73,6 +75,13 @@ def _load() -> ctypes.CDLL:
         "moe_get_error": (ctypes.c_int, [vp, vp]),
         "moe_clear_error": (ctypes.c_int, [vp, vp]),
         "moe_selftest_wait_timeout": (ctypes.c_int, [vp, sz, vp]),
+        "moe_forward_host": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                            vp, sz, vp]),
+        "moe_host_pipeline_create": (ctypes.c_int, [sp, ctypes.POINTER(vp)]),
+        "moe_host_pipeline_forward": (ctypes.c_int, [vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                                     vp, vp, vp, sz, vp]),
+        "moe_host_pipeline_join": (ctypes.c_int, [vp, vp]),
+        "moe_host_pipeline_destroy": (ctypes.c_int, [vp]),
         "moe_status_string": (ctypes.c_char_p, [ctypes.c_int]),
         "moe_last_error_detail": (ctypes.c_char_p, []),
         "moe_route_topk_noalloc": (ctypes.c_int, [sp, vp, vp, vp, vp, vp]),
@@ -299,6 +308,50 @@ def moe_get_error(ws, stream=None) -> int:
 
 def moe_clear_error(ws, stream=None):
     _check(LIB.moe_clear_error(_p(ws), _stream(stream)), "moe_clear_error")
+
+
+def moe_forward_host(s, ws, x_host, w_router, w1, w3, w2, y_host, x_dev, y_dev, router_bias=None,
+                     w1s=None, w3s=None, w2s=None, losses_host=None, stream=None):
+    """The layer from and to host memory (pinned host tensors x_host, y_host; device scratch
+    x_dev, y_dev of the same shape); see include/moe.h."""
+    _check(LIB.moe_forward_host(ctypes.byref(s), _p(x_host), _p(w_router), _p(router_bias),
+                                _p(w1), _p(w3), _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(y_host),
+                                _p(losses_host), _p(x_dev), _p(y_dev), _p(ws), ws.numel(),
+                                _stream(stream)), "moe_forward_host")
+
+
+class HostPipeline:
+    """Handle of a moe_host_pipeline (see include/moe.h): a stream of pinned host batches
+    through one layer, uploads and downloads on the pipeline's own streams overlapping the
+    layers on the caller's stream. `s_max` fixes d, dtype and the largest T."""
+
+    def __init__(self, s_max):
+        h = ctypes.c_void_p()
+        _check(LIB.moe_host_pipeline_create(ctypes.byref(s_max), ctypes.byref(h)),
+               "moe_host_pipeline_create")
+        self._h = h
+
+    def forward(self, s, ws, x_host, w_router, w1, w3, w2, y_host, router_bias=None, w1s=None,
+                w3s=None, w2s=None, losses_host=None, stream=None):
+        _check(LIB.moe_host_pipeline_forward(self._h, ctypes.byref(s), _p(x_host), _p(w_router),
+                                             _p(router_bias), _p(w1), _p(w3), _p(w2), _p(w1s),
+                                             _p(w3s), _p(w2s), _p(y_host), _p(losses_host),
+                                             _p(ws), ws.numel(), _stream(stream)),
+               "moe_host_pipeline_forward")
+
+    def join(self, stream=None):
+        _check(LIB.moe_host_pipeline_join(self._h, _stream(stream)), "moe_host_pipeline_join")
+
+    def close(self):
+        if self._h is not None and self._h.value is not None:
+            h, self._h = self._h, None
+            _check(LIB.moe_host_pipeline_destroy(h), "moe_host_pipeline_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
 
 
 def moe_selftest_wait_timeout(ws, stream=None):

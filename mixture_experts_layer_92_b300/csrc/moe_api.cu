@@ -498,12 +498,12 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
   return MOE_OK;
 }
 
-int forward_impl(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
-                 const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
-                 const void* w2s, void* y, int32_t* counts, int32_t* dropped, float* losses,
-                 void* ws, size_t ws_bytes, void* stream, void* const* ev, int n_ev,
-                 float* select_bias = nullptr, float gamma = 0.f,
-                 const Fp8Weights* q = nullptr) {
+// Every argument check of the layer's forward, made on the host before anything is queued.
+int check_forward(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
+                  const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
+                  const void* w2s, const void* y, const int32_t* counts, const int32_t* dropped,
+                  const float* losses, const void* ws, size_t ws_bytes, void* const* ev, int n_ev,
+                  const Fp8Weights* q) {
   TRY(check_shape(s));
   TRY(check_ws(s, ws, ws_bytes));
   if (q != nullptr) TRY(check_fp8(s, q));
@@ -531,6 +531,17 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   OPT_PTR4(counts, "counts");
   OPT_PTR4(dropped, "dropped");
   OPT_PTR4(losses, "losses");
+  return MOE_OK;
+}
+
+int forward_impl(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
+                 const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
+                 const void* w2s, void* y, int32_t* counts, int32_t* dropped, float* losses,
+                 void* ws, size_t ws_bytes, void* stream, void* const* ev, int n_ev,
+                 float* select_bias = nullptr, float gamma = 0.f,
+                 const Fp8Weights* q = nullptr) {
+  TRY(check_forward(s, x, w_router, router_bias, w1, w3, w2, w1s, w3s, w2s, y, counts, dropped,
+                    losses, ws, ws_bytes, ev, n_ev, q));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Layout L = layout(s);
   DeviceError* err = at<DeviceError>(ws, L.err);
@@ -1387,6 +1398,165 @@ int moe_forward(const moe_shape* s, const void* x, const void* w_router, const f
                 void* ws, size_t ws_bytes, void* stream) {
   return forward_impl(s, x, w_router, router_bias, w1, w3, w2, w1s, w3s, w2s, y, counts, dropped,
                       losses, ws, ws_bytes, stream, nullptr, 0);
+}
+
+int moe_forward_host(const moe_shape* s, const void* x_host, const void* w_router,
+                     const float* router_bias, const void* w1, const void* w3, const void* w2,
+                     const void* w1s, const void* w3s, const void* w2s, void* y_host,
+                     float* losses_host, void* x_dev, void* y_dev, void* ws, size_t ws_bytes,
+                     void* stream) {
+  TRY(check_forward(s, x_dev, w_router, router_bias, w1, w3, w2, w1s, w3s, w2s, y_dev, nullptr,
+                    nullptr, nullptr, ws, ws_bytes, nullptr, 0, nullptr));
+  const size_t bytes = static_cast<size_t>(s->T) * s->d * esize(s);
+  if (s->T > 0) {
+    if (x_host == nullptr) return fail(MOE_ERR_INVALID, "x_host is NULL");
+    if (y_host == nullptr) return fail(MOE_ERR_INVALID, "y_host is NULL");
+  }
+  OPT_PTR4(losses_host, "losses_host");
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (bytes > 0 && cudaMemcpyAsync(x_dev, x_host, bytes, cudaMemcpyHostToDevice, st) != cudaSuccess)
+    return cuda_status("copy x to the device");
+  TRY(forward_impl(s, x_dev, w_router, router_bias, w1, w3, w2, w1s, w3s, w2s, y_dev, nullptr,
+                   nullptr, nullptr, ws, ws_bytes, stream, nullptr, 0));
+  if (bytes > 0 && cudaMemcpyAsync(y_host, y_dev, bytes, cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return cuda_status("copy y to the host");
+  if (losses_host != nullptr &&
+      cudaMemcpyAsync(losses_host, at<float>(ws, layout(s).losses), 2 * sizeof(float),
+                      cudaMemcpyDeviceToHost, st) != cudaSuccess)
+    return cuda_status("copy the losses to the host");
+  return ok();
+}
+
+#define CUDA_TRY(expr, what)                                                          \
+  do {                                                                                \
+    const cudaError_t e_ = (expr);                                                    \
+    if (e_ != cudaSuccess) return fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e_)); \
+  } while (0)
+
+struct moe_host_pipeline {
+  int d = 0, dtype = 0;
+  int64_t max_T = 0;
+  cudaStream_t up = nullptr, down = nullptr;
+  void* x_dev[2] = {nullptr, nullptr};
+  void* y_dev[2] = {nullptr, nullptr};
+  float* losses_dev[2] = {nullptr, nullptr};
+  // per slot: its upload finished / its layer finished / its download finished
+  cudaEvent_t uploaded[2] = {nullptr, nullptr};
+  cudaEvent_t layer_done[2] = {nullptr, nullptr};
+  cudaEvent_t downloaded[2] = {nullptr, nullptr};
+  uint64_t step = 0;
+};
+
+int moe_host_pipeline_destroy(moe_host_pipeline* p) {
+  if (p == nullptr) return MOE_OK;
+  int rc = MOE_OK;
+  auto note = [&](cudaError_t e, const char* what) {
+    if (e != cudaSuccess && rc == MOE_OK) rc = fail(MOE_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+  };
+  // the buffers may still be read by queued copies or layers
+  for (int b = 0; b < 2; ++b)
+    if (p->layer_done[b]) note(cudaEventSynchronize(p->layer_done[b]), "wait for a layer");
+  if (p->up) note(cudaStreamSynchronize(p->up), "wait for the uploads");
+  if (p->down) note(cudaStreamSynchronize(p->down), "wait for the downloads");
+  for (int b = 0; b < 2; ++b) {
+    if (p->x_dev[b]) note(cudaFree(p->x_dev[b]), "free x");
+    if (p->y_dev[b]) note(cudaFree(p->y_dev[b]), "free y");
+    if (p->losses_dev[b]) note(cudaFree(p->losses_dev[b]), "free losses");
+    for (cudaEvent_t e : {p->uploaded[b], p->layer_done[b], p->downloaded[b]})
+      if (e) note(cudaEventDestroy(e), "destroy an event");
+  }
+  if (p->up) note(cudaStreamDestroy(p->up), "destroy the upload stream");
+  if (p->down) note(cudaStreamDestroy(p->down), "destroy the download stream");
+  delete p;
+  return rc;
+}
+
+static int pipeline_setup(moe_host_pipeline* p, const moe_shape* s) {
+  p->d = s->d;
+  p->dtype = s->dtype;
+  p->max_T = s->T;
+  const size_t bytes = std::max<size_t>(static_cast<size_t>(s->T) * s->d * esize(s), 16);
+  CUDA_TRY(cudaStreamCreateWithFlags(&p->up, cudaStreamNonBlocking), "create the upload stream");
+  CUDA_TRY(cudaStreamCreateWithFlags(&p->down, cudaStreamNonBlocking), "create the download stream");
+  for (int b = 0; b < 2; ++b) {
+    CUDA_TRY(cudaMalloc(&p->x_dev[b], bytes), "allocate x");
+    CUDA_TRY(cudaMalloc(&p->y_dev[b], bytes), "allocate y");
+    CUDA_TRY(cudaMalloc(reinterpret_cast<void**>(&p->losses_dev[b]), 2 * sizeof(float)),
+             "allocate losses");
+    for (cudaEvent_t* e : {&p->uploaded[b], &p->layer_done[b], &p->downloaded[b]})
+      CUDA_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "create an event");
+  }
+  return MOE_OK;
+}
+
+int moe_host_pipeline_create(const moe_shape* s_max, moe_host_pipeline** out) {
+  if (out == nullptr) return fail(MOE_ERR_INVALID, "out is NULL");
+  *out = nullptr;
+  TRY(check_shape(s_max));
+  auto* p = new moe_host_pipeline();
+  const int rc = pipeline_setup(p, s_max);
+  if (rc != MOE_OK) {
+    moe_host_pipeline_destroy(p);
+    return rc;
+  }
+  *out = p;
+  return ok();
+}
+
+int moe_host_pipeline_forward(moe_host_pipeline* p, const moe_shape* s, const void* x_host,
+                              const void* w_router, const float* router_bias, const void* w1,
+                              const void* w3, const void* w2, const void* w1s, const void* w3s,
+                              const void* w2s, void* y_host, float* losses_host, void* ws,
+                              size_t ws_bytes, void* stream) {
+  if (p == nullptr) return fail(MOE_ERR_INVALID, "pipeline is NULL");
+  TRY(check_shape(s));
+  if (s->d != p->d || s->dtype != p->dtype || s->T > p->max_T)
+    return fail(MOE_ERR_INVALID, "shape (T %lld, d %d, dtype %d) outside the pipeline's "
+                "(T <= %lld, d %d, dtype %d)", static_cast<long long>(s->T), s->d, s->dtype,
+                static_cast<long long>(p->max_T), p->d, p->dtype);
+  const int b = static_cast<int>(p->step & 1);
+  TRY(check_forward(s, p->x_dev[b], w_router, router_bias, w1, w3, w2, w1s, w3s, w2s,
+                    p->y_dev[b], nullptr, nullptr, p->losses_dev[b], ws, ws_bytes, nullptr, 0,
+                    nullptr));
+  if (s->T > 0) {
+    if (x_host == nullptr) return fail(MOE_ERR_INVALID, "x_host is NULL");
+    if (y_host == nullptr) return fail(MOE_ERR_INVALID, "y_host is NULL");
+  }
+  OPT_PTR4(losses_host, "losses_host");
+  const size_t bytes = static_cast<size_t>(s->T) * s->d * esize(s);
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  // upload into the slot once the layer that last read its x is done
+  CUDA_TRY(cudaStreamWaitEvent(p->up, p->layer_done[b], 0), "order the upload");
+  if (bytes > 0)
+    CUDA_TRY(cudaMemcpyAsync(p->x_dev[b], x_host, bytes, cudaMemcpyHostToDevice, p->up),
+             "copy x to the device");
+  CUDA_TRY(cudaEventRecord(p->uploaded[b], p->up), "record the upload");
+  // the layer: after its upload and after the download that last read the slot's outputs
+  CUDA_TRY(cudaStreamWaitEvent(st, p->uploaded[b], 0), "order the layer");
+  CUDA_TRY(cudaStreamWaitEvent(st, p->downloaded[b], 0), "order the layer");
+  TRY(forward_impl(s, p->x_dev[b], w_router, router_bias, w1, w3, w2, w1s, w3s, w2s, p->y_dev[b],
+                   nullptr, nullptr, p->losses_dev[b], ws, ws_bytes, stream, nullptr, 0));
+  CUDA_TRY(cudaEventRecord(p->layer_done[b], st), "record the layer");
+  // download
+  CUDA_TRY(cudaStreamWaitEvent(p->down, p->layer_done[b], 0), "order the download");
+  if (bytes > 0)
+    CUDA_TRY(cudaMemcpyAsync(y_host, p->y_dev[b], bytes, cudaMemcpyDeviceToHost, p->down),
+             "copy y to the host");
+  if (losses_host != nullptr)
+    CUDA_TRY(cudaMemcpyAsync(losses_host, p->losses_dev[b], 2 * sizeof(float),
+                             cudaMemcpyDeviceToHost, p->down),
+             "copy the losses to the host");
+  CUDA_TRY(cudaEventRecord(p->downloaded[b], p->down), "record the download");
+  ++p->step;
+  return ok();
+}
+
+int moe_host_pipeline_join(moe_host_pipeline* p, void* stream) {
+  if (p == nullptr) return fail(MOE_ERR_INVALID, "pipeline is NULL");
+  for (int b = 0; b < 2; ++b)
+    CUDA_TRY(cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), p->downloaded[b], 0),
+             "join the downloads");
+  return ok();
 }
 
 int moe_forward_events(const moe_shape* s, const void* x, const void* w_router,

@@ -115,6 +115,17 @@ def test_entry_points_reject_before_any_launch():
     assert L.moe_combine(ctypes.byref(s), fake, fake, null, ctypes.c_void_p(0x7f0000000004),
                          null) == -1
     assert L.moe_aux_loss(ctypes.byref(s), null, fake, fake, null) == -1
+    # the host-memory forward checks everything before its first copy
+    def host_fwd(xh=fake, yh=fake, xd=fake, yd=fake, lh=null, wsp=fake, nbytes=need):
+        return L.moe_forward_host(ctypes.byref(s), xh, fake, null, fake, fake, fake, null, null,
+                                  null, yh, lh, xd, yd, wsp, nbytes, null)
+    assert host_fwd(xh=null) == -1
+    assert host_fwd(yh=null) == -1
+    assert host_fwd(xd=null) == -1
+    assert host_fwd(yd=ctypes.c_void_p(0x7f0000000008)) == -1     # misaligned device y
+    assert host_fwd(lh=ctypes.c_void_p(0x7f0000000002)) == -1     # misaligned host losses
+    assert host_fwd(wsp=null) == -4
+    assert host_fwd(nbytes=need - 1) == -4
 
 
 def test_status_strings():
@@ -159,6 +170,30 @@ def test_backward_rejects_before_any_launch():
     assert call(shp=s2, nbytes=moe.moe_backward_workspace_size(s2)) == -1   # shared grads missing
     assert call(ev=(ctypes.c_void_p * 3)(), nev=3) == -1
     assert call(shp=shape(d=96)) == -2
+
+
+def test_host_pipeline_rejects_before_any_cuda_call():
+    """The host pipeline's argument checks run on the host; on a machine without a GPU its
+    creation fails with MOE_ERR_CUDA and hands back no handle."""
+    import torch
+    L = _lib.LIB
+    s = shape()
+    h = ctypes.c_void_p()
+    assert L.moe_host_pipeline_create(ctypes.byref(s), None) == -1
+    bad = shape()
+    bad.k = bad.E + 1
+    assert L.moe_host_pipeline_create(ctypes.byref(bad), ctypes.byref(h)) == -1
+    assert h.value is None
+    null = ctypes.c_void_p(None)
+    fake = ctypes.c_void_p(0x7f0000000000)
+    assert L.moe_host_pipeline_forward(null, ctypes.byref(s), fake, fake, null, fake, fake, fake,
+                                       null, null, null, fake, null, fake,
+                                       moe.moe_workspace_size(s), null) == -1
+    assert L.moe_host_pipeline_join(null, null) == -1
+    assert L.moe_host_pipeline_destroy(null) == 0
+    if not torch.cuda.is_available():
+        assert L.moe_host_pipeline_create(ctypes.byref(s), ctypes.byref(h)) == -3
+        assert h.value is None
 
 
 def test_selftest_rejects_bad_workspace_before_any_launch():

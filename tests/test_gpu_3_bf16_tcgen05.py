@@ -181,19 +181,52 @@ def test_bf16_deterministic():
 
 
 def test_forward_host_stream_matches_device_forward():
-    """MoELayer.forward_host_stream (pipelined host->device->host over several batches)
-    returns, batch by batch, exactly what the device-resident forward returns."""
+    """MoELayer.forward_host_stream (the C ABI's host pipeline: uploads, layers and downloads
+    on three streams over several batches, two device slots reused in turn) returns, batch by
+    batch, exactly the y and losses of the device-resident forward; batches of several sizes,
+    an empty one included, and two calls on the same pipeline."""
     import mixture_experts_layer_92_b300 as moe
     w = WORKLOADS["mixtral_prefill"].scaled(T=256, d=256, E=8, k=2, d_ff=384)
     inp = dev_inputs(w)
     layer = moe.MoELayer(inp["w_router"], inp["w1"], inp["w3"], inp["w2"], k=w.k, gate=w.gate,
                          max_tokens=w.T)
-    xs = [torch.randn(w.T, w.d, generator=torch.Generator().manual_seed(i)).to(torch.bfloat16)
-          .pin_memory() for i in range(5)]
-    ys = [torch.empty(w.T, w.d, dtype=torch.bfloat16).pin_memory() for _ in range(5)]
-    layer.forward_host_stream(xs, ys)
+    sizes = [256, 200, 0, 256, 33, 256, 129]
+    xs = [torch.randn(T, w.d, generator=torch.Generator().manual_seed(i)).to(torch.bfloat16)
+          .pin_memory() for i, T in enumerate(sizes)]
+    ys = [torch.full((T, w.d), float("nan"), dtype=torch.bfloat16).pin_memory() for T in sizes]
+    ls = [torch.full((2,), float("nan")).pin_memory() for _ in sizes]
+    layer.forward_host_stream(xs[:4], ys[:4], ls[:4])
+    layer.forward_host_stream(xs[4:], ys[4:], ls[4:])
     torch.cuda.synchronize()
-    for xh, yh in zip(xs, ys):
+    assert layer.device_error() == 0
+    for xh, yh, lh in zip(xs, ys, ls):
         ref = layer.forward(xh.to(DEV))
         torch.cuda.synchronize()
         assert torch.equal(yh, ref.cpu())
+        assert torch.equal(lh, layer.losses.cpu())
+
+
+def test_forward_host_entry_point_matches_device_forward():
+    """moe_forward_host (host x in, the layer, host y and losses out, on one stream) returns
+    exactly what moe_forward returns on the same inputs, including a shared expert."""
+    import mixture_experts_layer_92_b300 as moe
+    w = WORKLOADS["deepseek_fine"].scaled(T=333, d=256, E=16, k=4, d_ff=256, d_ff_shared=128)
+    inp = dev_inputs(w)
+    layer = moe.MoELayer(inp["w_router"], inp["w1"], inp["w3"], inp["w2"], k=w.k, gate=w.gate,
+                         router_bias=inp["router_bias"], w1s=inp["w1s"], w3s=inp["w3s"],
+                         w2s=inp["w2s"], max_tokens=w.T)
+    ref = layer.forward(inp["x"])
+    torch.cuda.synchronize()
+    x_host = inp["x"].cpu().pin_memory()
+    y_host = torch.empty_like(x_host).pin_memory()
+    losses_host = torch.empty(2, dtype=torch.float32).pin_memory()
+    x_dev, y_dev = torch.empty_like(inp["x"]), torch.empty_like(inp["x"])
+    ws = moe.alloc_workspace(layer.shape(w.T), device=DEV)
+    moe.moe_forward_host(layer.shape(w.T), ws, x_host, inp["w_router"], inp["w1"], inp["w3"],
+                         inp["w2"], y_host, x_dev, y_dev, router_bias=inp["router_bias"],
+                         w1s=inp["w1s"], w3s=inp["w3s"], w2s=inp["w2s"],
+                         losses_host=losses_host)
+    torch.cuda.synchronize()
+    assert moe.moe_get_error(ws) == 0
+    assert torch.equal(y_host, ref.cpu())
+    assert torch.equal(losses_host, layer.losses.cpu())
