@@ -254,11 +254,22 @@ def oracle_threads() -> int:
         return os.cpu_count() or 1
 
 
+def grow_sample(n, t, n_max, target_s):
+    """The next sample size when a sample of n tokens took t seconds, aiming at target_s;
+    None once the sample is long enough (half the target) or the whole batch. The oracle has
+    a per-call cost that does not scale with n, so one extrapolation can fall well short."""
+    if t >= 0.5 * target_s or n >= n_max:
+        return None
+    return int(min(n_max, max(2 * n, n * target_s / max(t, 1e-3) * 0.8)))
+
+
 def cpu_baseline(w, inp_host: dict, target_s: float = 15.0):
     n = min(w.T, 16)
     t = oracle_sample(w, inp_host, n)
-    n2 = int(min(w.T, max(n, n * target_s / max(t, 1e-3) * 0.8)))
-    if n2 > n:
+    for _ in range(3):
+        n2 = grow_sample(n, t, w.T, target_s)
+        if n2 is None:
+            break
         t = oracle_sample(w, inp_host, n2)
         n = n2
     return dict(value=n / t, unit=UNIT, cores=oracle_threads(), kind="oracle",
@@ -659,8 +670,10 @@ def run_train(args, w, rank, world, local_rank):
         dyh64 = dy.float().cpu().numpy()
         n = min(w.T, 4)
         tt = oracle_train_sample(w, ih, dyh64, n)
-        n2 = int(min(w.T, max(n, n * args.cpu_seconds / max(tt, 1e-3) * 0.8)))
-        if n2 > n:
+        for _ in range(3):
+            n2 = grow_sample(n, tt, w.T, args.cpu_seconds)
+            if n2 is None:
+                break
             tt = oracle_train_sample(w, ih, dyh64, n2)
             n = n2
         cpu = dict(value=n / tt, unit=UNIT, cores=oracle_threads(), kind="oracle",

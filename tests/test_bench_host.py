@@ -45,6 +45,19 @@ def test_stage_roofline_binds_the_slower_roof():
     assert r["frac"] == pytest.approx(0.5)
 
 
+def test_cpu_sample_grows_until_half_the_target():
+    # a fixed per-call cost: 16 tokens in 2.4 s extrapolates to 80 tokens for a 15 s target
+    assert bench.grow_sample(16, 2.4, 4096, 15.0) == 80
+    # a sample that still took 2.25 s grows again, at least doubling
+    assert bench.grow_sample(80, 2.25, 4096, 15.0) == 426
+    assert bench.grow_sample(80, 7.0, 4096, 15.0) == 160
+    assert bench.grow_sample(80, 5.0, 4096, 15.0) == 192
+    # long enough, or already the whole batch
+    assert bench.grow_sample(426, 7.5, 4096, 15.0) is None
+    assert bench.grow_sample(4096, 1.0, 4096, 15.0) is None
+    assert bench.grow_sample(3000, 1.0, 4096, 15.0) == 4096
+
+
 def test_algorithmic_work_of_the_prefill_layer():
     """Mixtral prefill, no drop: R = T k kept rows, every expert touched."""
     w = WORKLOADS["mixtral_prefill"]
