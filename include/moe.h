@@ -377,7 +377,7 @@ int moe_backward(const moe_shape* s, const void* x, const void* w_router, const 
  * scratch (the per-block partial sums behind stats) in a fixed 2 MiB array inside the
  * library's own device memory, so it allocates nothing.
  *   - Limit: route_blocks(T) * (E + 1) * 4 bytes must fit in 2 MiB, where route_blocks(T) =
- *     min(ceil(T / 8), 1024): any T for E <= 511. Larger sizes return MOE_ERR_UNSUPPORTED
+ *     min(ceil(T / 8), 592): any T for E <= 884. Larger sizes return MOE_ERR_UNSUPPORTED
  *     with the needed and available bytes in moe_last_error_detail().
  *   - The array exists once per GPU that loads the library and is held until the process
  *     exits. Every call on a device shares it, so calls that overlap on the GPU (e.g. on two

@@ -107,12 +107,25 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int chunk,
   }
   grid_barrier(err, gridDim.x);
 
-  // phase 2: this CTA's base per expert, the totals, the kept counts
+  // phase 2: this CTA's base per expert, the totals, the kept counts (eight CTAs' counts
+  // loaded at a time, so their L2 latencies overlap)
   for (int e = tid; e < E; e += kDispThreads) {
     int before = 0, total = 0;
-    for (int b = 0; b < static_cast<int>(gridDim.x); ++b) {
+    const int nb = static_cast<int>(gridDim.x), me = static_cast<int>(blockIdx.x);
+    int b = 0;
+    for (; b + 8 <= nb; b += 8) {
+      int c[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) c[u] = __ldcg(blk_hist + static_cast<size_t>(b + u) * E + e);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) {
+        if (b + u < me) before += c[u];
+        total += c[u];
+      }
+    }
+    for (; b < nb; ++b) {
       const int c = __ldcg(blk_hist + static_cast<size_t>(b) * E + e);
-      if (b < static_cast<int>(blockIdx.x)) before += c;
+      if (b < me) before += c;
       total += c;
     }
     s_base[e] = before;

@@ -21,7 +21,7 @@ namespace moe {
 namespace {
 
 // 2 MiB: partials of route_blocks(T) blocks x (E + 1) floats. Enough for any T when
-// E <= 511 (at most 1024 blocks), and for larger E while T is small enough.
+// E <= 884 (at most 592 blocks), and for larger E while T is small enough.
 constexpr size_t kNoAllocScratchBytes = 2u << 20;
 
 static __device__ __align__(256) float g_route_scratch[kNoAllocScratchBytes / sizeof(float)];
