@@ -266,7 +266,7 @@ def grow_sample(n, t, n_max, target_s):
 def cpu_baseline(w, inp_host: dict, target_s: float = 15.0):
     n = min(w.T, 16)
     t = oracle_sample(w, inp_host, n)
-    for _ in range(3):
+    for _ in range(5):
         n2 = grow_sample(n, t, w.T, target_s)
         if n2 is None:
             break
@@ -670,7 +670,7 @@ def run_train(args, w, rank, world, local_rank):
         dyh64 = dy.float().cpu().numpy()
         n = min(w.T, 4)
         tt = oracle_train_sample(w, ih, dyh64, n)
-        for _ in range(3):
+        for _ in range(5):
             n2 = grow_sample(n, tt, w.T, args.cpu_seconds)
             if n2 is None:
                 break
