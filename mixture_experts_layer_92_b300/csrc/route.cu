@@ -57,14 +57,30 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
   float lse2 = 0.f;
 
   const int nwarps = gridDim.x * kRouteWarps;
-  // the rows of a warp's next token are pulled into L2 while it works on this one
+  // A warp's next token is fetched while it works on this one: the first split plane of its
+  // logits into registers, the other planes (if any) into L2.
   const int lines = (E * 4 + 127) / 128;
+  float nxt[JM];
+  {
+    const int t0 = blockIdx.x * kRouteWarps + warp;
+#pragma unroll
+    for (int j = 0; j < JM; ++j)
+      nxt[j] = (t0 < T && (FULL || lane + 32 * j < E))
+                   ? __ldg(logits + static_cast<size_t>(t0) * E + lane + 32 * j) : 0.f;
+  }
   for (int t = blockIdx.x * kRouteWarps + warp; t < T; t += nwarps) {
     const float* row = logits + static_cast<size_t>(t) * E;
+    float first[JM];
+#pragma unroll
+    for (int j = 0; j < JM; ++j) first[j] = nxt[j];
     if (t + nwarps < T) {
-      for (int i = lane; i < lines * nsplit; i += 32) {
-        const int sp = i / lines;
-        const float* p = row + static_cast<size_t>(nwarps) * E + sp * split_stride + (i - sp * lines) * 32;
+      const float* row_n = row + static_cast<size_t>(nwarps) * E;
+#pragma unroll
+      for (int j = 0; j < JM; ++j)
+        if (FULL || lane + 32 * j < E) nxt[j] = __ldg(row_n + lane + 32 * j);
+      for (int i = lane; i < lines * (nsplit - 1); i += 32) {
+        const int sp = 1 + i / lines;
+        const float* p = row_n + sp * split_stride + (i - (sp - 1) * lines) * 32;
         asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
       }
     }
@@ -77,7 +93,7 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
       slot[j] = -1;
       if (FULL || e < E) {
         // split-K partial sums of the router GEMM, added in split order, then the bias
-        float acc = __ldg(row + e);
+        float acc = first[j];
         for (int sp = 1; sp < nsplit; ++sp) acc += __ldg(row + sp * split_stride + e);
         if (bias != nullptr) acc += __ldg(bias + e);
         if (logits_out != nullptr) logits_out[static_cast<size_t>(t) * E + e] = acc;
