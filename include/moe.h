@@ -17,7 +17,9 @@
  * Conventions for every entry point:
  *   - Every pointer argument is a DEVICE pointer unless stated otherwise. The caller owns
  *     all buffers; the library allocates no device memory and keeps no state between
- *     calls, except a per-device cache of kernel attributes and tensor-map entry point.
+ *     calls, except a per-device cache of kernel attributes and tensor-map entry point, the
+ *     fixed scratch array of moe_route_topk_noalloc, and the host pipeline handles that the
+ *     caller creates and destroys (their streams and events).
  *   - Matrices are row-major and contiguous. Element type is moe_shape.dtype (fp32 or
  *     bf16) for x, weights, y and the permuted buffers; logits, gates, statistics and
  *     losses are always fp32; indices and counts are int32.
@@ -193,14 +195,19 @@ int moe_forward_host(const moe_shape* s, const void* x_host, const void* w_route
 /* A pipeline for a stream of host batches through one layer: batch i's x is uploaded on the
  * pipeline's own upload stream, the layer runs on the caller's stream, and y (and the two
  * losses) come back on its own download stream, so the upload of batch i+1 and the download
- * of batch i-1 overlap the layer on batch i and both copy directions stay busy. It owns two
- * slots of device buffers (x and y [T_max, d], losses [2]), the two copy streams (non-blocking)
- * and the events that order a slot's reuse: a slot's upload waits for the layer that last read
- * it, and its layer waits for its upload and for the download that last read its outputs.
+ * of batch i-1 overlap the layer on batch i and both copy directions stay busy. It keeps two
+ * slots of device buffers (x and y [T_max, d], losses [2]) in a buffer the caller provides, and
+ * owns the two copy streams (non-blocking) and the events that order a slot's reuse: a slot's
+ * upload waits for the layer that last read it, and its layer waits for its upload and for
+ * the download that last read its outputs.
  *
- * moe_host_pipeline_create: `s_max` fixes d and dtype and the largest T; `*out` receives the
- * handle (NULL on error). Allocates on the current CUDA device, which every later call on the
- * handle must also have current.
+ * moe_host_pipeline_buffer_size: bytes of device buffer a pipeline for shapes up to `s_max`
+ * needs (0 for an invalid shape).
+ * moe_host_pipeline_create: `s_max` fixes d and dtype and the largest T; `buf` is a device
+ * buffer of at least moe_host_pipeline_buffer_size(s_max) bytes, 256-byte aligned, owned by
+ * the caller and kept until moe_host_pipeline_destroy returns (MOE_ERR_WORKSPACE otherwise);
+ * `*out` receives the handle (NULL on error). Creates its streams and events on the current
+ * CUDA device, which every later call on the handle must also have current.
  * moe_host_pipeline_forward: one batch, arguments as in moe_forward_host (x_host [T, d] and
  * y_host [T, d] page-locked, losses_host [2] or NULL), with s->d and s->dtype as at create
  * and s->T <= T_max. The layer runs on `stream` with workspace `ws`; calls that share a
@@ -208,10 +215,12 @@ int moe_forward_host(const moe_shape* s, const void* x_host, const void* w_route
  * queuing; the host buffers must stay valid until moe_host_pipeline_join's stream reaches the
  * join. Host-side argument errors return before anything is queued.
  * moe_host_pipeline_join: `stream` waits (on the device) for every download queued so far.
- * moe_host_pipeline_destroy: waits for the pipeline's queued work, then frees it; NULL is a
- * no-op. */
+ * moe_host_pipeline_destroy: waits for the pipeline's queued work, then destroys its streams,
+ * events and handle (the buffer stays the caller's); NULL is a no-op. */
 typedef struct moe_host_pipeline moe_host_pipeline;
-int moe_host_pipeline_create(const moe_shape* s_max, moe_host_pipeline** out);
+size_t moe_host_pipeline_buffer_size(const moe_shape* s_max);
+int moe_host_pipeline_create(const moe_shape* s_max, void* buf, size_t buf_bytes,
+                             moe_host_pipeline** out);
 int moe_host_pipeline_forward(moe_host_pipeline* p, const moe_shape* s, const void* x_host,
                               const void* w_router, const float* router_bias, const void* w1,
                               const void* w3, const void* w2, const void* w1s, const void* w3s,

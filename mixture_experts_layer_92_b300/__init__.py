@@ -99,7 +99,7 @@ class MoELayer:
             return self._forward_host_stream_copies(x_hosts, y_hosts)
         comp = torch.cuda.current_stream(self.device)
         if getattr(self, "_host_pipe", None) is None:
-            self._host_pipe = HostPipeline(self.shape(self.max_tokens))
+            self._host_pipe = HostPipeline(self.shape(self.max_tokens), device=self.device)
         for i, (xh, yh) in enumerate(zip(x_hosts, y_hosts)):
             self._host_pipe.forward(self.shape(xh.shape[0]), self.ws, xh, self.w["w_router"],
                                self.w["w1"], self.w["w3"], self.w["w2"], yh,

@@ -31,8 +31,8 @@ EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_
             "moe_update_select_bias", "moe_forward_balanced", "moe_expert_choice",
             "moe_grouped_swiglu_fp8w", "moe_forward_fp8w", "moe_backward_workspace_size",
             "moe_backward", "moe_selftest_wait_timeout", "moe_forward_host",
-            "moe_host_pipeline_create", "moe_host_pipeline_forward", "moe_host_pipeline_join",
-            "moe_host_pipeline_destroy")
+            "moe_host_pipeline_buffer_size", "moe_host_pipeline_create",
+            "moe_host_pipeline_forward", "moe_host_pipeline_join", "moe_host_pipeline_destroy")
 NUM_BWD_STAGES = 8
 BWD_STAGE_NAMES = ("route_dispatch", "gather_x_dy", "recompute_gu", "gemm_dh_swiglu_bwd",
                    "gate_logit_grads", "gemm_dx", "dx_combine", "gemm_wgrad")
@@ -77,7 +77,8 @@ def _load() -> ctypes.CDLL:
         "moe_selftest_wait_timeout": (ctypes.c_int, [vp, sz, vp]),
         "moe_forward_host": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                             vp, sz, vp]),
-        "moe_host_pipeline_create": (ctypes.c_int, [sp, ctypes.POINTER(vp)]),
+        "moe_host_pipeline_buffer_size": (sz, [sp]),
+        "moe_host_pipeline_create": (ctypes.c_int, [sp, vp, sz, ctypes.POINTER(vp)]),
         "moe_host_pipeline_forward": (ctypes.c_int, [vp, sp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                      vp, vp, vp, sz, vp]),
         "moe_host_pipeline_join": (ctypes.c_int, [vp, vp]),
@@ -323,12 +324,17 @@ def moe_forward_host(s, ws, x_host, w_router, w1, w3, w2, y_host, x_dev, y_dev, 
 class HostPipeline:
     """Handle of a moe_host_pipeline (see include/moe.h): a stream of pinned host batches
     through one layer, uploads and downloads on the pipeline's own streams overlapping the
-    layers on the caller's stream. `s_max` fixes d, dtype and the largest T."""
+    layers on the caller's stream. `s_max` fixes d, dtype and the largest T; the slot buffers
+    are one torch allocation on `device`, held by this object."""
 
-    def __init__(self, s_max):
+    def __init__(self, s_max, device=None):
+        n = LIB.moe_host_pipeline_buffer_size(ctypes.byref(s_max))
+        if n == 0:
+            _check(LIB.moe_check_shape(ctypes.byref(s_max)), "moe_host_pipeline_buffer_size")
+        self.buf = torch.empty(n, dtype=torch.uint8, device=device or "cuda")
         h = ctypes.c_void_p()
-        _check(LIB.moe_host_pipeline_create(ctypes.byref(s_max), ctypes.byref(h)),
-               "moe_host_pipeline_create")
+        _check(LIB.moe_host_pipeline_create(ctypes.byref(s_max), _p(self.buf), self.buf.numel(),
+                                            ctypes.byref(h)), "moe_host_pipeline_create")
         self._h = h
 
     def forward(self, s, ws, x_host, w_router, w1, w3, w2, y_host, router_bias=None, w1s=None,

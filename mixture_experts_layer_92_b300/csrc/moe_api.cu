@@ -1459,9 +1459,6 @@ int moe_host_pipeline_destroy(moe_host_pipeline* p) {
   if (p->up) note(cudaStreamSynchronize(p->up), "wait for the uploads");
   if (p->down) note(cudaStreamSynchronize(p->down), "wait for the downloads");
   for (int b = 0; b < 2; ++b) {
-    if (p->x_dev[b]) note(cudaFree(p->x_dev[b]), "free x");
-    if (p->y_dev[b]) note(cudaFree(p->y_dev[b]), "free y");
-    if (p->losses_dev[b]) note(cudaFree(p->losses_dev[b]), "free losses");
     for (cudaEvent_t e : {p->uploaded[b], p->layer_done[b], p->downloaded[b]})
       if (e) note(cudaEventDestroy(e), "destroy an event");
   }
@@ -1471,30 +1468,52 @@ int moe_host_pipeline_destroy(moe_host_pipeline* p) {
   return rc;
 }
 
-static int pipeline_setup(moe_host_pipeline* p, const moe_shape* s) {
+// The caller's buffer, slot by slot: x [T_max, d], y [T_max, d], losses [2], each rounded up
+// to kAlign bytes.
+size_t pipeline_slot_bytes(const moe_shape* s) {
+  const size_t rows = static_cast<size_t>(s->T) * s->d * esize(s);
+  const size_t r = (rows + kAlign - 1) / kAlign * kAlign;
+  return 2 * r + kAlign;
+}
+
+static int pipeline_setup(moe_host_pipeline* p, const moe_shape* s, void* buf) {
   p->d = s->d;
   p->dtype = s->dtype;
   p->max_T = s->T;
-  const size_t bytes = std::max<size_t>(static_cast<size_t>(s->T) * s->d * esize(s), 16);
+  const size_t slot = pipeline_slot_bytes(s);
+  const size_t rows = (slot - kAlign) / 2;
+  for (int b = 0; b < 2; ++b) {
+    uint8_t* base = static_cast<uint8_t*>(buf) + b * slot;
+    p->x_dev[b] = base;
+    p->y_dev[b] = base + rows;
+    p->losses_dev[b] = reinterpret_cast<float*>(base + 2 * rows);
+  }
   CUDA_TRY(cudaStreamCreateWithFlags(&p->up, cudaStreamNonBlocking), "create the upload stream");
   CUDA_TRY(cudaStreamCreateWithFlags(&p->down, cudaStreamNonBlocking), "create the download stream");
-  for (int b = 0; b < 2; ++b) {
-    CUDA_TRY(cudaMalloc(&p->x_dev[b], bytes), "allocate x");
-    CUDA_TRY(cudaMalloc(&p->y_dev[b], bytes), "allocate y");
-    CUDA_TRY(cudaMalloc(reinterpret_cast<void**>(&p->losses_dev[b]), 2 * sizeof(float)),
-             "allocate losses");
+  for (int b = 0; b < 2; ++b)
     for (cudaEvent_t* e : {&p->uploaded[b], &p->layer_done[b], &p->downloaded[b]})
       CUDA_TRY(cudaEventCreateWithFlags(e, cudaEventDisableTiming), "create an event");
-  }
   return MOE_OK;
 }
 
-int moe_host_pipeline_create(const moe_shape* s_max, moe_host_pipeline** out) {
+size_t moe_host_pipeline_buffer_size(const moe_shape* s_max) {
+  if (check_shape(s_max) != MOE_OK) return 0;
+  return 2 * pipeline_slot_bytes(s_max);
+}
+
+int moe_host_pipeline_create(const moe_shape* s_max, void* buf, size_t buf_bytes,
+                             moe_host_pipeline** out) {
   if (out == nullptr) return fail(MOE_ERR_INVALID, "out is NULL");
   *out = nullptr;
   TRY(check_shape(s_max));
+  if (buf == nullptr) return fail(MOE_ERR_WORKSPACE, "pipeline buffer is NULL");
+  if ((reinterpret_cast<uintptr_t>(buf) & (kAlign - 1)) != 0)
+    return fail(MOE_ERR_WORKSPACE, "pipeline buffer is not %zu-byte aligned", kAlign);
+  const size_t need = 2 * pipeline_slot_bytes(s_max);
+  if (buf_bytes < need)
+    return fail(MOE_ERR_WORKSPACE, "pipeline buffer has %zu bytes, needs %zu", buf_bytes, need);
   auto* p = new moe_host_pipeline();
-  const int rc = pipeline_setup(p, s_max);
+  const int rc = pipeline_setup(p, s_max, buf);
   if (rc != MOE_OK) {
     moe_host_pipeline_destroy(p);
     return rc;

@@ -179,20 +179,30 @@ def test_host_pipeline_rejects_before_any_cuda_call():
     L = _lib.LIB
     s = shape()
     h = ctypes.c_void_p()
-    assert L.moe_host_pipeline_create(ctypes.byref(s), None) == -1
-    bad = shape()
-    bad.k = bad.E + 1
-    assert L.moe_host_pipeline_create(ctypes.byref(bad), ctypes.byref(h)) == -1
-    assert h.value is None
     null = ctypes.c_void_p(None)
     fake = ctypes.c_void_p(0x7f0000000000)
+    # two slots of x and y [T, d] and the losses, each rounded up to 256 bytes
+    row_bytes = -(-s.T * s.d * (2 if s.dtype == 1 else 4) // 256) * 256
+    need = L.moe_host_pipeline_buffer_size(ctypes.byref(s))
+    assert need == 2 * (2 * row_bytes + 256)
+    assert L.moe_host_pipeline_create(ctypes.byref(s), fake, need, None) == -1
+    bad = shape()
+    bad.k = bad.E + 1
+    assert L.moe_host_pipeline_buffer_size(ctypes.byref(bad)) == 0
+    assert L.moe_host_pipeline_create(ctypes.byref(bad), fake, need, ctypes.byref(h)) == -1
+    assert h.value is None
+    assert L.moe_host_pipeline_create(ctypes.byref(s), null, need, ctypes.byref(h)) == -4
+    assert L.moe_host_pipeline_create(ctypes.byref(s), fake, need - 1, ctypes.byref(h)) == -4
+    assert L.moe_host_pipeline_create(ctypes.byref(s), ctypes.c_void_p(0x7f0000000010), need,
+                                      ctypes.byref(h)) == -4            # misaligned
+    assert h.value is None
     assert L.moe_host_pipeline_forward(null, ctypes.byref(s), fake, fake, null, fake, fake, fake,
                                        null, null, null, fake, null, fake,
                                        moe.moe_workspace_size(s), null) == -1
     assert L.moe_host_pipeline_join(null, null) == -1
     assert L.moe_host_pipeline_destroy(null) == 0
     if not torch.cuda.is_available():
-        assert L.moe_host_pipeline_create(ctypes.byref(s), ctypes.byref(h)) == -3
+        assert L.moe_host_pipeline_create(ctypes.byref(s), fake, need, ctypes.byref(h)) == -3
         assert h.value is None
 
 
