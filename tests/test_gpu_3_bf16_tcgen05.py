@@ -230,3 +230,24 @@ def test_forward_host_entry_point_matches_device_forward():
     assert moe.moe_get_error(ws) == 0
     assert torch.equal(y_host, ref.cpu())
     assert torch.equal(losses_host, layer.losses.cpu())
+
+
+@pytest.mark.parametrize("w", [
+    WORKLOADS["mixtral_prefill"].scaled(T=1000, d=256, E=8, k=2, d_ff=256),
+    WORKLOADS["switch_top1"].scaled(T=5000, d=256, E=128, k=1, d_ff=256),
+    WORKLOADS["deepseek_fine"].scaled(T=600, d=256, E=256, k=8, d_ff=128, d_ff_shared=128),
+    WORKLOADS["tiny_fp32"],
+], ids=["mixtral_shaped", "switch_shaped", "deepseek_shaped", "tiny_fp32"])
+def test_forward_losses_equal_step_by_step_losses(w):
+    """The forward's balance losses (its statistics-and-losses kernel) and the step-by-step
+    path (moe_route_topk's statistics fed to moe_aux_loss with the forward's counts) give the
+    same two numbers bit for bit: the same reduction order over the same partial sums. The
+    shapes reduce 9, 129 and 257 rows of partial sums, in bf16 and fp32."""
+    import mixture_experts_layer_92_b300 as moe
+    inp = dev_inputs(w)
+    g = gpu_forward(w, inp)
+    assert g["error"] == 0
+    losses2 = torch.full((2,), float("nan"), device=DEV)
+    moe.moe_aux_loss(g["shape"], g["stats"], g["counts"], losses2)
+    torch.cuda.synchronize()
+    assert torch.equal(g["losses"], losses2), (g["losses"], losses2)
