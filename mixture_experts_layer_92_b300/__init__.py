@@ -154,7 +154,17 @@ class MoELayer:
     def forward_host(self, x_host: torch.Tensor, x_dev: torch.Tensor, y_dev: torch.Tensor,
                      y_host: torch.Tensor, losses_host: Optional[torch.Tensor] = None):
         """End-to-end call from host memory: copy x (pinned) to the device, run the layer,
-        copy y (and the two losses) back, all on the current stream."""
+        copy y (and the two losses) back, all on the current stream. Plain bf16/fp32 layers
+        make this one moe_forward_host call (counts, dropped and losses then stay in the
+        workspace; losses_host receives the losses); 8-bit and balanced layers copy through
+        torch around their forward call."""
+        if self.fp8 is None and self.select_bias is None:
+            moe_forward_host(self.shape(x_host.shape[0]), self.ws, x_host, self.w["w_router"],
+                             self.w["w1"], self.w["w3"], self.w["w2"], y_host, x_dev, y_dev,
+                             router_bias=self.w["router_bias"], w1s=self.w["w1s"],
+                             w3s=self.w["w3s"], w2s=self.w["w2s"], losses_host=losses_host,
+                             stream=torch.cuda.current_stream(self.device))
+            return y_host
         x_dev.copy_(x_host, non_blocking=True)
         self.forward(x_dev, y_dev)
         y_host.copy_(y_dev, non_blocking=True)

@@ -230,6 +230,14 @@ def test_forward_host_entry_point_matches_device_forward():
     assert moe.moe_get_error(ws) == 0
     assert torch.equal(y_host, ref.cpu())
     assert torch.equal(losses_host, layer.losses.cpu())
+    # the same through MoELayer.forward_host
+    y_host2 = torch.empty_like(x_host).pin_memory()
+    losses_host2 = torch.empty(2, dtype=torch.float32).pin_memory()
+    layer.forward_host(x_host, x_dev, y_dev, y_host2, losses_host2)
+    torch.cuda.synchronize()
+    assert layer.device_error() == 0
+    assert torch.equal(y_host2, ref.cpu())
+    assert torch.equal(losses_host2, losses_host)
 
 
 @pytest.mark.parametrize("w", [
