@@ -221,7 +221,9 @@ class ClockSampler:
         pw = [num(r[2]) for r in self.rows if num(r[2]) is not None]
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
         reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v == "Active"})
-        busy = [s for s, p in zip(sm, pw) if p is not None and p > 300] or sm
+        # the clock under load: samples drawing more than 300 W (clock and power of one row)
+        busy = [num(r[0]) for r in self.rows
+                if num(r[0]) is not None and num(r[2]) is not None and num(r[2]) > 300] or sm
         return dict(sm_mhz=statistics.median(busy) if busy else None,
                     sm_max_mhz=max(mx) if mx else None, reasons=reasons, samples=len(self.rows),
                     power_w_max=max(pw) if pw else None)

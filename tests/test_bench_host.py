@@ -58,6 +58,48 @@ def test_cpu_sample_grows_until_half_the_target():
     assert bench.grow_sample(3000, 1.0, 4096, 15.0) == 4096
 
 
+def _row(sm, mx, pw, cap="Not Active", hw="Not Active"):
+    return [str(sm), str(mx), str(pw), "0x0", hw, "Not Active", "Not Active", cap]
+
+
+def test_clock_summary_takes_the_median_under_load():
+    c = bench.ClockSampler(0)
+    c.rows = [_row(2032, 2032, 120), _row(1300, 2032, 1050, cap="Active"),
+              _row("[N/A]", 2032, 900), _row(1400, 2032, 1000), _row(1350, 2032, 1090)]
+    s = c.summary()
+    # rows above 300 W with a readable clock: 1300, 1400, 1350 (the idle 2032 MHz sample and
+    # the unreadable one are left out, without shifting the clock/power pairing)
+    assert s["sm_mhz"] == 1350.0 and s["sm_max_mhz"] == 2032.0
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 5
+    assert s["power_w_max"] == 1090.0
+
+
+def test_clock_summary_reports_slowdowns_and_empty_records():
+    c = bench.ClockSampler(0)
+    c.rows = [_row(1000, 2032, 200, hw="Active")]
+    s = c.summary()
+    assert s["sm_mhz"] == 1000.0 and s["reasons"] == ["hw_slowdown"]
+    c.rows = []
+    assert bench.ClockSampler.summary(c) == dict(sm_mhz=None, sm_max_mhz=None, reasons=[],
+                                                  samples=0)
+
+
+def test_traffic_is_read_only_while_the_kernel_source_is_unchanged(tmp_path, monkeypatch):
+    (tmp_path / "profiles").mkdir()
+    csrc = tmp_path / "mixture_experts_layer_92_b300" / "csrc"
+    csrc.mkdir(parents=True)
+    (csrc / "k.cu").write_text("// kernel\n")
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    sha = bench.source_sha(str(csrc / "k.cu"))
+    prof = tmp_path / "profiles" / "gemm_x__wl.txt"
+    prof.write_text(f"source_file: k.cu\nsource_sha256_16: {sha}\n"
+                    "dram_bytes_per_launch: 1.5e9 (read + write)\n")
+    assert bench.traffic_from_profile("wl", "gemm_x") == 1.5e9
+    (csrc / "k.cu").write_text("// kernel, changed\n")
+    assert bench.traffic_from_profile("wl", "gemm_x") is None      # stale capture
+    assert bench.traffic_from_profile("other", "gemm_x") is None   # no capture
+
+
 def test_algorithmic_work_of_the_prefill_layer():
     """Mixtral prefill, no drop: R = T k kept rows, every expert touched."""
     w = WORKLOADS["mixtral_prefill"]
