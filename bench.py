@@ -295,16 +295,29 @@ def oracle_train_sample(w, inp_host: dict, dy_host, n_tokens: int):
     return time.perf_counter() - t0
 
 
+def step_tokens(n1, t1, n2, t2, n_max, target_s=3.0):
+    """Tokens per reference step from two timed samples, on the fit t(n) = a + b*n (a: the
+    oracle's per-call cost that does not depend on the tokens, b: per token). A step is sized
+    to max(target_s, 2a) seconds, so that at least half of it is per-token work; clamped to
+    [n1, n_max]."""
+    b = max((t2 - t1) / max(n2 - n1, 1), 1e-9)
+    a = max(t1 - b * n1, 0.0)
+    n = int(round((max(target_s, 2.0 * a) - a) / b))
+    return max(n1, min(n_max, n))
+
+
 def run_reference(args, w, rank):
     if rank != 0:
         return
     inp = make_inputs(w, device="cuda" if torch.cuda.is_available() else "cpu")
     ih = host_inputs(inp)
     del inp
-    # size one step to a few seconds
-    n = min(w.T, 8)
-    t = oracle_sample(w, ih, n)
-    n = int(min(w.T, max(n, n * 3.0 / max(t, 1e-3))))
+    # size one step to a few seconds, from two samples
+    n1 = min(w.T, 8)
+    t1 = oracle_sample(w, ih, n1)
+    n2 = min(w.T, 72)
+    t2 = oracle_sample(w, ih, n2) if n2 > n1 else t1
+    n = step_tokens(n1, t1, n2, t2, w.T)
     for _ in range(args.warmup):
         oracle_sample(w, ih, n)
     total = 0.0

@@ -100,6 +100,21 @@ def test_traffic_is_read_only_while_the_kernel_source_is_unchanged(tmp_path, mon
     assert bench.traffic_from_profile("other", "gemm_x") is None   # no capture
 
 
+def test_reference_step_size_from_a_two_point_fit():
+    # 2.4 s of fixed cost and 1 ms per token: a step of max(3, 4.8) s holds 2400 tokens
+    t = lambda n: 2.4 + 1e-3 * n
+    assert bench.step_tokens(8, t(8), 72, t(72), 4096) == 2400
+    # no fixed cost: 3 s of tokens
+    t = lambda n: 2e-3 * n
+    assert bench.step_tokens(8, t(8), 72, t(72), 4096) == 1500
+    # clamped to the batch, and never below the first sample
+    assert bench.step_tokens(8, 0.01, 72, 0.02, 256) == 256
+    # 4.5 s fixed, 62.5 ms per token: a 9 s step holds 72 tokens
+    assert bench.step_tokens(8, 5.0, 72, 9.0, 4096) == 72
+    # timing noise that makes the second sample faster: never below the first sample
+    assert bench.step_tokens(8, 2.0, 72, 1.9, 4096) >= 8
+
+
 def test_algorithmic_work_of_the_prefill_layer():
     """Mixtral prefill, no drop: R = T k kept rows, every expert touched."""
     w = WORKLOADS["mixtral_prefill"]
