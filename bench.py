@@ -113,33 +113,23 @@ def whole_job_rate(tokens_per_step, steps, world, total_ms):
     return tokens_per_step * steps * world / (total_ms / 1e3)
 
 
-def power_capped(clk):
-    """Did the timed region run with its clocks pulled down (the clock record's own evidence:
-    median SM clock under load below 90 % of maximum)? A momentary sw_power_cap flag with the
-    median at the maximum does not count."""
-    if not clk or not clk.get("sm_mhz"):
-        return False
-    return clk["sm_mhz"] < 0.9 * (clk.get("sm_max_mhz") or clk["sm_mhz"])
+def tensor_peak(pk):
+    """bf16 denominator: the burst figure (cuBLAS timed alone). Every kernel here is timed
+    inside millisecond-scale steps, not inside a loop that runs for seconds, so the burst
+    figure applies; the clocks the run saw are reported beside it, not folded into it."""
+    return pk["bf16_tflops"], "bf16 burst"
 
 
-def tensor_peak(pk, clk):
-    """bf16 denominator: the sustained figure (the dense GEMM run back to back for seconds,
-    under the power cap) when the timed region itself ran power-capped, else the burst one."""
-    if power_capped(clk) and pk.get("bf16_tflops_sustained"):
-        return pk["bf16_tflops_sustained"], "bf16 sustained (clocks pulled down by the power cap)"
-    return pk["bf16_tflops"], "bf16 burst (clocks at maximum during the timed region)"
-
-
-def stage_roofline(flops, nbytes, ms, pk, clk=None):
-    """Achieved rate of one kernel against whichever roofline binds it; tensor-bound kernels
-    also carry their fraction of the burst peak."""
-    peak, _ = tensor_peak(pk, clk)
+def stage_roofline(flops, nbytes, ms, pk):
+    """Achieved rate of one kernel against whichever roofline binds it (burst bf16 peak or
+    HBM copy bandwidth, both measured)."""
+    peak, _ = tensor_peak(pk)
     t_tensor = flops / (peak * 1e12)
     t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
     if flops > 0 and t_tensor >= t_hbm:
         ach = flops / (ms / 1e3) / 1e12
         return dict(ms=ms, bound="tensor", achieved=ach, unit="TFLOP/s", peak=peak,
-                    frac=ach / peak, frac_burst=ach / pk["bf16_tflops"], algorithmic=flops)
+                    frac=ach / peak, algorithmic=flops)
     ach = nbytes / (ms / 1e3) / 1e9 if ms > 0 else 0.0
     return dict(ms=ms, bound="hbm", achieved=ach, unit="GB/s", peak=pk["hbm_gbs"],
                 frac=ach / pk["hbm_gbs"], algorithmic=nbytes)
@@ -177,6 +167,7 @@ class ClockSampler:
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
         self.rows = []
+        self.times = []                 # host clock (perf_counter) of each sample
         self.proc = None
         self.thread = None
 
@@ -197,6 +188,7 @@ class ClockSampler:
             parts = [p.strip() for p in line.split(",")]
             if len(parts) == 8:
                 self.rows.append(parts)
+                self.times.append(time.perf_counter())
 
     def stop(self):
         if self.proc is not None:
@@ -208,24 +200,28 @@ class ClockSampler:
         if self.thread is not None:
             self.thread.join(timeout=5)
 
-    def summary(self):
-        if not self.rows:
+    def summary(self, window=None):
+        """Clocks of the samples taken inside `window` = (t0, t1) on the host clock (widened
+        by one sampling period on each side, so that a timed region shorter than the period
+        still gets its nearest samples); all samples when there is no window."""
+        rows = self.rows
+        if window is not None and self.times:
+            t0, t1 = window[0] - 0.2, window[1] + 0.2
+            rows = [r for r, t in zip(self.rows, self.times) if t0 <= t <= t1]
+        if not rows:
             return dict(sm_mhz=None, sm_max_mhz=None, reasons=[], samples=0)
         def num(v):
             try:
                 return float(v)
             except ValueError:
                 return None
-        sm = [num(r[0]) for r in self.rows if num(r[0]) is not None]
-        mx = [num(r[1]) for r in self.rows if num(r[1]) is not None]
-        pw = [num(r[2]) for r in self.rows if num(r[2]) is not None]
+        sm = [num(r[0]) for r in rows if num(r[0]) is not None]
+        mx = [num(r[1]) for r in rows if num(r[1]) is not None]
+        pw = [num(r[2]) for r in rows if num(r[2]) is not None]
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        reasons = sorted({n for r in self.rows for n, v in zip(names, r[4:8]) if v == "Active"})
-        # the clock under load: samples drawing more than 300 W (clock and power of one row)
-        busy = [num(r[0]) for r in self.rows
-                if num(r[0]) is not None and num(r[2]) is not None and num(r[2]) > 300] or sm
-        return dict(sm_mhz=statistics.median(busy) if busy else None,
-                    sm_max_mhz=max(mx) if mx else None, reasons=reasons, samples=len(self.rows),
+        reasons = sorted({n for r in rows for n, v in zip(names, r[4:8]) if v == "Active"})
+        return dict(sm_mhz=statistics.median(sm) if sm else None,
+                    sm_max_mhz=max(mx) if mx else None, reasons=reasons, samples=len(rows),
                     power_w_max=max(pw) if pw else None)
 
 
@@ -277,6 +273,53 @@ def cpu_baseline(w, inp_host: dict, target_s: float = 15.0):
     return dict(value=n / t, unit=UNIT, cores=oracle_threads(), kind="oracle",
                 sample=f"first {n} tokens of {w.name} (full routing/dispatch/FFN/combine/losses of "
                        f"that batch, fp64 numpy), {t:.2f} s")
+
+
+def routing_report(w, ih: dict, gpu_idx: np.ndarray, y_gpu, C: int, fp8: bool = False,
+                   n_sample: int = 32, seed: int = 7):
+    """The routing comparison with the fp64 oracle on the whole batch (part of the CPU
+    baseline leg: the oracle runs on the host, outside every timed region).
+
+    near_ties: tokens whose k-th and (k+1)-th oracle logits differ by less than 1e-3;
+    routed_differently: tokens whose GPU expert set differs from the oracle's (allowed only
+    among near ties). On a seeded sample of tokens, y from the GPU is compared with the
+    oracle's output under (a) the oracle's own routing of the whole batch (the direct end to
+    end comparison: a routing flip also moves capacity drops of later tokens) and (b) the
+    GPU's routing decisions (the FFN and combine numerics alone)."""
+    import oracle as O
+    t0 = time.perf_counter()
+    logits = O.router_logits(ih["x"], ih["w_router"], ih["router_bias"])
+    o_idx = O.select_topk(logits, w.k)
+    ties = O.near_tie_tokens(logits, w.k)
+    diff = np.nonzero(np.any(np.sort(o_idx, 1) != np.sort(gpu_idx, 1), axis=1))[0]
+    rep = dict(eps=1e-3, tokens=w.T, near_ties=int(len(ties)),
+               routed_differently=int(len(diff)),
+               all_differences_among_near_ties=bool(set(diff.tolist()) <= set(ties.tolist())))
+    if not fp8:
+        tokens = np.sort(np.random.default_rng(seed).choice(w.T, size=min(n_sample, w.T),
+                                                            replace=False))
+        y = y_gpu[torch.as_tensor(tokens, device=y_gpu.device)].double().cpu().numpy()
+        ref = {}
+        for name, idx in (("oracle_routing", o_idx), ("gpu_routing", gpu_idx)):
+            inv = O.dispatch(idx, w.E, C)["inv"].reshape(w.T, w.k)[tokens]
+            g = O.gates(logits[tokens], idx[tokens], w.gate)
+            rows = np.zeros((len(tokens) * w.k, w.d))
+            for e in np.unique(idx[tokens]):
+                sel = (idx[tokens] == e) & (inv >= 0)
+                tl, sl = np.nonzero(sel)
+                if len(tl):
+                    rows[tl * w.k + sl] = O.swiglu_ffn(ih["x"][tokens[tl]], ih["w1"][e],
+                                                       ih["w3"][e], ih["w2"][e])
+            inv_l = np.where(inv >= 0, np.arange(len(tokens) * w.k).reshape(-1, w.k), -1)
+            shared = (O.swiglu_ffn(ih["x"][tokens], ih["w1s"], ih["w3s"], ih["w2s"])
+                      if ih.get("w1s") is not None else None)
+            ref[name] = O.combine(g, inv_l, rows, len(tokens), w.k, shared)
+        rl2 = lambda a, b: float(np.linalg.norm(a - b) / max(np.linalg.norm(b), 1e-300))
+        rep.update(sample_tokens=int(len(tokens)),
+                   rel_l2_direct=rl2(y, ref["oracle_routing"]),
+                   rel_l2_gpu_routing=rl2(y, ref["gpu_routing"]))
+    rep["host_seconds"] = round(time.perf_counter() - t0, 2)
+    return rep
 
 
 def oracle_train_sample(w, inp_host: dict, dy_host, n_tokens: int):
@@ -390,16 +433,24 @@ def run_ours(args, w, rank, world, local_rank):
         if i == 0:
             spread.append(float(layer.counts.max().item()) / (w.T * w.k / w.E))
     barrier()
-    # timed steps: one event before and one after each forward (stage events between the
-    # kernels would keep each launch from overlapping the previous kernel's tail)
+    # timed steps: one event before and one after each forward, and one pair around the
+    # dominant kernel (the gate/up GEMM) only; the other kernel boundaries carry no event, so
+    # each launch still overlaps the previous kernel's tail
+    ev_dom = [[None] * (len(STAGES) + 1) for _ in range(args.steps)]
+    j_dom = STAGES.index(DOMINANT)
+    for i in range(args.steps):
+        ev_dom[i][j_dom] = torch.cuda.Event(enable_timing=True)
+        ev_dom[i][j_dom + 1] = torch.cuda.Event(enable_timing=True)
     t_wall = time.perf_counter()
+    t_timed0 = t_wall
     for i in range(args.steps):
         flush.zero_()
         ev_step[i][0].record(stream)
-        layer.forward(x, y)
+        layer.forward(x, y, events=ev_dom[i])
         ev_step[i][1].record(stream)
     barrier()
-    t_wall = time.perf_counter() - t_wall
+    t_timed1 = time.perf_counter()
+    t_wall = t_timed1 - t_wall
     # the per-stage breakdown: the same steps again with an event at every stage boundary
     for i in range(args.steps):
         flush.zero_()
@@ -409,9 +460,15 @@ def run_ours(args, w, rank, world, local_rank):
     if err != 0:
         raise RuntimeError(f"device error {moe.moe_status_string(err)}")
     step_ms = [ev_step[i][0].elapsed_time(ev_step[i][1]) for i in range(args.steps)]
+    dom_ms = [ev_dom[i][j_dom].elapsed_time(ev_dom[i][j_dom + 1]) for i in range(args.steps)]
     stage_ms = {name: [evs[i][j].elapsed_time(evs[i][j + 1]) for i in range(args.steps)]
                 for j, name in enumerate(STAGES)}
     total_ms = sum(step_ms)
+    # for the routing report: the GPU's own top-k of the whole batch (the same routing
+    # kernels moe_forward runs), read back once, outside every timed region
+    gpu_idx = None
+    if w.gate != "expert_choice" and args.balance_gamma is None:
+        gpu_idx = layer.route(x).cpu().numpy().astype(np.int64)
 
     # end to end through the public API from pinned host memory: every step copies its own
     # x in and its y out; MoELayer.forward_host_stream overlaps those copies with the layer
@@ -447,30 +504,39 @@ def run_ours(args, w, rank, world, local_rank):
     tokens = w.T * args.steps * world
     value = whole_job_rate(w.T, args.steps, world, total_ms)
     ms_per_step = total_ms / args.steps
-    clk = sampler.summary()
-    tpeak, tpeak_name = tensor_peak(pk, clk)
+    clk = sampler.summary(window=(t_timed0, t_timed1))
+    tpeak, tpeak_name = tensor_peak(pk)
     stages = {}
     for name in STAGES:
         flops, nbytes = work["per_stage"][name]
-        stages[name] = stage_roofline(flops, nbytes, statistics.mean(stage_ms[name]), pk, clk)
+        stages[name] = stage_roofline(flops, nbytes, statistics.mean(stage_ms[name]), pk)
     roofline = None
     if w.dtype == "bf16":
-        dom = stages[DOMINANT]
+        # the dominant kernel as timed inside the timed steps themselves (its own event pair)
+        dom = stage_roofline(*work["per_stage"][DOMINANT], statistics.mean(dom_ms), pk)
         tr = traffic_from_profile(w.name, DOMINANT)
         roofline = dict(bound=dom["bound"], kernel=DOMINANT, achieved=dom["achieved"],
                         peak=dom["peak"], unit=dom["unit"], frac=dom["frac"], traffic=tr,
                         peak_source=f"{pk['source']} " + (
                             tpeak_name if dom["bound"] == "tensor" else "HBM copy"),
-                        frac_burst=dom.get("frac_burst"),
-                        algorithmic_per_launch=dom["algorithmic"])
+                        kernel_ms=dom["ms"], algorithmic_per_launch=dom["algorithmic"],
+                        timing="CUDA events around this kernel's launch inside the timed steps")
+        if clk.get("sm_mhz") and clk.get("sm_max_mhz"):
+            roofline["clock_note"] = (
+                f"median SM clock {clk['sm_mhz']:.0f} of {clk['sm_max_mhz']:.0f} MHz around the "
+                f"timed steps; at the maximum clock this kernel time would be "
+                f"{dom['ms'] * clk['sm_mhz'] / clk['sm_max_mhz']:.4f} ms")
     t_roof = max(work["flops"] / (tpeak * 1e12), work["bytes"] / (pk["hbm_gbs"] * 1e9))
     layer_roof = dict(flops=work["flops"], bytes=work["bytes"], roofline_ms=t_roof * 1e3,
                       measured_ms=ms_per_step, frac=t_roof * 1e3 / ms_per_step,
-                      note=f"max(FLOPs / {tpeak_name.split(' (')[0]} peak, bytes / HBM peak), "
-                           "measured peaks")
+                      note=f"max(FLOPs / {tpeak_name} peak, bytes / HBM peak), measured peaks")
     cpu = None
+    report = None
     if world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(w, host_inputs(inp), target_s=args.cpu_seconds)
+        ih = host_inputs(inp)
+        cpu = cpu_baseline(w, ih, target_s=args.cpu_seconds)
+        if gpu_idx is not None:
+            report = routing_report(w, ih, gpu_idx, y, C, fp8=args.fp8_weights)
     es = x.element_size()
     line = dict(
         metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
@@ -483,7 +549,7 @@ def run_ours(args, w, rank, world, local_rank):
                     kept_assignments=R, experts_touched=touched,
                     wall_s=t_wall),
         roofline=roofline, layer_roofline=layer_roof, stages=stages,
-        cpu_baseline=cpu,
+        cpu_baseline=cpu, routing_report=report,
         e2e=dict(value=whole_job_rate(w.T, args.steps, world, e2e_ms), unit=UNIT,
                  h2d_bytes_per_step=w.T * w.d * es,
                  d2h_bytes_per_step=w.T * w.d * es,
@@ -495,7 +561,9 @@ def run_ours(args, w, rank, world, local_rank):
         gpu_launches=(launches_per_forward(w) + (1 if args.balance_gamma is not None else 0))
         * args.steps,
         clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"], reasons=clk["reasons"],
-                    samples=clk["samples"]))
+                    samples=clk["samples"],
+                    window="nvidia-smi samples (every 200 ms) from 0.2 s before the timed steps "
+                           "to 0.2 s after them"))
     if args.balance_gamma is not None:
         line["balance"] = dict(gamma=args.balance_gamma, load_spread_first_step=spread[0],
                                load_spread_last_step=spread[-1],
@@ -601,6 +669,7 @@ def run_train(args, w, rank, world, local_rank):
         layer.forward(x, y)
         backward(x, dy)
     barrier()
+    t_timed0 = time.perf_counter()
     for i in range(args.steps):                 # timed: start and end events only
         flush.zero_()
         ev_step[i][0].record(stream)
@@ -608,6 +677,7 @@ def run_train(args, w, rank, world, local_rank):
         backward(x, dy)
         ev_step[i][1].record(stream)
     barrier()
+    t_timed1 = time.perf_counter()
     for i in range(args.steps):                 # per-stage breakdown
         flush.zero_()
         layer.forward(x, y, events=fevs[i])
@@ -661,10 +731,9 @@ def run_train(args, w, rank, world, local_rank):
     fw = algorithmic_work(w, R, touched)
     bw = backward_work(w, R, touched)
     tokens = w.T * args.steps * world
-    clk = sampler.summary()
-    tpeak, tpeak_name = tensor_peak(pk, clk)
-    stages = {name: stage_roofline(*bw["per_stage"][name], statistics.mean(bstage_ms[name]), pk,
-                                   clk)
+    clk = sampler.summary(window=(t_timed0, t_timed1))
+    tpeak, tpeak_name = tensor_peak(pk)
+    stages = {name: stage_roofline(*bw["per_stage"][name], statistics.mean(bstage_ms[name]), pk)
               for name in BWD_STAGES}
     dom = stages[BWD_DOMINANT]
     roofline = dict(bound=dom["bound"], kernel=BWD_DOMINANT, achieved=dom["achieved"],
@@ -672,7 +741,6 @@ def run_train(args, w, rank, world, local_rank):
                     traffic=traffic_from_profile(w.name + "+train", BWD_DOMINANT),
                     peak_source=f"{pk['source']} " + (
                         tpeak_name if dom["bound"] == "tensor" else "HBM copy"),
-                    frac_burst=dom.get("frac_burst"),
                     algorithmic_per_step=dom["algorithmic"],
                     note="gemm_wgrad = all weight-gradient GEMM launches of one backward")
     flops = fw["flops"] + bw["flops"]
@@ -709,8 +777,8 @@ def run_train(args, w, rank, world, local_rank):
         roofline=roofline,
         layer_roofline=dict(flops=flops, bytes=nbytes, roofline_ms=t_roof * 1e3,
                             measured_ms=ms_per_step, frac=t_roof * 1e3 / ms_per_step,
-                            note=f"max(FLOPs / {tpeak_name.split(' (')[0]} peak, bytes / HBM "
-                                 "peak), measured peaks"),
+                            note=f"max(FLOPs / {tpeak_name} peak, bytes / HBM peak), "
+                                 "measured peaks"),
         stages=stages, cpu_baseline=cpu,
         e2e=dict(value=whole_job_rate(w.T, args.steps, world, e2e_ms), unit=UNIT,
                  h2d_bytes_per_step=2 * w.T * w.d * es,

@@ -170,7 +170,13 @@ int moe_aux_loss(const moe_shape* s, const float* stats, const int32_t* counts,
 /* The whole layer: steps 1-6 on one stream, no host synchronisation.
  *   x [T, d], w_router [E, d], router_bias [E] or NULL, w1/w3/w2 as above,
  *   w1s/w3s/w2s or NULL (required iff d_ff_shared > 0), y [T, d] out,
- *   counts [E] / dropped [1] / losses [2] out, each may be NULL. */
+ *   counts [E] / dropped [1] / losses [2] out, each may be NULL.
+ * MOE_OK means every kernel was queued, not that the outputs are valid: a fault found on the
+ * device (non-finite logits, an out-of-range index, a pipeline wait that ran past its 2 s
+ * limit) is recorded in the workspace's sticky error word and the kernels carry on, so y,
+ * counts and losses are then meaningless. Check moe_get_error(ws) after synchronising before
+ * using the outputs of a call that may have failed; the word stays set until
+ * moe_clear_error. */
 int moe_forward(const moe_shape* s, const void* x, const void* w_router,
                 const float* router_bias, const void* w1, const void* w3, const void* w2,
                 const void* w1s, const void* w3s, const void* w2s, void* y,
@@ -233,7 +239,10 @@ int moe_host_pipeline_destroy(moe_host_pipeline* p);
  * stream before stage i and events[MOE_NUM_STAGES] after the last one, so that each
  * stage's device time can be read with cudaEventElapsedTime. Stages: 0 router GEMM,
  * 1 gates + top-k, 2 dispatch, 3 gather, 4 gate/up GEMM + SwiGLU, 5 down GEMM + gate
- * scale, 6 combine, 7 balance losses. n_events must be MOE_NUM_STAGES + 1. */
+ * scale, 6 combine, 7 balance losses. n_events must be MOE_NUM_STAGES + 1. A NULL entry
+ * records nothing at that boundary, so the kernels on either side of it still overlap (each
+ * kernel's launch and set-up start during the previous one's tail); an event between two
+ * kernels serialises them. */
 int moe_forward_events(const moe_shape* s, const void* x, const void* w_router,
                        const float* router_bias, const void* w1, const void* w3,
                        const void* w2, const void* w1s, const void* w3s, const void* w2s,
@@ -395,6 +404,10 @@ int moe_backward(const moe_shape* s, const void* x, const void* w_router, const 
  *     with that device current); make that first call before any stream capture.
  *   - Device-side error reporting needs a workspace, so this variant does not flag
  *     non-finite logits (moe_route_topk does).
+ *   - Errors found on the host, before anything is queued: MOE_ERR_INVALID for a NULL
+ *     logits_in / topk_idx / topk_gate (T > 0) or any pointer not 4-byte aligned;
+ *     MOE_ERR_UNSUPPORTED for expert-choice layers (they route with moe_expert_choice) and
+ *     for sizes beyond the scratch.
  * Pointers are device pointers; asynchronous on `stream`. */
 int moe_route_topk_noalloc(const moe_shape* s, const float* logits_in, int32_t* topk_idx,
                            float* topk_gate, float* stats, void* stream);

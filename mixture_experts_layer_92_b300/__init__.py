@@ -85,6 +85,16 @@ class MoELayer:
                     dropped=self.dropped, losses=self.losses, stream=stream, events=events)
         return y
 
+    def route(self, x: torch.Tensor) -> torch.Tensor:
+        """Top-k expert indices [T, k] int32 of device x: moe_route_topk with this layer's
+        router (selection on the logits alone, without a balancing bias)."""
+        T = x.shape[0]
+        idx = torch.empty(T, self.k, dtype=torch.int32, device=self.device)
+        gate = torch.empty(T, self.k, dtype=torch.float32, device=self.device)
+        moe_route_topk(self.shape(T), self.ws, idx, gate, x=x, w_router=self.w["w_router"],
+                       router_bias=self.w["router_bias"])
+        return idx
+
     def forward_host_stream(self, x_hosts, y_hosts, losses_hosts=None):
         """End-to-end layer over a sequence of host batches (pinned memory), pipelined.
 

@@ -228,10 +228,7 @@ def moe_forward(s, ws, x, w_router, w1, w3, w2, y, router_bias=None, w1s=None, w
                                _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(y), _p(counts), _p(dropped),
                                _p(losses), _p(ws), ws.numel(), _stream(stream)), "moe_forward")
         return
-    for e in events:
-        if e.cuda_event == 0:          # torch creates the CUDA event on first record
-            e.record()
-    arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    arr = _event_array(events)
     _check(LIB.moe_forward_events(ctypes.byref(s), _p(x), _p(w_router), _p(router_bias), _p(w1),
                                   _p(w3), _p(w2), _p(w1s), _p(w3s), _p(w2s), _p(y), _p(counts),
                                   _p(dropped), _p(losses), _p(ws), ws.numel(), _stream(stream),
@@ -286,10 +283,12 @@ def moe_update_select_bias(s, counts, select_bias, gamma, stream=None):
 
 
 def _event_array(events):
+    """cudaEvent_t handles of torch events; None stays NULL (no event at that boundary)."""
     for e in events:
-        if e.cuda_event == 0:          # torch creates the CUDA event on first record
+        if e is not None and e.cuda_event == 0:   # torch creates the CUDA event on first record
             e.record()
-    return (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+    return (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(None if e is None else e.cuda_event)
+                                            for e in events])
 
 
 def moe_forward_balanced(s, ws, x, w_router, w1, w3, w2, y, select_bias, gamma, router_bias=None,

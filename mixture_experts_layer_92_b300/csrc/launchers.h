@@ -214,7 +214,7 @@ struct RouteArgs {
   int T, E, k, gate_mode;   // k = 0: no selection (probabilities and statistics only)
   int32_t* topk_idx;        // [T][k]
   float* topk_gate;         // [T][k]
-  float* partials;          // [route_blocks(T)][E + 1]
+  float* partials;          // [E + 1][route_blocks(T)], expert-major
   DeviceError* err;         // nullptr: no device error reporting
 };
 int launch_route_topk(const RouteArgs& a, cudaStream_t stream);

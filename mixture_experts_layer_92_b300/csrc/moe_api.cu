@@ -309,7 +309,7 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
   const int max_group_rows = std::min(s->T, s->capacity);
 
   auto rec = [&](int i) {
-    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+    if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
   };
 
   // stage 3: gather
@@ -509,9 +509,6 @@ int check_forward(const moe_shape* s, const void* x, const void* w_router, const
   if (q != nullptr) TRY(check_fp8(s, q));
   if (ev != nullptr && n_ev != MOE_NUM_STAGES + 1)
     return fail(MOE_ERR_INVALID, "n_events = %d, expected %d", n_ev, MOE_NUM_STAGES + 1);
-  if (ev != nullptr)
-    for (int i = 0; i < n_ev; ++i)
-      if (ev[i] == nullptr) return fail(MOE_ERR_INVALID, "events[%d] is NULL", i);
   if (s->T > 0) {
     REQUIRE_PTR(x, "x");
     REQUIRE_PTR(w_router, "w_router");
@@ -559,7 +556,7 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   void* yp = at<void>(ws, L.yp);
   void* ys = s->d_ff_shared > 0 ? at<void>(ws, L.ys) : nullptr;
   auto rec = [&](int i) {
-    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+    if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
   };
 
   const bool ec = expert_choice(s);
@@ -777,9 +774,6 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
     return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu", ws_bytes, B.total);
   if (ev != nullptr && n_ev != MOE_NUM_BWD_STAGES + 1)
     return fail(MOE_ERR_INVALID, "n_events = %d, expected %d", n_ev, MOE_NUM_BWD_STAGES + 1);
-  if (ev != nullptr)
-    for (int i = 0; i < n_ev; ++i)
-      if (ev[i] == nullptr) return fail(MOE_ERR_INVALID, "events[%d] is NULL", i);
   const bool shared = s->d_ff_shared > 0;
   REQUIRE_PTR(dw_router, "dw_router");
   REQUIRE_PTR(dw1, "dw1");
@@ -810,7 +804,7 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
   }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   auto rec = [&](int i) {
-    if (ev) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+    if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
   };
   const size_t T = s->T, E = s->E, d = s->d, F = s->d_ff, Fs = s->d_ff_shared;
   const bool ec = expert_choice(s);

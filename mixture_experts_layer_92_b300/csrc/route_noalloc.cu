@@ -11,6 +11,7 @@
 // the same array. Calls that overlap on the GPU (for instance on two streams at once) race
 // on it; serialise them. The kernels write every partial before reading it, so nothing has
 // to be cleared between calls.
+#include <cstdint>
 #include <cstdio>
 #include <mutex>
 
@@ -20,8 +21,9 @@
 namespace moe {
 namespace {
 
-// 2 MiB: partials of route_blocks(T) blocks x (E + 1) floats. Enough for any T when
-// E <= 884 (at most 592 blocks), and for larger E while T is small enough.
+// 2 MiB: partials of (E + 1) x route_blocks(T) floats (expert-major: the statistics of
+// expert e for every block, then expert e + 1). Enough for any T when E <= 884 (at most 592
+// blocks), and for larger E while T is small enough.
 constexpr size_t kNoAllocScratchBytes = 2u << 20;
 
 static __device__ __align__(256) float g_route_scratch[kNoAllocScratchBytes / sizeof(float)];
@@ -57,14 +59,26 @@ extern "C" int moe_route_topk_noalloc(const moe_shape* s, const float* logits_in
   using namespace moe;
   const int rc = moe_check_shape(s);
   if (rc != MOE_OK) return rc;
+  if (s->gate == MOE_GATE_EXPERT_CHOICE)
+    return set_error_detail(MOE_ERR_UNSUPPORTED,
+                            "expert-choice layers route with moe_expert_choice");
+  // every pointer is checked before anything is queued, as the workspace entry points do
+  auto misaligned4 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 3u) != 0; };
+  if (stats != nullptr && misaligned4(stats))
+    return set_error_detail(MOE_ERR_INVALID, "stats is not 4-byte aligned");
+  if (s->T > 0) {
+    if (logits_in == nullptr || topk_idx == nullptr || topk_gate == nullptr)
+      return set_error_detail(MOE_ERR_INVALID, "logits_in, topk_idx and topk_gate are required");
+    if (misaligned4(logits_in) || misaligned4(topk_idx) || misaligned4(topk_gate))
+      return set_error_detail(MOE_ERR_INVALID,
+                              "logits_in, topk_idx and topk_gate must be 4-byte aligned");
+  }
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   if (s->T == 0) {
     if (stats != nullptr && cudaMemsetAsync(stats, 0, (s->E + 1) * sizeof(float), st) != cudaSuccess)
       return MOE_ERR_CUDA;
     return MOE_OK;
   }
-  if (logits_in == nullptr || topk_idx == nullptr || topk_gate == nullptr)
-    return set_error_detail(MOE_ERR_INVALID, "logits_in, topk_idx and topk_gate are required");
   const size_t need = static_cast<size_t>(route_blocks(s->T)) * (s->E + 1) * sizeof(float);
   if (need > kNoAllocScratchBytes) {
     char msg[160];

@@ -13,7 +13,7 @@ Every step is the plain definition, written in the order the pages give it. The 
 * [Starphix] "Mixture of Experts (MoE)" (learn.starphix.com): "Key Equations",
   "Shared + Specialized".
 
-Readings where the pages are silent or disagree (also listed in the design doc):
+Readings where the pages are silent or disagree:
 
 * selection compares raw logits, descending, the lower expert index winning ties;
 * gates: softmax over all E ("softmax_all"), softmax over the k selected logits

@@ -212,3 +212,25 @@ def test_selftest_rejects_bad_workspace_before_any_launch():
     assert L.moe_selftest_wait_timeout(None, 4096, None) == -4
     assert L.moe_selftest_wait_timeout(ctypes.c_void_p(0x7f0000000008), 4096, None) == -4  # misaligned
     assert L.moe_selftest_wait_timeout(ctypes.c_void_p(0x7f0000000000), 8, None) == -4      # too small
+
+
+def test_noalloc_rejects_before_any_launch():
+    """moe_route_topk_noalloc checks its pointers and the gate mode on the host, like the
+    workspace entry points: a misaligned pointer or an expert-choice layer is refused before
+    any CUDA call (so this runs without a GPU)."""
+    L = _lib.LIB
+    s = shape()
+    fake = ctypes.c_void_p(0x7f0000000000)          # never dereferenced
+    odd = ctypes.c_void_p(0x7f0000000002)
+    null = ctypes.c_void_p(None)
+    call = lambda l, i, g, st, sh=s: L.moe_route_topk_noalloc(ctypes.byref(sh), l, i, g, st, null)
+    assert call(null, fake, fake, null) == -1       # no logits
+    assert call(odd, fake, fake, null) == -1        # misaligned logits
+    assert call(fake, odd, fake, null) == -1        # misaligned indices
+    assert call(fake, fake, odd, null) == -1        # misaligned gates
+    assert call(fake, fake, fake, odd) == -1        # misaligned statistics
+    assert "aligned" in _lib.LIB.moe_last_error_detail().decode()
+    ec = shape(gate=3, capacity=16)
+    assert call(fake, fake, fake, null, ec) == -2   # expert choice has no top-k step
+    empty = shape(T=0)
+    assert call(null, null, null, odd, empty) == -1  # checked even for an empty batch

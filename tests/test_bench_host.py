@@ -1,5 +1,5 @@
-"""Host logic of bench.py (no GPU): the roofline denominators chosen from the clock record,
-the per-kernel roofline classification, and the algorithmic work of the headline workload
+"""Host logic of bench.py (no GPU): the roofline denominators, the clock record of the timed
+steps, the per-kernel roofline classification, and the algorithmic work of the headline workload
 against its closed forms."""
 import math
 
@@ -11,36 +11,20 @@ from moe_inputs import WORKLOADS
 PK = dict(hbm_gbs=6000.0, bf16_tflops=1800.0, bf16_tflops_sustained=1400.0, source="test")
 
 
-@pytest.mark.parametrize("clk,capped", [
-    (dict(sm_mhz=1300.0, sm_max_mhz=2032.0, reasons=["sw_power_cap"]), True),
-    (dict(sm_mhz=1800.0, sm_max_mhz=2032.0, reasons=[]), True),          # below 90 % of max
-    (dict(sm_mhz=2032.0, sm_max_mhz=2032.0, reasons=["sw_power_cap"]), False),  # a momentary flag
-    (dict(sm_mhz=1900.0, sm_max_mhz=2032.0, reasons=[]), False),
-    (dict(sm_mhz=None, sm_max_mhz=None, reasons=[]), False),
-    (None, False),
-])
-def test_power_capped(clk, capped):
-    assert bench.power_capped(clk) is capped
-
-
-def test_tensor_peak_follows_the_clock_record():
-    peak, name = bench.tensor_peak(PK, dict(sm_mhz=1200.0, sm_max_mhz=2032.0, reasons=[]))
-    assert peak == 1400.0 and "sustained" in name
-    peak, name = bench.tensor_peak(PK, dict(sm_mhz=2032.0, sm_max_mhz=2032.0, reasons=[]))
+def test_tensor_peak_is_the_burst_figure():
+    # every kernel is timed inside millisecond-scale steps: the burst peak applies
+    peak, name = bench.tensor_peak(PK)
     assert peak == 1800.0 and "burst" in name
-    no_sustained = dict(PK, bf16_tflops_sustained=None)
-    assert bench.tensor_peak(no_sustained, dict(sm_mhz=1200.0, sm_max_mhz=2032.0))[0] == 1800.0
 
 
 def test_stage_roofline_binds_the_slower_roof():
-    capped = dict(sm_mhz=1200.0, sm_max_mhz=2032.0, reasons=[])
-    # 1.4e12 FLOP and 6e9 bytes: 1.0 ms at the sustained tensor peak, 1.0 ms at HBM -> tensor
-    r = bench.stage_roofline(1.4e12, 6e9, 2.0, PK, capped)
+    # 1.8e12 FLOP and 6e9 bytes: 1.0 ms at the burst tensor peak, 1.0 ms at HBM -> tensor
+    r = bench.stage_roofline(1.8e12, 6e9, 2.0, PK)
     assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s"
-    assert r["achieved"] == pytest.approx(700.0)
-    assert r["frac"] == pytest.approx(0.5) and r["frac_burst"] == pytest.approx(700.0 / 1800.0)
+    assert r["achieved"] == pytest.approx(900.0)
+    assert r["frac"] == pytest.approx(0.5) and r["peak"] == 1800.0
     # bandwidth work only
-    r = bench.stage_roofline(0.0, 6e9, 2.0, PK, capped)
+    r = bench.stage_roofline(0.0, 6e9, 2.0, PK)
     assert r["bound"] == "hbm" and r["achieved"] == pytest.approx(3000.0)
     assert r["frac"] == pytest.approx(0.5)
 
@@ -62,24 +46,30 @@ def _row(sm, mx, pw, cap="Not Active", hw="Not Active"):
     return [str(sm), str(mx), str(pw), "0x0", hw, "Not Active", "Not Active", cap]
 
 
-def test_clock_summary_takes_the_median_under_load():
+def test_clock_summary_takes_the_samples_around_the_timed_steps():
     c = bench.ClockSampler(0)
     c.rows = [_row(2032, 2032, 120), _row(1300, 2032, 1050, cap="Active"),
-              _row("[N/A]", 2032, 900), _row(1400, 2032, 1000), _row(1350, 2032, 1090)]
-    s = c.summary()
-    # rows above 300 W with a readable clock: 1300, 1400, 1350 (the idle 2032 MHz sample and
-    # the unreadable one are left out, without shifting the clock/power pairing)
+              _row("[N/A]", 2032, 900), _row(1400, 2032, 1000), _row(1350, 2032, 1090),
+              _row(2032, 2032, 150)]
+    c.times = [0.0, 10.0, 10.2, 10.4, 10.6, 20.0]
+    # the window 10.1 .. 10.5 s, widened by 0.2 s on each side: the samples at 10.0 .. 10.6
+    s = c.summary(window=(10.1, 10.5))
     assert s["sm_mhz"] == 1350.0 and s["sm_max_mhz"] == 2032.0
-    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 5
+    assert s["reasons"] == ["sw_power_cap"] and s["samples"] == 4
     assert s["power_w_max"] == 1090.0
+    # a window with no sample in reach has no clock record
+    assert c.summary(window=(15.0, 15.1))["samples"] == 0
+    # no window: every sample
+    assert c.summary()["samples"] == 6
 
 
 def test_clock_summary_reports_slowdowns_and_empty_records():
     c = bench.ClockSampler(0)
     c.rows = [_row(1000, 2032, 200, hw="Active")]
+    c.times = [1.0]
     s = c.summary()
     assert s["sm_mhz"] == 1000.0 and s["reasons"] == ["hw_slowdown"]
-    c.rows = []
+    c.rows, c.times = [], []
     assert bench.ClockSampler.summary(c) == dict(sm_mhz=None, sm_max_mhz=None, reasons=[],
                                                   samples=0)
 
@@ -140,3 +130,29 @@ def test_algorithmic_work_of_8bit_weights_counts_codes_and_scales():
     weights16 = 3 * E * w.d * w.d_ff * 2
     weights8 = 3 * E * w.d * w.d_ff + E * (2 * w.d_ff + w.d) * 4
     assert b16 - b8 == pytest.approx(weights16 - weights8)
+
+
+def test_routing_report_on_the_oracle_itself():
+    """The bench's routing report (run in its CPU-baseline leg) on a small drop workload,
+    fed the oracle's own routing and outputs: no difference, both rel L2 near 0; then one
+    token's expert set changed by hand is counted."""
+    import numpy as np
+    import torch
+    import oracle as O
+    from moe_inputs import make_inputs
+    w = WORKLOADS["tiny_fp32"]
+    inp = make_inputs(w, device="cpu")
+    ih = bench.host_inputs(inp)
+    C = O.capacity(w.cf, w.T, w.k, w.E)
+    ref = O.forward(ih["x"], ih["w_router"], ih["w1"], ih["w3"], ih["w2"], k=w.k, mode=w.gate,
+                    C=C, alpha=w.alpha, beta=w.beta)
+    y = torch.from_numpy(ref["y"])
+    rep = bench.routing_report(w, ih, ref["idx"].copy(), y, C)
+    assert rep["routed_differently"] == 0 and rep["all_differences_among_near_ties"]
+    assert rep["rel_l2_direct"] < 1e-6 and rep["rel_l2_gpu_routing"] < 1e-6
+    assert rep["near_ties"] == len(O.near_tie_tokens(ref["logits"], w.k))
+    idx = ref["idx"].copy()
+    t = 5
+    idx[t] = [e for e in range(w.E) if e not in idx[t]][:w.k]
+    rep = bench.routing_report(w, ih, idx, y, C)
+    assert rep["routed_differently"] == 1

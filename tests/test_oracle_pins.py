@@ -433,6 +433,24 @@ def test_expert_choice_everyone_chosen_with_identical_experts_is_the_dense_ffn()
     assert out["ec"]["unrouted"] == 0
 
 
+@pytest.mark.parametrize("T,E,C,k", [(12, 4, 5, 1), (12, 4, 12, 1), (7, 3, 20, 1), (9, 5, 0, 1),
+                                     (16, 8, 3, 2), (10, 6, 4, 3), (1, 2, 1, 1)])
+def test_expert_choice_balance_loss_closed_form(T, E, C, k):
+    """Expert choice ([Starphix] "Router Variants") gives every expert exactly C' = min(C, T)
+    rows, so f_i = C'/(T*k) for every i, and the all-E softmax makes sum_i P_i = 1: the
+    balance loss alpha*E*sum_i f_i*P_i is alpha*E*C'/(T*k), whatever the logits. A
+    normalisation by T instead of T*k, a dropped factor E, or f taken from the tokens
+    instead of the rows each move it off this value."""
+    rng = np.random.default_rng(T * 100 + E * 10 + C + k)
+    d, F, alpha = 5, 6, 0.01
+    x = rng.normal(size=(T, d))
+    W1, W3 = rng.normal(size=(E, F, d)), rng.normal(size=(E, F, d))
+    W2 = rng.normal(size=(E, d, F))
+    out = O.expert_choice_forward(x, rng.normal(size=(E, d)) * 3, W1, W3, W2, C=C, k=k,
+                                  alpha=alpha)
+    assert out["l_aux"] == pytest.approx(alpha * E * min(C, T) / (T * k), rel=1e-12, abs=0)
+
+
 # ---------------------------------------------------------------- 8-bit expert weights
 def test_e4m3_decode_closed_forms():
     """Bit patterns of the E4M3 format: 1.0, 1.5, 2.0, the largest 448, the smallest normal

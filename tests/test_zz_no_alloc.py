@@ -48,6 +48,37 @@ def test_noalloc_matches_workspace_entry_on_consecutive_calls():
     both(random_logits(16384, 128, seed=3), 1, "softmax_all")
 
 
+def test_noalloc_at_the_edge_of_its_scratch():
+    # route_blocks(T) = min(ceil(T / 8), 592) blocks of (E + 1) partial sums, 4 bytes each:
+    # E = 884 at 592 blocks fills the 2 MiB to within 1.2 KB, and E = 1024 fits while T
+    # keeps the block count at 511 or below
+    both(random_logits(4736, 884, seed=4), 4, "softmax_topk")
+    both(random_logits(4000, 1024, seed=5), 2, "sigmoid_topk")
+
+
+def test_noalloc_rejects_one_expert_past_the_edge():
+    T, E, k = 4736, 885, 2                        # 592 * 886 * 4 bytes > 2 MiB
+    s = L.make_shape(T, 16, E, k, 16, dtype=torch.float32)
+    l = torch.zeros(T, E, device=DEV)
+    idx = torch.empty(T, k, dtype=torch.int32, device=DEV)
+    gate = torch.empty(T, k, device=DEV)
+    with pytest.raises(L.MoeError) as ei:
+        L.moe_route_topk_noalloc(s, l, idx, gate)
+    assert ei.value.status == -2 and "scratch" in str(ei.value)
+
+
+def test_noalloc_refuses_expert_choice_layers():
+    # expert-choice layers have no top-k step; the workspace entry point refuses them too
+    T, E = 64, 8
+    s = L.make_shape(T, 16, E, 1, 16, gate="expert_choice", capacity=16, dtype=torch.float32)
+    l = torch.zeros(T, E, device=DEV)
+    idx = torch.empty(T, 1, dtype=torch.int32, device=DEV)
+    gate = torch.empty(T, 1, device=DEV)
+    with pytest.raises(L.MoeError) as ei:
+        L.moe_route_topk_noalloc(s, l, idx, gate)
+    assert ei.value.status == -2
+
+
 def test_noalloc_rejects_sizes_beyond_its_scratch():
     T, E, k = 8192, 1024, 2                       # needs 1024 * 1025 * 4 bytes > 2 MiB
     s = L.make_shape(T, 16, E, k, 16, dtype=torch.float32)
