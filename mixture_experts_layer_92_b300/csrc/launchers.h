@@ -218,6 +218,19 @@ struct RouteArgs {
   DeviceError* err;         // nullptr: no device error reporting
 };
 int launch_route_topk(const RouteArgs& a, cudaStream_t stream);
+// The fused router (router_fused.cu): logits of bf16 x [T, d] and w_router [E, d] (E <= 256)
+// on the tensor cores, split along d over the CTAs of a cluster, reduced on chip in a fixed
+// order, then the routing step of launch_route_topk on them (r.logits and r.nsplit unused).
+// Writes `grid` per-CTA statistic partials: r.partials [E + 1][grid].
+struct RouterFusedPlan {
+  int cs;       // CTAs per cluster (split of d), 1..8
+  int kb_per;   // 64-wide k-blocks per CTA
+  int stages;   // ring depth
+  int grid;     // CTAs: ceil(T / 128) * cs
+};
+RouterFusedPlan router_fused_plan(int T, int d, int E);
+int launch_router_fused(const RouterFusedPlan& plan, const void* x, const void* w_router,
+                        const RouteArgs& r, int d, cudaStream_t stream);
 int launch_update_select_bias(const int32_t* counts, float* select_bias, int T, int E, int k,
                               float gamma, cudaStream_t stream);
 int launch_stats_reduce(const float* partials, int nblocks, int E, float* stats,

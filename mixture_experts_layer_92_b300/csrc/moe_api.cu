@@ -62,6 +62,22 @@ RouterSplit router_split(const moe_shape* s) {
 
 bool expert_choice(const moe_shape* s) { return s->gate == MOE_GATE_EXPERT_CHOICE; }
 
+// bf16 layers with E <= 256 route from x with the fused router (router_fused.cu: logits on
+// chip, split-K partials reduced in a cluster); others run the router GEMM into split-K logit
+// planes and the top-k kernel on them.
+bool fused_router(const moe_shape* s) {
+  return s->dtype == MOE_BF16 && s->E <= 256 && s->T > 0;
+}
+
+// Per-block statistic partials the routing step writes from x (fused router: one per CTA),
+// and the most any routing call writes (the workspace holds that many).
+int route_partials_from_x(const moe_shape* s) {
+  return fused_router(s) ? router_fused_plan(s->T, s->d, s->E).grid : route_blocks(s->T);
+}
+int route_partial_blocks(const moe_shape* s) {
+  return std::max(route_blocks(s->T), route_partials_from_x(s));
+}
+
 // Rows of the permuted activations: T*k assignments, or E*min(C, T) for expert choice.
 size_t perm_rows(const moe_shape* s) {
   if (expert_choice(s))
@@ -92,7 +108,7 @@ Layout layout(const moe_shape* s) {
   L.logits = take(static_cast<size_t>(router_split(s).splits) * T * E * 4);
   L.idx = take(A * 4);
   L.gate = take(std::max(A, R) * 4);
-  L.partials = take(static_cast<size_t>(route_blocks(s->T)) * (E + 1) * 4);
+  L.partials = take(static_cast<size_t>(route_partial_blocks(s)) * (E + 1) * 4);
   L.stats = take((E + 1) * 4);
   L.counts = take(E * 4);
   L.offsets = take((E + 1) * 4);
@@ -265,6 +281,31 @@ RouteArgs route_args(const moe_shape* s, const float* logits, int nsplit, const 
   a.partials = partials;
   a.err = err;
   return a;
+}
+
+// Steps 1-2 from x: the logits, then the routing step `ra` (its logits / nsplit fields are
+// set here). Records `ev_mid` (if any) between the logits and the routing step: with the
+// fused router both are one kernel, so the event follows it. Writes
+// route_partials_from_x(s) statistic partials.
+int route_from_x(const moe_shape* s, const void* x, const void* wr, RouteArgs ra, float* planes,
+                 DeviceError* err, cudaStream_t st, cudaEvent_t ev_mid = nullptr) {
+  if (s->T == 0) {
+    if (ev_mid) cudaEventRecord(ev_mid, st);
+    return MOE_OK;
+  }
+  if (fused_router(s)) {
+    LAUNCH(launch_router_fused(router_fused_plan(s->T, s->d, s->E), x, wr, ra, s->d, st),
+           "router with fused gates/top-k");
+    if (ev_mid) cudaEventRecord(ev_mid, st);
+    return MOE_OK;
+  }
+  TRY(run_router(s, x, wr, planes, err, st));
+  if (ev_mid) cudaEventRecord(ev_mid, st);
+  ra.logits = planes;
+  ra.nsplit = router_split(s).splits;
+  ra.split_stride = static_cast<size_t>(s->T) * s->E;
+  LAUNCH(launch_route_topk(ra, st), "gates/top-k");
+  return MOE_OK;
 }
 
 // ---------------------------------------------------------------- stages 4-5: expert GEMMs
@@ -563,16 +604,15 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
   if (ec && select_bias != nullptr)
     return fail(MOE_ERR_UNSUPPORTED, "selection bias applies to top-k routing only");
   rec(0);
-  TRY(run_router(s, x, w_router, logits, err, st));
-  rec(1);
-  if (s->T > 0) {
-    RouteArgs ra = route_args(s, logits, router_split(s).splits, router_bias, nullptr, idx, gate,
-                              partials, err, select_bias);
+  {
+    RouteArgs ra = route_args(s, nullptr, 1, router_bias, nullptr, idx, gate, partials, err,
+                              select_bias);
     if (ec) {
       ra.k = 0;  // probabilities and statistics only; the experts choose below
       ra.probs_t = at<float>(ws, L.probs);
     }
-    LAUNCH(launch_route_topk(ra, st), "gates/top-k");
+    TRY(route_from_x(s, x, w_router, ra, logits, err, st,
+                     ev ? static_cast<cudaEvent_t>(ev[1]) : nullptr));
   }
   rec(2);
   if (ec) {
@@ -597,7 +637,7 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
          "combine");
   rec(7);
   if (s->T > 0) {
-    LAUNCH(launch_stats_loss(partials, route_blocks(s->T), s->E, stats, cnt, s->T, s->k, s->alpha,
+    LAUNCH(launch_stats_loss(partials, route_partials_from_x(s), s->E, stats, cnt, s->T, s->k, s->alpha,
                              s->beta, los, err, st),
            "router statistics and losses");
   } else {
@@ -674,13 +714,13 @@ int route_impl(const moe_shape* s, const void* x, const void* w_router, const fl
     return ok();
   }
   float* partials = at<float>(ws, L.partials);
+  int nb = route_blocks(s->T);
   if (logits_in == nullptr) {
-    float* planes = at<float>(ws, L.logits);
-    TRY(run_router(s, x, w_router, planes, err, st));
-    LAUNCH(launch_route_topk(route_args(s, planes, router_split(s).splits, router_bias, logits_out,
-                                        topk_idx, topk_gate, partials, err, select_bias),
-                             st),
-           "gates/top-k");
+    TRY(route_from_x(s, x, w_router,
+                     route_args(s, nullptr, 1, router_bias, logits_out, topk_idx, topk_gate,
+                                partials, err, select_bias),
+                     at<float>(ws, L.logits), err, st));
+    nb = route_partials_from_x(s);
   } else {
     LAUNCH(launch_route_topk(route_args(s, logits_in, 1, nullptr,
                                         logits_out == logits_in ? nullptr : logits_out, topk_idx,
@@ -688,7 +728,7 @@ int route_impl(const moe_shape* s, const void* x, const void* w_router, const fl
                              st),
            "gates/top-k");
   }
-  if (stats) LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
+  if (stats) LAUNCH(launch_stats_reduce(partials, nb, s->E, stats, st), "stats reduce");
   return ok();
 }
 
@@ -859,15 +899,14 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
   // 1. recompute the routing: logits (with bias), top-k, gates, dispatch -- or the experts'
   //    choices and their gates
   rec(0);
-  TRY(run_router(s, x, w_router, at<float>(ws, L.logits), err, st));
   {
-    RouteArgs ra = route_args(s, at<float>(ws, L.logits), router_split(s).splits, router_bias,
-                              logits, idx, gate, at<float>(ws, L.partials), err);
+    RouteArgs ra = route_args(s, nullptr, 1, router_bias, logits, idx, gate,
+                              at<float>(ws, L.partials), err);
     if (ec) {
       ra.k = 0;  // logits and probabilities only
       ra.probs_t = at<float>(ws, L.probs);
     }
-    LAUNCH(launch_route_topk(ra, st), "gates/top-k");
+    TRY(route_from_x(s, x, w_router, ra, at<float>(ws, L.logits), err, st));
   }
   if (ec) {
     LAUNCH(launch_expert_choice(at<float>(ws, L.probs), s->T, s->E, s->capacity, perm, gate, inv,
@@ -1216,16 +1255,22 @@ int moe_expert_choice(const moe_shape* s, const void* x, const void* w_router,
   DeviceError* err = at<DeviceError>(ws, L.err);
   float* partials = at<float>(ws, L.partials);
   if (s->T > 0) {
-    RouteArgs ra = (logits_in == nullptr)
-                       ? route_args(s, at<float>(ws, L.logits), router_split(s).splits,
-                                    router_bias, nullptr, nullptr, nullptr, partials, err)
-                       : route_args(s, logits_in, 1, nullptr, nullptr, nullptr, nullptr, partials,
-                                    err);
-    if (logits_in == nullptr) TRY(run_router(s, x, w_router, at<float>(ws, L.logits), err, st));
-    ra.k = 0;
-    ra.probs_t = at<float>(ws, L.probs);
-    LAUNCH(launch_route_topk(ra, st), "router probabilities");
-    if (stats) LAUNCH(launch_stats_reduce(partials, route_blocks(s->T), s->E, stats, st), "stats reduce");
+    int nb = route_blocks(s->T);
+    if (logits_in == nullptr) {
+      RouteArgs ra = route_args(s, nullptr, 1, router_bias, nullptr, nullptr, nullptr, partials,
+                                err);
+      ra.k = 0;
+      ra.probs_t = at<float>(ws, L.probs);
+      TRY(route_from_x(s, x, w_router, ra, at<float>(ws, L.logits), err, st));
+      nb = route_partials_from_x(s);
+    } else {
+      RouteArgs ra = route_args(s, logits_in, 1, nullptr, nullptr, nullptr, nullptr, partials,
+                                err);
+      ra.k = 0;
+      ra.probs_t = at<float>(ws, L.probs);
+      LAUNCH(launch_route_topk(ra, st), "router probabilities");
+    }
+    if (stats) LAUNCH(launch_stats_reduce(partials, nb, s->E, stats, st), "stats reduce");
   } else if (stats && cudaMemsetAsync(stats, 0, (s->E + 1) * sizeof(float), st) != cudaSuccess) {
     return cuda_status("memset stats");
   }

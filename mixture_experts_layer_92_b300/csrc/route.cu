@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "launchers.h"
+#include "route_token.cuh"
 
 namespace moe {
 
@@ -24,16 +25,7 @@ namespace {
 
 constexpr int kRouteWarps = 8;
 constexpr int kRouteThreads = kRouteWarps * 32;
-constexpr int kNoIdx = 0x7fffffff;
 constexpr int kRouteMaxBlocks = 592;
-
-// Order-preserving 32-bit image of a selection key: a > b as floats iff key(a) > key(b) as
-// unsigned integers, -0.0 and +0.0 map to the same value, and every finite value maps above
-// 0 (0 marks "not a candidate").
-__device__ __forceinline__ uint32_t order_key(float f) {
-  const uint32_t u = (f == 0.0f) ? 0u : __float_as_uint(f);
-  return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
-}
 
 // JM = values per lane: lane l holds the logits of experts l, l+32, ..., l+32*(JM-1).
 // FULL: E == 32 * JM, every slot is an expert (no bounds predicates).
@@ -84,13 +76,11 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
         asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
       }
     }
-    float v[JM], ex[JM];
-    int slot[JM];
-    bool bad = false;
+    float v[JM];
 #pragma unroll
     for (int j = 0; j < JM; ++j) {
       const int e = lane + 32 * j;
-      slot[j] = -1;
+      v[j] = 0.f;
       if (FULL || e < E) {
         // split-K partial sums of the router GEMM, added in split order, then the bias
         float acc = first[j];
@@ -98,106 +88,10 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
         if (bias != nullptr) acc += __ldg(bias + e);
         if (logits_out != nullptr) logits_out[static_cast<size_t>(t) * E + e] = acc;
         v[j] = acc;
-        if (!isfinite(acc)) bad = true;
-      } else {
-        v[j] = -INFINITY;
       }
     }
-    if (__any_sync(0xffffffffu, bad)) {
-      if (lane == 0) record_error(err, MOE_ERR_NONFINITE, SITE_ROUTE_NONFINITE, t);
-    }
-
-    // softmax over all E (for the gates of SOFTMAX_ALL and for P_i), and lse for L_z
-    float m = -INFINITY;
-#pragma unroll
-    for (int j = 0; j < JM; ++j) m = fmaxf(m, v[j]);
-    m = warp_max(m);
-    float s = 0.f;
-#pragma unroll
-    for (int j = 0; j < JM; ++j) {
-      ex[j] = (FULL || lane + 32 * j < E) ? expf(v[j] - m) : 0.f;
-      s += ex[j];
-    }
-    s = warp_sum(s);
-    const float inv_s = 1.0f / s;
-#pragma unroll
-    for (int j = 0; j < JM; ++j) {
-      const float pj = ex[j] * inv_s;
-      pacc[j] += pj;
-      // expert-choice routing reads the probabilities expert-major: probs_t[e][t]
-      if (probs_t != nullptr && (FULL || lane + 32 * j < E))
-        probs_t[static_cast<size_t>(lane + 32 * j) * T + t] = pj;
-    }
-    const float lse = m + logf(s);
-    if (lane == 0) lse2 += lse * lse;
-
-    // selection key: the raw logit, or (auxiliary-loss-free balancing) the gate affinity
-    // plus the expert's selection bias -- sigmoid(l) for sigmoid gating, the softmax
-    // probability otherwise. The gates below never include the bias.
-    float key[JM];
-#pragma unroll
-    for (int j = 0; j < JM; ++j) {
-      key[j] = v[j];
-      const int e = lane + 32 * j;
-      if (select_bias != nullptr && (FULL || e < E)) {
-        const float a = (gate_mode == MOE_GATE_SIGMOID_TOPK) ? 1.0f / (1.0f + expf(-v[j]))
-                                                             : ex[j] / s;
-        key[j] = a + __ldg(select_bias + e);
-      }
-    }
-
-    // k rounds of a warp arg-max over the not-yet-selected experts: each lane's best
-    // candidate (a strict '>' over ascending j keeps its lowest index among equals), the
-    // warp's largest key, then the lowest expert index holding it
-    uint32_t kk[JM];
-#pragma unroll
-    for (int j = 0; j < JM; ++j) kk[j] = (FULL || lane + 32 * j < E) ? order_key(key[j]) : 0u;
-    for (int r = 0; r < k; ++r) {
-      uint32_t best = 0u;
-      int bj = 0;
-#pragma unroll
-      for (int j = 0; j < JM; ++j)
-        if (kk[j] > best) {
-          best = kk[j];
-          bj = j;
-        }
-      const uint32_t m = __reduce_max_sync(0xffffffffu, best);
-      const int bi = __reduce_min_sync(0xffffffffu, (best == m && best != 0u) ? lane + 32 * bj
-                                                                               : kNoIdx);
-      if ((bi & 31) == lane) {
-#pragma unroll
-        for (int j = 0; j < JM; ++j)
-          if (j == (bi >> 5)) {
-            slot[j] = r;
-            kk[j] = 0u;
-          }
-      }
-    }
-
-    // gates of the selected experts
-    float sel_sum = 0.f;
-    float aff[JM];
-#pragma unroll
-    for (int j = 0; j < JM; ++j) {
-      aff[j] = 0.f;
-      if (slot[j] >= 0) {
-        if (gate_mode == MOE_GATE_SIGMOID_TOPK)
-          aff[j] = 1.0f / (1.0f + expf(-v[j]));
-        else
-          aff[j] = ex[j];
-        sel_sum += aff[j];
-      }
-    }
-    if (gate_mode != MOE_GATE_SOFTMAX_ALL) sel_sum = warp_sum(sel_sum);
-    const float inv_denom = (gate_mode == MOE_GATE_SOFTMAX_ALL) ? inv_s : 1.0f / sel_sum;
-#pragma unroll
-    for (int j = 0; j < JM; ++j) {
-      if (slot[j] >= 0) {
-        const size_t o = static_cast<size_t>(t) * k + slot[j];
-        topk_idx[o] = lane + 32 * j;
-        topk_gate[o] = aff[j] * inv_denom;
-      }
-    }
+    route_token<JM, FULL>(v, t, T, E, k, gate_mode, select_bias, probs_t, topk_idx, topk_gate,
+                          pacc, lse2, err, SITE_ROUTE_NONFINITE);
   }
 
   // per-block partial sums of p_{t,i} and lse^2, reduced over warps in a fixed order and

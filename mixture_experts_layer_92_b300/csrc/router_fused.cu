@@ -1,0 +1,389 @@
+// The fused router: score and select in one kernel, the logits never leaving the chip.
+//
+// "Mixture of experts (MoE)" (tirogla.com), How it works, steps 1-2: the router computes
+// l_t = x_t . W_r^T and each token keeps the top-k experts under the layer's gate
+// convention; Implementation notes: the router's arithmetic is kept in fp32 (here: bf16
+// operands, fp32 accumulation in tensor memory, fp32 logits); Complexity and constants: the
+// router costs 2*T*d*E FLOPs, so it is bound by reading x, not by the tensor cores.
+//
+// One thread-block cluster of CS CTAs owns a tile of 128 tokens. CTA r of the cluster
+// multiplies the tile's x rows by W_r over its own slice of the model width d (split K), so
+// CS CTAs stream the tile's x at once and T/128 tiles fill the chip:
+//   warp 0   TMA producer: x tile [128 x 64] and W_r tile [BN x 64] (bf16, 128-byte swizzle)
+//            into a ring of stages;
+//   warp 1   allocates TMEM; one thread issues tcgen05.mma (M = 128, N = BN >= E, K = 16)
+//            accumulating the tile's partial logits in TMEM;
+//   warps 2-5 drain TMEM (tcgen05.ld, one 32-lane quarter each) into a [128 x E] fp32 block
+//            of shared memory (the ring's space, free once the MMAs are done).
+// After a cluster barrier, CTA r finishes the logits of rows [r*128/CS, (r+1)*128/CS): each
+// of its 8 warps takes one token at a time, adds the CS partial rows read from the cluster's
+// shared memory (distributed shared memory) in rank order -- a fixed order, so the logits
+// are bit-reproducible -- adds the router bias, and runs the per-token routing step
+// (route_token.cuh: softmax over all E, lse, top-k with ties to the lower index, gates).
+// Per-CTA sums of the probabilities and of lse^2 go to `partials` for the balance losses. A
+// second cluster barrier keeps every CTA's shared memory alive until its peers have read it.
+// Every mbarrier wait is bounded; on a timeout the kernel records MOE_ERR_TIMEOUT, still
+// reaches both cluster barriers (its peers wait there) and frees its TMEM.
+#include <algorithm>
+#include <mutex>
+
+#include "common.cuh"
+#include "launchers.h"
+#include "route_token.cuh"
+#include "tma_host.h"
+
+namespace moe {
+namespace {
+
+constexpr int RF_BM = 128;        // tokens per cluster tile (the MMA's M)
+constexpr int RF_BK = 64;         // K elements per stage: 128-byte rows, 128-byte swizzle
+constexpr int RF_WARPS = 8;
+constexpr int RF_THREADS = RF_WARPS * 32;
+constexpr int RF_MAX_STAGES = 8;
+
+struct RfArgs {
+  int T, E, d;
+  int kb_per;               // k-blocks (of 64) per CTA of a cluster
+  int stages;               // ring depth
+  int cs;                   // CTAs per cluster
+  const float* bias;        // [E] or nullptr
+  const float* select_bias; // [E] or nullptr (selection only)
+  float* logits_out;        // [T][E] or nullptr
+  float* probs_t;           // [E][T] or nullptr
+  int k, gate_mode;
+  int32_t* topk_idx;
+  float* topk_gate;
+  float* partials;          // [E + 1][gridDim.x]
+  DeviceError* err;
+};
+
+template <int BN>
+struct RfCfg {
+  static constexpr int A_BYTES = RF_BM * RF_BK * 2;
+  static constexpr int B_BYTES = BN * RF_BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
+  // partial logits in shared memory: row stride BN + 4 floats keeps 16-byte stores of eight
+  // consecutive rows on distinct banks
+  static constexpr int PSTRIDE = BN + 4;
+  static constexpr int PART_BYTES = RF_BM * PSTRIDE * 4;
+  static constexpr uint32_t IDESC = idesc_bf16_f32(RF_BM, BN);
+  static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N % 16 == 0, 16..256");
+  static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
+  // bytes after the tile region (ring, later partial logits): per-warp statistics, then the
+  // barriers and the TMEM slot
+  __host__ __device__ static int stat_bytes(int E) { return RF_WARPS * (E + 1) * 4; }
+  __host__ __device__ static int tile_bytes(int stages) {
+    return stages * STAGE_BYTES > PART_BYTES ? stages * STAGE_BYTES : PART_BYTES;
+  }
+  // the deepest ring the shared memory holds (192 KB of stages)
+  __host__ __device__ static constexpr int max_stages() {
+    return (192 * 1024 / STAGE_BYTES) < RF_MAX_STAGES ? 192 * 1024 / STAGE_BYTES : RF_MAX_STAGES;
+  }
+  __host__ __device__ static int smem_bytes(int stages, int E) {
+    return 1024 + tile_bytes(stages) + stat_bytes(E) + (2 * RF_MAX_STAGES + 2) * 8 + 16;
+  }
+};
+
+// Loads a 32-bit word of CTA `rank`'s shared memory at this CTA's offset `p`.
+__device__ __forceinline__ float ld_cluster_f32(const float* p, uint32_t rank) {
+  float v;
+  asm volatile(
+      "{\n\t.reg .b32 ra;\n\t"
+      "mapa.shared::cluster.u32 ra, %1, %2;\n\t"
+      "ld.shared::cluster.f32 %0, [ra];\n\t}"
+      : "=f"(v)
+      : "r"(smem_u32(p)), "r"(rank)
+      : "memory");
+  return v;
+}
+
+template <int BN, int JM, bool FULL>
+__global__ void __launch_bounds__(RF_THREADS, 1)
+router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
+                    const __grid_constant__ CUtensorMap tmW, const RfArgs a) {
+  using C = RfCfg<BN>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int tile_bytes = C::tile_bytes(a.stages);
+  uint8_t* ring = smem;
+  float* part = reinterpret_cast<float*>(smem);  // after the MMAs: [128][PSTRIDE]
+  float* s_stat = reinterpret_cast<float*>(smem + tile_bytes);  // [RF_WARPS][E + 1]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + tile_bytes + C::stat_bytes(a.E));
+  uint64_t* full_bar = bars;
+  uint64_t* empty_bar = bars + RF_MAX_STAGES;
+  uint64_t* tfull_bar = bars + 2 * RF_MAX_STAGES;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * RF_MAX_STAGES + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_ctarank();
+  const int row0 = static_cast<int>(blockIdx.x / a.cs) * RF_BM;
+  const int nk_all = (a.d + RF_BK - 1) / RF_BK;
+  const int kb0 = static_cast<int>(rank) * a.kb_per;
+  const int nk = max(0, min(a.kb_per, nk_all - kb0));
+  DeviceError* err = a.err;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < a.stages; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    mbar_init(tfull_bar, 1);
+    *abort_flag = 0;
+    fence_barrier_init();
+  }
+  if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+  // x may be the previous kernel's output
+  pdl_wait();
+  pdl_launch_dependents();
+
+  if (warp == 0) {
+    if (lane == 0 && nk > 0) {
+      // ================= TMA producer =================
+      tma_prefetch_desc(&tmX);
+      tma_prefetch_desc(&tmW);
+      int stage = 0;
+      uint32_t phase = 0, issued = 0, parity = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, err,
+                               SITE_GEMM_WAIT_EMPTY))
+          break;
+        uint8_t* sa = ring + stage * C::STAGE_BYTES;
+        mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+        tma_load_2d(sa, &tmX, &full_bar[stage], (kb0 + kb) * RF_BK, row0);
+        tma_load_2d(sa + C::A_BYTES, &tmW, &full_bar[stage], (kb0 + kb) * RF_BK, 0);
+        issued |= 1u << stage;
+        parity = (parity & ~(1u << stage)) | (phase << stage);
+        if (++stage == a.stages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      // every copy this thread issued has landed before the ring is reused or the CTA exits
+      for (int s = 0; s < a.stages; ++s)
+        if (issued & (1u << s))
+          mbar_wait_bounded(&full_bar[s], (parity >> s) & 1u, nullptr, err, SITE_GEMM_WAIT_DRAIN);
+    }
+  } else if (warp == 1) {
+    if (lane == 0 && nk > 0) {
+      // ================= MMA issuer =================
+      int stage = 0;
+      uint32_t phase = 0;
+      for (int kb = 0; kb < nk; ++kb) {
+        if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, err, SITE_GEMM_WAIT_FULL))
+          break;
+        tc_fence_after();
+        const uint32_t a_addr = smem_u32(ring + stage * C::STAGE_BYTES);
+        const uint32_t b_addr = a_addr + C::A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < RF_BK / 16; ++kk)
+          tc_mma_bf16(tmem_base, smem_desc_kmajor<128>(a_addr + kk * 32),
+                      smem_desc_kmajor<128>(b_addr + kk * 32), C::IDESC,
+                      (kb | kk) != 0 ? 1u : 0u);
+        tc_commit(&empty_bar[stage]);
+        if (++stage == a.stages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+      // after the last MMA (or an abort): everything issued has completed
+      tc_commit(tfull_bar);
+    }
+  }
+  __syncwarp();
+
+  // ---- drain TMEM into the shared-memory block of partial logits (warps 2-5)
+  if (warp >= 2 && warp < 6) {
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    float* prow = part + r * C::PSTRIDE;
+    bool ok = true;
+    if (nk > 0) ok = mbar_wait_bounded(tfull_bar, 0, abort_flag, err, SITE_GEMM_WAIT_TMEM_FULL);
+    tc_fence_after();
+#pragma unroll 1
+    for (int c = 0; c < BN / 16; ++c) {
+      uint32_t v[16];
+      if (nk > 0 && ok) {
+        tmem_ld_16cols(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c * 16, v);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) v[i] = 0u;   // an empty K slice contributes zeros
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q)
+        *reinterpret_cast<uint4*>(prow + c * 16 + 4 * q) =
+            make_uint4(v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+    }
+  }
+  tc_fence_before();
+  cluster_sync_all();  // every CTA's partial logits are written and visible to the cluster
+
+  // ---- reduce the cluster's partials in rank order and route this CTA's rows
+  float pacc[JM];
+#pragma unroll
+  for (int j = 0; j < JM; ++j) pacc[j] = 0.f;
+  float lse2 = 0.f;
+  const int rows_per = RF_BM / a.cs;
+  for (int rl = warp; rl < rows_per; rl += RF_WARPS) {
+    const int r = static_cast<int>(rank) * rows_per + rl;
+    const int t = row0 + r;
+    if (t >= a.T) break;
+    float v[JM];
+#pragma unroll
+    for (int j = 0; j < JM; ++j) {
+      const int e = lane + 32 * j;
+      v[j] = 0.f;
+      if (FULL || e < a.E) {
+        const float* src = part + r * C::PSTRIDE + e;
+        float acc = ld_cluster_f32(src, 0);
+        for (int q = 1; q < a.cs; ++q) acc += ld_cluster_f32(src, q);
+        if (a.bias != nullptr) acc += __ldg(a.bias + e);
+        if (a.logits_out != nullptr) a.logits_out[static_cast<size_t>(t) * a.E + e] = acc;
+        v[j] = acc;
+      }
+    }
+    route_token<JM, FULL>(v, t, a.T, a.E, a.k, a.gate_mode, a.select_bias, a.probs_t,
+                          a.topk_idx, a.topk_gate, pacc, lse2, err, SITE_ROUTE_NONFINITE);
+  }
+
+  // per-CTA sums of p_{t,i} and lse^2 over the warps in a fixed order, expert-major
+#pragma unroll
+  for (int j = 0; j < JM; ++j) {
+    const int e = lane + 32 * j;
+    if (FULL || e < a.E) s_stat[warp * (a.E + 1) + e] = pacc[j];
+  }
+  if (lane == 0) s_stat[warp * (a.E + 1) + a.E] = lse2;
+  __syncthreads();
+  for (int e = threadIdx.x; e <= a.E; e += RF_THREADS) {
+    float acc = 0.f;
+    for (int w = 0; w < RF_WARPS; ++w) acc += s_stat[w * (a.E + 1) + e];
+    a.partials[static_cast<size_t>(e) * gridDim.x + blockIdx.x] = acc;
+  }
+
+  tc_fence_before();
+  cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc(tmem_base, C::TMEM_COLS);
+  }
+}
+
+int pick_bn(int E) {
+  if (E <= 16) return 16;
+  if (E <= 32) return 32;
+  if (E <= 64) return 64;
+  if (E <= 128) return 128;
+  return 256;
+}
+
+template <int BN, int JM, bool FULL>
+int launch_rf(const RouterFusedPlan& pl, const RfArgs& a, const void* x, const void* wr,
+              cudaStream_t stream) {
+  using C = RfCfg<BN>;
+  if (!get_encoder()) return MOE_ERR_CUDA;
+  CUtensorMap mX{}, mW{};
+  if (!encode_2d(&mX, x, a.d, a.T, RF_BM, RF_BK)) return MOE_ERR_CUDA;
+  if (!encode_2d(&mW, wr, a.d, a.E, BN, RF_BK)) return MOE_ERR_CUDA;
+  auto kernel = router_fused_kernel<BN, JM, FULL>;
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
+  static std::once_flag once[64];
+  static bool attr_ok[64];
+  std::call_once(once[dev], [&]() {
+    attr_ok[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        C::smem_bytes(C::max_stages(), 256)) == cudaSuccess;
+  });
+  if (a.stages > C::max_stages() || a.E > 256) return MOE_ERR_INVALID;
+  if (!attr_ok[dev]) return MOE_ERR_CUDA;
+  cudaLaunchAttribute attr[2];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = static_cast<unsigned>(pl.cs);
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(static_cast<unsigned>(pl.grid));
+  cfg.blockDim = dim3(RF_THREADS);
+  cfg.dynamicSmemBytes = static_cast<size_t>(C::smem_bytes(a.stages, a.E));
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 2;
+  if (cudaLaunchKernelEx(&cfg, kernel, mX, mW, a) != cudaSuccess) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+template <int BN, int JM>
+int launch_rf_jm(const RouterFusedPlan& pl, const RfArgs& a, const void* x, const void* wr,
+                 cudaStream_t stream) {
+  if (a.E == 32 * JM) return launch_rf<BN, JM, true>(pl, a, x, wr, stream);
+  return launch_rf<BN, JM, false>(pl, a, x, wr, stream);
+}
+
+}  // namespace
+
+// Cluster size and ring depth, from the shape alone (148 is the B300 SM count), so the
+// summation order of the partial logits -- and every bit of them -- depends on the shape
+// only. Aim at about two CTAs per SM for E <= 128 (their set-up and pipeline fill overlap
+// each other's streaming) and one for E > 128 (the 32 KB weight tile per stage).
+RouterFusedPlan router_fused_plan(int T, int d, int E) {
+  RouterFusedPlan pl{};
+  const int tiles = (T + RF_BM - 1) / RF_BM;
+  const int nk = (d + RF_BK - 1) / RF_BK;
+  const int per_sm = E <= 128 ? 2 : 1;
+  int cs = 1;
+  while (cs < 8 && tiles * cs * 2 <= 148 * per_sm && cs * 2 <= nk) cs *= 2;
+  pl.cs = cs;
+  pl.kb_per = (nk + cs - 1) / cs;
+  pl.grid = tiles * cs;
+  const int bn = pick_bn(E);
+  const int stage = RF_BM * RF_BK * 2 + bn * RF_BK * 2;
+  const int budget = per_sm == 2 ? 96 * 1024 : 192 * 1024;
+  pl.stages = std::max(2, std::min({RF_MAX_STAGES, budget / stage, std::max(pl.kb_per, 2)}));
+  return pl;
+}
+
+int launch_router_fused(const RouterFusedPlan& pl, const void* x, const void* w_router,
+                        const RouteArgs& r, int d, cudaStream_t stream) {
+  if (r.T == 0) return MOE_OK;
+  if (r.E > 256) return MOE_ERR_UNSUPPORTED;
+  if (pl.cs < 1 || pl.cs > 8 || (RF_BM % pl.cs) != 0) return MOE_ERR_INVALID;
+  RfArgs a{};
+  a.T = r.T;
+  a.E = r.E;
+  a.d = d;
+  a.kb_per = pl.kb_per;
+  a.stages = pl.stages;
+  a.cs = pl.cs;
+  a.bias = r.bias;
+  a.select_bias = r.select_bias;
+  a.logits_out = r.logits_out;
+  a.probs_t = r.probs_t;
+  a.k = r.k;
+  a.gate_mode = r.gate_mode;
+  a.topk_idx = r.topk_idx;
+  a.topk_gate = r.topk_gate;
+  a.partials = r.partials;
+  a.err = r.err;
+  const int bn = pick_bn(r.E);
+  const int jm = (r.E + 31) / 32;
+#define MOE_RF_CASE(BN_, JM_)                                   \
+  if (bn == BN_ && jm <= JM_) return launch_rf_jm<BN_, JM_>(pl, a, x, w_router, stream);
+  MOE_RF_CASE(16, 1)
+  MOE_RF_CASE(32, 1)
+  MOE_RF_CASE(64, 2)
+  MOE_RF_CASE(128, 4)
+  MOE_RF_CASE(256, 8)
+#undef MOE_RF_CASE
+  return MOE_ERR_UNSUPPORTED;
+}
+
+}  // namespace moe
