@@ -27,10 +27,10 @@ constexpr int kRouteWarps = 8;
 constexpr int kRouteThreads = kRouteWarps * 32;
 constexpr int kRouteMaxBlocks = 592;
 
-// JM = values per lane: lane l holds the logits of experts l, l+32, ..., l+32*(JM-1).
-// FULL: E == 32 * JM, every slot is an expert (no bounds predicates).
-template <int JM, bool FULL>
-__global__ void __launch_bounds__(kRouteThreads)
+// G lanes per token, J logits per lane, NT tokens per lane group at a time (route_token.cuh);
+// FULL: E == G * J (no bounds predicates).
+template <int G, int J, int NT, bool FULL>
+__global__ void __launch_bounds__(kRouteThreads, J >= 32 ? 1 : 2)
 route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_stride,
                   const float* __restrict__ bias, const float* __restrict__ select_bias,
                   float* __restrict__ logits_out, float* __restrict__ probs_t, int T, int E,
@@ -38,70 +38,56 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
                   int32_t* __restrict__ topk_idx, float* __restrict__ topk_gate,
                   float* __restrict__ partials, DeviceError* err) {
   extern __shared__ float s_part[];  // [kRouteWarps][E + 1]
+  constexpr int TPW = (32 / G) * NT;  // tokens per warp per iteration
   const int lane = threadIdx.x & 31;
   const int warp = threadIdx.x >> 5;
+  const int g = lane & (G - 1);
+  const int gi = lane / G;
   pdl_wait();
   pdl_launch_dependents();
 
-  float pacc[JM];
+  RouteStats<J> st;
+  st.zero();
+  const int stride = gridDim.x * kRouteWarps * TPW;
+  for (int base = (blockIdx.x * kRouteWarps + warp) * TPW; base < T; base += stride) {
+    float v[NT][J];
+    int t[NT];
+    bool valid[NT];
 #pragma unroll
-  for (int j = 0; j < JM; ++j) pacc[j] = 0.f;
-  float lse2 = 0.f;
-
-  const int nwarps = gridDim.x * kRouteWarps;
-  // A warp's next token is fetched while it works on this one: the first split plane of its
-  // logits into registers, the other planes (if any) into L2.
-  const int lines = (E * 4 + 127) / 128;
-  float nxt[JM];
-  {
-    const int t0 = blockIdx.x * kRouteWarps + warp;
+    for (int n = 0; n < NT; ++n) {
+      t[n] = base + gi * NT + n;
+      valid[n] = t[n] < T;
+      const float* row = logits + static_cast<size_t>(t[n]) * E;
 #pragma unroll
-    for (int j = 0; j < JM; ++j)
-      nxt[j] = (t0 < T && (FULL || lane + 32 * j < E))
-                   ? __ldg(logits + static_cast<size_t>(t0) * E + lane + 32 * j) : 0.f;
-  }
-  for (int t = blockIdx.x * kRouteWarps + warp; t < T; t += nwarps) {
-    const float* row = logits + static_cast<size_t>(t) * E;
-    float first[JM];
-#pragma unroll
-    for (int j = 0; j < JM; ++j) first[j] = nxt[j];
-    if (t + nwarps < T) {
-      const float* row_n = row + static_cast<size_t>(nwarps) * E;
-#pragma unroll
-      for (int j = 0; j < JM; ++j)
-        if (FULL || lane + 32 * j < E) nxt[j] = __ldg(row_n + lane + 32 * j);
-      for (int i = lane; i < lines * (nsplit - 1); i += 32) {
-        const int sp = 1 + i / lines;
-        const float* p = row_n + sp * split_stride + (i - (sp - 1) * lines) * 32;
-        asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+      for (int j = 0; j < J; ++j) {
+        const int e = g + G * j;
+        v[n][j] = 0.f;
+        if (valid[n] && (FULL || e < E)) {
+          // split-K partial sums of the router GEMM, added in split order, then the bias
+          float acc = __ldg(row + e);
+          for (int sp = 1; sp < nsplit; ++sp) acc += __ldg(row + sp * split_stride + e);
+          if (bias != nullptr) acc += __ldg(bias + e);
+          if (logits_out != nullptr) logits_out[static_cast<size_t>(t[n]) * E + e] = acc;
+          v[n][j] = acc;
+        }
       }
     }
-    float v[JM];
-#pragma unroll
-    for (int j = 0; j < JM; ++j) {
-      const int e = lane + 32 * j;
-      v[j] = 0.f;
-      if (FULL || e < E) {
-        // split-K partial sums of the router GEMM, added in split order, then the bias
-        float acc = first[j];
-        for (int sp = 1; sp < nsplit; ++sp) acc += __ldg(row + sp * split_stride + e);
-        if (bias != nullptr) acc += __ldg(bias + e);
-        if (logits_out != nullptr) logits_out[static_cast<size_t>(t) * E + e] = acc;
-        v[j] = acc;
-      }
-    }
-    route_token<JM, FULL>(v, t, T, E, k, gate_mode, select_bias, probs_t, topk_idx, topk_gate,
-                          pacc, lse2, err, SITE_ROUTE_NONFINITE);
+    route_tokens<G, J, NT, FULL>(v, t, valid, T, E, k, gate_mode, select_bias, probs_t, topk_idx,
+                                 topk_gate, st, err, SITE_ROUTE_NONFINITE);
   }
 
-  // per-block partial sums of p_{t,i} and lse^2, reduced over warps in a fixed order and
-  // stored expert-major, partials[e][block], so that the reduction below reads rows
+  // per-block partial sums of p_{t,i} and lse^2: over the warp's groups, then over the warps
+  // in a fixed order, stored expert-major, partials[e][block], so that the reduction below
+  // reads rows
+  route_stats_warp_sum<G, J>(st);
+  if (lane < G) {
 #pragma unroll
-  for (int j = 0; j < JM; ++j) {
-    const int e = lane + 32 * j;
-    if (FULL || e < E) s_part[warp * (E + 1) + e] = pacc[j];
+    for (int j = 0; j < J; ++j) {
+      const int e = g + G * j;
+      if (FULL || e < E) s_part[warp * (E + 1) + e] = st.pacc[j];
+    }
+    if (lane == 0) s_part[warp * (E + 1) + E] = st.lse2;
   }
-  if (lane == 0) s_part[warp * (E + 1) + E] = lse2;
   __syncthreads();
   for (int e = threadIdx.x; e <= E; e += blockDim.x) {
     float acc = 0.f;
@@ -209,11 +195,11 @@ __global__ void update_select_bias_kernel(const int32_t* __restrict__ counts,
   }
 }
 
-template <int JM, bool FULL>
+template <int G, int J, int NT, bool FULL>
 int launch_full(const RouteArgs& a, cudaStream_t stream) {
   const int nb = route_blocks(a.T);
   const size_t smem = static_cast<size_t>(kRouteWarps) * (a.E + 1) * sizeof(float);
-  if (launch_pdl(route_topk_kernel<JM, FULL>, dim3(nb), dim3(kRouteThreads), smem, stream,
+  if (launch_pdl(route_topk_kernel<G, J, NT, FULL>, dim3(nb), dim3(kRouteThreads), smem, stream,
                  a.logits, a.nsplit, a.split_stride, a.bias, a.select_bias, a.logits_out,
                  a.probs_t, a.T, a.E, a.k, a.gate_mode, a.topk_idx, a.topk_gate, a.partials,
                  a.err) != cudaSuccess)
@@ -221,10 +207,10 @@ int launch_full(const RouteArgs& a, cudaStream_t stream) {
   return MOE_OK;
 }
 
-template <int JM>
-int launch_jm(const RouteArgs& a, cudaStream_t stream) {
-  if (a.E == 32 * JM) return launch_full<JM, true>(a, stream);
-  return launch_full<JM, false>(a, stream);
+template <int G, int J, int NT>
+int launch_gj(const RouteArgs& a, cudaStream_t stream) {
+  if (a.E == G * J) return launch_full<G, J, NT, true>(a, stream);
+  return launch_full<G, J, NT, false>(a, stream);
 }
 
 }  // namespace
@@ -239,13 +225,16 @@ int route_blocks(int T) {
 }
 
 int launch_route_topk(const RouteArgs& a, cudaStream_t stream) {
+  // lane groups as route_group_lanes(E); two tokens per group at a time while J is small
+  if (a.E <= 8) return launch_gj<8, 1, 2>(a, stream);
+  if (a.E <= 16) return launch_gj<8, 2, 2>(a, stream);
+  if (a.E <= 32) return launch_gj<8, 4, 2>(a, stream);
+  if (a.E <= 64) return launch_gj<8, 8, 1>(a, stream);
+  if (a.E <= 128) return launch_gj<8, 16, 1>(a, stream);
+  if (a.E <= 256) return launch_gj<16, 16, 1>(a, stream);
   const int jm = (a.E + 31) / 32;
-  if (jm <= 1) return launch_jm<1>(a, stream);
-  if (jm <= 2) return launch_jm<2>(a, stream);
-  if (jm <= 4) return launch_jm<4>(a, stream);
-  if (jm <= 8) return launch_jm<8>(a, stream);
-  if (jm <= 16) return launch_jm<16>(a, stream);
-  return launch_jm<32>(a, stream);
+  if (jm <= 16) return launch_gj<32, 16, 1>(a, stream);
+  return launch_gj<32, 32, 1>(a, stream);
 }
 
 int launch_stats_reduce(const float* partials, int nblocks, int E, float* stats,

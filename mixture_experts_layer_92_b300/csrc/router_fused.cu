@@ -8,22 +8,23 @@
 //
 // One thread-block cluster of CS CTAs owns a tile of 128 tokens. CTA r of the cluster
 // multiplies the tile's x rows by W_r over its own slice of the model width d (split K), so
-// CS CTAs stream the tile's x at once and T/128 tiles fill the chip:
+// CS CTAs stream the tile's x at once and T/128 tiles fill the chip (one CTA per SM):
 //   warp 0   TMA producer: x tile [128 x 64] and W_r tile [BN x 64] (bf16, 128-byte swizzle)
 //            into a ring of stages;
 //   warp 1   allocates TMEM; one thread issues tcgen05.mma (M = 128, N = BN >= E, K = 16)
 //            accumulating the tile's partial logits in TMEM;
-//   warps 2-5 drain TMEM (tcgen05.ld, one 32-lane quarter each) into a [128 x E] fp32 block
-//            of shared memory (the ring's space, free once the MMAs are done).
-// After a cluster barrier, CTA r finishes the logits of rows [r*128/CS, (r+1)*128/CS): each
-// of its 8 warps takes one token at a time, adds the CS partial rows read from the cluster's
-// shared memory (distributed shared memory) in rank order -- a fixed order, so the logits
-// are bit-reproducible -- adds the router bias, and runs the per-token routing step
-// (route_token.cuh: softmax over all E, lse, top-k with ties to the lower index, gates).
-// Per-CTA sums of the probabilities and of lse^2 go to `partials` for the balance losses. A
-// second cluster barrier keeps every CTA's shared memory alive until its peers have read it.
-// Every mbarrier wait is bounded; on a timeout the kernel records MOE_ERR_TIMEOUT, still
-// reaches both cluster barriers (its peers wait there) and frees its TMEM.
+//   then all 16 warps drain TMEM (tcgen05.ld; warp w reads lane quarter w % 4) into a
+//   [128 x E] fp32 block of shared memory (the ring's space, free once the MMAs are done).
+// After a cluster barrier, CTA r finishes the logits of rows [r*128/CS, (r+1)*128/CS): its
+// warps add, per token, the CS partial rows read from the cluster's shared memory
+// (distributed shared memory) in rank order -- a fixed order, so the logits are
+// bit-reproducible -- add the router bias, and run the routing step (route_token.cuh:
+// softmax over all E, lse, top-k with ties to the lower index, gates) on several tokens per
+// warp at once. Per-CTA sums of the probabilities and of lse^2 go to `partials` for the
+// balance losses. A second cluster barrier keeps every CTA's shared memory alive until its
+// peers have read it. Every mbarrier wait is bounded; on a timeout the kernel records
+// MOE_ERR_TIMEOUT, still reaches both cluster barriers (its peers wait there) and frees its
+// TMEM.
 #include <algorithm>
 #include <mutex>
 
@@ -37,7 +38,7 @@ namespace {
 
 constexpr int RF_BM = 128;        // tokens per cluster tile (the MMA's M)
 constexpr int RF_BK = 64;         // K elements per stage: 128-byte rows, 128-byte swizzle
-constexpr int RF_WARPS = 8;
+constexpr int RF_WARPS = 16;
 constexpr int RF_THREADS = RF_WARPS * 32;
 constexpr int RF_MAX_STAGES = 8;
 
@@ -63,9 +64,9 @@ struct RfCfg {
   static constexpr int B_BYTES = BN * RF_BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr uint32_t TMEM_COLS = BN < 32 ? 32 : BN;
-  // partial logits in shared memory: row stride BN + 4 floats keeps 16-byte stores of eight
-  // consecutive rows on distinct banks
-  static constexpr int PSTRIDE = BN + 4;
+  // partial logits in shared memory: row stride BN + 8 floats puts the rows that the lane
+  // groups of a warp read at once (8 lanes x 4 rows) on distinct banks
+  static constexpr int PSTRIDE = BN + 8;
   static constexpr int PART_BYTES = RF_BM * PSTRIDE * 4;
   static constexpr uint32_t IDESC = idesc_bf16_f32(RF_BM, BN);
   static_assert(BN % 16 == 0 && BN >= 16 && BN <= 256, "M=128 MMA needs N % 16 == 0, 16..256");
@@ -98,7 +99,7 @@ __device__ __forceinline__ float ld_cluster_f32(const float* p, uint32_t rank) {
   return v;
 }
 
-template <int BN, int JM, bool FULL>
+template <int BN, int G, int J, int NT, bool FULL>
 __global__ void __launch_bounds__(RF_THREADS, 1)
 router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
                     const __grid_constant__ CUtensorMap tmW, const RfArgs a) {
@@ -126,6 +127,24 @@ router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
   const int nk = max(0, min(a.kb_per, nk_all - kb0));
   DeviceError* err = a.err;
 
+  // Set-up. Thread 0 (the TMA producer) initialises the barriers and issues the first ring's
+  // worth of loads at once (every stage starts free), so the first bytes of x are on their
+  // way while warp 1 allocates TMEM.
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, parity = 0;
+  int kb_issued = 0;
+  auto issue = [&](int kb) {
+    uint8_t* sa = ring + stage * C::STAGE_BYTES;
+    mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
+    tma_load_2d(sa, &tmX, &full_bar[stage], (kb0 + kb) * RF_BK, row0);
+    tma_load_2d(sa + C::A_BYTES, &tmW, &full_bar[stage], (kb0 + kb) * RF_BK, 0);
+    issued |= 1u << stage;
+    parity = (parity & ~(1u << stage)) | (phase << stage);
+    if (++stage == a.stages) {
+      stage = 0;
+      phase ^= 1;
+    }
+  };
   if (threadIdx.x == 0) {
     for (int s = 0; s < a.stages; ++s) {
       mbar_init(&full_bar[s], 1);
@@ -134,37 +153,28 @@ router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
     mbar_init(tfull_bar, 1);
     *abort_flag = 0;
     fence_barrier_init();
+    // x may be the previous kernel's output
+    pdl_wait();
+    tma_prefetch_desc(&tmX);
+    tma_prefetch_desc(&tmW);
+    for (; kb_issued < nk && kb_issued < a.stages; ++kb_issued) issue(kb_issued);
   }
   if (warp == 1) tmem_alloc(tmem_slot, C::TMEM_COLS);
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
-  // x may be the previous kernel's output
   pdl_wait();
   pdl_launch_dependents();
 
   if (warp == 0) {
     if (lane == 0 && nk > 0) {
-      // ================= TMA producer =================
-      tma_prefetch_desc(&tmX);
-      tma_prefetch_desc(&tmW);
-      int stage = 0;
-      uint32_t phase = 0, issued = 0, parity = 0;
-      for (int kb = 0; kb < nk; ++kb) {
+      // ================= TMA producer: the rest of the K slice =================
+      for (int kb = kb_issued; kb < nk; ++kb) {
         if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1, abort_flag, err,
                                SITE_GEMM_WAIT_EMPTY))
           break;
-        uint8_t* sa = ring + stage * C::STAGE_BYTES;
-        mbar_arrive_expect_tx(&full_bar[stage], C::STAGE_BYTES);
-        tma_load_2d(sa, &tmX, &full_bar[stage], (kb0 + kb) * RF_BK, row0);
-        tma_load_2d(sa + C::A_BYTES, &tmW, &full_bar[stage], (kb0 + kb) * RF_BK, 0);
-        issued |= 1u << stage;
-        parity = (parity & ~(1u << stage)) | (phase << stage);
-        if (++stage == a.stages) {
-          stage = 0;
-          phase ^= 1;
-        }
+        issue(kb);
       }
       // every copy this thread issued has landed before the ring is reused or the CTA exits
       for (int s = 0; s < a.stages; ++s)
@@ -174,23 +184,23 @@ router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
   } else if (warp == 1) {
     if (lane == 0 && nk > 0) {
       // ================= MMA issuer =================
-      int stage = 0;
-      uint32_t phase = 0;
+      int mstage = 0;
+      uint32_t mphase = 0;
       for (int kb = 0; kb < nk; ++kb) {
-        if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag, err, SITE_GEMM_WAIT_FULL))
+        if (!mbar_wait_bounded(&full_bar[mstage], mphase, abort_flag, err, SITE_GEMM_WAIT_FULL))
           break;
         tc_fence_after();
-        const uint32_t a_addr = smem_u32(ring + stage * C::STAGE_BYTES);
+        const uint32_t a_addr = smem_u32(ring + mstage * C::STAGE_BYTES);
         const uint32_t b_addr = a_addr + C::A_BYTES;
 #pragma unroll
         for (int kk = 0; kk < RF_BK / 16; ++kk)
           tc_mma_bf16(tmem_base, smem_desc_kmajor<128>(a_addr + kk * 32),
                       smem_desc_kmajor<128>(b_addr + kk * 32), C::IDESC,
                       (kb | kk) != 0 ? 1u : 0u);
-        tc_commit(&empty_bar[stage]);
-        if (++stage == a.stages) {
-          stage = 0;
-          phase ^= 1;
+        tc_commit(&empty_bar[mstage]);
+        if (++mstage == a.stages) {
+          mstage = 0;
+          mphase ^= 1;
         }
       }
       // after the last MMA (or an abort): everything issued has completed
@@ -199,8 +209,9 @@ router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
   }
   __syncwarp();
 
-  // ---- drain TMEM into the shared-memory block of partial logits (warps 2-5)
-  if (warp >= 2 && warp < 6) {
+  // ---- drain TMEM into the shared-memory block of partial logits (all warps: warp w reads
+  // TMEM lane quarter w % 4, columns chunks w / 4, w / 4 + 4, ... of 16)
+  {
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
     float* prow = part + r * C::PSTRIDE;
@@ -208,7 +219,7 @@ router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
     if (nk > 0) ok = mbar_wait_bounded(tfull_bar, 0, abort_flag, err, SITE_GEMM_WAIT_TMEM_FULL);
     tc_fence_after();
 #pragma unroll 1
-    for (int c = 0; c < BN / 16; ++c) {
+    for (int c = warp >> 2; c < BN / 16; c += RF_WARPS / 4) {
       uint32_t v[16];
       if (nk > 0 && ok) {
         tmem_ld_16cols(tmem_base + (static_cast<uint32_t>(quarter * 32) << 16) + c * 16, v);
@@ -224,43 +235,63 @@ router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
     }
   }
   tc_fence_before();
-  cluster_sync_all();  // every CTA's partial logits are written and visible to the cluster
+  // every CTA's partial logits are written and visible to the cluster
+  if (a.cs > 1) cluster_sync_all(); else __syncthreads();
 
-  // ---- reduce the cluster's partials in rank order and route this CTA's rows
-  float pacc[JM];
+  // ---- reduce the cluster's partials in rank order and route this CTA's rows: warp w takes
+  // TPW consecutive rows per iteration (32 / G token groups of NT rows each)
+  constexpr int TPW = (32 / G) * NT;
+  const int g = lane & (G - 1);
+  const int gi = lane / G;
+  RouteStats<J> st;
+  st.zero();
+  const int r_begin = static_cast<int>(rank) * RF_BM / a.cs;
+  const int r_end = static_cast<int>(rank + 1) * RF_BM / a.cs;
+  for (int base = r_begin + warp * TPW; base < r_end && row0 + base < a.T;
+       base += RF_WARPS * TPW) {
+    float v[NT][J];
+    int t[NT];
+    bool valid[NT];
 #pragma unroll
-  for (int j = 0; j < JM; ++j) pacc[j] = 0.f;
-  float lse2 = 0.f;
-  const int rows_per = RF_BM / a.cs;
-  for (int rl = warp; rl < rows_per; rl += RF_WARPS) {
-    const int r = static_cast<int>(rank) * rows_per + rl;
-    const int t = row0 + r;
-    if (t >= a.T) break;
-    float v[JM];
+    for (int n = 0; n < NT; ++n) {
+      const int r = base + gi * NT + n;
+      t[n] = row0 + r;
+      valid[n] = r < r_end && t[n] < a.T;
 #pragma unroll
-    for (int j = 0; j < JM; ++j) {
-      const int e = lane + 32 * j;
-      v[j] = 0.f;
-      if (FULL || e < a.E) {
-        const float* src = part + r * C::PSTRIDE + e;
-        float acc = ld_cluster_f32(src, 0);
-        for (int q = 1; q < a.cs; ++q) acc += ld_cluster_f32(src, q);
-        if (a.bias != nullptr) acc += __ldg(a.bias + e);
-        if (a.logits_out != nullptr) a.logits_out[static_cast<size_t>(t) * a.E + e] = acc;
-        v[j] = acc;
+      for (int j = 0; j < J; ++j) {
+        const int e = g + G * j;
+        v[n][j] = 0.f;
+        if (valid[n] && (FULL || e < a.E)) {
+          const float* src = part + r * C::PSTRIDE + e;
+          float acc;
+          if (a.cs == 1) {
+            acc = *src;
+          } else {
+            acc = ld_cluster_f32(src, 0);
+            for (int q = 1; q < a.cs; ++q) acc += ld_cluster_f32(src, q);
+          }
+          if (a.bias != nullptr) acc += __ldg(a.bias + e);
+          if (a.logits_out != nullptr) a.logits_out[static_cast<size_t>(t[n]) * a.E + e] = acc;
+          v[n][j] = acc;
+        }
       }
     }
-    route_token<JM, FULL>(v, t, a.T, a.E, a.k, a.gate_mode, a.select_bias, a.probs_t,
-                          a.topk_idx, a.topk_gate, pacc, lse2, err, SITE_ROUTE_NONFINITE);
+    route_tokens<G, J, NT, FULL>(v, t, valid, a.T, a.E, a.k, a.gate_mode, a.select_bias,
+                                 a.probs_t, a.topk_idx, a.topk_gate, st, err,
+                                 SITE_ROUTE_NONFINITE);
   }
 
-  // per-CTA sums of p_{t,i} and lse^2 over the warps in a fixed order, expert-major
+  // per-CTA sums of p_{t,i} and lse^2: over the warp's groups, then over the warps in a fixed
+  // order, expert-major
+  route_stats_warp_sum<G, J>(st);
+  if (lane < G) {
 #pragma unroll
-  for (int j = 0; j < JM; ++j) {
-    const int e = lane + 32 * j;
-    if (FULL || e < a.E) s_stat[warp * (a.E + 1) + e] = pacc[j];
+    for (int j = 0; j < J; ++j) {
+      const int e = g + G * j;
+      if (FULL || e < a.E) s_stat[warp * (a.E + 1) + e] = st.pacc[j];
+    }
+    if (lane == 0) s_stat[warp * (a.E + 1) + a.E] = st.lse2;
   }
-  if (lane == 0) s_stat[warp * (a.E + 1) + a.E] = lse2;
   __syncthreads();
   for (int e = threadIdx.x; e <= a.E; e += RF_THREADS) {
     float acc = 0.f;
@@ -269,7 +300,8 @@ router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
   }
 
   tc_fence_before();
-  cluster_sync_all();  // no CTA leaves while a peer may still read its shared memory
+  // no CTA leaves while a peer may still read its shared memory
+  if (a.cs > 1) cluster_sync_all(); else __syncthreads();
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::TMEM_COLS);
@@ -284,7 +316,7 @@ int pick_bn(int E) {
   return 256;
 }
 
-template <int BN, int JM, bool FULL>
+template <int BN, int G, int J, int NT, bool FULL>
 int launch_rf(const RouterFusedPlan& pl, const RfArgs& a, const void* x, const void* wr,
               cudaStream_t stream) {
   using C = RfCfg<BN>;
@@ -292,7 +324,7 @@ int launch_rf(const RouterFusedPlan& pl, const RfArgs& a, const void* x, const v
   CUtensorMap mX{}, mW{};
   if (!encode_2d(&mX, x, a.d, a.T, RF_BM, RF_BK)) return MOE_ERR_CUDA;
   if (!encode_2d(&mW, wr, a.d, a.E, BN, RF_BK)) return MOE_ERR_CUDA;
-  auto kernel = router_fused_kernel<BN, JM, FULL>;
+  auto kernel = router_fused_kernel<BN, G, J, NT, FULL>;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   static std::once_flag once[64];
@@ -321,33 +353,32 @@ int launch_rf(const RouterFusedPlan& pl, const RfArgs& a, const void* x, const v
   return MOE_OK;
 }
 
-template <int BN, int JM>
-int launch_rf_jm(const RouterFusedPlan& pl, const RfArgs& a, const void* x, const void* wr,
+template <int BN, int G, int J, int NT>
+int launch_rf_gj(const RouterFusedPlan& pl, const RfArgs& a, const void* x, const void* wr,
                  cudaStream_t stream) {
-  if (a.E == 32 * JM) return launch_rf<BN, JM, true>(pl, a, x, wr, stream);
-  return launch_rf<BN, JM, false>(pl, a, x, wr, stream);
+  if (a.E == G * J) return launch_rf<BN, G, J, NT, true>(pl, a, x, wr, stream);
+  return launch_rf<BN, G, J, NT, false>(pl, a, x, wr, stream);
 }
 
 }  // namespace
 
 // Cluster size and ring depth, from the shape alone (148 is the B300 SM count), so the
 // summation order of the partial logits -- and every bit of them -- depends on the shape
-// only. Aim at about two CTAs per SM for E <= 128 (their set-up and pipeline fill overlap
-// each other's streaming) and one for E > 128 (the 32 KB weight tile per stage).
+// only. One CTA per SM (clusters are placed one CTA per SM: cluster occupancy measured 74
+// two-CTA and 15 eight-CTA clusters at once), the split of d doubling while the grid still
+// fits in one wave.
 RouterFusedPlan router_fused_plan(int T, int d, int E) {
   RouterFusedPlan pl{};
   const int tiles = (T + RF_BM - 1) / RF_BM;
   const int nk = (d + RF_BK - 1) / RF_BK;
-  const int per_sm = E <= 128 ? 2 : 1;
   int cs = 1;
-  while (cs < 8 && tiles * cs * 2 <= 148 * per_sm && cs * 2 <= nk) cs *= 2;
+  while (cs < 8 && tiles * cs * 2 <= 148 && cs * 2 <= nk) cs *= 2;
   pl.cs = cs;
   pl.kb_per = (nk + cs - 1) / cs;
   pl.grid = tiles * cs;
   const int bn = pick_bn(E);
   const int stage = RF_BM * RF_BK * 2 + bn * RF_BK * 2;
-  const int budget = per_sm == 2 ? 96 * 1024 : 192 * 1024;
-  pl.stages = std::max(2, std::min({RF_MAX_STAGES, budget / stage, std::max(pl.kb_per, 2)}));
+  pl.stages = std::max(2, std::min({RF_MAX_STAGES, 192 * 1024 / stage, std::max(pl.kb_per, 2)}));
   return pl;
 }
 
@@ -374,14 +405,14 @@ int launch_router_fused(const RouterFusedPlan& pl, const void* x, const void* w_
   a.partials = r.partials;
   a.err = r.err;
   const int bn = pick_bn(r.E);
-  const int jm = (r.E + 31) / 32;
-#define MOE_RF_CASE(BN_, JM_)                                   \
-  if (bn == BN_ && jm <= JM_) return launch_rf_jm<BN_, JM_>(pl, a, x, w_router, stream);
-  MOE_RF_CASE(16, 1)
-  MOE_RF_CASE(32, 1)
-  MOE_RF_CASE(64, 2)
-  MOE_RF_CASE(128, 4)
-  MOE_RF_CASE(256, 8)
+#define MOE_RF_CASE(BN_, EMAX, G_, J_, NT_) \
+  if (bn == BN_ && r.E <= EMAX) return launch_rf_gj<BN_, G_, J_, NT_>(pl, a, x, w_router, stream);
+  MOE_RF_CASE(16, 8, 8, 1, 2)
+  MOE_RF_CASE(16, 16, 8, 2, 2)
+  MOE_RF_CASE(32, 32, 8, 4, 2)
+  MOE_RF_CASE(64, 64, 8, 8, 1)
+  MOE_RF_CASE(128, 128, 8, 16, 1)
+  MOE_RF_CASE(256, 256, 16, 16, 1)
 #undef MOE_RF_CASE
   return MOE_ERR_UNSUPPORTED;
 }
