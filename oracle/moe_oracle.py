@@ -24,7 +24,11 @@ Readings where the pages are silent or disagree:
 * f_i = (assignments routed to i before the drop) / (T*k); P_i = mean softmax-over-all
   probability; L_aux = alpha*E*sum_i f_i*P_i; L_z = beta*mean_t(logsumexp(l_t)^2);
 * capacity C = ceil(cf*T*k/E), computed in fp64; "no drop" is C = T;
-* an empty batch (T = 0) has both losses 0 (f and P are undefined there).
+* an empty batch (T = 0) has both losses 0 (f and P are undefined there);
+* block-scaled experts (forward_mx): weights stored as E4M3 or E2M1 codes with one
+  power-of-two scale per 32 values along K; the activations entering each expert GEMM
+  (x and H) quantized to E4M3 blocks with the smallest scale that holds the block's
+  maximum, rounding to nearest, ties to even.
 
 Every function here is pinned by a ``-m "not gpu"`` test against closed forms, the
 pages' worked example, or brute force; none is "parity unpinned".
@@ -366,6 +370,148 @@ def decode_e4m3(codes) -> np.ndarray:
 def dequantize_rows(codes, scales) -> np.ndarray:
     """W[..., n, k] = decode(codes[..., n, k]) * scales[..., n]."""
     return decode_e4m3(codes) * _f64(scales)[..., None]
+
+
+# ---------------------------------------------------------------------------------------
+# Block-scaled ("microscaling") experts: [Starphix] "Inference Optimization", Quantization
+# (experts stored in 8 or 4 bits, the router kept in 16 bits) and [DL-S077] section 8.2
+# (DeepSeek-V3 computes in FP8). The pages fix no format; the reading taken here:
+#   * every 32 consecutive values along a row (the reduction axis K of a GEMM operand) share
+#     one power-of-two scale 2^s, and each value is stored as an 8-bit E4M3 code or a 4-bit
+#     E2M1 code: value = decode(code) * 2^s;
+#   * expert weights are stored this way (E4M3 or E2M1 codes);
+#   * the activations entering each expert GEMM -- the token rows x and the hidden rows
+#     H = silu(x W1^T) * (x W3^T) -- are quantized to E4M3 blocks the same way, with
+#     s = the smallest integer such that amax <= qmax * 2^s (qmax = 448 for E4M3, 6 for
+#     E2M1; amax = 0 gives the smallest scale), s clamped to [-127, 127], and codes rounded to
+#     the nearest value, ties to even (no value ever exceeds qmax, so nothing saturates);
+#   * products of decoded values are exact and summed; the router, the gates and the combine
+#     are those of the plain layer. There is no shared expert in this form.
+# E2M1 (4 bits): sign bit 3, exponent bits 2..1 with bias 1, mantissa bit 0; exponent 0
+# encodes m * 0.5; the values are 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives.
+# ---------------------------------------------------------------------------------------
+MX_BLOCK = 32
+MX_QMAX = {"e4m3": 448.0, "e2m1": 6.0}
+
+
+def decode_e2m1(codes) -> np.ndarray:
+    """E2M1 codes (integers 0..15, one per value) -> fp64 values."""
+    b = np.asarray(codes).astype(np.int64) & 0xF
+    sign = np.where(b >> 3, -1.0, 1.0)
+    e = (b >> 1) & 0x3
+    m = (b & 1).astype(np.float64)
+    return sign * np.where(e == 0, m * 0.5, (1.0 + m / 2.0) * np.exp2(e.astype(np.float64) - 1.0))
+
+
+def mx_decode(codes, fmt: str) -> np.ndarray:
+    return decode_e4m3(codes) if fmt == "e4m3" else decode_e2m1(codes)
+
+
+def mx_scale_exponent(amax, qmax: float) -> np.ndarray:
+    """The smallest integer s with amax <= qmax * 2^s, clamped to [-127, 127]; -127 for
+    amax = 0. (Exact: qmax * 2^s is exact in fp64, and the candidate from log2 is moved to
+    the smallest integer that satisfies the inequality.)"""
+    a = _f64(amax)
+    pos = a > 0
+    s = np.zeros(a.shape, dtype=np.int64)
+    with np.errstate(divide="ignore"):
+        s[pos] = np.ceil(np.log2(a[pos] / qmax)).astype(np.int64)
+    s[pos] = np.where(a[pos] > qmax * np.exp2(s[pos].astype(np.float64)), s[pos] + 1, s[pos])
+    s[pos] = np.where(a[pos] <= qmax * np.exp2(s[pos].astype(np.float64) - 1.0), s[pos] - 1, s[pos])
+    s[~pos] = -127
+    return np.clip(s, -127, 127)
+
+
+def round_to_e4m3(v) -> np.ndarray:
+    """Codes of the E4M3 values nearest to v (|v| <= 448), ties to the even mantissa."""
+    v = _f64(v)
+    a = np.abs(v)
+    f, e = np.frexp(np.where(a > 0, a, 1.0))               # a = f * 2^e, f in [0.5, 1)
+    k = np.maximum(e - 1, -6)                              # binade; subnormals share 2^-6's ulp
+    ulp = np.exp2(k.astype(np.float64) - 3.0)
+    q = np.rint(a / ulp) * ulp                             # np.rint: half to even
+    # encode q: normal when q >= 2^-6 (exponent field k + 7, mantissa (q / 2^k - 1) * 8)
+    f2, e2 = np.frexp(np.where(q > 0, q, 1.0))
+    k2 = e2 - 1
+    normal = q >= 2.0 ** -6
+    mant = np.where(normal, (q / np.exp2(k2.astype(np.float64)) - 1.0) * 8.0, q / 2.0 ** -9)
+    code = np.where(normal, ((k2 + 7) << 3) | np.rint(mant).astype(np.int64),
+                    np.rint(mant).astype(np.int64))
+    code = np.where(q == 0, 0, code)
+    assert np.all(a <= 448.0), "E4M3 rounding expects |v| <= 448"
+    return (code | np.where(np.signbit(v), 0x80, 0)).astype(np.uint8)
+
+
+def round_to_e2m1(v) -> np.ndarray:
+    """Codes of the E2M1 values nearest to v (|v| <= 6), ties to the even mantissa: each
+    magnitude is compared with the 8 grid values."""
+    v = _f64(v)
+    a = np.abs(v)
+    assert np.all(a <= 6.0), "E2M1 rounding expects |v| <= 6"
+    grid = decode_e2m1(np.arange(8))
+    d = np.abs(a[..., None] - grid)
+    best = np.min(d, axis=-1, keepdims=True)
+    cand = d == best
+    # among the (at most two) nearest grid values, the one with mantissa bit 0 (even code)
+    even = cand & (np.arange(8) % 2 == 0)
+    code = np.where(np.any(even, axis=-1), np.argmax(even, axis=-1), np.argmax(cand, axis=-1))
+    return (code | np.where(np.signbit(v), 8, 0)).astype(np.uint8)
+
+
+def mx_quantize(v, fmt: str = "e4m3"):
+    """Blocks of 32 along the last axis -> (codes [..., n] uint8, s [..., n / 32] int64)."""
+    v = _f64(v)
+    n = v.shape[-1]
+    assert n % MX_BLOCK == 0
+    blocks = v.reshape(v.shape[:-1] + (n // MX_BLOCK, MX_BLOCK))
+    s = mx_scale_exponent(np.max(np.abs(blocks), axis=-1), MX_QMAX[fmt])
+    scaled = blocks / np.exp2(s.astype(np.float64))[..., None]
+    codes = round_to_e4m3(scaled) if fmt == "e4m3" else round_to_e2m1(scaled)
+    return codes.reshape(v.shape), s
+
+
+def mx_dequantize(codes, s, fmt: str = "e4m3") -> np.ndarray:
+    """decode(codes) * 2^s, one s per block of 32 along the last axis."""
+    vals = mx_decode(codes, fmt)
+    n = vals.shape[-1]
+    blocks = vals.reshape(vals.shape[:-1] + (n // MX_BLOCK, MX_BLOCK))
+    return (blocks * np.exp2(_f64(s))[..., None]).reshape(vals.shape)
+
+
+def swiglu_ffn_mx(x_rows, w1, w3, w2) -> np.ndarray:
+    """The expert FFN on block-scaled activations: x rows and the hidden rows H are each
+    quantized to E4M3 blocks before their GEMM; w1, w3, w2 are the decoded weights."""
+    xq = mx_dequantize(*mx_quantize(x_rows, "e4m3"), "e4m3")
+    g = xq @ _f64(w1).T
+    u = xq @ _f64(w3).T
+    h = silu(g) * u
+    hq = mx_dequantize(*mx_quantize(h, "e4m3"), "e4m3")
+    return hq @ _f64(w2).T
+
+
+def forward_mx(x, w_router, mxw: dict, *, k: int, mode: str, C: int, router_bias=None,
+               alpha: float = 0.01, beta: float = 1e-3, idx_override=None) -> dict:
+    """The layer with block-scaled experts. mxw: fmt ("e4m3" | "e2m1") and, for each of
+    w1, w3 ([E, F, d]) and w2 ([E, d, F]), its codes and block exponents (keys "w1", "w1_s",
+    ...). Steps 1-3, 5 and 6 as in forward(); step 4 is swiglu_ffn_mx."""
+    x = _f64(x)
+    T = x.shape[0]
+    E = np.asarray(w_router).shape[0]
+    fmt = mxw["fmt"]
+    W = {nm: mx_dequantize(mxw[nm], mxw[nm + "_s"], fmt) for nm in ("w1", "w3", "w2")}
+    logits = router_logits(x, w_router, router_bias)
+    idx = select_topk(logits, k) if idx_override is None else np.asarray(idx_override, np.int64)
+    g = gates(logits, idx, mode)
+    disp = dispatch(idx, E, C)
+    rows = np.zeros((disp["perm"].shape[0], x.shape[1]), dtype=np.float64)
+    for e in range(E):
+        lo, hi = int(disp["offsets"][e]), int(disp["offsets"][e + 1])
+        if hi > lo:
+            rows[lo:hi] = swiglu_ffn_mx(x[disp["perm"][lo:hi] // k], W["w1"][e], W["w3"][e],
+                                        W["w2"][e])
+    y = combine(g, disp["inv"], rows, T, k)
+    return dict(y=y, logits=logits, idx=idx, gate=g, dispatch=disp,
+                l_aux=aux_loss(logits, idx, alpha), l_z=z_loss(logits, beta))
 
 
 # ---------------------------------------------------------------------------------------

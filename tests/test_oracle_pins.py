@@ -473,3 +473,152 @@ def test_dequantize_rows_applies_one_scale_per_row():
     codes = np.array([[[0x38, 0x40], [0xB8, 0x3C]]], dtype=np.uint8)   # [1, 2, 2]
     w = O.dequantize_rows(codes, np.array([[0.5, 4.0]]))
     np.testing.assert_array_equal(w, [[[0.5, 1.0], [-4.0, 6.0]]])
+
+
+# ---------------------------------------------------------------- block-scaled experts
+def test_e2m1_decode_closed_forms():
+    """The 16 E2M1 codes: 0, 0.5, 1, 1.5, 2, 3, 4, 6 and their negatives (sign bit 3)."""
+    v = O.decode_e2m1(np.arange(16))
+    np.testing.assert_array_equal(v[:8], [0, 0.5, 1, 1.5, 2, 3, 4, 6])
+    np.testing.assert_array_equal(v[8:], -v[:8])
+    assert np.signbit(v[8])
+
+
+def test_e4m3_rounding_matches_torch_float8_conversion():
+    """Round-to-nearest-even onto E4M3 against torch's float32 -> float8_e4m3fn conversion on
+    float32 values: random magnitudes over every binade, the exact grid, the midpoints
+    between neighbours (ties), subnormals and signed zeros."""
+    rng = np.random.default_rng(41)
+    grid = O.decode_e4m3(np.arange(0x7F)).astype(np.float32)            # 0 .. 448
+    mids = ((grid[:-1].astype(np.float64) + grid[1:]) / 2).astype(np.float32)
+    rand = (np.exp2(rng.uniform(-12, 8.8, 20000)) * rng.choice([-1, 1], 20000)).astype(np.float32)
+    rand = rand[np.abs(rand) <= 448]
+    v = np.concatenate([grid, -grid, mids, -mids, rand, np.float32([0.0, -0.0])])
+    assert np.all(mids.astype(np.float64) == (grid[:-1].astype(np.float64) + grid[1:]) / 2)
+    ref = torch.from_numpy(v).to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+    np.testing.assert_array_equal(O.round_to_e4m3(v), ref)
+
+
+@pytest.mark.parametrize("v,code", [(0.0, 0), (0.24, 0), (0.25, 0), (0.26, 1), (0.5, 1), (0.75, 2),
+                                    (1.24, 2), (1.25, 2), (1.26, 3), (1.75, 4), (2.5, 4), (2.51, 5),
+                                    (3.49, 5), (3.5, 6), (5.0, 6), (5.01, 7), (6.0, 7), (-0.3, 9),
+                                    (-2.5, 12), (-6.0, 15)])
+def test_e2m1_rounding_by_hand(v, code):
+    """Nearest E2M1 value, ties to the even mantissa (0.25 -> 0, 0.75 -> 1, 1.25 -> 1,
+    1.75 -> 2, 2.5 -> 2, 3.5 -> 4, 5 -> 4); the codes worked out by hand."""
+    assert int(O.round_to_e2m1(np.array([v]))[0]) == code
+
+
+def test_rounding_is_monotone_and_within_half_a_step():
+    rng = np.random.default_rng(42)
+    for fmt, qmax, n in (("e4m3", 448.0, 0x7F), ("e2m1", 6.0, 8)):
+        v = np.sort(rng.uniform(-qmax, qmax, 5000))
+        codes = O.round_to_e4m3(v) if fmt == "e4m3" else O.round_to_e2m1(v)
+        q = O.mx_decode(codes, fmt)
+        assert np.all(np.diff(q) >= 0)
+        grid = np.sort(O.mx_decode(np.arange(n), fmt))
+        gap = np.diff(grid)
+        i = np.clip(np.searchsorted(grid, np.abs(v)) - 1, 0, len(gap) - 1)
+        assert np.all(np.abs(np.abs(q) - np.abs(v)) <= gap[i] / 2 + 1e-12)
+
+
+def test_mx_scale_exponent():
+    """The smallest s with amax <= qmax * 2^s: brute force over s for random amax, and the
+    closed cases (amax = qmax * 2^k gives k, a hair above gives k + 1, 0 gives -127)."""
+    rng = np.random.default_rng(43)
+    for qmax in (448.0, 6.0):
+        a = np.exp2(rng.uniform(-100, 100, 300))
+        s = O.mx_scale_exponent(a, qmax)
+        for ai, si in zip(a, s):
+            brute = next(t for t in range(-140, 140) if ai <= qmax * 2.0 ** t)
+            assert si == max(-127, min(127, brute))
+        k = np.arange(-20, 21)
+        np.testing.assert_array_equal(O.mx_scale_exponent(qmax * np.exp2(k), qmax), k)
+        np.testing.assert_array_equal(O.mx_scale_exponent(qmax * np.exp2(k) * (1 + 2.0 ** -40), qmax),
+                                      k + 1)
+        assert O.mx_scale_exponent(np.array([0.0]), qmax)[0] == -127
+        assert O.mx_scale_exponent(np.array([1e-60]), qmax)[0] == -127
+
+
+def test_mx_quantize_blocks():
+    """Blocks of 32 along the last axis: values already on a block's grid come back exactly;
+    each block's scale is set by its own maximum (a huge
+    value in block 0 leaves block 1's small values at full E4M3 precision); the block
+    maximum lands in (qmax / 2, qmax] before rounding, [qmax / 2, qmax] after; quantizing
+    twice gives the values of quantizing once."""
+    rng = np.random.default_rng(44)
+    for fmt in ("e4m3", "e2m1"):
+        n = 8 if fmt == "e2m1" else 0x7F
+        codes = rng.integers(0, n, size=(5, 64)) | (rng.integers(0, 2, size=(5, 64)) << (3 if fmt == "e2m1" else 7))
+        s = rng.integers(-20, 20, size=(5, 2))
+        v = O.mx_dequantize(codes, s, fmt)
+        v[:, 0] = O.MX_QMAX[fmt] * np.exp2(s[:, 0])                      # each block attains qmax
+        v[:, 32] = -O.MX_QMAX[fmt] * np.exp2(s[:, 1])
+        c2, s2 = O.mx_quantize(v, fmt)
+        np.testing.assert_array_equal(s2, s)
+        np.testing.assert_array_equal(O.mx_dequantize(c2, s2, fmt), v)
+    x = np.concatenate([np.full(32, 1000.0), np.full(32, 1e-3)])[None]
+    c, s = O.mx_quantize(x)
+    xq = O.mx_dequantize(c, s)
+    assert abs(xq[0, 40] - 1e-3) <= 1e-3 * 2.0 ** -4
+    a = rng.normal(size=(7, 96)) * np.exp2(rng.integers(-30, 30, size=(7, 1)))
+    c, s = O.mx_quantize(a)
+    blk = np.abs(O.mx_dequantize(c, s)).reshape(7, 3, 32).max(-1) / np.exp2(s)
+    assert np.all((blk >= 224) & (blk <= 448))
+    # quantizing the quantized values again returns the same values (the codes may move one
+    # binade when a block maximum rounded down to exactly qmax / 2)
+    deq = O.mx_dequantize(c, s)
+    np.testing.assert_array_equal(O.mx_dequantize(*O.mx_quantize(deq)), deq)
+
+
+def test_swiglu_ffn_mx_by_hand():
+    """d = F = 32, one row x = 1 (on the grid: x quantizes exactly), w1 = w3 = the first
+    column of ones, so gate = up = 1 for every hidden unit and H = silu(1) = 0.7310586;
+    the block's scale: 0.731 <= 448 * 2^-9 = 0.875 but > 448 * 2^-10, so s = -9 and
+    0.7310586 * 2^9 = 374.3 rounds to 384 (E4M3 spacing 32 in [256, 448)): H is quantized to
+    384 * 2^-9 = 0.75. w2 = all ones sums the 32 units: 24 (24.0, not 32 * 0.731 = 23.39)."""
+    d = F = 32
+    x = np.ones((1, d))
+    w1 = np.zeros((F, d))
+    w1[:, 0] = 1.0
+    w2 = np.ones((d, F))
+    y = O.swiglu_ffn_mx(x, w1, w1, w2)
+    np.testing.assert_array_equal(y, np.full((1, d), 24.0))
+    # x off the grid: 3.3 in a block whose maximum is 3.3: s = -7 (3.3 <= 448 / 128 = 3.5),
+    # 3.3 * 128 = 422.4 rounds to 416 (spacing 32): x is quantized to 416 / 128 = 3.25
+    x = np.zeros((1, d))
+    x[0, 0] = 3.3
+    w1 = np.zeros((F, d))
+    w1[0, 0] = 1.0
+    w3 = np.zeros((F, d))
+    w3[0, 0] = 1.0 / 3.25
+    w2 = np.zeros((d, F))
+    w2[0, 0] = 1.0
+    # gate = 3.25, up = 1: H_0 = silu(3.25) = 3.1271...; in its block: s = -7, *128 = 400.3,
+    # spacing 32 -> 416 -> 3.25; everything else is 0
+    y = O.swiglu_ffn_mx(x, w1, w3, w2)
+    assert y[0, 0] == 3.25 and np.all(y[0, 1:] == 0)
+
+
+def test_forward_mx_structure():
+    """Identical experts and C = T: the layer is one dense FFN of the quantized operands
+    (gates sum to 1); and against the same layer without any activation quantization the
+    error stays at the E4M3 rounding level (neither zero nor gross)."""
+    rng = np.random.default_rng(45)
+    T, d, E, F, k = 24, 64, 4, 64, 2
+    one = {nm: rng.normal(size=sh) / np.sqrt(sh[-1]) for nm, sh in
+           (("w1", (F, d)), ("w3", (F, d)), ("w2", (d, F)))}
+    mxw = dict(fmt="e4m3")
+    for nm, w in one.items():
+        c, s = O.mx_quantize(np.repeat(w[None], E, 0))
+        mxw[nm], mxw[nm + "_s"] = c, s
+    x = rng.normal(size=(T, d))
+    wr = rng.normal(size=(E, d))
+    out = O.forward_mx(x, wr, mxw, k=k, mode="softmax_topk", C=T)
+    W = {nm: O.mx_dequantize(mxw[nm], mxw[nm + "_s"])[0] for nm in one}
+    np.testing.assert_allclose(out["y"], O.swiglu_ffn_mx(x, W["w1"], W["w3"], W["w2"]),
+                               rtol=1e-12, atol=1e-12)
+    plain = O.forward(x, wr, *(O.mx_dequantize(mxw[nm], mxw[nm + "_s"]) for nm in ("w1", "w3", "w2")),
+                      k=k, mode="softmax_topk", C=T)
+    err = np.linalg.norm(out["y"] - plain["y"]) / np.linalg.norm(plain["y"])
+    assert 0.005 < err < 0.08
