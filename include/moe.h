@@ -330,6 +330,44 @@ int moe_forward_fp8w(const moe_shape* s, const void* x, const void* w_router,
                      float* losses, void* ws, size_t ws_bytes, void* stream, void* const* events,
                      int n_events);
 
+/* Block-scaled ("microscaling") experts -- "Mixture of Experts (MoE)", learn.starphix.com,
+ * Inference Optimization, Quantization (experts stored in 8 or 4 bits, the router in 16);
+ * "DL S077 - Mixture of Experts (MoE) Intuition", section 8.2 (DeepSeek-V3 in FP8). The
+ * tensor cores multiply 8-bit (or 4-bit) operands whose every 32 consecutive K values share
+ * one power-of-two scale 2^s, stored as the byte s + 127 (UE8M0):
+ *   - weights: w1, w3 [E, d_ff, d] and w2 [E, d, d_ff] (K = the last axis) as
+ *       MOE_MX_E4M3: E4M3 codes, one byte per value, [E, N, K];
+ *       MOE_MX_E2M1: E2M1 codes, two per byte (the even K index in the low nibble),
+ *                    [E, N, K / 2], 32-byte aligned;
+ *     and their scales in 512-byte atoms [E][N / 128][K / 128][512]: the scale of weight
+ *     row n, columns 32j..32j+31 is byte (n % 32) * 16 + ((n % 128) / 32) * 4 + (j % 4) of
+ *     atom (e, n / 128, j / 4);
+ *   - activations: the gathered x rows and the hidden rows H = silu(x W1^T) * (x W3^T) are
+ *     quantized on the GPU to E4M3 blocks of 32 along K with s the smallest integer such that
+ *     the block's largest magnitude is <= 448 * 2^s (clamped to [-127, 127]), codes rounded to
+ *     nearest, ties to even; a non-finite x or H value sets MOE_ERR_NONFINITE in the error
+ *     word.
+ * The router, dispatch, combine and losses are those of moe_forward; products are exact and
+ * accumulated in fp32, y is bf16. Requires dtype bf16, top-k routing, d_ff_shared = 0,
+ * d % 256 == 0 and d_ff % 128 == 0 (else MOE_ERR_UNSUPPORTED).
+ * moe_mx_workspace_size: workspace bytes of moe_forward_mx (0 for an invalid shape).
+ * moe_forward_mx: the layer; fmt MOE_MX_E4M3 or MOE_MX_E2M1; other arguments as
+ *   moe_forward_events (events/n_events may be NULL/0).
+ * moe_mx_quantize: the activation quantization alone: bf16 rows x [rows, K] (K % 32 == 0) to
+ *   E4M3 codes [rows, K] and scale bytes [rows, K / 32] (row-major). ws: NULL, or a
+ *   workspace whose error word receives MOE_ERR_NONFINITE for a non-finite input. */
+#define MOE_MX_E4M3 0
+#define MOE_MX_E2M1 1
+size_t moe_mx_workspace_size(const moe_shape* s);
+int moe_forward_mx(const moe_shape* s, int fmt, const void* x, const void* w_router,
+                   const float* router_bias, const uint8_t* w1q, const uint8_t* w1_scales,
+                   const uint8_t* w3q, const uint8_t* w3_scales, const uint8_t* w2q,
+                   const uint8_t* w2_scales, void* y, int32_t* counts, int32_t* dropped,
+                   float* losses, void* ws, size_t ws_bytes, void* stream, void* const* events,
+                   int n_events);
+int moe_mx_quantize(const void* x, int64_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
+                    void* ws, void* stream);
+
 /* Backward pass (training) of the layer moe_forward computes, for top-k and expert-choice
  * layers.
  * It returns the gradient of

@@ -32,7 +32,9 @@ EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_
             "moe_grouped_swiglu_fp8w", "moe_forward_fp8w", "moe_backward_workspace_size",
             "moe_backward", "moe_selftest_wait_timeout", "moe_forward_host",
             "moe_host_pipeline_buffer_size", "moe_host_pipeline_create",
-            "moe_host_pipeline_forward", "moe_host_pipeline_join", "moe_host_pipeline_destroy")
+            "moe_host_pipeline_forward", "moe_host_pipeline_join", "moe_host_pipeline_destroy",
+            "moe_mx_workspace_size", "moe_forward_mx", "moe_mx_quantize")
+MX_FORMATS = {"e4m3": 0, "e2m1": 1}
 NUM_BWD_STAGES = 8
 BWD_STAGE_NAMES = ("route_dispatch", "gather_x_dy", "recompute_gu", "gemm_dh_swiglu_bwd",
                    "gate_logit_grads", "gemm_dx", "dx_combine", "gemm_wgrad")
@@ -98,6 +100,11 @@ def _load() -> ctypes.CDLL:
         "moe_forward_balanced": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                                 vp, vp, ctypes.c_float, vp, sz, vp,
                                                 ctypes.POINTER(vp), ctypes.c_int]),
+        "moe_mx_workspace_size": (sz, [sp]),
+        "moe_forward_mx": (ctypes.c_int, [sp, ctypes.c_int, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
+                                          vp, vp, vp, vp, sz, vp, ctypes.POINTER(vp),
+                                          ctypes.c_int]),
+        "moe_mx_quantize": (ctypes.c_int, [vp, ctypes.c_int64, i32, vp, vp, vp, vp]),
         "moe_backward_workspace_size": (sz, [sp]),
         "moe_backward": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_float,
                                         ctypes.c_float, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
@@ -275,6 +282,41 @@ def moe_forward_fp8w(s, ws, x, w_router, w1q, w1_scale, w3q, w3_scale, w2q, w2_s
                                 _p(counts), _p(dropped), _p(losses), _p(ws), ws.numel(),
                                 _stream(stream), arr, 0 if events is None else len(events)),
            "moe_forward_fp8w")
+
+
+def moe_mx_workspace_size(s: moe_shape) -> int:
+    return LIB.moe_mx_workspace_size(ctypes.byref(s))
+
+
+def alloc_workspace_mx(s: moe_shape, device="cuda") -> torch.Tensor:
+    """Zero-filled uint8 device buffer of moe_mx_workspace_size bytes."""
+    n = moe_mx_workspace_size(s)
+    if n == 0:
+        _check(moe_check_shape(s), "moe_mx_workspace_size")
+    ws = torch.zeros(n + 256, dtype=torch.uint8, device=device)
+    off = (-ws.data_ptr()) % 256
+    return ws[off:off + n]
+
+
+def moe_forward_mx(s, ws, fmt, x, w_router, w1q, w1_scales, w3q, w3_scales, w2q, w2_scales, y,
+                   router_bias=None, counts=None, dropped=None, losses=None, stream=None,
+                   events=None):
+    """moe_forward on block-scaled expert weights (fmt "e4m3" or "e2m1")."""
+    arr = None if events is None else _event_array(events)
+    f = MX_FORMATS[fmt] if isinstance(fmt, str) else int(fmt)
+    _check(LIB.moe_forward_mx(ctypes.byref(s), f, _p(x), _p(w_router), _p(router_bias), _p(w1q),
+                              _p(w1_scales), _p(w3q), _p(w3_scales), _p(w2q), _p(w2_scales),
+                              _p(y), _p(counts), _p(dropped), _p(losses), _p(ws), ws.numel(),
+                              _stream(stream), arr, 0 if events is None else len(events)),
+           "moe_forward_mx")
+
+
+def moe_mx_quantize(x, codes, scales, ws=None, stream=None):
+    """E4M3 blocks of 32 of the bf16 rows x [rows, K]: codes [rows, K] uint8, scale bytes
+    [rows, K / 32] uint8 (s + 127)."""
+    rows, K = x.shape
+    _check(LIB.moe_mx_quantize(_p(x), rows, K, _p(codes), _p(scales), _p(ws), _stream(stream)),
+           "moe_mx_quantize")
 
 
 def moe_update_select_bias(s, counts, select_bias, gamma, stream=None):

@@ -36,6 +36,8 @@ enum ErrSite : int {
   SITE_DISPATCH_GRID_BARRIER = 20,
   SITE_F16_RANGE_X = 30,   // 8-bit-weight path: an activation outside fp16's finite range
   SITE_F16_RANGE_H = 31,   //                    an H value outside fp16's finite range
+  SITE_MX_NONFINITE_X = 32, // block-scaled path: a non-finite activation in x
+  SITE_MX_NONFINITE_H = 33, //                    a non-finite hidden value H
   SITE_SELFTEST_WAIT = 40, // moe_selftest_wait_timeout: a wait that nothing completes
 };
 
@@ -430,6 +432,64 @@ __device__ __forceinline__ void tc_commit_pair(uint64_t* bar, uint16_t cta_mask)
       "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
       " [%0], %1;" ::"r"(smem_u32(bar)),
       "h"(cta_mask)
+      : "memory");
+}
+
+// ------------------------------------------------------------------------------------
+// Block-scaled MMA (kind::mxf8f6f4): 8-bit (or 4-bit, unpacked to one byte in shared
+// memory) operands with one UE8M0 scale per 32 K values, scales in tensor memory.
+// ------------------------------------------------------------------------------------
+// One contiguous copy global -> shared of `bytes` (multiple of 16, both addresses 16-byte
+// aligned), completing on `bar`.
+__device__ __forceinline__ void bulk_load(void* smem_dst, const void* gsrc, uint32_t bytes,
+                                          uint64_t* bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+          "r"(smem_u32(smem_dst)),
+      "l"(reinterpret_cast<uint64_t>(gsrc)), "r"(bytes), "r"(smem_u32(bar))
+      : "memory");
+}
+
+// Shared-memory descriptor of a contiguous [rows x 16 bytes] block without swizzle (8-row
+// core matrices 128 bytes apart): the source of a scale-factor copy into tensor memory.
+__device__ __forceinline__ uint64_t smem_desc_plain16(uint32_t saddr) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);   // start address, 16-byte units
+  d |= static_cast<uint64_t>(1) << 16;                    // leading byte offset (one column)
+  d |= static_cast<uint64_t>(128 >> 4) << 32;             // stride byte offset: 8 rows
+  d |= static_cast<uint64_t>(1) << 46;                    // descriptor version
+  return d;
+}
+
+// One thread: copy a 512-byte scale atom (32 rows x 16 bytes) into 4 TMEM columns at
+// `taddr`, replicated into all four 32-lane quarters.
+__device__ __forceinline__ void tc_cp_scale_atom(uint32_t taddr, uint64_t sdesc) {
+  asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
+               : "memory");
+}
+
+// Instruction descriptor of kind::mxf8f6f4 with UE8M0 scales: A E4M3 (format 0), B E4M3 (0)
+// or E2M1 (5), both K-major; `sf` selects the byte of each scale column (K block of 32
+// inside a 128-wide scale atom) for A (bits 29-30) and B (bits 4-5).
+__host__ __device__ constexpr uint32_t idesc_mx(int M, int N, int b_format, int sf) {
+  return (static_cast<uint32_t>(sf) << 4)           // B scale factor id
+         | (static_cast<uint32_t>(b_format) << 10)  // B format (A format 0: E4M3)
+         | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
+         | (1u << 23)                               // UE8M0 scales
+         | (static_cast<uint32_t>(M >> 4) << 24)    // M / 16
+         | (static_cast<uint32_t>(sf) << 29);       // A scale factor id
+}
+
+// D (M x N fp32 in TMEM) (+)= (A * scale_A) . (B * scale_B)^T over K = 32.
+__device__ __forceinline__ void tc_mma_mx(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc,
+                                          uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                          uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %6, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%4], "
+      "[%5], p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
       : "memory");
 }
 

@@ -95,6 +95,50 @@ int launch_tc_gemm(int mode, int bn, int mt, int kb, bool w8, int ar, const TcPr
 // tiles on CTA pairs (tc_pair.cu); p.max_tiles counts 256-row tiles.
 int launch_tc_pair_gemm(int mode, const TcProblem& p, cudaStream_t stream);
 
+// ---------------------------------------------------------------- block-scaled expert GEMMs
+// (tc_mx.cu) A: E4M3 codes [a_rows, k] with tile-atom scales `sfa` (mx_quant.cu); B: E4M3
+// codes [groups, n_rows, k] or E2M1 codes packed two per byte, scales in atoms
+// [groups][n_rows / 128][k / 128][512]. k % 128 == 0, n_rows % 128 == 0 (TC_SCALE: % 256).
+struct MxArgs {
+  int groups;
+  const int32_t* offsets;   // device [groups + 1] row offsets
+  int n;                    // output columns per group (TC_SWIGLU: d_ff; TC_SCALE: d)
+  int n_rows;               // rows of B per group (= n)
+  int k;                    // reduction length
+  const uint8_t* sfa;       // activation scale atoms
+  const uint8_t* sfb0;      // weight scale atoms of B0 (W1 or W2)
+  const uint8_t* sfb1;      //                     of B1 (W3)
+  uint8_t* out_codes;       // TC_SWIGLU: H codes [rows, n]
+  uint8_t* out_atoms;       //            H scale atoms (the same row tiles)
+  void* out_rows;           // TC_SCALE: bf16 [rows, ldo]
+  long long ldo;
+  const int32_t* perm;      // TC_SCALE gates: gate[perm[r]], or row_gate[r]
+  const float* gate;
+  const float* row_gate;
+  DeviceError* err;
+};
+struct MxProblem {
+  MxArgs args;
+  const void* a;
+  long long a_rows;
+  const void* b0;
+  const void* b1;
+  long long max_tiles;
+  int num_sms;
+};
+// mode TC_SWIGLU or TC_SCALE; ar: rows per tile (128, or 32 when no group has more than
+// 32 rows); bfmt: 0 = E4M3 weights, 5 = E2M1 weights.
+int launch_mx_gemm(int mode, int ar, int bfmt, const MxProblem& p, cudaStream_t stream);
+// E4M3 blocks of 32 of bf16 rows x [rows, K] (mx_quant.cu): codes [rows, K], scale bytes
+// [rows, K / 32] (s + 127), row-major.
+int launch_mx_quant_rows(const void* x, long long rows, int K, uint8_t* codes, uint8_t* scales,
+                         DeviceError* err, cudaStream_t stream);
+// The gathered rows Xq[r] = E4M3 blocks of x[perm[r] / k] for r < offsets[G], with the scales
+// in tile atoms of TM-row tiles.
+int launch_mx_gather_quant(const void* x, const int32_t* perm, const int32_t* offsets, int G,
+                           int k, int K, int TM, long long max_rows, uint8_t* codes,
+                           uint8_t* atoms, DeviceError* err, int num_sms, cudaStream_t stream);
+
 // ---------------------------------------------------------------- tcgen05 backward GEMMs
 enum BwdMode : int {
   BW_DGRAD_H = 0,  // dH = dY.W2 (B = W2 read MN-major) + SwiGLU backward and dgate partials

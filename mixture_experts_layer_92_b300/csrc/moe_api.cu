@@ -539,21 +539,170 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
   return MOE_OK;
 }
 
+// ---------------------------------------------------------------- block-scaled experts
+// Weights as E4M3 codes (fmt MOE_MX_E4M3) or E2M1 codes packed two per byte (MOE_MX_E2M1),
+// each with its scale atoms (tc_mx.cu).
+struct MxWeights {
+  int fmt;
+  const uint8_t *w1q, *w3q, *w2q;
+  const uint8_t *w1sf, *w3sf, *w2sf;
+};
+
+// The forward's layout, then the block-scaled operands: the gathered x rows as E4M3 codes
+// [R, d] with their scale atoms, and the hidden rows H as E4M3 codes [R, d_ff] with theirs.
+// Row tiles: at most R / 32 + E + 1 (32-row tiles; each expert adds at most one partial tile).
+struct MxLayout {
+  Layout f;
+  size_t xq, xsf, hq, hsf, total;
+};
+
+MxLayout layout_mx(const moe_shape* s) {
+  MxLayout M;
+  M.f = layout(s);
+  const size_t R = perm_rows(s), d = s->d, F = s->d_ff;
+  const size_t tiles = R / 32 + static_cast<size_t>(s->E) + 1;
+  size_t o = M.f.total;
+  auto take = [&](size_t bytes) {
+    const size_t at = o;
+    o = align_up(o + std::max<size_t>(bytes, 1));
+    return at;
+  };
+  M.xq = take(R * d);
+  M.xsf = take(tiles * (d / 128) * 512);
+  M.hq = take(R * F);
+  M.hsf = take(tiles * (F / 128) * 512);
+  M.total = o;
+  return M;
+}
+
+int check_mx_shape(const moe_shape* s, int fmt) {
+  if (fmt != MOE_MX_E4M3 && fmt != MOE_MX_E2M1)
+    return fail(MOE_ERR_INVALID, "block-scaled weight format %d unknown", fmt);
+  if (s->dtype != MOE_BF16)
+    return fail(MOE_ERR_UNSUPPORTED, "block-scaled weights need a bf16 layer");
+  if (s->d_ff_shared != 0)
+    return fail(MOE_ERR_UNSUPPORTED, "block-scaled weights: no shared expert supported");
+  if (expert_choice(s))
+    return fail(MOE_ERR_UNSUPPORTED, "block-scaled weights: top-k routing only");
+  if (s->d % 256 != 0 || s->d_ff % 128 != 0)
+    return fail(MOE_ERR_UNSUPPORTED,
+                "block-scaled weights need d a multiple of 256 and d_ff a multiple of 128");
+  return MOE_OK;
+}
+
+bool aligned32(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 31u) == 0; }
+
+int check_mx(const moe_shape* s, const MxWeights* m) {
+  TRY(check_mx_shape(s, m->fmt));
+  const uint8_t* q[3] = {m->w1q, m->w3q, m->w2q};
+  const uint8_t* sf[3] = {m->w1sf, m->w3sf, m->w2sf};
+  const char* qn[3] = {"w1q", "w3q", "w2q"};
+  const char* sn[3] = {"w1_scales", "w3_scales", "w2_scales"};
+  for (int i = 0; i < 3; ++i) {
+    REQUIRE_PTR(q[i], qn[i]);
+    if (m->fmt == MOE_MX_E2M1 && !aligned32(q[i]))
+      return fail(MOE_ERR_INVALID, "%s (4-bit codes) is not 32-byte aligned", qn[i]);
+    REQUIRE_PTR(sf[i], sn[i]);
+  }
+  return MOE_OK;
+}
+
+// Stages 3-5 on block-scaled experts: gather + quantize x, gate/up GEMM writing H as
+// block-scaled E4M3, down GEMM writing g * (H . W2^T) as bf16 rows.
+int run_experts_mx(const moe_shape* s, const void* x, const int32_t* perm, const int32_t* offsets,
+                   const float* gate, const MxWeights* m, void* y_perm, void* ws, cudaStream_t st,
+                   void* const* ev, int ev_first) {
+  const MxLayout M = layout_mx(s);
+  DeviceError* err = at<DeviceError>(ws, M.f.err);
+  const long long A = static_cast<long long>(perm_rows(s));
+  const int sms = num_sms();
+  const int max_group_rows = std::min(s->T, s->capacity);
+  const int ar = max_group_rows <= 32 ? 32 : 128;
+  const int bfmt = m->fmt == MOE_MX_E2M1 ? 5 : 0;
+  const long long kept_max = std::min<long long>(A, static_cast<long long>(s->E) * max_group_rows);
+  const long long row_tiles = (kept_max + ar - 1) / ar + s->E;
+  uint8_t* xq = at<uint8_t>(ws, M.xq);
+  uint8_t* xsf = at<uint8_t>(ws, M.xsf);
+  uint8_t* hq = at<uint8_t>(ws, M.hq);
+  uint8_t* hsf = at<uint8_t>(ws, M.hsf);
+  auto rec = [&](int i) {
+    if (ev && ev[i]) cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), st);
+  };
+
+  rec(ev_first);
+  LAUNCH(launch_mx_gather_quant(x, perm, offsets, s->E, s->k, s->d, ar, A, xq, xsf, err, sms, st),
+         "gather + block quantization");
+  rec(ev_first + 1);
+  {
+    MxProblem p{};
+    p.args.groups = s->E;
+    p.args.offsets = offsets;
+    p.args.n = s->d_ff;
+    p.args.n_rows = s->d_ff;
+    p.args.k = s->d;
+    p.args.sfa = xsf;
+    p.args.sfb0 = m->w1sf;
+    p.args.sfb1 = m->w3sf;
+    p.args.out_codes = hq;
+    p.args.out_atoms = hsf;
+    p.args.err = err;
+    p.a = xq;
+    p.a_rows = std::max(A, 1ll);
+    p.b0 = m->w1q;
+    p.b1 = m->w3q;
+    p.max_tiles = row_tiles * (s->d_ff / 128);
+    p.num_sms = sms;
+    LAUNCH(launch_mx_gemm(TC_SWIGLU, ar, bfmt, p, st), "gate/up GEMM (block-scaled)");
+  }
+  rec(ev_first + 2);
+  {
+    MxProblem p{};
+    p.args.groups = s->E;
+    p.args.offsets = offsets;
+    p.args.n = s->d;
+    p.args.n_rows = s->d;
+    p.args.k = s->d_ff;
+    p.args.sfa = hsf;
+    p.args.sfb0 = m->w2sf;
+    p.args.out_rows = y_perm;
+    p.args.ldo = s->d;
+    p.args.perm = perm;
+    p.args.gate = gate;
+    p.args.err = err;
+    p.a = hq;
+    p.a_rows = std::max(A, 1ll);
+    p.b0 = m->w2q;
+    p.max_tiles = row_tiles * (s->d / 256);
+    p.num_sms = sms;
+    LAUNCH(launch_mx_gemm(TC_SCALE, ar, bfmt, p, st), "down GEMM (block-scaled)");
+  }
+  return MOE_OK;
+}
+
 // Every argument check of the layer's forward, made on the host before anything is queued.
 int check_forward(const moe_shape* s, const void* x, const void* w_router, const float* router_bias,
                   const void* w1, const void* w3, const void* w2, const void* w1s, const void* w3s,
                   const void* w2s, const void* y, const int32_t* counts, const int32_t* dropped,
                   const float* losses, const void* ws, size_t ws_bytes, void* const* ev, int n_ev,
-                  const Fp8Weights* q) {
+                  const Fp8Weights* q, const MxWeights* mx = nullptr) {
   TRY(check_shape(s));
-  TRY(check_ws(s, ws, ws_bytes));
+  if (mx != nullptr) {
+    TRY(check_mx(s, mx));
+    TRY(check_ws(s, ws, ws_bytes));
+    const size_t need = layout_mx(s).total;
+    if (ws_bytes < need)
+      return fail(MOE_ERR_WORKSPACE, "workspace has %zu bytes, needs %zu (moe_mx_workspace_size)",
+                  ws_bytes, need);
+  } else {
+    TRY(check_ws(s, ws, ws_bytes));
+  }
   if (q != nullptr) TRY(check_fp8(s, q));
   if (ev != nullptr && n_ev != MOE_NUM_STAGES + 1)
     return fail(MOE_ERR_INVALID, "n_events = %d, expected %d", n_ev, MOE_NUM_STAGES + 1);
   if (s->T > 0) {
     REQUIRE_PTR(x, "x");
     REQUIRE_PTR(w_router, "w_router");
-    if (q == nullptr) {
+    if (q == nullptr && mx == nullptr) {
       REQUIRE_PTR(w1, "w1");
       REQUIRE_PTR(w3, "w3");
       REQUIRE_PTR(w2, "w2");
@@ -577,9 +726,9 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
                  const void* w2s, void* y, int32_t* counts, int32_t* dropped, float* losses,
                  void* ws, size_t ws_bytes, void* stream, void* const* ev, int n_ev,
                  float* select_bias = nullptr, float gamma = 0.f,
-                 const Fp8Weights* q = nullptr) {
+                 const Fp8Weights* q = nullptr, const MxWeights* mx = nullptr) {
   TRY(check_forward(s, x, w_router, router_bias, w1, w3, w2, w1s, w3s, w2s, y, counts, dropped,
-                    losses, ws, ws_bytes, ev, n_ev, q));
+                    losses, ws, ws_bytes, ev, n_ev, q, mx));
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   const Layout L = layout(s);
   DeviceError* err = at<DeviceError>(ws, L.err);
@@ -624,7 +773,9 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
                            at<int32_t>(ws, L.blk_hist), err, num_sms(), st),
            "dispatch");
   }
-  if (s->T > 0) {
+  if (s->T > 0 && mx != nullptr) {
+    TRY(run_experts_mx(s, x, perm, off, gate, mx, yp, ws, st, ev, 3));
+  } else if (s->T > 0) {
     TRY(run_experts(s, x, perm, off, ec ? nullptr : gate, ec ? gate : nullptr, w1, w3, w2, w1s,
                     w3s, w2s, yp, ys, ws, st, ev, 3, q));
   } else {
@@ -1692,4 +1843,38 @@ int moe_backward(const moe_shape* s, const void* x, const void* w_router, const 
                        ws, ws_bytes, stream, events, n_events);
 }
 
+
+size_t moe_mx_workspace_size(const moe_shape* s) {
+  if (check_shape(s) != MOE_OK) return 0;
+  return layout_mx(s).total;
+}
+
+int moe_forward_mx(const moe_shape* s, int fmt, const void* x, const void* w_router,
+                   const float* router_bias, const uint8_t* w1q, const uint8_t* w1_scales,
+                   const uint8_t* w3q, const uint8_t* w3_scales, const uint8_t* w2q,
+                   const uint8_t* w2_scales, void* y, int32_t* counts, int32_t* dropped,
+                   float* losses, void* ws, size_t ws_bytes, void* stream, void* const* events,
+                   int n_events) {
+  const MxWeights m{fmt, w1q, w3q, w2q, w1_scales, w3_scales, w2_scales};
+  return forward_impl(s, x, w_router, router_bias, nullptr, nullptr, nullptr, nullptr, nullptr,
+                      nullptr, y, counts, dropped, losses, ws, ws_bytes, stream, events,
+                      events ? n_events : 0, nullptr, 0.f, nullptr, &m);
+}
+
+int moe_mx_quantize(const void* x, int64_t rows, int32_t K, uint8_t* codes, uint8_t* scales,
+                    void* ws, void* stream) {
+  if (rows < 0) return fail(MOE_ERR_INVALID, "rows = %lld < 0", static_cast<long long>(rows));
+  if (K < 32 || K % 32 != 0) return fail(MOE_ERR_INVALID, "K = %d is not a positive multiple of 32", K);
+  if (rows > 0) {
+    REQUIRE_PTR(x, "x");
+    REQUIRE_PTR(codes, "codes");
+    if (scales == nullptr) return fail(MOE_ERR_INVALID, "scales is NULL");
+  }
+  if (ws != nullptr && (reinterpret_cast<uintptr_t>(ws) & (kAlign - 1)) != 0)
+    return fail(MOE_ERR_WORKSPACE, "workspace is not %zu-byte aligned", kAlign);
+  LAUNCH(launch_mx_quant_rows(x, rows, K, codes, scales, static_cast<DeviceError*>(ws),
+                              static_cast<cudaStream_t>(stream)),
+         "block quantization");
+  return ok();
+}
 }  // extern "C"

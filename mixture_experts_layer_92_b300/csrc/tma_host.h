@@ -114,4 +114,46 @@ inline bool encode_3d_f32_store(CUtensorMap* m, void* base, uint64_t inner, uint
          CUDA_SUCCESS;
 }
 
+// 2-D map over bytes [rows, inner] (8-bit codes): box = [box_rows, 128 bytes], 128-byte swizzle.
+inline bool encode_2d_u8_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                               uint32_t box_rows) {
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner};
+  cuuint32_t box[2] = {128, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return encoder_slot()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over bytes [groups, rows, inner]: box = [1, box_rows, 128 bytes], 128-byte swizzle.
+inline bool encode_3d_u8_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                               uint64_t groups, uint32_t box_rows) {
+  cuuint64_t dims[3] = {inner, rows, groups};
+  cuuint64_t strides[2] = {inner, inner * rows};
+  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encoder_slot()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D map over 4-bit values packed two per byte, [groups, rows, inner values]: each group of
+// 16 values (8 bytes) lands in 16 bytes of shared memory (8 empty), i.e. one byte per value
+// as the block-scaled MMA reads 4-bit operands; box = [1, box_rows, 128 values] (the
+// required inner box), 128-byte swizzle. inner % 128 == 0; base 32-byte aligned.
+inline bool encode_3d_e2m1_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
+                                 uint64_t groups, uint32_t box_rows) {
+  cuuint64_t dims[3] = {inner, rows, groups};
+  cuuint64_t strides[2] = {inner / 2, inner / 2 * rows};
+  cuuint32_t box[3] = {128, box_rows, 1};
+  cuuint32_t es[3] = {1, 1, 1};
+  return encoder_slot()(m, CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B, 3, const_cast<void*>(base), dims,
+                        strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 }  // namespace moe

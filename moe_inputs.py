@@ -147,3 +147,58 @@ def quantize_rows_e4m3(w: torch.Tensor):
     scale = wf.abs().amax(dim=-1).clamp_min(1e-12) / 448.0
     codes = (wf / scale.unsqueeze(-1)).to(torch.float8_e4m3fn).view(torch.uint8)
     return codes, scale.contiguous()
+
+
+_E2M1_MAGNITUDES = (0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0)
+
+
+def quantize_weights_mx(w: torch.Tensor, fmt: str = "e4m3", host_codes: bool = False) -> dict:
+    """Block-scaled expert weights: every 32 values along the last axis (K) share a power-of-two
+    scale 2^s with s the smallest integer such that the block maximum fits the element format
+    (448 for E4M3, 6 for E2M1); the elements are E4M3 codes (torch's float8_e4m3fn cast) or
+    E2M1 codes (the nearest of the 8 magnitudes). Input preparation only: any valid codes
+    would do.
+
+    Returns on w's device:
+      q  : E4M3 codes uint8 [E, N, K], or E2M1 codes packed two per byte [E, N, K / 2] (the even
+           K index in the low nibble);
+      sf : scale bytes s + 127 in 512-byte atoms [E, N / 128, K / 128, 512]: the scale of row n,
+           columns 32j.. at byte (n % 32) * 16 + ((n % 128) / 32) * 4 + j % 4 of atom
+           (n / 128, j / 4);
+    and with host_codes, the same weights as numpy arrays for the CPU oracle: codes [E, N, K]
+    (one code per value) and s [E, N, K / 32]."""
+    E, N, K = w.shape
+    assert N % 128 == 0 and K % 128 == 0
+    qmax = 448.0 if fmt == "e4m3" else 6.0
+    mags = torch.tensor(_E2M1_MAGNITUDES, device=w.device)
+    qs, sfs, codes_h, s_h = [], [], [], []
+    for e in range(E):                                 # one expert at a time: bounded memory
+        blocks = w[e].double().reshape(N, K // 32, 32)
+        amax = blocks.abs().amax(dim=-1)
+        s = torch.ceil(torch.log2(amax.clamp_min(1e-300) / qmax))
+        s = torch.where(amax > qmax * torch.exp2(s), s + 1, s)
+        s = torch.where(amax <= qmax * torch.exp2(s - 1), s - 1, s)
+        s = torch.where(amax > 0, s, torch.full_like(s, -127.0)).clamp(-127, 127)
+        scaled = (blocks / torch.exp2(s).unsqueeze(-1)).float()
+        del blocks
+        if fmt == "e4m3":
+            codes = scaled.to(torch.float8_e4m3fn).view(torch.uint8).reshape(N, K)
+            q = codes
+        else:
+            idx = torch.empty(scaled.shape, dtype=torch.uint8, device=w.device)
+            for r0 in range(0, N, 1024):
+                a = scaled[r0:r0 + 1024].abs().unsqueeze(-1)
+                idx[r0:r0 + 1024] = (a - mags).abs().argmin(dim=-1).to(torch.uint8)
+            codes = (idx | (torch.signbit(scaled).to(torch.uint8) << 3)).reshape(N, K)
+            q = (codes[:, 0::2] | (codes[:, 1::2] << 4)).contiguous()
+        b = (s + 127).to(torch.uint8)                               # [N, K / 32]
+        sfs.append(b.reshape(N // 128, 4, 32, K // 128, 4)          # n1, n0, ka, j
+                   .permute(0, 3, 2, 1, 4).reshape(N // 128, K // 128, 512).contiguous())
+        qs.append(q)
+        if host_codes:
+            codes_h.append(codes.cpu())
+            s_h.append(s.to(torch.int64).cpu())
+    out = dict(fmt=fmt, q=torch.stack(qs).contiguous(), sf=torch.stack(sfs).contiguous())
+    if host_codes:
+        out.update(codes=torch.stack(codes_h).numpy(), s=torch.stack(s_h).numpy())
+    return out
