@@ -64,7 +64,7 @@ def capacity(w):
     return w.T if w.cf is None else moe_capacity(w.cf, w.T, w.k, w.E)
 
 
-def algorithmic_work(w, R: int, touched: int, wb=None):
+def algorithmic_work(w, R: int, touched: int, wb=None, block_scales: bool = False):
     """FLOPs and bytes the method itself must compute and move for one forward.
 
     Layer: FLOPs = router 2*T*d*E + 6*d*d_ff per kept assignment (three GEMMs) + 6*d*d_ff_s
@@ -74,24 +74,28 @@ def algorithmic_work(w, R: int, touched: int, wb=None):
     experts + its rows in and out; down GEMM 2*R*d*d_ff FLOPs over W2 + rows; the
     bandwidth kernels their rows in and out."""
     es = 4 if w.dtype == "f32" else 2
-    wb = es if wb is None else wb          # bytes per routed-expert weight (1: 8-bit codes)
+    wb = es if wb is None else wb          # bytes per routed-expert weight (1: 8-bit, 0.5: 4-bit)
     T, d, E, F, Fs, k = w.T, w.d, w.E, w.d_ff, w.d_ff_shared, w.k
     flops_router = 2.0 * T * d * E
     flops_gateup = 4.0 * R * d * F + 4.0 * T * d * Fs
     flops_down = 2.0 * R * d * F + 2.0 * T * d * Fs
-    sc = 4.0 if wb != es else 0.0          # fp32 per-row scales of 8-bit weights
-    bytes_gateup = (touched * 2.0 * F * (d * wb + sc) + (R * d + R * F + (2.0 * Fs * d + T * d
-                                                                            + T * Fs)) * es)
-    bytes_down = (touched * 1.0 * d * (F * wb + sc) + (R * F + R * d + (Fs * d + T * Fs + T * d))
-                  * es)
+    # weight scales: one byte per 32 weights (block-scaled), or an fp32 per row (8-bit rows)
+    def wbytes(rows, K):
+        if block_scales:
+            return rows * K * (wb + 1.0 / 32)
+        return rows * (K * wb + (4.0 if wb != es else 0.0))
+    ab = 1.0 if block_scales else es       # bytes per activation element in the expert GEMMs
+    bytes_gateup = (touched * wbytes(2.0 * F, d) + R * d * ab + R * F * ab
+                    + (2.0 * Fs * d + T * d + T * Fs) * es)
+    bytes_down = touched * wbytes(1.0 * d, F) + R * F * ab + R * d * es + (Fs * d + T * Fs + T * d) * es
     bytes_total = ((T * d + E * d + 3.0 * d * Fs + T * d) * es
-                   + touched * (3.0 * d * F * wb + (2.0 * F + d) * sc))
+                   + touched * (wbytes(2.0 * F, d) + wbytes(1.0 * d, F)))
     return dict(flops=flops_router + flops_gateup + flops_down, bytes=bytes_total,
                 per_stage=dict(
                     router_gemm=(flops_router, (T * d + E * d) * es + T * E * 4.0),
                     gates_topk=(0.0, T * E * 4.0 + T * k * 8.0),
                     dispatch=(0.0, T * k * 4.0 * 3 + R * 4.0),
-                    gather=(0.0, 2.0 * R * d * es),
+                    gather=(0.0, R * d * (es + (ab + ab / 32 if block_scales else es))),
                     gemm_gateup_swiglu=(flops_gateup, bytes_gateup),
                     gemm_down_scale=(flops_down, bytes_down),
                     combine=(0.0, (R * d + T * d * (2 if Fs else 1)) * es),
@@ -380,10 +384,12 @@ def run_reference(args, w, rank):
 
 # ------------------------------------------------------------------------------ GPU arm
 def launches_per_forward(w) -> int:
-    # router, top-k, dispatch, gather, gate/up GEMM, down GEMM, combine, statistics + losses;
-    # the fp32 path launches the shared expert's two GEMMs separately; expert choice runs a
-    # selection and an unrouted-token count in place of the dispatch
-    n = 8 + (2 if (w.dtype == "f32" and w.d_ff_shared) else 0)
+    # router (bf16 with E <= 256: the fused router, which also routes; else the router GEMM
+    # and the top-k kernel), dispatch, gather, gate/up GEMM, down GEMM, combine, statistics +
+    # losses; the fp32 path launches the shared expert's two GEMMs separately; expert choice
+    # runs a selection and an unrouted-token count in place of the dispatch
+    fused = w.dtype == "bf16" and w.E <= 256
+    n = (7 if fused else 8) + (2 if (w.dtype == "f32" and w.d_ff_shared) else 0)
     return n + (1 if w.gate == "expert_choice" else 0)
 
 
@@ -405,10 +411,19 @@ def run_ours(args, w, rank, world, local_rank):
             fp8[nm + "q"], fp8[nm + "s"] = quantize_rows_e4m3(inp[nm])
             inp[nm] = None                         # only the 8-bit copy stays resident
         torch.cuda.empty_cache()
+    mx = None
+    if args.mx_weights:
+        from moe_inputs import quantize_weights_mx
+        mx = dict(fmt=args.mx_weights)
+        for nm in ("w1", "w3", "w2"):
+            qw = quantize_weights_mx(inp[nm], args.mx_weights)
+            mx[nm + "q"], mx[nm + "sf"] = qw["q"], qw["sf"]
+            inp[nm] = None                         # only the block-scaled copy stays resident
+        torch.cuda.empty_cache()
     layer = moe.MoELayer(inp["w_router"], inp["w1"], inp["w3"], inp["w2"], k=w.k, gate=w.gate,
                          capacity=C, router_bias=inp["router_bias"], w1s=inp["w1s"],
                          w3s=inp["w3s"], w2s=inp["w2s"], alpha=w.alpha, beta=w.beta, max_tokens=w.T,
-                         balance_gamma=args.balance_gamma, fp8=fp8)
+                         balance_gamma=args.balance_gamma, fp8=fp8, mx=mx)
     x = inp["x"]
     y = torch.empty_like(x)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -500,7 +515,9 @@ def run_ours(args, w, rank, world, local_rank):
             dist.destroy_process_group()
         return
     pk = peaks()
-    work = algorithmic_work(w, R, touched, wb=1 if args.fp8_weights else None)
+    wb = 1 if (args.fp8_weights or args.mx_weights == "e4m3") else (
+        0.5 if args.mx_weights == "e2m1" else None)
+    work = algorithmic_work(w, R, touched, wb=wb, block_scales=bool(args.mx_weights))
     tokens = w.T * args.steps * world
     value = whole_job_rate(w.T, args.steps, world, total_ms)
     ms_per_step = total_ms / args.steps
@@ -532,11 +549,12 @@ def run_ours(args, w, rank, world, local_rank):
                       note=f"max(FLOPs / {tpeak_name} peak, bytes / HBM peak), measured peaks")
     cpu = None
     report = None
-    if world == 1 and not args.no_cpu_baseline:
+    quantized = bool(args.fp8_weights or args.mx_weights)
+    if world == 1 and not args.no_cpu_baseline and not quantized:
         ih = host_inputs(inp)
         cpu = cpu_baseline(w, ih, target_s=args.cpu_seconds)
         if gpu_idx is not None:
-            report = routing_report(w, ih, gpu_idx, y, C, fp8=args.fp8_weights)
+            report = routing_report(w, ih, gpu_idx, y, C)
     es = x.element_size()
     line = dict(
         metric=METRIC, value=value, unit=UNIT, n_gpus=world, steps=args.steps,
@@ -810,6 +828,10 @@ def main(argv=None):
                          "(cf = 1 when the workload has none)")
     ap.add_argument("--fp8-weights", action="store_true",
                     help="8-bit (E4M3, per-row scale) routed expert weights (weight streaming)")
+    ap.add_argument("--mx-weights", default=None, choices=["e4m3", "e2m1"],
+                    help="block-scaled routed expert weights (one power-of-two scale per 32 "
+                         "values) on the block-scaled tensor-core MMAs; activations quantized "
+                         "to E4M3 blocks on the GPU")
     ap.add_argument("--tokens", type=int, default=None,
                     help="override the workload's token count (smaller cases for profiling)")
     ap.add_argument("--experts", type=int, default=None,
@@ -838,6 +860,8 @@ def main(argv=None):
         w = w.scaled(name=f"{w.name}+balanced")
     if args.fp8_weights:
         w = w.scaled(name=f"{w.name}+fp8w")
+    if args.mx_weights:
+        w = w.scaled(name=f"{w.name}+mx_{args.mx_weights}")
     if args.expert_choice:
         w = w.scaled(gate="expert_choice", cf=w.cf if w.cf is not None else 1.0,
                      name=f"{w.name}+expert_choice")

@@ -19,7 +19,8 @@ from ._lib import (MoeError, alloc_workspace, make_shape, moe_aux_loss, moe_capa
                    moe_route_topk_balanced, moe_route_topk_noalloc, moe_status_string,
                    moe_update_select_bias, moe_workspace_size, NUM_STAGES, STAGE_NAMES,
                    alloc_workspace_backward, moe_backward, moe_backward_workspace_size,
-                   moe_forward_host, HostPipeline)
+                   moe_forward_host, HostPipeline, alloc_workspace_mx, moe_forward_mx,
+                   moe_mx_quantize, moe_mx_workspace_size)
 
 
 class MoELayer:
@@ -32,18 +33,28 @@ class MoELayer:
 
     def __init__(self, w_router, w1, w3, w2, *, k: int, gate: str, capacity: Optional[int] = None,
                  router_bias=None, w1s=None, w3s=None, w2s=None, alpha=0.01, beta=1e-3,
-                 max_tokens: int, balance_gamma: Optional[float] = None, fp8: Optional[dict] = None):
+                 max_tokens: int, balance_gamma: Optional[float] = None, fp8: Optional[dict] = None,
+                 mx: Optional[dict] = None):
         E, d = w_router.shape
         self.w = dict(w_router=w_router, w1=w1, w3=w3, w2=w2, router_bias=router_bias,
                       w1s=w1s, w3s=w3s, w2s=w2s)
-        d_ff = (w1 if w1 is not None else fp8["w1q"]).shape[1]
+        if w1 is not None:
+            d_ff = w1.shape[1]
+        elif fp8 is not None:
+            d_ff = fp8["w1q"].shape[1]
+        else:
+            d_ff = mx["w1q"].shape[1]
         self.E, self.d, self.k, self.d_ff = E, d, k, d_ff
         self.d_ff_shared = 0 if w1s is None else w1s.shape[0]
         self.gate, self.capacity, self.alpha, self.beta = gate, capacity, alpha, beta
         self.dtype = w_router.dtype
         self.device = w_router.device
         self.max_tokens = max_tokens
-        self.ws = alloc_workspace(self.shape(max_tokens), device=self.device)
+        # block-scaled expert weights: dict(fmt, w1q, w1sf, w3q, w3sf, w2q, w2sf) (codes and
+        # scale atoms, see moe_forward_mx)
+        self.mx = mx
+        self.ws = (alloc_workspace_mx if mx is not None else alloc_workspace)(
+            self.shape(max_tokens), device=self.device)
         self.counts = torch.zeros(E, dtype=torch.int32, device=self.device)
         self.dropped = torch.zeros(1, dtype=torch.int32, device=self.device)
         self.losses = torch.zeros(2, dtype=torch.float32, device=self.device)
@@ -64,6 +75,13 @@ class MoELayer:
         T = x.shape[0]
         if y is None:
             y = torch.empty_like(x)
+        if self.mx is not None:
+            m = self.mx
+            moe_forward_mx(self.shape(T), self.ws, m["fmt"], x, self.w["w_router"], m["w1q"],
+                           m["w1sf"], m["w3q"], m["w3sf"], m["w2q"], m["w2sf"], y,
+                           router_bias=self.w["router_bias"], counts=self.counts,
+                           dropped=self.dropped, losses=self.losses, stream=stream, events=events)
+            return y
         if self.fp8 is not None:
             q = self.fp8
             moe_forward_fp8w(self.shape(T), self.ws, x, self.w["w_router"], q["w1q"], q["w1s"],
@@ -103,9 +121,9 @@ class MoELayer:
         stream and y (and, if losses_hosts is given, the batch's two losses) come back on its
         download stream, so the upload of batch i+1 and the download of batch i-1 overlap the
         layer on batch i. The current stream waits for every download. Returns after queuing
-        all work. (8-bit-weight and balanced layers copy through torch around their own
-        forward calls instead.)"""
-        if self.fp8 is not None or self.select_bias is not None:
+        all work. (8-bit-weight, block-scaled and balanced layers copy through torch around
+        their own forward calls instead.)"""
+        if self.fp8 is not None or self.mx is not None or self.select_bias is not None:
             return self._forward_host_stream_copies(x_hosts, y_hosts)
         comp = torch.cuda.current_stream(self.device)
         if getattr(self, "_host_pipe", None) is None:
@@ -168,7 +186,7 @@ class MoELayer:
         make this one moe_forward_host call (counts, dropped and losses then stay in the
         workspace; losses_host receives the losses); 8-bit and balanced layers copy through
         torch around their forward call."""
-        if self.fp8 is None and self.select_bias is None:
+        if self.fp8 is None and self.mx is None and self.select_bias is None:
             moe_forward_host(self.shape(x_host.shape[0]), self.ws, x_host, self.w["w_router"],
                              self.w["w1"], self.w["w3"], self.w["w2"], y_host, x_dev, y_dev,
                              router_bias=self.w["router_bias"], w1s=self.w["w1s"],
