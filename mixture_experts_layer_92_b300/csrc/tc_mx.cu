@@ -28,7 +28,8 @@
 //                  four lane quarters) and issues the four block-scaled MMAs. A stage's scale
 //                  columns are rewritten only after its data was refilled, i.e. after the
 //                  MMAs that read them completed;
-//   warps 2..5     epilogue (one 32-lane quarter of TMEM each).
+//   warps 2..9     epilogue: two warps per 32-lane quarter of TMEM, each taking every other
+//                  32-column chunk.
 // One accumulator of 256 columns (the scale columns take the rest of TMEM), so a tile's
 // epilogue does not overlap the next tile's MMAs. Every wait is bounded (common.cuh).
 #include <algorithm>
@@ -54,7 +55,7 @@ struct MxCfg {
   static constexpr int STAGE_BYTES = (A_BYTES + B_BYTES + SF_BYTES + 1023) / 1024 * 1024;
   static constexpr int STAGES_RAW = (200 * 1024) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
-  static constexpr int EPI_WARPS = 4;
+  static constexpr int EPI_WARPS = 8;
   static constexpr int THREADS = 64 + 32 * EPI_WARPS;
   static constexpr int TM = AR;                          // rows per tile
   static constexpr int BN_OUT = MODE == TC_SWIGLU ? 128 : 256;
@@ -179,6 +180,13 @@ tc_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
   const uint32_t tmem_base = *tmem_slot;
   const int total = s_pre[G];
   constexpr uint32_t SF_BASE = C::ACC_COLS;
+  // Balanced persistent grid: the fewest CTAs that keep the largest per-CTA tile count (e.g.
+  // 896 tiles on 148 SMs: 128 CTAs of 7 tiles, not 8 of 7 and 140 of 6 with a last round
+  // that streams on 8 SMs); the rest stay idle. The weight-streaming tiles are bound by the
+  // bytes each SM keeps in flight, so a full last round matters more than the idle SMs.
+  const int per_cta = (total + static_cast<int>(gridDim.x) - 1) / static_cast<int>(gridDim.x);
+  const int nctas = per_cta > 0 ? (total + per_cta - 1) / per_cta : 0;
+  const int first_tile = static_cast<int>(blockIdx.x) < nctas ? static_cast<int>(blockIdx.x) : total;
 
   if (warp == 0) {
     // ================= producer =================
@@ -190,7 +198,7 @@ tc_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
       int stage = 0;
       uint32_t phase = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x) {
+      for (int tile = first_tile; tile < total && ok; tile += nctas) {
         const MxTile t = mx_decode_tile<TM>(tile, s_off, s_pre, G, nt);
         const uint8_t* sfa = args.sfa + static_cast<size_t>(s_pt[t.group] + t.m) * ka * 512;
         const size_t nrow_atoms = static_cast<size_t>(args.n_rows / 128);   // weight atoms along N
@@ -241,7 +249,7 @@ tc_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
       uint32_t phase = 0;
       int it = 0;
       bool ok = true, issued_any = false;
-      for (int tile = blockIdx.x; tile < total && ok; tile += gridDim.x, ++it) {
+      for (int tile = first_tile; tile < total && ok; tile += nctas, ++it) {
         if (!mbar_wait_bounded(tempty_bar, (it & 1) ^ 1, abort_flag, err,
                                SITE_GEMM_WAIT_TMEM_EMPTY))
           break;
@@ -281,9 +289,10 @@ tc_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
   } else {
     // ================= epilogue (warps 2..5) =================
     const int quarter = warp & 3;
+    const int half = (warp - 2) >> 2;        // which of the two warps of this lane quarter
     const int r_local = quarter * 32 + lane;
     int it = 0;
-    for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
+    for (int tile = first_tile; tile < total; tile += nctas, ++it) {
       if (!mbar_wait_bounded(tfull_bar, it & 1, abort_flag, err, SITE_GEMM_WAIT_TMEM_FULL)) break;
       tc_fence_after();
       const MxTile t = mx_decode_tile<TM>(tile, s_off, s_pre, G, nt);
@@ -298,7 +307,7 @@ tc_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
                           (static_cast<size_t>(s_pt[t.group] + t.m) * (args.n / 128) + t.n_blk) * 512 +
                           (r_local & 31) * 16 + (r_local >> 5) * 4;
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = half; c < 4; c += 2) {
             uint32_t g[32], u[32];
             tmem_ld_32cols(tbase + c * 32, g);
             tmem_ld_32cols(tbase + 128 + c * 32, u);
@@ -345,7 +354,7 @@ tc_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
             else if (args.gate != nullptr) gscale = args.gate[args.perm[row]];
           }
 #pragma unroll 1
-          for (int c = 0; c < MX_BN / 32; ++c) {
+          for (int c = half; c < MX_BN / 32; c += 2) {
             uint32_t v[32];
             tmem_ld_32cols(tbase + c * 32, v);
             tmem_ld_wait();
