@@ -167,6 +167,28 @@ router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
   pdl_wait();
   pdl_launch_dependents();
 
+  if (warp >= 2) {
+    // Warps 2..15 wait for the MMAs anyway: they run the routing step once on no token (every
+    // slot invalid at run time, so it reads and writes nothing), which brings its code into
+    // the instruction cache. The routing code runs only a few times per CTA, and fetching it
+    // cold cost more than executing it.
+    float v[NT][J];
+    int t[NT];
+    bool valid[NT];
+#pragma unroll
+    for (int n = 0; n < NT; ++n) {
+      t[n] = 0;
+      valid[n] = a.T < 0;
+#pragma unroll
+      for (int j = 0; j < J; ++j) v[n][j] = static_cast<float>(lane + j);
+    }
+    RouteStats<J> none;
+    none.zero();
+    route_tokens<G, J, NT, FULL>(v, t, valid, a.T, a.E, a.k, a.gate_mode, a.select_bias,
+                                 a.probs_t, a.topk_idx, a.topk_gate, none, err,
+                                 SITE_ROUTE_NONFINITE);
+  }
+
   if (warp == 0) {
     if (lane == 0 && nk > 0) {
       // ================= TMA producer: the rest of the K slice =================
@@ -257,25 +279,75 @@ router_fused_kernel(const __grid_constant__ CUtensorMap tmX,
       const int r = base + gi * NT + n;
       t[n] = row0 + r;
       valid[n] = r < r_end && t[n] < a.T;
+    }
+    // the partial rows: rank 0's, then each further rank's added in order; every load of a
+    // rank is issued before the sums that use it
+    bool use[NT][J];
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
 #pragma unroll
       for (int j = 0; j < J; ++j) {
-        const int e = g + G * j;
+        use[n][j] = valid[n] && (FULL || g + G * j < a.E);
         v[n][j] = 0.f;
-        if (valid[n] && (FULL || e < a.E)) {
-          const float* src = part + r * C::PSTRIDE + e;
-          float acc;
-          if (a.cs == 1) {
-            acc = *src;
-          } else {
-            acc = ld_cluster_f32(src, 0);
-            for (int q = 1; q < a.cs; ++q) acc += ld_cluster_f32(src, q);
-          }
-          if (a.bias != nullptr) acc += __ldg(a.bias + e);
-          if (a.logits_out != nullptr) a.logits_out[static_cast<size_t>(t[n]) * a.E + e] = acc;
-          v[n][j] = acc;
+      }
+    const int r0 = base + gi * NT;
+    if (a.cs == 1) {
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+          if (use[n][j]) v[n][j] = part[(r0 + n) * C::PSTRIDE + g + G * j];
+    } else {
+#pragma unroll
+      for (int n = 0; n < NT; ++n)
+#pragma unroll
+        for (int j = 0; j < J; ++j)
+          if (use[n][j]) v[n][j] = ld_cluster_f32(part + (r0 + n) * C::PSTRIDE + g + G * j, 0);
+      if constexpr (NT * J <= 4) {
+        // few values per lane (small E, where the clusters are widest): every rank's loads
+        // go out before the first sum, so the ranks' latencies overlap
+        float w[8][NT][J];
+#pragma unroll
+        for (int q = 1; q < 8; ++q)
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+              w[q][n][j] = (q < a.cs && use[n][j])
+                               ? ld_cluster_f32(part + (r0 + n) * C::PSTRIDE + g + G * j, q)
+                               : 0.f;
+#pragma unroll
+        for (int q = 1; q < 8; ++q)
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+              if (q < a.cs) v[n][j] += w[q][n][j];
+      } else {
+        for (int q = 1; q < a.cs; ++q) {
+          float w[NT][J];
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int j = 0; j < J; ++j)
+              w[n][j] =
+                  use[n][j] ? ld_cluster_f32(part + (r0 + n) * C::PSTRIDE + g + G * j, q) : 0.f;
+#pragma unroll
+          for (int n = 0; n < NT; ++n)
+#pragma unroll
+            for (int j = 0; j < J; ++j) v[n][j] += w[n][j];
         }
       }
     }
+#pragma unroll
+    for (int n = 0; n < NT; ++n)
+#pragma unroll
+      for (int j = 0; j < J; ++j)
+        if (use[n][j]) {
+          const int e = g + G * j;
+          if (a.bias != nullptr) v[n][j] += __ldg(a.bias + e);
+          if (a.logits_out != nullptr) a.logits_out[static_cast<size_t>(t[n]) * a.E + e] = v[n][j];
+        }
     route_tokens<G, J, NT, FULL>(v, t, valid, a.T, a.E, a.k, a.gate_mode, a.select_bias,
                                  a.probs_t, a.topk_idx, a.topk_gate, st, err,
                                  SITE_ROUTE_NONFINITE);

@@ -117,3 +117,52 @@ def test_mx_rejects_unsupported_shapes():
     with pytest.raises(L.MoeError) as ei:
         L.moe_forward_mx(s, ws, "e4m3", x, x, dummy, dummy, dummy, dummy, dummy, dummy, x)
     assert ei.value.status == -2
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name,fmt", [("mixtral_decode", "e4m3"), ("mixtral_decode", "e2m1"),
+                                      ("switch_top1", "e4m3")])
+def test_mx_full_size_sampled(name, fmt):
+    """The block-scaled layer at full size, in the launch configuration bench.py times, on
+    sampled tokens that the oracle computes one expert at a time (weights decoded per expert),
+    on the GPU's routing of the whole batch; counts and drops over all tokens."""
+    w = WORKLOADS[name]
+    inp = make_inputs(w, device=DEV)
+    C = w.T if w.cf is None else O.capacity(w.cf, w.T, w.k, w.E)
+    mx = {nm: quantize_weights_mx(inp[nm], fmt, host_codes=True) for nm in ("w1", "w3", "w2")}
+    s = L.make_shape(w.T, w.d, w.E, w.k, w.d_ff, gate=w.gate, dtype=torch.bfloat16, capacity=C,
+                     alpha=w.alpha, beta=w.beta)
+    ws = L.alloc_workspace_mx(s, DEV)
+    y = torch.empty_like(inp["x"])
+    counts = torch.zeros(w.E, dtype=torch.int32, device=DEV)
+    dropped = torch.zeros(1, dtype=torch.int32, device=DEV)
+    L.moe_forward_mx(s, ws, fmt, inp["x"], inp["w_router"], mx["w1"]["q"], mx["w1"]["sf"],
+                     mx["w3"]["q"], mx["w3"]["sf"], mx["w2"]["q"], mx["w2"]["sf"], y,
+                     router_bias=inp["router_bias"], counts=counts, dropped=dropped)
+    idx = torch.empty(w.T, w.k, dtype=torch.int32, device=DEV)
+    gate = torch.empty(w.T, w.k, device=DEV)
+    L.moe_route_topk(s, ws, idx, gate, x=inp["x"], w_router=inp["w_router"],
+                     router_bias=inp["router_bias"])
+    torch.cuda.synchronize()
+    assert L.moe_get_error(ws) == 0
+    gidx = idx.cpu().numpy().astype(np.int64)
+    disp = O.dispatch(gidx, w.E, C)
+    np.testing.assert_array_equal(counts.cpu().numpy(), disp["counts"])
+    assert int(dropped.item()) == disp["dropped"]
+    bias = None if inp["router_bias"] is None else host64(inp["router_bias"])
+    x64 = host64(inp["x"])
+    logits = O.router_logits(x64, host64(inp["w_router"]), bias)
+    tokens = np.sort(np.random.default_rng(9).choice(w.T, size=min(w.T, 32), replace=False))
+    inv = disp["inv"].reshape(w.T, w.k)[tokens]
+    g = O.gates(logits[tokens], gidx[tokens], w.gate)
+    yref = np.zeros((len(tokens), w.d))
+    for e in np.unique(gidx[tokens][inv >= 0]):
+        W = {nm: O.mx_dequantize(mx[nm]["codes"][e], mx[nm]["s"][e], fmt) for nm in ("w1", "w3", "w2")}
+        tl, sl = np.nonzero((gidx[tokens] == e) & (inv >= 0))
+        rows = O.swiglu_ffn_mx(x64[tokens[tl]], W["w1"], W["w3"], W["w2"])
+        for i, (t, sidx) in enumerate(zip(tl, sl)):
+            yref[t] += g[t, sidx] * rows[i]
+    got = y[torch.as_tensor(tokens, device=DEV)].double().cpu().numpy()
+    err = rel_l2(got, yref)
+    print(f"{name} {fmt}: sampled rel L2 {err:.3e}, dropped {disp['dropped']}")
+    assert err < 2e-2
