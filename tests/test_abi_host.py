@@ -234,3 +234,44 @@ def test_noalloc_rejects_before_any_launch():
     assert call(fake, fake, fake, null, ec) == -2   # expert choice has no top-k step
     empty = shape(T=0)
     assert call(null, null, null, odd, empty) == -1  # checked even for an empty batch
+
+
+def test_block_scaled_entry_points_reject_before_any_launch():
+    """moe_forward_mx and moe_mx_quantize check shapes, formats and pointers on the host: no
+    CUDA call is made for these (so this runs without a GPU)."""
+    L = _lib.LIB
+    fake = ctypes.c_void_p(0x7f0000000000)
+    odd32 = ctypes.c_void_p(0x7f0000000010)         # 16- but not 32-byte aligned
+    null = ctypes.c_void_p(None)
+    s = shape(d=256, d_ff=256)
+    need = _lib.moe_mx_workspace_size(s)
+    assert need > moe.moe_workspace_size(s)         # the block-scaled operands come on top
+    def fwd(fmt=0, sh=s, w=(fake,) * 6, nbytes=need, ws=fake):
+        return L.moe_forward_mx(ctypes.byref(sh), fmt, fake, fake, null, *w, fake, null, null,
+                                null, ws, nbytes, null, None, 0)
+    assert fwd(fmt=7) == -1                         # unknown format
+    assert fwd(sh=shape(d=200, d_ff=256)) == -2     # d % 256
+    assert fwd(sh=shape(d=256, d_ff=200)) == -2     # d_ff % 128
+    assert fwd(sh=shape(d=256, d_ff=256, dtype=torch.float32)) == -2
+    assert fwd(sh=shape(d=256, d_ff=256, d_ff_shared=128)) == -2
+    assert fwd(sh=shape(d=256, d_ff=256, gate=3, capacity=16)) == -2   # expert choice
+    assert fwd(nbytes=need - 1) == -4               # the plain workspace is not enough
+    assert fwd(w=(null,) + (fake,) * 5) == -1       # missing codes
+    assert fwd(w=(fake, null) + (fake,) * 4) == -1  # missing scales
+    assert fwd(fmt=1, w=(odd32,) + (fake,) * 5) == -1   # 4-bit codes need 32-byte alignment
+    q = L.moe_mx_quantize
+    assert q(fake, 4, 100, fake, fake, null, null) == -1     # K not a multiple of 32
+    assert q(fake, -1, 64, fake, fake, null, null) == -1
+    assert q(null, 4, 64, fake, fake, null, null) == -1
+    assert q(fake, 4, 64, fake, null, null, null) == -1
+    assert q(fake, 4, 64, fake, fake, ctypes.c_void_p(0x7f0000000010), null) == -4
+    assert q(null, 0, 64, null, null, null, null) == 0       # nothing to do
+
+
+@pytest.mark.parametrize("T", [1, 64, 4096])
+def test_block_scaled_workspace_grows_with_the_layer(T):
+    a = _lib.moe_mx_workspace_size(shape(T=T, d=256, d_ff=256))
+    b = _lib.moe_mx_workspace_size(shape(T=T, d=512, d_ff=256))
+    c = _lib.moe_mx_workspace_size(shape(T=T, d=256, d_ff=512))
+    assert 0 < a < b and a < c
+    assert a % 256 == 0
