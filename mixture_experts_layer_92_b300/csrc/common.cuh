@@ -90,6 +90,9 @@ __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {
 // Largest finite fp16 value.
 constexpr float kF16Max = 65504.0f;
 
+// Dynamic shared memory one CTA may opt in to on sm_100-class GPUs (227 KB).
+constexpr int kMaxDynSmem = 227 * 1024;
+
 // Orders this thread's generic-proxy shared-memory writes before later async-proxy reads
 // (tensor-core operand fetches) of the same memory.
 __device__ __forceinline__ void fence_proxy_async_smem() {
@@ -268,12 +271,24 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* s
       "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* smem_src, int c0,
+                                             int c1) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(m)),
+      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
+      : "memory");
+}
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 // Wait until the issuing thread's bulk stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_group_read0() {
   asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+// ... all but the most recent bulk group (double-buffered staging).
+__device__ __forceinline__ void bulk_wait_group_read1() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 // Wait until the issuing thread's bulk stores are complete.
 __device__ __forceinline__ void bulk_wait_group0() {

@@ -64,7 +64,13 @@ struct TcArgs {
   void* gu_shared;          //   as bf16 [rows, 2N] (G in columns 0..N-1, U in N..2N-1); out_* may
                             //   then be nullptr (H not written)
   DeviceError* err;
+  int tma_out;              // set by launch_tc_gemm: bit 0 (routed) / bit 1 (shared) outputs
+                            //   leave through tensor stores
 };
+
+// Largest group count for which launch_tc_gemm takes mt = 2 (its tile table and store
+// staging then still fit in shared memory).
+constexpr int kTcMt2MaxGroups = 240;
 
 struct TcProblem {
   TcArgs args;

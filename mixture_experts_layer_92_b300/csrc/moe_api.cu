@@ -426,8 +426,9 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
   // 128-row tiles with double-buffered accumulators.
   const long long kept_max = std::min<long long>(A, static_cast<long long>(s->E) * max_group_rows);
   const bool w8 = q != nullptr;  // 8-bit weights: 128-row tiles only
-  const int mt_gateup = (!w8 && kept_max / s->E >= 512) ? 2 : 1;
-  const int mt_down = (!w8 && kept_max / s->E >= 512 && s->d_ff >= 8192) ? 2 : 1;
+  const bool mt2_ok = !w8 && s->E <= kTcMt2MaxGroups && kept_max / s->E >= 512;
+  const int mt_gateup = mt2_ok ? 2 : 1;
+  const int mt_down = (mt2_ok && s->d_ff >= 8192) ? 2 : 1;
   // 256-row tiles on CTA pairs (tc_pair.cu): both halves' accumulators double-buffered, but
   // a pair always multiplies 256 rows, where a single CTA skips the empty second half of a
   // group's last tile. So pairs only where the host knows every group's size and the last
@@ -1167,7 +1168,7 @@ int backward_impl(const moe_shape* s, const void* x, const void* w_router, const
     p.b1_s = w3s;
     p.b_rows_s = s->d_ff_shared;
     // the forward's row-tile policy: 256-row tiles when experts average >= 512 rows
-    const int mt_gu = (A / s->E >= 512) ? 2 : 1;
+    const int mt_gu = (A / s->E >= 512 && s->E <= kTcMt2MaxGroups) ? 2 : 1;
     const long long tm = 128ll * mt_gu;
     p.max_tiles = (static_cast<long long>((A + tm - 1) / tm) + static_cast<long long>(E)) *
                       ((s->d_ff + 127) / 128) +

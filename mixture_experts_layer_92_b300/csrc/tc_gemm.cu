@@ -96,10 +96,18 @@ struct Cfg {
   static constexpr int NUM_ACC = (MT == 1) ? 2 : 1;    // accumulator sets (double buffering)
   static constexpr uint32_t TMEM_COLS = pow2_at_least(NUM_ACC * MT * BN);
   static constexpr uint32_t IDESC = W8 ? idesc_f16_f32(BM, BN) : idesc_bf16_f32(BM, BN);
+  // epilogue chunk: output columns per TMEM read (SwiGLU: CW gate + CW up columns)
+  static constexpr int CW = (MODE == TC_SWIGLU && BN_OUT % 32 != 0) ? 16 : 32;
+  // 16-bit outputs leave through tensor stores: each epilogue warp stages 32 rows x CW
+  // columns (CW * 2-byte rows, swizzled like the output map) in one of two buffers
+  static constexpr int STG_ROW_BYTES = CW * 2;
+  static constexpr int STG_BUF = 32 * STG_ROW_BYTES;
+  static constexpr int STG_BYTES = (MODE == TC_F32OUT) ? 0 : EPI_WARPS * 2 * STG_BUF;
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int OFF_TILES = 0;
   static constexpr int OFF_CONV = STAGES * STAGE_BYTES;
-  static constexpr int OFF_BARS = OFF_CONV + CSTAGES * CSTAGE_BYTES;
+  static constexpr int OFF_STG = OFF_CONV + CSTAGES * CSTAGE_BYTES;
+  static constexpr int OFF_BARS = OFF_STG + STG_BYTES;
   // full, empty, tmem_full[2], tmem_empty[2], drain, converted[CSTAGES], conv_free[CSTAGES]
   static constexpr int NUM_BARS = 2 * STAGES + 5 + 2 * CSTAGES;
   static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;     // tmem slot, abort flag
@@ -117,6 +125,8 @@ struct Cfg {
   static_assert(AR == BM || (MT == 1 && AR % 8 == 0 && AR >= 8), "short row tiles: MT = 1");
   static_assert(STAGE_BYTES >= BM * BK * 2, "the MMA's 128-row A window stays in its stage");
   static_assert((CSTAGE_BYTES % 1024) == 0, "conversion slots stay 1024-byte aligned");
+  static_assert((STG_BUF % 1024) == 0, "staging buffers stay 1024-byte aligned (swizzle atoms)");
+  static_assert(smem_bytes(1) <= kMaxDynSmem, "shared memory");
 };
 
 struct Tile {
@@ -186,7 +196,9 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB1,
                        const __grid_constant__ CUtensorMap tmAs,
                        const __grid_constant__ CUtensorMap tmB0s,
-                       const __grid_constant__ CUtensorMap tmB1s, const TcArgs args) {
+                       const __grid_constant__ CUtensorMap tmB1s,
+                       const __grid_constant__ CUtensorMap tmO,
+                       const __grid_constant__ CUtensorMap tmOs, const TcArgs args) {
   using C = Cfg<MODE, BN, MT, KB, W8, AR>;
   constexpr int TM = C::TM;  // rows per CTA tile
   constexpr int BK = C::BK;
@@ -460,6 +472,35 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const int half = (warp - 2) >> 2;      // which 128-row half of the CTA tile
     const int quarter = warp & 3;          // TMEM lanes this warp may read: 32*quarter .. +31
     const int r_local = half * BM + quarter * 32 + lane;
+    // this warp's two staging buffers and the count of tensor stores it has issued
+    uint8_t* stg = smem + C::OFF_STG + (warp - 2) * 2 * C::STG_BUF;
+    uint32_t n_stores = 0;
+    // Rows leave through a tensor store when all 32 of the warp's rows belong to the tile:
+    // the box is then inside the group (a tile's rows past its group's end are the next
+    // expert's rows, so a partial block is stored row by row instead).
+    auto store_rows16 = [&](const CUtensorMap* map, const uint32_t* packed, int col0,
+                            long long row_first) {
+      uint8_t* buf = stg + (n_stores & 1) * C::STG_BUF;
+      if (n_stores >= 2) {
+        if (lane == 0) bulk_wait_group_read1();   // the store that last read `buf` is done
+        __syncwarp();
+      }
+      // row `lane`, 16-byte unit q at the position the map's swizzle expects: 64-byte rows
+      // q ^ (lane / 2 % 4), 32-byte rows q ^ (lane / 4 % 2)
+#pragma unroll
+      for (int q = 0; q < C::STG_ROW_BYTES / 16; ++q) {
+        const int pos = C::STG_ROW_BYTES == 64 ? (q ^ ((lane >> 1) & 3)) : (q ^ ((lane >> 2) & 1));
+        *reinterpret_cast<uint4*>(buf + lane * C::STG_ROW_BYTES + (pos << 4)) =
+            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map, buf, col0, static_cast<int>(row_first));
+        bulk_commit_group();
+      }
+      ++n_stores;
+    };
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const int acc = it % C::NUM_ACC;
@@ -480,11 +521,15 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                static_cast<uint32_t>((acc * MT + half) * BN);
         const int col_base = t.n_blk * C::BN_OUT;
 
+        const long long row_first = static_cast<long long>(t.row0) + half * BM + quarter * 32;
+        const bool whole_block = half * BM + quarter * 32 + 32 <= t.rows;
+        const bool tma_rows = whole_block && ((args.tma_out >> t.shared) & 1);
+        const CUtensorMap* omap = t.shared ? &tmOs : &tmO;
         if (MODE == TC_SWIGLU) {
           __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.shared ? args.out_shared
                                                                           : args.out_routed);
           // chunks of CW columns of H: gate columns [c*CW, +CW) and up columns BN/2 later
-          constexpr int CW = (C::BN_OUT % 32 == 0) ? 32 : 16;
+          constexpr int CW = C::CW;
 #pragma unroll 1
           for (int c = 0; c < C::BN_OUT / CW; ++c) {
             uint32_t g[CW], u[CW];
@@ -547,12 +592,16 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               }
               if (W8 && out_of_range)
                 record_error(args.err, MOE_ERR_NONFINITE, SITE_F16_RANGE_H, static_cast<int>(row));
-              __nv_bfloat16* dst = out + row * ldo + col0;
+              if (tma_rows) {
+                store_rows16(omap, packed, col0, row_first);
+              } else {
+                __nv_bfloat16* dst = out + row * ldo + col0;
 #pragma unroll
-              for (int q = 0; q < CW / 8; ++q)
-                if (col0 + q * 8 < N)
-                  *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
-                      packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                for (int q = 0; q < CW / 8; ++q)
+                  if (col0 + q * 8 < N)
+                    *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
+                        packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+              }
             }
           }
         } else if (MODE == TC_SCALE) {
@@ -583,12 +632,16 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               for (int i = 0; i < 16; ++i)
                 packed[i] = pack_bf16x2(gscale * __uint_as_float(v[2 * i]),
                                         gscale * __uint_as_float(v[2 * i + 1]));
-              __nv_bfloat16* dst = out + row * ldo + col0;
+              if (tma_rows) {
+                store_rows16(omap, packed, col0, row_first);
+              } else {
+                __nv_bfloat16* dst = out + row * ldo + col0;
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                if (col0 + q * 8 < N)
-                  *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
-                      packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                for (int q = 0; q < 4; ++q)
+                  if (col0 + q * 8 < N)
+                    *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
+                        packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+              }
             }
           }
         } else {  // TC_F32OUT
@@ -626,6 +679,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
     }
+    // this warp's tensor stores are complete before the CTA exits
+    if (lane == 0 && n_stores > 0) bulk_wait_group0();
   }
 
   // ---- teardown: all roles are done with TMEM before it is freed
@@ -673,27 +728,46 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
       return MOE_ERR_CUDA;
   }
 
+  // 16-bit outputs through tensor stores where the buffers allow (16-byte aligned base and
+  // row stride); otherwise the epilogue stores element-wise
+  TcArgs args = p.args;
+  args.tma_out = 0;
+  CUtensorMap mO{}, mOs{};
+  if (MODE != TC_F32OUT) {
+    if (encode_2d_out16(&mO, args.out_routed, args.n_routed, p.a_rows, args.ldo_routed, C::CW))
+      args.tma_out |= 1;
+    if (args.has_shared &&
+        encode_2d_out16(&mOs, args.out_shared, args.n_shared, args.m_shared, args.ldo_shared, C::CW))
+      args.tma_out |= 2;
+  }
+
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
   const int smem = C::smem_bytes(groups);
+  if (smem > kMaxDynSmem) return MOE_ERR_UNSUPPORTED;
   static std::once_flag attr_once[64];
   static bool attr_ok[64];
   if (dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   std::call_once(attr_once[dev], [&]() {
     attr_ok[dev] = cudaFuncSetAttribute(tc_grouped_gemm_kernel<MODE, BN, MT, KB, W8, AR>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        C::smem_bytes(kMaxGroups)) == cudaSuccess;
+                                        std::min(C::smem_bytes(kMaxGroups), kMaxDynSmem)) ==
+                   cudaSuccess;
   });
   if (!attr_ok[dev]) return MOE_ERR_CUDA;
 
   long long grid = std::min<long long>(p.max_tiles, p.num_sms);
   if (grid < 1) return MOE_OK;
   if (launch_pdl(tc_grouped_gemm_kernel<MODE, BN, MT, KB, W8, AR>, dim3(static_cast<int>(grid)),
-                 dim3(C::THREADS), smem, stream, mA, mB0, mB1, mAs, mB0s, mB1s,
-                 p.args) != cudaSuccess)
+                 dim3(C::THREADS), smem, stream, mA, mB0, mB1, mAs, mB0s, mB1s, mO, mOs,
+                 args) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
+
+static_assert(Cfg<TC_SWIGLU, 256, 2, 64>::smem_bytes(kTcMt2MaxGroups) <= kMaxDynSmem &&
+                  Cfg<TC_SCALE, 256, 2, 64>::smem_bytes(kTcMt2MaxGroups) <= kMaxDynSmem,
+              "256-row tiles fit up to kTcMt2MaxGroups groups");
 
 }  // namespace
 
