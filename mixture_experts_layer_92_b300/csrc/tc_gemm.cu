@@ -36,8 +36,11 @@
 //                  keeps two accumulators so the epilogue of tile i overlaps the MMAs of
 //                  i+1; MT = 2 uses all 512 columns for the two row halves;
 //   warps 2..      epilogue, 4 warps per row half: tcgen05.ld (each warp reads its 32-lane
-//                  quarter of TMEM), element-wise math, predicated 16-byte global stores
-//                  (rows past the group's end are masked: A tiles may straddle two experts);
+//                  quarter of TMEM), element-wise math, then a 16-bit output block of 32
+//                  rows x CW columns is staged in shared memory (swizzled, two buffers per
+//                  warp) and written by one TMA tensor store; a block that reaches past its
+//                  group's end (A tiles may straddle two experts) is stored row by row with
+//                  those rows masked;
 //   (W8) 8 warps   converters: E4M3 weight tile in the TMA ring -> fp16 tile in a separate
 //                  2-slot ring that the MMA reads, so the TMA ring holds only A and the
 //                  8-bit staging and keeps more weight bytes in flight. The conversion is

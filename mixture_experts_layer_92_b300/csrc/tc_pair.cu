@@ -20,7 +20,9 @@
 //                   of CTA 0 issues the M = 256 MMAs and commits to the empty and
 //                   accumulator-full barriers of both CTAs;
 //   warps 2..9      epilogue, two warps per TMEM lane quarter splitting the columns; each CTA
-//                   stores its 128 rows and arrives on CTA 0's accumulator-empty barrier.
+//                   stores its 128 rows (32-row blocks staged in shared memory and written
+//                   by TMA tensor stores, row by row where a block passes its group's end)
+//                   and arrives on CTA 0's accumulator-empty barrier.
 // Every mbarrier wait is bounded (2 s); the last step is a cluster barrier, so neither CTA
 // leaves while the other may still touch its shared memory or TMEM.
 #include <algorithm>
@@ -51,7 +53,11 @@ struct PCfg {
   static constexpr int BN_OUT = (MODE == TC_SWIGLU) ? BN / 2 : BN;
   static constexpr uint32_t TMEM_COLS = 2 * BN;        // two accumulators of BN columns
   static constexpr uint32_t IDESC = idesc_bf16_f32(2 * PBM, BN);
-  static constexpr int OFF_BARS = STAGES * STAGE_BYTES;
+  // tensor-store staging: one buffer of 32 rows x 32 bf16 columns (64-byte rows, swizzled
+  // like the output map) per epilogue warp
+  static constexpr int STG_BUF = 32 * 64;
+  static constexpr int OFF_STG = STAGES * STAGE_BYTES;
+  static constexpr int OFF_BARS = OFF_STG + EPI_WARPS * STG_BUF;
   // full[STAGES], empty[STAGES], tmem_full[2], tmem_empty[2], drain
   static constexpr int NUM_BARS = 2 * STAGES + 5;
   static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;     // tmem slot, abort flag
@@ -62,6 +68,7 @@ struct PCfg {
   static_assert(TMEM_COLS <= 512, "TMEM has 512 columns");
   static_assert(STAGE_BYTES % 1024 == 0, "stages stay 1024-byte aligned");
   static_assert(STAGES >= 4, "pipeline depth");
+  static_assert(smem_bytes(kPairMaxGroups) <= kMaxDynSmem, "shared memory");
 };
 
 struct PTile {
@@ -111,7 +118,9 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                     const __grid_constant__ CUtensorMap tmB1,
                     const __grid_constant__ CUtensorMap tmAs,
                     const __grid_constant__ CUtensorMap tmB0s,
-                    const __grid_constant__ CUtensorMap tmB1s, const TcArgs args) {
+                    const __grid_constant__ CUtensorMap tmB1s,
+                    const __grid_constant__ CUtensorMap tmO,
+                    const __grid_constant__ CUtensorMap tmOs, const TcArgs args) {
   using C = PCfg<MODE, BN>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -294,6 +303,30 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const int quarter = warp & 3;           // TMEM lanes this warp may read: 32*quarter .. +31
     const int chalf = (warp - 2) >> 2;      // which half of the tile's columns
     const int r_local = static_cast<int>(rank) * PBM + quarter * 32 + lane;  // row in the tile
+    // Full 32-row blocks leave through a tensor store from this warp's staging buffer (a
+    // block reaching past its group's end -- the next expert's rows -- row by row instead).
+    uint8_t* stg = smem + C::OFF_STG + (warp - 2) * C::STG_BUF;
+    uint32_t n_stores = 0;
+    auto store_rows16 = [&](const CUtensorMap* map, const uint32_t* packed, int col0,
+                            long long row_first) {
+      if (n_stores > 0) {
+        if (lane == 0) bulk_wait_group_read0();   // the previous store has read the buffer
+        __syncwarp();
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {   // 64-byte rows: 16-byte unit q at q ^ (lane / 2 % 4)
+        const int pos = q ^ ((lane >> 1) & 3);
+        *reinterpret_cast<uint4*>(stg + lane * 64 + (pos << 4)) =
+            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map, stg, col0, static_cast<int>(row_first));
+        bulk_commit_group();
+      }
+      ++n_stores;
+    };
     int it = 0;
     for (int tile = cl; tile < total; tile += ncl, ++it) {
       const int acc = it & 1;
@@ -312,6 +345,11 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                                static_cast<uint32_t>(acc * BN);
         const int col_base = t.n_blk * C::BN_OUT;
         constexpr int CPW = C::BN_OUT / 32 / 2;   // 32-column chunks per warp
+        const long long row_first =
+            static_cast<long long>(t.row0) + static_cast<int>(rank) * PBM + quarter * 32;
+        const bool tma_rows = static_cast<int>(rank) * PBM + quarter * 32 + 32 <= t.rows &&
+                              ((args.tma_out >> t.shared) & 1);
+        const CUtensorMap* omap = t.shared ? &tmOs : &tmO;
         if (MODE == TC_SWIGLU) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(t.shared ? args.out_shared
                                                                     : args.out_routed);
@@ -350,12 +388,16 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                 packed[i] = pack_bf16x2(
                     silu_fast(__uint_as_float(g[2 * i])) * __uint_as_float(u[2 * i]),
                     silu_fast(__uint_as_float(g[2 * i + 1])) * __uint_as_float(u[2 * i + 1]));
-              __nv_bfloat16* dst = out + row * ldo + col0;
+              if (tma_rows) {
+                store_rows16(omap, packed, col0, row_first);
+              } else {
+                __nv_bfloat16* dst = out + row * ldo + col0;
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                if (col0 + q * 8 < N)
-                  *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
-                      packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                for (int q = 0; q < 4; ++q)
+                  if (col0 + q * 8 < N)
+                    *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
+                        packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+              }
             }
           }
         } else {  // TC_SCALE
@@ -379,12 +421,16 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               for (int i = 0; i < 16; ++i)
                 packed[i] = pack_bf16x2(gscale * __uint_as_float(v[2 * i]),
                                         gscale * __uint_as_float(v[2 * i + 1]));
-              __nv_bfloat16* dst = out + row * ldo + col0;
+              if (tma_rows) {
+                store_rows16(omap, packed, col0, row_first);
+              } else {
+                __nv_bfloat16* dst = out + row * ldo + col0;
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                if (col0 + q * 8 < N)
-                  *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
-                      packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                for (int q = 0; q < 4; ++q)
+                  if (col0 + q * 8 < N)
+                    *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
+                        packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+              }
             }
           }
         }
@@ -393,6 +439,7 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
       __syncwarp();
       if (lane == 0) mbar_arrive_cluster(&tempty_bar[acc], 0);
     }
+    if (lane == 0 && n_stores > 0) bulk_wait_group0();   // stores complete before exit
   }
 
   // ---- teardown: both CTAs are done with each other's shared memory and TMEM
@@ -427,6 +474,15 @@ int launch_pair_impl(const TcProblem& p, cudaStream_t stream) {
       return MOE_ERR_CUDA;
   }
 
+  TcArgs args = p.args;
+  args.tma_out = 0;
+  CUtensorMap mO{}, mOs{};
+  if (encode_2d_out16(&mO, args.out_routed, args.n_routed, p.a_rows, args.ldo_routed, 32))
+    args.tma_out |= 1;
+  if (args.has_shared &&
+      encode_2d_out16(&mOs, args.out_shared, args.n_shared, args.m_shared, args.ldo_shared, 32))
+    args.tma_out |= 2;
+
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   auto kernel = tc_pair_gemm_kernel<MODE, BN>;
@@ -455,7 +511,7 @@ int launch_pair_impl(const TcProblem& p, cudaStream_t stream) {
   if (pairs < 1) return MOE_OK;
   const int smem = C::smem_bytes(groups);
   if (launch_pdl(kernel, dim3(static_cast<int>(2 * pairs)), dim3(C::THREADS), smem, stream, mA,
-                 mB0, mB1, mAs, mB0s, mB1s, p.args) != cudaSuccess)
+                 mB0, mB1, mAs, mB0s, mB1s, mO, mOs, args) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
