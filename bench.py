@@ -383,14 +383,19 @@ def run_reference(args, w, rank):
 
 
 # ------------------------------------------------------------------------------ GPU arm
-def launches_per_forward(w) -> int:
+def launches_per_forward(w, quantized=False) -> int:
     # router (bf16 with E <= 256: the fused router, which also routes; else the router GEMM
-    # and the top-k kernel), dispatch, gather, gate/up GEMM, down GEMM, combine, statistics +
-    # losses; the fp32 path launches the shared expert's two GEMMs separately; expert choice
-    # runs a selection and an unrouted-token count in place of the dispatch
+    # and the top-k kernel); top-k layers: dispatch (it also reduces the router statistics
+    # to the losses), gather, gate/up GEMM, down GEMM, combine -- none for top-1 bf16 layers
+    # without a shared expert, whose down projection writes y itself; the fp32 path launches
+    # the shared expert's two GEMMs separately; expert choice: a selection and an
+    # unrouted-token count in place of the dispatch, and the statistics kernel
     fused = w.dtype == "bf16" and w.E <= 256
-    n = (7 if fused else 8) + (2 if (w.dtype == "f32" and w.d_ff_shared) else 0)
-    return n + (1 if w.gate == "expert_choice" else 0)
+    n = (1 if fused else 2) + 3 + (2 if (w.dtype == "f32" and w.d_ff_shared) else 0)
+    if w.gate == "expert_choice":
+        return n + 2 + 1 + 1
+    direct = w.k == 1 and w.d_ff_shared == 0 and w.dtype == "bf16" and not quantized
+    return n + 1 + (0 if direct else 1)
 
 
 def run_ours(args, w, rank, world, local_rank):
@@ -576,7 +581,8 @@ def run_ours(args, w, rank, world, local_rank):
                       "the pipeline's upload stream, the layer on the compute stream, y -> pinned "
                       "host on its download stream; copies of neighbouring steps overlap the "
                       "layer); 8-bit and balanced layers copy through torch around the call"),
-        gpu_launches=(launches_per_forward(w) + (1 if args.balance_gamma is not None else 0))
+        gpu_launches=(launches_per_forward(w, quantized)
+                      + (1 if args.balance_gamma is not None else 0))
         * args.steps,
         clocks=dict(sm_mhz=clk["sm_mhz"], sm_max_mhz=clk["sm_max_mhz"], reasons=clk["reasons"],
                     samples=clk["samples"],

@@ -239,7 +239,11 @@ int moe_host_pipeline_destroy(moe_host_pipeline* p);
  * stream before stage i and events[MOE_NUM_STAGES] after the last one, so that each
  * stage's device time can be read with cudaEventElapsedTime. Stages: 0 router GEMM,
  * 1 gates + top-k, 2 dispatch, 3 gather, 4 gate/up GEMM + SwiGLU, 5 down GEMM + gate
- * scale, 6 combine, 7 balance losses. n_events must be MOE_NUM_STAGES + 1. A NULL entry
+ * scale, 6 combine, 7 balance losses. A stage that another one absorbs runs no kernel: the
+ * fused router (bf16, E <= 256) computes stage 1 in stage 0; for top-k layers the dispatch
+ * also reduces the router statistics to the losses (stage 7 empty); top-1 bf16 layers
+ * without a shared expert write y in the down projection's epilogue (stage 6 empty).
+ * n_events must be MOE_NUM_STAGES + 1. A NULL entry
  * records nothing at that boundary, so the kernels on either side of it still overlap (each
  * kernel's launch and set-up start during the previous one's tail); an event between two
  * kernels serialises them. */

@@ -18,10 +18,18 @@
 //      routed to its expert is base_b + its warp's prefix + the running count + the number
 //      of lower lanes in the piece with the same expert. rank < C -> kept at offsets[e] + rank.
 // Integer-only and order-preserving: the outputs are bit-exact and independent of nb.
+//
+// With the router's per-CTA statistics (partials [E+1][nbr]: sums of p_{t,i}, then of
+// lse^2) ceil((E+1)/32) more CTAs join the grid: while the others build the histogram they
+// reduce the partials to stats[E+1], one warp per row, and after the grid barrier the first
+// of them forms the two losses from the counts (the balance loss alpha * E * sum_i f_i P_i
+// and the z-loss beta * mean lse^2, same page, step 6). The arithmetic is route_stats.cuh's,
+// which moe_aux_loss also uses: the forward's losses equal that entry point's bit for bit.
 #include <algorithm>
 
 #include "common.cuh"
 #include "launchers.h"
+#include "route_stats.cuh"
 
 namespace moe {
 
@@ -59,11 +67,48 @@ __device__ __forceinline__ void grid_barrier(DeviceError* sync, unsigned nblocks
   __syncthreads();
 }
 
+// The statistics CTAs (see the header): CTA nb_assign + c reduces rows 32c .. 32c + 31 of
+// the partials (one warp per row, route_stats.cuh); after the grid barrier CTA nb_assign
+// forms the losses from the counts.
+__device__ void dispatch_loss_cta(const DispatchLoss& la, int E, int nb_assign,
+                                  const int32_t* __restrict__ blk_hist, int* s_mem,
+                                  DeviceError* err) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c = static_cast<int>(blockIdx.x) - nb_assign;
+  const int e = c * kDispWarps + warp;
+  if (e <= E) {
+    const float v = stats_row_sum_warp(la.partials + static_cast<size_t>(e) * la.nbr, la.nbr, lane);
+    if (lane == 0) la.stats[e] = v;
+  }
+  grid_barrier(err, gridDim.x);
+  if (c != 0) return;
+  int* s_tot = s_mem;   // [E]: assignments per expert (the dispatch's counts)
+  for (int i = threadIdx.x; i < E; i += kDispThreads) {
+    int total = 0, b = 0;
+    for (; b + 8 <= nb_assign; b += 8) {
+      int v[8];
+#pragma unroll
+      for (int u = 0; u < 8; ++u) v[u] = __ldcg(blk_hist + static_cast<size_t>(b + u) * E + i);
+#pragma unroll
+      for (int u = 0; u < 8; ++u) total += v[u];
+    }
+    for (; b < nb_assign; ++b) total += __ldcg(blk_hist + static_cast<size_t>(b) * E + i);
+    s_tot[i] = total;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    const double sum = balance_sum_warp(s_tot, la.stats, E, lane);
+    if (lane == 0)
+      write_losses(sum, __ldcg(la.stats + E), la.T, E, la.k, la.alpha, la.beta, la.losses);
+  }
+}
+
 __global__ void __launch_bounds__(kDispThreads)
-dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int chunk,
+dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int chunk, int nb_assign,
                 int32_t* __restrict__ counts, int32_t* __restrict__ offsets,
                 int32_t* __restrict__ perm, int32_t* __restrict__ inv,
-                int32_t* __restrict__ dropped, int32_t* __restrict__ blk_hist, DeviceError* err) {
+                int32_t* __restrict__ dropped, int32_t* __restrict__ blk_hist, DeviceError* err,
+                const DispatchLoss la) {
   extern __shared__ int s_mem[];
   int* hist = s_mem;                       // [kDispWarps][E]
   int* s_base = hist + kDispWarps * E;     // [E]
@@ -71,6 +116,10 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int chunk,
   int* s_wsum = s_off + E + 1;             // [kDispWarps]
   const int tid = threadIdx.x;
   pdl_launch_dependents();                 // the gather may start launching (it waits for us)
+  if (static_cast<int>(blockIdx.x) >= nb_assign) {
+    dispatch_loss_cta(la, E, nb_assign, blk_hist, s_mem, err);
+    return;
+  }
   const int lane = tid & 31;
   const int warp = tid >> 5;
   const unsigned lt_mask = (1u << lane) - 1u;
@@ -111,7 +160,7 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int chunk,
   // loaded at a time, so their L2 latencies overlap)
   for (int e = tid; e < E; e += kDispThreads) {
     int before = 0, total = 0;
-    const int nb = static_cast<int>(gridDim.x), me = static_cast<int>(blockIdx.x);
+    const int nb = nb_assign, me = static_cast<int>(blockIdx.x);
     int b = 0;
     for (; b + 8 <= nb; b += 8) {
       int c[8];
@@ -197,7 +246,15 @@ int dispatch_max_blocks(int num_sms) { return std::max(1, std::min(num_sms, 148)
 
 int launch_dispatch(const int32_t* topk_idx, int A, int E, int C, int32_t* counts,
                     int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dropped,
-                    int32_t* blk_hist, DeviceError* err, int num_sms, cudaStream_t stream) {
+                    int32_t* blk_hist, DeviceError* err, int num_sms, cudaStream_t stream,
+                    const DispatchLoss* loss) {
+  DispatchLoss la{};
+  const int extra = (loss != nullptr && loss->partials != nullptr) ? (E + 1 + kDispWarps - 1) / kDispWarps : 0;
+  if (extra) {
+    la = *loss;
+    if (la.nbr < 1 || la.stats == nullptr || la.losses == nullptr || la.T < 1 || la.k < 1)
+      return MOE_ERR_INVALID;
+  }
   const size_t smem =
       (static_cast<size_t>(kDispWarps) * E + E + E + 1 + kDispWarps) * sizeof(int);
   if (cudaFuncSetAttribute(dispatch_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -208,16 +265,18 @@ int launch_dispatch(const int32_t* topk_idx, int A, int E, int C, int32_t* count
           cudaSuccess ||
       per_sm < 1)
     return MOE_ERR_CUDA;
-  const int max_blocks = std::min(dispatch_max_blocks(num_sms), num_sms * per_sm);
+  // the statistics CTAs are co-resident too
+  const int max_blocks = std::min(dispatch_max_blocks(num_sms), num_sms * per_sm - extra);
+  if (max_blocks < 1) return MOE_ERR_CUDA;
   int chunk = kChunk;
   int nb = std::max(1, (A + chunk - 1) / chunk);
   if (nb > max_blocks) {
     chunk = ((A + max_blocks - 1) / max_blocks + kChunk - 1) / kChunk * kChunk;
     nb = std::max(1, (A + chunk - 1) / chunk);
   }
-  void* args[] = {const_cast<int32_t**>(&topk_idx), &A, &E, &C, &chunk, &counts, &offsets, &perm,
-                  &inv, &dropped, &blk_hist, &err};
-  if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(dispatch_kernel), dim3(nb),
+  void* args[] = {const_cast<int32_t**>(&topk_idx), &A, &E, &C, &chunk, &nb, &counts, &offsets,
+                  &perm, &inv, &dropped, &blk_hist, &err, &la};
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(dispatch_kernel), dim3(nb + extra),
                                   dim3(kDispThreads), args, smem, stream) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;

@@ -66,6 +66,8 @@ struct TcArgs {
   DeviceError* err;
   int tma_out;              // set by launch_tc_gemm: bit 0 (routed) / bit 1 (shared) outputs
                             //   leave through tensor stores
+  int scatter_rows;         // TC_SCALE, top-1 layers: routed row r is written at output row
+                            //   perm[r] (the token: the combine folded into the epilogue)
 };
 
 // Largest group count for which launch_tc_gemm takes mt = 2 (its tile table and store
@@ -295,10 +297,22 @@ int launch_aux_loss(const float* stats, const int32_t* counts, int T, int E, int
 // ---------------------------------------------------------------- dispatch
 // blk_hist: [dispatch_max_blocks(num_sms)][E] int32 scratch; err: the workspace header
 // (required: it also holds the grid-barrier words).
+// loss (optional): the router's per-CTA statistics partials [E+1][nbr]; ceil((E+1)/32)
+// more CTAs of the dispatch reduce them to stats[E+1] and write losses[2] from the counts
+// with launch_aux_loss's arithmetic (bit-identical results), replacing launch_stats_loss.
+struct DispatchLoss {
+  const float* partials;
+  int nbr;
+  float* stats;
+  int T, k;
+  float alpha, beta;
+  float* losses;
+};
 int dispatch_max_blocks(int num_sms);
 int launch_dispatch(const int32_t* topk_idx, int A, int E, int C, int32_t* counts,
                     int32_t* offsets, int32_t* perm, int32_t* inv, int32_t* dropped,
-                    int32_t* blk_hist, DeviceError* err, int num_sms, cudaStream_t stream);
+                    int32_t* blk_hist, DeviceError* err, int num_sms, cudaStream_t stream,
+                    const DispatchLoss* loss = nullptr);
 
 // ---------------------------------------------------------------- expert-choice routing
 // probs_t [E][T]; writes perm/row_gate [E*C'] (C' = min(C, T)), inv [T][E] (-1 = not chosen),
@@ -315,5 +329,9 @@ int launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, in
                   DeviceError* to_f16_err = nullptr);
 int launch_combine(int dtype, const void* yp, const int32_t* inv, const void* ys, void* y, int T,
                    int k, int d, int num_sms, cudaStream_t stream);
+// Top-1 layers with the combine folded into the down projection: Xp[inv[t]] = x[t] for kept
+// tokens, y[t] = 0 for dropped ones (inv[t] < 0); 16-bit rows of row_bytes (multiple of 16).
+int launch_gather_tokens(const void* x, const int32_t* inv, int T, int row_bytes, void* xp,
+                         void* y, int num_sms, cudaStream_t stream);
 
 }  // namespace moe

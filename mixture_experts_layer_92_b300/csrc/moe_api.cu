@@ -330,14 +330,26 @@ int check_fp8(const moe_shape* s, const Fp8Weights* q) {
   return MOE_OK;
 }
 
+// Top-1 bf16 layers without a shared expert (and not expert choice) need no combine: the
+// down projection's epilogue writes g * (H W2^T) of row r straight to y[perm[r]], and the
+// gather zeroes the rows of dropped tokens.
+bool combine_in_epilogue(const moe_shape* s) {
+  return s->k == 1 && !expert_choice(s) && s->d_ff_shared == 0 && s->dtype == MOE_BF16;
+}
+
 // Expert-choice layers pass row_gate (gate per row) and perm holding token indices; top-k
 // layers pass gate (per assignment, looked up through perm) and perm holding assignments.
 // q != nullptr: the routed expert weights are 8-bit (w1/w3/w2 are ignored).
+// inv and y non-null (combine_in_epilogue layers, bf16 weights): the layer's output is
+// written here directly (y_perm unused).
 int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const int32_t* offsets,
                 const float* gate, const float* row_gate, const void* w1, const void* w3,
                 const void* w2, const void* w1s, const void* w3s, const void* w2s, void* y_perm,
                 void* y_shared, void* ws, cudaStream_t st, void* const* ev, int ev_first,
-                const Fp8Weights* q = nullptr) {
+                const Fp8Weights* q = nullptr, const int32_t* inv = nullptr, void* y = nullptr) {
+  const bool direct = inv != nullptr && y != nullptr;
+  if (direct && (!combine_in_epilogue(s) || q != nullptr || gate == nullptr))
+    return fail(MOE_ERR_INVALID, "direct output needs a top-1 bf16 layer");
   const Layout L = layout(s);
   DeviceError* err = at<DeviceError>(ws, L.err);
   const int A = static_cast<int>(perm_rows(s));
@@ -355,9 +367,13 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
 
   // stage 3: gather
   rec(ev_first);
-  LAUNCH(launch_gather(x, perm, offsets, s->E, gather_k, static_cast<int>(s->d * esize(s)), A, xp,
-                       sms, st, q != nullptr ? err : nullptr),
-         "gather");
+  if (direct)
+    LAUNCH(launch_gather_tokens(x, inv, s->T, static_cast<int>(s->d * esize(s)), xp, y, sms, st),
+           "gather (token-major)");
+  else
+    LAUNCH(launch_gather(x, perm, offsets, s->E, gather_k, static_cast<int>(s->d * esize(s)), A,
+                         xp, sms, st, q != nullptr ? err : nullptr),
+           "gather");
 
   if (s->dtype == MOE_F32) {
     rec(ev_first + 1);
@@ -507,8 +523,9 @@ int run_experts(const moe_shape* s, const void* x, const int32_t* perm, const in
     p.args.offsets = offsets;
     p.args.n_routed = s->d;
     p.args.k_routed = s->d_ff;
-    p.args.out_routed = y_perm;
+    p.args.out_routed = direct ? y : y_perm;
     p.args.ldo_routed = s->d;
+    p.args.scatter_rows = direct ? 1 : 0;
     if (w8) p.args.scale0 = q->w2s;
     p.args.has_shared = shared;
     p.args.m_shared = s->T;
@@ -770,28 +787,36 @@ int forward_impl(const moe_shape* s, const void* x, const void* w_router, const 
                                 cnt, off, drp, st),
            "expert choice");
   } else {
+    // the statistics and losses ride along in one more CTA of the dispatch
+    DispatchLoss dl{partials, route_partials_from_x(s), stats, s->T, s->k, s->alpha, s->beta, los};
     LAUNCH(launch_dispatch(idx, s->T * s->k, s->E, s->capacity, cnt, off, perm, inv, drp,
-                           at<int32_t>(ws, L.blk_hist), err, num_sms(), st),
-           "dispatch");
+                           at<int32_t>(ws, L.blk_hist), err, num_sms(), st,
+                           s->T > 0 ? &dl : nullptr),
+           "dispatch (with the router statistics and losses)");
   }
+  // top-1 bf16 layers: the down projection writes y itself (no combine launch)
+  const bool direct = combine_in_epilogue(s) && q == nullptr && mx == nullptr;
   if (s->T > 0 && mx != nullptr) {
     TRY(run_experts_mx(s, x, perm, off, gate, mx, yp, ws, st, ev, 3));
   } else if (s->T > 0) {
     TRY(run_experts(s, x, perm, off, ec ? nullptr : gate, ec ? gate : nullptr, w1, w3, w2, w1s,
-                    w3s, w2s, yp, ys, ws, st, ev, 3, q));
+                    w3s, w2s, yp, ys, ws, st, ev, 3, q, direct ? inv : nullptr,
+                    direct ? y : nullptr));
   } else {
     rec(3);
     rec(4);
     rec(5);
   }
   rec(6);
-  LAUNCH(launch_combine(s->dtype, yp, inv, ys, y, s->T, ec ? s->E : s->k, s->d, num_sms(), st),
-         "combine");
+  if (!direct)
+    LAUNCH(launch_combine(s->dtype, yp, inv, ys, y, s->T, ec ? s->E : s->k, s->d, num_sms(), st),
+           "combine");
   rec(7);
   if (s->T > 0) {
-    LAUNCH(launch_stats_loss(partials, route_partials_from_x(s), s->E, stats, cnt, s->T, s->k, s->alpha,
-                             s->beta, los, err, st),
-           "router statistics and losses");
+    if (ec)
+      LAUNCH(launch_stats_loss(partials, route_partials_from_x(s), s->E, stats, cnt, s->T, s->k,
+                               s->alpha, s->beta, los, err, st),
+             "router statistics and losses");
   } else {
     LAUNCH(launch_aux_loss(stats, cnt, s->T, s->E, s->k, s->alpha, s->beta, los, st), "aux loss");
   }

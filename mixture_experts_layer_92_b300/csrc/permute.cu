@@ -2,7 +2,9 @@
 //
 // gather : Xp[r] = x[perm[r] / k] for the kept rows r < R = offsets[E] -- the tokens of each
 //          expert laid out as one contiguous batch ("Mixture of experts (MoE)", tirogla.com,
-//          How it works, step 4: each expert runs on its contiguous batch).
+//          How it works, step 4: each expert runs on its contiguous batch). For top-1 layers
+//          whose down projection writes y directly, a token-major form that also zeroes the
+//          rows of dropped tokens (step 5 with k = 1 is a copy, which the GEMM's epilogue does).
 // combine: y[t] = sum over slots s < k with inv[t*k+s] >= 0 of Yp[inv[t*k+s]] (+ S[t]),
 //          summed in slot order in fp32; a dropped assignment adds nothing (same page,
 //          step 5). Yp already carries the gate (applied in the down-projection epilogue).
@@ -44,6 +46,39 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm
       dst[i + 96] = d;
     }
     for (; i < nvec; i += 32) dst[i] = __ldg(src + i);
+  }
+}
+
+// Top-1 layers whose down projection writes y itself (its epilogue stores row r at token
+// perm[r]): one warp per token t, Xp[inv[t]] = x[t] for a kept token, y[t] = 0 for a dropped
+// one (the combine's result for a token with no kept assignment). Each y row is written
+// exactly once between this kernel and the GEMM.
+__global__ void __launch_bounds__(kMoveThreads)
+gather_tokens_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ inv, int T,
+                     int nvec, uint4* __restrict__ xp, uint4* __restrict__ y) {
+  pdl_wait();
+  pdl_launch_dependents();
+  const int lane = threadIdx.x & 31;
+  const int nw = gridDim.x * kMoveWarps;
+  for (int t = blockIdx.x * kMoveWarps + (threadIdx.x >> 5); t < T; t += nw) {
+    const int r = __ldg(inv + t);
+    if (r >= 0) {
+      const uint4* src = x + static_cast<size_t>(t) * nvec;
+      uint4* dst = xp + static_cast<size_t>(r) * nvec;
+      int i = lane;
+      for (; i + 96 < nvec; i += 128) {
+        const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
+                    d = __ldg(src + i + 96);
+        dst[i] = a;
+        dst[i + 32] = b;
+        dst[i + 64] = c;
+        dst[i + 96] = d;
+      }
+      for (; i < nvec; i += 32) dst[i] = __ldg(src + i);
+    } else {
+      uint4* dst = y + static_cast<size_t>(t) * nvec;
+      for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
   }
 }
 
@@ -199,6 +234,15 @@ int launch_gather(const void* x, const int32_t* perm, const int32_t* offsets, in
   return launch_pdl(gather_rows_kernel, dim3(grid_for_rows(max_rows, num_sms)), dim3(kMoveThreads),
                     0, stream, static_cast<const uint4*>(x), perm, offsets, E, k, row_bytes / 16,
                     static_cast<uint4*>(xp)) == cudaSuccess
+             ? MOE_OK : MOE_ERR_CUDA;
+}
+
+int launch_gather_tokens(const void* x, const int32_t* inv, int T, int row_bytes, void* xp,
+                         void* y, int num_sms, cudaStream_t stream) {
+  if (T <= 0) return MOE_OK;
+  return launch_pdl(gather_tokens_kernel, dim3(grid_for_rows(T, num_sms)), dim3(kMoveThreads), 0,
+                    stream, static_cast<const uint4*>(x), inv, T, row_bytes / 16,
+                    static_cast<uint4*>(xp), static_cast<uint4*>(y)) == cudaSuccess
              ? MOE_OK : MOE_ERR_CUDA;
 }
 

@@ -17,6 +17,7 @@
 
 #include "common.cuh"
 #include "launchers.h"
+#include "route_stats.cuh"
 #include "route_token.cuh"
 
 namespace moe {
@@ -96,31 +97,14 @@ route_topk_kernel(const float* __restrict__ logits, int nsplit, size_t split_str
   }
 }
 
-// Sum over the 256 threads of a block in double, in a fixed order (each warp a butterfly of
-// shuffles, then the 8 warp sums in warp order); the result is valid in thread 0.
-__device__ __forceinline__ double block_sum_256(double v, double* s_w) {
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
-  if ((threadIdx.x & 31) == 0) s_w[threadIdx.x >> 5] = v;
-  __syncthreads();
-  double t = 0.0;
-  if (threadIdx.x == 0)
-    for (int w = 0; w < 8; ++w) t += s_w[w];
-  __syncthreads();
-  return t;
-}
-
-// stats[e] = sum over the blocks b of partials[e][b]: one CTA per expert e, each thread sums
-// a fixed stride of blocks in double, then block_sum_256 (deterministic: the order depends
-// only on the block count).
+// stats[e] = sum over the blocks b of partials[e][b] (route_stats.cuh): one warp per row e,
+// eight rows per CTA.
 __global__ void __launch_bounds__(256)
 stats_reduce_kernel(const float* __restrict__ partials, int nb, int E, float* __restrict__ stats) {
-  __shared__ double s_w[8];
-  const int e = blockIdx.x;
-  double acc = 0.0;
-  for (int b = threadIdx.x; b < nb; b += 256) acc += partials[static_cast<size_t>(e) * nb + b];
-  acc = block_sum_256(acc, s_w);
-  if (threadIdx.x == 0) stats[e] = static_cast<float>(acc);
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
+  if (e > E) return;   // warp-uniform
+  const float v = stats_row_sum_warp(partials + static_cast<size_t>(e) * nb, nb, threadIdx.x & 31);
+  if ((threadIdx.x & 31) == 0) stats[e] = v;
 }
 
 // stats as stats_reduce_kernel, and the block that finishes last (a counter in the workspace
@@ -130,56 +114,39 @@ __global__ void __launch_bounds__(256)
 stats_loss_kernel(const float* __restrict__ partials, int nb, int E, float* __restrict__ stats,
                   const int32_t* __restrict__ counts, int T, int k, float alpha, float beta,
                   float* __restrict__ losses, DeviceError* hdr) {
-  __shared__ double s_w[8];
   __shared__ bool s_last;
-  const int e = blockIdx.x;
+  const int lane = threadIdx.x & 31;
+  const int e = blockIdx.x * 8 + (threadIdx.x >> 5);
   pdl_wait();
   pdl_launch_dependents();
-  double acc = 0.0;
-  for (int b = threadIdx.x; b < nb; b += 256) acc += partials[static_cast<size_t>(e) * nb + b];
-  acc = block_sum_256(acc, s_w);
-  if (threadIdx.x == 0) {
-    stats[e] = static_cast<float>(acc);
-    __threadfence();
-    s_last = atomicAdd(&hdr->done_count, 1u) == static_cast<unsigned>(E);
+  if (e <= E) {
+    const float v = stats_row_sum_warp(partials + static_cast<size_t>(e) * nb, nb, lane);
+    if (lane == 0) {
+      stats[e] = v;
+      __threadfence();
+    }
   }
   __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  acc = 0.0;
-  for (int i = threadIdx.x; i < E; i += blockDim.x)
-    acc += static_cast<double>(counts[i]) * static_cast<double>(__ldcg(stats + i));
-  acc = block_sum_256(acc, s_w);
   if (threadIdx.x == 0) {
-    const double Td = static_cast<double>(T);
-    losses[0] = static_cast<float>(static_cast<double>(alpha) * E * acc /
-                                   (Td * static_cast<double>(k) * Td));
-    losses[1] = static_cast<float>(static_cast<double>(beta) * __ldcg(stats + E) / Td);
+    __threadfence();
+    s_last = atomicAdd(&hdr->done_count, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (!s_last || threadIdx.x >= 32) return;
+  __threadfence();
+  const double sum = balance_sum_warp(counts, stats, E, lane);
+  if (lane == 0) {
+    write_losses(sum, __ldcg(stats + E), T, E, k, alpha, beta, losses);
     hdr->done_count = 0u;
   }
 }
 
-// losses[0] = alpha*E*sum_i (counts_i/(T*k)) * (stats_i/T); losses[1] = beta*stats[E]/T.
-// One block of 256 threads; the sum in stats_loss_kernel's order.
-__global__ void __launch_bounds__(256)
+// losses from stats and counts (route_stats.cuh): one warp.
+__global__ void __launch_bounds__(32)
 aux_loss_kernel(const float* __restrict__ stats, const int32_t* __restrict__ counts, int T, int E,
                 int k, float alpha, float beta, float* __restrict__ losses) {
-  __shared__ double s_w[8];
-  double acc = 0.0;
-  for (int i = threadIdx.x; i < E; i += blockDim.x)
-    acc += static_cast<double>(counts[i]) * static_cast<double>(stats[i]);
-  acc = block_sum_256(acc, s_w);
-  if (threadIdx.x == 0) {
-    if (T == 0) {
-      losses[0] = 0.f;
-      losses[1] = 0.f;
-    } else {
-      const double Td = static_cast<double>(T);
-      losses[0] = static_cast<float>(static_cast<double>(alpha) * E * acc /
-                                     (Td * static_cast<double>(k) * Td));
-      losses[1] = static_cast<float>(static_cast<double>(beta) * stats[E] / Td);
-    }
-  }
+  const double sum = balance_sum_warp(counts, stats, E, threadIdx.x);
+  if (threadIdx.x == 0) write_losses(sum, __ldcg(stats + E), T, E, k, alpha, beta, losses);
 }
 
 // Auxiliary-loss-free balancing: b_i += gamma if expert i got fewer than T*k/E assignments,
@@ -239,7 +206,7 @@ int launch_route_topk(const RouteArgs& a, cudaStream_t stream) {
 
 int launch_stats_reduce(const float* partials, int nblocks, int E, float* stats,
                         cudaStream_t stream) {
-  stats_reduce_kernel<<<E + 1, 256, 0, stream>>>(partials, nblocks, E, stats);
+  stats_reduce_kernel<<<(E + 1 + 7) / 8, 256, 0, stream>>>(partials, nblocks, E, stats);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
@@ -253,7 +220,7 @@ int launch_update_select_bias(const int32_t* counts, float* select_bias, int T, 
 int launch_stats_loss(const float* partials, int nblocks, int E, float* stats,
                       const int32_t* counts, int T, int k, float alpha, float beta, float* losses,
                       DeviceError* hdr, cudaStream_t stream) {
-  if (launch_pdl(stats_loss_kernel, dim3(E + 1), dim3(256), 0, stream, partials, nblocks, E, stats,
+  if (launch_pdl(stats_loss_kernel, dim3((E + 1 + 7) / 8), dim3(256), 0, stream, partials, nblocks, E, stats,
                  counts, T, k, alpha, beta, losses, hdr) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
@@ -261,7 +228,7 @@ int launch_stats_loss(const float* partials, int nblocks, int E, float* stats,
 
 int launch_aux_loss(const float* stats, const int32_t* counts, int T, int E, int k, float alpha,
                     float beta, float* losses, cudaStream_t stream) {
-  aux_loss_kernel<<<1, 256, 0, stream>>>(stats, counts, T, E, k, alpha, beta, losses);
+  aux_loss_kernel<<<1, 32, 0, stream>>>(stats, counts, T, E, k, alpha, beta, losses);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 

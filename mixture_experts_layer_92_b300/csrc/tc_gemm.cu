@@ -611,9 +611,15 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
           __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(t.shared ? args.out_shared
                                                                           : args.out_routed);
           float gscale = 1.0f;
+          long long orow = row;   // output row: the tile row, or its token (scatter_rows)
           if (rvalid && !t.shared) {
-            if (args.row_gate != nullptr) gscale = args.row_gate[row];
-            else if (args.gate != nullptr) gscale = args.gate[args.perm[row]];
+            if (args.row_gate != nullptr) {
+              gscale = args.row_gate[row];
+            } else if (args.gate != nullptr || args.scatter_rows) {
+              const int a = args.perm[row];
+              if (args.gate != nullptr) gscale = args.gate[a];
+              if (args.scatter_rows) orow = a;
+            }
           }
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
@@ -638,7 +644,7 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
               if (tma_rows) {
                 store_rows16(omap, packed, col0, row_first);
               } else {
-                __nv_bfloat16* dst = out + row * ldo + col0;
+                __nv_bfloat16* dst = out + orow * ldo + col0;
 #pragma unroll
                 for (int q = 0; q < 4; ++q)
                   if (col0 + q * 8 < N)
@@ -736,8 +742,12 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
   TcArgs args = p.args;
   args.tma_out = 0;
   CUtensorMap mO{}, mOs{};
+  if (MODE == TC_SCALE && args.scatter_rows && (args.perm == nullptr || args.row_gate != nullptr))
+    return MOE_ERR_INVALID;
   if (MODE != TC_F32OUT) {
-    if (encode_2d_out16(&mO, args.out_routed, args.n_routed, p.a_rows, args.ldo_routed, C::CW))
+    // routed rows scattered to their tokens are stored row by row
+    if (!args.scatter_rows &&
+        encode_2d_out16(&mO, args.out_routed, args.n_routed, p.a_rows, args.ldo_routed, C::CW))
       args.tma_out |= 1;
     if (args.has_shared &&
         encode_2d_out16(&mOs, args.out_shared, args.n_shared, args.m_shared, args.ldo_shared, C::CW))

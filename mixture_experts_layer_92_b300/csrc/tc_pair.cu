@@ -475,6 +475,7 @@ int launch_pair_impl(const TcProblem& p, cudaStream_t stream) {
   }
 
   TcArgs args = p.args;
+  if (args.scatter_rows) return MOE_ERR_UNSUPPORTED;   // rows stay in expert order here
   args.tma_out = 0;
   CUtensorMap mO{}, mOs{};
   if (encode_2d_out16(&mO, args.out_routed, args.n_routed, p.a_rows, args.ldo_routed, 32))
