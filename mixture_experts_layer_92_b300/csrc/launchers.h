@@ -124,6 +124,7 @@ struct MxArgs {
   const float* gate;
   const float* row_gate;
   DeviceError* err;
+  int tma_out;              // set by launch_mx_gemm: outputs leave through tensor stores
 };
 struct MxProblem {
   MxArgs args;

@@ -102,10 +102,11 @@ struct Cfg {
   // epilogue chunk: output columns per TMEM read (SwiGLU: CW gate + CW up columns)
   static constexpr int CW = (MODE == TC_SWIGLU && BN_OUT % 32 != 0) ? 16 : 32;
   // 16-bit outputs leave through tensor stores: each epilogue warp stages 32 rows x CW
-  // columns (CW * 2-byte rows, swizzled like the output map) in one of two buffers
+  // columns (CW * 2-byte rows, swizzled like the output map) in one of STG_BUFS buffers
   static constexpr int STG_ROW_BYTES = CW * 2;
   static constexpr int STG_BUF = 32 * STG_ROW_BYTES;
-  static constexpr int STG_BYTES = (MODE == TC_F32OUT) ? 0 : EPI_WARPS * 2 * STG_BUF;
+  static constexpr int STG_BUFS = 2;
+  static constexpr int STG_BYTES = (MODE == TC_F32OUT) ? 0 : EPI_WARPS * STG_BUFS * STG_BUF;
   // shared memory layout (offsets from a 1024-byte aligned base)
   static constexpr int OFF_TILES = 0;
   static constexpr int OFF_CONV = STAGES * STAGE_BYTES;
@@ -476,16 +477,19 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
     const int quarter = warp & 3;          // TMEM lanes this warp may read: 32*quarter .. +31
     const int r_local = half * BM + quarter * 32 + lane;
     // this warp's two staging buffers and the count of tensor stores it has issued
-    uint8_t* stg = smem + C::OFF_STG + (warp - 2) * 2 * C::STG_BUF;
+    uint8_t* stg = smem + C::OFF_STG + (warp - 2) * C::STG_BUFS * C::STG_BUF;
     uint32_t n_stores = 0;
     // Rows leave through a tensor store when all 32 of the warp's rows belong to the tile:
     // the box is then inside the group (a tile's rows past its group's end are the next
     // expert's rows, so a partial block is stored row by row instead).
     auto store_rows16 = [&](const CUtensorMap* map, const uint32_t* packed, int col0,
                             long long row_first) {
-      uint8_t* buf = stg + (n_stores & 1) * C::STG_BUF;
-      if (n_stores >= 2) {
-        if (lane == 0) bulk_wait_group_read1();   // the store that last read `buf` is done
+      uint8_t* buf = stg + (n_stores % C::STG_BUFS) * C::STG_BUF;
+      if (n_stores >= C::STG_BUFS) {
+        // the store that last read `buf` is done
+        if (lane == 0) {
+          if (C::STG_BUFS == 2) bulk_wait_group_read1(); else bulk_wait_group_read0();
+        }
         __syncwarp();
       }
       // row `lane`, 16-byte unit q at the position the map's swizzle expects: 64-byte rows

@@ -68,6 +68,16 @@ struct MxCfg {
   static constexpr int OFF_MISC = OFF_BARS + NUM_BARS * 8;
   static constexpr int OFF_TABLE = OFF_MISC + 16;        // offsets, tile prefix, row-tile prefix
   static constexpr int smem_bytes(int groups) { return 1024 + OFF_TABLE + 3 * (groups + 1) * 4; }
+  // tensor-store staging after the table, where it fits: one buffer per epilogue warp of 32
+  // rows x 32 outputs (H codes: 32-byte rows; bf16 rows: 64 bytes), swizzled like the map
+  static constexpr int STG_ROW_BYTES = MODE == TC_SWIGLU ? 32 : 64;
+  static constexpr int STG_BUF = 32 * STG_ROW_BYTES;
+  static constexpr int stg_offset(int groups) {
+    return (OFF_TABLE + 3 * (groups + 1) * 4 + 1023) / 1024 * 1024;
+  }
+  static constexpr int smem_bytes_stg(int groups) {
+    return 1024 + stg_offset(groups) + EPI_WARPS * STG_BUF;
+  }
   static_assert(AR == 128 || AR == 32, "128- or 32-row tiles");
   static_assert(STAGES >= 2, "at least two stages");
   static_assert(ACC_COLS + SF_COLS * STAGES <= 512, "TMEM holds the accumulator and the scales");
@@ -100,7 +110,8 @@ __device__ __forceinline__ MxTile mx_decode_tile(int tile, const int* s_off, con
 template <int MODE, int AR, int BFMT>
 __global__ void __launch_bounds__(MxCfg<MODE, AR>::THREADS, 1)
 tc_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                  const __grid_constant__ CUtensorMap tmB1, const MxArgs args) {
+                  const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmO,
+                  const MxArgs args) {
   using C = MxCfg<MODE, AR>;
   constexpr int TM = C::TM;
   extern __shared__ uint8_t smem_raw[];
@@ -291,92 +302,159 @@ tc_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
     const int quarter = warp & 3;
     const int half = (warp - 2) >> 2;        // which of the two warps of this lane quarter
     const int r_local = quarter * 32 + lane;
+    // Full 32-row blocks leave through a tensor store from this warp's staging buffer (a
+    // block reaching past its group's end -- the next expert's rows -- row by row instead).
+    uint8_t* stg = smem + C::stg_offset(G) + (warp - 2) * C::STG_BUF;
+    uint32_t n_stores = 0;
+    auto store_block = [&](const uint32_t* words, int col0, long long row_first) {
+      if (n_stores > 0) {
+        if (lane == 0) bulk_wait_group_read0();   // the previous store has read the buffer
+        __syncwarp();
+      }
+      // row `lane`, 16-byte unit q where the map's swizzle expects it: 64-byte rows
+      // q ^ (lane / 2 % 4), 32-byte rows q ^ (lane / 4 % 2)
+#pragma unroll
+      for (int q = 0; q < C::STG_ROW_BYTES / 16; ++q) {
+        const int pos = C::STG_ROW_BYTES == 64 ? (q ^ ((lane >> 1) & 3)) : (q ^ ((lane >> 2) & 1));
+        *reinterpret_cast<uint4*>(stg + lane * C::STG_ROW_BYTES + (pos << 4)) =
+            make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(&tmO, stg, col0, static_cast<int>(row_first));
+        bulk_commit_group();
+      }
+      ++n_stores;
+    };
     int it = 0;
     for (int tile = first_tile; tile < total; tile += nctas, ++it) {
       if (!mbar_wait_bounded(tfull_bar, it & 1, abort_flag, err, SITE_GEMM_WAIT_TMEM_FULL)) break;
       tc_fence_after();
       const MxTile t = mx_decode_tile<TM>(tile, s_off, s_pre, G, nt);
-      if (quarter * 32 < t.rows) {
-        const bool rvalid = r_local < t.rows;
-        const long long row = static_cast<long long>(t.row0) + r_local;
-        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
-        if (MODE == TC_SWIGLU) {
-          // H = silu(gate) * up for 128 columns, quantized in blocks of 32 to E4M3
-          uint8_t* hq = args.out_codes + row * args.n + t.n_blk * 128;
-          uint8_t* atom = args.out_atoms +
-                          (static_cast<size_t>(s_pt[t.group] + t.m) * (args.n / 128) + t.n_blk) * 512 +
-                          (r_local & 31) * 16 + (r_local >> 5) * 4;
-#pragma unroll 1
-          for (int c = half; c < 4; c += 2) {
-            uint32_t g[32], u[32];
-            tmem_ld_32cols(tbase + c * 32, g);
-            tmem_ld_32cols(tbase + 128 + c * 32, u);
+      const bool any = quarter * 32 < t.rows;   // warp-uniform
+      const uint32_t tbase = tmem_base + (static_cast<uint32_t>(quarter * 32) << 16);
+      constexpr int NCH = MODE == TC_SWIGLU ? 2 : 4;   // 32-column chunks: c = half + 2 j
+      // EARLY: this warp's share of the accumulator -- 32 rows x 128 values -- goes to
+      // registers first and the accumulator is released at once, so the next tile's MMAs run
+      // under the element-wise math and the stores (measured faster for the SwiGLU epilogue
+      // with 4-bit weights only; elsewhere the extra registers spill and it is slower).
+      // Otherwise each chunk is read just before its math and the accumulator is released
+      // after the last one.
+      constexpr bool EARLY = MODE == TC_SWIGLU && BFMT == 5;
+      constexpr int NLD = EARLY ? NCH : 1;             // chunks held in registers at once
+      uint32_t v0[NLD][32], v1[MODE == TC_SWIGLU ? NLD : 1][32];
+      auto load_chunk = [&](int c, uint32_t (&a)[32], uint32_t (&b)[32]) {
+        tmem_ld_32cols(tbase + c * 32, a);                              // gate, or the output
+        if (MODE == TC_SWIGLU) tmem_ld_32cols(tbase + 128 + c * 32, b); // up
+      };
+      auto release = [&]() {
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(tempty_bar);
+      };
+      if (EARLY) {
+        if (any) {
+#pragma unroll
+          for (int j = 0; j < NLD; ++j) load_chunk(half + 2 * j, v0[j], v1[MODE == TC_SWIGLU ? j : 0]);
+          tmem_ld_wait();
+        }
+        release();
+      }
+      if (!any) {
+        if (!EARLY) release();
+        continue;
+      }
+      const bool rvalid = r_local < t.rows;
+      const long long row = static_cast<long long>(t.row0) + r_local;
+      const long long row_first = static_cast<long long>(t.row0) + quarter * 32;
+      const bool tma_rows = args.tma_out && quarter * 32 + 32 <= t.rows;   // warp-uniform
+      if (MODE == TC_SWIGLU) {
+        // H = silu(gate) * up for 128 columns, quantized in blocks of 32 to E4M3
+        uint8_t* hq = args.out_codes + row * args.n + t.n_blk * 128;
+        uint8_t* atom = args.out_atoms +
+                        (static_cast<size_t>(s_pt[t.group] + t.m) * (args.n / 128) + t.n_blk) * 512 +
+                        (r_local & 31) * 16 + (r_local >> 5) * 4;
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          const int c = half + 2 * j;
+          const int jl = EARLY ? j : 0;
+          if (!EARLY) {
+            load_chunk(c, v0[0], v1[0]);
             tmem_ld_wait();
-            if (rvalid) {
-              float h[32];
-#pragma unroll
-              for (int i = 0; i < 32; ++i)
-                h[i] = silu_fast(__uint_as_float(g[i])) * __uint_as_float(u[i]);
-              float amax = 0.f;
-#pragma unroll
-              for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
-              if (!isfinite(amax)) {
-                record_error(err, MOE_ERR_NONFINITE, SITE_MX_NONFINITE_H, static_cast<int>(row));
-                amax = 0.f;
-              }
-              int s = -127;
-              if (amax > 0.f) {
-                int e;
-                const float f = frexpf(amax, &e);
-                s = max(-127, min(127, e - 9 + (f > 0.875f ? 1 : 0)));
-              }
-              const float mul = __int_as_float((127 - s) << 23);
-              uint32_t w[8];
-#pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                uint16_t a2, b2;
-                asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
-                    : "=h"(a2) : "f"(h[4 * i + 1] * mul), "f"(h[4 * i] * mul));
-                asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
-                    : "=h"(b2) : "f"(h[4 * i + 3] * mul), "f"(h[4 * i + 2] * mul));
-                w[i] = static_cast<uint32_t>(a2) | (static_cast<uint32_t>(b2) << 16);
-              }
-              *reinterpret_cast<uint4*>(hq + c * 32) = make_uint4(w[0], w[1], w[2], w[3]);
-              *reinterpret_cast<uint4*>(hq + c * 32 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
-              atom[c] = static_cast<uint8_t>(s + 127);
-            }
           }
-        } else {
-          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out_rows);
-          float gscale = 1.0f;
+          uint32_t w[8];
+          int s = -127;
           if (rvalid) {
-            if (args.row_gate != nullptr) gscale = args.row_gate[row];
-            else if (args.gate != nullptr) gscale = args.gate[args.perm[row]];
-          }
-#pragma unroll 1
-          for (int c = half; c < MX_BN / 32; c += 2) {
-            uint32_t v[32];
-            tmem_ld_32cols(tbase + c * 32, v);
-            tmem_ld_wait();
-            if (rvalid) {
-              uint32_t packed[16];
+            float h[32];
 #pragma unroll
-              for (int i = 0; i < 16; ++i)
-                packed[i] = pack_bf16x2(gscale * __uint_as_float(v[2 * i]),
-                                        gscale * __uint_as_float(v[2 * i + 1]));
-              __nv_bfloat16* dst = out + row * args.ldo + t.n_blk * 256 + c * 32;
+            for (int i = 0; i < 32; ++i)
+              h[i] = silu_fast(__uint_as_float(v0[jl][i])) * __uint_as_float(v1[jl][i]);
+            float amax = 0.f;
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
-                    packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(h[i]));
+            if (!isfinite(amax)) {
+              record_error(err, MOE_ERR_NONFINITE, SITE_MX_NONFINITE_H, static_cast<int>(row));
+              amax = 0.f;
             }
+            if (amax > 0.f) {
+              int e;
+              const float f = frexpf(amax, &e);
+              s = max(-127, min(127, e - 9 + (f > 0.875f ? 1 : 0)));
+            }
+            const float mul = __int_as_float((127 - s) << 23);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              uint16_t a2, b2;
+              asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+                  : "=h"(a2) : "f"(h[4 * i + 1] * mul), "f"(h[4 * i] * mul));
+              asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;"
+                  : "=h"(b2) : "f"(h[4 * i + 3] * mul), "f"(h[4 * i + 2] * mul));
+              w[i] = static_cast<uint32_t>(a2) | (static_cast<uint32_t>(b2) << 16);
+            }
+          }
+          if (tma_rows) {
+            store_block(w, t.n_blk * 128 + c * 32, row_first);
+          } else if (rvalid) {
+            *reinterpret_cast<uint4*>(hq + c * 32) = make_uint4(w[0], w[1], w[2], w[3]);
+            *reinterpret_cast<uint4*>(hq + c * 32 + 16) = make_uint4(w[4], w[5], w[6], w[7]);
+          }
+          if (rvalid) atom[c] = static_cast<uint8_t>(s + 127);
+        }
+      } else {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(args.out_rows);
+        float gscale = 1.0f;
+        if (rvalid) {
+          if (args.row_gate != nullptr) gscale = args.row_gate[row];
+          else if (args.gate != nullptr) gscale = args.gate[args.perm[row]];
+        }
+#pragma unroll
+        for (int j = 0; j < NCH; ++j) {
+          const int c = half + 2 * j;
+          const int jl = EARLY ? j : 0;
+          if (!EARLY) {
+            load_chunk(c, v0[0], v1[0]);
+            tmem_ld_wait();
+          }
+          uint32_t packed[16];
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            packed[i] = pack_bf16x2(gscale * __uint_as_float(v0[jl][2 * i]),
+                                    gscale * __uint_as_float(v0[jl][2 * i + 1]));
+          if (tma_rows) {
+            store_block(packed, t.n_blk * 256 + c * 32, row_first);
+          } else if (rvalid) {
+            __nv_bfloat16* dst = out + row * args.ldo + t.n_blk * 256 + c * 32;
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+              *reinterpret_cast<uint4*>(dst + q * 8) = make_uint4(
+                  packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
           }
         }
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(tempty_bar);
+      if (!EARLY) release();
     }
+    if (lane == 0 && n_stores > 0) bulk_wait_group0();   // stores complete before exit
   }
 
   tc_fence_before();
@@ -411,15 +489,29 @@ int launch_mx_impl(const MxProblem& p, cudaStream_t stream) {
   auto kernel = tc_mx_gemm_kernel<MODE, AR, BFMT>;
   static std::once_flag once[64];
   static bool attr_ok[64];
+  // the outputs through tensor stores when the staging fits beside this layer's tile table
+  MxArgs args = p.args;
+  CUtensorMap mO{};
+  args.tma_out = 0;
+  int smem = C::smem_bytes(G);
+  if (C::smem_bytes_stg(G) <= kMaxDynSmem) {
+    const bool enc = MODE == TC_SWIGLU
+                         ? encode_2d_out8(&mO, args.out_codes, args.n, p.a_rows, args.n)
+                         : encode_2d_out16(&mO, args.out_rows, args.n, p.a_rows, args.ldo, 32);
+    if (enc) {
+      args.tma_out = 1;
+      smem = C::smem_bytes_stg(G);
+    }
+  }
   std::call_once(once[dev], [&]() {
     attr_ok[dev] = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        C::smem_bytes(MX_MAX_GROUPS)) == cudaSuccess;
+                                        kMaxDynSmem) == cudaSuccess;
   });
   if (!attr_ok[dev]) return MOE_ERR_CUDA;
   const long long grid = std::min<long long>(p.max_tiles, p.num_sms);
   if (grid < 1) return MOE_OK;
-  if (launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS), C::smem_bytes(G),
-                 stream, mA, mB0, mB1, p.args) != cudaSuccess)
+  if (launch_pdl(kernel, dim3(static_cast<unsigned>(grid)), dim3(C::THREADS), smem, stream, mA,
+                 mB0, mB1, mO, args) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }

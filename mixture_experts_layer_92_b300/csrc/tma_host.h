@@ -134,6 +134,22 @@ inline bool encode_2d_out16(CUtensorMap* m, void* base, uint64_t cols, uint64_t 
          CUDA_SUCCESS;
 }
 
+// 2-D map for tensor stores of 8-bit codes [rows, cols] (row stride ld bytes): box = [32 rows,
+// 32 bytes], 32-byte swizzle. False when the base or the row stride is not 16-byte aligned.
+inline bool encode_2d_out8(CUtensorMap* m, void* base, uint64_t cols, uint64_t rows, uint64_t ld) {
+  if (base == nullptr || (reinterpret_cast<uintptr_t>(base) & 15) != 0 || ld % 16 != 0 ||
+      cols == 0 || rows == 0 || cols > ld)
+    return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {ld};
+  cuuint32_t box[2] = {32, 32};
+  cuuint32_t es[2] = {1, 1};
+  return encoder_slot()(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, base, dims, strides, box, es,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_32B,
+                        CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 // 2-D map over bytes [rows, inner] (8-bit codes): box = [box_rows, 128 bytes], 128-byte swizzle.
 inline bool encode_2d_u8_sw128(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows,
                                uint32_t box_rows) {
