@@ -156,3 +156,23 @@ def test_routing_report_on_the_oracle_itself():
     idx[t] = [e for e in range(w.E) if e not in idx[t]][:w.k]
     rep = bench.routing_report(w, ih, idx, y, C)
     assert rep["routed_differently"] == 1
+
+
+def test_launches_per_forward_follow_the_layer_structure():
+    """The kernel count a forward launches (the bench line's gpu_launches per step): fused
+    router, dispatch (with the statistics and losses), gather, two GEMMs, and a combine except
+    for top-1 bf16 layers without a shared expert; the unfused router adds the top-k kernel;
+    fp32 shared experts run two more GEMMs; expert choice runs its selection, an unrouted
+    count and the statistics kernel in place of the dispatch."""
+    W = WORKLOADS
+    assert bench.launches_per_forward(W["mixtral_prefill"]) == 6
+    assert bench.launches_per_forward(W["mixtral_decode"]) == 6
+    assert bench.launches_per_forward(W["switch_top1"]) == 5                    # no combine
+    assert bench.launches_per_forward(W["switch_top1"], quantized=True) == 6    # 8-bit: combine
+    assert bench.launches_per_forward(W["deepseek_fine"]) == 6
+    assert bench.launches_per_forward(W["switch_top1"].scaled(d_ff_shared=256)) == 6
+    assert bench.launches_per_forward(W["switch_top1"].scaled(E=512)) == 6     # router + top-k
+    assert bench.launches_per_forward(W["tiny_fp32"]) == 7                      # fp32 router pair
+    assert bench.launches_per_forward(W["tiny_fp32"].scaled(d_ff_shared=64)) == 9
+    ec = W["mixtral_prefill"].scaled(gate="expert_choice", cf=1.0)
+    assert bench.launches_per_forward(ec) == 8
