@@ -64,8 +64,8 @@ struct TcArgs {
   void* gu_shared;          //   as bf16 [rows, 2N] (G in columns 0..N-1, U in N..2N-1); out_* may
                             //   then be nullptr (H not written)
   DeviceError* err;
-  int tma_out;              // set by launch_tc_gemm: bit 0 (routed) / bit 1 (shared) outputs
-                            //   leave through tensor stores
+  int tma_out;              // set by launch_tc_gemm: bit 0 (routed) / bit 1 (shared) outputs,
+                            //   bit 2 / bit 3 the G | U outputs, leave through tensor stores
   int scatter_rows;         // TC_SCALE, top-1 layers: routed row r is written at output row
                             //   perm[r] (the token: the combine folded into the epilogue)
 };

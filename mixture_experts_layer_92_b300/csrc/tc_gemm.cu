@@ -202,7 +202,9 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
                        const __grid_constant__ CUtensorMap tmB0s,
                        const __grid_constant__ CUtensorMap tmB1s,
                        const __grid_constant__ CUtensorMap tmO,
-                       const __grid_constant__ CUtensorMap tmOs, const TcArgs args) {
+                       const __grid_constant__ CUtensorMap tmOs,
+                       const __grid_constant__ CUtensorMap tmGU,
+                       const __grid_constant__ CUtensorMap tmGUs, const TcArgs args) {
   using C = Cfg<MODE, BN, MT, KB, W8, AR>;
   constexpr int TM = C::TM;  // rows per CTA tile
   constexpr int BK = C::BK;
@@ -549,7 +551,21 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
             }
             tmem_ld_wait();
             void* gu = t.shared ? args.gu_shared : args.gu_routed;
-            if (rvalid && gu != nullptr && !W8) {
+            if (gu != nullptr && !W8 && whole_block && ((args.tma_out >> (2 + t.shared)) & 1) &&
+                col_base + c * CW + CW <= N) {
+              // pre-activations for the backward pass, whole chunk of a whole block: G at
+              // columns col0.., U at N + col0.. of the [rows, 2N] map, two tensor stores
+              const int col0 = col_base + c * CW;
+              uint32_t pg[CW / 2], pu[CW / 2];
+#pragma unroll
+              for (int i = 0; i < CW / 2; ++i) {
+                pg[i] = pack_bf16x2(__uint_as_float(g[2 * i]), __uint_as_float(g[2 * i + 1]));
+                pu[i] = pack_bf16x2(__uint_as_float(u[2 * i]), __uint_as_float(u[2 * i + 1]));
+              }
+              const CUtensorMap* gmap = t.shared ? &tmGUs : &tmGU;
+              store_rows16(gmap, pg, col0, row_first);
+              store_rows16(gmap, pu, N + col0, row_first);
+            } else if (rvalid && gu != nullptr && !W8) {
               // pre-activations for the backward pass: G | U as bf16 [rows, 2N]
               const int col0 = col_base + c * CW;
               __nv_bfloat16* gdst = static_cast<__nv_bfloat16*>(gu) + row * 2 * N + col0;
@@ -757,6 +773,18 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
         encode_2d_out16(&mOs, args.out_shared, args.n_shared, args.m_shared, args.ldo_shared, C::CW))
       args.tma_out |= 2;
   }
+  // the backward's pre-activations G | U [rows, 2N]: U starts at column N, so N % 8 == 0
+  CUtensorMap mGU{}, mGUs{};
+  if (MODE == TC_SWIGLU && !W8) {
+    if (args.n_routed % 8 == 0 &&
+        encode_2d_out16(&mGU, args.gu_routed, 2ull * args.n_routed, p.a_rows,
+                        2ull * args.n_routed, C::CW))
+      args.tma_out |= 4;
+    if (args.has_shared && args.n_shared % 8 == 0 &&
+        encode_2d_out16(&mGUs, args.gu_shared, 2ull * args.n_shared, args.m_shared,
+                        2ull * args.n_shared, C::CW))
+      args.tma_out |= 8;
+  }
 
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return MOE_ERR_CUDA;
@@ -776,8 +804,8 @@ int launch_impl(const TcProblem& p, cudaStream_t stream) {
   long long grid = std::min<long long>(p.max_tiles, p.num_sms);
   if (grid < 1) return MOE_OK;
   if (launch_pdl(tc_grouped_gemm_kernel<MODE, BN, MT, KB, W8, AR>, dim3(static_cast<int>(grid)),
-                 dim3(C::THREADS), smem, stream, mA, mB0, mB1, mAs, mB0s, mB1s, mO, mOs,
-                 args) != cudaSuccess)
+                 dim3(C::THREADS), smem, stream, mA, mB0, mB1, mAs, mB0s, mB1s, mO, mOs, mGU,
+                 mGUs, args) != cudaSuccess)
     return MOE_ERR_CUDA;
   return MOE_OK;
 }
