@@ -177,6 +177,7 @@ struct BwdArgs {
                             //   (expert-choice rows); gate == nullptr: 1
   const float* gate;
   DeviceError* err;
+  int tma_out;              // set by launch_bwd_gemm (DGRAD): outputs through tensor stores
 };
 
 struct BwdProblem {

@@ -67,8 +67,9 @@ struct BCfg {
   static constexpr int B_BYTES = BN * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
   static constexpr int NUM_ACC = (MT == 1) ? 2 : 1;   // accumulator sets (double buffering)
-  // BW_WGRAD: one staging block per epilogue warp for the tensor stores
-  static constexpr int STG_BYTES = (MODE == BW_WGRAD) ? EPI_WARPS * kStgBytes : 0;
+  // one staging block per epilogue warp for the tensor stores (BW_WGRAD: 32 x 16 fp32;
+  // DGRAD: 32 x 32 bf16, the same 2 KB)
+  static constexpr int STG_BYTES = EPI_WARPS * kStgBytes;
   static constexpr int STAGES_RAW = (212 * 1024 - STG_BYTES) / STAGE_BYTES;
   static constexpr int STAGES = STAGES_RAW > 8 ? 8 : STAGES_RAW;
   static constexpr int OFF_STG = STAGES * STAGE_BYTES;
@@ -377,6 +378,28 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
     constexpr int CPW = (MT == 1) ? BN / 64 : BN / 32;   // 32-column chunks per warp
     uint8_t* stg = smem + C::OFF_STG + (warp - 2) * kStgBytes;
     bool stg_busy = false;                     // a tensor store may still read `stg`
+    // DGRAD: one 32-row x 32-column bf16 block staged in the output map's 64-byte swizzle
+    // (16-byte unit q of row `lane` at q ^ (lane / 2 % 4)) and written by one tensor store
+    auto stage_store = [&](const CUtensorMap* map, const uint32_t* packed, int col0,
+                           long long row_first) {
+      if (stg_busy) {
+        if (lane == 0) bulk_wait_group_read0();
+        __syncwarp();
+      }
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const int pos = q ^ ((lane >> 1) & 3);
+        *reinterpret_cast<uint4*>(stg + lane * 64 + (pos << 4)) =
+            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+      }
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_store_2d(map, stg, col0, static_cast<int>(row_first));
+        bulk_commit_group();
+      }
+      stg_busy = true;
+    };
     int it = 0;
     for (int tile = blockIdx.x; tile < total; tile += gridDim.x, ++it) {
       const int acc = it % C::NUM_ACC;
@@ -437,6 +460,9 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       } else if (quarter * 32 < t.rows) {
         const bool rvalid = r_local < t.rows;
         const long long row = static_cast<long long>(t.row0) + r_local;
+        // whole 32-row blocks of whole 32-column chunks leave through tensor stores
+        const long long row_first = static_cast<long long>(t.row0) + quarter * 32;
+        const bool tma_blk = args.tma_out && quarter * 32 + 32 <= t.rows;   // warp-uniform
         if (MODE == BW_DGRAD_X) {
           __nv_bfloat16* out = static_cast<__nv_bfloat16*>(args.out);
 #pragma unroll 1
@@ -451,12 +477,16 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
 #pragma unroll
               for (int i = 0; i < 16; ++i)
                 packed[i] = pack_bf16x2(__uint_as_float(v[2 * i]), __uint_as_float(v[2 * i + 1]));
-              __nv_bfloat16* dst = out + row * args.ldo + col0;
+              if (tma_blk && col0 + 32 <= N) {
+                stage_store(&tmO0, packed, col0, row_first);
+              } else {
+                __nv_bfloat16* dst = out + row * args.ldo + col0;
 #pragma unroll
-              for (int q = 0; q < 4; ++q)
-                if (col0 + 8 * q < N)
-                  *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(
-                      packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+                for (int q = 0; q < 4; ++q)
+                  if (col0 + 8 * q < N)
+                    *reinterpret_cast<uint4*>(dst + 8 * q) = make_uint4(
+                        packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
+              }
             }
           }
         } else {  // BW_DGRAD_H
@@ -475,6 +505,8 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
             tmem_ld_wait();
             const int col0 = n0 + c * 32;
             if (rvalid && col0 < N) {
+              const bool tma_chunk = tma_blk && col0 + 32 <= N;   // warp-uniform
+              uint32_t dgp[16], dup[16], hp[16];                 // tma_chunk: the packed chunk
               // all of the chunk's G and U loads first (read-only), then the math and stores
               uint4 gqs[4], uqs[4];
 #pragma unroll
@@ -513,12 +545,27 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                   duw[i] = pack_bf16x2(duv[0], duv[1]);
                   hw[i] = pack_bf16x2(hv[0], hv[1]);
                 }
-                *reinterpret_cast<uint4*>(dgu + col0 + 8 * q) =
-                    make_uint4(dgw[0], dgw[1], dgw[2], dgw[3]);
-                *reinterpret_cast<uint4*>(dgu + N + col0 + 8 * q) =
-                    make_uint4(duw[0], duw[1], duw[2], duw[3]);
-                *reinterpret_cast<uint4*>(hrow + col0 + 8 * q) =
-                    make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                if (tma_chunk) {
+#pragma unroll
+                  for (int i = 0; i < 4; ++i) {
+                    dgp[4 * q + i] = dgw[i];
+                    dup[4 * q + i] = duw[i];
+                    hp[4 * q + i] = hw[i];
+                  }
+                } else {
+                  *reinterpret_cast<uint4*>(dgu + col0 + 8 * q) =
+                      make_uint4(dgw[0], dgw[1], dgw[2], dgw[3]);
+                  *reinterpret_cast<uint4*>(dgu + N + col0 + 8 * q) =
+                      make_uint4(duw[0], duw[1], duw[2], duw[3]);
+                  *reinterpret_cast<uint4*>(hrow + col0 + 8 * q) =
+                      make_uint4(hw[0], hw[1], hw[2], hw[3]);
+                }
+              }
+              if (tma_chunk) {
+                // dG at column col0 and dU at N + col0 of dG | dU [rows, 2N], H at col0 of H
+                stage_store(&tmO0, dgp, col0, row_first);
+                stage_store(&tmO0, dup, N + col0, row_first);
+                stage_store(&tmO1, hp, col0, row_first);
               }
             }
           }
@@ -531,7 +578,7 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty_bar[acc]);
     }
-    if (MODE == BW_WGRAD && lane == 0) bulk_wait_group0();   // tensor stores done before exit
+    if (lane == 0 && stg_busy) bulk_wait_group0();   // tensor stores done before exit
   }
 
   tc_fence_before();
@@ -573,6 +620,18 @@ int launch_impl(const BwdProblem& p, cudaStream_t stream) {
       mB1 = mB0;
     }
   }
+  // DGRAD outputs through tensor stores where the buffers allow it (16-byte aligned bases and
+  // row strides; dG | dU needs N % 8 == 0 for U's first column)
+  BwdArgs args = p.args;
+  args.tma_out = 0;
+  const unsigned long long N = static_cast<unsigned long long>(p.args.N);
+  if (MODE == BW_DGRAD_X && args.out != nullptr &&
+      encode_2d_out16(&mO0, args.out, N, p.a_rows, args.ldo, 32))
+    args.tma_out = 1;
+  if (MODE == BW_DGRAD_H && N % 8 == 0 && args.dgu != nullptr && args.h != nullptr &&
+      encode_2d_out16(&mO0, args.dgu, 2 * N, p.a_rows, 2 * N, 32) &&
+      encode_2d_out16(&mO1, args.h, N, p.a_rows, N, 32))
+    args.tma_out = 1;
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return MOE_ERR_CUDA;
   static std::once_flag attr_once[64];
@@ -586,7 +645,7 @@ int launch_impl(const BwdProblem& p, cudaStream_t stream) {
   const long long grid = std::min<long long>(p.max_tiles, p.num_sms);
   if (grid < 1) return MOE_OK;
   tc_bwd_kernel<MODE, BN, MT><<<static_cast<int>(grid), C::THREADS, C::smem_bytes(groups), stream>>>(
-      mA, mB0, mB1, mO0, mO1, p.args);
+      mA, mB0, mB1, mO0, mO1, MODE == BW_WGRAD ? p.args : args);
   return cudaGetLastError() == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }
 
