@@ -271,13 +271,36 @@ __device__ __forceinline__ void tma_store_3d(const CUtensorMap* m, const void* s
       "r"(smem_u32(smem_src)), "r"(c0), "r"(c1), "r"(c2)
       : "memory");
 }
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap* m, const void* smem_src, int c0,
-                                             int c1) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-          reinterpret_cast<uint64_t>(m)),
-      "r"(smem_u32(smem_src)), "r"(c0), "r"(c1)
-      : "memory");
+// One warp's 32-row block for a tensor store: row `lane`'s ROW_BYTES bytes (the 16-byte
+// units words[4q .. 4q+3]) written into `buf` where a tensor map with ROW_BYTES-wide rows
+// and the matching swizzle (128-, 64- or 32-byte) expects them: unit q of row r at q ^ (r % 8),
+// q ^ (r / 2 % 4) or q ^ (r / 4 % 2). Every eight consecutive lanes then cover all 32 banks.
+template <int ROW_BYTES>
+__device__ __forceinline__ void stage_row_swizzled(uint8_t* buf, const uint32_t* words, int lane) {
+  static_assert(ROW_BYTES == 128 || ROW_BYTES == 64 || ROW_BYTES == 32, "swizzle span");
+#pragma unroll
+  for (int q = 0; q < ROW_BYTES / 16; ++q) {
+    const int pos = ROW_BYTES == 128 ? (q ^ (lane & 7))
+                    : ROW_BYTES == 64 ? (q ^ ((lane >> 1) & 3))
+                                      : (q ^ ((lane >> 2) & 1));
+    *reinterpret_cast<uint4*>(buf + lane * ROW_BYTES + (pos << 4)) =
+        make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
+  }
+}
+// After every lane has staged its row: make the block visible to the async proxy and let
+// lane 0 write it with one tensor store at (c0, c1) of `map` (one bulk group).
+__device__ __forceinline__ void store_staged_2d(const CUtensorMap* map, const uint8_t* buf,
+                                                int c0, int c1, int lane) {
+  fence_proxy_async_smem();
+  __syncwarp();
+  if (lane == 0) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+            reinterpret_cast<uint64_t>(map)),
+        "r"(smem_u32(buf)), "r"(c0), "r"(c1)
+        : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+  }
 }
 __device__ __forceinline__ void bulk_commit_group() {
   asm volatile("cp.async.bulk.commit_group;" ::: "memory");

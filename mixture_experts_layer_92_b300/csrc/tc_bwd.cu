@@ -386,18 +386,8 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
         if (lane == 0) bulk_wait_group_read0();
         __syncwarp();
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const int pos = q ^ ((lane >> 1) & 3);
-        *reinterpret_cast<uint4*>(stg + lane * 64 + (pos << 4)) =
-            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(map, stg, col0, static_cast<int>(row_first));
-        bulk_commit_group();
-      }
+      stage_row_swizzled<64>(stg, packed, lane);
+      store_staged_2d(map, stg, col0, static_cast<int>(row_first), lane);
       stg_busy = true;
     };
     int it = 0;
@@ -438,15 +428,8 @@ tc_bwd_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ C
                 if (lane == 0) bulk_wait_group_read0();
                 __syncwarp();
               }
-              // row `lane` of the 32-row block; 16-byte unit q goes where the tensor map's
-              // swizzle expects it (128-byte rows: q ^ (lane % 8); 64-byte rows: q ^ (lane/2 % 4))
-#pragma unroll
-              for (int q = 0; q < kStgCols / 4; ++q) {
-                const int pos = kStgCols == 32 ? (q ^ (lane & 7)) : (q ^ ((lane >> 1) & 3));
-                const int vi = part * kStgCols + 4 * q;
-                *reinterpret_cast<uint4*>(stg + lane * (kStgCols * 4) + (pos << 4)) =
-                    make_uint4(v[vi], v[vi + 1], v[vi + 2], v[vi + 3]);
-              }
+              // row `lane` of the 32-row block, kStgCols fp32 values from column part * kStgCols
+              stage_row_swizzled<kStgCols * 4>(stg, v + part * kStgCols, lane);
               fence_proxy_async_smem();
               __syncwarp();
               if (lane == 0) {

@@ -494,20 +494,8 @@ tc_grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         }
         __syncwarp();
       }
-      // row `lane`, 16-byte unit q at the position the map's swizzle expects: 64-byte rows
-      // q ^ (lane / 2 % 4), 32-byte rows q ^ (lane / 4 % 2)
-#pragma unroll
-      for (int q = 0; q < C::STG_ROW_BYTES / 16; ++q) {
-        const int pos = C::STG_ROW_BYTES == 64 ? (q ^ ((lane >> 1) & 3)) : (q ^ ((lane >> 2) & 1));
-        *reinterpret_cast<uint4*>(buf + lane * C::STG_ROW_BYTES + (pos << 4)) =
-            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(map, buf, col0, static_cast<int>(row_first));
-        bulk_commit_group();
-      }
+      stage_row_swizzled<C::STG_ROW_BYTES>(buf, packed, lane);
+      store_staged_2d(map, buf, col0, static_cast<int>(row_first), lane);
       ++n_stores;
     };
     int it = 0;

@@ -311,20 +311,8 @@ tc_mx_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant
         if (lane == 0) bulk_wait_group_read0();   // the previous store has read the buffer
         __syncwarp();
       }
-      // row `lane`, 16-byte unit q where the map's swizzle expects it: 64-byte rows
-      // q ^ (lane / 2 % 4), 32-byte rows q ^ (lane / 4 % 2)
-#pragma unroll
-      for (int q = 0; q < C::STG_ROW_BYTES / 16; ++q) {
-        const int pos = C::STG_ROW_BYTES == 64 ? (q ^ ((lane >> 1) & 3)) : (q ^ ((lane >> 2) & 1));
-        *reinterpret_cast<uint4*>(stg + lane * C::STG_ROW_BYTES + (pos << 4)) =
-            make_uint4(words[4 * q], words[4 * q + 1], words[4 * q + 2], words[4 * q + 3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(&tmO, stg, col0, static_cast<int>(row_first));
-        bulk_commit_group();
-      }
+      stage_row_swizzled<C::STG_ROW_BYTES>(stg, words, lane);
+      store_staged_2d(&tmO, stg, col0, static_cast<int>(row_first), lane);
       ++n_stores;
     };
     int it = 0;

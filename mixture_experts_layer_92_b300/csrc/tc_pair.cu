@@ -313,18 +313,8 @@ tc_pair_gemm_kernel(const __grid_constant__ CUtensorMap tmA,
         if (lane == 0) bulk_wait_group_read0();   // the previous store has read the buffer
         __syncwarp();
       }
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {   // 64-byte rows: 16-byte unit q at q ^ (lane / 2 % 4)
-        const int pos = q ^ ((lane >> 1) & 3);
-        *reinterpret_cast<uint4*>(stg + lane * 64 + (pos << 4)) =
-            make_uint4(packed[4 * q], packed[4 * q + 1], packed[4 * q + 2], packed[4 * q + 3]);
-      }
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_store_2d(map, stg, col0, static_cast<int>(row_first));
-        bulk_commit_group();
-      }
+      stage_row_swizzled<64>(stg, packed, lane);
+      store_staged_2d(map, stg, col0, static_cast<int>(row_first), lane);
       ++n_stores;
     };
     int it = 0;
