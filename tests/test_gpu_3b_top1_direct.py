@@ -92,3 +92,35 @@ def test_top1_layer_every_row_written(case):
     L.moe_aux_loss(s, stats, counts, losses2)
     torch.cuda.synchronize()
     assert torch.equal(losses, losses2), (losses, losses2)
+
+
+def test_e1024_top2_layer_statistics_in_the_dispatch():
+    """E = 1024 (the largest E, the unfused router): the dispatch runs 33 statistics CTAs beside
+    its own, at one CTA per SM (its shared memory) -- the co-residency bound of its grid barrier
+    in the tightest case. Every row against the oracle, losses bit-identical to moe_aux_loss."""
+    w = WORKLOADS["deepseek_fine"].scaled(T=2048, d=128, E=1024, k=2, d_ff=128, d_ff_shared=0,
+                                          gate="softmax_topk", cf=1.5)
+    C = O.capacity(w.cf, w.T, w.k, w.E)
+    inp, s, ws, y, counts, dropped, losses, idx = forward_nan_filled(w, C)
+    logits64 = O.router_logits(host64(inp["x"]), host64(inp["w_router"]), None)
+    gidx = idx.cpu().numpy().astype(np.int64)
+    bad, ties = routing_check(logits64, gidx, w.k)
+    assert set(bad.tolist()) <= set(ties.tolist())
+    disp = O.dispatch(gidx, w.E, C)
+    np.testing.assert_array_equal(counts.cpu().numpy(), disp["counts"])
+    assert int(dropped.item()) == disp["dropped"]
+    yh = y.double().cpu().numpy()
+    assert np.isfinite(yh).all()
+    yref = oracle_y_for_tokens(w, inp, logits64, gidx, disp["inv"], np.arange(w.T))
+    assert rel_l2(yh, yref) < 2e-2
+    l = losses.cpu().numpy()
+    assert l[0] == pytest.approx(O.aux_loss(logits64, gidx, w.alpha), rel=1e-3)
+    assert l[1] == pytest.approx(O.z_loss(logits64, w.beta), rel=1e-3)
+    stats = torch.empty(w.E + 1, device=DEV)
+    L.moe_route_topk(s, ws, torch.empty(w.T, w.k, dtype=torch.int32, device=DEV),
+                     torch.empty(w.T, w.k, device=DEV), x=inp["x"], w_router=inp["w_router"],
+                     stats=stats)
+    losses2 = torch.full((2,), float("nan"), device=DEV)
+    L.moe_aux_loss(s, stats, counts, losses2)
+    torch.cuda.synchronize()
+    assert torch.equal(losses, losses2), (losses, losses2)
