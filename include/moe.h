@@ -454,6 +454,16 @@ int moe_backward(const moe_shape* s, const void* x, const void* w_router, const 
 int moe_route_topk_noalloc(const moe_shape* s, const float* logits_in, int32_t* topk_idx,
                            float* topk_gate, float* stats, void* stream);
 
+/* Where the forward keeps its dispatch results inside a workspace for shape `s` (host only,
+ * no GPU call): byte offsets from the workspace's start of perm [T*k] (int32; rows
+ * 0..offsets[E]-1 meaningful), inv [T*k] (int32) and offsets [E+1] (int32) -- what
+ * moe_dispatch would return for the batch's routing, left by the last moe_forward (or
+ * variant) that ran on the workspace, until the next call on it. For tests and tools that
+ * inspect the routing. MOE_ERR_INVALID for an invalid shape or a NULL output pointer;
+ * MOE_ERR_UNSUPPORTED for expert-choice shapes (their perm / inv differ in meaning). */
+int moe_workspace_dispatch_offsets(const moe_shape* s, size_t* perm_offset, size_t* inv_offset,
+                                   size_t* offsets_offset);
+
 /* Reads (synchronising `stream`) the sticky device error word in the workspace:
  * MOE_OK, or the first moe_status a kernel recorded since the last moe_clear_error. */
 int moe_get_error(const void* ws, void* stream);

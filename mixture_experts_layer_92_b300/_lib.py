@@ -33,7 +33,8 @@ EXPORTED = ("moe_capacity", "moe_check_shape", "moe_workspace_size", "moe_route_
             "moe_backward", "moe_selftest_wait_timeout", "moe_forward_host",
             "moe_host_pipeline_buffer_size", "moe_host_pipeline_create",
             "moe_host_pipeline_forward", "moe_host_pipeline_join", "moe_host_pipeline_destroy",
-            "moe_mx_workspace_size", "moe_forward_mx", "moe_mx_quantize")
+            "moe_mx_workspace_size", "moe_forward_mx", "moe_mx_quantize",
+            "moe_workspace_dispatch_offsets")
 MX_FORMATS = {"e4m3": 0, "e2m1": 1}
 NUM_BWD_STAGES = 8
 BWD_STAGE_NAMES = ("route_dispatch", "gather_x_dy", "recompute_gu", "gemm_dh_swiglu_bwd",
@@ -74,6 +75,8 @@ def _load() -> ctypes.CDLL:
                                        vp, sz, vp]),
         "moe_forward_events": (ctypes.c_int, [sp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp, vp,
                                               vp, vp, sz, vp, ctypes.POINTER(vp), ctypes.c_int]),
+        "moe_workspace_dispatch_offsets": (ctypes.c_int, [sp, ctypes.POINTER(sz),
+                                                          ctypes.POINTER(sz), ctypes.POINTER(sz)]),
         "moe_get_error": (ctypes.c_int, [vp, vp]),
         "moe_clear_error": (ctypes.c_int, [vp, vp]),
         "moe_selftest_wait_timeout": (ctypes.c_int, [vp, sz, vp]),
@@ -167,6 +170,25 @@ def alloc_workspace(s: moe_shape, device="cuda") -> torch.Tensor:
     ws = torch.zeros(n + 256, dtype=torch.uint8, device=device)
     off = (-ws.data_ptr()) % 256
     return ws[off:off + n]
+
+
+def moe_workspace_dispatch_offsets(s: moe_shape):
+    """Byte offsets of perm, inv and offsets (the forward's dispatch results) in a workspace."""
+    po, io, oo = ctypes.c_size_t(), ctypes.c_size_t(), ctypes.c_size_t()
+    _check(LIB.moe_workspace_dispatch_offsets(ctypes.byref(s), ctypes.byref(po), ctypes.byref(io),
+                                              ctypes.byref(oo)), "moe_workspace_dispatch_offsets")
+    return po.value, io.value, oo.value
+
+
+def workspace_dispatch(s: moe_shape, ws: torch.Tensor):
+    """Views (int32) of the perm [T*k], inv [T*k] and offsets [E+1] a forward left in `ws`."""
+    po, io, oo = moe_workspace_dispatch_offsets(s)
+    A = s.T * s.k
+
+    def view(off, n):
+        return ws[off:off + 4 * n].view(torch.int32)
+
+    return view(po, A), view(io, A), view(oo, s.E + 1)
 
 
 def moe_backward_workspace_size(s: moe_shape) -> int:

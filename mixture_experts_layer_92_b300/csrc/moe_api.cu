@@ -1831,6 +1831,20 @@ int moe_selftest_wait_timeout(void* ws, size_t ws_bytes, void* stream) {
   return ok();
 }
 
+int moe_workspace_dispatch_offsets(const moe_shape* s, size_t* perm_offset, size_t* inv_offset,
+                                   size_t* offsets_offset) {
+  TRY(check_shape(s));
+  if (perm_offset == nullptr || inv_offset == nullptr || offsets_offset == nullptr)
+    return fail(MOE_ERR_INVALID, "an output pointer is NULL");
+  if (expert_choice(s))
+    return fail(MOE_ERR_UNSUPPORTED, "expert-choice layers keep token rows, not a dispatch");
+  const Layout L = layout(s);
+  *perm_offset = L.perm;
+  *inv_offset = L.inv;
+  *offsets_offset = L.offsets;
+  return ok();
+}
+
 int moe_clear_error(void* ws, void* stream) {
   if (ws == nullptr) return fail(MOE_ERR_WORKSPACE, "workspace is NULL");
   if (cudaMemsetAsync(ws, 0, sizeof(DeviceError), static_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -69,6 +69,27 @@ def test_valid_shapes_and_workspace_monotone():
     assert moe.moe_workspace_size(ds) < 4 << 30
 
 
+def test_workspace_dispatch_offsets():
+    """The forward's perm, inv and offsets sit inside the workspace, apart from one another,
+    4-byte aligned; expert-choice shapes and invalid shapes are refused."""
+    for kw in (dict(T=64), dict(T=1000, E=128, k=1), dict(T=8192, d=7168, E=256, k=8, d_ff=2048,
+                                                        gate="sigmoid_topk")):
+        s = shape(**kw)
+        n = moe.moe_workspace_size(s)
+        po, io, oo = _lib.moe_workspace_dispatch_offsets(s)
+        A, E = s.T * s.k, s.E
+        spans = sorted([(po, po + 4 * A), (io, io + 4 * A), (oo, oo + 4 * (E + 1))])
+        assert all(b <= n for _, b in spans)
+        assert all(spans[i][1] <= spans[i + 1][0] for i in range(2))
+        assert po % 4 == io % 4 == oo % 4 == 0
+    with pytest.raises(_lib.MoeError) as ei:
+        _lib.moe_workspace_dispatch_offsets(shape(T=64, gate="expert_choice"))
+    assert ei.value.status == -2
+    with pytest.raises(_lib.MoeError) as ei:
+        _lib.moe_workspace_dispatch_offsets(shape(T=64, k=9))
+    assert ei.value.status == -1
+
+
 def _ws_bytes(n):
     return ctypes.c_size_t(n)
 
