@@ -9,8 +9,9 @@
 //          summed in slot order in fp32; a dropped assignment adds nothing (same page,
 //          step 5). Yp already carries the gate (applied in the down-projection epilogue).
 //
-// Both are HBM-bound copies: one warp per row, 16-byte vector loads and stores, several
-// loads in flight per lane, grid sized as a multiple of the SM count.
+// Both are HBM-bound copies: one warp per row (the combine: per 1 KB segment of a row),
+// 16-byte vector loads and stores, every load of a row's piece issued before its stores,
+// grid sized as a multiple of the SM count.
 #include <algorithm>
 
 #include "common.cuh"
@@ -23,6 +24,26 @@ namespace {
 constexpr int kMoveThreads = 256;
 constexpr int kMoveWarps = kMoveThreads / 32;
 
+// Copies one row of nvec 16-byte chunks with one warp: up to 16 chunks per lane are loaded
+// before any is stored, so a row of up to 8 KB costs one memory round trip.
+__device__ __forceinline__ void copy_row(const uint4* __restrict__ src, uint4* __restrict__ dst,
+                                         int nvec, int lane) {
+  constexpr int U = 16;
+  for (int i0 = 0; i0 < nvec; i0 += 32 * U) {
+    uint4 v[U];
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + lane + 32 * u;
+      if (i < nvec) v[u] = __ldg(src + i);
+    }
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+      const int i = i0 + lane + 32 * u;
+      if (i < nvec) dst[i] = v[u];
+    }
+  }
+}
+
 __global__ void __launch_bounds__(kMoveThreads)
 gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm,
                    const int32_t* __restrict__ offsets, int E, int k, int nvec,
@@ -34,18 +55,7 @@ gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ perm
   const int nw = gridDim.x * kMoveWarps;
   for (int r = blockIdx.x * kMoveWarps + (threadIdx.x >> 5); r < R; r += nw) {
     const int t = perm[r] / k;
-    const uint4* src = x + static_cast<size_t>(t) * nvec;
-    uint4* dst = xp + static_cast<size_t>(r) * nvec;
-    int i = lane;
-    for (; i + 96 < nvec; i += 128) {
-      const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
-                  d = __ldg(src + i + 96);
-      dst[i] = a;
-      dst[i + 32] = b;
-      dst[i + 64] = c;
-      dst[i + 96] = d;
-    }
-    for (; i < nvec; i += 32) dst[i] = __ldg(src + i);
+    copy_row(x + static_cast<size_t>(t) * nvec, xp + static_cast<size_t>(r) * nvec, nvec, lane);
   }
 }
 
@@ -63,18 +73,7 @@ gather_tokens_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ in
   for (int t = blockIdx.x * kMoveWarps + (threadIdx.x >> 5); t < T; t += nw) {
     const int r = __ldg(inv + t);
     if (r >= 0) {
-      const uint4* src = x + static_cast<size_t>(t) * nvec;
-      uint4* dst = xp + static_cast<size_t>(r) * nvec;
-      int i = lane;
-      for (; i + 96 < nvec; i += 128) {
-        const uint4 a = __ldg(src + i), b = __ldg(src + i + 32), c = __ldg(src + i + 64),
-                    d = __ldg(src + i + 96);
-        dst[i] = a;
-        dst[i + 32] = b;
-        dst[i + 64] = c;
-        dst[i + 96] = d;
-      }
-      for (; i < nvec; i += 32) dst[i] = __ldg(src + i);
+      copy_row(x + static_cast<size_t>(t) * nvec, xp + static_cast<size_t>(r) * nvec, nvec, lane);
     } else {
       uint4* dst = y + static_cast<size_t>(t) * nvec;
       for (int i = lane; i < nvec; i += 32) dst[i] = make_uint4(0u, 0u, 0u, 0u);
@@ -143,53 +142,72 @@ __device__ __forceinline__ uint4 pack_chunk(const float (&acc)[8]) {
                     __float_as_uint(acc[3]));
 }
 
-// One warp per (token, segment of 64 16-byte chunks); each lane owns chunks c and c + 32
-// of the segment. KS > 0 unrolls the slot loop (all 2*KS loads issued before the adds);
-// KS == 0 handles any k. Sums run in slot order in fp32, the shared expert last.
+// One warp per (token, segment of 64 16-byte chunks); each lane owns chunks c and c + 32 of
+// the segment. KS > 0 unrolls the slot loop: all 2 * KS loads, and the shared expert's two,
+// are issued before the first add (one memory round trip per task; more chunks per task left
+// too few tasks for small batches). KS == 0 handles any k. Sums run in slot order in fp32,
+// the shared expert last.
 template <bool BF16, int KS>
 __global__ void __launch_bounds__(kMoveThreads)
 combine_kernel(const uint4* __restrict__ yp, const int32_t* __restrict__ inv,
                const uint4* __restrict__ ys, uint4* __restrict__ y, int T, int k, int nvec) {
   pdl_wait();
   pdl_launch_dependents();
+  constexpr int CH = 2;
   const int lane = threadIdx.x & 31;
-  const int nseg = (nvec + 63) / 64;
+  const int nseg = (nvec + 32 * CH - 1) / (32 * CH);
   const long long total = static_cast<long long>(T) * nseg;
   const long long nw = static_cast<long long>(gridDim.x) * kMoveWarps;
   for (long long w = static_cast<long long>(blockIdx.x) * kMoveWarps + (threadIdx.x >> 5); w < total;
        w += nw) {
     const int t = static_cast<int>(w / nseg);
     const int seg = static_cast<int>(w - static_cast<long long>(t) * nseg);
-    const int c0 = seg * 64 + lane, c1 = c0 + 32;
-    const bool h0 = c0 < nvec, h1 = c1 < nvec;
+    const int c_first = seg * 32 * CH + lane;
     const int32_t* slots = inv + static_cast<size_t>(t) * k;
-    float a0[8], a1[8];
-#pragma unroll
-    for (int q = 0; q < 8; ++q) a0[q] = a1[q] = 0.f;
+    uint4* out = y + static_cast<size_t>(t) * nvec;
     if (KS > 0) {
       int r[KS > 0 ? KS : 1];
-      uint4 v0[KS > 0 ? KS : 1], v1[KS > 0 ? KS : 1];
+      uint4 v[KS > 0 ? KS : 1][CH], vs[CH];
 #pragma unroll
-      for (int s = 0; s < KS; ++s) r[s] = __ldg(slots + s);
+      for (int sl = 0; sl < KS; ++sl) r[sl] = __ldg(slots + sl);
 #pragma unroll
-      for (int s = 0; s < KS; ++s) {
-        v0[s] = v1[s] = make_uint4(0, 0, 0, 0);
-        if (r[s] >= 0) {
-          const uint4* row = yp + static_cast<size_t>(r[s]) * nvec;
-          if (h0) v0[s] = __ldg(row + c0);
-          if (h1) v1[s] = __ldg(row + c1);
+      for (int sl = 0; sl < KS; ++sl) {
+        const uint4* row = yp + static_cast<size_t>(r[sl] >= 0 ? r[sl] : 0) * nvec;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int i = c_first + 32 * c;
+          v[sl][c] = (r[sl] >= 0 && i < nvec) ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (ys != nullptr) {
+        const uint4* row = ys + static_cast<size_t>(t) * nvec;
+#pragma unroll
+        for (int c = 0; c < CH; ++c) {
+          const int i = c_first + 32 * c;
+          vs[c] = i < nvec ? __ldg(row + i) : make_uint4(0, 0, 0, 0);
         }
       }
 #pragma unroll
-      for (int s = 0; s < KS; ++s) {
-        if (r[s] >= 0) {
-          add_chunk<BF16>(a0, v0[s]);
-          add_chunk<BF16>(a1, v1[s]);
-        }
+      for (int c = 0; c < CH; ++c) {
+        const int i = c_first + 32 * c;
+        if (i >= nvec) continue;
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.f;
+#pragma unroll
+        for (int sl = 0; sl < KS; ++sl)
+          if (r[sl] >= 0) add_chunk<BF16>(acc, v[sl][c]);
+        if (ys != nullptr) add_chunk<BF16>(acc, vs[c]);
+        out[i] = pack_chunk<BF16>(acc);
       }
     } else {
       // any k (e.g. the dense [T, E] inverse of expert choice): lanes read 32 slots at a
       // time, a ballot marks the used ones, and they are added in slot order
+      const int c0 = c_first, c1 = c0 + 32;
+      const bool h0 = c0 < nvec, h1 = c1 < nvec;
+      float a0[8], a1[8];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) a0[q] = a1[q] = 0.f;
       for (int base = 0; base < k; base += 32) {
         const int mine = (base + lane < k) ? __ldg(slots + base + lane) : -1;
         unsigned used = __ballot_sync(0xffffffffu, mine >= 0);
@@ -202,15 +220,14 @@ combine_kernel(const uint4* __restrict__ yp, const int32_t* __restrict__ inv,
           if (h1) add_chunk<BF16>(a1, __ldg(row + c1));
         }
       }
+      if (ys != nullptr) {
+        const uint4* row = ys + static_cast<size_t>(t) * nvec;
+        if (h0) add_chunk<BF16>(a0, __ldg(row + c0));
+        if (h1) add_chunk<BF16>(a1, __ldg(row + c1));
+      }
+      if (h0) out[c0] = pack_chunk<BF16>(a0);
+      if (h1) out[c1] = pack_chunk<BF16>(a1);
     }
-    if (ys != nullptr) {
-      const uint4* row = ys + static_cast<size_t>(t) * nvec;
-      if (h0) add_chunk<BF16>(a0, __ldg(row + c0));
-      if (h1) add_chunk<BF16>(a1, __ldg(row + c1));
-    }
-    uint4* out = y + static_cast<size_t>(t) * nvec;
-    if (h0) out[c0] = pack_chunk<BF16>(a0);
-    if (h1) out[c1] = pack_chunk<BF16>(a1);
   }
 }
 
