@@ -143,6 +143,7 @@ dispatch_kernel(const int32_t* __restrict__ idx, int A, int E, int C, int chunk,
     }
     const unsigned peers = __match_any_sync(0xffffffffu, key);
     if (key >= 0 && lane == __ffs(peers) - 1) hist[warp * E + key] += __popc(peers);
+    __syncwarp();   // the next piece's leader may add to the same counter
   }
   __syncthreads();
   for (int e = tid; e < E; e += kDispThreads) {

@@ -8,9 +8,9 @@ forward's routing (moe_route_topk from x: the same fused router, the same bits);
 are bit-identical to moe_aux_loss on that routing's statistics and the counts. Shapes cover
 router cluster splits of 1, 2, 4 and 8 (CTAs of 128, 64, 32 and 16 tokens, so the router's
 statistic partials come in different counts), ragged token counts, k = 1 .. 8, E = 8 .. 256,
-heavy drops (Zipf-biased router, cf < 1), C = 0 and a batch of 36000 assignments; a second
-test runs forwards of different sizes on one workspace (the dispatch's grid-barrier counters
-must return to zero after each)."""
+heavy drops (Zipf-biased router, cf < 1), C = 0, a batch of 36000 assignments and one of
+160000 (two 32-wide pieces per dispatch warp); a second test runs forwards of different sizes
+on one workspace (the dispatch's grid-barrier counters must return to zero after each)."""
 import numpy as np
 import pytest
 import torch
@@ -34,6 +34,8 @@ CASES = [
     ("ragged_tail", "switch_top1", 130, 384, 16, 4, "softmax_topk", 0.5),
     ("decode_empty_ctas", "mixtral_prefill", 32, 1024, 8, 2, "softmax_topk", None),
     ("large_batch", "mixtral_prefill", 18000, 128, 8, 2, "softmax_topk", 1.0),
+    # 160000 assignments: more than 148 CTAs x 1024, so each dispatch warp walks two pieces
+    ("two_pieces_per_warp", "switch_top1", 40000, 128, 16, 4, "softmax_topk", 1.0),
 ]
 
 
