@@ -3,8 +3,10 @@ run on the GPU's own routing decisions (top-k parity is tested bit for bit elsew
 mismatch may only fall on a near tie). The shapes are drawn, from a fixed seed, over what the
 boundary accepts: ragged K and N (d and d_ff any multiple of 8, of 4 for fp32), 1..48
 experts, k up to 6, the three gate modes, no drop / capacity factors that drop, a shared
-expert, a Zipf-skewed router and batches from one token up. Bars: bf16 relative L2 <= 2e-2,
-fp32 max-abs <= 1e-4 RMS; counts and drops exact; losses to 1e-3 (bf16) / 1e-5 (fp32)."""
+expert, a Zipf-skewed router and batches from one token up; then the degenerate corners a
+draw need not reach (a single expert, k = E with and without drops, one token over 256
+experts, d = d_ff = 8, capacity 1, E = 1024). Bars: bf16 relative L2 <= 2e-2, fp32 max-abs
+<= 1e-4 RMS; counts and drops exact; losses to 1e-3 (bf16) / 1e-5 (fp32)."""
 import numpy as np
 import pytest
 
@@ -36,6 +38,29 @@ def draw(seed: int, dtype: str):
 
 
 CASES = [draw(i, "bf16") for i in range(16)] + [draw(i, "f32") for i in range(16, 24)]
+
+
+def edge(name, **kw):
+    base = dict(gate="softmax_topk", dtype="bf16", cf=None, d_ff_shared=0, zipf_s=None)
+    base.update(kw)
+    return WORKLOADS["mixtral_prefill"].scaled(name=name, **base)
+
+
+# the degenerate corners of the method, which a draw need not reach
+EDGES = [
+    edge("edge_single_expert", T=300, d=64, E=1, k=1, d_ff=48),
+    edge("edge_single_expert_sigmoid_f32", T=77, d=32, E=1, k=1, d_ff=36, gate="sigmoid_topk",
+         dtype="f32"),
+    edge("edge_k_equals_E", T=200, d=128, E=8, k=8, d_ff=64),
+    edge("edge_k_equals_E_shared_drop", T=150, d=64, E=4, k=4, d_ff=40, gate="softmax_all",
+         cf=0.5, d_ff_shared=32),
+    edge("edge_one_token_256_experts", T=1, d=256, E=256, k=8, d_ff=32, gate="sigmoid_topk"),
+    edge("edge_smallest_dims", T=40, d=8, E=3, k=2, d_ff=8),
+    edge("edge_capacity_one_E256", T=512, d=128, E=256, k=1, d_ff=32, gate="softmax_all",
+         cf=0.25, zipf_s=1.2),
+    edge("edge_unfused_router_E1024", T=96, d=64, E=1024, k=3, d_ff=16, cf=2.0),
+]
+CASES += EDGES
 
 
 @pytest.mark.parametrize("w", CASES, ids=[w.name for w in CASES])
