@@ -85,6 +85,11 @@ CASES = [
     ("decode_e2m1", 24, 256, 8, 2, 384, "softmax_topk", None, "e2m1"),
     ("drops_softmax_all", 400, 256, 16, 1, 128, "softmax_all", 1.0, "e4m3"),
     ("drops_e2m1", 333, 512, 8, 3, 256, "sigmoid_topk", 0.8, "e2m1"),
+    # degenerate corners: one expert, k = E, one token, capacity 1
+    ("single_expert_e4m3", 200, 256, 1, 1, 128, "softmax_topk", None, "e4m3"),
+    ("k_equals_E_e2m1", 150, 256, 4, 4, 128, "softmax_all", None, "e2m1"),
+    ("one_token_e4m3", 1, 512, 16, 4, 256, "sigmoid_topk", None, "e4m3"),
+    ("capacity_one_e4m3", 256, 256, 32, 1, 128, "softmax_topk", 0.125, "e4m3"),
 ]
 
 
