@@ -46,7 +46,8 @@ def run_ec(s, ws, T, E, C, **kw):
 
 
 @pytest.mark.parametrize("T,E,C", [(300, 8, 75), (300, 8, 0), (64, 16, 64), (1000, 128, 8),
-                                   (4097, 64, 130), (5, 4, 9), (2048, 256, 64)])
+                                   (4097, 64, 130), (5, 4, 9), (2048, 256, 64),
+                                   (300, 1, 50), (1, 3, 1)])   # one expert; one token
 @pytest.mark.parametrize("ties", [False, True])
 def test_expert_choice_matches_oracle(T, E, C, ties):
     l = random_logits(T, E, seed=T + E + C, ties=ties)

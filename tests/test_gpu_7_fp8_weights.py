@@ -35,6 +35,7 @@ def dequant_expert(q, name, e):
     (32, 256, 8, 2, 1120),      # decode-sized groups (<= 32 rows): 32-row A tiles
     (1, 256, 4, 2, 512),        # one token
     (20, 208, 5, 1, 336),       # short row tiles with ragged K and N
+    (50, 256, 1, 1, 256),       # one expert
 ])
 def test_grouped_swiglu_fp8_weights(T, d, E, k, F):
     w = WORKLOADS["mixtral_prefill"].scaled(T=T, d=d, E=E, k=k, d_ff=F)
