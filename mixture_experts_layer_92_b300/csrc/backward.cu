@@ -49,15 +49,28 @@ gather_dy_kernel(const uint4* __restrict__ dy, const int32_t* __restrict__ perm,
     const uint4* src = dy + static_cast<size_t>(a / k) * nvec;
     uint4* d0 = dyp + static_cast<size_t>(r) * nvec;
     uint4* d1 = dO + static_cast<size_t>(r) * nvec;
-    for (int i = lane; i < nvec; i += 32) {
-      const uint4 v = __ldg(src + i);
-      d0[i] = v;
-      const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-      uint32_t o[4];
+    // up to U chunks per lane loaded before any is stored: a 4 KB piece of the row per round trip
+    constexpr int U = 8;
+    for (int i0 = 0; i0 < nvec; i0 += 32 * U) {
+      uint4 v[U];
 #pragma unroll
-      for (int q = 0; q < 4; ++q)
-        o[q] = pack_bf16x2(g * __uint_as_float(w[q] << 16), g * __uint_as_float(w[q] & 0xffff0000u));
-      d1[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + lane + 32 * u;
+        if (i < nvec) v[u] = __ldg(src + i);
+      }
+#pragma unroll
+      for (int u = 0; u < U; ++u) {
+        const int i = i0 + lane + 32 * u;
+        if (i >= nvec) continue;
+        d0[i] = v[u];
+        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+        uint32_t o[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q)
+          o[q] = pack_bf16x2(g * __uint_as_float(w[q] << 16),
+                             g * __uint_as_float(w[q] & 0xffff0000u));
+        d1[i] = make_uint4(o[0], o[1], o[2], o[3]);
+      }
     }
   }
 }
